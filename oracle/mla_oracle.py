@@ -1,0 +1,350 @@
+"""fp64 CPU oracle for absorbed Multi-head Latent Attention decode.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by
+the CPU-baseline leg of the bench, never by the product package.  Nothing in
+here is blocked, fused or reordered beyond what the definitions state; numpy
+matrix products serve as single steps.
+
+Sources (pages are cited by title and section):
+  [audit]    "DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界"
+             (DEEPSEEK_MLA_ABSORB_AUDIT.md)
+  [report]   "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化 — 完整实验报告"
+             (mla_absorbed_cache_report.md)
+  [tutorial] "手搓 MLA:从 MHA 到 weight absorption,看懂 DeepSeek 的 KV 压缩"
+  [budget]   "kv_budget.py" (算子实战 IV：MoE 与 MLA · 代码)
+
+Pins (tests/test_oracle.py): the worked example's byte counts ([audit] §4.1,
+§4.2), naive == absorbed to 1e-10 in fp64 ([audit] §2.2/§2.3, [tutorial] §四),
+pure-Python brute-force attention on tiny inputs, closed forms (one token,
+zero query, one dominant token), and hand-worked quantizer vectors.
+The quantizer's rounding rules are readings of [report] §3.2, which gives no
+formula; the pages' own error figures use an unstated metric, so the
+quantization *error* is parity unpinned (the codes themselves are pinned to
+the stated rules by hand-worked vectors).
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+D_C = 512
+D_R = 64
+D_NOPE = 128
+D_V = 128
+PAGE = 64
+
+__all__ = [
+    "D_C", "D_R", "D_NOPE", "D_V", "PAGE",
+    "split_wkv_b", "naive_decode", "absorbed_decode", "softmax",
+    "latent_cache_bytes", "expanded_cache_bytes", "decode_arithmetic_intensity",
+    "bf16_round", "bf16_from_bits", "bf16_to_bits",
+    "quantize_int8", "quantize_int4_asym", "dequantize_int8", "dequantize_int4",
+    "pack_nibbles", "page_bytes", "PAGE_LAYOUT",
+    "quantize_token", "dequantized_tokens", "expected_page_pool",
+    "decode_batch",
+]
+
+
+# ----------------------------------------------------------------------------
+# weights
+# ----------------------------------------------------------------------------
+
+def split_wkv_b(wkv_b, H: int, d_nope: int = D_NOPE, d_v: int = D_V):
+    """Split the up-projection wkv_b [H*(d_nope+d_v), d_c] into W_UK, W_UV.
+
+    [tutorial] §三 ("k_nope, v = split(kv_up)") splits the up-projected
+    vector per head into the no-RoPE key part and the value part; read as a
+    per-head interleave, rows [h*(dn+dv), h*(dn+dv)+dn) are W_UK[h] and the
+    next dv rows are W_UV[h].  Returns fp64 arrays W_UK [H, dn, dc] and
+    W_UV [H, dv, dc], index order h, d, c as in the absorbed einsums of
+    [tutorial] §四.
+    """
+    W = np.asarray(wkv_b, dtype=np.float64)
+    W = W.reshape(H, d_nope + d_v, W.shape[-1])
+    return W[:, :d_nope, :].copy(), W[:, d_nope:, :].copy()
+
+
+# ----------------------------------------------------------------------------
+# attention, both paths
+# ----------------------------------------------------------------------------
+
+def softmax(s: np.ndarray) -> np.ndarray:
+    """Softmax over the last axis: subtract the max, exponentiate, normalise."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def naive_decode(q_nope, q_pe, c_kv, k_pe, W_UK, W_UV, scale: float):
+    """Expand-then-attend decode for one query token over n cached tokens.
+
+    [audit] §2.1: every head expands each cached latent into its own key
+    k_t = W_UK c_t and value v_t = W_UV c_t; [audit] §2.4 / [tutorial] §三:
+    the key is concatenated with the shared RoPE key, k = [k_nope; k_pe], and
+    the query is [q_nope; q_pe].  Standard attention follows.
+
+    q_nope [H, dn], q_pe [H, dr], c_kv [n, dc], k_pe [n, dr] -> out [H, dv].
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_pe = np.asarray(q_pe, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    Kpe = np.asarray(k_pe, np.float64)
+    H = q_nope.shape[0]
+    n = C.shape[0]
+    out = np.zeros((H, W_UV.shape[1]), dtype=np.float64)
+    if n == 0:
+        return out
+    for h in range(H):
+        k_nope = C @ W_UK[h].T                       # [n, dn]: k_t = W_UK[h] c_t
+        v = C @ W_UV[h].T                            # [n, dv]: v_t = W_UV[h] c_t
+        K = np.concatenate([k_nope, Kpe], axis=1)    # [n, dn+dr]
+        q = np.concatenate([q_nope[h], q_pe[h]])     # [dn+dr]
+        p = softmax(scale * (K @ q))
+        out[h] = p @ v
+    return out
+
+
+def absorbed_decode(q_nope, q_pe, c_kv, k_pe, W_UK, W_UV, scale: float):
+    """Absorbed decode for one query token over n cached tokens.
+
+    [audit] §2.2: q^T (W_UK c_t) = (W_UK^T q)^T c_t, so the query is moved
+    into latent space, q_lat = W_UK^T q_nope, and dotted with the cached
+    latent directly; the RoPE part q_pe . k_pe_t is added unchanged
+    ([audit] §2.4).  [audit] §2.3: sum_t p_t W_UV c_t = W_UV (sum_t p_t c_t),
+    so the probabilities weight the latents and W_UV is applied once.
+    [tutorial] §四 writes the same steps as einsums.
+
+    Returns out [H, dv], o_lat [H, dc] and lse [H] (natural-log sum of the
+    exponentiated scaled scores; -inf when n == 0).
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_pe = np.asarray(q_pe, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    Kpe = np.asarray(k_pe, np.float64)
+    H = q_nope.shape[0]
+    n = C.shape[0]
+    if n == 0:
+        return (np.zeros((H, W_UV.shape[1])), np.zeros((H, C.shape[1])),
+                np.full(H, -np.inf))
+    q_lat = np.einsum("hd,hdc->hc", q_nope, W_UK)    # W_UK[h]^T q_nope[h]
+    s = scale * (q_lat @ C.T + q_pe @ Kpe.T)         # [H, n]
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = np.sum(e, axis=1, keepdims=True)
+    o_lat = (e / l) @ C                              # sum_t p_t c_t
+    out = np.einsum("hc,hdc->hd", o_lat, W_UV)       # W_UV[h] o_lat[h]
+    lse = m[:, 0] + np.log(l[:, 0])
+    return out, o_lat, lse
+
+
+def decode_batch(q_nope, q_pe, seqs, W_UK, W_UV, scale: float, rows=None):
+    """Absorbed decode for every (or the listed) batch row.
+
+    seqs[b] = (c_kv [n_b, dc], k_pe [n_b, dr]) as real values.  Returns
+    {b: (out, o_lat, lse)}.
+    """
+    rows = range(len(seqs)) if rows is None else rows
+    return {b: absorbed_decode(q_nope[b], q_pe[b], seqs[b][0], seqs[b][1], W_UK, W_UV, scale)
+            for b in rows}
+
+
+# ----------------------------------------------------------------------------
+# byte accounting
+# ----------------------------------------------------------------------------
+
+def latent_cache_bytes(ntok: int, d_c: int = D_C, d_r: int = D_R, elem_bytes: int = 2) -> int:
+    """Absorbed cache: one c_KV and one k_pe per token ([audit] §2.4, §4.1)."""
+    return ntok * (d_c + d_r) * elem_bytes
+
+
+def expanded_cache_bytes(ntok: int, H: int, d_qk: int = D_NOPE + D_R, d_v: int = D_V,
+                         elem_bytes: int = 2) -> int:
+    """Naive cache: per-head expanded key (nope+rope) and value ([audit] §2.1, §4.1)."""
+    return ntok * H * (d_qk + d_v) * elem_bytes
+
+
+def decode_arithmetic_intensity(H: int, d_c: int = D_C, d_r: int = D_R, elem_bytes: int = 2) -> float:
+    """FLOP per cached byte of one absorbed decode query ([budget] part B):
+    each token costs 2*H*(d_c+d_r) for the scores and 2*H*d_c for the
+    latent sum over (d_c+d_r)*elem_bytes bytes."""
+    return 2.0 * H * (2 * d_c + d_r) / (elem_bytes * (d_c + d_r))
+
+
+# ----------------------------------------------------------------------------
+# bfloat16 and the cache quantizers (fp32 decisions, bit-exact)
+# ----------------------------------------------------------------------------
+
+def bf16_round(x) -> np.ndarray:
+    """float32 -> nearest-even bfloat16, returned as float32 values."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16))
+    return (r.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_to_bits(x) -> np.ndarray:
+    """bfloat16-representable float32 values -> uint16 bit patterns."""
+    return (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_from_bits(bits) -> np.ndarray:
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def quantize_int8(x, group: int):
+    """Symmetric INT8 over contiguous groups of `group` channels of one token.
+
+    [report] §3.2 lists per-channel INT8 in 32-element blocks for c_KV and
+    INT8 in 8-element blocks for k_pe.  Reading (no formula on the page):
+    scale s = bf16(amax / 127) computed in fp32, code = clamp(rint(x / s),
+    -127, 127) with round-half-even; a group whose s is 0 stores all-zero
+    codes.  x: float32 [..., k*group].  Returns int8 codes (same shape) and
+    float32 scales [..., k] holding bf16 values.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    g = x.reshape(*x.shape[:-1], x.shape[-1] // group, group)
+    amax = np.max(np.abs(g), axis=-1)
+    s = bf16_round(amax / np.float32(127.0))
+    safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+    q = np.rint(g / safe[..., None])
+    q = np.clip(q, -127, 127)
+    q = np.where((s == 0)[..., None], 0, q)
+    return q.astype(np.int8).reshape(x.shape), s
+
+
+def quantize_int4_asym(x, group: int = 32):
+    """Asymmetric INT4 over contiguous groups of one token's channels.
+
+    [report] §3.2 names asymmetric INT4 in 32-element blocks (scale + zero).
+    Reading: mn, mx = group min and max; s = bf16((mx - mn) / 15) in fp32;
+    zero = bf16(mn); code = clamp(rint((x - zero) / s), 0, 15), all-zero codes
+    when s is 0.  Dequantised value = code * s + zero.  Returns uint8 codes
+    0..15 (unpacked, same shape as x), float32 scales and zeros [..., k].
+    """
+    x = np.asarray(x, dtype=np.float32)
+    g = x.reshape(*x.shape[:-1], x.shape[-1] // group, group)
+    mn = np.min(g, axis=-1)
+    mx = np.max(g, axis=-1)
+    s = bf16_round((mx - mn) / np.float32(15.0))
+    z = bf16_round(mn)
+    safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+    q = np.rint((g - z[..., None]) / safe[..., None])
+    q = np.clip(q, 0, 15)
+    q = np.where((s == 0)[..., None], 0, q)
+    return q.astype(np.uint8).reshape(x.shape), s, z
+
+
+def dequantize_int8(codes, scales, group: int) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.float64)
+    c = c.reshape(*c.shape[:-1], c.shape[-1] // group, group)
+    return (c * np.asarray(scales, np.float64)[..., None]).reshape(np.shape(codes))
+
+
+def dequantize_int4(codes, scales, zeros, group: int = 32) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.float64)
+    c = c.reshape(*c.shape[:-1], c.shape[-1] // group, group)
+    v = c * np.asarray(scales, np.float64)[..., None] + np.asarray(zeros, np.float64)[..., None]
+    return v.reshape(np.shape(codes))
+
+
+def pack_nibbles(codes) -> np.ndarray:
+    """Two 4-bit codes per byte: element 2i in the low nibble, 2i+1 in the high."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+# ----------------------------------------------------------------------------
+# page format (the cache contract of the library, restated independently)
+# ----------------------------------------------------------------------------
+# Each physical page holds PAGE token slots.  Sections (byte offset, dtype,
+# per-token shape) in page order:
+PAGE_LAYOUT = {
+    "bf16": [("tok", "bf16", (D_C + D_R,))],            # c_kv then k_pe per slot
+    "int8": [("c_code", "i8", (D_C,)), ("pe_code", "i8", (D_R,)),
+             ("c_scale", "bf16", (D_C // 32,)), ("pe_scale", "bf16", (D_R // 8,))],
+    "int4": [("c_code", "u4x2", (D_C // 2,)), ("pe_code", "i8", (D_R,)),
+             ("c_scale", "bf16", (D_C // 32,)), ("c_zero", "bf16", (D_C // 32,)),
+             ("pe_scale", "bf16", (D_R // 8,))],
+}
+_ELEM = {"bf16": 2, "i8": 1, "u4x2": 1}
+
+
+def _sections(fmt: str, page: int = PAGE):
+    off = 0
+    out = {}
+    for name, dt, shp in PAGE_LAYOUT[fmt]:
+        nbytes = page * int(np.prod(shp)) * _ELEM[dt]
+        out[name] = (off, dt, shp, nbytes)
+        off += nbytes
+    return out, off
+
+
+def page_bytes(fmt: str, page: int = PAGE) -> int:
+    return _sections(fmt, page)[1]
+
+
+def quantize_token(fmt: str, c_kv, k_pe):
+    """Per-token payload of one format, as {section: array} for `n` tokens.
+
+    c_kv [n, dc], k_pe [n, dr] are bf16-representable float32 values.
+    """
+    c = np.asarray(c_kv, np.float32)
+    p = np.asarray(k_pe, np.float32)
+    if fmt == "bf16":
+        return {"tok": bf16_to_bits(np.concatenate([c, p], axis=1))}
+    pc, ps = quantize_int8(p, 8)
+    if fmt == "int8":
+        cc, cs = quantize_int8(c, 32)
+        return {"c_code": cc, "pe_code": pc, "c_scale": bf16_to_bits(cs),
+                "pe_scale": bf16_to_bits(ps)}
+    if fmt == "int4":
+        cc, cs, cz = quantize_int4_asym(c, 32)
+        return {"c_code": pack_nibbles(cc), "pe_code": pc, "c_scale": bf16_to_bits(cs),
+                "c_zero": bf16_to_bits(cz), "pe_scale": bf16_to_bits(ps)}
+    raise ValueError(fmt)
+
+
+def dequantized_tokens(fmt: str, c_kv, k_pe):
+    """The real values a decode over a `fmt` cache attends to (fp64)."""
+    c = np.asarray(c_kv, np.float32)
+    p = np.asarray(k_pe, np.float32)
+    if fmt == "bf16":
+        return c.astype(np.float64), p.astype(np.float64)
+    pc, ps = quantize_int8(p, 8)
+    pe = dequantize_int8(pc, ps, 8)
+    if fmt == "int8":
+        cc, cs = quantize_int8(c, 32)
+        return dequantize_int8(cc, cs, 32), pe
+    cc, cs, cz = quantize_int4_asym(c, 32)
+    return dequantize_int4(cc, cs, cz, 32), pe
+
+
+def expected_page_pool(fmt: str, num_pages: int, writes, page: int = PAGE) -> np.ndarray:
+    """Byte image of a page pool after appending tokens, starting from zeros.
+
+    writes: iterable of (page_table_row, pos, c_kv [T, dc], k_pe [T, dr]);
+    token t of the row lands in physical page row[(pos+t) // page], slot
+    (pos+t) % page.  Returns uint8 [num_pages, page_bytes(fmt)].
+    """
+    secs, pb = _sections(fmt, page)
+    pool = np.zeros((num_pages, pb), dtype=np.uint8)
+    for row, pos, c, p in writes:
+        payload = quantize_token(fmt, c, p)
+        for t in range(np.shape(c)[0]):
+            lp = (pos + t) // page
+            slot = (pos + t) % page
+            phys = int(row[lp])
+            for name, arr in payload.items():
+                off, dt, shp, nbytes = secs[name]
+                per_tok = nbytes // page
+                raw = np.ascontiguousarray(arr[t]).view(np.uint8).reshape(-1)
+                assert raw.size == per_tok
+                pool[phys, off + slot * per_tok: off + (slot + 1) * per_tok] = raw
+    return pool
+
+
+def _self_check():  # pragma: no cover - debugging aid
+    assert latent_cache_bytes(26) == 29952
+    assert expanded_cache_bytes(26, 16) == 266240
+    assert math.isclose(decode_arithmetic_intensity(128), 241.7777, rel_tol=1e-4)

@@ -1,0 +1,370 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, brute force.
+
+None of these compare the oracle with itself: each expected value is either
+printed on a page (tests/golden/*.json, with the citation inside), follows
+from a closed form of a special case, or comes from a separate pure-Python
+brute-force loop.
+"""
+
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------------------
+# byte accounting: the worked example of the audit page
+# ----------------------------------------------------------------------------
+
+def test_cache_bytes_worked_example():
+    g = _gold("audit_cache_bytes.json")
+    H, n, slots = g["H"], g["active_tokens"], g["allocated_slots"]
+    a = g["active_bytes"]
+    assert O.latent_cache_bytes(n) == a["absorb_total"]
+    assert O.latent_cache_bytes(n, d_r=0) == a["absorb_latent"]
+    assert O.latent_cache_bytes(n, d_c=0) == a["absorb_rope"]
+    assert O.expanded_cache_bytes(n, H) == a["naive_total"]
+    assert O.expanded_cache_bytes(n, H, d_v=0) == a["naive_key"]
+    assert O.expanded_cache_bytes(n, H, d_qk=0) == a["naive_value"]
+    al = g["allocated_bytes"]
+    assert O.latent_cache_bytes(slots) == al["absorb_total"]
+    assert O.expanded_cache_bytes(slots, H) == al["naive_total"]
+    assert O.expanded_cache_bytes(slots, H, d_v=0) == al["naive_key"]
+    ratio = O.expanded_cache_bytes(n, H) / O.latent_cache_bytes(n)
+    assert abs(ratio - g["ratio_naive_over_absorb"]) < 1e-6
+    assert ratio == pytest.approx(80.0 / 9.0)
+    assert 100.0 * (1 - 1 / ratio) == pytest.approx(g["reduction_percent"])
+    e = g["elements_per_token"]
+    assert O.expanded_cache_bytes(1, H, elem_bytes=1) == e["naive_total"]
+    assert O.latent_cache_bytes(1, elem_bytes=1) == e["absorbed_total"]
+
+
+def test_cache_bytes_against_real_buffers():
+    """Count the bytes of actual arrays shaped like both caches (audit §4.1)."""
+    g = _gold("audit_cache_bytes.json")
+    n, H = g["active_tokens"], g["H"]
+    k = np.zeros((1, n, H, O.D_NOPE + O.D_R), dtype=np.uint16)
+    v = np.zeros((1, n, H, O.D_V), dtype=np.uint16)
+    lat = np.zeros((1, n, O.D_C), dtype=np.uint16)
+    pe = np.zeros((1, n, O.D_R), dtype=np.uint16)
+    assert k.nbytes == g["active_bytes"]["naive_key"]
+    assert v.nbytes == g["active_bytes"]["naive_value"]
+    assert lat.nbytes == g["active_bytes"]["absorb_latent"]
+    assert pe.nbytes == g["active_bytes"]["absorb_rope"]
+
+
+def test_v3_bytes_table():
+    g = _gold("tutorial_v3_bytes.json")
+    assert O.latent_cache_bytes(1, elem_bytes=1) == g["per_token_layer"]["MLA"]["elements"]
+    assert O.latent_cache_bytes(1) == g["per_token_layer"]["MLA"]["bf16_bytes"]
+    mha = g["per_token_layer"]["MHA"]["elements"]
+    assert round(mha / O.latent_cache_bytes(1, elem_bytes=1)) == g["mha_over_mla_approx"]
+    kb = O.latent_cache_bytes(1) * g["layers"] / 1000   # 70,272 B: "about 70 KB"
+    assert round(kb) == g["mla_61_layer_kb_approx"]
+
+
+def test_report_quantized_sizes():
+    """Codes-only per-token sizes over 27 layers (report §3.1, §4.1)."""
+    g = _gold("report_quant_sizes.json")
+    L = g["layers"]
+    mha = O.expanded_cache_bytes(1, 16) * L
+    assert mha == g["mha_equiv_bytes"]
+    absorbed = O.latent_cache_bytes(1) * L
+    int8 = O.latent_cache_bytes(1, elem_bytes=1) * L
+    int4 = O.latent_cache_bytes(1, elem_bytes=1) * L // 2
+    assert round(absorbed / 1024, 1) == g["absorbed_kb"]
+    assert round(int8 / 1024, 1) == g["int8_kb"]
+    assert round(int4 / 1024, 1) == g["int4_kb"]
+    assert round(mha / absorbed, 1) == g["ratio_absorbed"]
+    assert round(mha / int8, 1) == g["ratio_int8"]
+    assert round(mha / int4, 1) == g["ratio_int4"]
+
+
+def test_page_formats():
+    """Per-token page payload: 1152 B bf16, 624 B INT8, 400 B INT4 (codes+scales+zeros)."""
+    assert O.page_bytes("bf16") == 64 * 1152
+    assert O.page_bytes("int8") == 64 * (512 + 64 + 2 * 16 + 2 * 8)
+    assert O.page_bytes("int4") == 64 * (256 + 64 + 2 * 16 + 2 * 16 + 2 * 8)
+
+
+def test_arithmetic_intensity_closed_form():
+    # kv_budget.py part B: 2*Hq*(2dc+dr)/(b*(dc+dr)); V3 shape -> 241.8 FLOP/B
+    assert O.decode_arithmetic_intensity(128) == pytest.approx(2 * 128 * 1088 / 1152)
+    # heads needed to reach a 1000/3 FLOP/B machine balance (H100 spec on the page)
+    need = (1000.0 / 3.0) * 2 * 576 / (2 * 1088)
+    assert round(need) == 176
+
+
+# ----------------------------------------------------------------------------
+# weight split
+# ----------------------------------------------------------------------------
+
+def test_split_wkv_b_rows():
+    H = 3
+    w = np.arange(H * 256, dtype=np.float64)[:, None] * np.ones((1, 5))
+    uk, uv = O.split_wkv_b(w, H)
+    for h in range(H):
+        assert np.all(uk[h][:, 0] == h * 256 + np.arange(128))
+        assert np.all(uv[h][:, 0] == h * 256 + 128 + np.arange(128))
+
+
+# ----------------------------------------------------------------------------
+# attention: brute force, associativity, closed forms
+# ----------------------------------------------------------------------------
+
+def _bruteforce(q_nope, q_pe, C, Kpe, Wuk, Wuv, scale):
+    """Pure-Python loops: expand K/V per head, softmax by max-subtract-exp-divide."""
+    H, dn = len(q_nope), len(q_nope[0])
+    n, dc = len(C), len(C[0])
+    dv = len(Wuv[0])
+    out = []
+    for h in range(H):
+        s = []
+        vs = []
+        for t in range(n):
+            k = [math.fsum(Wuk[h][d][c] * C[t][c] for c in range(dc)) for d in range(dn)]
+            k += list(Kpe[t])
+            q = list(q_nope[h]) + list(q_pe[h])
+            s.append(scale * math.fsum(a * b for a, b in zip(q, k)))
+            vs.append([math.fsum(Wuv[h][d][c] * C[t][c] for c in range(dc)) for d in range(dv)])
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = math.fsum(e)
+        out.append([math.fsum(e[t] / z * vs[t][d] for t in range(n)) for d in range(dv)])
+    return out
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_bruteforce_tiny_odd_dims(n):
+    """Odd, unequal dims so a transposed or swapped operand fails."""
+    rng = np.random.default_rng(11 + n)
+    H, dn, dr, dc, dv = 2, 3, 2, 7, 5
+    q_nope, q_pe = _rand(rng, H, dn), _rand(rng, H, dr)
+    C, Kpe = _rand(rng, n, dc), _rand(rng, n, dr)
+    Wuk, Wuv = _rand(rng, H, dn, dc), _rand(rng, H, dv, dc)
+    scale = 0.37
+    ref = np.array(_bruteforce(q_nope.tolist(), q_pe.tolist(), C.tolist(), Kpe.tolist(),
+                               Wuk.tolist(), Wuv.tolist(), scale))
+    naive = O.naive_decode(q_nope, q_pe, C, Kpe, Wuk, Wuv, scale)
+    absorbed, _, _ = O.absorbed_decode(q_nope, q_pe, C, Kpe, Wuk, Wuv, scale)
+    assert np.max(np.abs(naive - ref)) < 1e-12
+    assert np.max(np.abs(absorbed - ref)) < 1e-12
+
+
+def test_lse_bruteforce():
+    rng = np.random.default_rng(5)
+    H, n = 2, 6
+    q_nope, q_pe = _rand(rng, H, 3), _rand(rng, H, 2)
+    C, Kpe = _rand(rng, n, 4), _rand(rng, n, 2)
+    Wuk, Wuv = _rand(rng, H, 3, 4), _rand(rng, H, 2, 4)
+    _, _, lse = O.absorbed_decode(q_nope, q_pe, C, Kpe, Wuk, Wuv, 0.5)
+    for h in range(H):
+        s = []
+        for t in range(n):
+            k = [sum(Wuk[h][d][c] * C[t][c] for c in range(4)) for d in range(3)] + list(Kpe[t])
+            q = list(q_nope[h]) + list(q_pe[h])
+            s.append(0.5 * sum(a * b for a, b in zip(q, k)))
+        assert lse[h] == pytest.approx(math.log(math.fsum(math.exp(x) for x in s)), abs=1e-12)
+
+
+def _tiny_inputs():
+    w = synth.get_workload("v2lite_tiny")
+    wkv = synth.bf16_bits_to_f32(synth.gen_weights(w.H, w.seed))
+    qn, qp = synth.gen_queries(w.H, [w.seqlen], w.seed)
+    c, p = synth.gen_sequence(w.seed, 0, w.seqlen)
+    Wuk, Wuv = O.split_wkv_b(wkv, w.H)
+    return (synth.bf16_bits_to_f32(qn)[0], synth.bf16_bits_to_f32(qp)[0],
+            synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p), Wuk, Wuv, w.scale)
+
+
+def test_naive_equals_absorbed_v2lite_tiny():
+    """Associativity (audit §2.2, §2.3; tutorial §四): equal to 1e-10 in fp64."""
+    qn, qp, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    a, _, _ = O.absorbed_decode(qn, qp, C, P, Wuk, Wuv, sc)
+    b = O.naive_decode(qn, qp, C, P, Wuk, Wuv, sc)
+    assert a.shape == (16, 128)
+    assert np.max(np.abs(a - b)) <= 1e-10
+
+
+def test_naive_equals_absorbed_v3_shape():
+    w = synth.get_workload("v3_paged")
+    wkv = synth.bf16_bits_to_f32(synth.gen_weights(w.H, w.seed))
+    Wuk, Wuv = O.split_wkv_b(wkv, w.H)
+    n = 96
+    qn, qp = synth.gen_queries(w.H, [n], w.seed)
+    c, p = synth.gen_sequence(w.seed, 0, n)
+    args = (synth.bf16_bits_to_f32(qn)[0], synth.bf16_bits_to_f32(qp)[0],
+            synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p), Wuk, Wuv, w.scale)
+    a, _, _ = O.absorbed_decode(*args)
+    b = O.naive_decode(*args)
+    assert np.max(np.abs(a - b)) <= 1e-10
+
+
+def test_single_token_closed_form():
+    """n = 1: the softmax weight is 1, so o_lat = c_0 and out = W_UV c_0."""
+    qn, qp, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    out, o_lat, lse = O.absorbed_decode(qn, qp, C[:1], P[:1], Wuk, Wuv, sc)
+    assert np.array_equal(o_lat, np.broadcast_to(C[0].astype(np.float64), o_lat.shape))
+    for h in range(16):
+        assert np.allclose(out[h], Wuv[h] @ C[0], atol=1e-13)
+
+
+def test_zero_query_is_mean():
+    """q = 0: all scores equal, so o_lat is the plain mean of the latents."""
+    qn, qp, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    out, o_lat, lse = O.absorbed_decode(qn * 0, qp * 0, C, P, Wuk, Wuv, sc)
+    assert np.allclose(o_lat, C.astype(np.float64).mean(axis=0)[None, :], atol=1e-14)
+    assert np.allclose(lse, math.log(C.shape[0]), atol=1e-14)
+
+
+def test_dominant_rope_token():
+    """A RoPE key aligned with every head's q_pe and scaled up selects that token."""
+    qn, qp, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    H = qp.shape[0]
+    qp = np.ones_like(qp)           # identical q_pe for all heads
+    P = P.copy()
+    j = 7
+    P[j] = 1.0e3                    # q_pe . k_pe_j = 64e3, far above every other score
+    out, o_lat, _ = O.absorbed_decode(qn, qp, C, P, Wuk, Wuv, sc)
+    assert np.allclose(o_lat, np.broadcast_to(C[j], (H, C.shape[1])), atol=1e-12)
+    for h in range(H):
+        assert np.allclose(out[h], Wuv[h] @ C[j], atol=1e-12)
+
+
+def test_empty_sequence():
+    qn, qp, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    out, o_lat, lse = O.absorbed_decode(qn, qp, C[:0], P[:0], Wuk, Wuv, sc)
+    assert np.all(out == 0) and np.all(o_lat == 0) and np.all(np.isneginf(lse))
+
+
+def test_scale_is_inverse_sqrt_192():
+    assert synth.get_workload("v3_paged").scale == pytest.approx(1 / math.sqrt(128 + 64))
+
+
+# ----------------------------------------------------------------------------
+# bf16 rounding and quantizers: hand-worked vectors
+# ----------------------------------------------------------------------------
+
+def test_bf16_round_hand_values():
+    x = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -7, -2.5, 1 + 2 ** -8 + 2 ** -20,
+                  3.4e38], dtype=np.float32)   # above the largest finite bf16 (3.3895e38)
+    want = np.array([1.0, 1.0, 1 + 2 ** -6, 1 + 2 ** -7, -2.5, 1 + 2 ** -7, np.inf],
+                    dtype=np.float32)
+    got = O.bf16_round(x)
+    assert np.array_equal(got, want)
+
+
+def test_int8_hand_vector():
+    # amax 127 -> s = 1 exactly; codes = round-half-even of x
+    x = np.zeros(32, dtype=np.float32)
+    x[:8] = [127, -127, 63.5, 62.5, -0.5, 1.5, 2.5, -3.5]
+    codes, s = O.quantize_int8(x, 32)
+    assert s.tolist() == [1.0]
+    assert codes[:8].tolist() == [127, -127, 64, 62, 0, 2, 2, -4]
+    assert np.all(codes[8:] == 0)
+
+
+def test_int8_scale_rounding():
+    # amax 1 -> 1/127 = 0.0078740157..., bf16 -> 0.00787353515625 (mantissa 1.0078125 * 2^-7)
+    x = np.zeros(8, dtype=np.float32)
+    x[0], x[1] = 1.0, -0.5
+    codes, s = O.quantize_int8(x, 8)
+    assert s.tolist() == [0.00787353515625]
+    assert codes[0] == 127                 # 1/s = 127.007 -> 127
+    assert codes[1] == -64                 # -0.5/s = -63.5039 -> -64
+    # an all-zero group keeps scale 0 and zero codes
+    c0, s0 = O.quantize_int8(np.zeros(8, np.float32), 8)
+    assert s0.tolist() == [0.0] and np.all(c0 == 0)
+
+
+def test_int4_hand_vector():
+    # mn = -1, mx = 2: s = bf16(3/15 = 0.2) = 0.2001953125, zero = -1
+    x = np.full(32, -1.0, dtype=np.float32)
+    x[1], x[2], x[3] = 2.0, 0.0, -0.9
+    codes, s, z = O.quantize_int4_asym(x, 32)
+    assert s.tolist() == [0.2001953125] and z.tolist() == [-1.0]
+    # (2+1)/s = 14.985 -> 15; (0+1)/s = 4.995 -> 5; (0.1)/s = 0.4995 -> 0
+    assert codes[:4].tolist() == [0, 15, 5, 0]
+    # constant group: s = 0, zero = value, dequantises exactly
+    c, s2, z2 = O.quantize_int4_asym(np.full(32, 0.75, np.float32), 32)
+    assert s2.tolist() == [0.0] and z2.tolist() == [0.75] and np.all(c == 0)
+    assert np.all(O.dequantize_int4(c, s2, z2, 32) == 0.75)
+
+
+def test_nibble_packing():
+    assert O.pack_nibbles(np.array([1, 2, 15, 0], np.uint8)).tolist() == [0x21, 0x0F]
+
+
+@pytest.mark.parametrize("fmt,group", [("int8", 32), ("int8", 8), ("int4", 32)])
+def test_quantizer_error_bound(fmt, group):
+    """|x - dequant(x)| <= s/2 (plus the bf16 rounding slack of s itself)."""
+    rng = np.random.default_rng(3)
+    x = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(
+        rng.standard_normal((200, 512)).astype(np.float32) * 3))
+    if fmt == "int8":
+        c, s = O.quantize_int8(x, group)
+        xr = O.dequantize_int8(c, s, group)
+    else:
+        c, s, z = O.quantize_int4_asym(x, group)
+        xr = O.dequantize_int4(c, s, z, group)
+    err = np.abs(x.astype(np.float64) - xr).reshape(200, -1, group).max(axis=-1)
+    assert np.all(err <= s.astype(np.float64) * 0.5 * (1 + 2 ** -6) + 1e-30)
+
+
+def test_expected_page_pool_placement():
+    """Token t of row b lands in page_table[b][(pos+t)//64], slot (pos+t)%64."""
+    rng = np.random.default_rng(0)
+    row = np.array([3, 0, 2], np.int32)
+    c = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((70, 512)).astype(np.float32)))
+    p = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((70, 64)).astype(np.float32)))
+    pool = O.expected_page_pool("bf16", 4, [(row, 60, c, p)])
+    tok = pool.view(np.uint16).reshape(4, 64, 576)
+    assert np.array_equal(tok[3, 60], O.bf16_to_bits(np.concatenate([c[0], p[0]])))
+    assert np.array_equal(tok[0, 0], O.bf16_to_bits(np.concatenate([c[4], p[4]])))
+    assert np.array_equal(tok[0, 63], O.bf16_to_bits(np.concatenate([c[67], p[67]])))
+    assert np.array_equal(tok[2, 1], O.bf16_to_bits(np.concatenate([c[69], p[69]])))
+    assert np.all(tok[1] == 0) and np.all(tok[3, :60] == 0)
+
+
+def test_quant_pool_sections():
+    rng = np.random.default_rng(1)
+    c = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((2, 512)).astype(np.float32)))
+    p = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((2, 64)).astype(np.float32)))
+    pool = O.expected_page_pool("int4", 1, [(np.array([0]), 5, c, p)])[0]
+    codes, s, z = O.quantize_int4_asym(c, 32)
+    assert np.array_equal(pool[5 * 256:6 * 256], O.pack_nibbles(codes[0]))
+    off_scale = 64 * 256 + 64 * 64
+    got_s = pool[off_scale + 6 * 32: off_scale + 6 * 32 + 32].view(np.uint16)
+    assert np.array_equal(got_s, O.bf16_to_bits(s[1]))
+    off_zero = off_scale + 64 * 32
+    got_z = pool[off_zero + 5 * 32: off_zero + 6 * 32].view(np.uint16)
+    assert np.array_equal(got_z, O.bf16_to_bits(z[0]))
+
+
+def test_random_roundtrip_rope_norm():
+    """Generator sanity (not oracle): RoPE keeps pair norms, c_KV rows have unit RMS."""
+    c, p = synth.gen_sequence(0, 0, 30)
+    cf = synth.bf16_bits_to_f32(c).astype(np.float64)
+    assert np.allclose(np.sqrt(np.mean(cf ** 2, axis=1)), 1.0, atol=5e-3)
+    x = np.random.default_rng(0).standard_normal((3, 64))
+    y = synth.rope_interleaved(x, np.array([0.0, 5.0, 77.0]))
+    assert np.allclose(x[0], y[0])
+    assert np.allclose(np.hypot(x[:, 0::2], x[:, 1::2]), np.hypot(y[:, 0::2], y[:, 1::2]))
+    random.seed(0)
