@@ -1,0 +1,366 @@
+"""Absorbed-MLA decode benchmark: latent-cache GB/s, % of HBM peak, queries/s.
+
+One step = one full decode (plan, query absorption, split-KV attend, merge +
+up-projection) over one batch whose latent cache is resident in HBM.  The
+default workload is the DeepSeek-V3 attention shape: 128 heads, 64 rows,
+8192 cached tokens each, bf16 cache in 64-token pages behind a random page
+table (603,979,776 cache bytes per step, larger than the 129 MB L2, so no
+flush is needed between steps).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--fmt bf16|int8|int4]
+
+--impl reference times the fp64 CPU oracle on this host's cores on a bounded
+sample of the same workload (the only place the bench runs the oracle, with
+the cpu_baseline leg of the default arm).
+Under torchrun (N > 1) every rank decodes its own replica batch (weak
+scaling, no collective on the data path); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "absorbed-MLA decode latent-cache GB/s (% HBM peak) and queries/s, 1 GB300"
+BYTES_PER_TOKEN = {"bf16": 1152, "int8": 624, "int4": 400}
+DESCR = {
+    "v2lite_batch": "V2-Lite shape decode: H=16, B=32, seqlen 4096, contiguous bf16 latent cache",
+    "v3_paged": "DeepSeek-V3 shape decode: H=128, B=64, seqlen 8192, paged bf16 latent cache "
+                "(page 64, seeded random page table)",
+    "v3_ragged": "DeepSeek-V3 shape ragged decode: H=128, B=128, lognormal seqlens (median 4096, clip 256..32768), "
+                 "paged",
+    "v3_quant": "DeepSeek-V3 shape decode over a quantized cache: H=128, B=64, seqlen 32768, paged",
+}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_traffic(kind: str):
+    """DRAM bytes per launch of the attend kernel from the committed ncu summary,
+    or None when missing or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "attend_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        src = os.path.join(ROOT, "mla_absorbed_latent_gb300", "csrc", d["source"])
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        if h != d["source_sha256"] or d.get("kind") != kind:
+            return None
+        return int(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                mx.append(float(row[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------
+
+def oracle_time(prob, budget_s: float, max_rows: int | None = None):
+    """Time the fp64 absorbed oracle over successive rows until budget_s of oracle
+    work; returns (cache bytes processed, seconds, rows)."""
+    import oracle as O
+    Wuk, Wuv = O.split_wkv_b(synth.bf16_bits_to_f32(prob.wkv), prob.H)
+    qn = synth.bf16_bits_to_f32(prob.q_nope)
+    qp = synth.bf16_bits_to_f32(prob.q_pe)
+    done_bytes, spent, rows = 0, 0.0, 0
+    bpt = BYTES_PER_TOKEN[prob.fmt]
+    for b in range(prob.B):
+        c, p = prob.sequence(b)
+        C, P = O.dequantized_tokens(prob.fmt, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))
+        t0 = time.perf_counter()
+        O.absorbed_decode(qn[b], qp[b], C, P, Wuk, Wuv, prob.scale)
+        spent += time.perf_counter() - t0
+        done_bytes += int(prob.seqlens[b]) * bpt
+        rows += 1
+        if spent >= budget_s or (max_rows is not None and rows >= max_rows):
+            break
+    return done_bytes, spent, rows
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_reference(args, wl, fmt):
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    from synth.device import problem_from_workload
+    prob = problem_from_workload(wl, fmt)
+    # warm-up: one row, untimed
+    for _ in range(args.warmup):
+        oracle_time(prob, 0.0, max_rows=1)
+    total_bytes, total_s = 0, 0.0
+    for _ in range(args.steps):
+        nbytes, s, _rows = oracle_time(prob, 0.0, max_rows=1)   # one row per step
+        total_bytes += nbytes
+        total_s += s
+    gbs = total_bytes / total_s / 1e9
+    bpq = int(prob.seqlens[0]) * BYTES_PER_TOKEN[fmt]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {DESCR.get(wl.name, '')}", "cache_fmt": fmt,
+                   "sample": "one batch row (all heads, full sequence) per step"},
+        "queries_per_s": gbs * 1e9 / bpq,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": f"{args.steps} rows of {wl.name}, one per step, fp64 numpy absorbed oracle"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl, fmt):
+    import torch
+    import torch.distributed as dist
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import mla_absorbed_latent_gb300 as mla
+    from synth.device import DeviceDecode, problem_from_workload
+
+    prob = problem_from_workload(wl, fmt)
+    dev = DeviceDecode(prob)
+    H, B = prob.H, prob.B
+    stream = torch.cuda.current_stream()
+    cache_bytes = int(np.sum(prob.seqlens)) * BYTES_PER_TOKEN[fmt]
+    kind = mla.mla_decode_kernel_kind(H) if fmt == "bf16" else 1
+
+    def step(ev=None):
+        p = prob
+        mla.mla_decode_plan(H, fmt, dev.seqlens, B, p.max_pages, dev.workspace, dev.ws_bytes, stream)
+        mla.mla_decode_absorb_q(dev.q_nope, dev.q_pe, dev.W_UK, H, B, dev.workspace, dev.ws_bytes, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mla.mla_decode_attend(H, dev.cache, dev.page_table, p.max_pages, dev.seqlens, B, p.scale, dev.workspace,
+                              dev.ws_bytes, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mla.mla_decode_combine(dev.W_UV, H, B, dev.workspace, dev.ws_bytes, dev.out, None, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
+
+    attend_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(attend_ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks else None
+    elapsed_ms = t0.elapsed_time(t1)
+    attend_ms = float(np.mean([a.elapsed_time(b) for a, b in attend_ev]))
+    if world > 1:
+        t = torch.tensor([elapsed_ms, attend_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, attend_ms = float(t[0]), float(t[1])
+        dist.barrier()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after timing: {mla.mla_status_string(st)} ({info})")
+
+    # end to end through the public call: pinned host query in, host result out
+    h_qn = dev.q_nope.cpu().pin_memory()
+    h_qp = dev.q_pe.cpu().pin_memory()
+    h_out = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev.q_nope.copy_(h_qn, non_blocking=True)
+        dev.q_pe.copy_(h_qp, non_blocking=True)
+        dev.decode(stream)
+        h_out.copy_(dev.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = h_qn.numel() * 2 + h_qp.numel() * 2
+    d2h = h_out.numel() * 2
+
+    # CPU oracle on the host cores (rank 0, one GPU only), bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nbytes, secs, rows = oracle_time(prob, args.cpu_seconds)
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{rows} of {B} rows of {wl.name} (all {H} heads, full sequences), fp64 numpy absorbed "
+                         f"oracle, {secs:.1f} s"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    ms_step = elapsed_ms / args.steps
+    total_bytes = cache_bytes * world
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+    attend_gbs = cache_bytes / (attend_ms * 1e-3) / 1e9
+    flops_tok = 2 * H * (576 + 512)
+    traffic = kernel_traffic("tcgen05" if kind == 1 else "cuda-core")
+    if kind == 1:
+        roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s", "frac": attend_gbs / hbm,
+                "traffic": traffic, "peak_source": peak_src,
+                "tensor_tflops": cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12}
+    else:
+        # CUDA-core kernel: fp32 FMA bound; peak = SMs x 128 FMA/clk x 2 FLOP x max SM clock
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        sm_max = (clock_info or {}).get("sm_max_mhz", 2070.0)
+        alu_peak = props.multi_processor_count * 128 * 2 * sm_max * 1e6 / 1e12
+        achieved = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": traffic, "peak_source": "derived: SMs*128 FMA*2*max clock",
+                "hbm_gbs": attend_gbs, "hbm_frac": attend_gbs / hbm}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {DESCR.get(wl.name, '')}", "H": H, "B": B,
+                   "seqlen": int(prob.seqlens.max()), "cache_fmt": fmt, "cache_bytes_per_step": cache_bytes,
+                   "l2": "inputs larger than L2 (cache stream per step > 129 MB), no flush",
+                   "parallelism": f"replicas x{world} (batch-sharded, no collective)",
+                   "attend_kernel": "tcgen05" if kind == 1 else "cuda-core"},
+        "pct_hbm_peak": 100.0 * value / (hbm * world),
+        "queries_per_s": B * world / (ms_step * 1e-3),
+        "roofline": roof,
+        "attend_ms": attend_ms,
+        "cpu_baseline": cpu,
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR))
+    ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = synth.get_workload(args.workload)
+    fmt = args.fmt or wl.fmts[0]
+    if args.impl == "reference":
+        return run_reference(args, wl, fmt)
+    return run_ours(args, wl, fmt)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

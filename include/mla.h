@@ -1,0 +1,203 @@
+/*
+ * mla.h — C ABI of the absorbed Multi-head Latent Attention decode library
+ * (libmla.so, GB300 / sm_103a).
+ *
+ * What it computes.  One decode step of DeepSeek MLA in absorbed form over a
+ * paged latent KV cache:
+ *   q_lat[b,h,:] = W_UK[h]^T q_nope[b,h,:]                         (key absorption)
+ *   s[b,h,t]     = scale * (q_lat[b,h,:] . c_t + q_pe[b,h,:] . k_pe_t)
+ *   p            = softmax_t(s)           (split over the sequence, merged by LSE)
+ *   o_lat[b,h,:] = sum_t p[b,h,t] c_t                               (latent sum)
+ *   out[b,h,:]   = W_UV[h] o_lat[b,h,:]                              (value absorption)
+ * Sources: "DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界"
+ * (DEEPSEEK_MLA_ABSORB_AUDIT.md) §2.2 (q^T W_UK c = (W_UK^T q)^T c), §2.3
+ * (sum_t p_t W_UV c_t = W_UV sum_t p_t c_t), §2.4 (the 64-wide RoPE key is
+ * cached beside the 512-wide latent: 576 elements per token and layer), §6.1
+ * (MQA mode over the latent: key width 576, value width 512); "手搓 MLA:从 MHA
+ * 到 weight absorption" §四 (the absorbed einsums).  Cache quantization:
+ * "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化 — 完整实验报告" §3.2 (per-channel
+ * INT8 in 32-element blocks, asymmetric INT4 in 32-element blocks, k_pe INT8
+ * in 8-element blocks).
+ *
+ * Conventions for every call below.
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates and frees nothing.  bf16 means IEEE bfloat16 bit patterns.
+ *  - Calls are asynchronous on `stream` and never synchronise the host, except
+ *    mla_get_device_status.
+ *  - Argument checks happen on the host before anything is enqueued; a failed
+ *    check returns a negative mla_status_t and enqueues nothing.
+ *  - Problems only the device can see (a page id outside the pool, a sequence
+ *    longer than its page-table row, a bounded wait that gave up) are recorded
+ *    in a device status word; the affected kernel skips the bad access (it
+ *    substitutes page 0, or clamps the length) and the first such error is
+ *    reported by mla_get_device_status.
+ *  - The functions act on the CUDA device current on the calling thread.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fixed MLA dimensions (DeepSeek-V2-Lite and DeepSeek-V3 attention layers). */
+#define MLA_D_C 512      /* kv_lora_rank: width of the cached latent c_KV      */
+#define MLA_D_R 64       /* qk_rope_head_dim: width of the shared RoPE key     */
+#define MLA_D_NOPE 128   /* qk_nope_head_dim                                  */
+#define MLA_D_V 128      /* v_head_dim                                        */
+#define MLA_PAGE 64      /* tokens per cache page                              */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID = -1,      /* null pointer, negative size, misaligned buffer        */
+  MLA_ERR_UNSUPPORTED = -2,  /* head count or format outside the supported set        */
+  MLA_ERR_CUDA = -3,         /* a CUDA runtime call (launch, attribute) failed        */
+  MLA_ERR_BOUNDS = -4,       /* device: page id outside the pool / sequence too long  */
+  MLA_ERR_TIMEOUT = -5,      /* device: a bounded wait inside a kernel gave up        */
+  MLA_ERR_WORKSPACE = -6     /* workspace smaller than mla_decode_workspace_bytes     */
+} mla_status_t;
+
+/* Cache storage formats. */
+typedef enum {
+  MLA_FMT_BF16 = 0,  /* c_KV and k_pe in bfloat16                                   */
+  MLA_FMT_INT8 = 1,  /* c_KV INT8 per 32-channel group, k_pe INT8 per 8, bf16 scales */
+  MLA_FMT_INT4 = 2   /* c_KV asymmetric INT4 per 32 (bf16 scale + zero), k_pe INT8/8 */
+} mla_fmt_t;
+
+/*
+ * Page layout (one physical page = MLA_PAGE token slots; section offsets are
+ * in bytes from the start of the page; per-slot rows are contiguous):
+ *
+ * MLA_FMT_BF16, 73,728 B:  [0)      slot s: 576 bf16 = c_KV[0..511], k_pe[0..63]
+ * MLA_FMT_INT8, 39,936 B:  [0)      c codes    int8 [64][512]
+ *                          [32768)  k_pe codes int8 [64][64]
+ *                          [36864)  c scales   bf16 [64][16]   (group g = channels 32g..32g+31)
+ *                          [38912)  k_pe scale bf16 [64][8]    (group g = dims 8g..8g+7)
+ * MLA_FMT_INT4, 25,600 B:  [0)      c codes    u8   [64][256]  (channel 2i low nibble, 2i+1 high)
+ *                          [16384)  k_pe codes int8 [64][64]
+ *                          [20480)  c scales   bf16 [64][16]
+ *                          [22528)  c zeros    bf16 [64][16]
+ *                          [24576)  k_pe scale bf16 [64][8]
+ * Quantizer (fp32 arithmetic, bit-exact and deterministic):
+ *   INT8 group:  s = bf16_rne(amax / 127); code = clamp(rint(x / s), -127, 127); x^ = code * s
+ *   INT4 group:  s = bf16_rne((max - min) / 15); z = min;
+ *                code = clamp(rint((x - z) / s), 0, 15); x^ = code * s + z
+ *   rint rounds half to even; a group with s == 0 stores zero codes.
+ */
+typedef struct {
+  int fmt;          /* mla_fmt_t                                                  */
+  int num_pages;    /* physical pages in the pool                                 */
+  void* pages;      /* device, num_pages * mla_cache_page_bytes(fmt) bytes,
+                       256-byte aligned; owned by the caller                       */
+} mla_cache_t;
+
+/* Bytes of one physical page of `fmt` (0 for an unknown format). */
+size_t mla_cache_page_bytes(int fmt);
+
+/*
+ * Split the up-projection wkv_b into the absorbed weights.
+ *   wkv_b : bf16 [H*(128+128)][512]; rows h*256 .. h*256+127 are head h's
+ *           no-RoPE key projection, the next 128 rows its value projection
+ *           ("手搓 MLA" §三, k_nope, v = split(kv_up), read per head).
+ *   W_UK  : bf16 [H][512][128], written; W_UK[h][c][d] = wkv_b[h*256 + d][c]
+ *           (the key projection stored transposed, d fastest).
+ *   W_UV  : bf16 [H][128][512], written; W_UV[h][d][c] = wkv_b[h*256 + 128 + d][c].
+ * Bit-exact copy.  H in {16, 128}.  All three buffers 16-byte aligned.
+ */
+int mla_absorb_weights(const void* wkv_b, int H, void* W_UK, void* W_UV, cudaStream_t stream);
+
+/*
+ * Append T new tokens to each of B sequences.
+ *   c_kv       : bf16 [B][T][512], k_pe : bf16 [B][T][64] (k_pe already RoPE-rotated)
+ *   page_table : int32 [B][max_pages]; logical page j of row b lives in physical
+ *                page page_table[b*max_pages + j]
+ *   pos        : int32 [B] (device): token t of row b goes to position pos[b]+t,
+ *                i.e. page (pos[b]+t)/64, slot (pos[b]+t)%64
+ * The token's payload is written (quantized when cache->fmt asks for it);
+ * nothing else in the pool changes.  A position beyond max_pages*64 or a
+ * page id outside [0, num_pages) is skipped and raises MLA_ERR_BOUNDS.
+ * Rows of the same call must not target the same slot.
+ */
+int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_pe,
+                     const int32_t* page_table, int max_pages, const int32_t* pos,
+                     int B, int T, cudaStream_t stream);
+
+/*
+ * Workspace needed by mla_decode for B rows and H heads on the current
+ * device (the split-KV partials, the query-side latent and the split plan).
+ */
+size_t mla_decode_workspace_bytes(int B, int H);
+
+/*
+ * One absorbed decode step (q_len = 1 per row).
+ *   q_nope    : bf16 [B][H][128]      q_pe : bf16 [B][H][64] (RoPE-rotated)
+ *   W_UK      : bf16 [H][512][128]    W_UV : bf16 [H][128][512] (mla_absorb_weights)
+ *   cache     : the page pool; page_table int32 [B][max_pages]
+ *   seqlens   : int32 [B] (device): row b attends to its tokens 0 .. seqlens[b]-1
+ *               (the new token included when it was appended first).  A row
+ *               with seqlen 0 produces zeros.
+ *   scale     : softmax scale (1/sqrt(192) for these models)
+ *   workspace : device scratch of >= mla_decode_workspace_bytes(B, H) bytes,
+ *               256-byte aligned; contents need no initialisation
+ *   out       : bf16 [B][H][128], written
+ * H in {16, 128}: H = 128 runs the tcgen05 tensor-core kernel, H = 16 the
+ * CUDA-core kernel.  Equivalent to mla_decode_plan + mla_decode_absorb_q +
+ * mla_decode_attend + mla_decode_combine on the same stream.
+ */
+int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,
+               const mla_cache_t* cache, const int32_t* page_table, int max_pages,
+               const int32_t* seqlens, int B, float scale,
+               void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream);
+
+/* The four steps of mla_decode, callable one by one (same arguments). */
+
+/* Step 0: split plan.  Cuts the rows' 64-token pages into contiguous,
+ * near-equal ranges, one per persistent worker of the attend kernel that
+ * (H, fmt) selects; stored in the workspace.  Lengths beyond max_pages*64
+ * are clamped and raise MLA_ERR_BOUNDS (negative lengths count as 0). */
+int mla_decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 1: q_lat = W_UK^T q_nope (fp32 accumulation, rounded to bf16) and
+ * q_pe, stored in the workspace as the query operand of step 2. */
+int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 2: the split-KV online-softmax pass over the plan of step 0; leaves
+ * per-split (o_lat / l, LSE) partials in the workspace.  Reads the lengths
+ * as clamped by step 0. */
+int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table, int max_pages,
+                      const int32_t* seqlens, int B, float scale,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step 3: LSE-merge of the splits into o_lat, then out = W_UV o_lat (bf16).
+ * o_lat_out (fp32 [B][H][512]) may be NULL; when given, the merged latent
+ * sum is stored there too. */
+int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes,
+                       void* out, float* o_lat_out, cudaStream_t stream);
+
+/*
+ * Wait for `stream`, then return (and clear) the first device-detected error
+ * recorded since the last call on the current device: MLA_OK,
+ * MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).
+ * If `info` is non-NULL it receives a detail value (the offending row or page).
+ */
+int mla_get_device_status(cudaStream_t stream, int* info);
+
+/* Which attend kernel mla_decode uses for H heads: 1 = tcgen05, 0 = CUDA cores,
+ * -1 = unsupported. */
+int mla_decode_kernel_kind(int H);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,156 @@
+"""ctypes binding of libmla.so: the C ABI of include/mla.h, same names.
+
+Argument marshalling only: torch tensors (device memory owned by the
+caller) are passed as raw pointers, the stream defaults to torch's current
+stream, and a negative status raises MLAError.  Every step of the decode
+path runs in the library's CUDA kernels; there is no fallback of any kind:
+if libmla.so is missing the import fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmla.so")
+
+MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
+MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = -4, -5, -6
+FMT = {"bf16": 0, "int8": 1, "int4": 2}
+D_C, D_R, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.mla_status_string(status).decode()} ({status})")
+
+
+class mla_cache_t(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("num_pages", ctypes.c_int), ("pages", ctypes.c_void_p)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (python mla_absorbed_latent_gb300/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    cp = ctypes.POINTER(mla_cache_t)
+    sigs = {
+        "mla_cache_page_bytes": (sz, [i]),
+        "mla_absorb_weights": (i, [vp, i, vp, vp, vp]),
+        "mla_cache_append": (i, [cp, vp, vp, vp, i, vp, i, i, vp]),
+        "mla_decode_workspace_bytes": (sz, [i, i]),
+        "mla_decode": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, sz, vp, vp]),
+        "mla_decode_plan": (i, [i, i, vp, i, i, vp, sz, vp]),
+        "mla_decode_absorb_q": (i, [vp, vp, vp, i, i, vp, sz, vp]),
+        "mla_decode_attend": (i, [i, cp, vp, i, vp, i, f, vp, sz, vp]),
+        "mla_decode_combine": (i, [vp, i, i, vp, sz, vp, vp, vp]),
+        "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
+        "mla_decode_kernel_kind": (i, [i]),
+        "mla_status_string": (ctypes.c_char_p, [i]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != MLA_OK:
+        raise MLAError(status, where)
+
+
+def cache_struct(fmt: str | int, num_pages: int, pages) -> mla_cache_t:
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    return mla_cache_t(f, int(num_pages), _ptr(pages))
+
+
+def mla_cache_page_bytes(fmt: str | int) -> int:
+    return int(_lib.mla_cache_page_bytes(FMT[fmt] if isinstance(fmt, str) else int(fmt)))
+
+
+def mla_absorb_weights(wkv_b, H: int, W_UK, W_UV, stream=None) -> None:
+    _check(_lib.mla_absorb_weights(_ptr(wkv_b), H, _ptr(W_UK), _ptr(W_UV), _stream(stream)), "mla_absorb_weights")
+
+
+def mla_cache_append(cache: mla_cache_t, c_kv, k_pe, page_table, max_pages: int, pos, B: int, T: int,
+                     stream=None) -> None:
+    _check(_lib.mla_cache_append(ctypes.byref(cache), _ptr(c_kv), _ptr(k_pe), _ptr(page_table), max_pages,
+                                 _ptr(pos), B, T, _stream(stream)), "mla_cache_append")
+
+
+def mla_decode_workspace_bytes(B: int, H: int) -> int:
+    return int(_lib.mla_decode_workspace_bytes(B, H))
+
+
+def mla_decode(q_nope, q_pe, W_UK, W_UV, H: int, cache: mla_cache_t, page_table, max_pages: int, seqlens,
+               B: int, scale: float, workspace, workspace_bytes: int, out, stream=None) -> None:
+    _check(_lib.mla_decode(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, ctypes.byref(cache),
+                           _ptr(page_table), max_pages, _ptr(seqlens), B, scale, _ptr(workspace),
+                           workspace_bytes, _ptr(out), _stream(stream)), "mla_decode")
+
+
+def mla_decode_plan(H: int, fmt: str | int, seqlens, B: int, max_pages: int, workspace, workspace_bytes: int,
+                    stream=None) -> None:
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(_lib.mla_decode_plan(H, f, _ptr(seqlens), B, max_pages, _ptr(workspace), workspace_bytes,
+                                _stream(stream)), "mla_decode_plan")
+
+
+def mla_decode_absorb_q(q_nope, q_pe, W_UK, H: int, B: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(_lib.mla_decode_absorb_q(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), H, B, _ptr(workspace),
+                                    workspace_bytes, _stream(stream)), "mla_decode_absorb_q")
+
+
+def mla_decode_attend(H: int, cache: mla_cache_t, page_table, max_pages: int, seqlens, B: int, scale: float,
+                      workspace, workspace_bytes: int, stream=None) -> None:
+    _check(_lib.mla_decode_attend(H, ctypes.byref(cache), _ptr(page_table), max_pages, _ptr(seqlens), B, scale,
+                                  _ptr(workspace), workspace_bytes, _stream(stream)), "mla_decode_attend")
+
+
+def mla_decode_combine(W_UV, H: int, B: int, workspace, workspace_bytes: int, out, o_lat_out=None,
+                       stream=None) -> None:
+    _check(_lib.mla_decode_combine(_ptr(W_UV), H, B, _ptr(workspace), workspace_bytes, _ptr(out),
+                                   _ptr(o_lat_out), _stream(stream)), "mla_decode_combine")
+
+
+def mla_get_device_status(stream=None) -> tuple[int, int]:
+    """(status, detail) of the first device-detected error since the last call; clears it."""
+    info = ctypes.c_int(0)
+    st = _lib.mla_get_device_status(_stream(stream), ctypes.byref(info))
+    return int(st), int(info.value)
+
+
+def mla_decode_kernel_kind(H: int) -> int:
+    return int(_lib.mla_decode_kernel_kind(H))
+
+
+def mla_status_string(status: int) -> str:
+    return _lib.mla_status_string(status).decode()
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded ctypes library (for callers that marshal arguments themselves)."""
+    return _lib

@@ -1,0 +1,79 @@
+// Split-KV plan for one decode step, computed on the device from the
+// sequence lengths (no host round trip, so the step stays asynchronous).
+//
+// Every row's sequence is cut into 64-token tiles (one cache page each).  The
+// tiles of all rows, in row order, form one global list of T tiles which is
+// cut into `workers` contiguous, near-equal ranges, one per persistent CTA
+// (or CTA pair) of the attend kernel: worker w owns tiles
+// [floor(w*T/W), floor((w+1)*T/W)).  A worker whose range crosses row
+// boundaries emits one partial (segment) per row it touches; segment (w, b)
+// is stored at index w + b, which is unique because ranges are ordered.
+// Ragged batches therefore cost the same per SM as uniform ones.
+#include "mla_common.cuh"
+
+namespace mla {
+namespace {
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seqlens, int B, int max_pages,
+                                                     int workers, int* __restrict__ plan, int* err) {
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  const int per = (B + blockDim.x - 1) / blockDim.x;
+  const int lo = min(B, tid * per), hi = min(B, lo + per);
+  const long long cap = (long long)max_pages * PAGE;
+  int* prefix = plan + PLAN_HDR;
+  int* seq_c = plan + PLAN_HDR + B + 1;
+
+  int local = 0;
+  for (int b = lo; b < hi; ++b) {
+    long long n = seqlens[b];
+    if (n < 0 || n > cap) {
+      raise_error(err, MLA_ERR_BOUNDS, b);
+      n = n < 0 ? 0 : cap;
+    }
+    seq_c[b] = (int)n;
+    local += (int)((n + PAGE - 1) / PAGE);
+  }
+  // block-wide exclusive scan of the per-thread tile counts
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x / 32) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+  for (int b = lo; b < hi; ++b) {
+    prefix[b] = run;
+    run += (seq_c[b] + PAGE - 1) / PAGE;
+  }
+  if (tid == blockDim.x - 1) {
+    prefix[B] = run;
+    plan[0] = run;
+    plan[1] = workers;
+    plan[2] = B;
+    plan[3] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,
+                        cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(seqlens, B, max_pages, workers, plan, err);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

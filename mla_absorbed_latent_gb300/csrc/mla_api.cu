@@ -1,0 +1,258 @@
+// C ABI of libmla: argument checks, workspace layout, kernel dispatch and the
+// device error word.  Declarations and the contract live in include/mla.h.
+#include <mutex>
+
+#include "mla_common.cuh"
+
+namespace mla {
+
+// First device-detected error: [0] status, [1] detail.  One copy per device.
+__device__ int g_error_word[2];
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_mu;
+int* g_err_ptr[MAX_DEVICES] = {};
+int g_sms[MAX_DEVICES] = {};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1;
+  return dev;
+}
+
+// device address of this device's error word (resolved once per device)
+int* err_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool heads_ok(int H) { return H == 16 || H == 128; }
+bool fmt_ok(int fmt) { return fmt == MLA_FMT_BF16 || fmt == MLA_FMT_INT8 || fmt == MLA_FMT_INT4; }
+
+size_t page_bytes(int fmt) {
+  switch (fmt) {
+    case MLA_FMT_BF16: return PAGE_BYTES_BF16;
+    case MLA_FMT_INT8: return PAGE_BYTES_INT8;
+    case MLA_FMT_INT4: return PAGE_BYTES_INT4;
+    default: return 0;
+  }
+}
+
+// attend kernel for H heads over a `fmt` cache: 1 = tcgen05, 0 = CUDA cores, -1 = none
+int attend_kind(int H, int fmt) {
+  if (!heads_ok(H) || !fmt_ok(fmt)) return -1;
+  if (fmt != MLA_FMT_BF16) return -1;
+  return 0;
+}
+
+int max_workers(int sms) { return attend_cc_workers(sms) > attend_tc_workers(sms) ? attend_cc_workers(sms)
+                                                                                 : attend_tc_workers(sms); }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+bool cache_ok(const mla_cache_t* c) {
+  return c != nullptr && fmt_ok(c->fmt) && c->num_pages > 0 && c->pages != nullptr && aligned(c->pages, 256);
+}
+
+int check_ws(int B, int H, void* ws, size_t ws_bytes, WsLayout* L) {
+  const int sms = num_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  *L = ws_layout(B, H, max_workers(sms));
+  if (ws == nullptr || !aligned(ws, 256)) return MLA_ERR_INVALID;
+  if (ws_bytes < L->total) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_cache_page_bytes(int fmt) { return page_bytes(fmt); }
+
+int mla_absorb_weights(const void* wkv_b, int H, void* W_UK, void* W_UV, cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (!wkv_b || !W_UK || !W_UV || !aligned(wkv_b, 16) || !aligned(W_UK, 16) || !aligned(W_UV, 16))
+    return MLA_ERR_INVALID;
+  return status_of(launch_absorb_weights(wkv_b, H, W_UK, W_UV, stream));
+}
+
+int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_pe, const int32_t* page_table,
+                     int max_pages, const int32_t* pos, int B, int T, cudaStream_t stream) {
+  if (cache == nullptr || !fmt_ok(cache->fmt)) return cache == nullptr ? MLA_ERR_INVALID : MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache) || B < 0 || T < 0 || max_pages <= 0) return MLA_ERR_INVALID;
+  if ((long long)B * T == 0) return MLA_OK;
+  if (!c_kv || !k_pe || !page_table || !pos || !aligned(c_kv, 16) || !aligned(k_pe, 16) || !aligned(page_table, 4) ||
+      !aligned(pos, 4))
+    return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  return status_of(launch_cache_append(cache->fmt, cache->num_pages, cache->pages, c_kv, k_pe, page_table, max_pages,
+                                       pos, B, T, err, stream));
+}
+
+size_t mla_decode_workspace_bytes(int B, int H) {
+  if (B < 0 || !heads_ok(H)) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  return ws_layout(B, H, max_workers(sms)).total;
+}
+
+int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (B < 0) return MLA_ERR_INVALID;
+  WsLayout L;
+  int st = check_ws(B, H, workspace, workspace_bytes, &L);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !W_UK || !aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(W_UK, 16))
+    return MLA_ERR_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return status_of(launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream));
+}
+
+int mla_decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  if (!heads_ok(H) || !fmt_ok(fmt)) return MLA_ERR_UNSUPPORTED;
+  const int kind = attend_kind(H, fmt);
+  if (kind < 0) return MLA_ERR_UNSUPPORTED;
+  if (B < 0 || max_pages <= 0) return MLA_ERR_INVALID;
+  WsLayout L;
+  int st = check_ws(B, H, workspace, workspace_bytes, &L);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!seqlens || !aligned(seqlens, 4)) return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  const int sms = num_sms();
+  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.plan);
+  return status_of(launch_plan(seqlens, B, max_pages, workers, plan, err, stream));
+}
+
+int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table, int max_pages,
+                      const int32_t* seqlens, int B, float scale, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (cache == nullptr || B < 0 || max_pages <= 0) return MLA_ERR_INVALID;
+  if (!fmt_ok(cache->fmt)) return MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache)) return MLA_ERR_INVALID;
+  const int kind = attend_kind(H, cache->fmt);
+  if (kind < 0) return MLA_ERR_UNSUPPORTED;
+  WsLayout L;
+  int st = check_ws(B, H, workspace, workspace_bytes, &L);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!page_table || !seqlens || !aligned(page_table, 4) || !aligned(seqlens, 4)) return MLA_ERR_INVALID;
+  if (!(scale == scale)) return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int* plan = reinterpret_cast<const int*>(ws + L.plan);
+  float* part_o = reinterpret_cast<float*>(ws + L.part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  const int sms = num_sms();
+  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  cudaError_t e;
+  if (kind == 1)
+    e = launch_attend_tc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+                         scale, plan, workers, part_o, part_lse, err, stream);
+  else
+    e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+                         scale, plan, workers, part_o, part_lse, err, stream);
+  return status_of(e);
+}
+
+int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes, void* out,
+                       float* o_lat_out, cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (B < 0) return MLA_ERR_INVALID;
+  WsLayout L;
+  int st = check_ws(B, H, workspace, workspace_bytes, &L);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!W_UV || !out || !aligned(W_UV, 16) || !aligned(out, 16) || (o_lat_out && !aligned(o_lat_out, 16)))
+    return MLA_ERR_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return status_of(launch_combine(W_UV, H, B, reinterpret_cast<const int*>(ws + L.plan),
+                                  reinterpret_cast<const float*>(ws + L.part_o),
+                                  reinterpret_cast<const float*>(ws + L.part_lse), out, o_lat_out, stream));
+}
+
+int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,
+               const mla_cache_t* cache, const int32_t* page_table, int max_pages, const int32_t* seqlens, int B,
+               float scale, void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (cache == nullptr || B < 0 || max_pages <= 0) return MLA_ERR_INVALID;
+  if (!fmt_ok(cache->fmt)) return MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache)) return MLA_ERR_INVALID;
+  if (attend_kind(H, cache->fmt) < 0) return MLA_ERR_UNSUPPORTED;
+  WsLayout L;
+  int st = check_ws(B, H, workspace, workspace_bytes, &L);
+  if (st != MLA_OK) return st;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !W_UK || !W_UV || !out || !page_table || !seqlens) return MLA_ERR_INVALID;
+  st = mla_decode_plan(H, cache->fmt, seqlens, B, max_pages, workspace, workspace_bytes, stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode_absorb_q(q_nope, q_pe, W_UK, H, B, workspace, workspace_bytes, stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode_attend(H, cache, page_table, max_pages, seqlens, B, scale, workspace, workspace_bytes, stream);
+  if (st != MLA_OK) return st;
+  return mla_decode_combine(W_UV, H, B, workspace, workspace_bytes, out, nullptr, stream);
+}
+
+int mla_get_device_status(cudaStream_t stream, int* info) {
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  int host[2] = {0, 0};
+  if (cudaMemcpyAsync(host, err, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (host[0] != 0) {
+    if (cudaMemsetAsync(err, 0, sizeof(host), stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  if (info != nullptr) *info = host[1];
+  return host[0];
+}
+
+int mla_decode_kernel_kind(int H) { return attend_kind(H, MLA_FMT_BF16); }
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_BOUNDS: return "page id or sequence length out of bounds";
+    case MLA_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MLA_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+// Shared definitions of the CUDA side of libmla: dimensions, the decode
+// workspace layout, the device error word, and thin inline-PTX wrappers for
+// mbarriers and bulk async copies (sm_90+ forms, used on sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int DC = MLA_D_C;        // 512
+constexpr int DR = MLA_D_R;        // 64
+constexpr int DK = DC + DR;        // 576: key width of the absorbed (MQA-style) attention
+constexpr int DN = MLA_D_NOPE;     // 128
+constexpr int DV = MLA_D_V;        // 128
+constexpr int PAGE = MLA_PAGE;     // 64 tokens per page
+
+constexpr size_t PAGE_BYTES_BF16 = (size_t)PAGE * DK * 2;                       // 73,728
+constexpr size_t PAGE_BYTES_INT8 = (size_t)PAGE * (DC + DR + 2 * 16 + 2 * 8);   // 39,936
+constexpr size_t PAGE_BYTES_INT4 = (size_t)PAGE * (DC / 2 + DR + 4 * 16 + 2 * 8);  // 25,600
+
+// section offsets inside a quantized page
+constexpr int I8_C_CODE = 0, I8_PE_CODE = 32768, I8_C_SCALE = 36864, I8_PE_SCALE = 38912;
+constexpr int I4_C_CODE = 0, I4_PE_CODE = 16384, I4_C_SCALE = 20480, I4_C_ZERO = 22528,
+              I4_PE_SCALE = 24576;
+
+// device error word: [0] = first mla_status_t recorded, [1] = detail
+__device__ __forceinline__ void raise_error(int* err, int code, int info) {
+  if (err != nullptr && atomicCAS(err, 0, code) == 0) {
+    atomicExch(err + 1, info);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// decode workspace: [q_cat bf16 B*H*576][plan int32][partial O fp32][partial lse fp32]
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  size_t q_cat, plan, part_o, part_lse, total;
+  int max_segments;
+};
+
+// plan block (int32): [0] total tiles, [1] workers, [2] B, [3] reserved,
+//                     [4 .. 4+B]  tile prefix (B+1 entries),
+//                     [5+B .. 5+2B) clamped sequence lengths
+constexpr int PLAN_HDR = 4;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int B, int H, int max_workers) {
+  WsLayout L;
+  size_t off = 0;
+  L.q_cat = off;
+  off = align_up(off + (size_t)B * H * DK * 2, 1024);
+  L.plan = off;
+  off = align_up(off + (size_t)(PLAN_HDR + 2 * B + 1) * 4, 1024);
+  L.max_segments = max_workers + B;
+  L.part_o = off;
+  off = align_up(off + (size_t)L.max_segments * H * DC * 4, 1024);
+  L.part_lse = off;
+  off = align_up(off + (size_t)L.max_segments * H * 4, 1024);
+  L.total = off;
+  return L;
+}
+
+// worker that owns global tile x when T tiles are cut into W contiguous ranges
+// [floor(w*T/W), floor((w+1)*T/W))
+__host__ __device__ __forceinline__ int worker_of_tile(long long x, long long T, long long W) {
+  return (int)(((x + 1) * W + T - 1) / T - 1);
+}
+__host__ __device__ __forceinline__ long long worker_begin(long long w, long long T, long long W) {
+  return (w * T) / W;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A bounded wait gives up after this long (far above any legal wait).
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with `parity` to complete; false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+// 1-D bulk async copy global -> shared, completion counted on `bar` (bytes).
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// host-side launchers (one per translation unit)
+// ---------------------------------------------------------------------------
+cudaError_t launch_absorb_weights(const void* wkv_b, int H, void* W_UK, void* W_UV, cudaStream_t s);
+cudaError_t launch_cache_append(int fmt, int num_pages, void* pages, const void* c_kv, const void* k_pe,
+                                const int32_t* page_table, int max_pages, const int32_t* pos, int B, int T,
+                                int* err, cudaStream_t s);
+cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
+                            cudaStream_t s);
+cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,
+                        cudaStream_t s);
+cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
+                             const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
+                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s);
+int attend_cc_workers(int num_sms);
+cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
+                             const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
+                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s);
+int attend_tc_workers(int num_sms);
+cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
+                           const float* part_lse, void* out, float* o_lat, cudaStream_t s);
+
+}  // namespace mla

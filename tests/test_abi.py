@@ -1,0 +1,71 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/mla.h declares, and rejects bad arguments before any
+CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._build_module().build_library()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(mla_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["mla_absorb_weights", "mla_cache_append", "mla_decode", "mla_decode_workspace_bytes",
+                     "mla_get_device_status", "mla_cache_page_bytes"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_page_bytes(lib):
+    lib.mla_cache_page_bytes.restype = ctypes.c_size_t
+    assert lib.mla_cache_page_bytes(0) == 64 * 1152
+    assert lib.mla_cache_page_bytes(1) == 64 * 624
+    assert lib.mla_cache_page_bytes(2) == 64 * 400
+    assert lib.mla_cache_page_bytes(7) == 0
+
+
+def test_host_validation_without_gpu(lib):
+    import mla_absorbed_latent_gb300 as m
+    raw = m.raw_library()
+    assert raw.mla_absorb_weights(None, 7, None, None, None) == m.MLA_ERR_UNSUPPORTED
+    assert raw.mla_absorb_weights(None, 16, None, None, None) == m.MLA_ERR_INVALID
+    assert raw.mla_absorb_weights(24, 16, 32, 48, None) == m.MLA_ERR_INVALID   # misaligned
+    bad_fmt = m.mla_cache_t(9, 1, 1024)
+    assert raw.mla_cache_append(ctypes.byref(bad_fmt), None, None, None, 1, None, 1, 1, None) == m.MLA_ERR_UNSUPPORTED
+    cache = m.mla_cache_t(0, 1, 1024)
+    assert raw.mla_cache_append(ctypes.byref(cache), None, None, None, 1, None, -1, 1, None) == m.MLA_ERR_INVALID
+    assert raw.mla_cache_append(ctypes.byref(cache), None, None, None, 1, None, 0, 5, None) == m.MLA_OK
+    unaligned = m.mla_cache_t(0, 1, 1024 + 16)
+    assert raw.mla_cache_append(ctypes.byref(unaligned), None, None, None, 1, None, 1, 1, None) == m.MLA_ERR_INVALID
+    assert raw.mla_decode(None, None, None, None, 12, ctypes.byref(cache), None, 1, None, 1, 0.1, None, 0, None,
+                          None) == m.MLA_ERR_UNSUPPORTED
+    assert raw.mla_decode_workspace_bytes(-1, 128) == 0
+    assert raw.mla_decode_workspace_bytes(4, 3) == 0
+
+
+def test_status_strings(lib):
+    import mla_absorbed_latent_gb300 as m
+    for st in range(0, -7, -1):
+        assert m.mla_status_string(st) != "unknown status"
+    assert m.mla_status_string(-99) == "unknown status"

@@ -1,0 +1,266 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bit-exact where the result is a copy or an integer decision (weight split,
+page placement, quantized codes and scales); abs 2e-2 + rel 1e-2 elementwise
+plus rel-RMS 1e-2 and cosine 0.9999 for the bf16 decode outputs.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")]
+
+import oracle as O  # noqa: E402
+import synth  # noqa: E402
+from synth.device import DeviceDecode, bits_to_device, make_problem, problem_from_workload  # noqa: E402
+from tests.parity import assert_close, oracle_rows, weights  # noqa: E402
+
+
+def _np_bf16(t):
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _out_f64(t):
+    return synth.bf16_bits_to_f32(_np_bf16(t)).astype(np.float64)
+
+
+def _status_ok():
+    import mla_absorbed_latent_gb300 as mla
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+
+
+# ----------------------------------------------------------------------------
+# weights and cache placement: bit-exact
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_absorb_weights_bitexact(H):
+    import mla_absorbed_latent_gb300 as mla
+    wkv = synth.gen_weights(H, seed=7)
+    W_UK = torch.empty((H, 512, 128), dtype=torch.bfloat16, device="cuda")
+    W_UV = torch.empty((H, 128, 512), dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_weights(bits_to_device(wkv), H, W_UK, W_UV)
+    uk, uv = O.split_wkv_b(synth.bf16_bits_to_f32(wkv), H)
+    got_uk = synth.bf16_bits_to_f32(_np_bf16(W_UK)).astype(np.float64)
+    got_uv = synth.bf16_bits_to_f32(_np_bf16(W_UV)).astype(np.float64)
+    assert np.array_equal(got_uk, np.transpose(uk, (0, 2, 1)))
+    assert np.array_equal(got_uv, uv)
+
+
+def _pool_bytes(dev):
+    return dev.pool.cpu().numpy().reshape(dev.prob.num_pages, -1)
+
+
+def _expected_pool(prob, writes):
+    return O.expected_page_pool(prob.fmt, prob.num_pages, writes)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4"])
+def test_append_prefill_then_decode_bitexact(fmt):
+    """V2-Lite tiny case: 25-token prefill append, then the decode token at position 25."""
+    w = synth.get_workload("v2lite_tiny")
+    prob = make_problem(w.H, [26], w.seed, paged=False, fmt=fmt)
+    dev = DeviceDecode(prob, prefill=25)
+    _status_ok()
+    c, p = prob.sequence(0)
+    want = _expected_pool(prob, [(prob.page_table[0], 0, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))])
+    assert np.array_equal(_pool_bytes(dev), want)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4"])
+def test_append_ragged_paged_bitexact(fmt):
+    """Several rows, random page table, appends that start mid-page and cross pages."""
+    import mla_absorbed_latent_gb300 as mla
+    seqlens = [70, 1, 130, 64, 200]
+    prob = make_problem(128, seqlens, seed=21, fmt=fmt, dist="outlier", spare_pages=3)
+    dev = DeviceDecode(prob, prefill=None)  # appends tokens 0..n-1 per row
+    # second append: 37 more tokens per row at pos = seqlen (rows with room)
+    extra = 37
+    rows = [0, 2, 3]
+    rng = np.random.default_rng(5)
+    c_new = synth.f32_to_bf16_bits(rng.standard_normal((len(rows), extra, 512)).astype(np.float32) * 3)
+    p_new = synth.f32_to_bf16_bits(rng.standard_normal((len(rows), extra, 64)).astype(np.float32))
+    # give those rows fresh pages for the spill-over (the spare pages)
+    table = prob.page_table.copy()
+    spare = list(range(prob.num_pages - 3, prob.num_pages))
+    for r in rows:
+        n = seqlens[r]
+        need = (n + extra + 63) // 64
+        for j in range((n + 63) // 64, need):
+            table = np.pad(table, ((0, 0), (0, max(0, j + 1 - table.shape[1]))), constant_values=-1)
+            table[r, j] = spare.pop(0)
+    pt = torch.from_numpy(np.ascontiguousarray(table[rows])).cuda()
+    pos = torch.tensor([seqlens[r] for r in rows], dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(dev.cache, bits_to_device(c_new), bits_to_device(p_new), pt, table.shape[1], pos,
+                         len(rows), extra)
+    torch.cuda.synchronize()
+    _status_ok()
+    writes = []
+    for b, n in enumerate(seqlens):
+        c, p = prob.sequence(b)
+        writes.append((prob.page_table[b], 0, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p)))
+    for i, r in enumerate(rows):
+        writes.append((table[r], seqlens[r], synth.bf16_bits_to_f32(c_new[i]), synth.bf16_bits_to_f32(p_new[i])))
+    assert np.array_equal(_pool_bytes(dev), _expected_pool(prob, writes))
+
+
+def test_append_out_of_bounds_is_reported_not_written():
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(16, [10], seed=3)
+    dev = DeviceDecode(prob)
+    before = dev.pool.clone()
+    c = torch.zeros((1, 1, 512), dtype=torch.bfloat16, device="cuda")
+    p = torch.zeros((1, 1, 64), dtype=torch.bfloat16, device="cuda")
+    pos = torch.tensor([64 * prob.max_pages], dtype=torch.int32, device="cuda")   # one past capacity
+    mla.mla_cache_append(dev.cache, c, p, dev.page_table, prob.max_pages, pos, 1, 1)
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_BOUNDS and info == 0
+    bad_table = torch.tensor([[prob.num_pages + 5]], dtype=torch.int32, device="cuda")
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(dev.cache, c, p, bad_table, 1, pos, 1, 1)
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_BOUNDS and info == prob.num_pages + 5
+    assert torch.equal(before, dev.pool)
+    _status_ok()
+
+
+# ----------------------------------------------------------------------------
+# decode parity
+# ----------------------------------------------------------------------------
+
+def _check_rows(dev, rows, o_lat=None):
+    prob = dev.prob
+    ref = oracle_rows(prob, rows)
+    got = _out_f64(dev.out)
+    worst = 0.0
+    for b in rows:
+        _, r = assert_close(got[b], ref[b][0], what=f"out[{b}]")
+        worst = max(worst, r)
+        if o_lat is not None:
+            assert_close(o_lat[b].cpu().numpy(), ref[b][1], what=f"o_lat[{b}]")
+    return worst
+
+
+def test_decode_v2lite_tiny():
+    w = synth.get_workload("v2lite_tiny")
+    prob = problem_from_workload(w)
+    dev = DeviceDecode(prob, prefill=25)
+    o_lat = torch.empty((1, 16, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, [0], o_lat)
+    # the oracle's naive path gives the same reference
+    Wuk, Wuv = weights(prob)
+    c, p = prob.sequence(0)
+    naive = O.naive_decode(synth.bf16_bits_to_f32(prob.q_nope)[0], synth.bf16_bits_to_f32(prob.q_pe)[0],
+                           synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p), Wuk, Wuv, prob.scale)
+    assert_close(_out_f64(dev.out)[0], naive)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_ragged_edges(H):
+    """Lengths around the page and half-page edges, an empty row, several tiles."""
+    seqlens = [1, 31, 32, 33, 63, 64, 65, 0, 200, 1000, 129]
+    prob = make_problem(H, seqlens, seed=11 + H)
+    dev = DeviceDecode(prob)
+    o_lat = torch.empty((len(seqlens), H, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    rows = [b for b, n in enumerate(seqlens) if n > 0]
+    _check_rows(dev, rows, o_lat)
+    empty = seqlens.index(0)
+    assert torch.count_nonzero(dev.out[empty]) == 0
+    assert torch.count_nonzero(o_lat[empty]) == 0
+
+
+def test_decode_steps_equal_decode():
+    prob = make_problem(128, [300, 77, 1], seed=5)
+    dev = DeviceDecode(prob)
+    a = dev.decode().clone()
+    b = dev.decode_steps().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_decode_page_permutation_bitexact():
+    """Same tokens behind a different physical page order: identical output bits."""
+    seqlens = [500, 130, 64]
+    p1 = make_problem(128, seqlens, seed=9, paged=False)
+    p2 = make_problem(128, seqlens, seed=9, paged=True)
+    assert not np.array_equal(p1.page_table, p2.page_table)
+    a = DeviceDecode(p1).decode().clone()
+    b = DeviceDecode(p2).decode().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_decode_v2lite_batch_full():
+    """H=16, B=32, every seqlen 4096, contiguous cache: every row against the oracle."""
+    prob = problem_from_workload(synth.get_workload("v2lite_batch"))
+    dev = DeviceDecode(prob)
+    dev.decode()
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, list(range(prob.B)))
+
+
+def test_decode_v3_paged_full():
+    """H=128, B=64, seqlen 8192, random page table: sampled rows + whole-batch sanity."""
+    prob = problem_from_workload(synth.get_workload("v3_paged"))
+    dev = DeviceDecode(prob)
+    o_lat = torch.empty((prob.B, 128, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, [0, 21, 42, 63], o_lat)
+    out = _out_f64(dev.out)
+    assert np.all(np.isfinite(out))
+    # every row's o_lat is a convex combination of unit-RMS latents: RMS <= 1
+    rms = torch.sqrt(torch.mean(o_lat ** 2, dim=-1))
+    assert bool(torch.all(rms <= 1.0 + 1e-3))
+
+
+def test_decode_v3_ragged_full():
+    """H=128, B=128, lognormal lengths: shortest, longest and a middle row."""
+    prob = problem_from_workload(synth.get_workload("v3_ragged"))
+    dev = DeviceDecode(prob)
+    dev.decode()
+    torch.cuda.synchronize()
+    _status_ok()
+    order = np.argsort(prob.seqlens)
+    rows = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})
+    _check_rows(dev, rows)
+
+
+def test_decode_bad_page_id_reports_bounds():
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(16, [100], seed=4)
+    dev = DeviceDecode(prob)
+    dev.page_table[0, 1] = prob.num_pages + 100
+    dev.decode()
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_BOUNDS and info == prob.num_pages + 100
+
+
+def test_decode_seqlen_over_capacity_reports_bounds():
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(16, [100], seed=4)
+    dev = DeviceDecode(prob)
+    dev.seqlens[0] = 64 * prob.max_pages + 1
+    dev.decode()
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_BOUNDS and info == 0
+
+
+def test_workspace_too_small_is_rejected():
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(16, [10], seed=4)
+    dev = DeviceDecode(prob)
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode(dev.q_nope, dev.q_pe, dev.W_UK, dev.W_UV, 16, dev.cache, dev.page_table, prob.max_pages,
+                       dev.seqlens, 1, prob.scale, dev.workspace, dev.ws_bytes - 1, dev.out)
+    assert e.value.status == mla.MLA_ERR_WORKSPACE
