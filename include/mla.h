@@ -182,6 +182,30 @@ int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t w
                        void* out, float* o_lat_out, cudaStream_t stream);
 
 /*
+ * Decode without any allocation (no counterpart on the pages: an interface
+ * addition of this library for hosts that cannot allocate device memory, e.g.
+ * an engine whose custom-op interface passes only inputs and outputs, a
+ * runtime that owns all device memory through its own pool, or a serving loop
+ * that forbids cudaMalloc once running).  Same arguments and result as
+ * mla_decode, minus the workspace: the scratch is a fixed array of
+ * MLA_NOALLOC_SCRATCH_BYTES in device global memory inside the library image,
+ * held by every GPU that loads the library until the process exits.
+ *  - All calls on a device share that array and it keeps the last call's
+ *    contents; calls that overlap on the GPU race on it, so order them (one
+ *    stream).  No part of it needs to start at zero.
+ *  - The first call on a device resolves the array's address for that device
+ *    (it must be current); make that first call before any stream capture.
+ *  - A batch whose scratch cannot fit (even with a single split worker) is
+ *    rejected with MLA_ERR_WORKSPACE; to fit, fewer split workers than
+ *    mla_decode may be used, so results may differ in the last bits.
+ *  - Calls no allocating routine.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
+int mla_decode_noalloc(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,
+                       const mla_cache_t* cache, const int32_t* page_table, int max_pages,
+                       const int32_t* seqlens, int B, float scale, void* out, cudaStream_t stream);
+
+/*
  * Wait for `stream`, then return (and clear) the first device-detected error
  * recorded since the last call on the current device: MLA_OK,
  * MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).

@@ -151,6 +151,19 @@ def mla_status_string(status: int) -> str:
     return _lib.mla_status_string(status).decode()
 
 
+def mla_decode_noalloc(q_nope, q_pe, W_UK, W_UV, H: int, cache: mla_cache_t, page_table, max_pages: int, seqlens,
+                       B: int, scale: float, out, stream=None) -> None:
+    """mla_decode with the library's fixed device scratch instead of a workspace
+    (for hosts that cannot allocate; see include/mla.h)."""
+    fn = _lib.mla_decode_noalloc
+    if fn.argtypes is None:
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        fn.restype = i
+        fn.argtypes = [vp, vp, vp, vp, i, ctypes.POINTER(mla_cache_t), vp, i, vp, i, ctypes.c_float, vp, vp]
+    _check(fn(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, ctypes.byref(cache), _ptr(page_table),
+              max_pages, _ptr(seqlens), B, scale, _ptr(out), _stream(stream)), "mla_decode_noalloc")
+
+
 def raw_library() -> ctypes.CDLL:
     """The loaded ctypes library (for callers that marshal arguments themselves)."""
     return _lib

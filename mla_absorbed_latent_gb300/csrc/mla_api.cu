@@ -86,6 +86,12 @@ int check_ws(int B, int H, void* ws, size_t ws_bytes, WsLayout* L) {
 }
 
 }  // namespace
+
+// accessors for other translation units of the library
+int* device_error_word() { return err_ptr(); }
+int device_sm_count() { return num_sms(); }
+int attend_kernel_kind(int H, int fmt) { return attend_kind(H, fmt); }
+
 }  // namespace mla
 
 using namespace mla;

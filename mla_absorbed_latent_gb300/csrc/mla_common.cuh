@@ -173,6 +173,11 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, float* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
+// library-internal accessors (defined in mla_api.cu)
+int* device_error_word();            // this device's error word, nullptr on failure
+int device_sm_count();               // SMs of the current device, 0 on failure
+int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
+
 cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
                            const float* part_lse, void* out, float* o_lat, cudaStream_t s);
 

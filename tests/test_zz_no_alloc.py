@@ -1,0 +1,49 @@
+"""mla_decode_noalloc: the decode entry point for callers that cannot allocate
+device memory (no workspace argument; the library keeps a fixed scratch array
+in device memory).  Called through the C ABI and compared with mla_decode, the
+entry point that takes a caller workspace, on two calls in a row, within the
+parity tolerance of the other tests.  Kept in a file that pytest collects last.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")]
+
+import synth  # noqa: E402
+from synth.device import DeviceDecode, make_problem  # noqa: E402
+from tests.parity import assert_close  # noqa: E402
+
+
+def _f64(t):
+    return synth.bf16_bits_to_f32(t.detach().view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+
+
+@pytest.mark.parametrize("H,seqlens", [(16, [26, 4096, 1, 700]), (128, [8192, 65, 0, 3000, 64])])
+def test_noalloc_matches_workspace_decode_twice(H, seqlens):
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(H, seqlens, seed=40 + H)
+    dev = DeviceDecode(prob)
+    ref = _f64(dev.decode())
+    torch.cuda.synchronize()
+    for _ in range(2):                     # two calls in a row share the scratch
+        out = torch.full_like(dev.out, float("nan"))
+        mla.mla_decode_noalloc(dev.q_nope, dev.q_pe, dev.W_UK, dev.W_UV, H, dev.cache, dev.page_table,
+                               prob.max_pages, dev.seqlens, prob.B, prob.scale, out)
+        torch.cuda.synchronize()
+        st, info = mla.mla_get_device_status()
+        assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+        assert_close(_f64(out), ref, what="noalloc vs workspace decode")
+
+
+def test_noalloc_rejects_batch_beyond_scratch():
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(128, [64], seed=3)
+    dev = DeviceDecode(prob)
+    B = 1024                                # q-side latent alone exceeds the fixed scratch
+    big = torch.empty((B, 128, 128), dtype=torch.bfloat16, device="cuda")
+    pt = torch.zeros((B, 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_noalloc(big, big, dev.W_UK, dev.W_UV, 128, dev.cache, pt, 1, pt, B, prob.scale, big)
+    assert e.value.status == mla.MLA_ERR_WORKSPACE
