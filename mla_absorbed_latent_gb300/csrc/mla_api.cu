@@ -64,7 +64,7 @@ size_t page_bytes(int fmt) {
 int attend_kind(int H, int fmt) {
   if (!heads_ok(H) || !fmt_ok(fmt)) return -1;
   if (fmt != MLA_FMT_BF16) return -1;
-  return 0;
+  return H == 128 ? 1 : 0;
 }
 
 int max_workers(int sms) { return attend_cc_workers(sms) > attend_tc_workers(sms) ? attend_cc_workers(sms)
