@@ -141,7 +141,7 @@ size_t mla_decode_workspace_bytes(int B, int H);
  *   seqlens   : int32 [B] (device): row b attends to its tokens 0 .. seqlens[b]-1
  *               (the new token included when it was appended first).  A row
  *               with seqlen 0 produces zeros.
- *   scale     : softmax scale (1/sqrt(192) for these models)
+ *   scale     : softmax scale, > 0 (1/sqrt(192) for these models)
  *   workspace : device scratch of >= mla_decode_workspace_bytes(B, H) bytes,
  *               256-byte aligned; contents need no initialisation
  *   out       : bf16 [B][H][128], written

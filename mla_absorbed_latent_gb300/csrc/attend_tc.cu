@@ -4,32 +4,38 @@
 // What it computes (per worker range of 64-token pages, see decode_plan.cu),
 // following "DeepSeek MLA 吸收式缓存" §2.2–§2.4 and §6.1 (MQA over the latent:
 // key width 576, value width 512):
-//   S[h,t] = q_lat[h] . c_t + q_pe[h] . k_pe_t          (M = 128 heads, N = 64 tokens, K = 576)
+//   S[h,t] = q_lat[h] . c_t + q_pe[h] . k_pe_t          (M = 128 heads, K = 576)
 //   online softmax over t (log2 domain, scale folded in)
-//   O[h,:] += P[h,t] c_t                                (M = 128, N = 512, K = 64)
+//   O[h,:] += P[h,t] c_t                                (M = 128, N = 512)
 //   emitted per segment as O / l and LSE = (m + log2 l) ln 2.
 //
-// Why a CTA pair.  O is 128 x 512 fp32 = 256 KB, all of one SM's tensor memory,
-// leaving nothing for S.  The pair splits the latent width: CTA r owns latent
-// dims [256r, 256r+256) and RoPE dims [32r, 32r+32).  Each CTA
-//  * TMA-loads only its half of every page tile (HBM bytes are not duplicated),
-//  * computes a partial S over its 288 dims into TMEM,
-//  * sends that partial (fp32) to the peer through distributed shared memory
-//    and adds the peer's; fp32 addition commutes, so both CTAs hold identical
-//    scores and take identical softmax decisions,
-//  * accumulates its O half (128 x 256 fp32) in TMEM with P (bf16, in TMEM)
-//    as the A operand and its V half (shared memory, latent-major) as B.
+// Why a CTA pair.  O is 128 x 512 fp32 = 256 KB, all of one SM's tensor memory.
+// The pair splits the latent width: CTA r owns latent dims [256r, 256r+256)
+// and RoPE dims [32r, 32r+32).  Each CTA
+//  * TMA-loads only its half of every 64-token page (HBM bytes are not
+//    duplicated), 4 pages in flight;
+//  * keeps its half of the 128-head query (288 bf16 per head) in TMEM as the
+//    A operand of the score MMA;
+//  * per 32-token half page, computes a partial S (M=128, N=32, K=288) into
+//    TMEM and sends it to the peer's shared memory; adds the peer's partial.
+//    fp32 addition commutes, so both CTAs hold identical scores and take
+//    identical softmax decisions;
+//  * accumulates its O half (128 x 256 fp32) in TMEM with P (bf16, TMEM) as the
+//    A operand and its V half (shared memory, latent-major) as B.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2..5 softmax (thread = head row = TMEM lane).  Every wait is
-// bounded; a timeout records MLA_ERR_TIMEOUT, stops all roles, lets in-flight
-// copies and MMAs land, frees TMEM and returns.
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2..9 softmax.  Softmax warps w and w+4 share TMEM lanes
+// 32*(w%4)..+31 (one head per lane) and split each half page's 32 columns
+// 16/16; the partners combine row maxima and sums through shared memory.
+// The softmax loop is software-pipelined: it sends half page h while it
+// finishes half page h-1, so the exchange latency hides behind work.  Each
+// thread sends its 16 partial scores with asynchronous remote stores that
+// complete on the peer's transaction-counted barrier.
+// Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, stops all roles,
+// lets in-flight copies and MMAs land, frees TMEM and returns.
 //
-// Tensor memory map (512 columns): O half [0,256), S double buffer [256,384),
-// P double buffer (bf16 pairs) [384,448).
-// Shared memory: Q half (4 x [128][64] 128B-swizzled + [128][32] 64B-swizzled),
-// 3 stages of page-tile halves (4 x [64][64] + [64][32]), the peer's partial
-// scores [128][68] fp32, barriers.
+// Tensor memory (512 columns): O [0,256), q_lat half [256,384), q_pe half
+// [384,400), S double buffer [400,464), P double buffer (bf16 pairs) [464,496).
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -39,39 +45,40 @@ namespace {
 
 using namespace tc;
 
-constexpr int TC_THREADS = 192;
-constexpr int STAGES = 3;
-constexpr int TILE = 64;
+constexpr int TC_THREADS = 320;
+constexpr int NSOFT = 256;                                    // softmax threads (warps 2..9)
+constexpr int STAGES = 4;
+constexpr int TILE = 64;                                      // tokens per page / TMA stage
+constexpr int HT = 32;                                        // tokens per half page (MMA N, softmax unit)
 constexpr int HALF_C = 256;
 constexpr int PE_HALF = 32;
-constexpr uint32_t Q_CHUNK = 128 * 64 * 2;                   // 16,384
-constexpr uint32_t Q_PE_OFF = 4 * Q_CHUNK;                   // 65,536
-constexpr uint32_t Q_BYTES = 128 * (HALF_C + PE_HALF) * 2;   // 73,728
-constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                 // 8,192
-constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                 // 32,768
-constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2; // 36,864
-constexpr int XLD = 68;                                      // padded row of the exchange buffer
+constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                  // 8,192: [64 tokens][64 dims] 128B-swizzled
+constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                  // 32,768: [64 tokens][32 dims] 64B-swizzled
+constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2;  // 36,864
+constexpr uint32_t XBYTES = 128 * HT * 4;                     // 16,384: one partial score half tile
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 384;
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_QPE = 384, TM_S = 400, TM_P = 464;
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 struct __align__(1024) SmemTC {
-  uint8_t q[Q_BYTES];
   uint8_t kv[STAGES][KV_BYTES];
-  float xbuf[128 * XLD];
+  float xin[2][128 * HT];   // the peer's partial scores, row-major, 16-byte chunks swizzled by row
+  float red_m[2][2][128];   // partner row maxima [buffer][column half][row]
+  float red_l[2][128];      // partner row sums at a segment end
   uint64_t kv_full[STAGES], kv_empty[STAGES];
-  uint64_t q_full, q_empty;
+  uint64_t q_ready;
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t o_free, mma_done;
-  uint64_t x_full, x_empty;
+  uint64_t x_full[2], x_empty[2];
   uint32_t tmem_base;
   volatile int abort_flag;
 };
-
 static_assert(sizeof(SmemTC) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
-static_assert(offsetof(SmemTC, kv) % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(KV_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct TcArgs {
+  const uint16_t* q_cat;  // [B][128][576] bf16
   const int* plan;
   const int32_t* page_table;
   float* part_o;
@@ -88,14 +95,18 @@ template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(SmemTC& S, uint64_t* bar, uint32_t parity, int* err, int where) {
   auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  // the SM cycle counter is cheap to read; the abort flag and the time limit
+  // are checked every 8 probes (each probe may itself suspend the thread)
+  const long long t0 = clock64();
+  for (uint32_t k = 1;; ++k) {
     if (probe()) return true;
-    if (S.abort_flag) return false;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-      S.abort_flag = 1;
-      raise_error(err, MLA_ERR_TIMEOUT, where);
-      return false;
+    if ((k & 7) == 0) {
+      if (S.abort_flag) return false;
+      if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        S.abort_flag = 1;
+        raise_error(err, MLA_ERR_TIMEOUT, where);
+        return false;
+      }
     }
   }
 }
@@ -110,12 +121,42 @@ __device__ __forceinline__ int row_of_tile(const int* prefix, int B, int x) {
   return lo;
 }
 
+// row of the tile cursor: tiles [start, end) belong to row b of length n
+struct RowCursor {
+  int b, start, end, n;
+  __device__ __forceinline__ void init(const int* prefix, const int* seq_c, int B, int x) {
+    b = row_of_tile(prefix, B, x);
+    start = prefix[b];
+    end = prefix[b + 1];
+    n = seq_c[b];
+  }
+  // loads only when the tile moves to a later row
+  __device__ __forceinline__ void advance(const int* prefix, const int* seq_c, int x) {
+    while (x >= end) {
+      ++b;
+      start = end;
+      end = prefix[b + 1];
+      n = seq_c[b];
+    }
+  }
+};
+
+// what the softmax warps need to know about one half page
+struct HalfInfo {
+  int b;        // row
+  int nvalid;   // valid tokens of the whole page (1..64)
+  int j;        // half index in the page (0, 1)
+  bool seg_first, seg_last;  // first / last half page of the row's segment
+};
+
 __device__ __forceinline__ float u2f(uint32_t v) { return __uint_as_float(v); }
 __device__ __forceinline__ uint32_t f2u(float v) { return __float_as_uint(v); }
 
+// byte offset of 16-byte chunk c (0..7) of row r in a [128][32] fp32 exchange buffer
+__device__ __forceinline__ uint32_t xchunk(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_q_c, const __grid_constant__ CUtensorMap tm_q_pe,
-                     const __grid_constant__ CUtensorMap tm_kv_c, const __grid_constant__ CUtensorMap tm_kv_pe,
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_kv_c, const __grid_constant__ CUtensorMap tm_kv_pe,
                      const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   SmemTC& S = *reinterpret_cast<SmemTC*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,25 +167,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int* prefix = a.plan + PLAN_HDR;
   const int* seq_c = a.plan + PLAN_HDR + B + 1;
   const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
-  const bool has_work = x0 < x1;
+  const int ntiles = x1 - x0;
+  const int nhalf = 2 * ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.kv_full[s], 1);
       mbar_init(&S.kv_empty[s], 1);
     }
-    mbar_init(&S.q_full, 1);
-    mbar_init(&S.q_empty, 1);
+    mbar_init(&S.q_ready, 8);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
-      mbar_init(&S.s_free[s], 4);
-      mbar_init(&S.p_full[s], 4);
+      mbar_init(&S.s_free[s], 8);
+      mbar_init(&S.p_full[s], 8);
       mbar_init(&S.pv_done[s], 1);
+      mbar_init(&S.x_full[s], 1);   // local expect_tx arrival + the peer's bulk bytes
+      mbar_init(&S.x_empty[s], 8);  // one arrival per peer softmax warp
     }
-    mbar_init(&S.o_free, 4);
+    mbar_init(&S.o_free, 8);
     mbar_init(&S.mma_done, 1);
-    mbar_init(&S.x_full, 128);
-    mbar_init(&S.x_empty, 128);
     S.abort_flag = 0;
     fence_barrier_init();
   }
@@ -154,203 +195,271 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   fence_before_sync();
   __syncthreads();
-  cluster_sync();  // the peer arrives on our barriers and writes our exchange buffer
+  cluster_sync();  // the peer arrives on our barriers and writes our exchange buffers
   fence_after_sync();
   const uint32_t tmem = S.tmem_base;
 
-  if (has_work && warp == 0 && lane == 0) {
+  if (ntiles > 0 && warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    prefetch_tmap(&tm_q_c);
-    prefetch_tmap(&tm_q_pe);
-    prefetch_tmap(&tm_kv_c);
-    prefetch_tmap(&tm_kv_pe);
+    // The whole warp walks the tiles; lane l holds the page id of tile
+    // jbase + l of the current row (one gather per 32 tiles), lane 0 waits and
+    // issues the copies.
+    if (lane == 0) {
+      prefetch_tmap(&tm_kv_c);
+      prefetch_tmap(&tm_kv_pe);
+    }
     const uint64_t pol = policy_evict_first();
     int last_use[STAGES];
     for (int s = 0; s < STAGES; ++s) last_use[s] = -1;
-    int q_loads = 0;
-    int b = row_of_tile(prefix, B, x0);
+    RowCursor rc;
+    rc.init(prefix, seq_c, B, x0);
+    int page_row = -1, jbase = 0, page_reg = 0;
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
-      while (b < B - 1 && x >= prefix[b + 1]) ++b;
-      if (x == x0 || x == prefix[b]) {  // new segment: this row's query half
-        if (!wait_bar<false>(S, &S.q_empty, (q_loads & 1) ^ 1, a.err, 1)) break;
-        mbar_arrive_expect_tx(&S.q_full, Q_BYTES);
-        for (int ci = 0; ci < 4; ++ci)
-          tma_load_3d(S.q + ci * Q_CHUNK, &tm_q_c, HALF_C * rank + 64 * ci, 0, b, &S.q_full);
-        tma_load_3d(S.q + Q_PE_OFF, &tm_q_pe, DC + PE_HALF * rank, 0, b, &S.q_full);
-        ++q_loads;
+      rc.advance(prefix, seq_c, x);
+      const int j = x - rc.start;
+      if (rc.b != page_row || j - jbase >= 32) {
+        page_row = rc.b;
+        jbase = j;
+        page_reg = (j + lane < rc.end - rc.start) ? a.page_table[(size_t)rc.b * a.max_pages + j + lane] : 0;
       }
-      const int st = i % STAGES, u = i / STAGES;
-      if (!wait_bar<false>(S, &S.kv_empty[st], (u & 1) ^ 1, a.err, 2)) break;
-      int page = a.page_table[(size_t)b * a.max_pages + (x - prefix[b])];
-      if (page < 0 || page >= a.num_pages) {
-        raise_error(a.err, MLA_ERR_BOUNDS, page);
-        page = 0;
+      int page = __shfl_sync(0xffffffffu, page_reg, j - jbase);
+      int ok = 1;
+      if (lane == 0) {
+        const int st = i % STAGES, u = i / STAGES;
+        ok = wait_bar<false>(S, &S.kv_empty[st], (u & 1) ^ 1, a.err, 2);
+        if (ok) {
+          if (page < 0 || page >= a.num_pages) {
+            raise_error(a.err, MLA_ERR_BOUNDS, page);
+            page = 0;
+          }
+          mbar_arrive_expect_tx(&S.kv_full[st], KV_BYTES);
+          for (int ci = 0; ci < 4; ++ci)
+            tma_load_3d_hint(S.kv[st] + ci * KV_CHUNK, &tm_kv_c, HALF_C * rank + 64 * ci, 0, page, &S.kv_full[st],
+                             pol);
+          tma_load_3d_hint(S.kv[st] + KV_PE_OFF, &tm_kv_pe, DC + PE_HALF * rank, 0, page, &S.kv_full[st], pol);
+          last_use[st] = u;
+        }
       }
-      mbar_arrive_expect_tx(&S.kv_full[st], KV_BYTES);
-      for (int ci = 0; ci < 4; ++ci)
-        tma_load_3d_hint(S.kv[st] + ci * KV_CHUNK, &tm_kv_c, HALF_C * rank + 64 * ci, 0, page, &S.kv_full[st], pol);
-      tma_load_3d_hint(S.kv[st] + KV_PE_OFF, &tm_kv_pe, DC + PE_HALF * rank, 0, page, &S.kv_full[st], pol);
-      last_use[st] = u;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
-    if (S.abort_flag) {  // let copies in flight land before the CTA can exit
+    if (lane == 0 && S.abort_flag) {  // let copies in flight land before the CTA can exit
       for (int s = 0; s < STAGES; ++s)
         if (last_use[s] >= 0) (void)mbar_wait(&S.kv_full[s], last_use[s] & 1);
-      if (q_loads > 0) (void)mbar_wait(&S.q_full, (q_loads - 1) & 1);
     }
-  } else if (has_work && warp == 1 && lane == 0) {
+  } else if (ntiles > 0 && warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc_s = idesc_bf16_f32(128, TILE, false, false);
+    // order: S(h), then PV(h-2); S(h) needs the softmax to have read S(h-2),
+    // PV(h-2) needs P(h-2).
+    const uint32_t idesc_s = idesc_bf16_f32(128, HT, false, false);
     const uint32_t idesc_pv = idesc_bf16_f32(128, HALF_C, false, true);
-    const uint32_t q_addr = smem_u32(S.q);
     int q_seen = 0, pv_segments = 0;
-    int prev_i = -1, prev_st = 0;
-    bool prev_first = false, ok = true;
+    bool ok = true;
+    RowCursor rc;          // cursor of the S side
+    RowCursor rc_pv;       // cursor of the PV side (two half pages behind)
+    rc.init(prefix, seq_c, B, x0);
+    rc_pv = rc;
 
-    auto issue_pv = [&](int j, int st, bool first) -> bool {
-      const int sb = j & 1;
-      if (!wait_bar<false>(S, &S.p_full[sb], (j >> 1) & 1, a.err, 6)) return false;
-      if (first) {
+    auto issue_pv = [&](int g) -> bool {  // PV of half page g
+      const int i = g >> 1, jj = g & 1, pb = g & 1, st = i % STAGES;
+      if (!wait_bar<false>(S, &S.p_full[pb], (g >> 1) & 1, a.err, 6)) return false;
+      bool seg_first = false;
+      if (jj == 0) {
+        const int xr = x0 + i;
+        rc_pv.advance(prefix, seq_c, xr);
+        seg_first = (xr == x0) || (xr == rc_pv.start);
+      }
+      // the first half page of a segment overwrites O: wait for the previous
+      // segment's epilogue to have read it
+      if (seg_first) {
         if (pv_segments > 0 && !wait_bar<false>(S, &S.o_free, (pv_segments - 1) & 1, a.err, 7)) return false;
         ++pv_segments;
       }
       fence_after_sync();
       const uint32_t kv_addr = smem_u32(S.kv[st]);
 #pragma unroll
-      for (int kk = 0; kk < TILE / 16; ++kk)
-        mma_ts(tmem + TM_O, tmem + TM_P + 32 * sb + 8 * kk,
-               smem_desc(kv_addr + kk * 16 * 128, KV_CHUNK, 1024, SWIZZLE_128B), idesc_pv,
-               (first && kk == 0) ? 0u : 1u);
-      mma_commit(&S.pv_done[sb]);
-      mma_commit(&S.kv_empty[st]);
+      for (int kk = 0; kk < HT / 16; ++kk)
+        mma_ts(tmem + TM_O, tmem + TM_P + 16 * pb + 8 * kk,
+               smem_desc(kv_addr + (HT * jj + 16 * kk) * 128, KV_CHUNK, 1024, SWIZZLE_128B), idesc_pv,
+               (seg_first && kk == 0) ? 0u : 1u);
+      mma_commit(&S.pv_done[pb]);
+      if (jj == 1) mma_commit(&S.kv_empty[st]);
       return true;
     };
 
-    int b = row_of_tile(prefix, B, x0);
-    for (int x = x0, i = 0; x < x1; ++x, ++i) {
-      while (b < B - 1 && x >= prefix[b + 1]) ++b;
-      const bool first = (x == x0) || (x == prefix[b]);
-      const bool last = (x + 1 == x1) || (x + 1 == prefix[b + 1]);
-      if (first) {
-        if (!wait_bar<false>(S, &S.q_full, q_seen & 1, a.err, 3)) { ok = false; break; }
-        ++q_seen;
+    for (int h = 0; h < nhalf; ++h) {
+      const int i = h >> 1, jj = h & 1, st = i % STAGES, sb = h & 1;
+      if (jj == 0) {
+        const int x = x0 + i;
+        rc.advance(prefix, seq_c, x);
+        if (x == x0 || x == rc.start) {  // the query of this segment must be in TMEM
+          if (!wait_bar<false>(S, &S.q_ready, q_seen & 1, a.err, 3)) { ok = false; break; }
+          ++q_seen;
+        }
+        if (!wait_bar<false>(S, &S.kv_full[st], (i / STAGES) & 1, a.err, 4)) { ok = false; break; }
       }
-      const int st = i % STAGES, u = i / STAGES, sb = i & 1;
-      if (!wait_bar<false>(S, &S.kv_full[st], u & 1, a.err, 4)) { ok = false; break; }
-      if (!wait_bar<false>(S, &S.s_free[sb], ((i >> 1) & 1) ^ 1, a.err, 5)) { ok = false; break; }
+      if (!wait_bar<false>(S, &S.s_free[sb], ((h >> 1) & 1) ^ 1, a.err, 5)) { ok = false; break; }
       fence_after_sync();
       const uint32_t kv_addr = smem_u32(S.kv[st]);
-      const uint32_t d = tmem + TM_S + TILE * sb;
+      const uint32_t d = tmem + TM_S + HT * sb;
 #pragma unroll
       for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(d, smem_desc(q_addr + ci * Q_CHUNK + kk * 32, 16, 1024, SWIZZLE_128B),
-                 smem_desc(kv_addr + ci * KV_CHUNK + kk * 32, 16, 1024, SWIZZLE_128B), idesc_s,
+          mma_ts(d, tmem + TM_Q + ci * 32 + kk * 8,
+                 smem_desc(kv_addr + ci * KV_CHUNK + jj * (HT * 128) + kk * 32, 16, 1024, SWIZZLE_128B), idesc_s,
                  (ci | kk) != 0 ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
-        mma_ss(d, smem_desc(q_addr + Q_PE_OFF + kk * 32, 16, 512, SWIZZLE_64B),
-               smem_desc(kv_addr + KV_PE_OFF + kk * 32, 16, 512, SWIZZLE_64B), idesc_s, 1u);
+        mma_ts(d, tmem + TM_QPE + kk * 8,
+               smem_desc(kv_addr + KV_PE_OFF + jj * (HT * 64) + kk * 32, 16, 512, SWIZZLE_64B), idesc_s, 1u);
       mma_commit(&S.s_full[sb]);
-      if (last) mma_commit(&S.q_empty);
-      if (prev_i >= 0 && !issue_pv(prev_i, prev_st, prev_first)) { ok = false; break; }
-      prev_i = i;
-      prev_st = st;
-      prev_first = first;
+      if (h >= 2 && !issue_pv(h - 2)) { ok = false; break; }
     }
-    if (ok && prev_i >= 0) (void)issue_pv(prev_i, prev_st, prev_first);
+    if (ok && nhalf >= 2) ok = issue_pv(nhalf - 2);
+    if (ok) (void)issue_pv(nhalf - 1);
     mma_commit(&S.mma_done);
     (void)mbar_wait(&S.mma_done, 0);  // every issued MMA has finished
-  } else if (has_work && warp >= 2) {
+  } else if (ntiles > 0 && warp >= 2) {
     // ------------------------------------------------------------ softmax
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;  // head = TMEM lane
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + TM_S, t_p = tmem + lane_off + TM_P, t_o = tmem + lane_off + TM_O;
-    const uint32_t peer_row = mapa(smem_u32(&S.xbuf[row * XLD]), peer);
-    const uint32_t peer_full = mapa(smem_u32(&S.x_full), peer);
-    const uint32_t peer_empty = mapa(smem_u32(&S.x_empty), peer);
-    const float* my_row = &S.xbuf[row * XLD];
+    const int q4 = warp & 3;               // TMEM lane quadrant
+    const int ch = (warp - 2) >> 2;        // column half of each half page: 0 or 1
+    const int row = q4 * 32 + lane;        // head = TMEM lane
+    const int stid = threadIdx.x - 64;     // 0..255
+    const uint32_t t_row = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t pair_bar = 1 + q4;      // named barrier shared with the partner warp
+    const float c = a.scale_log2;          // > 0
+    uint32_t peer_xin[2], peer_xfull[2], peer_xempty[2];  // cluster addresses in the peer CTA
+    for (int k = 0; k < 2; ++k) {
+      peer_xin[k] = mapa(smem_u32(S.xin[k]), peer);
+      peer_xfull[k] = mapa(smem_u32(&S.x_full[k]), peer);
+      peer_xempty[k] = mapa(smem_u32(&S.x_empty[k]), peer);
+    }
     float m_ref = -INFINITY, l = 0.f;
-    int b = row_of_tile(prefix, B, x0);
-    for (int x = x0, i = 0; x < x1; ++x, ++i) {
-      while (b < B - 1 && x >= prefix[b + 1]) ++b;
-      const bool first = (x == x0) || (x == prefix[b]);
-      const bool last = (x + 1 == x1) || (x + 1 == prefix[b + 1]);
-      const int nvalid = min(TILE, seq_c[b] - TILE * (x - prefix[b]));
-      const int st = i % STAGES, sb = i & 1;
+    RowCursor rc;
+    rc.init(prefix, seq_c, B, x0);
+    uint32_t own_a[16], own_b[16];
+    HalfInfo info_a, info_b;
 
-      // (a) a tile past the end of its sequence: zero the unused value rows so
-      //     that P = 0 never meets stale (possibly non-finite) cache contents
-      if (nvalid < TILE) {
-        const bool ok = wait_bar<false>(S, &S.kv_full[st], (i / STAGES) & 1, a.err, 8);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int units = (TILE - nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
-        for (int idx = threadIdx.x - 64; idx < units; idx += 128) {
-          const int r = nvalid + idx / 32, ci = (idx % 32) / 8, v = idx % 8;
-          *reinterpret_cast<uint4*>(S.kv[st] + ci * KV_CHUNK + r * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+    // A wait that fails does not leave the stage: it marks the thread failed and
+    // the stage runs on (every later wait returns at once), so that the pair
+    // barrier is still reached by both partner warps; the partners leave the
+    // loop together, at the reduction barrier of stage B.
+    bool failed = false;
+
+    // A(h): read this CTA's partial scores of half page h and send them to the peer
+    auto stage_a = [&](int h, uint32_t* own, HalfInfo& inf) {
+      const int i = h >> 1, jj = h & 1, sb = h & 1, st = i % STAGES;
+      const int x = x0 + i;
+      if (jj == 0) rc.advance(prefix, seq_c, x);
+      inf.b = rc.b;
+      inf.nvalid = min(TILE, rc.n - TILE * (x - rc.start));
+      inf.j = jj;
+      inf.seg_first = jj == 0 && (x == x0 || x == rc.start);
+      inf.seg_last = jj == 1 && (x + 1 == x1 || x + 1 == rc.end);
+      if (inf.seg_first) {
+        // this row's query half into TMEM; every S of the previous segment has
+        // completed (this thread waited for each of them)
+        const uint16_t* qrow = a.q_cat + ((size_t)rc.b * 128 + row) * DK;
+        const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 128 * ch);
+        uint32_t v[64];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint4 u = qc[k];
+          v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
         }
-        fence_proxy_async_smem();
+        uint32_t pe[16];
+        const uint4* qp = reinterpret_cast<const uint4*>(qrow + DC + PE_HALF * rank);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 u = qp[k];
+          pe[4 * k] = u.x; pe[4 * k + 1] = u.y; pe[4 * k + 2] = u.z; pe[4 * k + 3] = u.w;
+        }
+        tmem_st32(t_row + TM_Q + 64 * ch, v);
+        tmem_st32(t_row + TM_Q + 64 * ch + 32, v + 32);
+        if (ch == 0) tmem_st16(t_row + TM_QPE, pe);
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.q_ready);
       }
-
-      // (b) this CTA's partial scores
-      bool ok = wait_bar<false>(S, &S.s_full[sb], (i >> 1) & 1, a.err, 9);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (stid == 0) mbar_arrive_expect_tx(&S.x_full[sb], XBYTES);  // the peer's partial for this half page
+      if (!wait_bar<false>(S, &S.s_full[sb], (h >> 1) & 1, a.err, 9)) failed = true;
+      __syncwarp();
       fence_after_sync();
-      uint32_t r[TILE];
-      tmem_ld32(t_s + TILE * sb, r);
-      tmem_ld32(t_s + TILE * sb + 32, r + 32);
+      tmem_ld16(t_row + TM_S + HT * sb + 16 * ch, own);
       tmem_ld_wait();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.s_free[sb]);
-
-      // (c) swap partial scores with the peer CTA
-      ok = wait_bar<true>(S, &S.x_empty, (i & 1) ^ 1, a.err, 10);
-      if (!__all_sync(0xffffffffu, ok)) break;
-#pragma unroll
-      for (int k = 0; k < TILE / 4; ++k)
-        st_cluster_v4(peer_row + 16 * k, u2f(r[4 * k]), u2f(r[4 * k + 1]), u2f(r[4 * k + 2]), u2f(r[4 * k + 3]));
-      mbar_arrive_remote(peer_full);
-      ok = wait_bar<true>(S, &S.x_full, i & 1, a.err, 11);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      float s[TILE];
-#pragma unroll
-      for (int k = 0; k < TILE / 4; ++k) {
-        const float4 v = *reinterpret_cast<const float4*>(my_row + 4 * k);
-        s[4 * k + 0] = u2f(r[4 * k + 0]) + v.x;
-        s[4 * k + 1] = u2f(r[4 * k + 1]) + v.y;
-        s[4 * k + 2] = u2f(r[4 * k + 2]) + v.z;
-        s[4 * k + 3] = u2f(r[4 * k + 3]) + v.w;
+      if (jj == 0 && inf.nvalid < TILE) {
+        // page past the end of its sequence: zero the unused value rows so that
+        // P = 0 never meets stale (possibly non-finite) cache contents
+        const int units = (TILE - inf.nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
+        for (int idx = stid; idx < units; idx += NSOFT) {
+          const int r = inf.nvalid + idx / 32, ci = (idx % 32) / 8, v = idx % 8;
+          *reinterpret_cast<uint4*>(S.kv[st] + ci * KV_CHUNK + r * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
       }
-      mbar_arrive_remote(peer_empty);
-
-      // (d) online softmax in the log2 domain with a lazily moved reference max
-      float mt = -INFINITY;
+      // the peer has consumed what we sent into this buffer two half pages ago
+      if (lane == 0 && !wait_bar<true>(S, &S.x_empty[sb], ((h >> 1) & 1) ^ 1, a.err, 10)) failed = true;
+      __syncwarp();
 #pragma unroll
-      for (int t = 0; t < TILE; ++t) {
-        s[t] = t < nvalid ? s[t] * a.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[t]);
+      for (int k = 0; k < 4; ++k)
+        st_async_v4(peer_xin[sb] + xchunk(row, 4 * ch + k), own[4 * k], own[4 * k + 1], own[4 * k + 2],
+                    own[4 * k + 3], peer_xfull[sb]);
+    };
+
+    // B(h): add the peer's partial, online softmax, P into TMEM, epilogue at a
+    // segment end; returns false (on both partner warps alike) once either failed
+    auto stage_b = [&](int h, const uint32_t* own, const HalfInfo& inf) -> bool {
+      const int sb = h & 1;
+      if (!wait_bar<false>(S, &S.x_full[sb], (h >> 1) & 1, a.err, 11)) failed = true;
+      __syncwarp();
+      const uint8_t* xi = reinterpret_cast<const uint8_t*>(S.xin[sb]);
+      float s[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(xi + xchunk(row, 4 * ch + k));
+        s[4 * k + 0] = u2f(own[4 * k + 0]) + v.x;
+        s[4 * k + 1] = u2f(own[4 * k + 1]) + v.y;
+        s[4 * k + 2] = u2f(own[4 * k + 2]) + v.z;
+        s[4 * k + 3] = u2f(own[4 * k + 3]) + v.w;
       }
-      if (first) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty[sb]);  // our buffer may be refilled
+      const int t0 = HT * inf.j + 16 * ch;  // token index of s[0] in the page
+      if (inf.nvalid < TILE) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (t0 + k >= inf.nvalid) s[k] = -INFINITY;
+      }
+      float mraw = s[0];
+#pragma unroll
+      for (int k = 1; k < 16; ++k) mraw = fmaxf(mraw, s[k]);
+      S.red_m[sb][ch][row] = mraw * c;
+      const bool pair_ok = named_barrier_and(pair_bar, 64, !failed);
+      const float mt = fmaxf(S.red_m[sb][0][row], S.red_m[sb][1][row]);
+      if (inf.seg_first) {
         m_ref = mt;
         l = 0.f;
       }
-      const bool need = !first && mt > m_ref + RESCALE_LOG2;
+      const bool need = !inf.seg_first && mt > m_ref + RESCALE_LOG2;
       if (__any_sync(0xffffffffu, need)) {
         // O may only be touched once every PV issued so far has completed
-        ok = wait_bar<false>(S, &S.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 12);
-        if (!__all_sync(0xffffffffu, ok)) break;
+        if (!wait_bar<false>(S, &S.pv_done[(h - 1) & 1], ((h - 1) >> 1) & 1, a.err, 12)) failed = true;
+        __syncwarp();
         fence_after_sync();
         const float alpha = need ? ex2(m_ref - mt) : 1.f;
 #pragma unroll 1
-        for (int ch = 0; ch < HALF_C / 32; ++ch) {
+        for (int k32 = 0; k32 < 4; ++k32) {
           uint32_t o[32];
-          tmem_ld32(t_o + 32 * ch, o);
+          const uint32_t col = t_row + TM_O + 128 * ch + 32 * k32;
+          tmem_ld32(col, o);
           tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = f2u(u2f(o[k]) * alpha);
-          tmem_st32(t_o + 32 * ch, o);
+          tmem_st32(col, o);
         }
         tmem_st_wait();
         if (need) {
@@ -358,50 +467,64 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           m_ref = mt;
         }
       }
+      // p = 2^(s*c - m_ref), two at a time in half precision (the exponent is
+      // <= RESCALE_LOG2, so p <= 256; P is rounded to bf16 for the MMA anyway)
+      uint32_t pk[8];
       float sum = 0.f;
-      uint32_t pk[TILE / 2];
 #pragma unroll
-      for (int c = 0; c < TILE / 2; ++c) {
-        const float p0 = ex2(s[2 * c] - m_ref), p1 = ex2(s[2 * c + 1] - m_ref);
-        sum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+      for (int k = 0; k < 8; ++k) {
+        const __half2 xh = __floats2half2_rn(fmaf(s[2 * k], c, -m_ref), fmaf(s[2 * k + 1], c, -m_ref));
+        const uint32_t yh = ex2_h2(*reinterpret_cast<const uint32_t*>(&xh));
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&yh));
+        sum += p.x + p.y;
+        pk[k] = pack_bf16x2(p.x, p.y);
       }
       l += sum;
-
-      // (e) P into TMEM once PV(i-2) has finished with that buffer
-      ok = wait_bar<false>(S, &S.pv_done[sb], ((i >> 1) & 1) ^ 1, a.err, 13);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // P buffer sb is free once PV(h-2) has completed
+      if (!wait_bar<false>(S, &S.pv_done[sb], ((h >> 1) & 1) ^ 1, a.err, 13)) failed = true;
+      __syncwarp();
       fence_after_sync();
-      tmem_st32(t_p + 32 * sb, pk);
+      tmem_st8(t_row + TM_P + 16 * sb + 8 * ch, pk);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.p_full[sb]);
-
-      // (f) end of the row's segment: O / l and the natural-log LSE
-      if (last) {
-        ok = wait_bar<false>(S, &S.pv_done[sb], (i >> 1) & 1, a.err, 14);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      if (inf.seg_last) {
+        if (!wait_bar<false>(S, &S.pv_done[sb], (h >> 1) & 1, a.err, 14)) failed = true;
+        __syncwarp();
         fence_after_sync();
-        const float inv = 1.f / l;
-        const int seg = worker + b;
-        float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank;
+        S.red_l[ch][row] = l;
+        named_barrier(pair_bar, 64);
+        const float L = S.red_l[0][row] + S.red_l[1][row];
+        const float inv = 1.f / L;
+        const int seg = worker + inf.b;
+        float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ch;
 #pragma unroll 1
-        for (int ch = 0; ch < HALF_C / 32; ++ch) {
+        for (int k32 = 0; k32 < 4; ++k32) {
           uint32_t o[32];
-          tmem_ld32(t_o + 32 * ch, o);
+          tmem_ld32(t_row + TM_O + 128 * ch + 32 * k32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            reinterpret_cast<float4*>(dst + 32 * ch)[k] =
+            reinterpret_cast<float4*>(dst + 32 * k32)[k] =
                 make_float4(u2f(o[4 * k]) * inv, u2f(o[4 * k + 1]) * inv, u2f(o[4 * k + 2]) * inv,
                             u2f(o[4 * k + 3]) * inv);
         }
-        if (rank == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
+        if (rank == 0 && ch == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.o_free);
       }
+      return pair_ok;
+    };
+
+    // software pipeline: A(h) then B(h-1); even and odd halves swap the buffers
+    for (int h = 0; h <= nhalf; h += 2) {
+      if (h < nhalf) stage_a(h, own_a, info_a);
+      if (h >= 1 && !stage_b(h - 1, own_b, info_b)) break;
+      if (h + 1 > nhalf) break;
+      if (h + 1 < nhalf) stage_a(h + 1, own_b, info_b);
+      if (!stage_b(h, own_a, info_a)) break;
     }
   }
 
@@ -455,6 +578,21 @@ constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
 std::mutex g_tc_mu;
 int g_tc_workers[64] = {};
 
+cudaLaunchConfig_t launch_config(int workers, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * workers);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 }  // namespace
 
 // persistent workers (CTA pairs) that fit on the device at once
@@ -466,17 +604,8 @@ int attend_tc_workers(int num_sms) {
     int clusters = 0;
     if (cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
         cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (num_sms / 2));
-      cfg.blockDim = dim3(TC_THREADS);
-      cfg.dynamicSmemBytes = kSmemBytes;
       cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
+      cudaLaunchConfig_t cfg = launch_config(num_sms / 2, nullptr, attr);
       if (cudaOccupancyMaxActiveClusters(&clusters, attend_tc_kernel, &cfg) != cudaSuccess) clusters = 0;
     }
     (void)cudaGetLastError();
@@ -489,16 +618,16 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, float* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (H != 128 || fmt != MLA_FMT_BF16 || workers < 1) return cudaErrorNotSupported;
-  CUtensorMap tq_c, tq_pe, tkv_c, tkv_pe;
-  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per query row / token slot
-  if (!encode_3d(&tq_c, q_cat, DK, 128, B, row, row * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_3d(&tkv_c, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling
+  CUtensorMap tkv_c, tkv_pe;
+  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per token slot
+  if (!encode_3d(&tkv_c, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_3d(&tkv_pe, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   TcArgs args;
+  args.q_cat = static_cast<const uint16_t*>(q_cat);
   args.plan = plan;
   args.page_table = page_table;
   args.part_o = part_o;
@@ -508,19 +637,9 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   args.max_pages = max_pages;
   args.num_pages = num_pages;
   args.scale_log2 = scale * 1.4426950408889634f;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * workers);
-  cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tq_c, tq_pe, tkv_c, tkv_pe, args);
+  cudaLaunchConfig_t cfg = launch_config(workers, s, attr);
+  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tkv_c, tkv_pe, args);
 }
 
 }  // namespace mla

@@ -175,7 +175,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   if (st != MLA_OK) return st;
   if (B == 0) return MLA_OK;
   if (!page_table || !seqlens || !aligned(page_table, 4) || !aligned(seqlens, 4)) return MLA_ERR_INVALID;
-  if (!(scale == scale)) return MLA_ERR_INVALID;
+  if (!(scale > 0.f) || scale == INFINITY) return MLA_ERR_INVALID;
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
