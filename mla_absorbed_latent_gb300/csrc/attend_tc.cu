@@ -11,31 +11,47 @@
 //
 // Why a CTA pair.  O is 128 x 512 fp32 = 256 KB, all of one SM's tensor memory.
 // The pair splits the latent width: CTA r owns latent dims [256r, 256r+256)
-// and RoPE dims [32r, 32r+32).  Each CTA
-//  * TMA-loads only its half of every 64-token page (HBM bytes are not
-//    duplicated), 4 pages in flight;
-//  * keeps its half of the 128-head query (288 bf16 per head) in TMEM as the
-//    A operand of the score MMA;
-//  * per 32-token half page, computes a partial S (M=128, N=32, K=288) into
-//    TMEM and sends it to the peer's shared memory; adds the peer's partial.
-//    fp32 addition commutes, so both CTAs hold identical scores and take
-//    identical softmax decisions;
-//  * accumulates its O half (128 x 256 fp32) in TMEM with P (bf16, TMEM) as the
-//    A operand and its V half (shared memory, latent-major) as B.
+// and RoPE dims [32r, 32r+32), TMA-loads only that half of every 64-token page
+// (HBM bytes are not duplicated), and accumulates its O half (128 x 256 fp32,
+// TMEM) += P . V_half.  The score of a head needs both halves, so the pair also
+// splits the softmax by head: CTA r runs the softmax of heads [64r, 64r+64).
+// Per page each CTA
+//  * computes its partial S (M=128, N=64, K=288) into TMEM, with its half of
+//    q_lat in TMEM and its half of q_pe in shared memory as A operands;
+//  * sends the peer the partial scores of the peer's 64 heads, already in log2
+//    units, as fp16 (8 KB; asynchronous remote stores counted on the peer's
+//    transaction barrier);
+//  * adds the peer's partial to its own for its 64 heads, runs the online
+//    softmax there and writes P (bf16) for those heads into its own P tile and
+//    into the peer's (8 KB), with each head's O rescale factor and, at a
+//    segment end, 1/l;
+//  * once both halves of P are in place, issues O_half += P . V_half.
+// Distributed shared memory moves ~14.5 bytes per cycle per SM each way, less
+// than the ~23 bytes per cycle per SM that HBM delivers, so the 16.5 KB per page
+// each way (against 36 KB of cache streamed) is the design's budget: fp32
+// partials for all 128 heads (32 KB) would cap the kernel well below the HBM
+// roofline.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2..9 softmax.  Softmax warps w and w+4 share TMEM lanes
-// 32*(w%4)..+31 (one head per lane) and split each half page's 32 columns
-// 16/16; the partners combine row maxima and sums through shared memory.
-// The softmax loop is software-pipelined: it sends half page h while it
-// finishes half page h-1, so the exchange latency hides behind work.  Each
-// thread sends its 16 partial scores with asynchronous remote stores that
-// complete on the peer's transaction-counted barrier.
-// Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, stops all roles,
-// lets in-flight copies and MMAs land, frees TMEM and returns.
+// MMA issue.  A tcgen05.mma blocks its issuing thread while an MMA on the same
+// accumulator is in flight, so three threads issue MMAs: S of even pages, S of
+// odd pages (two score buffers in TMEM), and P.V (O).  The P.V completion is
+// signalled to both CTAs (multicast commit): a P tile is rewritten only once
+// both CTAs' P.V have read it.
 //
-// Tensor memory (512 columns): O [0,256), q_lat half [256,384), q_pe half
-// [384,400), S double buffer [400,464), P double buffer (bf16 pairs) [464,496).
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 S issuer (even pages)
+// and TMEM owner, warp 2 S issuer (odd pages), warp 3 P.V issuer, warps 4..11
+// softmax.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31; two warps
+// share each quadrant and split a page's 64 tokens 32/32.  The four warps on
+// this CTA's own heads ("owners") run the softmax, combining row maxima and
+// sums with their partner through shared memory.  The four warps on the
+// peer's heads ("senders") ship those heads' partial scores, and one page
+// later apply the peer's rescale factors to the O rows of those heads and
+// release the P.V.  Every wait is bounded; a timeout records MLA_ERR_TIMEOUT,
+// raises the abort flag of both CTAs, lets in-flight copies and MMAs land,
+// frees TMEM and returns.
+//
+// Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
+// buffer [384,512).
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -45,37 +61,46 @@ namespace {
 
 using namespace tc;
 
-constexpr int TC_THREADS = 320;
-constexpr int NSOFT = 256;                                    // softmax threads (warps 2..9)
+constexpr int TC_THREADS = 384;
+constexpr int SOFT_WARP0 = 4;
 constexpr int STAGES = 4;
-constexpr int TILE = 64;                                      // tokens per page / TMA stage
-constexpr int HT = 32;                                        // tokens per half page (MMA N, softmax unit)
+constexpr int TILE = 64;                                      // tokens per page / TMA stage / S tile
 constexpr int HALF_C = 256;
 constexpr int PE_HALF = 32;
+constexpr int OWN_H = 64;                                     // heads whose softmax one CTA runs
 constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                  // 8,192: [64 tokens][64 dims] 128B-swizzled
 constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                  // 32,768: [64 tokens][32 dims] 64B-swizzled
 constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2;  // 36,864
-constexpr uint32_t XBYTES = 128 * HT * 4;                     // 16,384: one partial score half tile
+constexpr uint32_t P_BYTES = 128 * TILE * 2;                  // 16,384: [128 heads][64 tokens] 128B-swizzled
+constexpr uint32_t X_BYTES = OWN_H * TILE * 2;                // 8,192: fp16 partial scores of 64 heads
+constexpr uint32_t MSG_BYTES = OWN_H * 8;                     // 512: (rescale factor, 1/l) per head
+constexpr uint32_t PIN_BYTES = OWN_H * TILE * 2 + MSG_BYTES;  // P rows of the peer's heads + their messages
+constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0, TM_Q = 256, TM_QPE = 384, TM_S = 400, TM_P = 464;
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
+constexpr float FP16_MAX = 65504.f;
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 struct __align__(1024) SmemTC {
   uint8_t kv[STAGES][KV_BYTES];
-  float xin[2][128 * HT];   // the peer's partial scores, row-major, 16-byte chunks swizzled by row
-  float red_m[2][2][128];   // partner row maxima [buffer][column half][row]
-  float red_l[2][128];      // partner row sums at a segment end
+  uint8_t p[2][P_BYTES];
+  uint8_t xin[2][X_BYTES];  // the peer's fp16 partials for our heads; row = 128 B, chunks swizzled by row
+  uint8_t qpe[QPE_BYTES];
+  float2 msg[2][OWN_H];     // from the peer, per peer head: (O rescale factor, 1/l at a segment end)
+  float red_m[2][2][128];   // partner row maxima [page parity][column half][row]
+  float red_l[2][128];      // partner row sums at a segment end [column half][row]
   uint64_t kv_full[STAGES], kv_empty[STAGES];
-  uint64_t q_ready;
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t o_free, mma_done;
-  uint64_t x_full[2], x_empty[2];
+  uint64_t q_ready;         // q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], pv_done[2], pv_both[2];
+  uint64_t x_full[2], x_empty[2], pin_full[2];
+  uint64_t o_free, mma_done[3];
   uint32_t tmem_base;
   volatile int abort_flag;
 };
 static_assert(sizeof(SmemTC) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
-static_assert(KV_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(KV_BYTES % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct TcArgs {
   const uint16_t* q_cat;  // [B][128][576] bf16
@@ -88,15 +113,14 @@ struct TcArgs {
   float scale_log2;
 };
 
-// Bounded wait shared by all roles: gives up after WAIT_LIMIT_NS (records
-// MLA_ERR_TIMEOUT and raises the CTA's abort flag) or as soon as another role
-// has aborted.
+// Bounded wait shared by all roles: gives up after WAIT_LIMIT_CYCLES (records
+// MLA_ERR_TIMEOUT and raises the abort flag of this CTA and of its peer) or
+// once an abort was raised.  The abort flag and the clock are checked every 8
+// probes.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(SmemTC& S, uint64_t* bar, uint32_t parity, int* err, int where) {
   auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
-  // the SM cycle counter is cheap to read; the abort flag and the time limit
-  // are checked every 8 probes (each probe may itself suspend the thread)
   const long long t0 = clock64();
   for (uint32_t k = 1;; ++k) {
     if (probe()) return true;
@@ -104,6 +128,7 @@ __device__ __forceinline__ bool wait_bar(SmemTC& S, uint64_t* bar, uint32_t pari
       if (S.abort_flag) return false;
       if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
         S.abort_flag = 1;
+        st_cluster_u32(mapa(smem_u32((const void*)&S.abort_flag), cluster_ctarank() ^ 1u), 1u);
         raise_error(err, MLA_ERR_TIMEOUT, where);
         return false;
       }
@@ -141,23 +166,19 @@ struct RowCursor {
   }
 };
 
-// what the softmax warps need to know about one half page
-struct HalfInfo {
-  int b;        // row
-  int nvalid;   // valid tokens of the whole page (1..64)
-  int j;        // half index in the page (0, 1)
-  bool seg_first, seg_last;  // first / last half page of the row's segment
-};
-
 __device__ __forceinline__ float u2f(uint32_t v) { return __uint_as_float(v); }
 __device__ __forceinline__ uint32_t f2u(float v) { return __float_as_uint(v); }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+__device__ __forceinline__ float fp16_clamp(float v) { return fminf(fmaxf(v, -FP16_MAX), FP16_MAX); }
 
-// byte offset of 16-byte chunk c (0..7) of row r in a [128][32] fp32 exchange buffer
-__device__ __forceinline__ uint32_t xchunk(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+// byte offset of 16-byte chunk c (0..7, 8 tokens) of row r in a [64][64] fp16 exchange tile
+__device__ __forceinline__ uint32_t xoff(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+// byte offset of 16-byte unit u (0..7, 8 tokens) of row r in a 128B-swizzled [128][64] bf16 tile
+__device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_kv_c, const __grid_constant__ CUtensorMap tm_kv_pe,
-                     const TcArgs a) {
+                     const __grid_constant__ CUtensorMap tm_q_pe, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   SmemTC& S = *reinterpret_cast<SmemTC*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -168,24 +189,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int* seq_c = a.plan + PLAN_HDR + B + 1;
   const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
   const int ntiles = x1 - x0;
-  const int nhalf = 2 * ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.kv_full[s], 1);
       mbar_init(&S.kv_empty[s], 1);
     }
-    mbar_init(&S.q_ready, 8);
+    mbar_init(&S.q_ready, 9);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
       mbar_init(&S.s_free[s], 8);
       mbar_init(&S.p_full[s], 8);
       mbar_init(&S.pv_done[s], 1);
-      mbar_init(&S.x_full[s], 1);   // local expect_tx arrival + the peer's bulk bytes
-      mbar_init(&S.x_empty[s], 8);  // one arrival per peer softmax warp
+      mbar_init(&S.pv_both[s], 2);   // this CTA's and the peer's P.V commits
+      mbar_init(&S.x_full[s], 1);    // local expect_tx arrival + the peer's fp16 partial bytes
+      mbar_init(&S.x_empty[s], 4);   // one remote arrival per peer owner warp
+      mbar_init(&S.pin_full[s], 1);  // local expect_tx arrival + the peer's P rows and messages
     }
     mbar_init(&S.o_free, 8);
-    mbar_init(&S.mma_done, 1);
+    for (int k = 0; k < 3; ++k) mbar_init(&S.mma_done[k], 1);
     S.abort_flag = 0;
     fence_barrier_init();
   }
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (ntiles > 0 && warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // The whole warp walks the tiles; lane l holds the page id of tile
+    // The whole warp walks the pages; lane l holds the page id of tile
     // jbase + l of the current row (one gather per 32 tiles), lane 0 waits and
     // issues the copies.
     if (lane == 0) {
@@ -246,285 +268,356 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if (last_use[s] >= 0) (void)mbar_wait(&S.kv_full[s], last_use[s] & 1);
     }
-  } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    // order: S(h), then PV(h-2); S(h) needs the softmax to have read S(h-2),
-    // PV(h-2) needs P(h-2).
-    const uint32_t idesc_s = idesc_bf16_f32(128, HT, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, HALF_C, false, true);
-    int q_seen = 0, pv_segments = 0;
-    bool ok = true;
-    RowCursor rc;          // cursor of the S side
-    RowCursor rc_pv;       // cursor of the PV side (two half pages behind)
+  } else if (ntiles > 0 && (warp == 1 || warp == 2) && lane == 0) {
+    // ------------------------------------------------------------ S issuers
+    // warp 1: pages 0, 2, 4, ... of this worker; warp 2: pages 1, 3, 5, ...
+    const int parity = warp - 1;
+    const uint32_t idesc_s = idesc_bf16_f32(128, TILE, false, false);
+    const uint64_t qpe_desc = smem_desc(smem_u32(S.qpe), 16, 512, SWIZZLE_64B);
+    int q_seen = 0;
+    RowCursor rc;
     rc.init(prefix, seq_c, B, x0);
-    rc_pv = rc;
-
-    auto issue_pv = [&](int g) -> bool {  // PV of half page g
-      const int i = g >> 1, jj = g & 1, pb = g & 1, st = i % STAGES;
-      if (!wait_bar<false>(S, &S.p_full[pb], (g >> 1) & 1, a.err, 6)) return false;
-      bool seg_first = false;
-      if (jj == 0) {
-        const int xr = x0 + i;
-        rc_pv.advance(prefix, seq_c, xr);
-        seg_first = (xr == x0) || (xr == rc_pv.start);
-      }
-      // the first half page of a segment overwrites O: wait for the previous
-      // segment's epilogue to have read it
-      if (seg_first) {
-        if (pv_segments > 0 && !wait_bar<false>(S, &S.o_free, (pv_segments - 1) & 1, a.err, 7)) return false;
-        ++pv_segments;
-      }
+    for (int x = x0, i = 0; x < x1; ++x, ++i) {
+      rc.advance(prefix, seq_c, x);
+      if (x == x0 || x == rc.start) ++q_seen;  // every issuer counts every segment
+      if ((i & 1) != parity) continue;
+      const int st = i % STAGES, sb = i & 1;
+      // the query of this page's segment is in place (TMEM half + smem q_pe)
+      if (!wait_bar<false>(S, &S.q_ready, (q_seen - 1) & 1, a.err, 3)) break;
+      if (!wait_bar<false>(S, &S.kv_full[st], (i / STAGES) & 1, a.err, 4)) break;
+      if (!wait_bar<false>(S, &S.s_free[sb], ((i >> 1) & 1) ^ 1, a.err, 5)) break;
       fence_after_sync();
       const uint32_t kv_addr = smem_u32(S.kv[st]);
-#pragma unroll
-      for (int kk = 0; kk < HT / 16; ++kk)
-        mma_ts(tmem + TM_O, tmem + TM_P + 16 * pb + 8 * kk,
-               smem_desc(kv_addr + (HT * jj + 16 * kk) * 128, KV_CHUNK, 1024, SWIZZLE_128B), idesc_pv,
-               (seg_first && kk == 0) ? 0u : 1u);
-      mma_commit(&S.pv_done[pb]);
-      if (jj == 1) mma_commit(&S.kv_empty[st]);
-      return true;
-    };
-
-    for (int h = 0; h < nhalf; ++h) {
-      const int i = h >> 1, jj = h & 1, st = i % STAGES, sb = h & 1;
-      if (jj == 0) {
-        const int x = x0 + i;
-        rc.advance(prefix, seq_c, x);
-        if (x == x0 || x == rc.start) {  // the query of this segment must be in TMEM
-          if (!wait_bar<false>(S, &S.q_ready, q_seen & 1, a.err, 3)) { ok = false; break; }
-          ++q_seen;
-        }
-        if (!wait_bar<false>(S, &S.kv_full[st], (i / STAGES) & 1, a.err, 4)) { ok = false; break; }
-      }
-      if (!wait_bar<false>(S, &S.s_free[sb], ((h >> 1) & 1) ^ 1, a.err, 5)) { ok = false; break; }
-      fence_after_sync();
-      const uint32_t kv_addr = smem_u32(S.kv[st]);
-      const uint32_t d = tmem + TM_S + HT * sb;
+      const uint32_t d = tmem + TM_S + TILE * sb;
+      const uint64_t bdesc = smem_desc(kv_addr, 16, 1024, SWIZZLE_128B);
+      const uint64_t pdesc = smem_desc(kv_addr + KV_PE_OFF, 16, 512, SWIZZLE_64B);
 #pragma unroll
       for (int ci = 0; ci < 4; ++ci)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(d, tmem + TM_Q + ci * 32 + kk * 8,
-                 smem_desc(kv_addr + ci * KV_CHUNK + jj * (HT * 128) + kk * 32, 16, 1024, SWIZZLE_128B), idesc_s,
+          mma_ts(d, tmem + TM_Q + ci * 32 + kk * 8, bdesc + (uint64_t)((ci * KV_CHUNK + kk * 32) >> 4), idesc_s,
                  (ci | kk) != 0 ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
-        mma_ts(d, tmem + TM_QPE + kk * 8,
-               smem_desc(kv_addr + KV_PE_OFF + jj * (HT * 64) + kk * 32, 16, 512, SWIZZLE_64B), idesc_s, 1u);
+        mma_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4), pdesc + (uint64_t)((kk * 32) >> 4), idesc_s, 1u);
       mma_commit(&S.s_full[sb]);
-      if (h >= 2 && !issue_pv(h - 2)) { ok = false; break; }
     }
-    if (ok && nhalf >= 2) ok = issue_pv(nhalf - 2);
-    if (ok) (void)issue_pv(nhalf - 1);
-    mma_commit(&S.mma_done);
-    (void)mbar_wait(&S.mma_done, 0);  // every issued MMA has finished
-  } else if (ntiles > 0 && warp >= 2) {
-    // ------------------------------------------------------------ softmax
-    const int q4 = warp & 3;               // TMEM lane quadrant
-    const int ch = (warp - 2) >> 2;        // column half of each half page: 0 or 1
-    const int row = q4 * 32 + lane;        // head = TMEM lane
-    const int stid = threadIdx.x - 64;     // 0..255
-    const uint32_t t_row = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t pair_bar = 1 + q4;      // named barrier shared with the partner warp
-    const float c = a.scale_log2;          // > 0
-    uint32_t peer_xin[2], peer_xfull[2], peer_xempty[2];  // cluster addresses in the peer CTA
-    for (int k = 0; k < 2; ++k) {
-      peer_xin[k] = mapa(smem_u32(S.xin[k]), peer);
-      peer_xfull[k] = mapa(smem_u32(&S.x_full[k]), peer);
-      peer_xempty[k] = mapa(smem_u32(&S.x_empty[k]), peer);
-    }
-    float m_ref = -INFINITY, l = 0.f;
+    mma_commit(&S.mma_done[parity]);
+    (void)mbar_wait(&S.mma_done[parity], 0);  // every issued MMA has finished
+  } else if (ntiles > 0 && warp == 3 && lane == 0) {
+    // ------------------------------------------------------------ P.V issuer
+    const uint32_t idesc_pv = idesc_bf16_f32(128, HALF_C, false, true);
+    int segments = 0;
     RowCursor rc;
     rc.init(prefix, seq_c, B, x0);
-    uint32_t own_a[16], own_b[16];
-    HalfInfo info_a, info_b;
-
-    // A wait that fails does not leave the stage: it marks the thread failed and
-    // the stage runs on (every later wait returns at once), so that the pair
-    // barrier is still reached by both partner warps; the partners leave the
-    // loop together, at the reduction barrier of stage B.
-    bool failed = false;
-
-    // A(h): read this CTA's partial scores of half page h and send them to the peer
-    auto stage_a = [&](int h, uint32_t* own, HalfInfo& inf) {
-      const int i = h >> 1, jj = h & 1, sb = h & 1, st = i % STAGES;
-      const int x = x0 + i;
-      if (jj == 0) rc.advance(prefix, seq_c, x);
-      inf.b = rc.b;
-      inf.nvalid = min(TILE, rc.n - TILE * (x - rc.start));
-      inf.j = jj;
-      inf.seg_first = jj == 0 && (x == x0 || x == rc.start);
-      inf.seg_last = jj == 1 && (x + 1 == x1 || x + 1 == rc.end);
-      if (inf.seg_first) {
-        // this row's query half into TMEM; every S of the previous segment has
-        // completed (this thread waited for each of them)
-        const uint16_t* qrow = a.q_cat + ((size_t)rc.b * 128 + row) * DK;
-        const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 128 * ch);
-        uint32_t v[64];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint4 u = qc[k];
-          v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
-        }
-        uint32_t pe[16];
-        const uint4* qp = reinterpret_cast<const uint4*>(qrow + DC + PE_HALF * rank);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 u = qp[k];
-          pe[4 * k] = u.x; pe[4 * k + 1] = u.y; pe[4 * k + 2] = u.z; pe[4 * k + 3] = u.w;
-        }
-        tmem_st32(t_row + TM_Q + 64 * ch, v);
-        tmem_st32(t_row + TM_Q + 64 * ch + 32, v + 32);
-        if (ch == 0) tmem_st16(t_row + TM_QPE, pe);
-        tmem_st_wait();
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.q_ready);
+    for (int x = x0, i = 0; x < x1; ++x, ++i) {
+      rc.advance(prefix, seq_c, x);
+      const bool first = (x == x0) || (x == rc.start);
+      const int st = i % STAGES, pb = i & 1;
+      if (!wait_bar<false>(S, &S.p_full[pb], (i >> 1) & 1, a.err, 6)) break;
+      // the first page of a segment overwrites O: wait for the previous
+      // segment's epilogue to have read it
+      if (first) {
+        if (segments > 0 && !wait_bar<false>(S, &S.o_free, (segments - 1) & 1, a.err, 7)) break;
+        ++segments;
       }
-      if (stid == 0) mbar_arrive_expect_tx(&S.x_full[sb], XBYTES);  // the peer's partial for this half page
-      if (!wait_bar<false>(S, &S.s_full[sb], (h >> 1) & 1, a.err, 9)) failed = true;
-      __syncwarp();
       fence_after_sync();
-      tmem_ld16(t_row + TM_S + HT * sb + 16 * ch, own);
-      tmem_ld_wait();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.s_free[sb]);
-      if (jj == 0 && inf.nvalid < TILE) {
-        // page past the end of its sequence: zero the unused value rows so that
-        // P = 0 never meets stale (possibly non-finite) cache contents
-        const int units = (TILE - inf.nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
-        for (int idx = stid; idx < units; idx += NSOFT) {
-          const int r = inf.nvalid + idx / 32, ci = (idx % 32) / 8, v = idx % 8;
-          *reinterpret_cast<uint4*>(S.kv[st] + ci * KV_CHUNK + r * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-      }
-      // the peer has consumed what we sent into this buffer two half pages ago
-      if (lane == 0 && !wait_bar<true>(S, &S.x_empty[sb], ((h >> 1) & 1) ^ 1, a.err, 10)) failed = true;
-      __syncwarp();
+      fence_proxy_async_smem();  // P rows written by the peer's remote stores -> tensor core
+      const uint64_t adesc = smem_desc(smem_u32(S.p[pb]), 16, 1024, SWIZZLE_128B);
+      const uint64_t vdesc = smem_desc(smem_u32(S.kv[st]), KV_CHUNK, 1024, SWIZZLE_128B);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        st_async_v4(peer_xin[sb] + xchunk(row, 4 * ch + k), own[4 * k], own[4 * k + 1], own[4 * k + 2],
-                    own[4 * k + 3], peer_xfull[sb]);
-    };
+      for (int kk = 0; kk < TILE / 16; ++kk)
+        mma_ss(tmem + TM_O, adesc + (uint64_t)((kk * 32) >> 4), vdesc + (uint64_t)((kk * 16 * 128) >> 4),
+               idesc_pv, (first && kk == 0) ? 0u : 1u);
+      mma_commit(&S.pv_done[pb]);
+      mma_commit_mc(&S.pv_both[pb], (uint16_t)0x3);
+      mma_commit(&S.kv_empty[st]);
+    }
+    mma_commit(&S.mma_done[2]);
+    (void)mbar_wait(&S.mma_done[2], 0);
+  } else if (ntiles > 0 && warp >= SOFT_WARP0) {
+    // ------------------------------------------------------------ softmax warps
+    const int q4 = warp & 3;                  // TMEM lane quadrant
+    const int ch = (warp - SOFT_WARP0) >> 2;  // column half of each page: 0 or 1
+    const int row = q4 * 32 + lane;           // head = TMEM lane
+    const int hl = row & (OWN_H - 1);         // index among the 64 heads of the CTA that owns this head
+    const bool owner = (uint32_t)(q4 >> 1) == rank;
+    const int stid = threadIdx.x - 32 * SOFT_WARP0;  // 0..255
+    const uint32_t t_row = tmem + ((uint32_t)(q4 * 32) << 16);
+    const float c = a.scale_log2;  // > 0
+    RowCursor rc;
+    rc.init(prefix, seq_c, B, x0);
 
-    // B(h): add the peer's partial, online softmax, P into TMEM, epilogue at a
-    // segment end; returns false (on both partner warps alike) once either failed
-    auto stage_b = [&](int h, const uint32_t* own, const HalfInfo& inf) -> bool {
-      const int sb = h & 1;
-      if (!wait_bar<false>(S, &S.x_full[sb], (h >> 1) & 1, a.err, 11)) failed = true;
-      __syncwarp();
-      const uint8_t* xi = reinterpret_cast<const uint8_t*>(S.xin[sb]);
-      float s[16];
+    // the query of row b into place: the q_lat half into TMEM (each thread its
+    // 128 latent dims), the q_pe half into shared memory by one TMA copy
+    auto load_query = [&](int b) {
+      const uint16_t* qrow = a.q_cat + ((size_t)b * 128 + row) * DK;
+      const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 128 * ch);
+      uint32_t v[64];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 v = *reinterpret_cast<const float4*>(xi + xchunk(row, 4 * ch + k));
-        s[4 * k + 0] = u2f(own[4 * k + 0]) + v.x;
-        s[4 * k + 1] = u2f(own[4 * k + 1]) + v.y;
-        s[4 * k + 2] = u2f(own[4 * k + 2]) + v.z;
-        s[4 * k + 3] = u2f(own[4 * k + 3]) + v.w;
+      for (int k = 0; k < 16; ++k) {
+        const uint4 u = qc[k];
+        v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty[sb]);  // our buffer may be refilled
-      const int t0 = HT * inf.j + 16 * ch;  // token index of s[0] in the page
-      if (inf.nvalid < TILE) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (t0 + k >= inf.nvalid) s[k] = -INFINITY;
-      }
-      float mraw = s[0];
-#pragma unroll
-      for (int k = 1; k < 16; ++k) mraw = fmaxf(mraw, s[k]);
-      S.red_m[sb][ch][row] = mraw * c;
-      const bool pair_ok = named_barrier_and(pair_bar, 64, !failed);
-      const float mt = fmaxf(S.red_m[sb][0][row], S.red_m[sb][1][row]);
-      if (inf.seg_first) {
-        m_ref = mt;
-        l = 0.f;
-      }
-      const bool need = !inf.seg_first && mt > m_ref + RESCALE_LOG2;
-      if (__any_sync(0xffffffffu, need)) {
-        // O may only be touched once every PV issued so far has completed
-        if (!wait_bar<false>(S, &S.pv_done[(h - 1) & 1], ((h - 1) >> 1) & 1, a.err, 12)) failed = true;
-        __syncwarp();
-        fence_after_sync();
-        const float alpha = need ? ex2(m_ref - mt) : 1.f;
-#pragma unroll 1
-        for (int k32 = 0; k32 < 4; ++k32) {
-          uint32_t o[32];
-          const uint32_t col = t_row + TM_O + 128 * ch + 32 * k32;
-          tmem_ld32(col, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = f2u(u2f(o[k]) * alpha);
-          tmem_st32(col, o);
-        }
-        tmem_st_wait();
-        if (need) {
-          l *= alpha;
-          m_ref = mt;
-        }
-      }
-      // p = 2^(s*c - m_ref), two at a time in half precision (the exponent is
-      // <= RESCALE_LOG2, so p <= 256; P is rounded to bf16 for the MMA anyway)
-      uint32_t pk[8];
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const __half2 xh = __floats2half2_rn(fmaf(s[2 * k], c, -m_ref), fmaf(s[2 * k + 1], c, -m_ref));
-        const uint32_t yh = ex2_h2(*reinterpret_cast<const uint32_t*>(&xh));
-        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&yh));
-        sum += p.x + p.y;
-        pk[k] = pack_bf16x2(p.x, p.y);
-      }
-      l += sum;
-      // P buffer sb is free once PV(h-2) has completed
-      if (!wait_bar<false>(S, &S.pv_done[sb], ((h >> 1) & 1) ^ 1, a.err, 13)) failed = true;
-      __syncwarp();
-      fence_after_sync();
-      tmem_st8(t_row + TM_P + 16 * sb + 8 * ch, pk);
+      tmem_st32(t_row + TM_Q + 64 * ch, v);
+      tmem_st32(t_row + TM_Q + 64 * ch + 32, v + 32);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.p_full[sb]);
-      if (inf.seg_last) {
-        if (!wait_bar<false>(S, &S.pv_done[sb], (h >> 1) & 1, a.err, 14)) failed = true;
-        __syncwarp();
-        fence_after_sync();
-        S.red_l[ch][row] = l;
-        named_barrier(pair_bar, 64);
-        const float L = S.red_l[0][row] + S.red_l[1][row];
-        const float inv = 1.f / L;
-        const int seg = worker + inf.b;
-        float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ch;
-#pragma unroll 1
-        for (int k32 = 0; k32 < 4; ++k32) {
-          uint32_t o[32];
-          tmem_ld32(t_row + TM_O + 128 * ch + 32 * k32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            reinterpret_cast<float4*>(dst + 32 * k32)[k] =
-                make_float4(u2f(o[4 * k]) * inv, u2f(o[4 * k + 1]) * inv, u2f(o[4 * k + 2]) * inv,
-                            u2f(o[4 * k + 3]) * inv);
-        }
-        if (rank == 0 && ch == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.o_free);
+      if (lane == 0) mbar_arrive(&S.q_ready);
+      if (stid == 0) {
+        mbar_arrive_expect_tx(&S.q_ready, QPE_BYTES);
+        tma_load_3d(S.qpe, &tm_q_pe, DC + PE_HALF * rank, 0, b, &S.q_ready);
       }
-      return pair_ok;
+    };
+    // O row of this lane, this thread's 128 columns, times f
+    auto scale_o = [&](float f) {
+#pragma unroll 1
+      for (int k32 = 0; k32 < 4; ++k32) {
+        uint32_t o[32];
+        const uint32_t col = t_row + TM_O + 128 * ch + 32 * k32;
+        tmem_ld32(col, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = f2u(u2f(o[k]) * f);
+        tmem_st32(col, o);
+      }
+      tmem_st_wait();
+    };
+    // O row of this lane times inv -> the segment's partial output (this CTA's latent half)
+    auto store_o = [&](int seg, float inv) {
+      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ch;
+#pragma unroll 1
+      for (int k32 = 0; k32 < 4; ++k32) {
+        uint32_t o[32];
+        tmem_ld32(t_row + TM_O + 128 * ch + 32 * k32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          reinterpret_cast<float4*>(dst + 32 * k32)[k] = make_float4(
+              u2f(o[4 * k]) * inv, u2f(o[4 * k + 1]) * inv, u2f(o[4 * k + 2]) * inv, u2f(o[4 * k + 3]) * inv);
+      }
     };
 
-    // software pipeline: A(h) then B(h-1); even and odd halves swap the buffers
-    for (int h = 0; h <= nhalf; h += 2) {
-      if (h < nhalf) stage_a(h, own_a, info_a);
-      if (h >= 1 && !stage_b(h - 1, own_b, info_b)) break;
-      if (h + 1 > nhalf) break;
-      if (h + 1 < nhalf) stage_a(h + 1, own_b, info_b);
-      if (!stage_b(h, own_a, info_a)) break;
+    bool failed = false;
+    load_query(rc.b);
+    if (owner) {
+      // ---------------------------------------------------------- owners
+      const uint32_t pair_bar = 1 + q4;  // named barrier shared with the partner warp
+      const bool leader = (q4 == 2 * (int)rank) && ch == 0 && lane == 0;
+      const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0]), peer);
+      const uint32_t peer_p = mapa(smem_u32(S.p[0]), peer);
+      const uint32_t peer_msg = mapa(smem_u32(&S.msg[0][0]), peer);
+      const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0]), peer);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int x = x0, i = 0; x < x1; ++x, ++i) {
+        rc.advance(prefix, seq_c, x);
+        const bool first = (x == x0) || (x == rc.start);
+        const bool last = (x + 1 == x1) || (x + 1 == rc.end);
+        const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
+        const int sb = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+
+        if (leader) mbar_arrive_expect_tx(&S.x_full[sb], X_BYTES);  // the peer's partial for this page
+        // ---- this CTA's partial scores into registers; the S buffer is released
+        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) failed = true;
+        __syncwarp();
+        fence_after_sync();
+        uint32_t own[32];
+        tmem_ld32(t_row + TM_S + TILE * sb + 32 * ch, own);
+        tmem_ld_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_free[sb]);
+        // the next page starts a new segment: every S of this one has completed
+        // (this thread waited for each), so the next query may replace this one
+        if (last && x + 1 < x1) load_query(row_of_tile(prefix, B, x + 1));
+
+        // ---- add the peer's partial (fp16, log2 units) for these heads
+        if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
+        __syncwarp();
+        float s[32];
+        const uint8_t* xi = S.xin[sb];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xi + xoff(hl, 4 * ch + k));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+            s[8 * k + 2 * e] = fmaf(u2f(own[8 * k + 2 * e]), c, f.x);
+            s[8 * k + 2 * e + 1] = fmaf(u2f(own[8 * k + 2 * e + 1]), c, f.y);
+          }
+        }
+
+        // ---- online softmax in the log2 domain, lazily moved reference max
+        if (nvalid < TILE) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (32 * ch + k >= nvalid) s[k] = -INFINITY;
+        }
+        float mraw = s[0];
+#pragma unroll
+        for (int k = 1; k < 32; ++k) mraw = fmaxf(mraw, s[k]);
+        S.red_m[sb][ch][row] = mraw;
+        // every value read from the exchange buffer has been used by the store
+        // above, so the peer may refill it
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
+        if (!named_barrier_and(pair_bar, 64, !failed)) break;  // both partner warps leave together
+        const float mt = fmaxf(S.red_m[sb][0][row], S.red_m[sb][1][row]);
+        if (first) {
+          m_ref = mt;
+          l = 0.f;
+        }
+        const bool need = !first && mt > m_ref + RESCALE_LOG2;
+        float alpha = 1.f;
+        if (__any_sync(0xffffffffu, need)) {
+          // O may only be touched once every P.V issued so far has completed
+          if (!wait_bar<false>(S, &S.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 12)) failed = true;
+          __syncwarp();
+          fence_after_sync();
+          if (need) alpha = ex2(m_ref - mt);
+          scale_o(alpha);
+          if (need) {
+            l *= alpha;
+            m_ref = mt;
+          }
+        }
+        // p = 2^(s - m_ref), two at a time in half precision (the exponent is
+        // <= RESCALE_LOG2, so p <= 256; P is rounded to bf16 for the MMA anyway)
+        uint32_t pk[16];
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const __half2 xh = __floats2half2_rn(s[2 * k] - m_ref, s[2 * k + 1] - m_ref);
+          const uint32_t yh = ex2_h2(h2u(xh));
+          const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&yh));
+          sum += p.x + p.y;
+          pk[k] = pack_bf16x2(p.x, p.y);
+        }
+        l += sum;
+        float inv = 0.f, L = 0.f;
+        if (last) {
+          S.red_l[ch][row] = l;
+          named_barrier(pair_bar, 64);
+          L = S.red_l[0][row] + S.red_l[1][row];
+          inv = 1.f / L;
+        }
+        // P tile sb is free once the P.V of page i-2 has completed in both CTAs
+        if (!wait_bar<true>(S, &S.pv_both[sb], ph ^ 1u, a.err, 13)) failed = true;
+        __syncwarp();
+        uint8_t* pp = S.p[sb];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t off = sw128(row, 4 * ch + k);
+          *reinterpret_cast<uint4*>(pp + off) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          st_async_v4(peer_p + sb * P_BYTES + off, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
+                      peer_pin + 8u * sb);
+        }
+        if (ch == 0)
+          st_async_v2(peer_msg + sb * MSG_BYTES + 8u * hl, f2u(alpha), f2u(inv), peer_pin + 8u * sb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[sb]);
+
+        // ---- end of the row's segment: O / l and the natural-log LSE
+        if (last) {
+          if (!wait_bar<false>(S, &S.pv_done[sb], ph, a.err, 14)) failed = true;
+          __syncwarp();
+          fence_after_sync();
+          const int seg = worker + rc.b;
+          store_o(seg, inv);
+          if (ch == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.o_free);
+          named_barrier(pair_bar, 64);  // red_l may be rewritten only after both partners read it
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- senders
+      const bool leader = (q4 == 2 * (int)peer) && ch == 0 && lane == 0;
+      const int sid = (ch * 2 + (q4 & 1)) * 32 + lane;  // 0..127
+      const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer);
+      const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0]), peer);
+      // page i of this worker, one page behind the shipping of partials: the
+      // peer's P rows and messages have arrived -> rescale these heads' O rows,
+      // release the P.V, and at a segment end write these rows' output
+      auto finish = [&](int i, bool last, int seg) -> bool {
+        const int sb = i & 1;
+        bool ok = wait_bar<true>(S, &S.pin_full[sb], (uint32_t)(i >> 1) & 1u, a.err, 20);
+        __syncwarp();
+        const float2 mg = S.msg[sb][hl];
+        const bool need = mg.x != 1.f;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!wait_bar<false>(S, &S.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 21)) ok = false;
+          __syncwarp();
+          fence_after_sync();
+          scale_o(mg.x);
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[sb]);
+        if (last) {
+          if (!wait_bar<false>(S, &S.pv_done[sb], (uint32_t)(i >> 1) & 1u, a.err, 22)) ok = false;
+          __syncwarp();
+          fence_after_sync();
+          store_o(seg, mg.y);
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.o_free);
+        }
+        return ok;
+      };
+      int pend_i = -1, pend_seg = 0;
+      bool pend_last = false;
+      for (int x = x0, i = 0; x < x1; ++x, ++i) {
+        rc.advance(prefix, seq_c, x);
+        const bool last = (x + 1 == x1) || (x + 1 == rc.end);
+        const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
+        const int st = i % STAGES, sb = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+
+        if (leader) mbar_arrive_expect_tx(&S.pin_full[sb], PIN_BYTES);  // the peer's P rows for this page
+        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) failed = true;
+        __syncwarp();
+        fence_after_sync();
+        uint32_t v[32];
+        tmem_ld32(t_row + TM_S + TILE * sb + 32 * ch, v);
+        tmem_ld_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_free[sb]);
+        if (last && x + 1 < x1) load_query(row_of_tile(prefix, B, x + 1));
+        if (nvalid < TILE) {
+          // page past the end of its sequence: zero the unused value rows so that
+          // P = 0 never meets stale (possibly non-finite) cache contents
+          const int units = (TILE - nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
+          for (int idx = sid; idx < units; idx += 128) {
+            const int r = nvalid + idx / 32, ci = (idx % 32) / 8, u = idx % 8;
+            *reinterpret_cast<uint4*>(S.kv[st] + ci * KV_CHUNK + r * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          h[k] = h2u(__floats2half2_rn(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c)));
+        // the peer has consumed what we sent into this buffer two pages ago
+        if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_async_v4(peer_xin + sb * X_BYTES + xoff(hl, 4 * ch + k), h[4 * k], h[4 * k + 1], h[4 * k + 2],
+                      h[4 * k + 3], peer_xfull + 8u * sb);
+        if (pend_i >= 0 && !finish(pend_i, pend_last, pend_seg)) failed = true;
+        pend_i = i;
+        pend_last = last;
+        pend_seg = worker + rc.b;
+        if (__any_sync(0xffffffffu, failed)) break;
+      }
+      if (!failed && pend_i >= 0) (void)finish(pend_i, pend_last, pend_seg);
     }
   }
 
@@ -619,10 +712,11 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
                              int workers, float* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (H != 128 || fmt != MLA_FMT_BF16 || workers < 1) return cudaErrorNotSupported;
   if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling
-  CUtensorMap tkv_c, tkv_pe;
-  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per token slot
+  CUtensorMap tkv_c, tkv_pe, tq_pe;
+  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per token slot / query row
   if (!encode_3d(&tkv_c, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_3d(&tkv_pe, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B))
+      !encode_3d(&tkv_pe, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -639,7 +733,7 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   args.scale_log2 = scale * 1.4426950408889634f;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(workers, s, attr);
-  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tkv_c, tkv_pe, args);
+  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tkv_c, tkv_pe, tq_pe, args);
 }
 
 }  // namespace mla

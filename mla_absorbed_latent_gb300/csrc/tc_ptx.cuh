@@ -41,6 +41,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
       "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
       : "memory");
 }
+__device__ __forceinline__ void st_async_v2(uint32_t addr, uint32_t a, uint32_t b, uint32_t remote_bar) {
+  asm volatile("st.async.weak.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(remote_bar)
+               : "memory");
+}
+// plain 32-bit store into another CTA's shared memory (cluster address)
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 // bulk copy of `bytes` from this CTA's shared memory into another CTA's shared
 // memory (cluster address), completion counted on that CTA's mbarrier
 __device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
@@ -188,6 +197,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+// the same, on the mbarrier at `bar`'s offset in every CTA of the cluster named by `cta_mask`
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane
