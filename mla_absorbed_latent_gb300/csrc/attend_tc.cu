@@ -19,12 +19,12 @@
 //  * computes its partial S (M=128, N=64, K=288) into TMEM, with its half of
 //    q_lat in TMEM and its half of q_pe in shared memory as A operands;
 //  * sends the peer the partial scores of the peer's 64 heads, already in log2
-//    units, as fp16 (8 KB; asynchronous remote stores counted on the peer's
-//    transaction barrier);
+//    units, as fp16 (8 KB: written to a local staging tile, then one bulk
+//    shared-to-peer copy counted on the peer's transaction barrier);
 //  * adds the peer's partial to its own for its 64 heads, runs the online
-//    softmax there and writes P (bf16) for those heads into its own P tile and
-//    into the peer's (8 KB), with each head's O rescale factor and, at a
-//    segment end, 1/l;
+//    softmax there and writes P (bf16) for those heads into its own P tile,
+//    then copies those 64 rows (8 KB) into the peer's P tile, with each head's
+//    O rescale factor and, at a segment end, 1/l;
 //  * once both halves of P are in place, issues O_half += P . V_half.
 // Distributed shared memory moves ~14.5 bytes per cycle per SM each way, less
 // than the ~23 bytes per cycle per SM that HBM delivers, so the 16.5 KB per page
@@ -38,9 +38,10 @@
 // signalled to both CTAs (multicast commit): a P tile is rewritten only once
 // both CTAs' P.V have read it.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 S issuer (even pages)
-// and TMEM owner, warp 2 S issuer (odd pages), warp 3 P.V issuer, warps 4..11
-// softmax.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31; two warps
+// Warp roles (384 threads): warps 0..3 are the TMA producer, the P.V issuer
+// and the two S issuers (even / odd pages), assigned per rank so that the S
+// issuers share sub-partitions with the light sender warps; warp 1 owns TMEM;
+// warps 4..11 run the softmax.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31; two warps
 // share each quadrant and split a page's 64 tokens 32/32.  The four warps on
 // this CTA's own heads ("owners") run the softmax, combining row maxima and
 // sums with their partner through shared memory.  The four warps on the
@@ -52,6 +53,7 @@
 //
 // Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
 // buffer [384,512).
+#include <cstring>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -80,14 +82,17 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
+constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of the 128 owner / sender threads (1..4: pairs)
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 struct __align__(1024) SmemTC {
   uint8_t kv[STAGES][KV_BYTES];
   uint8_t p[2][P_BYTES];
   uint8_t xin[2][X_BYTES];  // the peer's fp16 partials for our heads; row = 128 B, chunks swizzled by row
+  uint8_t xout[2][X_BYTES]; // our fp16 partials for the peer's heads, same layout, shipped by one bulk copy
   uint8_t qpe[QPE_BYTES];
   float2 msg[2][OWN_H];     // from the peer, per peer head: (O rescale factor, 1/l at a segment end)
+  float2 msg_out[2][OWN_H]; // the same for our heads, shipped to the peer
   float red_m[2][2][128];   // partner row maxima [page parity][column half][row]
   float red_l[2][128];      // partner row sums at a segment end [column half][row]
   uint64_t kv_full[STAGES], kv_empty[STAGES];
@@ -168,7 +173,18 @@ struct RowCursor {
 
 __device__ __forceinline__ float u2f(uint32_t v) { return __uint_as_float(v); }
 __device__ __forceinline__ uint32_t f2u(float v) { return __float_as_uint(v); }
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+// two fp16 in one 32-bit word <-> two floats, in registers (low half = first value)
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+__device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return __half22float2(h);
+}
 __device__ __forceinline__ float fp16_clamp(float v) { return fminf(fmaxf(v, -FP16_MAX), FP16_MAX); }
 
 // byte offset of 16-byte chunk c (0..7, 8 tokens) of row r in a [64][64] fp16 exchange tile
@@ -221,7 +237,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   fence_after_sync();
   const uint32_t tmem = S.tmem_base;
 
-  if (ntiles > 0 && warp == 0) {
+  // Roles of warps 0..3 rotate with the rank so that the two S issuers run on
+  // the SM sub-partitions of the sender warps (warp w runs on sub-partition
+  // w % 4, the one that can reach TMEM lanes 32(w%4)..+31): role 0 producer,
+  // 1 P.V issuer, 2 / 3 S issuers of even / odd pages.
+  const int role = warp < 4 ? (warp ^ (int)(2 * rank)) : -1;
+  if (ntiles > 0 && role == 0) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp walks the pages; lane l holds the page id of tile
     // jbase + l of the current row (one gather per 32 tiles), lane 0 waits and
@@ -231,8 +252,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       prefetch_tmap(&tm_kv_pe);
     }
     const uint64_t pol = policy_evict_first();
-    int last_use[STAGES];
-    for (int s = 0; s < STAGES; ++s) last_use[s] = -1;
+    int issued = 0;  // pages whose copies were started (page k used stage k % STAGES)
     RowCursor rc;
     rc.init(prefix, seq_c, B, x0);
     int page_row = -1, jbase = 0, page_reg = 0;
@@ -259,19 +279,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_load_3d_hint(S.kv[st] + ci * KV_CHUNK, &tm_kv_c, HALF_C * rank + 64 * ci, 0, page, &S.kv_full[st],
                              pol);
           tma_load_3d_hint(S.kv[st] + KV_PE_OFF, &tm_kv_pe, DC + PE_HALF * rank, 0, page, &S.kv_full[st], pol);
-          last_use[st] = u;
+          ++issued;
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
     if (lane == 0 && S.abort_flag) {  // let copies in flight land before the CTA can exit
-      for (int s = 0; s < STAGES; ++s)
-        if (last_use[s] >= 0) (void)mbar_wait(&S.kv_full[s], last_use[s] & 1);
+      for (int k = max(0, issued - STAGES); k < issued; ++k)
+        (void)mbar_wait(&S.kv_full[k % STAGES], (k / STAGES) & 1);
     }
-  } else if (ntiles > 0 && (warp == 1 || warp == 2) && lane == 0) {
+  } else if (ntiles > 0 && (role == 2 || role == 3) && lane == 0) {
     // ------------------------------------------------------------ S issuers
     // warp 1: pages 0, 2, 4, ... of this worker; warp 2: pages 1, 3, 5, ...
-    const int parity = warp - 1;
+    const int parity = role - 2;
     const uint32_t idesc_s = idesc_bf16_f32(128, TILE, false, false);
     const uint64_t qpe_desc = smem_desc(smem_u32(S.qpe), 16, 512, SWIZZLE_64B);
     int q_seen = 0;
@@ -304,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     mma_commit(&S.mma_done[parity]);
     (void)mbar_wait(&S.mma_done[parity], 0);  // every issued MMA has finished
-  } else if (ntiles > 0 && warp == 3 && lane == 0) {
+  } else if (ntiles > 0 && role == 1 && lane == 0) {
     // ------------------------------------------------------------ P.V issuer
     const uint32_t idesc_pv = idesc_bf16_f32(128, HALF_C, false, true);
     int segments = 0;
@@ -441,13 +461,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint4 v = *reinterpret_cast<const uint4*>(xi + xoff(hl, 4 * ch + k));
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-            s[8 * k + 2 * e] = fmaf(u2f(own[8 * k + 2 * e]), c, f.x);
-            s[8 * k + 2 * e + 1] = fmaf(u2f(own[8 * k + 2 * e + 1]), c, f.y);
-          }
+          const float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y), f2 = h2_to_f2(v.z), f3 = h2_to_f2(v.w);
+          s[8 * k + 0] = fmaf(u2f(own[8 * k + 0]), c, f0.x);
+          s[8 * k + 1] = fmaf(u2f(own[8 * k + 1]), c, f0.y);
+          s[8 * k + 2] = fmaf(u2f(own[8 * k + 2]), c, f1.x);
+          s[8 * k + 3] = fmaf(u2f(own[8 * k + 3]), c, f1.y);
+          s[8 * k + 4] = fmaf(u2f(own[8 * k + 4]), c, f2.x);
+          s[8 * k + 5] = fmaf(u2f(own[8 * k + 5]), c, f2.y);
+          s[8 * k + 6] = fmaf(u2f(own[8 * k + 6]), c, f3.x);
+          s[8 * k + 7] = fmaf(u2f(own[8 * k + 7]), c, f3.y);
         }
 
         // ---- online softmax in the log2 domain, lazily moved reference max
@@ -464,7 +486,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // above, so the peer may refill it
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
-        if (!named_barrier_and(pair_bar, 64, !failed)) break;  // both partner warps leave together
+        named_barrier(pair_bar, 64);
         const float mt = fmaxf(S.red_m[sb][0][row], S.red_m[sb][1][row]);
         if (first) {
           m_ref = mt;
@@ -484,18 +506,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             m_ref = mt;
           }
         }
-        // p = 2^(s - m_ref), two at a time in half precision (the exponent is
-        // <= RESCALE_LOG2, so p <= 256; P is rounded to bf16 for the MMA anyway)
+        // p = 2^(s - m_ref) <= 2^RESCALE_LOG2, rounded to bf16 for the MMA (the
+        // single-precision ex2 moves as many values per clock as the paired
+        // half-precision one and needs no conversions around it)
         uint32_t pk[16];
-        float sum = 0.f;
+        float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const __half2 xh = __floats2half2_rn(s[2 * k] - m_ref, s[2 * k + 1] - m_ref);
-          const uint32_t yh = ex2_h2(h2u(xh));
-          const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&yh));
-          sum += p.x + p.y;
-          pk[k] = pack_bf16x2(p.x, p.y);
+          const float p0 = ex2(s[2 * k] - m_ref), p1 = ex2(s[2 * k + 1] - m_ref);
+          sum0 += p0;
+          sum1 += p1;
+          pk[k] = pack_bf16x2(p0, p1);
         }
+        const float sum = sum0 + sum1;
         l += sum;
         float inv = 0.f, L = 0.f;
         if (last) {
@@ -509,17 +532,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         uint8_t* pp = S.p[sb];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t off = sw128(row, 4 * ch + k);
-          *reinterpret_cast<uint4*>(pp + off) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          st_async_v4(peer_p + sb * P_BYTES + off, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3],
-                      peer_pin + 8u * sb);
-        }
-        if (ch == 0)
-          st_async_v2(peer_msg + sb * MSG_BYTES + 8u * hl, f2u(alpha), f2u(inv), peer_pin + 8u * sb);
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(pp + sw128(row, 4 * ch + k)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        if (ch == 0) S.msg_out[sb][hl] = make_float2(alpha, inv);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.p_full[sb]);
+        // our 64 rows of P (contiguous: rows 64r..64r+63) and their messages to the
+        // peer; every owner thread passes here each page, so this is also where
+        // they leave together after a failed wait
+        if (!named_barrier_and(OWNER_BAR, 128, !failed)) break;
+        if (leader) {
+          const uint32_t rows = (uint32_t)OWN_H * 128u * rank;
+          bulk_s2peer(peer_p + sb * P_BYTES + rows, pp + rows, OWN_H * 128, peer_pin + 8u * sb);
+          bulk_s2peer(peer_msg + sb * MSG_BYTES, &S.msg_out[sb][0], MSG_BYTES, peer_pin + 8u * sb);
+        }
 
         // ---- end of the row's segment: O / l and the natural-log LSE
         if (last) {
@@ -603,19 +631,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t h[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          h[k] = h2u(__floats2half2_rn(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c)));
+          h[k] = f2_to_h2(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c));
         // the peer has consumed what we sent into this buffer two pages ago
         if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
         __syncwarp();
+        // (the copy that read xout[sb] two pages ago has completed: its bytes were consumed)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          st_async_v4(peer_xin + sb * X_BYTES + xoff(hl, 4 * ch + k), h[4 * k], h[4 * k + 1], h[4 * k + 2],
-                      h[4 * k + 3], peer_xfull + 8u * sb);
+          *reinterpret_cast<uint4*>(S.xout[sb] + xoff(hl, 4 * ch + k)) =
+              make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+        fence_proxy_async_smem();
+        if (!named_barrier_and(SENDER_BAR, 128, !failed)) break;  // all senders leave together
+        if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, S.xout[sb], X_BYTES, peer_xfull + 8u * sb);
         if (pend_i >= 0 && !finish(pend_i, pend_last, pend_seg)) failed = true;
         pend_i = i;
         pend_last = last;
         pend_seg = worker + rc.b;
-        if (__any_sync(0xffffffffu, failed)) break;
       }
       if (!failed && pend_i >= 0) (void)finish(pend_i, pend_last, pend_seg);
     }
