@@ -146,7 +146,10 @@ size_t mla_decode_workspace_bytes(int B, int H);
  *               256-byte aligned; contents need no initialisation
  *   out       : bf16 [B][H][128], written
  * H in {16, 128}: H = 128 runs the tcgen05 tensor-core kernel, H = 16 the
- * CUDA-core kernel.  Equivalent to mla_decode_plan + mla_decode_absorb_q +
+ * CUDA-core kernel.  Formats: H = 128 reads bf16, INT8 and INT4 pools (codes
+ * are dequantized to bf16 in the kernel's load stage, x = code*s (+ z), fp32
+ * then one bf16 rounding); H = 16 reads bf16 pools only (MLA_ERR_UNSUPPORTED
+ * otherwise).  Equivalent to mla_decode_plan + mla_decode_absorb_q +
  * mla_decode_attend + mla_decode_combine on the same stream.
  */
 int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,

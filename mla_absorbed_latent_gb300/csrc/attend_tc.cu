@@ -65,7 +65,6 @@ using namespace tc;
 
 constexpr int TC_THREADS = 384;
 constexpr int SOFT_WARP0 = 4;
-constexpr int STAGES = 4;
 constexpr int TILE = 64;                                      // tokens per page / TMA stage / S tile
 constexpr int HALF_C = 256;
 constexpr int PE_HALF = 32;
@@ -85,17 +84,48 @@ constexpr float FP16_MAX = 65504.f;
 constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of the 128 owner / sender threads (1..4: pairs)
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
+// Per cache format: bf16 pages are TMA-copied straight into the MMA operand
+// stages (4 of them).  Quantized pages land in a small staging ring of codes
+// and scales; the sender warps dequantize each into a bf16 operand stage (3 of
+// them: shared memory holds no more next to the staging ring).  Offsets are
+// bytes inside one staging slot (this CTA's half of a page, unswizzled rows):
+//   INT8: c codes i8 [64][256] | k_pe codes i8 [64][32] | c scales bf16 [64][8]
+//         | k_pe scales bf16 [64][8] (all 8 groups of the token)
+//   INT4: c codes u8 [64][128] (2 per byte) | k_pe codes i8 [64][32] | c scales
+//         bf16 [64][8] | c zeros bf16 [64][8] | k_pe scales bf16 [64][8]
+template <int FMT> struct FmtTraits;
+template <> struct FmtTraits<MLA_FMT_BF16> {
+  static constexpr int KV_ST = 4, CODE_ST = 0;
+  static constexpr uint32_t CODE_BYTES = 0, C_OFF = 0, PE_OFF = 0, CS_OFF = 0, ZS_OFF = 0, PS_OFF = 0;
+};
+template <> struct FmtTraits<MLA_FMT_INT8> {
+  static constexpr int KV_ST = 3, CODE_ST = 2;
+  static constexpr uint32_t C_OFF = 0, PE_OFF = 16384, CS_OFF = 18432, ZS_OFF = 0, PS_OFF = 19456;
+  static constexpr uint32_t CODE_BYTES = 20480;
+};
+template <> struct FmtTraits<MLA_FMT_INT4> {
+  static constexpr int KV_ST = 3, CODE_ST = 3;
+  static constexpr uint32_t C_OFF = 0, PE_OFF = 8192, CS_OFF = 10240, ZS_OFF = 11264, PS_OFF = 12288;
+  static constexpr uint32_t CODE_BYTES = 13312;
+};
+
+template <int FMT>
 struct __align__(1024) SmemTC {
-  uint8_t kv[STAGES][KV_BYTES];
+  static constexpr int KV_ST = FmtTraits<FMT>::KV_ST;
+  static constexpr int CODE_ST = FmtTraits<FMT>::CODE_ST > 0 ? FmtTraits<FMT>::CODE_ST : 1;
+  static constexpr uint32_t CODE_BYTES = FmtTraits<FMT>::CODE_BYTES > 0 ? FmtTraits<FMT>::CODE_BYTES : 128;
+  uint8_t kv[KV_ST][KV_BYTES];
   uint8_t p[2][P_BYTES];
   uint8_t xin[2][X_BYTES];  // the peer's fp16 partials for our heads; row = 128 B, chunks swizzled by row
   uint8_t xout[2][X_BYTES]; // our fp16 partials for the peer's heads, same layout, shipped by one bulk copy
+  uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
   uint8_t qpe[QPE_BYTES];
   float2 msg[2][OWN_H];     // from the peer, per peer head: (O rescale factor, 1/l at a segment end)
   float2 msg_out[2][OWN_H]; // the same for our heads, shipped to the peer
   float red_m[2][2][128];   // partner row maxima [page parity][column half][row]
   float red_l[2][128];      // partner row sums at a segment end [column half][row]
-  uint64_t kv_full[STAGES], kv_empty[STAGES];
+  uint64_t kv_full[KV_ST], kv_empty[KV_ST];
+  uint64_t code_full[CODE_ST], code_empty[CODE_ST];
   uint64_t q_ready;         // q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2], pv_both[2];
@@ -104,7 +134,9 @@ struct __align__(1024) SmemTC {
   uint32_t tmem_base;
   volatile int abort_flag;
 };
-static_assert(sizeof(SmemTC) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
+static_assert(sizeof(SmemTC<MLA_FMT_BF16>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
+static_assert(sizeof(SmemTC<MLA_FMT_INT8>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
+static_assert(sizeof(SmemTC<MLA_FMT_INT4>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(KV_BYTES % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct TcArgs {
@@ -122,8 +154,8 @@ struct TcArgs {
 // MLA_ERR_TIMEOUT and raises the abort flag of this CTA and of its peer) or
 // once an abort was raised.  The abort flag and the clock are checked every 8
 // probes.
-template <bool kCluster>
-__device__ __forceinline__ bool wait_bar(SmemTC& S, uint64_t* bar, uint32_t parity, int* err, int where) {
+template <bool kCluster, class Smem>
+__device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity, int* err, int where) {
   auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
   const long long t0 = clock64();
@@ -192,11 +224,54 @@ __device__ __forceinline__ uint32_t xoff(int r, int c) { return (uint32_t)(r * 1
 // byte offset of 16-byte unit u (0..7, 8 tokens) of row r in a 128B-swizzled [128][64] bf16 tile
 __device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
 
+// ---- dequantization ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 block
+// quantizers): x = code * s (INT8), x = code * s + z (INT4), evaluated in fp32
+// and rounded once to bf16 for the MMA.  Integer codes reach fp32 exactly by
+// placing them in the low mantissa bits of 2^23 and subtracting the offset.
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// byte k (0..3) of a word of signed 8-bit codes, as an exact float
+__device__ __forceinline__ float i8_at(uint32_t w, int k) {
+  const uint32_t biased = w ^ 0x80808080u;  // code + 128 in 0..255
+  return __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u + (uint32_t)k)) - 8388736.f;  // 2^23 + 128
+}
+// 8 signed 8-bit codes times s -> 8 bf16 (one 16-byte unit)
+__device__ __forceinline__ uint4 deq_i8x8(uint2 w, float s) {
+  uint4 o;
+  o.x = pack_bf16x2(i8_at(w.x, 0) * s, i8_at(w.x, 1) * s);
+  o.y = pack_bf16x2(i8_at(w.x, 2) * s, i8_at(w.x, 3) * s);
+  o.z = pack_bf16x2(i8_at(w.y, 0) * s, i8_at(w.y, 1) * s);
+  o.w = pack_bf16x2(i8_at(w.y, 2) * s, i8_at(w.y, 3) * s);
+  return o;
+}
+// nibble j (0..7) of a word of 4-bit codes (element 2i in the low nibble of byte i), as an exact float
+__device__ __forceinline__ float u4_at(uint32_t w, int j) {
+  return __uint_as_float(0x4B000000u | ((w >> (4 * j)) & 0xFu)) - 8388608.f;  // 2^23
+}
+__device__ __forceinline__ uint4 deq_u4x8(uint32_t w, float s, float z) {
+  uint4 o;
+  o.x = pack_bf16x2(fmaf(u4_at(w, 0), s, z), fmaf(u4_at(w, 1), s, z));
+  o.y = pack_bf16x2(fmaf(u4_at(w, 2), s, z), fmaf(u4_at(w, 3), s, z));
+  o.z = pack_bf16x2(fmaf(u4_at(w, 4), s, z), fmaf(u4_at(w, 5), s, z));
+  o.w = pack_bf16x2(fmaf(u4_at(w, 6), s, z), fmaf(u4_at(w, 7), s, z));
+  return o;
+}
+
+// The cache tensor maps: bf16 pages use m0 (latent, 128B-swizzled boxes of 64
+// dims) and m1 (RoPE key, 64B-swizzled boxes of 32); quantized pages use m0
+// (c codes), m1 (k_pe codes), m2 (c scales), m3 (INT4: c zeros, INT8: k_pe
+// scales), m4 (INT4: k_pe scales).
+template <int FMT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_kv_c, const __grid_constant__ CUtensorMap tm_kv_pe,
-                     const __grid_constant__ CUtensorMap tm_q_pe, const TcArgs a) {
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tm_m0, const __grid_constant__ CUtensorMap tm_m1,
+                     const __grid_constant__ CUtensorMap tm_m2, const __grid_constant__ CUtensorMap tm_m3,
+                     const __grid_constant__ CUtensorMap tm_m4, const __grid_constant__ CUtensorMap tm_q_pe,
+                     const TcArgs a) {
+  using Smem = SmemTC<FMT>;
+  using FT = FmtTraits<FMT>;
+  constexpr bool kQuant = FMT != MLA_FMT_BF16;
+  constexpr int KV_ST = Smem::KV_ST, CODE_ST = Smem::CODE_ST;
   extern __shared__ uint8_t smem_raw[];
-  SmemTC& S = *reinterpret_cast<SmemTC*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int worker = blockIdx.x >> 1;
@@ -207,9 +282,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int ntiles = x1 - x0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&S.kv_full[s], 1);
+    for (int s = 0; s < KV_ST; ++s) {
+      mbar_init(&S.kv_full[s], kQuant ? 4 : 1);  // quantized: the four sender warps after dequantizing
       mbar_init(&S.kv_empty[s], 1);
+    }
+    for (int s = 0; s < CODE_ST; ++s) {
+      mbar_init(&S.code_full[s], 1);
+      mbar_init(&S.code_empty[s], 4);
     }
     mbar_init(&S.q_ready, 9);
     for (int s = 0; s < 2; ++s) {
@@ -248,11 +327,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // jbase + l of the current row (one gather per 32 tiles), lane 0 waits and
     // issues the copies.
     if (lane == 0) {
-      prefetch_tmap(&tm_kv_c);
-      prefetch_tmap(&tm_kv_pe);
+      prefetch_tmap(&tm_m0);
+      prefetch_tmap(&tm_m1);
+      if (kQuant) {
+        prefetch_tmap(&tm_m2);
+        prefetch_tmap(&tm_m3);
+        if (FMT == MLA_FMT_INT4) prefetch_tmap(&tm_m4);
+      }
     }
     const uint64_t pol = policy_evict_first();
-    int issued = 0;  // pages whose copies were started (page k used stage k % STAGES)
+    constexpr int RING = kQuant ? CODE_ST : KV_ST;  // slots the copies land in
+    int issued = 0;  // pages whose copies were started (page k used slot k % RING)
     RowCursor rc;
     rc.init(prefix, seq_c, B, x0);
     int page_row = -1, jbase = 0, page_reg = 0;
@@ -267,26 +352,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int page = __shfl_sync(0xffffffffu, page_reg, j - jbase);
       int ok = 1;
       if (lane == 0) {
-        const int st = i % STAGES, u = i / STAGES;
-        ok = wait_bar<false>(S, &S.kv_empty[st], (u & 1) ^ 1, a.err, 2);
+        const int st = i % RING, u = i / RING;
+        ok = wait_bar<false>(S, kQuant ? &S.code_empty[st] : &S.kv_empty[st], (u & 1) ^ 1, a.err, 2);
         if (ok) {
           if (page < 0 || page >= a.num_pages) {
             raise_error(a.err, MLA_ERR_BOUNDS, page);
             page = 0;
           }
-          mbar_arrive_expect_tx(&S.kv_full[st], KV_BYTES);
-          for (int ci = 0; ci < 4; ++ci)
-            tma_load_3d_hint(S.kv[st] + ci * KV_CHUNK, &tm_kv_c, HALF_C * rank + 64 * ci, 0, page, &S.kv_full[st],
+          if constexpr (!kQuant) {
+            mbar_arrive_expect_tx(&S.kv_full[st], KV_BYTES);
+            for (int ci = 0; ci < 4; ++ci)
+              tma_load_3d_hint(S.kv[st] + ci * KV_CHUNK, &tm_m0, HALF_C * rank + 64 * ci, 0, page, &S.kv_full[st],
+                               pol);
+            tma_load_3d_hint(S.kv[st] + KV_PE_OFF, &tm_m1, DC + PE_HALF * rank, 0, page, &S.kv_full[st], pol);
+          } else {
+            uint64_t* bar = &S.code_full[st];
+            uint8_t* dst = S.code[st];
+            mbar_arrive_expect_tx(bar, FT::CODE_BYTES);
+            // c codes of this CTA's 256 latent dims (INT4: 128 bytes of them)
+            tma_load_3d_hint(dst + FT::C_OFF, &tm_m0, (FMT == MLA_FMT_INT8 ? 256 : 128) * (int)rank, 0, page, bar,
                              pol);
-          tma_load_3d_hint(S.kv[st] + KV_PE_OFF, &tm_kv_pe, DC + PE_HALF * rank, 0, page, &S.kv_full[st], pol);
+            tma_load_3d_hint(dst + FT::PE_OFF, &tm_m1, PE_HALF * rank, 0, page, bar, pol);  // k_pe codes
+            tma_load_3d_hint(dst + FT::CS_OFF, &tm_m2, 8 * rank, 0, page, bar, pol);        // c scales
+            if constexpr (FMT == MLA_FMT_INT4) {
+              tma_load_3d_hint(dst + FT::ZS_OFF, &tm_m3, 8 * rank, 0, page, bar, pol);  // c zeros
+              tma_load_3d_hint(dst + FT::PS_OFF, &tm_m4, 0, 0, page, bar, pol);         // k_pe scales
+            } else {
+              tma_load_3d_hint(dst + FT::PS_OFF, &tm_m3, 0, 0, page, bar, pol);  // k_pe scales
+            }
+          }
           ++issued;
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     }
     if (lane == 0 && S.abort_flag) {  // let copies in flight land before the CTA can exit
-      for (int k = max(0, issued - STAGES); k < issued; ++k)
-        (void)mbar_wait(&S.kv_full[k % STAGES], (k / STAGES) & 1);
+      for (int k = max(0, issued - RING); k < issued; ++k)
+        (void)mbar_wait(kQuant ? &S.code_full[k % RING] : &S.kv_full[k % RING], (k / RING) & 1);
     }
   } else if (ntiles > 0 && (role == 2 || role == 3) && lane == 0) {
     // ------------------------------------------------------------ S issuers
@@ -301,10 +403,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       rc.advance(prefix, seq_c, x);
       if (x == x0 || x == rc.start) ++q_seen;  // every issuer counts every segment
       if ((i & 1) != parity) continue;
-      const int st = i % STAGES, sb = i & 1;
+      const int st = i % KV_ST, sb = i & 1;
       // the query of this page's segment is in place (TMEM half + smem q_pe)
       if (!wait_bar<false>(S, &S.q_ready, (q_seen - 1) & 1, a.err, 3)) break;
-      if (!wait_bar<false>(S, &S.kv_full[st], (i / STAGES) & 1, a.err, 4)) break;
+      if (!wait_bar<false>(S, &S.kv_full[st], (i / KV_ST) & 1, a.err, 4)) break;
       if (!wait_bar<false>(S, &S.s_free[sb], ((i >> 1) & 1) ^ 1, a.err, 5)) break;
       fence_after_sync();
       const uint32_t kv_addr = smem_u32(S.kv[st]);
@@ -333,7 +435,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const bool first = (x == x0) || (x == rc.start);
-      const int st = i % STAGES, pb = i & 1;
+      const int st = i % KV_ST, pb = i & 1;
       if (!wait_bar<false>(S, &S.p_full[pb], (i >> 1) & 1, a.err, 6)) break;
       // the first page of a segment overwrites O: wait for the previous
       // segment's epilogue to have read it
@@ -569,6 +671,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int sid = (ch * 2 + (q4 & 1)) * 32 + lane;  // 0..127
       const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer);
       const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0]), peer);
+      // quantized formats: page j's staged codes -> bf16 operand stage j % KV_ST
+      // (rows at or past nvalid are written as zeros), then release both
+      auto dequant = [&](int j, int nvalid) -> bool {
+        const int st = j % KV_ST, cs = j % CODE_ST;
+        bool ok = wait_bar<false>(S, &S.code_full[cs], (uint32_t)(j / CODE_ST) & 1u, a.err, 23);
+        // the P.V that last read this operand stage has completed
+        if (!wait_bar<false>(S, &S.kv_empty[st], ((uint32_t)(j / KV_ST) & 1u) ^ 1u, a.err, 24)) ok = false;
+        __syncwarp();
+        const uint8_t* cd = S.code[cs];
+        uint8_t* kv = S.kv[st];
+        // latent: 4 chunks x 64 tokens x 8 units of 8 dims, 128B-swizzled rows
+        for (int idx = sid; idx < 4 * TILE * 8; idx += 128) {
+          const int t = idx >> 5, ci = (idx >> 3) & 3, u = idx & 7;
+          const int d0 = 64 * ci + 8 * u;  // local latent dim of the unit's first element
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (t < nvalid) {
+            const float sc = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::CS_OFF)[t * 8 + (d0 >> 5)]);
+            if constexpr (FMT == MLA_FMT_INT8) {
+              o = deq_i8x8(*reinterpret_cast<const uint2*>(cd + FT::C_OFF + t * 256 + d0), sc);
+            } else {
+              const float z = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::ZS_OFF)[t * 8 + (d0 >> 5)]);
+              o = deq_u4x8(*reinterpret_cast<const uint32_t*>(cd + FT::C_OFF + t * 128 + (d0 >> 1)), sc, z);
+            }
+          }
+          *reinterpret_cast<uint4*>(kv + ci * KV_CHUNK + t * 128 + ((u ^ (t & 7)) << 4)) = o;
+        }
+        // RoPE key: 64 tokens x 4 units of 8 dims, 64B-swizzled rows; unit u is
+        // the 8-dim group 4r + u of the token
+        for (int idx = sid; idx < TILE * 4; idx += 128) {
+          const int t = idx >> 2, u = idx & 3;
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (t < nvalid) {
+            const float sc = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::PS_OFF)[t * 8 + 4 * (int)rank + u]);
+            o = deq_i8x8(*reinterpret_cast<const uint2*>(cd + FT::PE_OFF + t * 32 + 8 * u), sc);
+          }
+          *reinterpret_cast<uint4*>(kv + KV_PE_OFF + t * 64 + ((u ^ ((t >> 1) & 3)) << 4)) = o;
+        }
+        fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.kv_full[st]);
+          mbar_arrive(&S.code_empty[cs]);
+        }
+        return ok;
+      };
+      RowCursor rn;  // row of the next page, for its dequantization
+      if constexpr (kQuant) {
+        rn.init(prefix, seq_c, B, x0);
+        if (!dequant(0, min(TILE, rn.n - TILE * (x0 - rn.start)))) failed = true;
+      }
       // page i of this worker, one page behind the shipping of partials: the
       // peer's P rows and messages have arrived -> rescale these heads' O rows,
       // release the P.V, and at a segment end write these rows' output
@@ -604,7 +756,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         rc.advance(prefix, seq_c, x);
         const bool last = (x + 1 == x1) || (x + 1 == rc.end);
         const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
-        const int st = i % STAGES, sb = i & 1;
+        const int st = i % KV_ST, sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
         if (leader) mbar_arrive_expect_tx(&S.pin_full[sb], PIN_BYTES);  // the peer's P rows for this page
@@ -618,9 +770,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
         if (last && x + 1 < x1) load_query(row_of_tile(prefix, B, x + 1));
-        if (nvalid < TILE) {
+        if (!kQuant && nvalid < TILE) {
           // page past the end of its sequence: zero the unused value rows so that
           // P = 0 never meets stale (possibly non-finite) cache contents
+          // (quantized pages: the dequantization writes those rows as zeros)
           const int units = (TILE - nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
           for (int idx = sid; idx < units; idx += 128) {
             const int r = nvalid + idx / 32, ci = (idx % 32) / 8, u = idx % 8;
@@ -643,6 +796,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         if (!named_barrier_and(SENDER_BAR, 128, !failed)) break;  // all senders leave together
         if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, S.xout[sb], X_BYTES, peer_xfull + 8u * sb);
+        if constexpr (kQuant) {
+          // the next page's operands, ahead of its S (its stage was last read by page i+1-KV_ST's P.V)
+          if (x + 1 < x1) {
+            rn.advance(prefix, seq_c, x + 1);
+            if (!dequant(i + 1, min(TILE, rn.n - TILE * (x + 1 - rn.start)))) failed = true;
+          }
+        }
         if (pend_i >= 0 && !finish(pend_i, pend_last, pend_seg)) failed = true;
         pend_i = i;
         pend_last = last;
@@ -683,21 +843,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 tensor map: dims (d0 fastest), byte strides of dims 1 and 2, box (b0, b1, 1)
+// 3-D tensor map: dims (d0 fastest), byte strides of dims 1 and 2, box (b0, b1, 1)
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-               uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+               uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {s1, s2};
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = sizeof(SmemTC) + 1024;
+template <int FMT>
+constexpr size_t smem_bytes() { return sizeof(SmemTC<FMT>) + 1024; }
 
 std::mutex g_tc_mu;
 int g_tc_workers[64] = {};
@@ -706,7 +868,7 @@ cudaLaunchConfig_t launch_config(int workers, cudaStream_t s, cudaLaunchAttribut
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * workers);
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes<MLA_FMT_BF16>();
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -726,11 +888,11 @@ int attend_tc_workers(int num_sms) {
   std::lock_guard<std::mutex> lk(g_tc_mu);
   if (g_tc_workers[dev] == 0) {
     int clusters = 0;
-    if (cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(attend_tc_kernel<MLA_FMT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<MLA_FMT_BF16>()) == cudaSuccess) {
       cudaLaunchAttribute attr[1];
       cudaLaunchConfig_t cfg = launch_config(num_sms / 2, nullptr, attr);
-      if (cudaOccupancyMaxActiveClusters(&clusters, attend_tc_kernel, &cfg) != cudaSuccess) clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, attend_tc_kernel<MLA_FMT_BF16>, &cfg) != cudaSuccess) clusters = 0;
     }
     (void)cudaGetLastError();
     g_tc_workers[dev] = clusters > 0 ? std::min(clusters, num_sms / 2) : num_sms / 2;
@@ -741,16 +903,36 @@ int attend_tc_workers(int num_sms) {
 cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, float* part_o, float* part_lse, int* err, cudaStream_t s) {
-  if (H != 128 || fmt != MLA_FMT_BF16 || workers < 1) return cudaErrorNotSupported;
+  if (H != 128 || workers < 1) return cudaErrorNotSupported;
+  if (fmt != MLA_FMT_BF16 && fmt != MLA_FMT_INT8 && fmt != MLA_FMT_INT4) return cudaErrorNotSupported;
   if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling
-  CUtensorMap tkv_c, tkv_pe, tq_pe;
-  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per token slot / query row
-  if (!encode_3d(&tkv_c, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_3d(&tkv_pe, pages, DK, PAGE, num_pages, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
+  CUtensorMap m[5], tq_pe;
+  const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per bf16 token slot / query row
+  const uint8_t* pg = static_cast<const uint8_t*>(pages);
+  const uint64_t P = (uint64_t)num_pages;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+  bool ok = encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (fmt == MLA_FMT_BF16) {
+    ok = ok && encode_3d(&m[0], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_3d(&m[1], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B);
+    m[2] = m[3] = m[4] = m[0];
+  } else if (fmt == MLA_FMT_INT8) {
+    const uint64_t PB = PAGE_BYTES_INT8;  // sections at 0, 32768, 36864, 38912
+    ok = ok && encode_3d(&m[0], pg, DC, PAGE, P, DC, PB, 256, TILE, NS, U8) &&
+         encode_3d(&m[1], pg + 32768, DR, PAGE, P, DR, PB, 32, TILE, NS, U8) &&
+         encode_3d(&m[2], pg + 36864, DC / 32, PAGE, P, (DC / 32) * 2, PB, 8, TILE, NS, BF) &&
+         encode_3d(&m[3], pg + 38912, DR / 8, PAGE, P, (DR / 8) * 2, PB, 8, TILE, NS, BF);
+    m[4] = m[0];
+  } else {
+    const uint64_t PB = PAGE_BYTES_INT4;  // sections at 0, 16384, 20480, 22528, 24576
+    ok = ok && encode_3d(&m[0], pg, DC / 2, PAGE, P, DC / 2, PB, 128, TILE, NS, U8) &&
+         encode_3d(&m[1], pg + 16384, DR, PAGE, P, DR, PB, 32, TILE, NS, U8) &&
+         encode_3d(&m[2], pg + 20480, DC / 32, PAGE, P, (DC / 32) * 2, PB, 8, TILE, NS, BF) &&
+         encode_3d(&m[3], pg + 22528, DC / 32, PAGE, P, (DC / 32) * 2, PB, 8, TILE, NS, BF) &&
+         encode_3d(&m[4], pg + 24576, DR / 8, PAGE, P, (DR / 8) * 2, PB, 8, TILE, NS, BF);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   TcArgs args;
   args.q_cat = static_cast<const uint16_t*>(q_cat);
   args.plan = plan;
@@ -764,7 +946,15 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   args.scale_log2 = scale * 1.4426950408889634f;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(workers, s, attr);
-  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tkv_c, tkv_pe, tq_pe, args);
+  auto go = [&](auto kernel, size_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, kernel, m[0], m[1], m[2], m[3], m[4], tq_pe, args);
+  };
+  if (fmt == MLA_FMT_BF16) return go(attend_tc_kernel<MLA_FMT_BF16>, smem_bytes<MLA_FMT_BF16>());
+  if (fmt == MLA_FMT_INT8) return go(attend_tc_kernel<MLA_FMT_INT8>, smem_bytes<MLA_FMT_INT8>());
+  return go(attend_tc_kernel<MLA_FMT_INT4>, smem_bytes<MLA_FMT_INT4>());
 }
 
 }  // namespace mla

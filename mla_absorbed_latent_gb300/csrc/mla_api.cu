@@ -63,8 +63,8 @@ size_t page_bytes(int fmt) {
 // attend kernel for H heads over a `fmt` cache: 1 = tcgen05, 0 = CUDA cores, -1 = none
 int attend_kind(int H, int fmt) {
   if (!heads_ok(H) || !fmt_ok(fmt)) return -1;
-  if (fmt != MLA_FMT_BF16) return -1;
-  return H == 128 ? 1 : 0;
+  if (H == 128) return 1;  // every format: quantized pages are dequantized in the load stage
+  return fmt == MLA_FMT_BF16 ? 0 : -1;
 }
 
 int max_workers(int sms) { return attend_cc_workers(sms) > attend_tc_workers(sms) ? attend_cc_workers(sms)

@@ -236,6 +236,49 @@ def test_decode_v3_ragged_full():
     _check_rows(dev, rows)
 
 
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_decode_quant_ragged_edges(fmt):
+    """H=128 over INT8 / INT4 pages (dequantized in the load stage): lengths
+    around the page edges, an empty row, outlier channels; against the oracle
+    over the dequantized values."""
+    seqlens = [1, 31, 33, 63, 64, 65, 0, 200, 1000, 129]
+    prob = make_problem(128, seqlens, seed=31, fmt=fmt, dist="outlier")
+    dev = DeviceDecode(prob)
+    o_lat = torch.empty((len(seqlens), 128, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    rows = [b for b, n in enumerate(seqlens) if n > 0]
+    _check_rows(dev, rows)  # the bf16 outputs, at the stated tolerance
+    # o_lat: the dequantized values are rounded once to bf16 for the MMA
+    # (half an ulp, 2^-9 relative), which the outlier channels (|x| up to ~40)
+    # turn into absolute errors above the output tolerance; bound each channel
+    # by 2^-8 of its largest magnitude on top of the usual tolerance
+    ref = oracle_rows(prob, rows)
+    got = o_lat.cpu().numpy().astype(np.float64)
+    for b in rows:
+        c, p = prob.sequence(b)
+        C, _ = O.dequantized_tokens(fmt, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))
+        bound = 2e-2 + 1e-2 * np.abs(ref[b][1]) + 2.0 ** -8 * np.max(np.abs(C), axis=0)[None, :]
+        err = np.abs(got[b] - ref[b][1])
+        assert np.all(err <= bound), f"o_lat[{b}]: worst excess {np.max(err - bound):.3e}"
+    empty = seqlens.index(0)
+    assert torch.count_nonzero(dev.out[empty]) == 0
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_decode_v3_quant_full(fmt):
+    """H=128, B=64, seqlen 32768, random page table, quantized pool: first and
+    last rows against the oracle, the whole batch finite."""
+    prob = problem_from_workload(synth.get_workload("v3_quant"), fmt=fmt)
+    dev = DeviceDecode(prob)
+    dev.decode()
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, [0, prob.B - 1])
+    assert np.all(np.isfinite(_out_f64(dev.out)))
+
+
 def test_decode_bad_page_id_reports_bounds():
     import mla_absorbed_latent_gb300 as mla
     prob = make_problem(16, [100], seed=4)
