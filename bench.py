@@ -68,7 +68,7 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_traffic(kind: str):
+def kernel_traffic(kind: str, fmt: str = "bf16"):
     """DRAM bytes per launch of the attend kernel from the committed ncu summary,
     or None when missing or taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", "attend_traffic.json")
@@ -78,7 +78,7 @@ def kernel_traffic(kind: str):
         src = os.path.join(ROOT, "mla_absorbed_latent_gb300", "csrc", d["source"])
         with open(src, "rb") as f:
             h = hashlib.sha256(f.read()).hexdigest()
-        if h != d["source_sha256"] or d.get("kind") != kind:
+        if h != d["source_sha256"] or d.get("kind") != kind or d.get("fmt", "bf16") != fmt:
             return None
         return int(d["dram_bytes_per_launch"])
     except Exception:
@@ -303,11 +303,19 @@ def run_ours(args, wl, fmt):
     value = total_bytes / (ms_step * 1e-3) / 1e9
     attend_gbs = cache_bytes / (attend_ms * 1e-3) / 1e9
     flops_tok = 2 * H * (576 + 512)
-    traffic = kernel_traffic("tcgen05" if kind == 1 else "cuda-core")
+    traffic = kernel_traffic("tcgen05" if kind == 1 else "cuda-core", fmt)
     if kind == 1:
-        roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s", "frac": attend_gbs / hbm,
-                "traffic": traffic, "peak_source": peak_src,
-                "tensor_tflops": cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12}
+        tflops = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12
+        ai = flops_tok / BYTES_PER_TOKEN[fmt]            # FLOP per cache byte
+        ridge = tf_burst * 1e12 / (hbm * 1e9)
+        if ai < ridge:  # bf16 pages (AI ~242): the cache stream binds
+            roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s", "frac": attend_gbs / hbm,
+                    "traffic": traffic, "peak_source": peak_src, "tensor_tflops": tflops,
+                    "tensor_frac": tflops / tf_burst, "arith_intensity": ai}
+        else:  # quantized pages: the bf16 MMAs on the dequantized tiles bind
+            roof = {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s",
+                    "frac": tflops / tf_burst, "traffic": traffic, "peak_source": peak_src + " (bf16, burst)",
+                    "hbm_gbs": attend_gbs, "hbm_frac": attend_gbs / hbm, "arith_intensity": ai}
     else:
         # CUDA-core kernel: fp32 FMA bound; peak = SMs x 128 FMA/clk x 2 FLOP x max SM clock
         props = torch.cuda.get_device_properties(torch.cuda.current_device())
