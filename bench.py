@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -358,12 +359,18 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR))
     ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = synth.get_workload(args.workload)
+    if args.seqlen is not None:
+        if wl.ragged or args.seqlen < 1:
+            raise SystemExit("--seqlen needs a uniform-length workload and a positive length")
+        wl = dataclasses.replace(wl, seqlen=args.seqlen)
     fmt = args.fmt or wl.fmts[0]
     if args.impl == "reference":
         return run_reference(args, wl, fmt)
