@@ -159,6 +159,24 @@ def oracle_time(prob, budget_s: float, max_rows: int | None = None):
     return done_bytes, spent, rows
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of a list of floats over the ranks of the default process
+    group (the values unchanged without one): each rank's timings, so the job is
+    timed by its slowest rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_throughput(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank decodes its own replica batch (weak scaling), so
+    the job moves world x the per-rank cache bytes in the slowest rank's time."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -258,9 +276,7 @@ def run_ours(args, wl, fmt):
     elapsed_ms = t0.elapsed_time(t1)
     attend_ms = float(np.mean([a.elapsed_time(b) for a, b in attend_ev]))
     if world > 1:
-        t = torch.tensor([elapsed_ms, attend_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, attend_ms = float(t[0]), float(t[1])
+        elapsed_ms, attend_ms = max_over_ranks([elapsed_ms, attend_ms], dist, device="cuda")
         dist.barrier()
     st, info = mla.mla_get_device_status()
     if st != mla.MLA_OK:
@@ -301,7 +317,7 @@ def run_ours(args, wl, fmt):
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
     ms_step = elapsed_ms / args.steps
     total_bytes = cache_bytes * world
-    value = total_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput(cache_bytes, world, ms_step)
     attend_gbs = cache_bytes / (attend_ms * 1e-3) / 1e9
     flops_tok = 2 * H * (576 + 512)
     traffic = kernel_traffic("tcgen05" if kind == 1 else "cuda-core", fmt)
