@@ -38,18 +38,20 @@
 // signalled to both CTAs (multicast commit): a P tile is rewritten only once
 // both CTAs' P.V have read it.
 //
-// Warp roles (384 threads): warps 0..3 are the TMA producer, the P.V issuer
+// Warp roles (640 threads): warps 0..3 are the TMA producer, the P.V issuer
 // and the two S issuers (even / odd pages), assigned per rank so that the S
 // issuers share sub-partitions with the light sender warps; warp 1 owns TMEM;
-// warps 4..11 run the softmax.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31; two warps
-// share each quadrant and split a page's 64 tokens 32/32.  The four warps on
-// this CTA's own heads ("owners") run the softmax, combining row maxima and
-// sums with their partner through shared memory.  The four warps on the
-// peer's heads ("senders") ship those heads' partial scores, and one page
-// later apply the peer's rescale factors to the O rows of those heads and
-// release the P.V.  Every wait is bounded; a timeout records MLA_ERR_TIMEOUT,
-// raises the abort flag of both CTAs, lets in-flight copies and MMAs land,
-// frees TMEM and returns.
+// warps 4..19 run the softmax.  TMEM lane quadrant q = warp % 4 holds heads
+// 32q..32q+31; NSUB = 4 warps share each quadrant and split a page's 64 tokens
+// into slices of 16 (more warps per sub-partition hide the latency of the
+// per-page chain).  The eight warps on this CTA's own heads ("owners") run the
+// softmax, combining row maxima and sums across the slices through shared
+// memory.  The eight warps on the peer's heads ("senders") ship those heads'
+// partial scores, and one page later apply the peer's rescale factors to the O
+// rows of those heads and release the P.V; for quantized pools they also
+// dequantize the next page.  Every wait is bounded; a timeout records
+// MLA_ERR_TIMEOUT, raises the abort flag of both CTAs, lets in-flight copies
+// and MMAs land, frees TMEM and returns.
 //
 // Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
 // buffer [384,512).
@@ -63,12 +65,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int TC_THREADS = 384;
+constexpr int NSUB = 4;                                       // softmax warps per TMEM lane quadrant
+constexpr int TC_THREADS = 128 + 128 * NSUB;                  // 4 role warps + 4 quadrants x NSUB
 constexpr int SOFT_WARP0 = 4;
 constexpr int TILE = 64;                                      // tokens per page / TMA stage / S tile
 constexpr int HALF_C = 256;
 constexpr int PE_HALF = 32;
 constexpr int OWN_H = 64;                                     // heads whose softmax one CTA runs
+constexpr int TPW = 64 / NSUB;                                // tokens of a page per softmax thread
+constexpr int OCOLS = 256 / NSUB;                             // O columns (of 256) per softmax thread
+constexpr int QCOLS = 128 / NSUB;                             // q_lat TMEM columns (bf16 pairs) per thread
 constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                  // 8,192: [64 tokens][64 dims] 128B-swizzled
 constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                  // 32,768: [64 tokens][32 dims] 64B-swizzled
 constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2;  // 36,864
@@ -81,7 +87,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
-constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of the 128 owner / sender threads (1..4: pairs)
+constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of all owner / sender threads (1..4: quadrants)
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 // Per cache format: bf16 pages are TMA-copied straight into the MMA operand
@@ -122,8 +128,8 @@ struct __align__(1024) SmemTC {
   uint8_t qpe[QPE_BYTES];
   float2 msg[2][OWN_H];     // from the peer, per peer head: (O rescale factor, 1/l at a segment end)
   float2 msg_out[2][OWN_H]; // the same for our heads, shipped to the peer
-  float red_m[2][2][128];   // partner row maxima [page parity][column half][row]
-  float red_l[2][128];      // partner row sums at a segment end [column half][row]
+  float red_m[2][NSUB][OWN_H];  // row maxima of the NSUB token slices [page parity][slice][own head]
+  float red_l[NSUB][OWN_H];     // row sums of the slices at a segment end [slice][own head]
   uint64_t kv_full[KV_ST], kv_empty[KV_ST];
   uint64_t code_full[CODE_ST], code_empty[CODE_ST];
   uint64_t q_ready;         // q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
@@ -204,6 +210,12 @@ struct RowCursor {
 };
 
 __device__ __forceinline__ float u2f(uint32_t v) { return __uint_as_float(v); }
+// N (16 or 32) consecutive TMEM columns of this thread's lane
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
+}
 __device__ __forceinline__ uint32_t f2u(float v) { return __float_as_uint(v); }
 // two fp16 in one 32-bit word <-> two floats, in registers (low half = first value)
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
@@ -283,25 +295,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_ST; ++s) {
-      mbar_init(&S.kv_full[s], kQuant ? 4 : 1);  // quantized: the four sender warps after dequantizing
+      mbar_init(&S.kv_full[s], kQuant ? 2 * NSUB : 1);  // quantized: the sender warps after dequantizing
       mbar_init(&S.kv_empty[s], 1);
     }
     for (int s = 0; s < CODE_ST; ++s) {
       mbar_init(&S.code_full[s], 1);
-      mbar_init(&S.code_empty[s], 4);
+      mbar_init(&S.code_empty[s], 2 * NSUB);
     }
-    mbar_init(&S.q_ready, 9);
+    mbar_init(&S.q_ready, 4 * NSUB + 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
-      mbar_init(&S.s_free[s], 8);
-      mbar_init(&S.p_full[s], 8);
+      mbar_init(&S.s_free[s], 4 * NSUB);
+      mbar_init(&S.p_full[s], 4 * NSUB);
       mbar_init(&S.pv_done[s], 1);
       mbar_init(&S.pv_both[s], 2);   // this CTA's and the peer's P.V commits
       mbar_init(&S.x_full[s], 1);    // local expect_tx arrival + the peer's fp16 partial bytes
-      mbar_init(&S.x_empty[s], 4);   // one remote arrival per peer owner warp
+      mbar_init(&S.x_empty[s], 2 * NSUB);  // one remote arrival per peer owner warp
       mbar_init(&S.pin_full[s], 1);  // local expect_tx arrival + the peer's P rows and messages
     }
-    mbar_init(&S.o_free, 8);
+    mbar_init(&S.o_free, 4 * NSUB);
     for (int k = 0; k < 3; ++k) mbar_init(&S.mma_done[k], 1);
     S.abort_flag = 0;
     fence_barrier_init();
@@ -460,7 +472,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (ntiles > 0 && warp >= SOFT_WARP0) {
     // ------------------------------------------------------------ softmax warps
     const int q4 = warp & 3;                  // TMEM lane quadrant
-    const int ch = (warp - SOFT_WARP0) >> 2;  // column half of each page: 0 or 1
+    const int sub = (warp - SOFT_WARP0) >> 2;  // token slice of each page: [TPW*sub, TPW*sub + TPW)
     const int row = q4 * 32 + lane;           // head = TMEM lane
     const int hl = row & (OWN_H - 1);         // index among the 64 heads of the CTA that owns this head
     const bool owner = (uint32_t)(q4 >> 1) == rank;
@@ -471,18 +483,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     rc.init(prefix, seq_c, B, x0);
 
     // the query of row b into place: the q_lat half into TMEM (each thread its
-    // 128 latent dims), the q_pe half into shared memory by one TMA copy
+    // 2*QCOLS latent dims), the q_pe half into shared memory by one TMA copy
     auto load_query = [&](int b) {
       const uint16_t* qrow = a.q_cat + ((size_t)b * 128 + row) * DK;
-      const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 128 * ch);
-      uint32_t v[64];
+      const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 2 * QCOLS * sub);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint4 u = qc[k];
-        v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
+      for (int k32 = 0; k32 < QCOLS / 32; ++k32) {
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = qc[8 * k32 + k];
+          v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
+        }
+        tmem_st32(t_row + TM_Q + QCOLS * sub + 32 * k32, v);
       }
-      tmem_st32(t_row + TM_Q + 64 * ch, v);
-      tmem_st32(t_row + TM_Q + 64 * ch + 32, v + 32);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
@@ -492,12 +506,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_load_3d(S.qpe, &tm_q_pe, DC + PE_HALF * rank, 0, b, &S.q_ready);
       }
     };
-    // O row of this lane, this thread's 128 columns, times f
+    // O row of this lane, this thread's OCOLS columns, times f
     auto scale_o = [&](float f) {
 #pragma unroll 1
-      for (int k32 = 0; k32 < 4; ++k32) {
+      for (int k32 = 0; k32 < OCOLS / 32; ++k32) {
         uint32_t o[32];
-        const uint32_t col = t_row + TM_O + 128 * ch + 32 * k32;
+        const uint32_t col = t_row + TM_O + OCOLS * sub + 32 * k32;
         tmem_ld32(col, o);
         tmem_ld_wait();
 #pragma unroll
@@ -508,11 +522,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
     // O row of this lane times inv -> the segment's partial output (this CTA's latent half)
     auto store_o = [&](int seg, float inv) {
-      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ch;
+      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + OCOLS * sub;
 #pragma unroll 1
-      for (int k32 = 0; k32 < 4; ++k32) {
+      for (int k32 = 0; k32 < OCOLS / 32; ++k32) {
         uint32_t o[32];
-        tmem_ld32(t_row + TM_O + 128 * ch + 32 * k32, o);
+        tmem_ld32(t_row + TM_O + OCOLS * sub + 32 * k32, o);
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -525,8 +539,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     load_query(rc.b);
     if (owner) {
       // ---------------------------------------------------------- owners
-      const uint32_t pair_bar = 1 + q4;  // named barrier shared with the partner warp
-      const bool leader = (q4 == 2 * (int)rank) && ch == 0 && lane == 0;
+      const uint32_t quad_bar = 1 + q4;  // named barrier of the NSUB warps of this quadrant
+      const bool leader = (q4 == 2 * (int)rank) && sub == 0 && lane == 0;
       const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0]), peer);
       const uint32_t peer_p = mapa(smem_u32(S.p[0]), peer);
       const uint32_t peer_msg = mapa(smem_u32(&S.msg[0][0]), peer);
@@ -545,8 +559,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) failed = true;
         __syncwarp();
         fence_after_sync();
-        uint32_t own[32];
-        tmem_ld32(t_row + TM_S + TILE * sb + 32 * ch, own);
+        uint32_t own[TPW];
+        tmem_ld_cols<TPW>(t_row + TM_S + TILE * sb + TPW * sub, own);
         tmem_ld_wait();
         fence_before_sync();
         __syncwarp();
@@ -558,11 +572,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- add the peer's partial (fp16, log2 units) for these heads
         if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
         __syncwarp();
-        float s[32];
+        float s[TPW];
         const uint8_t* xi = S.xin[sb];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xi + xoff(hl, 4 * ch + k));
+        for (int k = 0; k < TPW / 8; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xi + xoff(hl, (TPW / 8) * sub + k));
           const float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y), f2 = h2_to_f2(v.z), f3 = h2_to_f2(v.w);
           s[8 * k + 0] = fmaf(u2f(own[8 * k + 0]), c, f0.x);
           s[8 * k + 1] = fmaf(u2f(own[8 * k + 1]), c, f0.y);
@@ -577,19 +591,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- online softmax in the log2 domain, lazily moved reference max
         if (nvalid < TILE) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (32 * ch + k >= nvalid) s[k] = -INFINITY;
+          for (int k = 0; k < TPW; ++k)
+            if (TPW * sub + k >= nvalid) s[k] = -INFINITY;
         }
         float mraw = s[0];
 #pragma unroll
-        for (int k = 1; k < 32; ++k) mraw = fmaxf(mraw, s[k]);
-        S.red_m[sb][ch][row] = mraw;
+        for (int k = 1; k < TPW; ++k) mraw = fmaxf(mraw, s[k]);
+        S.red_m[sb][sub][hl] = mraw;
         // every value read from the exchange buffer has been used by the store
         // above, so the peer may refill it
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
-        named_barrier(pair_bar, 64);
-        const float mt = fmaxf(S.red_m[sb][0][row], S.red_m[sb][1][row]);
+        named_barrier(quad_bar, 32 * NSUB);
+        float mt = S.red_m[sb][0][hl];
+#pragma unroll
+        for (int k = 1; k < NSUB; ++k) mt = fmaxf(mt, S.red_m[sb][k][hl]);
         if (first) {
           m_ref = mt;
           l = 0.f;
@@ -611,10 +627,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // p = 2^(s - m_ref) <= 2^RESCALE_LOG2, rounded to bf16 for the MMA (the
         // single-precision ex2 moves as many values per clock as the paired
         // half-precision one and needs no conversions around it)
-        uint32_t pk[16];
+        uint32_t pk[TPW / 2];
         float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < TPW / 2; ++k) {
           const float p0 = ex2(s[2 * k] - m_ref), p1 = ex2(s[2 * k + 1] - m_ref);
           sum0 += p0;
           sum1 += p1;
@@ -624,9 +640,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         l += sum;
         float inv = 0.f, L = 0.f;
         if (last) {
-          S.red_l[ch][row] = l;
-          named_barrier(pair_bar, 64);
-          L = S.red_l[0][row] + S.red_l[1][row];
+          S.red_l[sub][hl] = l;
+          named_barrier(quad_bar, 32 * NSUB);
+#pragma unroll
+          for (int k = 0; k < NSUB; ++k) L += S.red_l[k][hl];
           inv = 1.f / L;
         }
         // P tile sb is free once the P.V of page i-2 has completed in both CTAs
@@ -634,17 +651,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         uint8_t* pp = S.p[sb];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<uint4*>(pp + sw128(row, 4 * ch + k)) =
+        for (int k = 0; k < TPW / 8; ++k)
+          *reinterpret_cast<uint4*>(pp + sw128(row, (TPW / 8) * sub + k)) =
               make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        if (ch == 0) S.msg_out[sb][hl] = make_float2(alpha, inv);
+        if (sub == 0) S.msg_out[sb][hl] = make_float2(alpha, inv);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.p_full[sb]);
         // our 64 rows of P (contiguous: rows 64r..64r+63) and their messages to the
         // peer; every owner thread passes here each page, so this is also where
         // they leave together after a failed wait
-        if (!named_barrier_and(OWNER_BAR, 128, !failed)) break;
+        if (!named_barrier_and(OWNER_BAR, 64 * NSUB, !failed)) break;
         if (leader) {
           const uint32_t rows = (uint32_t)OWN_H * 128u * rank;
           bulk_s2peer(peer_p + sb * P_BYTES + rows, pp + rows, OWN_H * 128, peer_pin + 8u * sb);
@@ -658,17 +675,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_after_sync();
           const int seg = worker + rc.b;
           store_o(seg, inv);
-          if (ch == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
+          if (sub == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
           fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.o_free);
-          named_barrier(pair_bar, 64);  // red_l may be rewritten only after both partners read it
+          named_barrier(quad_bar, 32 * NSUB);  // red_l may be rewritten only after every slice read it
         }
       }
     } else {
       // ---------------------------------------------------------- senders
-      const bool leader = (q4 == 2 * (int)peer) && ch == 0 && lane == 0;
-      const int sid = (ch * 2 + (q4 & 1)) * 32 + lane;  // 0..127
+      const bool leader = (q4 == 2 * (int)peer) && sub == 0 && lane == 0;
+      constexpr int NSEND = 64 * NSUB;                   // sender threads
+      const int sid = (sub * 2 + (q4 & 1)) * 32 + lane;  // 0..NSEND-1
       const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer);
       const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0]), peer);
       // quantized formats: page j's staged codes -> bf16 operand stage j % KV_ST
@@ -682,7 +700,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint8_t* cd = S.code[cs];
         uint8_t* kv = S.kv[st];
         // latent: 4 chunks x 64 tokens x 8 units of 8 dims, 128B-swizzled rows
-        for (int idx = sid; idx < 4 * TILE * 8; idx += 128) {
+        for (int idx = sid; idx < 4 * TILE * 8; idx += NSEND) {
           const int t = idx >> 5, ci = (idx >> 3) & 3, u = idx & 7;
           const int d0 = 64 * ci + 8 * u;  // local latent dim of the unit's first element
           uint4 o = make_uint4(0u, 0u, 0u, 0u);
@@ -699,7 +717,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         // RoPE key: 64 tokens x 4 units of 8 dims, 64B-swizzled rows; unit u is
         // the 8-dim group 4r + u of the token
-        for (int idx = sid; idx < TILE * 4; idx += 128) {
+        for (int idx = sid; idx < TILE * 4; idx += NSEND) {
           const int t = idx >> 2, u = idx & 3;
           uint4 o = make_uint4(0u, 0u, 0u, 0u);
           if (t < nvalid) {
@@ -763,8 +781,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) failed = true;
         __syncwarp();
         fence_after_sync();
-        uint32_t v[32];
-        tmem_ld32(t_row + TM_S + TILE * sb + 32 * ch, v);
+        uint32_t v[TPW];
+        tmem_ld_cols<TPW>(t_row + TM_S + TILE * sb + TPW * sub, v);
         tmem_ld_wait();
         fence_before_sync();
         __syncwarp();
@@ -775,26 +793,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // P = 0 never meets stale (possibly non-finite) cache contents
           // (quantized pages: the dequantization writes those rows as zeros)
           const int units = (TILE - nvalid) * 4 * 8;  // 16-byte units in 4 chunks of 128-byte rows
-          for (int idx = sid; idx < units; idx += 128) {
+          for (int idx = sid; idx < units; idx += NSEND) {
             const int r = nvalid + idx / 32, ci = (idx % 32) / 8, u = idx % 8;
             *reinterpret_cast<uint4*>(S.kv[st] + ci * KV_CHUNK + r * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
         }
-        uint32_t h[16];
+        uint32_t h[TPW / 2];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
+        for (int k = 0; k < TPW / 2; ++k)
           h[k] = f2_to_h2(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c));
         // the peer has consumed what we sent into this buffer two pages ago
         if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
         __syncwarp();
         // (the copy that read xout[sb] two pages ago has completed: its bytes were consumed)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<uint4*>(S.xout[sb] + xoff(hl, 4 * ch + k)) =
+        for (int k = 0; k < TPW / 8; ++k)
+          *reinterpret_cast<uint4*>(S.xout[sb] + xoff(hl, (TPW / 8) * sub + k)) =
               make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         fence_proxy_async_smem();
-        if (!named_barrier_and(SENDER_BAR, 128, !failed)) break;  // all senders leave together
+        if (!named_barrier_and(SENDER_BAR, NSEND, !failed)) break;  // all senders leave together
         if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, S.xout[sb], X_BYTES, peer_xfull + 8u * sb);
         if constexpr (kQuant) {
           // the next page's operands, ahead of its S (its stage was last read by page i+1-KV_ST's P.V)
