@@ -239,16 +239,23 @@ def run_ours(args, wl, fmt):
     kind = mla.mla_decode_kernel_kind(H) if fmt == "bf16" else 1
 
     def step(ev=None):
+        # ev: 5 events bracketing plan | absorb_q | attend | combine
         p = prob
-        mla.mla_decode_plan(H, fmt, dev.seqlens, B, p.max_pages, dev.workspace, dev.ws_bytes, stream)
-        mla.mla_decode_absorb_q(dev.q_nope, dev.q_pe, dev.W_UK, H, B, dev.workspace, dev.ws_bytes, stream)
         if ev is not None:
             ev[0].record(stream)
+        mla.mla_decode_plan(H, fmt, dev.seqlens, B, p.max_pages, dev.workspace, dev.ws_bytes, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mla.mla_decode_absorb_q(dev.q_nope, dev.q_pe, dev.W_UK, H, B, dev.workspace, dev.ws_bytes, stream)
+        if ev is not None:
+            ev[2].record(stream)
         mla.mla_decode_attend(H, dev.cache, dev.page_table, p.max_pages, dev.seqlens, B, p.scale, dev.workspace,
                               dev.ws_bytes, stream)
         if ev is not None:
-            ev[1].record(stream)
+            ev[3].record(stream)
         mla.mla_decode_combine(dev.W_UV, H, B, dev.workspace, dev.ws_bytes, dev.out, None, stream)
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -257,8 +264,7 @@ def run_ours(args, wl, fmt):
     if st != mla.MLA_OK:
         raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
 
-    attend_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)]
+    attend_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if world > 1:
@@ -274,7 +280,9 @@ def run_ours(args, wl, fmt):
     torch.cuda.synchronize()
     clock_info = clocks.stop() if clocks else None
     elapsed_ms = t0.elapsed_time(t1)
-    attend_ms = float(np.mean([a.elapsed_time(b) for a, b in attend_ev]))
+    attend_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in attend_ev]))
+    stage_ms = {name: float(np.mean([e[k].elapsed_time(e[k + 1]) for e in attend_ev]))
+                for k, name in enumerate(("plan", "absorb_q", "attend", "combine"))}
     if world > 1:
         elapsed_ms, attend_ms = max_over_ranks([elapsed_ms, attend_ms], dist, device="cuda")
         dist.barrier()
@@ -355,6 +363,7 @@ def run_ours(args, wl, fmt):
         "queries_per_s": B * world / (ms_step * 1e-3),
         "roofline": roof,
         "attend_ms": attend_ms,
+        "stage_ms": stage_ms,  # mean per-stage times of one step, from events recorded between its launches
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -179,21 +179,11 @@ __device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity
   }
 }
 
-// largest row b with prefix[b] <= x (rows with no tiles are skipped)
-__device__ __forceinline__ int row_of_tile(const int* prefix, int B, int x) {
-  int lo = 0, hi = B;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= x) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 // row of the tile cursor: tiles [start, end) belong to row b of length n
 struct RowCursor {
   int b, start, end, n;
-  __device__ __forceinline__ void init(const int* prefix, const int* seq_c, int B, int x) {
-    b = row_of_tile(prefix, B, x);
+  __device__ __forceinline__ void init(const int* prefix, const int* seq_c, int row) {
+    b = row;
     start = prefix[b];
     end = prefix[b + 1];
     n = seq_c[b];
@@ -290,6 +280,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int T = a.plan[0], W = a.plan[1], B = a.B;
   const int* prefix = a.plan + PLAN_HDR;
   const int* seq_c = a.plan + PLAN_HDR + B + 1;
+  const int row0 = a.plan[PLAN_HDR + 2 * B + 1 + worker];  // first row of this worker's range
   const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
   const int ntiles = x1 - x0;
 
@@ -351,12 +342,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr int RING = kQuant ? CODE_ST : KV_ST;  // slots the copies land in
     int issued = 0;  // pages whose copies were started (page k used slot k % RING)
     RowCursor rc;
-    rc.init(prefix, seq_c, B, x0);
+    rc.init(prefix, seq_c, row0);
     int page_row = -1, jbase = 0, page_reg = 0;
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const int j = x - rc.start;
       if (rc.b != page_row || j - jbase >= 32) {
+        if (rc.b != page_row && rc.end < x1) {
+          // entering a row whose segment is not this worker's last: warm L2
+          // with the next row's query and page-table entries, which the
+          // softmax warps and this warp need at the next segment change
+          RowCursor nx = rc;
+          nx.advance(prefix, seq_c, rc.end);
+          if (lane == 0 && rank == 0) prefetch_l2_bulk(a.q_cat + (size_t)nx.b * 128 * DK, 128 * DK * 2);
+          const int32_t* pt = a.page_table + (size_t)nx.b * a.max_pages;
+          const int nt = nx.end - nx.start;
+          for (int k = 32 * lane; k < nt; k += 32 * 32) prefetch_l2_line(pt + k);
+        }
         page_row = rc.b;
         jbase = j;
         page_reg = (j + lane < rc.end - rc.start) ? a.page_table[(size_t)rc.b * a.max_pages + j + lane] : 0;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint64_t qpe_desc = smem_desc(smem_u32(S.qpe), 16, 512, SWIZZLE_64B);
     int q_seen = 0;
     RowCursor rc;
-    rc.init(prefix, seq_c, B, x0);
+    rc.init(prefix, seq_c, row0);
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       if (x == x0 || x == rc.start) ++q_seen;  // every issuer counts every segment
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, HALF_C, false, true);
     int segments = 0;
     RowCursor rc;
-    rc.init(prefix, seq_c, B, x0);
+    rc.init(prefix, seq_c, row0);
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const bool first = (x == x0) || (x == rc.start);
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t t_row = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = a.scale_log2;  // > 0
     RowCursor rc;
-    rc.init(prefix, seq_c, B, x0);
+    rc.init(prefix, seq_c, row0);
 
     // the query of row b into place: the q_lat half into TMEM (each thread its
     // 2*QCOLS latent dims), the q_pe half into shared memory by one TMA copy
@@ -567,7 +569,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
         // the next page starts a new segment: every S of this one has completed
         // (this thread waited for each), so the next query may replace this one
-        if (last && x + 1 < x1) load_query(row_of_tile(prefix, B, x + 1));
+        if (last && x + 1 < x1) {
+          RowCursor nx = rc;
+          nx.advance(prefix, seq_c, x + 1);
+          load_query(nx.b);
+        }
 
         // ---- add the peer's partial (fp16, log2 units) for these heads
         if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
@@ -736,7 +742,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       };
       RowCursor rn;  // row of the next page, for its dequantization
       if constexpr (kQuant) {
-        rn.init(prefix, seq_c, B, x0);
+        rn.init(prefix, seq_c, row0);
         if (!dequant(0, min(TILE, rn.n - TILE * (x0 - rn.start)))) failed = true;
       }
       // page i of this worker, one page behind the shipping of partials: the
@@ -787,7 +793,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
-        if (last && x + 1 < x1) load_query(row_of_tile(prefix, B, x + 1));
+        if (last && x + 1 < x1) {
+          RowCursor nx = rc;
+          nx.advance(prefix, seq_c, x + 1);
+          load_query(nx.b);
+        }
         if (!kQuant && nvalid < TILE) {
           // page past the end of its sequence: zero the unused value rows so that
           // P = 0 never meets stale (possibly non-finite) cache contents

@@ -66,6 +66,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     plan[2] = B;
     plan[3] = 0;
   }
+  __syncthreads();  // the prefix is complete (block-wide visibility of the global writes)
+  // first row of each worker's range: the largest b with prefix[b] <= its first
+  // tile (so a worker starts its cursor with one load instead of a search)
+  int* wrow = plan + PLAN_HDR + 2 * B + 1;
+  const long long T = prefix[B];
+  for (int w = tid; w < workers; w += blockDim.x) {
+    const long long x = worker_begin(w, T, workers);
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= x) lo = mid; else hi = mid;
+    }
+    wrow[w] = lo;
+  }
 }
 
 }  // namespace

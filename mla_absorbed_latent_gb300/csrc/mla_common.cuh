@@ -45,7 +45,8 @@ struct WsLayout {
 
 // plan block (int32): [0] total tiles, [1] workers, [2] B, [3] reserved,
 //                     [4 .. 4+B]  tile prefix (B+1 entries),
-//                     [5+B .. 5+2B) clamped sequence lengths
+//                     [5+B .. 5+2B) clamped sequence lengths,
+//                     [5+2B .. 5+2B+W) first row of each worker's tile range
 constexpr int PLAN_HDR = 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -56,7 +57,7 @@ inline WsLayout ws_layout(int B, int H, int max_workers) {
   L.q_cat = off;
   off = align_up(off + (size_t)B * H * DK * 2, 1024);
   L.plan = off;
-  off = align_up(off + (size_t)(PLAN_HDR + 2 * B + 1) * 4, 1024);
+  off = align_up(off + (size_t)(PLAN_HDR + 2 * B + 1 + max_workers) * 4, 1024);
   L.max_segments = max_workers + B;
   L.part_o = off;
   off = align_up(off + (size_t)L.max_segments * H * DC * 4, 1024);
