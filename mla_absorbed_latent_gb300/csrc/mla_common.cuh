@@ -3,6 +3,7 @@
 // mbarriers and bulk async copies (sm_90+ forms, used on sm_103a).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -181,5 +182,11 @@ int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = un
 
 cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
                            const float* part_lse, void* out, float* o_lat, cudaStream_t s);
+
+// 3-D TMA tensor map (tensor_map.cu): dims (d0 fastest), byte strides of dims 1
+// and 2, box (b0, b1, 1); false when the driver refuses the description
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+               uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 }  // namespace mla
