@@ -188,5 +188,9 @@ cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, cons
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
                uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw,
                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+// the same with a box extent in all three dims
+bool encode_3d_box(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                   uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw,
+                   CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 }  // namespace mla

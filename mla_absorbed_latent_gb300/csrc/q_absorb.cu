@@ -5,130 +5,118 @@
 // "手搓 MLA" §四 writes it as einsum("thd,hdc->thc", q_nope, W_UK).
 //
 // Per head this is a small GEMM, M = B rows, N = 512, K = 128, run on the
-// warp-level bf16 tensor-core MMA with fp32 accumulation; the result is
-// rounded once to bf16 because it is the bf16 A operand of the score MMA.
-// The output row is the 576-wide query of the latent attention: q_lat
-// followed by a copy of q_pe.
+// fifth-generation tensor core: one CTA per head; q_nope rows (A) and W_UK[h]
+// (B) arrive as K-major 128B-swizzled TMA tiles; 16 tcgen05.mma (M=128 rows,
+// N=256, K=16) accumulate the 128 x 512 fp32 result in tensor memory; the
+// epilogue rounds it once to bf16, the A operand of the score MMA.  The output
+// row is the 576-wide query of the latent attention: q_lat followed by a copy
+// of q_pe.
 #include "tc_ptx.cuh"
 
 namespace mla {
 namespace {
 
-__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
+using namespace tc;
 
-// One CTA per head, 8 warps.  W_UK[h] (512 x 128 bf16, 128 KB) arrives by four
-// 2-D TMA tiles of 256 rows x 64 dims (128B swizzle: conflict-free fragment
-// reads) issued at entry, so it is read from HBM exactly once.  The batch is
-// processed 64 rows at a time: the rows' q_nope are staged in padded rows, and
-// warp w computes latent columns [64w, 64w+64) of all 64 rows.
-constexpr int QROWS = 64;
-constexpr int QLD = DN + 8;           // padded bf16 row stride (272 B) of the staged queries
-constexpr uint32_t W_TILE = 256 * 128;  // 32 KB: 256 latent columns x 64 dims, 128B-swizzled
+constexpr int QROWS = 128;                // batch rows per pass (MMA M)
+constexpr uint32_t W_TILE = 256 * 128;    // 32 KB: 256 latent columns x 64 dims, 128B-swizzled
+constexpr uint32_t Q_TILE = QROWS * 128;  // 16 KB: 128 rows x 64 dims, 128B-swizzled
 
 struct __align__(1024) QaSmem {
-  uint8_t w[4][W_TILE];     // tile 2*dc + ch: dims [64dc, 64dc+64) of latent columns [256ch, 256ch+256)
-  uint16_t q[QROWS * QLD];  // q_nope rows of the current pass
-  uint64_t w_full;
+  uint8_t w[4][W_TILE];  // tile 2*dc + nh: dims [64dc, 64dc+64) of latent columns [256nh, 256nh+256)
+  uint8_t q[2][Q_TILE];  // q_nope rows of the pass, dims [64dc, 64dc+64)
+  uint64_t w_full, q_full, mma_done;
+  uint32_t tmem_base;
 };
 
-__global__ void __launch_bounds__(256, 1) q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
-                                                           const uint16_t* __restrict__ q_nope,
+__global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                           const __grid_constant__ CUtensorMap tm_q,
                                                            const uint16_t* __restrict__ q_pe, int H, int B,
                                                            uint16_t* __restrict__ q_cat) {
   extern __shared__ uint8_t smem_raw[];
   QaSmem& S = *reinterpret_cast<QaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int h = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int n_base = warp * 64;
+  const int passes = (B + QROWS - 1) / QROWS;
 
   if (tid == 0) {
     mbar_init(&S.w_full, 1);
+    mbar_init(&S.q_full, 1);
+    mbar_init(&S.mma_done, 1);
     fence_barrier_init();
     mbar_arrive_expect_tx(&S.w_full, 4 * W_TILE);
     for (int dc = 0; dc < 2; ++dc)
-      for (int ch = 0; ch < 2; ++ch) tc::tma_load_3d(S.w[2 * dc + ch], &tm_w, 64 * dc, 256 * ch, h, &S.w_full);
+      for (int nh = 0; nh < 2; ++nh) tma_load_3d(S.w[2 * dc + nh], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
   }
-  // fragment W_UK[h][c][k .. k+1] from the swizzled tiles (k even)
-  auto wfrag = [&](int c, int k) -> uint32_t {
-    const int kb = (k & 63) * 2, r = c & 255;
-    return *reinterpret_cast<const uint32_t*>(S.w[2 * (k >> 6) + (c >> 8)] + r * 128 + ((((kb >> 4) ^ (r & 7))) << 4) +
-                                              (kb & 15));
-  };
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = S.tmem_base;
+  const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
 
-  bool w_ready = false;
-  for (int b0 = 0; b0 < B; b0 += QROWS) {
-    for (int i = tid; i < QROWS * (DN / 8); i += blockDim.x) {
-      const int r = i / (DN / 8), v = i % (DN / 8);
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (b0 + r < B) x = __ldg(reinterpret_cast<const uint4*>(q_nope + ((size_t)(b0 + r) * H + h) * DN) + v);
-      *reinterpret_cast<uint4*>(S.q + r * QLD + v * 8) = x;
+  for (int p = 0; p < passes; ++p) {
+    const int b0 = p * QROWS;
+    if (tid == 0) {
+      // rows past B read as zeros (out-of-bounds fill)
+      mbar_arrive_expect_tx(&S.q_full, 2 * Q_TILE);
+      for (int dc = 0; dc < 2; ++dc) tma_load_3d(S.q[dc], &tm_q, 64 * dc, h, b0, &S.q_full);
+      bool ok = mbar_wait(&S.q_full, (uint32_t)p & 1u);
+      if (p == 0) ok = mbar_wait(&S.w_full, 0) && ok;
+      if (ok) {
+        fence_after_sync();
+        for (int nh = 0; nh < 2; ++nh)
+          for (int dc = 0; dc < 2; ++dc) {
+            const uint64_t ad = smem_desc(smem_u32(S.q[dc]), 16, 1024, SWIZZLE_128B);
+            const uint64_t bd = smem_desc(smem_u32(S.w[2 * dc + nh]), 16, 1024, SWIZZLE_128B);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + 256 * nh, ad + (uint64_t)((kk * 32) >> 4), bd + (uint64_t)((kk * 32) >> 4), idesc,
+                     (dc | kk) != 0 ? 1u : 0u);
+          }
+      }
+      mma_commit(&S.mma_done);  // arrives even if nothing was issued
     }
-    // q_pe rows of this pass: 64 rows x 8 vectors of 16 bytes
+    // q_pe rows of this pass, while the MMAs run
     for (int i = tid; i < QROWS * 8; i += blockDim.x) {
       const int r = b0 + i / 8, v = i % 8;
       if (r < B)
         reinterpret_cast<uint4*>(q_cat + ((size_t)r * H + h) * DK + DC)[v] =
             __ldg(reinterpret_cast<const uint4*>(q_pe + ((size_t)r * H + h) * DR) + v);
     }
-    if (!w_ready) {
-      (void)mbar_wait(&S.w_full, 0);  // bounded; the copies of a valid buffer always land
-      w_ready = true;
-    }
-    __syncthreads();
-
-    float acc[4][8][4];
+    (void)mbar_wait(&S.mma_done, (uint32_t)p & 1u);
+    __syncwarp();
+    fence_after_sync();
+    // epilogue: warp w owns TMEM lanes (rows) 32w..32w+31
+    const int r = b0 + warp * 32 + lane;
+    uint16_t* dst = q_cat + ((size_t)r * H + h) * DK;
+    for (int c32 = 0; c32 < DC / 32; ++c32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * c32, v);
+      tmem_ld_wait();
+      if (r < B) {
 #pragma unroll
-    for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-      for (int ni = 0; ni < 8; ++ni)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[mi][ni][r] = 0.f;
-#pragma unroll 2
-    for (int k0 = 0; k0 < DN; k0 += 16) {
-      uint32_t bf[8][2];
-#pragma unroll
-      for (int ni = 0; ni < 8; ++ni) {
-        const int c = n_base + ni * 8 + g;
-        bf[ni][0] = wfrag(c, k0 + 2 * t);
-        bf[ni][1] = wfrag(c, k0 + 8 + 2 * t);
-      }
-#pragma unroll
-      for (int mi = 0; mi < 4; ++mi) {
-        const uint16_t* a0 = S.q + (mi * 16 + g) * QLD + k0 + 2 * t;
-        const uint16_t* a1 = a0 + 8 * QLD;
-        uint32_t af[4];
-        af[0] = *reinterpret_cast<const uint32_t*>(a0);
-        af[1] = *reinterpret_cast<const uint32_t*>(a1);
-        af[2] = *reinterpret_cast<const uint32_t*>(a0 + 8);
-        af[3] = *reinterpret_cast<const uint32_t*>(a1 + 8);
-#pragma unroll
-        for (int ni = 0; ni < 8; ++ni) mma_bf16_16816(acc[mi][ni], af, bf[ni]);
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<uint4*>(dst + 32 * c32)[k] =
+              make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
       }
     }
-#pragma unroll
-    for (int mi = 0; mi < 4; ++mi) {
-      const int r0 = b0 + mi * 16 + g, r1 = r0 + 8;
-#pragma unroll
-      for (int ni = 0; ni < 8; ++ni) {
-        const int col = n_base + ni * 8 + 2 * t;
-        if (r0 < B)
-          *reinterpret_cast<uint32_t*>(q_cat + ((size_t)r0 * H + h) * DK + col) =
-              pack_bf16x2(acc[mi][ni][0], acc[mi][ni][1]);
-        if (r1 < B)
-          *reinterpret_cast<uint32_t*>(q_cat + ((size_t)r1 * H + h) * DK + col) =
-              pack_bf16x2(acc[mi][ni][2], acc[mi][ni][3]);
-      }
-    }
-    __syncthreads();  // the staged rows are rewritten by the next pass
+    fence_before_sync();
+    __syncthreads();  // TMEM and the q tiles are rewritten by the next pass
+    fence_after_sync();
   }
-  if (!w_ready) (void)mbar_wait(&S.w_full, 0);  // no pass ran: let the copies land before exit
+  if (passes == 0 && tid == 0) (void)mbar_wait(&S.w_full, 0);  // let the weight copies land before exit
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 }  // namespace
@@ -136,14 +124,17 @@ __global__ void __launch_bounds__(256, 1) q_absorb_kernel(const __grid_constant_
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
                             cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  CUtensorMap tm_w;  // W_UK: (128 dims, 512 latent columns, H heads), tiles of 64 x 256, 128B swizzle
+  CUtensorMap tm_w, tm_q;
+  // W_UK: (128 dims, 512 latent columns, H heads), tiles of 64 x 256; q_nope: (128 dims, H, B), tiles of 64 x 1 x 128
   if (!encode_3d(&tm_w, W_UK, DN, DC, H, DN * 2, (uint64_t)DC * DN * 2, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_3d_box(&tm_q, q_nope, DN, H, B, DN * 2, (uint64_t)H * DN * 2, 64, 1, QROWS, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(QaSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  q_absorb_kernel<<<H, 256, smem, s>>>(tm_w, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe),
-                                       H, B, static_cast<uint16_t*>(q_cat));
+  q_absorb_kernel<<<H, 128, smem, s>>>(tm_w, tm_q, static_cast<const uint16_t*>(q_pe), H, B,
+                                       static_cast<uint16_t*>(q_cat));
   return cudaGetLastError();
 }
 
