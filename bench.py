@@ -275,11 +275,16 @@ def run_ours(args, wl, fmt):
         time.sleep(0.3)
     t0.record(stream)
     for k in range(args.steps):
-        step(attend_ev[k])
+        step()  # no events between the launches: consecutive kernels overlap their prologues
     t1.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop() if clocks else None
     elapsed_ms = t0.elapsed_time(t1)
+    # per-stage times (and the attend time of the roofline) from a second run of
+    # the same steps with events between the launches
+    for k in range(args.steps):
+        step(attend_ev[k])
+    torch.cuda.synchronize()
     attend_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in attend_ev]))
     stage_ms = {name: float(np.mean([e[k].elapsed_time(e[k + 1]) for e in attend_ev]))
                 for k, name in enumerate(("plan", "absorb_q", "attend", "combine"))}

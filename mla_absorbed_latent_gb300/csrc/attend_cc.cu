@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(THREADS, 2)
                      int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SmemCC& S = *reinterpret_cast<SmemCC*>(smem_raw);
+  grid_dep_wait();  // the plan, the query and the cache may come from the kernel before this one
+  grid_dep_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int worker = blockIdx.x, hg = blockIdx.y;
   const int T = plan[0], W = plan[1];
@@ -273,10 +275,9 @@ cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, c
   const size_t smem = sizeof(SmemCC);
   cudaError_t e = cudaFuncSetAttribute(attend_cc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attend_cc_kernel<<<dim3(workers, H / HG), THREADS, smem, s>>>(
-      static_cast<const uint16_t*>(q_cat), H, num_pages, static_cast<const uint8_t*>(pages), page_table, max_pages,
-      B, scale * 1.4426950408889634f, plan, part_o, part_lse, err);
-  return cudaGetLastError();
+  return launch_pdl(attend_cc_kernel, dim3(workers, H / HG), dim3(THREADS), smem, s,
+                    static_cast<const uint16_t*>(q_cat), H, num_pages, static_cast<const uint8_t*>(pages), page_table,
+                    max_pages, B, scale * 1.4426950408889634f, plan, part_o, part_lse, err);
 }
 
 }  // namespace mla

@@ -277,12 +277,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int worker = blockIdx.x >> 1;
-  const int T = a.plan[0], W = a.plan[1], B = a.B;
-  const int* prefix = a.plan + PLAN_HDR;
-  const int* seq_c = a.plan + PLAN_HDR + B + 1;
-  const int row0 = a.plan[PLAN_HDR + 2 * B + 1 + worker];  // first row of this worker's range
-  const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
-  const int ntiles = x1 - x0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_ST; ++s) {
@@ -318,6 +312,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   cluster_sync();  // the peer arrives on our barriers and writes our exchange buffers
   fence_after_sync();
   const uint32_t tmem = S.tmem_base;
+  // everything above overlaps the end of the kernel before this one; the plan,
+  // the query and the cache may come from it
+  grid_dep_wait();
+  grid_dep_launch();
+  const int T = a.plan[0], W = a.plan[1], B = a.B;
+  const int* prefix = a.plan + PLAN_HDR;
+  const int* seq_c = a.plan + PLAN_HDR + B + 1;
+  const int row0 = a.plan[PLAN_HDR + 2 * B + 1 + worker];  // first row of this worker's range
+  const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
+  const int ntiles = x1 - x0;
 
   // Roles of warps 0..3 rotate with the rank so that the two S issuers run on
   // the SM sub-partitions of the sender warps (warp w runs on sub-partition
@@ -869,8 +873,10 @@ cudaLaunchConfig_t launch_config(int workers, cudaStream_t s, cudaLaunchAttribut
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dep_wait in the kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -885,7 +891,7 @@ int attend_tc_workers(int num_sms) {
     int clusters = 0;
     if (cudaFuncSetAttribute(attend_tc_kernel<MLA_FMT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<MLA_FMT_BF16>()) == cudaSuccess) {
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = launch_config(num_sms / 2, nullptr, attr);
       if (cudaOccupancyMaxActiveClusters(&clusters, attend_tc_kernel<MLA_FMT_BF16>, &cfg) != cudaSuccess) clusters = 0;
     }
@@ -939,7 +945,7 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   args.max_pages = max_pages;
   args.num_pages = num_pages;
   args.scale_log2 = scale * 1.4426950408889634f;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(workers, s, attr);
   auto go = [&](auto kernel, size_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -59,6 +59,8 @@ __device__ __forceinline__ size_t merged_slot(const int* prefix, long long T, lo
 __global__ void __launch_bounds__(256) merge_kernel(int H, int B, const int* __restrict__ plan,
                                                      float* __restrict__ part_o, const float* __restrict__ part_lse,
                                                      float* __restrict__ o_lat_out) {
+  grid_dep_wait();  // the partials of the attend step
+  grid_dep_launch();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (gw >= B * H) return;
   const int b = gw / H, h = gw % H;
@@ -151,9 +153,13 @@ __global__ void __launch_bounds__(256, 1) upproj_kernel(const __grid_constant__ 
   }
   __syncthreads();
   if (tid == 0) {
+    // W_UV is read before the wait: this kernel always follows the merge
+    // kernel, which itself waited for all earlier work
     mbar_arrive_expect_tx(&S.w_full, 8 * W_CHUNK);
     for (int kc = 0; kc < 8; ++kc) tc::tma_load_3d(S.w[kc], &tm_w, 64 * kc, 0, h, &S.w_full);
   }
+  grid_dep_wait();  // the merged rows
+  grid_dep_launch();
   // pass p's rows into buffer p & 1: thread r < 16 copies row b0 + r (zeros
   // for empty rows and rows past B) and arrives once
   auto issue_rows = [&](int p) {
@@ -230,8 +236,7 @@ cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, cons
                            const float* part_lse, void* out, float* o_lat, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   float* po = const_cast<float*>(part_o);  // the merge writes each row's o_lat into its first partial slot
-  merge_kernel<<<(B * H + 7) / 8, 256, 0, s>>>(H, B, plan, po, part_lse, o_lat);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(merge_kernel, dim3((B * H + 7) / 8), dim3(256), 0, s, H, B, plan, po, part_lse, o_lat);
   if (e != cudaSuccess) return e;
   CUtensorMap tm_w;  // W_UV: (512 latent, 128 rows, H heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, H, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -239,8 +244,8 @@ cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, cons
   const size_t smem = sizeof(UpSmem) + 1024;
   e = cudaFuncSetAttribute(upproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  upproj_kernel<<<H, 256, smem, s>>>(tm_w, H, B, plan, po, static_cast<uint16_t*>(out));
-  return cudaGetLastError();
+  return launch_pdl(upproj_kernel, dim3(H), dim3(256), smem, s, tm_w, H, B, plan, static_cast<const float*>(po),
+                    static_cast<uint16_t*>(out));
 }
 
 }  // namespace mla

@@ -17,6 +17,8 @@ namespace {
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seqlens, int B, int max_pages,
                                                      int workers, int* __restrict__ plan, int* err) {
   __shared__ int warp_sums[32];
+  grid_dep_wait();  // earlier work may still write the lengths or read this plan
+  grid_dep_launch();
   const int tid = threadIdx.x;
   const int per = (B + blockDim.x - 1) / blockDim.x;
   const int lo = min(B, tid * per), hi = min(B, lo + per);
@@ -86,8 +88,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,
                         cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(seqlens, B, max_pages, workers, plan, err);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, seqlens, B, max_pages, workers, plan, err);
 }
 
 }  // namespace mla

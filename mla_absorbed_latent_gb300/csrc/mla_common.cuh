@@ -193,4 +193,28 @@ bool encode_3d_box(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
                    uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw,
                    CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
+// Programmatic dependent launch.  A kernel of the decode chain is launched
+// with launch_pdl, so it may start while the kernel before it in the stream is
+// still running; it must call grid_dep_wait before touching any memory that
+// earlier work may write (or read), and calls grid_dep_launch after that wait,
+// letting the next kernel of the chain begin its own prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace mla

@@ -44,6 +44,10 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     mbar_init(&S.q_full, 1);
     mbar_init(&S.mma_done, 1);
     fence_barrier_init();
+  }
+  grid_dep_wait();  // the weights and queries may come from the work before this kernel
+  grid_dep_launch();
+  if (tid == 0) {
     mbar_arrive_expect_tx(&S.w_full, 4 * W_TILE);
     for (int dc = 0; dc < 2; ++dc)
       for (int nh = 0; nh < 2; ++nh) tma_load_3d(S.w[2 * dc + nh], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
@@ -133,9 +137,8 @@ cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_
   const size_t smem = sizeof(QaSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  q_absorb_kernel<<<H, 128, smem, s>>>(tm_w, tm_q, static_cast<const uint16_t*>(q_pe), H, B,
-                                       static_cast<uint16_t*>(q_cat));
-  return cudaGetLastError();
+  return launch_pdl(q_absorb_kernel, dim3(H), dim3(128), smem, s, tm_w, tm_q, static_cast<const uint16_t*>(q_pe), H,
+                    B, static_cast<uint16_t*>(q_cat));
 }
 
 }  // namespace mla
