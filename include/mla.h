@@ -59,7 +59,9 @@ typedef enum {
   MLA_ERR_CUDA = -3,         /* a CUDA runtime call (launch, attribute) failed        */
   MLA_ERR_BOUNDS = -4,       /* device: page id outside the pool / sequence too long  */
   MLA_ERR_TIMEOUT = -5,      /* device: a bounded wait inside a kernel gave up        */
-  MLA_ERR_WORKSPACE = -6     /* workspace smaller than mla_decode_workspace_bytes     */
+  MLA_ERR_WORKSPACE = -6,    /* workspace smaller than mla_decode_workspace_bytes     */
+  MLA_ERR_RANGE = -7         /* device: a score exceeded its segment's running maximum
+                                by more than 100 (log2 units); weights were capped  */
 } mla_status_t;
 
 /* Cache storage formats. */

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
-MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = -4, -5, -6
+MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE, MLA_ERR_RANGE = -4, -5, -6, -7
 FMT = {"bf16": 0, "int8": 1, "int4": 2}
 D_C, D_R, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
 

@@ -65,35 +65,34 @@ namespace {
 
 using namespace tc;
 
-constexpr int NSUB = 4;                                       // softmax warps per TMEM lane quadrant
-constexpr int TC_THREADS = 128 + 128 * NSUB;                  // 4 role warps + 4 quadrants x NSUB
+constexpr int TC_THREADS = 512;  // 4 role warps + per TMEM lane quadrant 2 MT warps and 1 PT warp
 constexpr int SOFT_WARP0 = 4;
 constexpr int TILE = 64;                                      // tokens per page / TMA stage / S tile
 constexpr int HALF_C = 256;
 constexpr int PE_HALF = 32;
-constexpr int OWN_H = 64;                                     // heads whose softmax one CTA runs
-constexpr int TPW = 64 / NSUB;                                // tokens of a page per softmax thread
-constexpr int OCOLS = 256 / NSUB;                             // O columns (of 256) per softmax thread
-constexpr int QCOLS = 128 / NSUB;                             // q_lat TMEM columns (bf16 pairs) per thread
+constexpr int HALF_T = 32;                                    // tokens of a page whose softmax one CTA runs
+constexpr int TPW = 16;                                       // tokens of a page per MT thread
+constexpr int QCOLS = 64;                                     // q_lat TMEM columns (bf16 pairs) per MT thread
 constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                  // 8,192: [64 tokens][64 dims] 128B-swizzled
 constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                  // 32,768: [64 tokens][32 dims] 64B-swizzled
 constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2;  // 36,864
-constexpr uint32_t P_BYTES = 128 * TILE * 2;                  // 16,384: [128 heads][64 tokens] 128B-swizzled
-constexpr uint32_t X_BYTES = OWN_H * TILE * 2;                // 8,192: fp16 partial scores of 64 heads
-constexpr uint32_t MSG_BYTES = OWN_H * 8;                     // 512: (rescale factor, 1/l) per head
-constexpr uint32_t PIN_BYTES = OWN_H * TILE * 2 + MSG_BYTES;  // P rows of the peer's heads + their messages
+constexpr uint32_t PH_BYTES = 128 * HALF_T * 2;               // 8,192: P of a token half, [128][32] 64B-swizzled
+constexpr uint32_t X_BYTES = 128 * HALF_T * 2;                // 8,192: fp16 partial scores of a token half
+constexpr uint32_t MSG_BYTES = 128 * 8;                       // 1,024: two floats per head
+constexpr uint32_t PIN_BYTES = PH_BYTES + MSG_BYTES;          // the peer's P half and its message
 constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
-constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of all owner / sender threads (1..4: quadrants)
+constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p tolerated (O and l stay finite in fp32)
+constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of the 256 MT / 256 PT threads
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 // Per cache format: bf16 pages are TMA-copied straight into the MMA operand
 // stages (4 of them).  Quantized pages land in a small staging ring of codes
 // and scales; the sender warps dequantize each into a bf16 operand stage (3 of
-// them: shared memory holds no more next to the staging ring).  Offsets are
+// them, 2: shared memory holds no more next to the staging ring).  Offsets are
 // bytes inside one staging slot (this CTA's half of a page, unswizzled rows):
 //   INT8: c codes i8 [64][256] | k_pe codes i8 [64][32] | c scales bf16 [64][8]
 //         | k_pe scales bf16 [64][8] (all 8 groups of the token)
@@ -105,12 +104,12 @@ template <> struct FmtTraits<MLA_FMT_BF16> {
   static constexpr uint32_t CODE_BYTES = 0, C_OFF = 0, PE_OFF = 0, CS_OFF = 0, ZS_OFF = 0, PS_OFF = 0;
 };
 template <> struct FmtTraits<MLA_FMT_INT8> {
-  static constexpr int KV_ST = 3, CODE_ST = 2;
+  static constexpr int KV_ST = 2, CODE_ST = 3;
   static constexpr uint32_t C_OFF = 0, PE_OFF = 16384, CS_OFF = 18432, ZS_OFF = 0, PS_OFF = 19456;
   static constexpr uint32_t CODE_BYTES = 20480;
 };
 template <> struct FmtTraits<MLA_FMT_INT4> {
-  static constexpr int KV_ST = 3, CODE_ST = 3;
+  static constexpr int KV_ST = 2, CODE_ST = 4;
   static constexpr uint32_t C_OFF = 0, PE_OFF = 8192, CS_OFF = 10240, ZS_OFF = 11264, PS_OFF = 12288;
   static constexpr uint32_t CODE_BYTES = 13312;
 };
@@ -121,21 +120,21 @@ struct __align__(1024) SmemTC {
   static constexpr int CODE_ST = FmtTraits<FMT>::CODE_ST > 0 ? FmtTraits<FMT>::CODE_ST : 1;
   static constexpr uint32_t CODE_BYTES = FmtTraits<FMT>::CODE_BYTES > 0 ? FmtTraits<FMT>::CODE_BYTES : 128;
   uint8_t kv[KV_ST][KV_BYTES];
-  uint8_t p[2][P_BYTES];
-  uint8_t xin[2][X_BYTES];  // the peer's fp16 partials for our heads; row = 128 B, chunks swizzled by row
-  uint8_t xout[2][X_BYTES]; // our fp16 partials for the peer's heads, same layout, shipped by one bulk copy
+  uint8_t p[2][2][PH_BYTES];  // P per page parity and token half ([128 heads][32 tokens], 64B-swizzled)
+  uint8_t xin[2][X_BYTES];    // the peer's fp16 partials of our token half, rows 64 B, chunks swizzled
+  uint8_t xout[2][X_BYTES];   // ours of the peer's token half, same layout, shipped by one bulk copy
   uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
   uint8_t qpe[QPE_BYTES];
-  float2 msg[2][OWN_H];     // from the peer, per peer head: (O rescale factor, 1/l at a segment end)
-  float2 msg_out[2][OWN_H]; // the same for our heads, shipped to the peer
-  float red_m[2][NSUB][OWN_H];  // row maxima of the NSUB token slices [page parity][slice][own head]
-  float red_l[NSUB][OWN_H];     // row sums of the slices at a segment end [slice][own head]
+  float2 msg_in[2][128];   // from the peer per page and head: its two slices' maxima (sums at a segment end)
+  float2 msg_out[2][128];  // ours, shipped with our P half
+  float2 mx_in[2][128];    // first page of a segment: the peer's two slices' maxima, exchanged before P
+  float2 mx_out[2][128];
   uint64_t kv_full[KV_ST], kv_empty[KV_ST];
   uint64_t code_full[CODE_ST], code_empty[CODE_ST];
   uint64_t q_ready;         // q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2], pv_both[2];
-  uint64_t x_full[2], x_empty[2], pin_full[2];
+  uint64_t x_full[2], x_empty[2], pin_full[2], mx_full[2];
   uint64_t o_free, mma_done[3];
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -143,7 +142,7 @@ struct __align__(1024) SmemTC {
 static_assert(sizeof(SmemTC<MLA_FMT_BF16>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT8>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT4>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
-static_assert(KV_BYTES % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(KV_BYTES % 1024 == 0 && PH_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct TcArgs {
   const uint16_t* q_cat;  // [B][128][576] bf16
@@ -221,10 +220,13 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
 }
 __device__ __forceinline__ float fp16_clamp(float v) { return fminf(fmaxf(v, -FP16_MAX), FP16_MAX); }
 
-// byte offset of 16-byte chunk c (0..7, 8 tokens) of row r in a [64][64] fp16 exchange tile
-__device__ __forceinline__ uint32_t xoff(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-// byte offset of 16-byte unit u (0..7, 8 tokens) of row r in a 128B-swizzled [128][64] bf16 tile
-__device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
+// byte offset of 16-byte unit u (0..3, 8 tokens) of row r in a 64B-swizzled tile of 64-byte rows
+// (the P half tiles, read by the tensor core, and the fp16 exchange tiles)
+__device__ __forceinline__ uint32_t sw64(int r, int u) { return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4)); }
+// two bf16 in one word times f, rounded again to bf16
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float f) {
+  return pack_bf16x2(__uint_as_float(v << 16) * f, __uint_as_float(v & 0xffff0000u) * f);
+}
 
 // ---- dequantization ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 block
 // quantizers): x = code * s (INT8), x = code * s + z (INT4), evaluated in fp32
@@ -280,25 +282,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KV_ST; ++s) {
-      mbar_init(&S.kv_full[s], kQuant ? 2 * NSUB : 1);  // quantized: the sender warps after dequantizing
+      mbar_init(&S.kv_full[s], kQuant ? 4 : 1);  // quantized: the 4 PT warps after dequantizing
       mbar_init(&S.kv_empty[s], 1);
     }
     for (int s = 0; s < CODE_ST; ++s) {
       mbar_init(&S.code_full[s], 1);
-      mbar_init(&S.code_empty[s], 2 * NSUB);
+      mbar_init(&S.code_empty[s], 4);
     }
-    mbar_init(&S.q_ready, 4 * NSUB + 1);
+    mbar_init(&S.q_ready, 9);  // the 8 MT warps' q_lat + the q_pe copy
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
-      mbar_init(&S.s_free[s], 4 * NSUB);
-      mbar_init(&S.p_full[s], 4 * NSUB);
+      mbar_init(&S.s_free[s], 12);  // every softmax warp
+      mbar_init(&S.p_full[s], 8);  // the MT warps' checks
       mbar_init(&S.pv_done[s], 1);
       mbar_init(&S.pv_both[s], 2);   // this CTA's and the peer's P.V commits
       mbar_init(&S.x_full[s], 1);    // local expect_tx arrival + the peer's fp16 partial bytes
-      mbar_init(&S.x_empty[s], 2 * NSUB);  // one remote arrival per peer owner warp
-      mbar_init(&S.pin_full[s], 1);  // local expect_tx arrival + the peer's P rows and messages
+      mbar_init(&S.x_empty[s], 8);   // one remote arrival per peer MT warp
+      mbar_init(&S.pin_full[s], 1);  // local expect_tx arrival + the peer's P half and message
+      mbar_init(&S.mx_full[s], 1);   // local expect_tx arrival + the peer's first-page maxima
     }
-    mbar_init(&S.o_free, 4 * NSUB);
+    mbar_init(&S.o_free, 8);  // the MT warps' epilogues
     for (int k = 0; k < 3; ++k) mbar_init(&S.mma_done[k], 1);
     S.abort_flag = 0;
     fence_barrier_init();
@@ -462,13 +465,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         ++segments;
       }
       fence_after_sync();
-      fence_proxy_async_smem();  // P rows written by the peer's remote stores -> tensor core
-      const uint64_t adesc = smem_desc(smem_u32(S.p[pb]), 16, 1024, SWIZZLE_128B);
+      fence_proxy_async_smem();  // P written or rescaled by this CTA's threads -> tensor core
       const uint64_t vdesc = smem_desc(smem_u32(S.kv[st]), KV_CHUNK, 1024, SWIZZLE_128B);
 #pragma unroll
-      for (int kk = 0; kk < TILE / 16; ++kk)
-        mma_ss(tmem + TM_O, adesc + (uint64_t)((kk * 32) >> 4), vdesc + (uint64_t)((kk * 16 * 128) >> 4),
+      for (int kk = 0; kk < TILE / 16; ++kk) {
+        // tokens 16kk..16kk+15: the half tile kk/2, K step kk%2 inside it
+        const uint64_t adesc = smem_desc(smem_u32(S.p[pb][kk >> 1]), 16, 512, SWIZZLE_64B);
+        mma_ss(tmem + TM_O, adesc + (uint64_t)(((kk & 1) * 32) >> 4), vdesc + (uint64_t)((kk * 16 * 128) >> 4),
                idesc_pv, (first && kk == 0) ? 0u : 1u);
+      }
       mma_commit(&S.pv_done[pb]);
       mma_commit_mc(&S.pv_both[pb], (uint16_t)0x3);
       mma_commit(&S.kv_empty[st]);
@@ -478,10 +483,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (ntiles > 0 && warp >= SOFT_WARP0) {
     // ------------------------------------------------------------ softmax warps
     const int q4 = warp & 3;                  // TMEM lane quadrant
-    const int sub = (warp - SOFT_WARP0) >> 2;  // token slice of each page: [TPW*sub, TPW*sub + TPW)
+    const int sub = (warp - SOFT_WARP0) >> 2;  // 0, 1: MT slice; 2: PT
     const int row = q4 * 32 + lane;           // head = TMEM lane
-    const int hl = row & (OWN_H - 1);         // index among the 64 heads of the CTA that owns this head
-    const bool owner = (uint32_t)(q4 >> 1) == rank;
     const int stid = threadIdx.x - 32 * SOFT_WARP0;  // 0..255
     const uint32_t t_row = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = a.scale_log2;  // > 0
@@ -512,12 +515,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_load_3d(S.qpe, &tm_q_pe, DC + PE_HALF * rank, 0, b, &S.q_ready);
       }
     };
-    // O row of this lane, this thread's OCOLS columns, times f
+    // The pair splits every page by token half: CTA r runs the softmax of all
+    // 128 heads over tokens [32r, 32r+32) ("my" tokens).  In each lane quadrant
+    // the warps with sub 0, 1 ("MT") own 16 of my tokens each and keep O (128
+    // columns each) and the query; the warp with sub 2 ("PT") ships the peer's
+    // 32 tokens' partial scores and, for quantized pools, dequantizes the next
+    // page.
+    const bool mt = sub < 2;
+    const int ms = sub & 1;                   // MT: slice index within the token half
+    // O row of this lane, MT slice ms's 128 columns, times f
     auto scale_o = [&](float f) {
 #pragma unroll 1
-      for (int k32 = 0; k32 < OCOLS / 32; ++k32) {
+      for (int k32 = 0; k32 < 4; ++k32) {
         uint32_t o[32];
-        const uint32_t col = t_row + TM_O + OCOLS * sub + 32 * k32;
+        const uint32_t col = t_row + TM_O + 128 * ms + 32 * k32;
         tmem_ld32(col, o);
         tmem_ld_wait();
 #pragma unroll
@@ -526,13 +537,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       tmem_st_wait();
     };
-    // O row of this lane times inv -> the segment's partial output (this CTA's latent half)
+    // the same columns times inv -> the segment's partial output (this CTA's latent half)
     auto store_o = [&](int seg, float inv) {
-      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + OCOLS * sub;
+      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms;
 #pragma unroll 1
-      for (int k32 = 0; k32 < OCOLS / 32; ++k32) {
+      for (int k32 = 0; k32 < 4; ++k32) {
         uint32_t o[32];
-        tmem_ld32(t_row + TM_O + OCOLS * sub + 32 * k32, o);
+        tmem_ld32(t_row + TM_O + 128 * ms + 32 * k32, o);
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -542,16 +553,88 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
 
     bool failed = false;
-    load_query(rc.b);
-    if (owner) {
-      // ---------------------------------------------------------- owners
-      const uint32_t quad_bar = 1 + q4;  // named barrier of the NSUB warps of this quadrant
-      const bool leader = (q4 == 2 * (int)rank) && sub == 0 && lane == 0;
+    if (mt) load_query(rc.b);
+    if (mt) {
+      // ---------------------------------------------------------- MT warps
+      const bool leader = q4 == 0 && ms == 0 && lane == 0;
       const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0]), peer);
-      const uint32_t peer_p = mapa(smem_u32(S.p[0]), peer);
-      const uint32_t peer_msg = mapa(smem_u32(&S.msg[0][0]), peer);
+      const uint32_t peer_p = mapa(smem_u32(S.p[0][0]), peer);
+      const uint32_t peer_msg = mapa(smem_u32(&S.msg_in[0][0]), peer);
+      const uint32_t peer_mx = mapa(smem_u32(&S.mx_in[0][0]), peer);
       const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0]), peer);
-      float m_ref = -INFINITY, l = 0.f;
+      const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[0]), peer);
+      const int tok0 = HALF_T * (int)rank + TPW * ms;  // first page token of this thread's slice
+      // softmax state of this head (lane), log2 domain:
+      //  m_ref      reference of the P written from now on
+      //  l          sum of this slice's p over the segment so far, in m_ref
+      //  alpha_due  factor by which P of the page after the last checked one
+      //             and O must still be rescaled (a reference move), 1 if none
+      float m_ref = -INFINITY, l = 0.f, alpha_due = 1.f;
+      int fcnt0 = 0, fcnt1 = 0;  // first pages seen per page parity (phases of mx_full)
+      // lagged check of page j: the peer's P half and message have arrived ->
+      // decide reference moves, rescale what page j still needs, release its
+      // P.V; at a segment end write the segment's output.  ref_j: the
+      // reference page j's P was written in.
+      auto check = [&](int j, bool j_last, int seg, float ref_j) -> bool {
+        const int jb = j & 1;
+        bool ok = wait_bar<true>(S, &S.pin_full[jb], (uint32_t)(j >> 1) & 1u, a.err, 20);
+        __syncwarp();
+        const float2 mine = S.msg_out[jb][row], theirs = S.msg_in[jb][row];
+        // a move decided at the previous check: page j's P (both halves, this
+        // CTA's copy) and O (after page j-1's P.V) go to the new reference
+        const float alpha = alpha_due;
+        alpha_due = 1.f;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!wait_bar<false>(S, &S.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.err, 21)) ok = false;
+          __syncwarp();
+          fence_after_sync();
+          scale_o(alpha);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint8_t* ph = S.p[jb][hf];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              uint4* u = reinterpret_cast<uint4*>(ph + sw64(row, 2 * ms + k));
+              uint4 v = *u;
+              v.x = scale_bf16x2(v.x, alpha); v.y = scale_bf16x2(v.y, alpha);
+              v.z = scale_bf16x2(v.z, alpha); v.w = scale_bf16x2(v.w, alpha);
+              *u = v;
+            }
+          }
+          fence_proxy_async_smem();
+          fence_before_sync();
+        }
+        if (!j_last) {
+          // page j's maximum over all four slices against the reference it used
+          const float m_comb = fmaxf(fmaxf(mine.x, mine.y), fmaxf(theirs.x, theirs.y));
+          if (m_comb > ref_j + RESCALE_LOG2) {
+            const float m_new = fmaxf(m_comb, m_ref);
+            alpha_due = ex2(m_ref - m_new);  // for page j+1's P and O, at the next check
+            l *= alpha_due;                  // the sums so far (pages <= j+1)
+            m_ref = m_new;                   // pages from j+2 on
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[jb]);
+        if (j_last) {
+          // the four slices' sums, in page j's reference; O is in that
+          // reference times alpha after a move applied above
+          const float Lm = mine.x + mine.y + theirs.x + theirs.y;
+          const float L = alpha * Lm;
+          if (!wait_bar<false>(S, &S.pv_done[jb], (uint32_t)(j >> 1) & 1u, a.err, 22)) ok = false;
+          __syncwarp();
+          fence_after_sync();
+          store_o(seg, 1.f / L);
+          if (rank == 0 && ms == 0) a.part_lse[(size_t)seg * 128 + row] = (ref_j + log2f(Lm)) * 0.69314718055994531f;
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.o_free);
+        }
+        return ok;
+      };
+      int pend_i = -1, pend_seg = 0;
+      bool pend_last = false;
+      float pend_ref = 0.f;
       for (int x = x0, i = 0; x < x1; ++x, ++i) {
         rc.advance(prefix, seq_c, x);
         const bool first = (x == x0) || (x == rc.start);
@@ -560,33 +643,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
-        if (leader) mbar_arrive_expect_tx(&S.x_full[sb], X_BYTES);  // the peer's partial for this page
-        // ---- this CTA's partial scores into registers; the S buffer is released
+        if (leader) {
+          mbar_arrive_expect_tx(&S.x_full[sb], X_BYTES);      // the peer's partials of my tokens
+          mbar_arrive_expect_tx(&S.pin_full[sb], PIN_BYTES);  // the peer's P half and message
+          if (first) mbar_arrive_expect_tx(&S.mx_full[sb], MSG_BYTES);  // the peer's first-page maxima
+        }
+        // ---- this CTA's partial scores of my tokens; the S buffer is released
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) failed = true;
         __syncwarp();
         fence_after_sync();
         uint32_t own[TPW];
-        tmem_ld_cols<TPW>(t_row + TM_S + TILE * sb + TPW * sub, own);
+        tmem_ld_cols<TPW>(t_row + TM_S + TILE * sb + tok0, own);
         tmem_ld_wait();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
-        // the next page starts a new segment: every S of this one has completed
-        // (this thread waited for each), so the next query may replace this one
         if (last && x + 1 < x1) {
           RowCursor nx = rc;
           nx.advance(prefix, seq_c, x + 1);
           load_query(nx.b);
         }
 
-        // ---- add the peer's partial (fp16, log2 units) for these heads
+        // ---- add the peer's partial (fp16, log2 units) of my tokens
         if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
         __syncwarp();
         float s[TPW];
         const uint8_t* xi = S.xin[sb];
 #pragma unroll
         for (int k = 0; k < TPW / 8; ++k) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xi + xoff(hl, (TPW / 8) * sub + k));
+          const uint4 v = *reinterpret_cast<const uint4*>(xi + sw64(row, (TPW / 8) * ms + k));
           const float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y), f2 = h2_to_f2(v.z), f3 = h2_to_f2(v.w);
           s[8 * k + 0] = fmaf(u2f(own[8 * k + 0]), c, f0.x);
           s[8 * k + 1] = fmaf(u2f(own[8 * k + 1]), c, f0.y);
@@ -597,108 +682,81 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           s[8 * k + 6] = fmaf(u2f(own[8 * k + 6]), c, f3.x);
           s[8 * k + 7] = fmaf(u2f(own[8 * k + 7]), c, f3.y);
         }
-
-        // ---- online softmax in the log2 domain, lazily moved reference max
         if (nvalid < TILE) {
 #pragma unroll
           for (int k = 0; k < TPW; ++k)
-            if (TPW * sub + k >= nvalid) s[k] = -INFINITY;
+            if (tok0 + k >= nvalid) s[k] = -INFINITY;
         }
         float mraw = s[0];
 #pragma unroll
         for (int k = 1; k < TPW; ++k) mraw = fmaxf(mraw, s[k]);
-        S.red_m[sb][sub][hl] = mraw;
-        // every value read from the exchange buffer has been used by the store
-        // above, so the peer may refill it
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
-        named_barrier(quad_bar, 32 * NSUB);
-        float mt = S.red_m[sb][0][hl];
-#pragma unroll
-        for (int k = 1; k < NSUB; ++k) mt = fmaxf(mt, S.red_m[sb][k][hl]);
+
+        // ---- the reference of this page's P
         if (first) {
-          m_ref = mt;
+          // segment start: the exact row maximum over the page's four slices
+          float2* mo = &S.mx_out[sb][row];
+          if (ms == 0) mo->x = mraw; else mo->y = mraw;
+          fence_proxy_async_smem();
+          if (!named_barrier_and(OWNER_BAR, 32 * 8, !failed)) break;
+          if (leader) bulk_s2peer(peer_mx + sb * MSG_BYTES, &S.mx_out[sb][0], MSG_BYTES, peer_mxf + 8u * sb);
+          const int fc = sb ? fcnt1++ : fcnt0++;
+          if (!wait_bar<true>(S, &S.mx_full[sb], (uint32_t)fc & 1u, a.err, 19)) failed = true;
+          __syncwarp();
+          const float2 a2 = S.mx_out[sb][row], b2 = S.mx_in[sb][row];
+          m_ref = fmaxf(fmaxf(a2.x, a2.y), fmaxf(b2.x, b2.y));
           l = 0.f;
         }
-        const bool need = !first && mt > m_ref + RESCALE_LOG2;
-        float alpha = 1.f;
-        if (__any_sync(0xffffffffu, need)) {
-          // O may only be touched once every P.V issued so far has completed
-          if (!wait_bar<false>(S, &S.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 12)) failed = true;
-          __syncwarp();
-          fence_after_sync();
-          if (need) alpha = ex2(m_ref - mt);
-          scale_o(alpha);
-          if (need) {
-            l *= alpha;
-            m_ref = mt;
-          }
-        }
-        // p = 2^(s - m_ref) <= 2^RESCALE_LOG2, rounded to bf16 for the MMA (the
-        // single-precision ex2 moves as many values per clock as the paired
-        // half-precision one and needs no conversions around it)
+        if (mraw - m_ref > RANGE_LOG2) raise_error(a.err, MLA_ERR_RANGE, 0);
+        // p = 2^(s - m_ref), rounded to bf16 for the MMA (exponent capped at
+        // RANGE_LOG2, beyond which the range error above is reported)
         uint32_t pk[TPW / 2];
         float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
         for (int k = 0; k < TPW / 2; ++k) {
-          const float p0 = ex2(s[2 * k] - m_ref), p1 = ex2(s[2 * k + 1] - m_ref);
+          const float p0 = ex2(fminf(s[2 * k] - m_ref, RANGE_LOG2));
+          const float p1 = ex2(fminf(s[2 * k + 1] - m_ref, RANGE_LOG2));
           sum0 += p0;
           sum1 += p1;
           pk[k] = pack_bf16x2(p0, p1);
         }
-        const float sum = sum0 + sum1;
-        l += sum;
-        float inv = 0.f, L = 0.f;
-        if (last) {
-          S.red_l[sub][hl] = l;
-          named_barrier(quad_bar, 32 * NSUB);
-#pragma unroll
-          for (int k = 0; k < NSUB; ++k) L += S.red_l[k][hl];
-          inv = 1.f / L;
-        }
+        l += sum0 + sum1;
         // P tile sb is free once the P.V of page i-2 has completed in both CTAs
         if (!wait_bar<true>(S, &S.pv_both[sb], ph ^ 1u, a.err, 13)) failed = true;
         __syncwarp();
-        uint8_t* pp = S.p[sb];
+        uint8_t* pm = S.p[sb][rank];
 #pragma unroll
         for (int k = 0; k < TPW / 8; ++k)
-          *reinterpret_cast<uint4*>(pp + sw128(row, (TPW / 8) * sub + k)) =
+          *reinterpret_cast<uint4*>(pm + sw64(row, (TPW / 8) * ms + k)) =
               make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        if (sub == 0) S.msg_out[sb][hl] = make_float2(alpha, inv);
-        fence_proxy_async_smem();
+        // message: this slice's maximum, or its sum at a segment's last page
+        float2* mo = &S.msg_out[sb][row];
+        if (ms == 0) mo->x = last ? l : mraw; else mo->y = last ? l : mraw;
+        // every value read from the exchange buffer has been used by the store
+        // above (mraw depends on all of them), so the peer may refill it
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.p_full[sb]);
-        // our 64 rows of P (contiguous: rows 64r..64r+63) and their messages to the
-        // peer; every owner thread passes here each page, so this is also where
-        // they leave together after a failed wait
-        if (!named_barrier_and(OWNER_BAR, 64 * NSUB, !failed)) break;
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
+        fence_proxy_async_smem();
+        // every MT thread passes here each page: also where they leave together
+        if (!named_barrier_and(OWNER_BAR, 32 * 8, !failed)) break;
         if (leader) {
-          const uint32_t rows = (uint32_t)OWN_H * 128u * rank;
-          bulk_s2peer(peer_p + sb * P_BYTES + rows, pp + rows, OWN_H * 128, peer_pin + 8u * sb);
+          bulk_s2peer(peer_p + (sb * 2 + rank) * PH_BYTES, pm, PH_BYTES, peer_pin + 8u * sb);
           bulk_s2peer(peer_msg + sb * MSG_BYTES, &S.msg_out[sb][0], MSG_BYTES, peer_pin + 8u * sb);
         }
-
-        // ---- end of the row's segment: O / l and the natural-log LSE
-        if (last) {
-          if (!wait_bar<false>(S, &S.pv_done[sb], ph, a.err, 14)) failed = true;
-          __syncwarp();
-          fence_after_sync();
-          const int seg = worker + rc.b;
-          store_o(seg, inv);
-          if (sub == 0) a.part_lse[(size_t)seg * 128 + row] = (m_ref + log2f(L)) * 0.69314718055994531f;
-          fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.o_free);
-          named_barrier(quad_bar, 32 * NSUB);  // red_l may be rewritten only after every slice read it
-        }
+        if (pend_i >= 0 && !check(pend_i, pend_last, pend_seg, pend_ref)) failed = true;
+        pend_i = i;
+        pend_last = last;
+        pend_seg = worker + rc.b;
+        pend_ref = m_ref;
       }
+      if (!failed && pend_i >= 0) (void)check(pend_i, pend_last, pend_seg, pend_ref);
     } else {
-      // ---------------------------------------------------------- senders
-      const bool leader = (q4 == 2 * (int)peer) && sub == 0 && lane == 0;
-      constexpr int NSEND = 64 * NSUB;                   // sender threads
-      const int sid = (sub * 2 + (q4 & 1)) * 32 + lane;  // 0..NSEND-1
+      // ---------------------------------------------------------- PT warps
+      const bool leader = q4 == 0 && lane == 0;
+      constexpr int NSEND = 128;                       // PT threads
+      const int sid = q4 * 32 + lane;                  // 0..NSEND-1
       const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer);
       const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0]), peer);
+      const int tok0 = HALF_T * (int)peer;             // the peer's token half
       // quantized formats: page j's staged codes -> bf16 operand stage j % KV_ST
       // (rows at or past nvalid are written as zeros), then release both
       auto dequant = [&](int j, int nvalid) -> bool {
@@ -749,37 +807,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         rn.init(prefix, seq_c, row0);
         if (!dequant(0, min(TILE, rn.n - TILE * (x0 - rn.start)))) failed = true;
       }
-      // page i of this worker, one page behind the shipping of partials: the
-      // peer's P rows and messages have arrived -> rescale these heads' O rows,
-      // release the P.V, and at a segment end write these rows' output
-      auto finish = [&](int i, bool last, int seg) -> bool {
-        const int sb = i & 1;
-        bool ok = wait_bar<true>(S, &S.pin_full[sb], (uint32_t)(i >> 1) & 1u, a.err, 20);
-        __syncwarp();
-        const float2 mg = S.msg[sb][hl];
-        const bool need = mg.x != 1.f;
-        if (__any_sync(0xffffffffu, need)) {
-          if (!wait_bar<false>(S, &S.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, a.err, 21)) ok = false;
-          __syncwarp();
-          fence_after_sync();
-          scale_o(mg.x);
-        }
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.p_full[sb]);
-        if (last) {
-          if (!wait_bar<false>(S, &S.pv_done[sb], (uint32_t)(i >> 1) & 1u, a.err, 22)) ok = false;
-          __syncwarp();
-          fence_after_sync();
-          store_o(seg, mg.y);
-          fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.o_free);
-        }
-        return ok;
-      };
-      int pend_i = -1, pend_seg = 0;
-      bool pend_last = false;
       for (int x = x0, i = 0; x < x1; ++x, ++i) {
         rc.advance(prefix, seq_c, x);
         const bool last = (x + 1 == x1) || (x + 1 == rc.end);
@@ -787,21 +814,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int st = i % KV_ST, sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
-        if (leader) mbar_arrive_expect_tx(&S.pin_full[sb], PIN_BYTES);  // the peer's P rows for this page
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) failed = true;
         __syncwarp();
         fence_after_sync();
-        uint32_t v[TPW];
-        tmem_ld_cols<TPW>(t_row + TM_S + TILE * sb + TPW * sub, v);
+        uint32_t v[HALF_T];
+        tmem_ld32(t_row + TM_S + TILE * sb + tok0, v);
         tmem_ld_wait();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
-        if (last && x + 1 < x1) {
-          RowCursor nx = rc;
-          nx.advance(prefix, seq_c, x + 1);
-          load_query(nx.b);
-        }
         if (!kQuant && nvalid < TILE) {
           // page past the end of its sequence: zero the unused value rows so that
           // P = 0 never meets stale (possibly non-finite) cache contents
@@ -813,20 +834,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           fence_proxy_async_smem();
         }
-        uint32_t h[TPW / 2];
+        uint32_t h[HALF_T / 2];
 #pragma unroll
-        for (int k = 0; k < TPW / 2; ++k)
+        for (int k = 0; k < HALF_T / 2; ++k)
           h[k] = f2_to_h2(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c));
         // the peer has consumed what we sent into this buffer two pages ago
+        // (so the copy that read xout[sb] then has completed too)
         if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
         __syncwarp();
-        // (the copy that read xout[sb] two pages ago has completed: its bytes were consumed)
 #pragma unroll
-        for (int k = 0; k < TPW / 8; ++k)
-          *reinterpret_cast<uint4*>(S.xout[sb] + xoff(hl, (TPW / 8) * sub + k)) =
+        for (int k = 0; k < HALF_T / 8; ++k)
+          *reinterpret_cast<uint4*>(S.xout[sb] + sw64(row, k)) =
               make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         fence_proxy_async_smem();
-        if (!named_barrier_and(SENDER_BAR, NSEND, !failed)) break;  // all senders leave together
+        if (!named_barrier_and(SENDER_BAR, NSEND, !failed)) break;  // the PT warps leave together
         if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, S.xout[sb], X_BYTES, peer_xfull + 8u * sb);
         if constexpr (kQuant) {
           // the next page's operands, ahead of its S (its stage was last read by page i+1-KV_ST's P.V)
@@ -835,12 +856,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!dequant(i + 1, min(TILE, rn.n - TILE * (x + 1 - rn.start)))) failed = true;
           }
         }
-        if (pend_i >= 0 && !finish(pend_i, pend_last, pend_seg)) failed = true;
-        pend_i = i;
-        pend_last = last;
-        pend_seg = worker + rc.b;
       }
-      if (!failed && pend_i >= 0) (void)finish(pend_i, pend_last, pend_seg);
     }
   }
 

@@ -257,6 +257,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_BOUNDS: return "page id or sequence length out of bounds";
     case MLA_ERR_TIMEOUT: return "bounded device wait timed out";
     case MLA_ERR_WORKSPACE: return "workspace too small";
+    case MLA_ERR_RANGE: return "score range beyond the kernel's reference tracking (weights capped)";
     default: return "unknown status";
   }
 }
