@@ -354,6 +354,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const int j = x - rc.start;
+      if (x + 1 == rc.end && rc.end < x1 && lane == 0 && rank == 0) {
+        // last page of a row whose segment is not this worker's last: the
+        // softmax warps load the next row's query in a few pages; warm L2 again
+        RowCursor nx = rc;
+        nx.advance(prefix, seq_c, rc.end);
+        prefetch_l2_bulk(a.q_cat + (size_t)nx.b * 128 * DK, 128 * DK * 2);
+      }
       if (rc.b != page_row || j - jbase >= 32) {
         if (rc.b != page_row && rc.end < x1) {
           // entering a row whose segment is not this worker's last: warm L2
@@ -537,7 +544,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       tmem_st_wait();
     };
-    // the same columns times inv -> the segment's partial output (this CTA's latent half)
+    // the same columns times inv -> the segment's partial output (this CTA's
+    // latent half), 32 bytes per store (a whole sector per lane)
     auto store_o = [&](int seg, float inv) {
       float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms;
 #pragma unroll 1
@@ -546,9 +554,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_ld32(t_row + TM_O + 128 * ms + 32 * k32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          reinterpret_cast<float4*>(dst + 32 * k32)[k] = make_float4(
-              u2f(o[4 * k]) * inv, u2f(o[4 * k + 1]) * inv, u2f(o[4 * k + 2]) * inv, u2f(o[4 * k + 3]) * inv);
+        for (int k = 0; k < 4; ++k)
+          st_global_v8(dst + 32 * k32 + 8 * k, u2f(o[8 * k]) * inv, u2f(o[8 * k + 1]) * inv, u2f(o[8 * k + 2]) * inv,
+                       u2f(o[8 * k + 3]) * inv, u2f(o[8 * k + 4]) * inv, u2f(o[8 * k + 5]) * inv,
+                       u2f(o[8 * k + 6]) * inv, u2f(o[8 * k + 7]) * inv);
       }
     };
 
@@ -658,11 +667,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
-        if (last && x + 1 < x1) {
-          RowCursor nx = rc;
-          nx.advance(prefix, seq_c, x + 1);
-          load_query(nx.b);
-        }
 
         // ---- add the peer's partial (fp16, log2 units) of my tokens
         if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
@@ -741,6 +745,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (leader) {
           bulk_s2peer(peer_p + (sb * 2 + rank) * PH_BYTES, pm, PH_BYTES, peer_pin + 8u * sb);
           bulk_s2peer(peer_msg + sb * MSG_BYTES, &S.msg_out[sb][0], MSG_BYTES, peer_pin + 8u * sb);
+        }
+        // the next page starts a new segment: every S of this one has completed
+        // (this thread waited for each), so the next query may replace this one
+        if (last && x + 1 < x1) {
+          RowCursor nx = rc;
+          nx.advance(prefix, seq_c, x + 1);
+          load_query(nx.b);
         }
         if (pend_i >= 0 && !check(pend_i, pend_last, pend_seg, pend_ref)) failed = true;
         pend_i = i;

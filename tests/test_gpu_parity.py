@@ -289,6 +289,28 @@ def test_decode_bad_page_id_reports_bounds():
     assert st == mla.MLA_ERR_BOUNDS and info == prob.num_pages + 100
 
 
+def test_decode_score_beyond_tracked_range_is_reported():
+    """H=128: a token of the second page whose RoPE key is 200 x one head's
+    q_pe raises that head's score far more than 100 (log2 units) above the
+    first page's maximum; the kernel reports MLA_ERR_RANGE (weights capped)
+    and the output stays finite.  The row is long enough (304 pages) that the
+    first worker's range holds several pages, so page 1 is not the first page
+    of its split."""
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(128, [64 * 304], seed=6, paged=False)
+    dev = DeviceDecode(prob)
+    qpe0 = synth.bf16_bits_to_f32(prob.q_pe)[0, 0]  # [64] of head 0
+    big = torch.from_numpy(synth.f32_to_bf16_bits(200.0 * qpe0).view(np.uint8).copy())
+    phys = int(dev.page_table[0, 1])
+    off = phys * dev.page_bytes + 0 * 1152 + 1024  # token 64 (slot 0 of page 1): its k_pe
+    dev.pool[off:off + 128] = big.to(dev.pool.device)
+    dev.decode()
+    torch.cuda.synchronize()
+    st, _ = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_RANGE
+    assert bool(torch.all(torch.isfinite(dev.out.float())))
+
+
 def test_decode_seqlen_over_capacity_reports_bounds():
     import mla_absorbed_latent_gb300 as mla
     prob = make_problem(16, [100], seed=4)
