@@ -92,7 +92,8 @@ constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM
 // Per cache format: bf16 pages are TMA-copied straight into the MMA operand
 // stages (4 of them).  Quantized pages land in a small staging ring of codes
 // and scales; the sender warps dequantize each into a bf16 operand stage (3 of
-// them, 2: shared memory holds no more next to the staging ring).  Offsets are
+// them, and a single staging tile for the shipped partial scores: shared
+// memory holds no more next to the staging ring).  Offsets are
 // bytes inside one staging slot (this CTA's half of a page, unswizzled rows):
 //   INT8: c codes i8 [64][256] | k_pe codes i8 [64][32] | c scales bf16 [64][8]
 //         | k_pe scales bf16 [64][8] (all 8 groups of the token)
@@ -104,12 +105,12 @@ template <> struct FmtTraits<MLA_FMT_BF16> {
   static constexpr uint32_t CODE_BYTES = 0, C_OFF = 0, PE_OFF = 0, CS_OFF = 0, ZS_OFF = 0, PS_OFF = 0;
 };
 template <> struct FmtTraits<MLA_FMT_INT8> {
-  static constexpr int KV_ST = 2, CODE_ST = 3;
+  static constexpr int KV_ST = 3, CODE_ST = 2;
   static constexpr uint32_t C_OFF = 0, PE_OFF = 16384, CS_OFF = 18432, ZS_OFF = 0, PS_OFF = 19456;
   static constexpr uint32_t CODE_BYTES = 20480;
 };
 template <> struct FmtTraits<MLA_FMT_INT4> {
-  static constexpr int KV_ST = 2, CODE_ST = 4;
+  static constexpr int KV_ST = 3, CODE_ST = 3;
   static constexpr uint32_t C_OFF = 0, PE_OFF = 8192, CS_OFF = 10240, ZS_OFF = 11264, PS_OFF = 12288;
   static constexpr uint32_t CODE_BYTES = 13312;
 };
@@ -122,7 +123,8 @@ struct __align__(1024) SmemTC {
   uint8_t kv[KV_ST][KV_BYTES];
   uint8_t p[2][2][PH_BYTES];  // P per page parity and token half ([128 heads][32 tokens], 64B-swizzled)
   uint8_t xin[2][X_BYTES];    // the peer's fp16 partials of our token half, rows 64 B, chunks swizzled
-  uint8_t xout[2][X_BYTES];   // ours of the peer's token half, same layout, shipped by one bulk copy
+  static constexpr int XOUT_N = FMT == MLA_FMT_BF16 ? 2 : 1;
+  uint8_t xout[XOUT_N][X_BYTES];  // ours of the peer's token half, same layout, shipped by one bulk copy
   uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
   uint8_t qpe[QPE_BYTES];
   float2 msg_in[2][128];   // from the peer per page and head: its two slices' maxima (sums at a segment end)
@@ -813,10 +815,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         return ok;
       };
-      RowCursor rn;  // row of the next page, for its dequantization
+      RowCursor rn;  // row of the page being dequantized
       if constexpr (kQuant) {
+        // two pages ahead of the S MMAs: pages 0 and 1 now, page i+2 at page i
         rn.init(prefix, seq_c, row0);
-        if (!dequant(0, min(TILE, rn.n - TILE * (x0 - rn.start)))) failed = true;
+        for (int x = x0; x < min(x0 + 2, x1) && !failed; ++x) {
+          rn.advance(prefix, seq_c, x);
+          if (!dequant(x - x0, min(TILE, rn.n - TILE * (x - rn.start)))) failed = true;
+        }
       }
       for (int x = x0, i = 0; x < x1; ++x, ++i) {
         rc.advance(prefix, seq_c, x);
@@ -849,22 +855,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < HALF_T / 2; ++k)
           h[k] = f2_to_h2(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c));
-        // the peer has consumed what we sent into this buffer two pages ago
-        // (so the copy that read xout[sb] then has completed too)
+        // the peer has consumed what we sent into its buffer two pages ago (so
+        // the copy that read xout[sb] then has completed too); with a single
+        // staging tile, also last page's
         if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
+        if (Smem::XOUT_N == 1 && i > 0 &&
+            !wait_bar<true>(S, &S.x_empty[sb ^ 1], (uint32_t)((i - 1) >> 1) & 1u, a.err, 17))
+          failed = true;
         __syncwarp();
+        uint8_t* xo = S.xout[sb % Smem::XOUT_N];
 #pragma unroll
         for (int k = 0; k < HALF_T / 8; ++k)
-          *reinterpret_cast<uint4*>(S.xout[sb] + sw64(row, k)) =
-              make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+          *reinterpret_cast<uint4*>(xo + sw64(row, k)) = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         fence_proxy_async_smem();
         if (!named_barrier_and(SENDER_BAR, NSEND, !failed)) break;  // the PT warps leave together
-        if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, S.xout[sb], X_BYTES, peer_xfull + 8u * sb);
+        if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, xo, X_BYTES, peer_xfull + 8u * sb);
         if constexpr (kQuant) {
-          // the next page's operands, ahead of its S (its stage was last read by page i+1-KV_ST's P.V)
-          if (x + 1 < x1) {
-            rn.advance(prefix, seq_c, x + 1);
-            if (!dequant(i + 1, min(TILE, rn.n - TILE * (x + 1 - rn.start)))) failed = true;
+          // page i+2's operands (its stage was last read by page i+2-KV_ST's P.V)
+          if (x + 2 < x1) {
+            rn.advance(prefix, seq_c, x + 2);
+            if (!dequant(i + 2, min(TILE, rn.n - TILE * (x + 2 - rn.start)))) failed = true;
           }
         }
       }
