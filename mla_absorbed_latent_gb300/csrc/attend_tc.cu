@@ -13,24 +13,34 @@
 // The pair splits the latent width: CTA r owns latent dims [256r, 256r+256)
 // and RoPE dims [32r, 32r+32), TMA-loads only that half of every 64-token page
 // (HBM bytes are not duplicated), and accumulates its O half (128 x 256 fp32,
-// TMEM) += P . V_half.  The score of a head needs both halves, so the pair also
-// splits the softmax by head: CTA r runs the softmax of heads [64r, 64r+64).
-// Per page each CTA
-//  * computes its partial S (M=128, N=64, K=288) into TMEM, with its half of
-//    q_lat in TMEM and its half of q_pe in shared memory as A operands;
-//  * sends the peer the partial scores of the peer's 64 heads, already in log2
+// TMEM) += P . V_half.  A score needs both halves of the width, so the pair
+// splits the softmax by token: CTA r runs the softmax of all 128 heads over
+// tokens [32r, 32r+32) of every page ("my" tokens).  Per page each CTA
+//  * computes its partial S (M=128 heads, N=64 tokens, K=288) into TMEM, with
+//    its half of q_lat in TMEM and its half of q_pe in shared memory as A
+//    operands;
+//  * sends the peer the partial scores of the peer's 32 tokens, already in log2
 //    units, as fp16 (8 KB: written to a local staging tile, then one bulk
 //    shared-to-peer copy counted on the peer's transaction barrier);
-//  * adds the peer's partial to its own for its 64 heads, runs the online
-//    softmax there and writes P (bf16) for those heads into its own P tile,
-//    then copies those 64 rows (8 KB) into the peer's P tile, with each head's
-//    O rescale factor and, at a segment end, 1/l;
-//  * once both halves of P are in place, issues O_half += P . V_half.
+//  * adds the peer's partial to its own for my tokens, forms P = 2^(s - m_ref)
+//    in bf16 for those 32 columns of its P tile and copies them (8 KB) with a
+//    per-head message (slice maxima, or slice sums at a segment end, 1 KB) into
+//    the peer's P tile;
+//  * once both token halves of P are in place, issues O_half += P . V_half.
 // Distributed shared memory moves ~14.5 bytes per cycle per SM each way, less
-// than the ~23 bytes per cycle per SM that HBM delivers, so the 16.5 KB per page
+// than the ~23 bytes per cycle per SM that HBM delivers, so the 17 KB per page
 // each way (against 36 KB of cache streamed) is the design's budget: fp32
-// partials for all 128 heads (32 KB) would cap the kernel well below the HBM
-// roofline.
+// partials (32 KB) would cap the kernel well below the HBM roofline.
+//
+// The reference maximum.  Both CTAs must write P in the same reference m_ref
+// (their halves feed one accumulator).  At a segment's first page the pair
+// swaps its slice maxima and both take the exact maximum.  Later pages use the
+// running reference; one page later, when the peer's message has arrived, both
+// CTAs see the same four slice maxima and move the reference only when it grew
+// by more than 2^8: O and the next page's P (already written in the old
+// reference) are then rescaled by the same factor on both sides.  A score more
+// than 2^100 above its reference is capped there and reported as
+// MLA_ERR_RANGE (the result stays finite; it is no longer exact).
 //
 // MMA issue.  A tcgen05.mma blocks its issuing thread while an MMA on the same
 // accumulator is in flight, so three threads issue MMAs: S of even pages, S of
@@ -38,20 +48,15 @@
 // signalled to both CTAs (multicast commit): a P tile is rewritten only once
 // both CTAs' P.V have read it.
 //
-// Warp roles (640 threads): warps 0..3 are the TMA producer, the P.V issuer
-// and the two S issuers (even / odd pages), assigned per rank so that the S
-// issuers share sub-partitions with the light sender warps; warp 1 owns TMEM;
-// warps 4..19 run the softmax.  TMEM lane quadrant q = warp % 4 holds heads
-// 32q..32q+31; NSUB = 4 warps share each quadrant and split a page's 64 tokens
-// into slices of 16 (more warps per sub-partition hide the latency of the
-// per-page chain).  The eight warps on this CTA's own heads ("owners") run the
-// softmax, combining row maxima and sums across the slices through shared
-// memory.  The eight warps on the peer's heads ("senders") ship those heads'
-// partial scores, and one page later apply the peer's rescale factors to the O
-// rows of those heads and release the P.V; for quantized pools they also
-// dequantize the next page.  Every wait is bounded; a timeout records
-// MLA_ERR_TIMEOUT, raises the abort flag of both CTAs, lets in-flight copies
-// and MMAs land, frees TMEM and returns.
+// Warp roles (512 threads): warps 0..3 are the TMA producer, the P.V issuer
+// and the two S issuers (even / odd pages), assigned per rank; warp 1 owns
+// TMEM.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31 and is served
+// by three softmax warps: two "MT" warps own 16 of my tokens each (and 128
+// columns each of O and of the query), one "PT" warp ships the partial scores
+// of the peer's tokens and, for quantized pools, dequantizes the page two
+// ahead.  Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, raises the
+// abort flag of both CTAs, lets in-flight copies and MMAs land, frees TMEM and
+// returns.
 //
 // Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
 // buffer [384,512).
@@ -328,10 +333,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
   const int ntiles = x1 - x0;
 
-  // Roles of warps 0..3 rotate with the rank so that the two S issuers run on
-  // the SM sub-partitions of the sender warps (warp w runs on sub-partition
-  // w % 4, the one that can reach TMEM lanes 32(w%4)..+31): role 0 producer,
-  // 1 P.V issuer, 2 / 3 S issuers of even / odd pages.
+  // Roles of warps 0..3 (warp w runs on SM sub-partition w % 4; the pair's two
+  // CTAs place them differently): role 0 producer, 1 P.V issuer, 2 / 3 S
+  // issuers of even / odd pages.
   const int role = warp < 4 ? (warp ^ (int)(2 * rank)) : -1;
   if (ntiles > 0 && role == 0) {
     // ------------------------------------------------------------ TMA producer
