@@ -60,6 +60,7 @@
 //
 // Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
 // buffer [384,512).
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -88,6 +89,8 @@ constexpr uint32_t PIN_BYTES = PH_BYTES + MSG_BYTES;          // the peer's P ha
 constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
+constexpr int Q_AHEAD = 8;
+constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 heads][64 dims] 128B-swizzled  // pages before a row's end at which the producer prefetches the next query
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
 constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p tolerated (O and l stay finite in fp32)
@@ -126,19 +129,20 @@ struct __align__(1024) SmemTC {
   static constexpr int CODE_ST = FmtTraits<FMT>::CODE_ST > 0 ? FmtTraits<FMT>::CODE_ST : 1;
   static constexpr uint32_t CODE_BYTES = FmtTraits<FMT>::CODE_BYTES > 0 ? FmtTraits<FMT>::CODE_BYTES : 128;
   uint8_t kv[KV_ST][KV_BYTES];
+  uint8_t qpe[QPE_BYTES];     // 64B-swizzled MMA operand: 1 KB aligned (follows 1 KB multiples)
   uint8_t p[2][2][PH_BYTES];  // P per page parity and token half ([128 heads][32 tokens], 64B-swizzled)
   uint8_t xin[2][X_BYTES];    // the peer's fp16 partials of our token half, rows 64 B, chunks swizzled
   static constexpr int XOUT_N = FMT == MLA_FMT_BF16 ? 2 : 1;
   uint8_t xout[XOUT_N][X_BYTES];  // ours of the peer's token half, same layout, shipped by one bulk copy
   uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
-  uint8_t qpe[QPE_BYTES];
   float2 msg_in[2][128];   // from the peer per page and head: its two slices' maxima (sums at a segment end)
   float2 msg_out[2][128];  // ours, shipped with our P half
   float2 mx_in[2][128];    // first page of a segment: the peer's two slices' maxima, exchanged before P
   float2 mx_out[2][128];
   uint64_t kv_full[KV_ST], kv_empty[KV_ST];
   uint64_t code_full[CODE_ST], code_empty[CODE_ST];
-  uint64_t q_ready;         // q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
+  uint64_t q_ready;         // quantized: q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
+  uint64_t q_done, qpe_full;  // bf16: the segment's q_lat half copied into TMEM / its q_pe half into qpe
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2], pv_both[2];
   uint64_t x_full[2], x_empty[2], pin_full[2], mx_full[2];
@@ -149,7 +153,11 @@ struct __align__(1024) SmemTC {
 static_assert(sizeof(SmemTC<MLA_FMT_BF16>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT8>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT4>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
-static_assert(KV_BYTES % 1024 == 0 && PH_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(KV_BYTES % 1024 == 0 && PH_BYTES % 1024 == 0 && QPE_BYTES % 1024 == 0,
+              "swizzled tiles need 1 KB alignment");
+static_assert(offsetof(SmemTC<MLA_FMT_BF16>, qpe) % 1024 == 0 && offsetof(SmemTC<MLA_FMT_BF16>, p) % 1024 == 0 &&
+                  offsetof(SmemTC<MLA_FMT_INT8>, qpe) % 1024 == 0 && offsetof(SmemTC<MLA_FMT_INT4>, qpe) % 1024 == 0,
+              "swizzled operand tiles start on 1 KB boundaries");
 
 struct TcArgs {
   const uint16_t* q_cat;  // [B][128][576] bf16
@@ -268,9 +276,19 @@ __device__ __forceinline__ uint4 deq_u4x8(uint32_t w, float s, float z) {
 }
 
 // The cache tensor maps: bf16 pages use m0 (latent, 128B-swizzled boxes of 64
-// dims) and m1 (RoPE key, 64B-swizzled boxes of 32); quantized pages use m0
-// (c codes), m1 (k_pe codes), m2 (c scales), m3 (INT4: c zeros, INT8: k_pe
-// scales), m4 (INT4: k_pe scales).
+// dims) and m1 (RoPE key, 64B-swizzled boxes of 32), and the query maps m2
+// (q_lat: 128B-swizzled boxes of 64 dims x 128 heads) and m3 (q_pe:
+// 64B-swizzled boxes of 32 dims x 64 heads); quantized pages use m0 (c codes),
+// m1 (k_pe codes), m2 (c scales), m3 (INT4: c zeros, INT8: k_pe scales), m4
+// (INT4: k_pe scales), and tm_q_pe (q_pe: 32 dims x 128 heads).
+//
+// Operand ring (bf16).  The producer streams ring "uses" in order: at the start
+// of every segment two uses carry the segment's query (each: 128 heads x 128
+// latent dims of this CTA's half, two 128B-swizzled tiles, plus 64 heads of its
+// q_pe half), then one use per page.  Page i of segment k (both counted from 0
+// within the worker) is use i + 2(k+1).  The S issuer of a segment's first page
+// copies the query into TMEM (tcgen05.cp) and q_pe into qpe, then releases the
+// two uses; no thread-issued global load is on the path of a segment change.
 template <int FMT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tm_m0, const __grid_constant__ CUtensorMap tm_m1,
@@ -297,6 +315,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&S.code_empty[s], 4);
     }
     mbar_init(&S.q_ready, 9);  // the 8 MT warps' q_lat + the q_pe copy
+    mbar_init(&S.q_done, 1);
+    mbar_init(&S.qpe_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
       mbar_init(&S.s_free[s], 12);  // every softmax warp
@@ -346,35 +366,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       prefetch_tmap(&tm_m0);
       prefetch_tmap(&tm_m1);
       if (kQuant) {
-        prefetch_tmap(&tm_m2);
-        prefetch_tmap(&tm_m3);
         if (FMT == MLA_FMT_INT4) prefetch_tmap(&tm_m4);
       }
+      prefetch_tmap(&tm_m2);
+      prefetch_tmap(&tm_m3);
     }
     const uint64_t pol = policy_evict_first();
     constexpr int RING = kQuant ? CODE_ST : KV_ST;  // slots the copies land in
-    int issued = 0;  // pages whose copies were started (page k used slot k % RING)
+    int issued = 0;  // ring uses whose copies were started (use k went to slot k % RING)
     RowCursor rc;
     rc.init(prefix, seq_c, row0);
-    int page_row = -1, jbase = 0, page_reg = 0;
+    int page_row = -1, jbase = 0, page_reg = 0, seg = -1;
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const int j = x - rc.start;
-      if (x + 1 == rc.end && rc.end < x1 && lane == 0 && rank == 0) {
-        // last page of a row whose segment is not this worker's last: the
-        // softmax warps load the next row's query in a few pages; warm L2 again
+      if (x == x0 || x == rc.start) ++seg;
+      if (x == max(max(x0, rc.start), rc.end - Q_AHEAD) && rc.end < x1 && lane == 0) {
+        // a few pages (this warp runs up to KV_ST pages ahead of the softmax)
+        // before the end of a row whose segment is not this worker's last:
+        // the next row's query is loaded at the row change; bring it into L2
+        // with a high retention priority (each CTA of the pair half of it)
         RowCursor nx = rc;
         nx.advance(prefix, seq_c, rc.end);
-        prefetch_l2_bulk(a.q_cat + (size_t)nx.b * 128 * DK, 128 * DK * 2);
+        prefetch_l2_bulk_hint(a.q_cat + ((size_t)nx.b * 128 + 64 * rank) * DK, 64 * DK * 2, policy_evict_last());
       }
       if (rc.b != page_row || j - jbase >= 32) {
         if (rc.b != page_row && rc.end < x1) {
           // entering a row whose segment is not this worker's last: warm L2
-          // with the next row's query and page-table entries, which the
-          // softmax warps and this warp need at the next segment change
+          // with the next row's page-table entries, which this warp needs at
+          // the next segment change
           RowCursor nx = rc;
           nx.advance(prefix, seq_c, rc.end);
-          if (lane == 0 && rank == 0) prefetch_l2_bulk(a.q_cat + (size_t)nx.b * 128 * DK, 128 * DK * 2);
           const int32_t* pt = a.page_table + (size_t)nx.b * a.max_pages;
           const int nt = nx.end - nx.start;
           for (int k = 32 * lane; k < nt; k += 32 * 32) prefetch_l2_line(pt + k);
@@ -385,9 +407,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       int page = __shfl_sync(0xffffffffu, page_reg, j - jbase);
       int ok = 1;
-      if (lane == 0) {
-        const int st = i % RING, u = i / RING;
-        ok = wait_bar<false>(S, kQuant ? &S.code_empty[st] : &S.kv_empty[st], (u & 1) ^ 1, a.err, 2);
+      if constexpr (!kQuant) {
+        if (lane == 0 && (x == x0 || x == rc.start)) {
+          // the segment's query: two ring uses (q_lat dims [128h, 128h+128) of
+          // this CTA's half and q_pe heads [64h, 64h+64) in use h)
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int u = i + 2 * seg + h, st = u % KV_ST;
+            ok = wait_bar<false>(S, &S.kv_empty[st], ((u / KV_ST) & 1) ^ 1, a.err, 1);
+            if (ok) {
+              mbar_arrive_expect_tx(&S.kv_full[st], 2 * QT_BYTES + QPE_BYTES / 2);
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(S.kv[st] + c * QT_BYTES, &tm_m2, HALF_C * rank + 128 * h + 64 * c, 0, rc.b, &S.kv_full[st]);
+              tma_load_3d(S.kv[st] + 2 * QT_BYTES, &tm_m3, DC + PE_HALF * rank, 64 * h, rc.b, &S.kv_full[st]);
+              ++issued;
+            }
+          }
+        }
+      }
+      if (lane == 0 && ok) {
+        const int u = kQuant ? i : i + 2 * (seg + 1);  // ring use of this page
+        const int st = u % RING;
+        ok = wait_bar<false>(S, kQuant ? &S.code_empty[st] : &S.kv_empty[st], ((u / RING) & 1) ^ 1, a.err, 2);
         if (ok) {
           if (page < 0 || page >= a.num_pages) {
             raise_error(a.err, MLA_ERR_BOUNDS, page);
@@ -430,17 +470,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int parity = role - 2;
     const uint32_t idesc_s = idesc_bf16_f32(128, TILE, false, false);
     const uint64_t qpe_desc = smem_desc(smem_u32(S.qpe), 16, 512, SWIZZLE_64B);
-    int q_seen = 0;
+    int q_seen = 0;     // segments counted so far (the current one included)
+    int q_have = 0;     // bf16: segments whose query this issuer has seen installed
     RowCursor rc;
     rc.init(prefix, seq_c, row0);
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
-      if (x == x0 || x == rc.start) ++q_seen;  // every issuer counts every segment
+      const bool first = (x == x0) || (x == rc.start);
+      if (first) ++q_seen;  // every issuer counts every segment
       if ((i & 1) != parity) continue;
-      const int st = i % KV_ST, sb = i & 1;
-      // the query of this page's segment is in place (TMEM half + smem q_pe)
-      if (!wait_bar<false>(S, &S.q_ready, (q_seen - 1) & 1, a.err, 3)) break;
-      if (!wait_bar<false>(S, &S.kv_full[st], (i / KV_ST) & 1, a.err, 4)) break;
+      const int seg = q_seen - 1;
+      const int u = kQuant ? i : i + 2 * (seg + 1);  // ring use of this page
+      const int st = u % KV_ST, sb = i & 1;
+      if constexpr (kQuant) {
+        // the query of this page's segment is in place (TMEM half + smem q_pe)
+        if (!wait_bar<false>(S, &S.q_ready, (uint32_t)seg & 1u, a.err, 3)) break;
+      } else {
+        if (first) {
+          // install the segment's query: its two ring uses have landed, and the
+          // previous segment's scores (the last reads of the old query) are done
+          const int ua = u - 2, ub = u - 1;
+          if (!wait_bar<false>(S, &S.kv_full[ua % KV_ST], (uint32_t)(ua / KV_ST) & 1u, a.err, 25)) break;
+          if (!wait_bar<false>(S, &S.kv_full[ub % KV_ST], (uint32_t)(ub / KV_ST) & 1u, a.err, 26)) break;
+          if (!wait_bar<false>(S, &S.s_free[sb], ((i >> 1) & 1) ^ 1, a.err, 5)) break;
+          if (i > 0 && !wait_bar<false>(S, &S.s_full[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u, a.err, 27)) break;
+          fence_after_sync();
+          mbar_arrive_expect_tx(&S.qpe_full, QPE_BYTES);
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t qa = smem_u32(S.kv[(u - 2 + h) % KV_ST]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // 16 dims per copy: TMEM columns of dims (2n, 2n+1)
+                tmem_cp_128x256b(tmem + TM_Q + 64 * h + 32 * c + 8 * kk,
+                                 smem_desc(qa + c * QT_BYTES + kk * 32, 16, 1024, SWIZZLE_128B));
+            bulk_s2peer(mapa(smem_u32(S.qpe + h * (QPE_BYTES / 2)), rank), S.kv[(u - 2 + h) % KV_ST] + 2 * QT_BYTES,
+                        QPE_BYTES / 2, mapa(smem_u32(&S.qpe_full), rank));
+          }
+          mma_commit(&S.q_done);
+        }
+        if (q_have < q_seen) {
+          // the segment's query is in TMEM and smem (copied by whichever issuer
+          // had its first page); that issuer then hands the two uses back
+          if (!wait_bar<false>(S, &S.q_done, (uint32_t)seg & 1u, a.err, 28)) break;
+          if (!wait_bar<false>(S, &S.qpe_full, (uint32_t)seg & 1u, a.err, 29)) break;
+          q_have = q_seen;
+          if (first) {
+            mbar_arrive(&S.kv_empty[(u - 2) % KV_ST]);
+            mbar_arrive(&S.kv_empty[(u - 1) % KV_ST]);
+          }
+        }
+      }
+      if (!wait_bar<false>(S, &S.kv_full[st], (uint32_t)(u / KV_ST) & 1u, a.err, 4)) break;
       if (!wait_bar<false>(S, &S.s_free[sb], ((i >> 1) & 1) ^ 1, a.err, 5)) break;
       fence_after_sync();
       const uint32_t kv_addr = smem_u32(S.kv[st]);
@@ -469,7 +551,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int x = x0, i = 0; x < x1; ++x, ++i) {
       rc.advance(prefix, seq_c, x);
       const bool first = (x == x0) || (x == rc.start);
-      const int st = i % KV_ST, pb = i & 1;
+      const int st = (kQuant ? i : i + 2 * (segments + (first ? 1 : 0))) % KV_ST, pb = i & 1;  // ring use of page i
       if (!wait_bar<false>(S, &S.p_full[pb], (i >> 1) & 1, a.err, 6)) break;
       // the first page of a segment overwrites O: wait for the previous
       // segment's epilogue to have read it
@@ -509,16 +591,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto load_query = [&](int b) {
       const uint16_t* qrow = a.q_cat + ((size_t)b * 128 + row) * DK;
       const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 2 * QCOLS * sub);
+      // every global read is issued before the first TMEM store (one round trip)
+      uint32_t v[QCOLS];
 #pragma unroll
-      for (int k32 = 0; k32 < QCOLS / 32; ++k32) {
-        uint32_t v[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 u = qc[8 * k32 + k];
-          v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
-        }
-        tmem_st32(t_row + TM_Q + QCOLS * sub + 32 * k32, v);
+      for (int k = 0; k < QCOLS / 4; ++k) {
+        const uint4 u = qc[k];
+        v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
       }
+#pragma unroll
+      for (int k32 = 0; k32 < QCOLS / 32; ++k32) tmem_st32(t_row + TM_Q + QCOLS * sub + 32 * k32, v + 32 * k32);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
@@ -539,14 +620,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // O row of this lane, MT slice ms's 128 columns, times f
     auto scale_o = [&](float f) {
 #pragma unroll 1
-      for (int k32 = 0; k32 < 4; ++k32) {
-        uint32_t o[32];
-        const uint32_t col = t_row + TM_O + 128 * ms + 32 * k32;
-        tmem_ld32(col, o);
+      for (int k16 = 0; k16 < 8; ++k16) {
+        uint32_t o[16];
+        const uint32_t col = t_row + TM_O + 128 * ms + 16 * k16;
+        tmem_ld16(col, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) o[k] = f2u(u2f(o[k]) * f);
-        tmem_st32(col, o);
+        for (int k = 0; k < 16; ++k) o[k] = f2u(u2f(o[k]) * f);
+        tmem_st16(col, o);
       }
       tmem_st_wait();
     };
@@ -568,7 +649,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
 
     bool failed = false;
-    if (mt) load_query(rc.b);
+    if (kQuant && mt) load_query(rc.b);  // bf16: the S issuers install each segment's query
     if (mt) {
       // ---------------------------------------------------------- MT warps
       const bool leader = q4 == 0 && ms == 0 && lane == 0;
@@ -754,7 +835,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         // the next page starts a new segment: every S of this one has completed
         // (this thread waited for each), so the next query may replace this one
-        if (last && x + 1 < x1) {
+        if (kQuant && last && x + 1 < x1) {
           RowCursor nx = rc;
           nx.advance(prefix, seq_c, x + 1);
           load_query(nx.b);
@@ -828,11 +909,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!dequant(x - x0, min(TILE, rn.n - TILE * (x - rn.start)))) failed = true;
         }
       }
+      int pseg = -1;  // segment of the page (bf16: two ring uses of query each)
       for (int x = x0, i = 0; x < x1; ++x, ++i) {
         rc.advance(prefix, seq_c, x);
-        const bool last = (x + 1 == x1) || (x + 1 == rc.end);
+        if (x == x0 || x == rc.start) ++pseg;
         const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
-        const int st = i % KV_ST, sb = i & 1;
+        const int st = (kQuant ? i : i + 2 * (pseg + 1)) % KV_ST, sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) failed = true;
@@ -957,8 +1039,10 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   bool ok = encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
   if (fmt == MLA_FMT_BF16) {
     ok = ok && encode_3d(&m[0], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_3d(&m[1], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B);
-    m[2] = m[3] = m[4] = m[0];
+         encode_3d(&m[1], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         encode_3d(&m[2], q_cat, DK, 128, B, row, row * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_3d(&m[3], q_cat, DK, 128, B, row, row * 128, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+    m[4] = m[0];
   } else if (fmt == MLA_FMT_INT8) {
     const uint64_t PB = PAGE_BYTES_INT8;  // sections at 0, 32768, 36864, 38912
     ok = ok && encode_3d(&m[0], pg, DC, PAGE, P, DC, PB, 256, TILE, NS, U8) &&

@@ -127,6 +127,12 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");
 }
+// the same with an L2 eviction-priority policy (createpolicy)
+__device__ __forceinline__ void prefetch_l2_bulk_hint(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes), "l"(policy)
+               : "memory");
+}
 // L2 prefetch of the cache line holding `p`
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
@@ -208,6 +214,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// shared memory -> TMEM: 128 rows x 32 bytes (described by a matrix descriptor,
+// like an MMA operand) into 128 lanes x 8 columns at taddr; asynchronous,
+// tracked by tcgen05.commit like an MMA
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // arrive once on `bar` when every tcgen05 op issued so far by this thread completes
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
