@@ -1,4 +1,4 @@
-// Merge of the split-KV partials and the value up-projection.
+// Merge of the split-KV partials and the value up-projection, in one kernel.
 //
 // Each split s of row b left O_s = (sum_{t in s} e^{x_t - m_s} c_t) / l_s and
 // LSE_s = m_s + ln l_s per head.  The exact softmax over the whole row is
@@ -7,245 +7,352 @@
 // applies the value projection once per head: out[b,h,:] = W_UV[h] o_lat[b,h,:]
 // ("手搓 MLA" §四, einsum("thc,hdc->thd", out_lat, W_UV)).
 //
-// Two kernels: the merge (one warp per row and head, bandwidth-bound) writes
-// each row's fp32 o_lat into the partial slot of the row's first split; the
-// up-projection (one CTA per head) stages W_UV[h] once and runs the GEMM
-// (M = rows, N = 128, K = 512) on the warp-level bf16 tensor-core MMA with
-// o_lat split into a bf16 high part and a bf16 residual, so the only rounding
-// left is W_UV's own bf16 and the fp32 accumulation.
+// One CTA per (head h, group of RB rows).  The segments of a group's rows are
+// consecutive slots of the partial buffer (slot w + b for worker w, row b), so
+// for every 64-wide latent chunk TMA boxes bring that chunk of up to 96
+// segments at a time ([segments][64] fp32) into shared memory.  The merge threads (one
+// per row and 8-dim unit) sum their row's segments with the softmax weights,
+// round o_lat once into a bf16 high part and a bf16 residual, and write both
+// as K-major 128B-swizzled operand tiles; one thread then issues the
+// fifth-generation tensor-core MMAs
+//   D[128 out dims][RB rows] += W_UV[h][:, chunk] . hi^T + W_UV[h][:, chunk] . lo^T
+// (M = 128, N = RB, K = 64 per chunk), so the only roundings left are W_UV's
+// own bf16, the residual's (relative 2^-16) and the fp32 accumulation.
+// W_UV[h] streams through a 2-stage ring of 128B-swizzled TMA tiles whose first
+// loads are issued before the kernel waits for the attention step.
 #include "tc_ptx.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int ROWS = 16;     // batch rows projected per pass
-constexpr int LDA = DC + 4;  // padded fp32 row stride of the o_lat tile (2,064 B)
-constexpr uint32_t W_CHUNK = DV * 64 * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
+using namespace tc;
 
-struct __align__(1024) UpSmem {
-  uint8_t w[8][W_CHUNK];      // W_UV[h] in 8 TMA tiles of 64 latent dims (K)
-  float a[2][ROWS * LDA];     // merged o_lat rows, double-buffered across passes
-  uint64_t w_full, a_full[2];
+constexpr int KC = 64;                    // latent dims per chunk
+constexpr int NCHUNK = DC / KC;           // 8
+constexpr int SEGB = 96;                  // segments per partial tile (TMA box)
+constexpr uint32_t W_TILE = DV * KC * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
+constexpr uint32_t P_TILE = SEGB * KC * 4;  // 24 KB: [96 segments][64 dims] fp32
+constexpr int WST = 2, PST = 2, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
+
+template <int RB>
+struct CombLayout {
+  static constexpr int NW = RB / 4;          // merge warps: 4 rows x 8 units each
+  static constexpr int THREADS = 32 * (NW + 1);  // + a loader / TMEM-owner warp
+  static constexpr uint32_t TCOLS = RB < 32 ? 32 : RB;  // TMEM columns (allocations are >= 32)
+  static constexpr uint32_t B_TILE = RB * 128;   // [RB rows][64 dims] bf16, 128B-swizzled
+  static constexpr uint32_t OFF_W = 0;
+  static constexpr uint32_t OFF_P = OFF_W + WST * W_TILE;
+  static constexpr uint32_t OFF_B = OFF_P + PST * P_TILE;  // [BST][hi, lo]
+  static constexpr uint32_t OFF_BAR = OFF_B + BST * 2 * B_TILE;
+  // barriers: w_full, w_empty, p_full, p_empty, b_full, b_free, d_full
+  static constexpr uint32_t NBAR = 2 * WST + 2 * PST + 2 * BST + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
+  static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;        // int2 [RB]: first / last segment of each row
+  static constexpr uint32_t OFF_WGT = OFF_ROWS + RB * 8;     // float [RB + max workers]: weight per segment
+  static size_t bytes(int max_workers) { return OFF_WGT + (size_t)(RB + max_workers) * 4 + 1024; }
 };
 
-__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// split two fp32 values into packed bf16 high parts and packed bf16 residuals
-__device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(v.x - hf.x, v.y - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-// slot of the merged o_lat of row b (the partial slot of the row's first segment)
-__device__ __forceinline__ size_t merged_slot(const int* prefix, long long T, long long W, int b) {
-  return (size_t)(worker_of_tile(prefix[b], T, W) + b);
-}
-
-// ---- merge: one warp per (row, head).  Lane k reads the LSE of the row's
-// k-th split (32 at a time), the weights e^{LSE_s - max} are formed once, and
-// every split row is loaded before any is summed (4 float4 per lane per
-// split), so a warp keeps all of its row's partial bytes in flight.  The
-// merged o_lat overwrites the row's first partial slot (only this warp reads
-// the row's partials of this head, and it has read them all by then).
-__global__ void __launch_bounds__(256) merge_kernel(int H, int B, const int* __restrict__ plan,
-                                                     float* __restrict__ part_o, const float* __restrict__ part_lse,
-                                                     float* __restrict__ o_lat_out) {
-  grid_dep_wait();  // the partials of the attend step
-  grid_dep_launch();
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (gw >= B * H) return;
-  const int b = gw / H, h = gw % H;
-  const long long T = plan[0], W = plan[1];
-  const int* prefix = plan + PLAN_HDR;
-  float4 acc[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (prefix[b + 1] <= prefix[b]) {  // empty row: o_lat = 0 (the up-projection reads no slot for it)
-    if (o_lat_out != nullptr)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(o_lat_out + ((size_t)b * H + h) * DC)[lane + 32 * i] = acc[i];
-    return;
-  }
-  const int wf = worker_of_tile(prefix[b], T, W);
-  const int wl = worker_of_tile(prefix[b + 1] - 1, T, W);
-  auto lse_of = [&](int w) -> float {  // -inf for a worker without tiles
-    if (w > wl || worker_begin(w, T, W) == worker_begin(w + 1, T, W)) return -INFINITY;
-    return part_lse[(size_t)(w + b) * H + h];
-  };
-  float mx = -INFINITY;
-  for (int w = wf; w <= wl; w += 32) mx = fmaxf(mx, lse_of(w + lane));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float den = 0.f;
-  for (int w0 = wf; w0 <= wl; w0 += 32) {
-    const float lw = lse_of(w0 + lane);
-    const float e = lw == -INFINITY ? 0.f : expf(lw - mx);
-    den += e;
-    const int n = min(32, wl - w0 + 1);
-    for (int k = 0; k < n; k += 4) {
-      float ek[4];
-      float4 v[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ek[j] = __shfl_sync(0xffffffffu, e, min(k + j, 31));
-        if (k + j >= n) ek[j] = 0.f;
-        const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)(w0 + k + j + b) * H + h) * DC);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[j][i] = ek[j] != 0.f ? src[lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+// bounded wait for the combine kernel: false after the time limit or once
+// another thread of the CTA gave up
+__device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t k = 1;; ++k) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((k & 7) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort = 1;
+        raise_error(err, MLA_ERR_TIMEOUT, 100 + where);
+        return false;
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[i].x = fmaf(ek[j], v[j][i].x, acc[i].x);
-          acc[i].y = fmaf(ek[j], v[j][i].y, acc[i].y);
-          acc[i].z = fmaf(ek[j], v[j][i].z, acc[i].z);
-          acc[i].w = fmaf(ek[j], v[j][i].w, acc[i].w);
-        }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  const float inv = 1.f / den;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc[i].x *= inv; acc[i].y *= inv; acc[i].z *= inv; acc[i].w *= inv;
-  }
-  __syncwarp();  // every lane's partial reads precede the in-place write
-  float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)(wf + b) * H + h) * DC);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dst[lane + 32 * i] = acc[i];
-    if (o_lat_out != nullptr) reinterpret_cast<float4*>(o_lat_out + ((size_t)b * H + h) * DC)[lane + 32 * i] = acc[i];
-  }
 }
 
-// ---- up-projection: one CTA per head.  W_UV[h] (128 KB) arrives by eight 2-D
-// TMA tiles (128B swizzle: conflict-free fragment reads) issued at entry; the
-// merged rows arrive 16 at a time by one bulk copy per row, the next pass's
-// rows in flight while the current pass computes.
-__global__ void __launch_bounds__(256, 1) upproj_kernel(const __grid_constant__ CUtensorMap tm_w, int H, int B,
-                                                         const int* __restrict__ plan,
-                                                         const float* __restrict__ part_o,
-                                                         uint16_t* __restrict__ out) {
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int RB>
+__global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
+    combine_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
+                   const uint16_t* __restrict__ W_UV, int H, int B,
+                   const int* __restrict__ plan, const float* __restrict__ part_lse, uint16_t* __restrict__ out,
+                   float* __restrict__ o_lat, int* err) {
+  using L = CombLayout<RB>;
+  constexpr int NW = L::NW;
   extern __shared__ uint8_t smem_raw[];
-  UpSmem& S = *reinterpret_cast<UpSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int h = blockIdx.x;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+  uint64_t* w_full = bars;
+  uint64_t* w_empty = w_full + WST;
+  uint64_t* p_full = w_empty + WST;
+  uint64_t* p_empty = p_full + PST;
+  uint64_t* b_full = p_empty + PST;
+  uint64_t* b_free = b_full + BST;
+  uint64_t* d_full = b_free + BST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 12);
+  int2* rows = reinterpret_cast<int2*>(sm + L::OFF_ROWS);
+  float* wgt = reinterpret_cast<float*>(sm + L::OFF_WGT);
+
+  const int h = blockIdx.x, b0 = blockIdx.y * RB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long T = plan[0], W = plan[1];
-  const int* prefix = plan + PLAN_HDR;
-  const int passes = (B + ROWS - 1) / ROWS;
+  const bool loader = warp == NW;
 
   if (tid == 0) {
-    mbar_init(&S.w_full, 1);
-    mbar_init(&S.a_full[0], ROWS);
-    mbar_init(&S.a_full[1], ROWS);
+    for (int s = 0; s < WST; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int s = 0; s < PST; ++s) {
+      mbar_init(&p_full[s], 1);
+      mbar_init(&p_empty[s], NW);
+    }
+    for (int s = 0; s < BST; ++s) {
+      mbar_init(&b_full[s], NW);
+      mbar_init(&b_free[s], 1);
+    }
+    mbar_init(d_full, 1);
+    *abort = 0;
     fence_barrier_init();
   }
+  if (loader) {
+    tmem_alloc(tmem_slot, L::TCOLS);
+    tmem_relinquish();
+  }
+  fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
-    // W_UV is read before the wait: this kernel always follows the merge
-    // kernel, which itself waited for all earlier work
-    mbar_arrive_expect_tx(&S.w_full, 8 * W_CHUNK);
-    for (int kc = 0; kc < 8; ++kc) tc::tma_load_3d(S.w[kc], &tm_w, 64 * kc, 0, h, &S.w_full);
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (loader && lane == 0) {
+    // W_UV is a weight: its first tiles load while the attention step finishes
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_p);
+    prefetch_l2_bulk(W_UV + (size_t)h * DV * DC, DV * DC * 2);  // W_UV[h] into L2 for the later tiles
+    for (int kc = 0; kc < WST; ++kc) {
+      mbar_arrive_expect_tx(&w_full[kc], W_TILE);
+      tma_load_3d(sm + L::OFF_W + kc * W_TILE, &tm_w, KC * kc, 0, h, &w_full[kc]);
+    }
   }
-  grid_dep_wait();  // the merged rows
+  grid_dep_wait();  // the partials and their log-sum-exps
   grid_dep_launch();
-  // pass p's rows into buffer p & 1: thread r < 16 copies row b0 + r (zeros
-  // for empty rows and rows past B) and arrives once
-  auto issue_rows = [&](int p) {
-    if (tid < ROWS) {
-      const int b = p * ROWS + tid;
-      float* dst = S.a[p & 1] + tid * LDA;
-      uint64_t* bar = &S.a_full[p & 1];
-      if (b < B && prefix[b + 1] > prefix[b]) {
-        mbar_arrive_expect_tx(bar, DC * 4);
-        bulk_g2s(dst, part_o + (merged_slot(prefix, T, W, b) * H + h) * DC, DC * 4, bar);
-      } else {
-        for (int v = 0; v < DC / 4; ++v) reinterpret_cast<float4*>(dst)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-        mbar_arrive(bar);
-      }
-    }
-  };
-  if (passes > 0) issue_rows(0);
 
-  const int g = lane >> 2, t = lane & 3;
-  bool w_ready = false;
-  // fragment of W_UV[h][n][k .. k+1] in the swizzled tiles (k even)
-  auto wfrag = [&](int n, int k) -> uint32_t {
-    const int kb = (k & 63) * 2;
-    return *reinterpret_cast<const uint32_t*>(S.w[k >> 6] + n * 128 + ((((kb >> 4) ^ (n & 7))) << 4) + (kb & 15));
-  };
-  for (int p = 0; p < passes; ++p) {
-    if (p + 1 < passes) issue_rows(p + 1);  // its buffer was released by the barrier ending pass p-1
-    (void)mbar_wait(&S.a_full[p & 1], (uint32_t)(p >> 1) & 1u);  // bounded
-    if (!w_ready) {
-      (void)mbar_wait(&S.w_full, 0);
-      w_ready = true;
-    }
-    __syncthreads();  // zero rows written with plain stores are visible too
-    const float* A = S.a[p & 1];
-    float d[2][4];
-#pragma unroll
-    for (int ni = 0; ni < 2; ++ni)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) d[ni][k] = 0.f;
+  // ---- the slots [s_lo, s_hi) that hold every segment of the group's rows:
+  // segment w + b of row b, rows and workers both increasing along the tiles
+  const long long T = plan[0], W = plan[1];
+  const int* prefix = plan + PLAN_HDR;
+  const int b_end = min(b0 + RB, B);
+  const int t0 = prefix[b0], t1 = prefix[b_end];
+  const int s_lo = t1 > t0 ? worker_of_tile(t0, T, W) + b0 : 0;
+  const int s_hi = t1 > t0 ? worker_of_tile(t1 - 1, T, W) + b_end : 0;
+  const int nsub = (s_hi - s_lo + SEGB - 1) / SEGB;  // partial tiles per chunk (0 when every row is empty)
+
+  if (!loader) {
+    // ---- each row's segments and their softmax weights (merge warps only;
+    // the loader already streams the partial tiles)
+    for (int k = tid; k < s_hi - s_lo; k += 32 * NW) wgt[k] = 0.f;
+    named_barrier(1, 32 * NW);
+    if (tid < RB) {
+      const int b = b0 + tid;
+      int2 r = make_int2(1, 0);  // empty
+      if (b < B && prefix[b + 1] > prefix[b]) {
+        r.x = worker_of_tile(prefix[b], T, W) + b;
+        r.y = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
+      }
+      rows[tid] = r;
+      // log-sum-exp of segment s = w + b (-inf for a worker without tiles)
+      // into wgt, all loads in flight together; then the weights in place
+      float mx = -INFINITY;
 #pragma unroll 4
-    for (int k0 = 0; k0 < DC; k0 += 16) {
-      const float* a0 = A + g * LDA + k0 + 2 * t;
-      const float* a1 = a0 + 8 * LDA;
-      uint32_t ah[4], al[4];
-      split2(*reinterpret_cast<const float2*>(a0), ah[0], al[0]);
-      split2(*reinterpret_cast<const float2*>(a1), ah[1], al[1]);
-      split2(*reinterpret_cast<const float2*>(a0 + 8), ah[2], al[2]);
-      split2(*reinterpret_cast<const float2*>(a1 + 8), ah[3], al[3]);
-#pragma unroll
-      for (int ni = 0; ni < 2; ++ni) {
-        const int n = warp * 16 + ni * 8 + g;
-        const uint32_t bf[2] = {wfrag(n, k0 + 2 * t), wfrag(n, k0 + 8 + 2 * t)};
-        mma_bf16_16816(d[ni], ah, bf);
-        mma_bf16_16816(d[ni], al, bf);
+      for (int s = r.x; s <= r.y; ++s) {
+        const long long w = s - b;
+        const float lw = worker_begin(w, T, W) == worker_begin(w + 1, T, W) ? -INFINITY : part_lse[(size_t)s * H + h];
+        wgt[s - s_lo] = lw;
+        mx = fmaxf(mx, lw);
+      }
+      float den = 0.f;
+      for (int s = r.x; s <= r.y; ++s) {
+        const float lw = wgt[s - s_lo];
+        const float e = lw == -INFINITY ? 0.f : expf(lw - mx);
+        wgt[s - s_lo] = e;
+        den += e;
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      for (int s = r.x; s <= r.y; ++s) wgt[s - s_lo] *= inv;
+    }
+    named_barrier(1, 32 * NW);
+  }
+
+  if (loader) {
+    // ------------------------------------------------------------ TMA loader
+    if (lane == 0) {
+      int pu = 0;  // partial tiles issued so far
+      bool ok = true;
+      for (int kc = 0; kc < NCHUNK && ok; ++kc) {
+        if (kc >= WST) {  // stage kc % WST was read by chunk kc - WST's MMAs
+          const int st = kc % WST;
+          ok = cwait(&w_empty[st], ((kc / WST) & 1) ^ 1, abort, err, 0);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&w_full[st], W_TILE);
+          tma_load_3d(sm + L::OFF_W + st * W_TILE, &tm_w, KC * kc, 0, h, &w_full[st]);
+        }
+        for (int sub = 0; sub < nsub; ++sub, ++pu) {
+          const int st = pu % PST;
+          ok = cwait(&p_empty[st], ((pu / PST) & 1) ^ 1, abort, err, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&p_full[st], P_TILE);
+          tma_load_3d(sm + L::OFF_P + st * P_TILE, &tm_p, KC * kc, h, s_lo + SEGB * sub, &p_full[st]);
+        }
+      }
+      if (*abort) {  // let copies in flight land before the CTA exits
+        for (int k = max(0, pu - PST); k < pu; ++k) (void)mbar_wait(&p_full[k % PST], (k / PST) & 1);
+        for (int kc = 0; kc < NCHUNK; ++kc) (void)mbar_wait(&w_full[kc % WST], (kc / WST) & 1);
       }
     }
-    const int r0 = p * ROWS + g, r1 = r0 + 8;
+  } else {
+    // ------------------------------------------------------------ merge warps
+    const int r = tid >> 3, u = tid & 7;  // row of the group, 8-dim unit of the chunk
+    const int b = b0 + r;
+    const int2 rs = rows[r];
+    const uint32_t idesc = idesc_bf16_f32(128, RB, false, false);
+    int pu = 0;
+    bool ok = true, final_commit = false;
+    for (int kc = 0; kc < NCHUNK && ok; ++kc) {
+      float acc[8];
 #pragma unroll
-    for (int ni = 0; ni < 2; ++ni) {
-      const int col = warp * 16 + ni * 8 + 2 * t;
-      if (r0 < B)
-        *reinterpret_cast<uint32_t*>(out + ((size_t)r0 * H + h) * DV + col) = pack_bf16x2(d[ni][0], d[ni][1]);
-      if (r1 < B)
-        *reinterpret_cast<uint32_t*>(out + ((size_t)r1 * H + h) * DV + col) = pack_bf16x2(d[ni][2], d[ni][3]);
+      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+      for (int sub = 0; sub < nsub; ++sub, ++pu) {
+        const int st = pu % PST;
+        if (!cwait(&p_full[st], (pu / PST) & 1, abort, err, 2)) {
+          ok = false;
+          break;
+        }
+        const float* tile = reinterpret_cast<const float*>(sm + L::OFF_P + st * P_TILE);
+        const int base = s_lo + SEGB * sub;
+        const int sa = max(rs.x, base), sz = min(rs.y, base + SEGB - 1);
+        for (int s = sa; s <= sz; ++s) {
+          const float wv = wgt[s - s_lo];
+          if (wv == 0.f) continue;  // a slot no worker wrote (its contents are undefined)
+          const float4* v = reinterpret_cast<const float4*>(tile + (s - base) * KC + 8 * u);
+          const float4 x = v[0], y = v[1];
+          acc[0] = fmaf(wv, x.x, acc[0]); acc[1] = fmaf(wv, x.y, acc[1]);
+          acc[2] = fmaf(wv, x.z, acc[2]); acc[3] = fmaf(wv, x.w, acc[3]);
+          acc[4] = fmaf(wv, y.x, acc[4]); acc[5] = fmaf(wv, y.y, acc[5]);
+          acc[6] = fmaf(wv, y.z, acc[6]); acc[7] = fmaf(wv, y.w, acc[7]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_empty[st]);
+      }
+      if (!ok) break;
+      if (o_lat != nullptr && b < B)
+        st_global_v8(o_lat + ((size_t)b * H + h) * DC + KC * kc + 8 * u, acc[0], acc[1], acc[2], acc[3], acc[4],
+                     acc[5], acc[6], acc[7]);
+      // o_lat = hi + lo, both bf16, into the operand tiles of this chunk
+      const int bs = kc % BST;
+      if (!cwait(&b_free[bs], ((kc / BST) & 1) ^ 1, abort, err, 3)) {
+        ok = false;
+        break;
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        hi[k] = pack2_bf16(acc[2 * k], acc[2 * k + 1]);
+        const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[k]));
+        lo[k] = pack2_bf16(acc[2 * k] - hf.x, acc[2 * k + 1] - hf.y);
+      }
+      const uint32_t off = r * 128 + ((u ^ (r & 7)) << 4);
+      uint8_t* bt = sm + L::OFF_B + bs * 2 * L::B_TILE;
+      *reinterpret_cast<uint4*>(bt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(bt + L::B_TILE + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b_full[bs]);
+      if (tid == 0) {
+        // ------------------------------------------------ MMA issue (one thread)
+        const int ws = kc % WST;
+        if (!cwait(&b_full[bs], (kc / BST) & 1, abort, err, 4) || !cwait(&w_full[ws], (kc / WST) & 1, abort, err, 5)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t wa = smem_u32(sm + L::OFF_W + ws * W_TILE), ba = smem_u32(bt);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kk = 0; kk < KC / 16; ++kk)
+            mma_ss(tmem, smem_desc(wa + kk * 32, 16, 1024, SWIZZLE_128B),
+                   smem_desc(ba + part * L::B_TILE + kk * 32, 16, 1024, SWIZZLE_128B), idesc,
+                   (kc | part | kk) != 0 ? 1u : 0u);
+        mma_commit(&b_free[bs]);
+        mma_commit(&w_empty[ws]);
+        if (kc == NCHUNK - 1) {
+          mma_commit(d_full);
+          final_commit = true;
+        }
+      }
     }
-    __syncthreads();  // buffer p & 1 is refilled by pass p + 2
+    // ---- epilogue: D[out dim][row] -> out[b][h][:] (bf16)
+    if (ok && cwait(d_full, 0, abort, err, 6)) {
+      fence_after_sync();
+      const int q = warp & 3, cg = warp >> 2;  // TMEM lane quadrant (32 out dims), 16-row column group
+      uint32_t v[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * cg, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int bb = b0 + 16 * cg + k;
+        if (bb < B) {
+          const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[k]));
+          out[((size_t)bb * H + h) * DV + 32 * q + lane] = *reinterpret_cast<const uint16_t*>(&o);
+        }
+      }
+    }
+    if (tid == 0 && *abort) {  // MMAs in flight finish before TMEM is freed
+      if (!final_commit) mma_commit(d_full);
+      (void)mbar_wait(d_full, 0);
+    }
   }
-  if (!w_ready) (void)mbar_wait(&S.w_full, 0);  // no pass ran: let the copies land before exit
+  fence_before_sync();
+  __syncthreads();
+  if (loader) {
+    fence_after_sync();
+    tmem_dealloc(tmem, L::TCOLS);
+  }
+}
+
+template <int RB>
+cudaError_t launch_rb(const CUtensorMap& tm_w, const CUtensorMap& tm_p, const void* W_UV, int H, int B, const int* plan,
+                      const float* part_lse, void* out, float* o_lat, int* err, int max_workers, cudaStream_t s) {
+  using L = CombLayout<RB>;
+  const size_t smem = L::bytes(max_workers);
+  cudaError_t e = cudaFuncSetAttribute(combine_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(combine_kernel<RB>, dim3(H, (B + RB - 1) / RB), dim3(L::THREADS), smem, s, tm_w, tm_p,
+                    static_cast<const uint16_t*>(W_UV), H, B, plan, part_lse, static_cast<uint16_t*>(out), o_lat, err);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
-                           const float* part_lse, void* out, float* o_lat, cudaStream_t s) {
+                           const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
+                           cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  float* po = const_cast<float*>(part_o);  // the merge writes each row's o_lat into its first partial slot
-  cudaError_t e = launch_pdl(merge_kernel, dim3((B * H + 7) / 8), dim3(256), 0, s, H, B, plan, po, part_lse, o_lat);
-  if (e != cudaSuccess) return e;
-  CUtensorMap tm_w;  // W_UV: (512 latent, 128 rows, H heads), tiles of 64 x 128, 128B swizzle
+  CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, H heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, H, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const size_t smem = sizeof(UpSmem) + 1024;
-  e = cudaFuncSetAttribute(upproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(upproj_kernel, dim3(H), dim3(256), smem, s, tm_w, H, B, plan, static_cast<const float*>(po),
-                    static_cast<uint16_t*>(out));
+  // partials: (512 latent, H heads, segments), boxes of 64 dims x 1 head x 128 segments
+  const uint64_t segs = (uint64_t)max_workers + B;
+  if (!encode_3d_box(&tm_p, part_o, DC, H, segs, DC * 4, (uint64_t)H * DC * 4, KC, 1, SEGB,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    return cudaErrorInvalidValue;
+  // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
+  const int sms = device_sm_count();
+  if ((long long)H * ((B + 31) / 32) >= sms)
+    return launch_rb<32>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+  return launch_rb<16>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
 }
 
 }  // namespace mla

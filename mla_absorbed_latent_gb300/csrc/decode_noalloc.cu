@@ -122,6 +122,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
     e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine(W_UV, H, B, plan, part_o, part_lse, out, nullptr, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine(W_UV, H, B, plan, part_o, part_lse, out, nullptr, err, workers, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }

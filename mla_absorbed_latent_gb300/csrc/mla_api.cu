@@ -204,10 +204,13 @@ int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t w
   if (B == 0) return MLA_OK;
   if (!W_UV || !out || !aligned(W_UV, 16) || !aligned(out, 16) || (o_lat_out && !aligned(o_lat_out, 16)))
     return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return status_of(launch_combine(W_UV, H, B, reinterpret_cast<const int*>(ws + L.plan),
                                   reinterpret_cast<const float*>(ws + L.part_o),
-                                  reinterpret_cast<const float*>(ws + L.part_lse), out, o_lat_out, stream));
+                                  reinterpret_cast<const float*>(ws + L.part_lse), out, o_lat_out, err,
+                                  L.max_segments - B, stream));
 }
 
 int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,

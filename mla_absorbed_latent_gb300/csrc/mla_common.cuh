@@ -185,8 +185,10 @@ int* device_error_word();            // this device's error word, nullptr on fai
 int device_sm_count();               // SMs of the current device, 0 on failure
 int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
 
+// max_workers: the partial buffer holds max_workers + B segment slots
 cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
-                           const float* part_lse, void* out, float* o_lat, cudaStream_t s);
+                           const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
+                           cudaStream_t s);
 
 // 3-D TMA tensor map (tensor_map.cu): dims (d0 fastest), byte strides of dims 1
 // and 2, box (b0, b1, 1); false when the driver refuses the description
