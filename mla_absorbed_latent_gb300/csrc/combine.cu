@@ -9,7 +9,7 @@
 //
 // One CTA per (head h, group of RB rows).  The segments of a group's rows are
 // consecutive slots of the partial buffer (slot w + b for worker w, row b), so
-// for every 64-wide latent chunk TMA boxes bring that chunk of up to 96
+// for every 64-wide latent chunk TMA boxes bring that chunk of up to 80
 // segments at a time ([segments][64] fp32) into shared memory.  The merge threads (one
 // per row and 8-dim unit) sum their row's segments with the softmax weights,
 // round o_lat once into a bf16 high part and a bf16 residual, and write both
@@ -29,10 +29,10 @@ using namespace tc;
 
 constexpr int KC = 64;                    // latent dims per chunk
 constexpr int NCHUNK = DC / KC;           // 8
-constexpr int SEGB = 96;                  // segments per partial tile (TMA box)
+constexpr int SEGB = 80;                  // segments per partial tile (TMA box)
 constexpr uint32_t W_TILE = DV * KC * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
-constexpr uint32_t P_TILE = SEGB * KC * 4;  // 24 KB: [96 segments][64 dims] fp32
-constexpr int WST = 2, PST = 2, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
+constexpr uint32_t P_TILE = SEGB * KC * 4;  // 20 KB: [80 segments][64 dims] fp32
+constexpr int WST = 2, PST = 3, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
 
 template <int RB>
 struct CombLayout {

@@ -14,9 +14,13 @@
 namespace mla {
 namespace {
 
+constexpr int SMEM_ROWS = 8192;  // rows whose tile prefix the worker search reads from shared memory
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seqlens, int B, int max_pages,
                                                      int workers, int* __restrict__ plan, int* err) {
   __shared__ int warp_sums[32];
+  __shared__ int s_prefix[SMEM_ROWS + 1];
+  const bool in_smem = B <= SMEM_ROWS;
   grid_dep_wait();  // earlier work may still write the lengths or read this plan
   grid_dep_launch();
   const int tid = threadIdx.x;
@@ -26,7 +30,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   int* prefix = plan + PLAN_HDR;
   int* seq_c = plan + PLAN_HDR + B + 1;
 
-  int local = 0;
+  int local = 0, first_n = 0;  // first_n: the clamped length of row lo (one row per thread when B <= 1024)
   for (int b = lo; b < hi; ++b) {
     long long n = seqlens[b];
     if (n < 0 || n > cap) {
@@ -34,6 +38,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       n = n < 0 ? 0 : cap;
     }
     seq_c[b] = (int)n;
+    if (b == lo) first_n = (int)n;
     local += (int)((n + PAGE - 1) / PAGE);
   }
   // block-wide exclusive scan of the per-thread tile counts
@@ -59,10 +64,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
   for (int b = lo; b < hi; ++b) {
     prefix[b] = run;
-    run += (seq_c[b] + PAGE - 1) / PAGE;
+    if (in_smem) s_prefix[b] = run;
+    run += ((b == lo ? first_n : seq_c[b]) + PAGE - 1) / PAGE;
   }
   if (tid == blockDim.x - 1) {
     prefix[B] = run;
+    if (in_smem) s_prefix[B] = run;
     plan[0] = run;
     plan[1] = workers;
     plan[2] = B;
@@ -71,14 +78,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   __syncthreads();  // the prefix is complete (block-wide visibility of the global writes)
   // first row of each worker's range: the largest b with prefix[b] <= its first
   // tile (so a worker starts its cursor with one load instead of a search)
+  const int* pf = in_smem ? s_prefix : prefix;
   int* wrow = plan + PLAN_HDR + 2 * B + 1;
-  const long long T = prefix[B];
+  const long long T = pf[B];
   for (int w = tid; w < workers; w += blockDim.x) {
     const long long x = worker_begin(w, T, workers);
     int lo = 0, hi = B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= x) lo = mid; else hi = mid;
+      if (pf[mid] <= x) lo = mid; else hi = mid;
     }
     wrow[w] = lo;
   }

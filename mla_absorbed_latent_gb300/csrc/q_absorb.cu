@@ -31,6 +31,7 @@ struct __align__(1024) QaSmem {
 
 __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                            const __grid_constant__ CUtensorMap tm_q,
+                                                           const __grid_constant__ CUtensorMap tm_qc,
                                                            const uint16_t* __restrict__ q_pe, int H, int B,
                                                            uint16_t* __restrict__ q_cat) {
   extern __shared__ uint8_t smem_raw[];
@@ -44,10 +45,8 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     mbar_init(&S.q_full, 1);
     mbar_init(&S.mma_done, 1);
     fence_barrier_init();
-  }
-  grid_dep_wait();  // the weights and queries may come from the work before this kernel
-  grid_dep_launch();
-  if (tid == 0) {
+    // W_UK is a weight, written (if at all) by a kernel that completed before
+    // this chain started: its tiles load while the kernel before this one runs
     mbar_arrive_expect_tx(&S.w_full, 4 * W_TILE);
     for (int dc = 0; dc < 2; ++dc)
       for (int nh = 0; nh < 2; ++nh) tma_load_3d(S.w[2 * dc + nh], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
@@ -59,6 +58,8 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+  grid_dep_wait();  // the queries, and the readers of q_cat in the step before
+  grid_dep_launch();
   const uint32_t tmem = S.tmem_base;
   const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
 
@@ -93,22 +94,42 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     (void)mbar_wait(&S.mma_done, (uint32_t)p & 1u);
     __syncwarp();
     fence_after_sync();
-    // epilogue: warp w owns TMEM lanes (rows) 32w..32w+31
-    const int r = b0 + warp * 32 + lane;
-    uint16_t* dst = q_cat + ((size_t)r * H + h) * DK;
-    for (int c32 = 0; c32 < DC / 32; ++c32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * c32, v);
-      tmem_ld_wait();
-      if (r < B) {
+    // epilogue: warp w owns TMEM lanes (rows) 32w..32w+31.  Each 128-column
+    // round goes TMEM -> bf16 in a 128B-swizzled staging tile (this warp's 8 KB
+    // of the q tiles, free now that the MMAs have read them) -> two TMA stores
+    // (rows past B are clipped by the tensor map)
+    const int r0 = b0 + warp * 32;
+    if (r0 < B) {
+      uint8_t* stg = &S.q[0][0] + warp * 8192;
+      for (int rd = 0; rd < DC / 128; ++rd) {
+        if (rd > 0 && lane == 0) bulk_wait_read_all();  // the last round's stores have read the tile
+        __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          reinterpret_cast<uint4*>(dst + 32 * c32)[k] =
-              make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
-                         pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
-                         pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
-                         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int c32 = 0; c32 < 2; ++c32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 128 * rd + 64 * half + 32 * c32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int chunk = 4 * c32 + k;  // 16-byte unit of the 128-byte row
+              *reinterpret_cast<uint4*>(stg + half * 4096 + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+            }
+          }
+        fence_proxy_async_smem();  // generic writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_qc, stg, 128 * rd, h, r0);
+          tma_store_3d(&tm_qc, stg + 4096, 128 * rd + 64, h, r0);
+          bulk_commit_group();
+        }
       }
+      if (lane == 0) bulk_wait_all();  // the staging tile is the next pass's q tile; stores complete before exit
     }
     fence_before_sync();
     __syncthreads();  // TMEM and the q tiles are rewritten by the next pass
@@ -134,10 +155,13 @@ cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_
     return cudaErrorInvalidValue;
   if (!encode_3d_box(&tm_q, q_nope, DN, H, B, DN * 2, (uint64_t)H * DN * 2, 64, 1, QROWS, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap tm_qc;  // q_cat: (576 dims, H, B), stores of 64 dims x 1 head x 32 rows
+  if (!encode_3d_box(&tm_qc, q_cat, DK, H, B, DK * 2, (uint64_t)H * DK * 2, 64, 1, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const size_t smem = sizeof(QaSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(q_absorb_kernel, dim3(H), dim3(128), smem, s, tm_w, tm_q, static_cast<const uint16_t*>(q_pe), H,
+  return launch_pdl(q_absorb_kernel, dim3(H), dim3(128), smem, s, tm_w, tm_q, tm_qc, static_cast<const uint16_t*>(q_pe), H,
                     B, static_cast<uint16_t*>(q_cat));
 }
 
