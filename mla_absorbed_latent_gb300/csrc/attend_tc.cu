@@ -82,10 +82,12 @@ constexpr int QCOLS = 64;                                     // q_lat TMEM colu
 constexpr uint32_t KV_CHUNK = TILE * 64 * 2;                  // 8,192: [64 tokens][64 dims] 128B-swizzled
 constexpr uint32_t KV_PE_OFF = 4 * KV_CHUNK;                  // 32,768: [64 tokens][32 dims] 64B-swizzled
 constexpr uint32_t KV_BYTES = TILE * (HALF_C + PE_HALF) * 2;  // 36,864
-constexpr uint32_t PH_BYTES = 128 * HALF_T * 2;               // 8,192: P of a token half, [128][32] 64B-swizzled
+constexpr uint32_t PG_BYTES = 128 * TPW * 2;                  // 4,096: P of 16 tokens, [128][16] 32B-swizzled
 constexpr uint32_t X_BYTES = 128 * HALF_T * 2;                // 8,192: fp16 partial scores of a token half
-constexpr uint32_t MSG_BYTES = 128 * 8;                       // 1,024: two floats per head
-constexpr uint32_t PIN_BYTES = PH_BYTES + MSG_BYTES;          // the peer's P half and its message
+constexpr uint32_t X_Q = X_BYTES / 4;                         // 2,048: the rows of one TMEM lane quadrant
+constexpr uint32_t PG_Q = PG_BYTES / 4;                       // 1,024: one MT warp's rows of its P tile
+constexpr uint32_t SL_Q = 32 * 4;                             // 128: one MT warp's message (a float per head)
+constexpr uint32_t PIN_Q = 2 * (PG_Q + SL_Q);                 // from the peer's two MT warps of a quadrant
 constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
@@ -94,7 +96,6 @@ constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 hea
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
 constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p tolerated (O and l stay finite in fp32)
-constexpr uint32_t OWNER_BAR = 5, SENDER_BAR = 6;  // named barriers of the 256 MT / 256 PT threads
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 // Per cache format: bf16 pages are TMA-copied straight into the MMA operand
@@ -130,22 +131,23 @@ struct __align__(1024) SmemTC {
   static constexpr uint32_t CODE_BYTES = FmtTraits<FMT>::CODE_BYTES > 0 ? FmtTraits<FMT>::CODE_BYTES : 128;
   uint8_t kv[KV_ST][KV_BYTES];
   uint8_t qpe[QPE_BYTES];     // 64B-swizzled MMA operand: 1 KB aligned (follows 1 KB multiples)
-  uint8_t p[2][2][PH_BYTES];  // P per page parity and token half ([128 heads][32 tokens], 64B-swizzled)
+  uint8_t p[2][4][PG_BYTES];  // P per page parity and 16-token group ([128 heads][16 tokens], 32B-swizzled)
   uint8_t xin[2][X_BYTES];    // the peer's fp16 partials of our token half, rows 64 B, chunks swizzled
   static constexpr int XOUT_N = FMT == MLA_FMT_BF16 ? 2 : 1;
   uint8_t xout[XOUT_N][X_BYTES];  // ours of the peer's token half, same layout, shipped by one bulk copy
   uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
-  float2 msg_in[2][128];   // from the peer per page and head: its two slices' maxima (sums at a segment end)
-  float2 msg_out[2][128];  // ours, shipped with our P half
-  float2 mx_in[2][128];    // first page of a segment: the peer's two slices' maxima, exchanged before P
-  float2 mx_out[2][128];
+  // per page parity, slice (2 rank + MT index) and head: the slice maximum
+  // (its sum at a segment end), ours written here and shipped, the peer's
+  // copied in; mxs: a segment's first-page maxima, exchanged before its P
+  float msgs[2][4][128];
+  float mxs[2][4][128];
   uint64_t kv_full[KV_ST], kv_empty[KV_ST];
   uint64_t code_full[CODE_ST], code_empty[CODE_ST];
   uint64_t q_ready;         // quantized: q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
   uint64_t q_done, qpe_full;  // bf16: the segment's q_lat half copied into TMEM / its q_pe half into qpe
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2], pv_both[2];
-  uint64_t x_full[2], x_empty[2], pin_full[2], mx_full[2];
+  uint64_t x_full[2][4], x_empty[2][4], pin_full[2][4], mx_full[2][4];  // per page parity and lane quadrant
   uint64_t o_free, mma_done[3];
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -153,7 +155,7 @@ struct __align__(1024) SmemTC {
 static_assert(sizeof(SmemTC<MLA_FMT_BF16>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT8>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
 static_assert(sizeof(SmemTC<MLA_FMT_INT4>) + 1024 <= 232448, "shared memory of one CTA exceeds 227 KB");
-static_assert(KV_BYTES % 1024 == 0 && PH_BYTES % 1024 == 0 && QPE_BYTES % 1024 == 0,
+static_assert(KV_BYTES % 1024 == 0 && PG_BYTES % 1024 == 0 && QPE_BYTES % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
 static_assert(offsetof(SmemTC<MLA_FMT_BF16>, qpe) % 1024 == 0 && offsetof(SmemTC<MLA_FMT_BF16>, p) % 1024 == 0 &&
                   offsetof(SmemTC<MLA_FMT_INT8>, qpe) % 1024 == 0 && offsetof(SmemTC<MLA_FMT_INT4>, qpe) % 1024 == 0,
@@ -323,10 +325,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&S.p_full[s], 8);  // the MT warps' checks
       mbar_init(&S.pv_done[s], 1);
       mbar_init(&S.pv_both[s], 2);   // this CTA's and the peer's P.V commits
-      mbar_init(&S.x_full[s], 1);    // local expect_tx arrival + the peer's fp16 partial bytes
-      mbar_init(&S.x_empty[s], 8);   // one remote arrival per peer MT warp
-      mbar_init(&S.pin_full[s], 1);  // local expect_tx arrival + the peer's P half and message
-      mbar_init(&S.mx_full[s], 1);   // local expect_tx arrival + the peer's first-page maxima
+      for (int q = 0; q < 4; ++q) {
+        mbar_init(&S.x_full[s][q], 1);    // local expect_tx arrival + the peer's fp16 partial rows
+        mbar_init(&S.x_empty[s][q], 2);   // one remote arrival per peer MT warp of the quadrant
+        mbar_init(&S.pin_full[s][q], 3);  // expect_tx + the 2 local MT warps' messages + the peer's P rows, messages
+        mbar_init(&S.mx_full[s][q], 3);   // the same for a segment's first-page maxima
+      }
     }
     mbar_init(&S.o_free, 8);  // the MT warps' epilogues
     for (int k = 0; k < 3; ++k) mbar_init(&S.mma_done[k], 1);
@@ -564,10 +568,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint64_t vdesc = smem_desc(smem_u32(S.kv[st]), KV_CHUNK, 1024, SWIZZLE_128B);
 #pragma unroll
       for (int kk = 0; kk < TILE / 16; ++kk) {
-        // tokens 16kk..16kk+15: the half tile kk/2, K step kk%2 inside it
-        const uint64_t adesc = smem_desc(smem_u32(S.p[pb][kk >> 1]), 16, 512, SWIZZLE_64B);
-        mma_ss(tmem + TM_O, adesc + (uint64_t)(((kk & 1) * 32) >> 4), vdesc + (uint64_t)((kk * 16 * 128) >> 4),
-               idesc_pv, (first && kk == 0) ? 0u : 1u);
+        // tokens 16kk..16kk+15: P tile kk (computed by CTA kk / 2)
+        const uint64_t adesc = smem_desc(smem_u32(S.p[pb][kk]), 16, 256, SWIZZLE_32B);
+        mma_ss(tmem + TM_O, adesc, vdesc + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
       }
       mma_commit(&S.pv_done[pb]);
       mma_commit_mc(&S.pv_both[pb], (uint16_t)0x3);
@@ -652,14 +655,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (kQuant && mt) load_query(rc.b);  // bf16: the S issuers install each segment's query
     if (mt) {
       // ---------------------------------------------------------- MT warps
-      const bool leader = q4 == 0 && ms == 0 && lane == 0;
-      const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0]), peer);
-      const uint32_t peer_p = mapa(smem_u32(S.p[0][0]), peer);
-      const uint32_t peer_msg = mapa(smem_u32(&S.msg_in[0][0]), peer);
-      const uint32_t peer_mx = mapa(smem_u32(&S.mx_in[0][0]), peer);
-      const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0]), peer);
-      const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[0]), peer);
+      // Exchange with the peer, per lane quadrant q4 and without group-wide
+      // barriers: this warp ships its own P rows (1 KB) and message (128 B) by
+      // bulk copies counted on the peer's pin_full[sb][q4]; the two local MT
+      // warps of the quadrant arrive on their own pin_full after writing their
+      // messages, so a check sees all four slices of its heads.
+      const bool qlead = ms == 0 && lane == 0;  // arms this quadrant's barriers each page
+      const int slot = 2 * (int)rank + ms;      // this warp's slice among the four of a page
+      const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0][q4]), peer);
+      const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0][q4]), peer);
+      const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[0][q4]), peer);
+      const uint32_t peer_p = mapa(smem_u32(&S.p[0][slot][0]), peer) + PG_Q * q4;
+      const uint32_t peer_msg = mapa(smem_u32(&S.msgs[0][slot][0]), peer) + SL_Q * q4;
+      const uint32_t peer_mx = mapa(smem_u32(&S.mxs[0][slot][0]), peer) + SL_Q * q4;
+      constexpr uint32_t BAR_SB = 4 * 8;                    // bytes between the page parities' quadrant barriers
+      constexpr uint32_t P_SB = 4 * PG_BYTES, M_SB = 4 * 128 * 4;  // bytes between page parities
       const int tok0 = HALF_T * (int)rank + TPW * ms;  // first page token of this thread's slice
+      // offset of 16-byte unit k (8 tokens) of this lane's row in a P tile
+      const uint32_t prow = (uint32_t)row * 32;
+      auto punit = [&](int k) -> uint32_t { return prow + ((uint32_t)(k ^ ((row >> 2) & 1)) << 4); };
       // softmax state of this head (lane), log2 domain:
       //  m_ref      reference of the P written from now on
       //  l          sum of this slice's p over the segment so far, in m_ref
@@ -667,17 +681,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       //             and O must still be rescaled (a reference move), 1 if none
       float m_ref = -INFINITY, l = 0.f, alpha_due = 1.f;
       int fcnt0 = 0, fcnt1 = 0;  // first pages seen per page parity (phases of mx_full)
-      // lagged check of page j: the peer's P half and message have arrived ->
-      // decide reference moves, rescale what page j still needs, release its
-      // P.V; at a segment end write the segment's output.  ref_j: the
-      // reference page j's P was written in.
+      // lagged check of page j: the peer's P rows and the four messages have
+      // arrived -> decide reference moves, rescale what page j still needs,
+      // release its P.V; at a segment end write the segment's output.  ref_j:
+      // the reference page j's P was written in.
       auto check = [&](int j, bool j_last, int seg, float ref_j) -> bool {
         const int jb = j & 1;
-        bool ok = wait_bar<true>(S, &S.pin_full[jb], (uint32_t)(j >> 1) & 1u, a.err, 20);
+        bool ok = wait_bar<true>(S, &S.pin_full[jb][q4], (uint32_t)(j >> 1) & 1u, a.err, 20);
         __syncwarp();
-        const float2 mine = S.msg_out[jb][row], theirs = S.msg_in[jb][row];
-        // a move decided at the previous check: page j's P (both halves, this
-        // CTA's copy) and O (after page j-1's P.V) go to the new reference
+        const float m0 = S.msgs[jb][0][row], m1 = S.msgs[jb][1][row], m2 = S.msgs[jb][2][row],
+                    m3 = S.msgs[jb][3][row];
+        // a move decided at the previous check: page j's P (this slice's
+        // tokens of both CTAs, this CTA's copy) and O (after page j-1's P.V) go
+        // to the new reference
         const float alpha = alpha_due;
         alpha_due = 1.f;
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -687,10 +703,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           scale_o(alpha);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            uint8_t* ph = S.p[jb][hf];
+            uint8_t* pt = S.p[jb][2 * hf + ms];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              uint4* u = reinterpret_cast<uint4*>(ph + sw64(row, 2 * ms + k));
+              uint4* u = reinterpret_cast<uint4*>(pt + punit(k));
               uint4 v = *u;
               v.x = scale_bf16x2(v.x, alpha); v.y = scale_bf16x2(v.y, alpha);
               v.z = scale_bf16x2(v.z, alpha); v.w = scale_bf16x2(v.w, alpha);
@@ -702,7 +718,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!j_last) {
           // page j's maximum over all four slices against the reference it used
-          const float m_comb = fmaxf(fmaxf(mine.x, mine.y), fmaxf(theirs.x, theirs.y));
+          const float m_comb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
           if (m_comb > ref_j + RESCALE_LOG2) {
             const float m_new = fmaxf(m_comb, m_ref);
             alpha_due = ex2(m_ref - m_new);  // for page j+1's P and O, at the next check
@@ -715,7 +731,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (j_last) {
           // the four slices' sums, in page j's reference; O is in that
           // reference times alpha after a move applied above
-          const float Lm = mine.x + mine.y + theirs.x + theirs.y;
+          const float Lm = (m0 + m1) + (m2 + m3);
           const float L = alpha * Lm;
           if (!wait_bar<false>(S, &S.pv_done[jb], (uint32_t)(j >> 1) & 1u, a.err, 22)) ok = false;
           __syncwarp();
@@ -739,13 +755,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
-        if (leader) {
-          mbar_arrive_expect_tx(&S.x_full[sb], X_BYTES);      // the peer's partials of my tokens
-          mbar_arrive_expect_tx(&S.pin_full[sb], PIN_BYTES);  // the peer's P half and message
-          if (first) mbar_arrive_expect_tx(&S.mx_full[sb], MSG_BYTES);  // the peer's first-page maxima
+        if (qlead) {
+          mbar_arrive_expect_tx(&S.x_full[sb][q4], X_Q);     // the peer's partials of my tokens, these rows
+          mbar_arrive_expect_tx(&S.pin_full[sb][q4], PIN_Q);  // the peer's P rows and messages
+          if (first) mbar_arrive_expect_tx(&S.mx_full[sb][q4], 2 * SL_Q);  // the peer's first-page maxima
         }
         // ---- this CTA's partial scores of my tokens; the S buffer is released
-        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) failed = true;
+        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) break;
         __syncwarp();
         fence_after_sync();
         uint32_t own[TPW];
@@ -756,7 +772,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
 
         // ---- add the peer's partial (fp16, log2 units) of my tokens
-        if (!wait_bar<true>(S, &S.x_full[sb], ph, a.err, 11)) failed = true;
+        if (!wait_bar<true>(S, &S.x_full[sb][q4], ph, a.err, 11)) break;
         __syncwarp();
         float s[TPW];
         const uint8_t* xi = S.xin[sb];
@@ -785,16 +801,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- the reference of this page's P
         if (first) {
           // segment start: the exact row maximum over the page's four slices
-          float2* mo = &S.mx_out[sb][row];
-          if (ms == 0) mo->x = mraw; else mo->y = mraw;
+          S.mxs[sb][slot][row] = mraw;
           fence_proxy_async_smem();
-          if (!named_barrier_and(OWNER_BAR, 32 * 8, !failed)) break;
-          if (leader) bulk_s2peer(peer_mx + sb * MSG_BYTES, &S.mx_out[sb][0], MSG_BYTES, peer_mxf + 8u * sb);
-          const int fc = sb ? fcnt1++ : fcnt0++;
-          if (!wait_bar<true>(S, &S.mx_full[sb], (uint32_t)fc & 1u, a.err, 19)) failed = true;
           __syncwarp();
-          const float2 a2 = S.mx_out[sb][row], b2 = S.mx_in[sb][row];
-          m_ref = fmaxf(fmaxf(a2.x, a2.y), fmaxf(b2.x, b2.y));
+          if (lane == 0) {
+            bulk_s2peer(peer_mx + M_SB * sb, &S.mxs[sb][slot][32 * q4], SL_Q, peer_mxf + BAR_SB * sb);
+            mbar_arrive(&S.mx_full[sb][q4]);
+          }
+          const int fc = sb ? fcnt1++ : fcnt0++;
+          if (!wait_bar<true>(S, &S.mx_full[sb][q4], (uint32_t)fc & 1u, a.err, 19)) break;
+          __syncwarp();
+          m_ref = fmaxf(fmaxf(S.mxs[sb][0][row], S.mxs[sb][1][row]), fmaxf(S.mxs[sb][2][row], S.mxs[sb][3][row]));
           l = 0.f;
         }
         if (mraw - m_ref > RANGE_LOG2) raise_error(a.err, MLA_ERR_RANGE, 0);
@@ -812,26 +829,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         l += sum0 + sum1;
         // P tile sb is free once the P.V of page i-2 has completed in both CTAs
-        if (!wait_bar<true>(S, &S.pv_both[sb], ph ^ 1u, a.err, 13)) failed = true;
+        if (!wait_bar<true>(S, &S.pv_both[sb], ph ^ 1u, a.err, 13)) break;
         __syncwarp();
-        uint8_t* pm = S.p[sb][rank];
+        uint8_t* pm = S.p[sb][slot];
 #pragma unroll
-        for (int k = 0; k < TPW / 8; ++k)
-          *reinterpret_cast<uint4*>(pm + sw64(row, (TPW / 8) * ms + k)) =
-              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int k = 0; k < 2; ++k)
+          *reinterpret_cast<uint4*>(pm + punit(k)) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         // message: this slice's maximum, or its sum at a segment's last page
-        float2* mo = &S.msg_out[sb][row];
-        if (ms == 0) mo->x = last ? l : mraw; else mo->y = last ? l : mraw;
+        S.msgs[sb][slot][row] = last ? l : mraw;
         // every value read from the exchange buffer has been used by the store
         // above (mraw depends on all of them), so the peer may refill it
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + 8u * sb);
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_xempty + BAR_SB * sb);
         fence_proxy_async_smem();
-        // every MT thread passes here each page: also where they leave together
-        if (!named_barrier_and(OWNER_BAR, 32 * 8, !failed)) break;
-        if (leader) {
-          bulk_s2peer(peer_p + (sb * 2 + rank) * PH_BYTES, pm, PH_BYTES, peer_pin + 8u * sb);
-          bulk_s2peer(peer_msg + sb * MSG_BYTES, &S.msg_out[sb][0], MSG_BYTES, peer_pin + 8u * sb);
+        __syncwarp();
+        if (lane == 0) {
+          bulk_s2peer(peer_p + P_SB * sb, pm + PG_Q * q4, PG_Q, peer_pin + BAR_SB * sb);
+          bulk_s2peer(peer_msg + M_SB * sb, &S.msgs[sb][slot][32 * q4], SL_Q, peer_pin + BAR_SB * sb);
+          mbar_arrive(&S.pin_full[sb][q4]);  // our message, for our partner's check
         }
         // the next page starts a new segment: every S of this one has completed
         // (this thread waited for each), so the next query may replace this one
@@ -840,20 +855,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           nx.advance(prefix, seq_c, x + 1);
           load_query(nx.b);
         }
-        if (pend_i >= 0 && !check(pend_i, pend_last, pend_seg, pend_ref)) failed = true;
+        if (pend_i >= 0 && !check(pend_i, pend_last, pend_seg, pend_ref)) break;
         pend_i = i;
         pend_last = last;
         pend_seg = worker + rc.b;
         pend_ref = m_ref;
       }
-      if (!failed && pend_i >= 0) (void)check(pend_i, pend_last, pend_seg, pend_ref);
+      if (!S.abort_flag && pend_i >= 0) (void)check(pend_i, pend_last, pend_seg, pend_ref);
     } else {
       // ---------------------------------------------------------- PT warps
-      const bool leader = q4 == 0 && lane == 0;
       constexpr int NSEND = 128;                       // PT threads
       const int sid = q4 * 32 + lane;                  // 0..NSEND-1
-      const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer);
-      const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0]), peer);
+      // this warp ships its quadrant's rows (2 KB) to the peer's x_full[sb][q4]
+      const uint32_t peer_xin = mapa(smem_u32(S.xin[0]), peer) + X_Q * q4;
+      const uint32_t peer_xfull = mapa(smem_u32(&S.x_full[0][q4]), peer);
+      constexpr uint32_t BAR_SB = 4 * 8;  // bytes between the page parities' quadrant barriers
       const int tok0 = HALF_T * (int)peer;             // the peer's token half
       // quantized formats: page j's staged codes -> bf16 operand stage j % KV_ST
       // (rows at or past nvalid are written as zeros), then release both
@@ -917,7 +933,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int st = (kQuant ? i : i + 2 * (pseg + 1)) % KV_ST, sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
-        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) failed = true;
+        if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 15)) break;
         __syncwarp();
         fence_after_sync();
         uint32_t v[HALF_T];
@@ -944,23 +960,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // the peer has consumed what we sent into its buffer two pages ago (so
         // the copy that read xout[sb] then has completed too); with a single
         // staging tile, also last page's
-        if (!wait_bar<true>(S, &S.x_empty[sb], ph ^ 1u, a.err, 16)) failed = true;
+        if (!wait_bar<true>(S, &S.x_empty[sb][q4], ph ^ 1u, a.err, 16)) break;
         if (Smem::XOUT_N == 1 && i > 0 &&
-            !wait_bar<true>(S, &S.x_empty[sb ^ 1], (uint32_t)((i - 1) >> 1) & 1u, a.err, 17))
-          failed = true;
+            !wait_bar<true>(S, &S.x_empty[sb ^ 1][q4], (uint32_t)((i - 1) >> 1) & 1u, a.err, 17))
+          break;
         __syncwarp();
         uint8_t* xo = S.xout[sb % Smem::XOUT_N];
 #pragma unroll
         for (int k = 0; k < HALF_T / 8; ++k)
           *reinterpret_cast<uint4*>(xo + sw64(row, k)) = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         fence_proxy_async_smem();
-        if (!named_barrier_and(SENDER_BAR, NSEND, !failed)) break;  // the PT warps leave together
-        if (leader) bulk_s2peer(peer_xin + sb * X_BYTES, xo, X_BYTES, peer_xfull + 8u * sb);
+        __syncwarp();
+        if (lane == 0) bulk_s2peer(peer_xin + sb * X_BYTES, xo + X_Q * q4, X_Q, peer_xfull + BAR_SB * sb);
         if constexpr (kQuant) {
           // page i+2's operands (its stage was last read by page i+2-KV_ST's P.V)
           if (x + 2 < x1) {
             rn.advance(prefix, seq_c, x + 2);
-            if (!dequant(i + 2, min(TILE, rn.n - TILE * (x + 2 - rn.start)))) failed = true;
+            if (!dequant(i + 2, min(TILE, rn.n - TILE * (x + 2 - rn.start)))) break;
           }
         }
       }

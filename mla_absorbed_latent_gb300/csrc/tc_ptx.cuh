@@ -184,7 +184,7 @@ __device__ __forceinline__ void fence_after_sync() {
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (>> 4), descriptor version 1 (bits 46-47), swizzle mode in
 // bits 61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
-constexpr uint32_t SWIZZLE_128B = 2, SWIZZLE_64B = 4;
+constexpr uint32_t SWIZZLE_128B = 2, SWIZZLE_64B = 4, SWIZZLE_32B = 6;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t swizzle) {
   uint64_t d = 0;
