@@ -87,7 +87,7 @@ constexpr uint32_t X_BYTES = 128 * HALF_T * 2;                // 8,192: fp16 par
 constexpr uint32_t X_Q = X_BYTES / 4;                         // 2,048: the rows of one TMEM lane quadrant
 constexpr uint32_t PG_Q = PG_BYTES / 4;                       // 1,024: one MT warp's rows of its P tile
 constexpr uint32_t SL_Q = 32 * 4;                             // 128: one MT warp's message (a float per head)
-constexpr uint32_t PIN_Q = 2 * (PG_Q + SL_Q);                 // from the peer's two MT warps of a quadrant
+constexpr uint32_t PIN_Q = 2 * SL_Q;                          // messages from the peer's two MT warps of a quadrant
 constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
@@ -322,13 +322,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.s_full[s], 1);
       mbar_init(&S.s_free[s], 12);  // every softmax warp
-      mbar_init(&S.p_full[s], 8);  // the MT warps' checks
+      mbar_init(&S.p_full[s], 8);  // each local MT warp once its P rows are written (expect_tx) + the peer's P rows
       mbar_init(&S.pv_done[s], 1);
       mbar_init(&S.pv_both[s], 2);   // this CTA's and the peer's P.V commits
       for (int q = 0; q < 4; ++q) {
         mbar_init(&S.x_full[s][q], 1);    // local expect_tx arrival + the peer's fp16 partial rows
         mbar_init(&S.x_empty[s][q], 2);   // one remote arrival per peer MT warp of the quadrant
-        mbar_init(&S.pin_full[s][q], 3);  // expect_tx + the 2 local MT warps' messages + the peer's P rows, messages
+        mbar_init(&S.pin_full[s][q], 3);  // expect_tx + the 2 local MT warps' messages + the peer's messages
         mbar_init(&S.mx_full[s][q], 3);   // the same for a segment's first-page maxima
       }
     }
@@ -639,13 +639,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto store_o = [&](int seg, float inv) {
       float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms;
 #pragma unroll 1
-      for (int k32 = 0; k32 < 4; ++k32) {
-        uint32_t o[32];
-        tmem_ld32(t_row + TM_O + 128 * ms + 32 * k32, o);
+      for (int k16 = 0; k16 < 8; ++k16) {
+        uint32_t o[16];
+        tmem_ld16(t_row + TM_O + 128 * ms + 16 * k16, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          st_global_v8(dst + 32 * k32 + 8 * k, u2f(o[8 * k]) * inv, u2f(o[8 * k + 1]) * inv, u2f(o[8 * k + 2]) * inv,
+        for (int k = 0; k < 2; ++k)
+          st_global_v8(dst + 16 * k16 + 8 * k, u2f(o[8 * k]) * inv, u2f(o[8 * k + 1]) * inv, u2f(o[8 * k + 2]) * inv,
                        u2f(o[8 * k + 3]) * inv, u2f(o[8 * k + 4]) * inv, u2f(o[8 * k + 5]) * inv,
                        u2f(o[8 * k + 6]) * inv, u2f(o[8 * k + 7]) * inv);
       }
@@ -656,14 +656,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (mt) {
       // ---------------------------------------------------------- MT warps
       // Exchange with the peer, per lane quadrant q4 and without group-wide
-      // barriers: this warp ships its own P rows (1 KB) and message (128 B) by
-      // bulk copies counted on the peer's pin_full[sb][q4]; the two local MT
-      // warps of the quadrant arrive on their own pin_full after writing their
-      // messages, so a check sees all four slices of its heads.
+      // barriers: this warp ships its own P rows (1 KB, counted on the peer's
+      // p_full[sb]) and message (128 B, on the peer's pin_full[sb][q4]) by bulk
+      // copies.  p_full[sb] completes once all 8 local MT warps wrote their P
+      // rows and the peer's 8 KB arrived: the P.V of the page needs nothing
+      // else.  The two local MT warps of a quadrant also arrive on their own
+      // pin_full after writing their messages, so a check sees all four slices
+      // of its heads.
       const bool qlead = ms == 0 && lane == 0;  // arms this quadrant's barriers each page
       const int slot = 2 * (int)rank + ms;      // this warp's slice among the four of a page
       const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0][q4]), peer);
       const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0][q4]), peer);
+      const uint32_t peer_pfull = mapa(smem_u32(&S.p_full[0]), peer);
       const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[0][q4]), peer);
       const uint32_t peer_p = mapa(smem_u32(&S.p[0][slot][0]), peer) + PG_Q * q4;
       const uint32_t peer_msg = mapa(smem_u32(&S.msgs[0][slot][0]), peer) + SL_Q * q4;
@@ -675,64 +679,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t prow = (uint32_t)row * 32;
       auto punit = [&](int k) -> uint32_t { return prow + ((uint32_t)(k ^ ((row >> 2) & 1)) << 4); };
       // softmax state of this head (lane), log2 domain:
-      //  m_ref      reference of the P written from now on
-      //  l          sum of this slice's p over the segment so far, in m_ref
-      //  alpha_due  factor by which P of the page after the last checked one
-      //             and O must still be rescaled (a reference move), 1 if none
-      float m_ref = -INFINITY, l = 0.f, alpha_due = 1.f;
+      //  m_ref       reference of the P written from now on
+      //  l           sum of this slice's p over the segment so far, in m_ref
+      //  alpha_prev  factor of the reference move made at the last check (1 if none)
+      float m_ref = -INFINITY, l = 0.f, alpha_prev = 1.f;
       int fcnt0 = 0, fcnt1 = 0;  // first pages seen per page parity (phases of mx_full)
-      // lagged check of page j: the peer's P rows and the four messages have
-      // arrived -> decide reference moves, rescale what page j still needs,
-      // release its P.V; at a segment end write the segment's output.  ref_j:
-      // the reference page j's P was written in.
+      // check of page j, at the end of page j+1 (so it waits for nothing in
+      // the common case): the four slice messages of page j have arrived.  If
+      // page j's maximum exceeded its reference by more than RESCALE_LOG2 the
+      // reference moves: the P of pages <= j+1 is already in the old one, so O
+      // is rescaled once page j+1's P.V has completed (before page j+2's, which
+      // needs this warp's next P), and l with it.  At a segment end the output
+      // is written.  ref_j: the reference page j's P was written in.
       auto check = [&](int j, bool j_last, int seg, float ref_j) -> bool {
         const int jb = j & 1;
         bool ok = wait_bar<true>(S, &S.pin_full[jb][q4], (uint32_t)(j >> 1) & 1u, a.err, 20);
         __syncwarp();
         const float m0 = S.msgs[jb][0][row], m1 = S.msgs[jb][1][row], m2 = S.msgs[jb][2][row],
                     m3 = S.msgs[jb][3][row];
-        // a move decided at the previous check: page j's P (this slice's
-        // tokens of both CTAs, this CTA's copy) and O (after page j-1's P.V) go
-        // to the new reference
-        const float alpha = alpha_due;
-        alpha_due = 1.f;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_bar<false>(S, &S.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.err, 21)) ok = false;
-          __syncwarp();
-          fence_after_sync();
-          scale_o(alpha);
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint8_t* pt = S.p[jb][2 * hf + ms];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              uint4* u = reinterpret_cast<uint4*>(pt + punit(k));
-              uint4 v = *u;
-              v.x = scale_bf16x2(v.x, alpha); v.y = scale_bf16x2(v.y, alpha);
-              v.z = scale_bf16x2(v.z, alpha); v.w = scale_bf16x2(v.w, alpha);
-              *u = v;
-            }
-          }
-          fence_proxy_async_smem();
-          fence_before_sync();
-        }
         if (!j_last) {
           // page j's maximum over all four slices against the reference it used
           const float m_comb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+          float alpha = 1.f;
           if (m_comb > ref_j + RESCALE_LOG2) {
             const float m_new = fmaxf(m_comb, m_ref);
-            alpha_due = ex2(m_ref - m_new);  // for page j+1's P and O, at the next check
-            l *= alpha_due;                  // the sums so far (pages <= j+1)
-            m_ref = m_new;                   // pages from j+2 on
+            alpha = ex2(m_ref - m_new);
+            l *= alpha;  // the sums of pages <= j+1
+            m_ref = m_new;  // pages from j+2 on
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.p_full[jb]);
-        if (j_last) {
-          // the four slices' sums, in page j's reference; O is in that
-          // reference times alpha after a move applied above
+          alpha_prev = alpha;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            if (!wait_bar<false>(S, &S.pv_done[(j + 1) & 1], ((j + 1) >> 1) & 1, a.err, 21)) ok = false;
+            __syncwarp();
+            fence_after_sync();
+            scale_o(alpha);
+            fence_before_sync();
+          }
+        } else {
+          // the four slices' sums were sent before the check of page j-1, so
+          // they miss that check's move; O has it
           const float Lm = (m0 + m1) + (m2 + m3);
-          const float L = alpha * Lm;
+          const float L = alpha_prev * Lm;
+          alpha_prev = 1.f;
           if (!wait_bar<false>(S, &S.pv_done[jb], (uint32_t)(j >> 1) & 1u, a.err, 22)) ok = false;
           __syncwarp();
           fence_after_sync();
@@ -757,7 +745,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
         if (qlead) {
           mbar_arrive_expect_tx(&S.x_full[sb][q4], X_Q);     // the peer's partials of my tokens, these rows
-          mbar_arrive_expect_tx(&S.pin_full[sb][q4], PIN_Q);  // the peer's P rows and messages
+          mbar_arrive_expect_tx(&S.pin_full[sb][q4], PIN_Q);  // the peer's messages
           if (first) mbar_arrive_expect_tx(&S.mx_full[sb][q4], 2 * SL_Q);  // the peer's first-page maxima
         }
         // ---- this CTA's partial scores of my tokens; the S buffer is released
@@ -844,9 +832,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          bulk_s2peer(peer_p + P_SB * sb, pm + PG_Q * q4, PG_Q, peer_pin + BAR_SB * sb);
+          bulk_s2peer(peer_p + P_SB * sb, pm + PG_Q * q4, PG_Q, peer_pfull + 8u * sb);
           bulk_s2peer(peer_msg + M_SB * sb, &S.msgs[sb][slot][32 * q4], SL_Q, peer_pin + BAR_SB * sb);
-          mbar_arrive(&S.pin_full[sb][q4]);  // our message, for our partner's check
+          mbar_arrive_expect_tx(&S.p_full[sb], PG_Q);  // our P rows; the peer's counterpart rows
+          mbar_arrive(&S.pin_full[sb][q4]);            // our message, for our partner's check
         }
         // the next page starts a new segment: every S of this one has completed
         // (this thread waited for each), so the next query may replace this one
