@@ -136,18 +136,24 @@ struct __align__(1024) SmemTC {
   static constexpr int XOUT_N = FMT == MLA_FMT_BF16 ? 2 : 1;
   uint8_t xout[XOUT_N][X_BYTES];  // ours of the peer's token half, same layout, shipped by one bulk copy
   uint8_t code[CODE_ST][CODE_BYTES];  // quantized formats: staged codes and scales of a page half
-  // per page parity, slice (2 rank + MT index) and head: the slice maximum
+  // per page (mod 4), slice (2 rank + MT index) and head: the slice maximum
   // (its sum at a segment end), ours written here and shipped, the peer's
-  // copied in; mxs: a segment's first-page maxima, exchanged before its P
-  float msgs[2][4][128];
-  float mxs[2][4][128];
+  // copied in.  Four pages deep: a check reads page j's one page later, and
+  // page j+4's arrive only after this CTA's P of page j+2, which comes after
+  // that check in every MT warp.  mxs: a segment's first-page slice maxima
+  // (bf16: both CTAs take the reference from the same rounded values),
+  // exchanged before its P; rewritten at the next segment start only after
+  // all four MT warps of the quadrant have read them (mx_empty)
+  float msgs[4][4][128];
+  uint16_t mxs[4][128];
   uint64_t kv_full[KV_ST], kv_empty[KV_ST];
   uint64_t code_full[CODE_ST], code_empty[CODE_ST];
   uint64_t q_ready;         // quantized: q_lat half in TMEM (8 warp arrivals) + q_pe half in smem (1 arrival + bytes)
   uint64_t q_done, qpe_full;  // bf16: the segment's q_lat half copied into TMEM / its q_pe half into qpe
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2], pv_both[2];
-  uint64_t x_full[2][4], x_empty[2][4], pin_full[2][4], mx_full[2][4];  // per page parity and lane quadrant
+  uint64_t x_full[2][4], x_empty[2][4], pin_full[2][4];  // per page parity and lane quadrant
+  uint64_t mx_full[4], mx_empty[4];  // per lane quadrant, one phase per segment start
   uint64_t o_free, mma_done[3];
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -329,10 +335,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init(&S.x_full[s][q], 1);    // local expect_tx arrival + the peer's fp16 partial rows
         mbar_init(&S.x_empty[s][q], 2);   // one remote arrival per peer MT warp of the quadrant
         mbar_init(&S.pin_full[s][q], 3);  // expect_tx + the 2 local MT warps' messages + the peer's messages
-        mbar_init(&S.mx_full[s][q], 3);   // the same for a segment's first-page maxima
       }
     }
     mbar_init(&S.o_free, 8);  // the MT warps' epilogues
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&S.mx_full[q], 3);   // expect_tx + the 2 local MT warps' maxima + the peer's maxima
+      mbar_init(&S.mx_empty[q], 4);  // those maxima read by the 2 local and the 2 peer MT warps
+    }
     for (int k = 0; k < 3; ++k) mbar_init(&S.mma_done[k], 1);
     S.abort_flag = 0;
     fence_barrier_init();
@@ -668,12 +677,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t peer_xempty = mapa(smem_u32(&S.x_empty[0][q4]), peer);
       const uint32_t peer_pin = mapa(smem_u32(&S.pin_full[0][q4]), peer);
       const uint32_t peer_pfull = mapa(smem_u32(&S.p_full[0]), peer);
-      const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[0][q4]), peer);
+      const uint32_t peer_mxf = mapa(smem_u32(&S.mx_full[q4]), peer);
+      const uint32_t peer_mxe = mapa(smem_u32(&S.mx_empty[q4]), peer);
       const uint32_t peer_p = mapa(smem_u32(&S.p[0][slot][0]), peer) + PG_Q * q4;
       const uint32_t peer_msg = mapa(smem_u32(&S.msgs[0][slot][0]), peer) + SL_Q * q4;
-      const uint32_t peer_mx = mapa(smem_u32(&S.mxs[0][slot][0]), peer) + SL_Q * q4;
+      constexpr uint32_t MX_Q = 32 * 2;  // one MT warp's first-page maxima (bf16)
+      const uint32_t peer_mx = mapa(smem_u32(&S.mxs[slot][0]), peer) + MX_Q * q4;
       constexpr uint32_t BAR_SB = 4 * 8;                    // bytes between the page parities' quadrant barriers
-      constexpr uint32_t P_SB = 4 * PG_BYTES, M_SB = 4 * 128 * 4;  // bytes between page parities
+      constexpr uint32_t P_SB = 4 * PG_BYTES, M_SB = 4 * 128 * 4;  // bytes between pages of the P / message rings
       const int tok0 = HALF_T * (int)rank + TPW * ms;  // first page token of this thread's slice
       // offset of 16-byte unit k (8 tokens) of this lane's row in a P tile
       const uint32_t prow = (uint32_t)row * 32;
@@ -683,7 +694,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       //  l           sum of this slice's p over the segment so far, in m_ref
       //  alpha_prev  factor of the reference move made at the last check (1 if none)
       float m_ref = -INFINITY, l = 0.f, alpha_prev = 1.f;
-      int fcnt0 = 0, fcnt1 = 0;  // first pages seen per page parity (phases of mx_full)
+      int fcnt = 0;  // segment starts seen (phases of mx_full, mx_empty)
       // check of page j, at the end of page j+1 (so it waits for nothing in
       // the common case): the four slice messages of page j have arrived.  If
       // page j's maximum exceeded its reference by more than RESCALE_LOG2 the
@@ -695,8 +706,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int jb = j & 1;
         bool ok = wait_bar<true>(S, &S.pin_full[jb][q4], (uint32_t)(j >> 1) & 1u, a.err, 20);
         __syncwarp();
-        const float m0 = S.msgs[jb][0][row], m1 = S.msgs[jb][1][row], m2 = S.msgs[jb][2][row],
-                    m3 = S.msgs[jb][3][row];
+        const int jm = j & 3;
+        const float m0 = S.msgs[jm][0][row], m1 = S.msgs[jm][1][row], m2 = S.msgs[jm][2][row],
+                    m3 = S.msgs[jm][3][row];
         if (!j_last) {
           // page j's maximum over all four slices against the reference it used
           const float m_comb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
@@ -746,7 +758,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (qlead) {
           mbar_arrive_expect_tx(&S.x_full[sb][q4], X_Q);     // the peer's partials of my tokens, these rows
           mbar_arrive_expect_tx(&S.pin_full[sb][q4], PIN_Q);  // the peer's messages
-          if (first) mbar_arrive_expect_tx(&S.mx_full[sb][q4], 2 * SL_Q);  // the peer's first-page maxima
+          if (first) mbar_arrive_expect_tx(&S.mx_full[q4], 2 * MX_Q);  // the peer's first-page maxima
         }
         // ---- this CTA's partial scores of my tokens; the S buffer is released
         if (!wait_bar<false>(S, &S.s_full[sb], ph, a.err, 9)) break;
@@ -789,17 +801,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- the reference of this page's P
         if (first) {
           // segment start: the exact row maximum over the page's four slices
-          S.mxs[sb][slot][row] = mraw;
+          const uint32_t fph = (uint32_t)(fcnt++) & 1u;
+          if (!wait_bar<true>(S, &S.mx_empty[q4], fph ^ 1u, a.err, 18)) break;  // the last ones were read
+          __syncwarp();
+          {
+            const __nv_bfloat16 mb = __float2bfloat16_rn(mraw);
+            S.mxs[slot][row] = *reinterpret_cast<const uint16_t*>(&mb);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            bulk_s2peer(peer_mx + M_SB * sb, &S.mxs[sb][slot][32 * q4], SL_Q, peer_mxf + BAR_SB * sb);
-            mbar_arrive(&S.mx_full[sb][q4]);
+            bulk_s2peer(peer_mx, &S.mxs[slot][32 * q4], MX_Q, peer_mxf);
+            mbar_arrive(&S.mx_full[q4]);
           }
-          const int fc = sb ? fcnt1++ : fcnt0++;
-          if (!wait_bar<true>(S, &S.mx_full[sb][q4], (uint32_t)fc & 1u, a.err, 19)) break;
+          if (!wait_bar<true>(S, &S.mx_full[q4], fph, a.err, 19)) break;
           __syncwarp();
-          m_ref = fmaxf(fmaxf(S.mxs[sb][0][row], S.mxs[sb][1][row]), fmaxf(S.mxs[sb][2][row], S.mxs[sb][3][row]));
+          m_ref = fmaxf(fmaxf(bf16_to_f(S.mxs[0][row]), bf16_to_f(S.mxs[1][row])),
+                        fmaxf(bf16_to_f(S.mxs[2][row]), bf16_to_f(S.mxs[3][row])));
+          __syncwarp();
+          if (lane == 0) {  // both CTAs may write their maxima of the next segment start
+            mbar_arrive(&S.mx_empty[q4]);
+            mbar_arrive_remote_relaxed(peer_mxe);
+          }
           l = 0.f;
         }
         if (mraw - m_ref > RANGE_LOG2) raise_error(a.err, MLA_ERR_RANGE, 0);
@@ -824,7 +847,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int k = 0; k < 2; ++k)
           *reinterpret_cast<uint4*>(pm + punit(k)) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         // message: this slice's maximum, or its sum at a segment's last page
-        S.msgs[sb][slot][row] = last ? l : mraw;
+        S.msgs[i & 3][slot][row] = last ? l : mraw;
         // every value read from the exchange buffer has been used by the store
         // above (mraw depends on all of them), so the peer may refill it
         __syncwarp();
@@ -833,7 +856,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           bulk_s2peer(peer_p + P_SB * sb, pm + PG_Q * q4, PG_Q, peer_pfull + 8u * sb);
-          bulk_s2peer(peer_msg + M_SB * sb, &S.msgs[sb][slot][32 * q4], SL_Q, peer_pin + BAR_SB * sb);
+          bulk_s2peer(peer_msg + M_SB * (i & 3), &S.msgs[i & 3][slot][32 * q4], SL_Q, peer_pin + BAR_SB * sb);
           mbar_arrive_expect_tx(&S.p_full[sb], PG_Q);  // our P rows; the peer's counterpart rows
           mbar_arrive(&S.pin_full[sb][q4]);            // our message, for our partner's check
         }
