@@ -747,10 +747,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int pend_i = -1, pend_seg = 0;
       bool pend_last = false;
       float pend_ref = 0.f;
-      for (int x = x0, i = 0; x < x1; ++x, ++i) {
+      // one pass more than there are pages: the last one only checks the last
+      // page (a single call site keeps the loop's code compact)
+      for (int x = x0, i = 0; x <= x1; ++x, ++i) {
+        bool last = false;
+        if (x < x1) {
         rc.advance(prefix, seq_c, x);
         const bool first = (x == x0) || (x == rc.start);
-        const bool last = (x + 1 == x1) || (x + 1 == rc.end);
+        last = (x + 1 == x1) || (x + 1 == rc.end);
         const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
         const int sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
@@ -867,13 +871,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           nx.advance(prefix, seq_c, x + 1);
           load_query(nx.b);
         }
+        }
         if (pend_i >= 0 && !check(pend_i, pend_last, pend_seg, pend_ref)) break;
+        if (x == x1) break;
         pend_i = i;
         pend_last = last;
         pend_seg = worker + rc.b;
         pend_ref = m_ref;
       }
-      if (!S.abort_flag && pend_i >= 0) (void)check(pend_i, pend_last, pend_seg, pend_ref);
     } else {
       // ---------------------------------------------------------- PT warps
       constexpr int NSEND = 128;                       // PT threads
