@@ -182,23 +182,33 @@ struct TcArgs {
 // MLA_ERR_TIMEOUT and raises the abort flag of this CTA and of its peer) or
 // once an abort was raised.  The abort flag and the clock are checked every 8
 // probes.
-template <bool kCluster, class Smem>
-__device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity, int* err, int where) {
-  auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (probe()) return true;
+template <bool kCluster>
+__device__ __forceinline__ bool probe_bar(uint64_t* bar, uint32_t parity) {
+  return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+// the polling part, out of line: waits are many and usually end at the first
+// probe, so the inlined part stays one instruction sequence per call site
+template <bool kCluster>
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                           int where) {
   const long long t0 = clock64();
   for (uint32_t k = 1;; ++k) {
-    if (probe()) return true;
+    if (probe_bar<kCluster>(bar, parity)) return true;
     if ((k & 7) == 0) {
-      if (S.abort_flag) return false;
+      if (*abort_flag) return false;
       if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-        S.abort_flag = 1;
-        st_cluster_u32(mapa(smem_u32((const void*)&S.abort_flag), cluster_ctarank() ^ 1u), 1u);
+        *abort_flag = 1;
+        st_cluster_u32(mapa(smem_u32((const void*)abort_flag), cluster_ctarank() ^ 1u), 1u);
         raise_error(err, MLA_ERR_TIMEOUT, where);
         return false;
       }
     }
   }
+}
+template <bool kCluster, class Smem>
+__device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity, int* err, int where) {
+  if (probe_bar<kCluster>(bar, parity)) return true;
+  return wait_bar_slow<kCluster>(bar, parity, &S.abort_flag, err, where);
 }
 
 // row of the tile cursor: tiles [start, end) belong to row b of length n
