@@ -182,6 +182,9 @@ struct TcArgs {
 // MLA_ERR_TIMEOUT and raises the abort flag of this CTA and of its peer) or
 // once an abort was raised.  The abort flag and the clock are checked every 8
 // probes.
+// error reports from hot loops, out of line
+__device__ __noinline__ void report_error(int* err, int code, int info) { raise_error(err, code, info); }
+
 template <bool kCluster>
 __device__ __forceinline__ bool probe_bar(uint64_t* bar, uint32_t parity) {
   return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
@@ -199,7 +202,7 @@ __device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, volat
       if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
         *abort_flag = 1;
         st_cluster_u32(mapa(smem_u32((const void*)abort_flag), cluster_ctarank() ^ 1u), 1u);
-        raise_error(err, MLA_ERR_TIMEOUT, where);
+        report_error(err, MLA_ERR_TIMEOUT, where);
         return false;
       }
     }
@@ -211,6 +214,37 @@ __device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity
   return wait_bar_slow<kCluster>(bar, parity, &S.abort_flag, err, where);
 }
 
+// Rare per-lane TMEM passes over 128 O columns, out of line (whole warps call
+// them): times f in place (a reference move) ...
+__device__ __noinline__ void scale_o_cols(uint32_t taddr, float f) {
+#pragma unroll 1
+  for (int k16 = 0; k16 < 8; ++k16) {
+    uint32_t o[16];
+    const uint32_t col = taddr + 16 * k16;
+    tmem_ld16(col, o);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+    tmem_st16(col, o);
+  }
+  tmem_st_wait();
+}
+// ... and times inv into 128 floats at dst (a segment's partial output), 32
+// bytes per store (a whole sector per lane)
+__device__ __noinline__ void store_o_cols(uint32_t taddr, float* dst, float inv) {
+#pragma unroll 1
+  for (int k16 = 0; k16 < 8; ++k16) {
+    uint32_t o[16];
+    tmem_ld16(taddr + 16 * k16, o);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      st_global_v8(dst + 16 * k16 + 8 * k, __uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv,
+                   __uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv,
+                   __uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv,
+                   __uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+  }
+}
 // row of the tile cursor: tiles [start, end) belong to row b of length n
 struct RowCursor {
   int b, start, end, n;
@@ -453,7 +487,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         ok = wait_bar<false>(S, kQuant ? &S.code_empty[st] : &S.kv_empty[st], ((u / RING) & 1) ^ 1, a.err, 2);
         if (ok) {
           if (page < 0 || page >= a.num_pages) {
-            raise_error(a.err, MLA_ERR_BOUNDS, page);
+            report_error(a.err, MLA_ERR_BOUNDS, page);
             page = 0;
           }
           if constexpr (!kQuant) {
@@ -639,35 +673,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // page.
     const bool mt = sub < 2;
     const int ms = sub & 1;                   // MT: slice index within the token half
-    // O row of this lane, MT slice ms's 128 columns, times f
-    auto scale_o = [&](float f) {
-#pragma unroll 1
-      for (int k16 = 0; k16 < 8; ++k16) {
-        uint32_t o[16];
-        const uint32_t col = t_row + TM_O + 128 * ms + 16 * k16;
-        tmem_ld16(col, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) o[k] = f2u(u2f(o[k]) * f);
-        tmem_st16(col, o);
-      }
-      tmem_st_wait();
-    };
-    // the same columns times inv -> the segment's partial output (this CTA's
-    // latent half), 32 bytes per store (a whole sector per lane)
+    auto scale_o = [&](float f) { scale_o_cols(t_row + TM_O + 128 * ms, f); };
     auto store_o = [&](int seg, float inv) {
-      float* dst = a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms;
-#pragma unroll 1
-      for (int k16 = 0; k16 < 8; ++k16) {
-        uint32_t o[16];
-        tmem_ld16(t_row + TM_O + 128 * ms + 16 * k16, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          st_global_v8(dst + 16 * k16 + 8 * k, u2f(o[8 * k]) * inv, u2f(o[8 * k + 1]) * inv, u2f(o[8 * k + 2]) * inv,
-                       u2f(o[8 * k + 3]) * inv, u2f(o[8 * k + 4]) * inv, u2f(o[8 * k + 5]) * inv,
-                       u2f(o[8 * k + 6]) * inv, u2f(o[8 * k + 7]) * inv);
-      }
+      store_o_cols(t_row + TM_O + 128 * ms, a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms, inv);
     };
 
     bool failed = false;
@@ -839,7 +847,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           l = 0.f;
         }
-        if (mraw - m_ref > RANGE_LOG2) raise_error(a.err, MLA_ERR_RANGE, 0);
+        if (mraw - m_ref > RANGE_LOG2) report_error(a.err, MLA_ERR_RANGE, 0);
         // p = 2^(s - m_ref), rounded to bf16 for the MMA (exponent capped at
         // RANGE_LOG2, beyond which the range error above is reported)
         uint32_t pk[TPW / 2];
