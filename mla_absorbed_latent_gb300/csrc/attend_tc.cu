@@ -272,7 +272,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
   static_assert(N == 16 || N == 32, "16 or 32 columns");
   if constexpr (N == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
 }
-__device__ __forceinline__ uint32_t f2u(float v) { return __float_as_uint(v); }
 // two fp16 in one 32-bit word <-> two floats, in registers (low half = first value)
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -290,10 +289,6 @@ __device__ __forceinline__ float fp16_clamp(float v) { return fminf(fmaxf(v, -FP
 // byte offset of 16-byte unit u (0..3, 8 tokens) of row r in a 64B-swizzled tile of 64-byte rows
 // (the P half tiles, read by the tensor core, and the fp16 exchange tiles)
 __device__ __forceinline__ uint32_t sw64(int r, int u) { return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4)); }
-// two bf16 in one word times f, rounded again to bf16
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float f) {
-  return pack_bf16x2(__uint_as_float(v << 16) * f, __uint_as_float(v & 0xffff0000u) * f);
-}
 
 // ---- dequantization ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 block
 // quantizers): x = code * s (INT8), x = code * s + z (INT4), evaluated in fp32

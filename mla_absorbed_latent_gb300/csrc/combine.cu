@@ -53,9 +53,8 @@ struct CombLayout {
 };
 
 // bounded wait for the combine kernel: false after the time limit or once
-// another thread of the CTA gave up
-__device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+// another thread of the CTA gave up (the polling loop out of line)
+__device__ __noinline__ bool cwait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int where) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t k = 1;; ++k) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -68,6 +67,10 @@ __device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, volatile i
       }
     }
   }
+}
+__device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return cwait_slow(bar, parity, abort, err, where);
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {

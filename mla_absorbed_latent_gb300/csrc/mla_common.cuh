@@ -116,13 +116,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with `parity` to complete; false after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// (the polling loop out of line: call sites stay small, most waits end at the
+// first probe)
+__device__ __noinline__ static bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 
 // 1-D bulk async copy global -> shared, completion counted on `bar` (bytes).
