@@ -20,13 +20,16 @@
 //    its half of q_lat in TMEM and its half of q_pe in shared memory as A
 //    operands;
 //  * sends the peer the partial scores of the peer's 32 tokens, already in log2
-//    units, as fp16 (8 KB: written to a local staging tile, then one bulk
-//    shared-to-peer copy counted on the peer's transaction barrier);
+//    units, as fp16 (8 KB: each lane-quadrant warp writes its 32 heads' rows to
+//    a local staging tile and ships them, 2 KB, with one bulk shared-to-peer
+//    copy counted on the peer's transaction barrier of that quadrant);
 //  * adds the peer's partial to its own for my tokens, forms P = 2^(s - m_ref)
-//    in bf16 for those 32 columns of its P tile and copies them (8 KB) with a
-//    per-head message (slice maxima, or slice sums at a segment end, 1 KB) into
-//    the peer's P tile;
-//  * once both token halves of P are in place, issues O_half += P . V_half.
+//    in bf16 for those 32 columns (two 16-token tiles of its P) and ships them
+//    (each softmax warp its own 1 KB of rows) with a per-head message (its
+//    slice maximum, or its slice sum at a segment end);
+//  * issues O_half += P . V_half as soon as both token halves of P are in
+//    place: one transaction barrier counts the local warps' P and the peer's
+//    8 KB, so a page's P.V waits for nothing else.
 // Distributed shared memory moves ~14.5 bytes per cycle per SM each way, less
 // than the ~23 bytes per cycle per SM that HBM delivers, so the 17 KB per page
 // each way (against 36 KB of cache streamed) is the design's budget: fp32
@@ -35,12 +38,14 @@
 // The reference maximum.  Both CTAs must write P in the same reference m_ref
 // (their halves feed one accumulator).  At a segment's first page the pair
 // swaps its slice maxima and both take the exact maximum.  Later pages use the
-// running reference; one page later, when the peer's message has arrived, both
-// CTAs see the same four slice maxima and move the reference only when it grew
-// by more than 2^8: O and the next page's P (already written in the old
-// reference) are then rescaled by the same factor on both sides.  A score more
-// than 2^100 above its reference is capped there and reported as
-// MLA_ERR_RANGE (the result stays finite; it is no longer exact).
+// running reference; at the end of the next page, when all four slice
+// messages of a page have arrived, both CTAs move the reference if the page
+// maximum exceeded it by more than 2^8: the P of the pages written so far is
+// already in the old reference, so O is rescaled by the same factor on both
+// sides once the last of those pages' P.V has completed, before the next
+// page's P.V (which needs this CTA's next P).  A score more than 2^100 above
+// its reference is capped there and reported as MLA_ERR_RANGE (the result
+// stays finite; it is no longer exact).
 //
 // MMA issue.  A tcgen05.mma blocks its issuing thread while an MMA on the same
 // accumulator is in flight, so three threads issue MMAs: S of even pages, S of
@@ -52,11 +57,14 @@
 // and the two S issuers (even / odd pages), assigned per rank; warp 1 owns
 // TMEM.  TMEM lane quadrant q = warp % 4 holds heads 32q..32q+31 and is served
 // by three softmax warps: two "MT" warps own 16 of my tokens each (and 128
-// columns each of O and of the query), one "PT" warp ships the partial scores
-// of the peer's tokens and, for quantized pools, dequantizes the page two
-// ahead.  Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, raises the
-// abort flag of both CTAs, lets in-flight copies and MMAs land, frees TMEM and
-// returns.
+// columns each of O), one "PT" warp ships the partial scores of the peer's
+// tokens and, for quantized pools, dequantizes the page two ahead.  Exchange
+// buffers and barriers are per lane quadrant, so the page loop has no
+// group-wide barrier.  Every wait is bounded; its polling loop is out of line
+// (most waits end at the first probe, and the kernel's code must stay small:
+// instruction fetch is on the per-page chain).  A timeout records
+// MLA_ERR_TIMEOUT, raises the abort flag of both CTAs, lets in-flight copies
+// and MMAs land, frees TMEM and returns.
 //
 // Tensor memory (512 columns): O [0,256), q_lat half [256,384), S double
 // buffer [384,512).
