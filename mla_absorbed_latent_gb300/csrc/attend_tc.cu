@@ -222,9 +222,11 @@ __device__ __forceinline__ bool wait_bar(Smem& S, uint64_t* bar, uint32_t parity
   return wait_bar_slow<kCluster>(bar, parity, &S.abort_flag, err, where);
 }
 
-// Rare per-lane TMEM passes over 128 O columns, out of line (whole warps call
-// them): times f in place (a reference move) ...
+// Per-lane TMEM passes over 128 O columns (whole warps call them): times f in
+// place (a reference move, rare: out of line; the warp reconverges first, as
+// the tcgen05 loads and stores are warp-aligned) ...
 __device__ __noinline__ void scale_o_cols(uint32_t taddr, float f) {
+  __syncwarp();
 #pragma unroll 1
   for (int k16 = 0; k16 < 8; ++k16) {
     uint32_t o[16];
@@ -237,20 +239,48 @@ __device__ __noinline__ void scale_o_cols(uint32_t taddr, float f) {
   }
   tmem_st_wait();
 }
-// ... and times inv into 128 floats at dst (a segment's partial output), 32
-// bytes per store (a whole sector per lane)
-__device__ __noinline__ void store_o_cols(uint32_t taddr, float* dst, float inv) {
+// ... and times inv into 128 floats at dst (a segment's partial output; dst
+// of lane l is row l).  Each 128-byte line of the rows is written by four
+// lanes: the lanes of a group of four transpose their four rows' 32-byte
+// chunks (two xor-shuffle stages), so a store instruction covers eight whole
+// lines instead of 32 sectors of 32 lines (the store is transaction-bound).
+// Inlined: an out-of-line copy called from the segment-end branch returned
+// wrong data.
+__device__ __forceinline__ void store_o_cols(uint32_t taddr, float* dst, float inv) {
+  const int lane = threadIdx.x & 31, j = lane & 3;
 #pragma unroll 1
-  for (int k16 = 0; k16 < 8; ++k16) {
-    uint32_t o[16];
-    tmem_ld16(taddr + 16 * k16, o);
+  for (int line = 0; line < 4; ++line) {
+    uint32_t raw[32];
+    tmem_ld32(taddr + 32 * line, raw);
     tmem_ld_wait();
+    float c[4][8];  // c[k]: chunk k (8 floats) of a row of this group
 #pragma unroll
-    for (int k = 0; k < 2; ++k)
-      st_global_v8(dst + 16 * k16 + 8 * k, __uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv,
-                   __uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv,
-                   __uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv,
-                   __uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[k][e] = __uint_as_float(raw[8 * k + e]) * inv;
+    // 4 x 4 transpose of chunks across the group: afterwards c[s] of lane j is
+    // chunk j of row s of the group
+#pragma unroll
+    for (int b = 2; b >= 1; b >>= 1) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (t & b) continue;  // t: the slot pair (t, t | b)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool hi = (j & b) != 0;
+          const float send = hi ? c[t][e] : c[t | b][e];
+          const float got = __shfl_xor_sync(0xffffffffu, send, b);
+          if (hi) c[t][e] = got; else c[t | b][e] = got;
+        }
+      }
+    }
+    // row 4(lane/4) + s of the warp, chunk j of this line
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      float* p = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), (lane & ~3) | s4)) +
+                 32 * line + 8 * j;
+      st_global_v8(p, c[s4][0], c[s4][1], c[s4][2], c[s4][3], c[s4][4], c[s4][5], c[s4][6], c[s4][7]);
+    }
   }
 }
 // row of the tile cursor: tiles [start, end) belong to row b of length n
