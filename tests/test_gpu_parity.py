@@ -311,6 +311,35 @@ def test_decode_score_beyond_tracked_range_is_reported():
     assert bool(torch.all(torch.isfinite(dev.out.float())))
 
 
+def test_decode_reference_moves_keep_the_result_exact():
+    """H=128: tokens of later pages whose RoPE keys are 3x one head's q_pe lift
+    that head's scores by about 20 log2 units over the first page's maximum, so
+    the kernel moves its running reference (rescaling O) while staying far
+    inside its tracked range; the output must still match the oracle on the
+    same modified cache."""
+    import mla_absorbed_latent_gb300 as mla
+    n = 64 * 304
+    prob = make_problem(128, [n], seed=7, paged=False)
+    dev = DeviceDecode(prob)
+    qn = synth.bf16_bits_to_f32(prob.q_nope)
+    qp = synth.bf16_bits_to_f32(prob.q_pe)
+    c, p = prob.sequence(0)
+    C, P = synth.bf16_bits_to_f32(c).astype(np.float64), synth.bf16_bits_to_f32(p).astype(np.float64)
+    for head, token, lam in ((0, 64 * 3 + 5, 3.0), (1, 64 * 9 + 40, 3.0), (0, 64 * 40 + 1, 5.0)):
+        bits = synth.f32_to_bf16_bits((lam * qp[0, head]).astype(np.float32))
+        P[token] = synth.bf16_bits_to_f32(bits)
+        page, slot = divmod(token, 64)
+        off = int(dev.page_table[0, page]) * dev.page_bytes + slot * 1152 + 1024  # the token's k_pe
+        dev.pool[off:off + 128] = torch.from_numpy(bits.view(np.uint8).copy()).to(dev.pool.device)
+    dev.decode()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+    Wuk, Wuv = weights(prob)
+    ref = O.absorbed_decode(qn[0], qp[0], C, P, Wuk, Wuv, prob.scale)[0]
+    assert_close(_out_f64(dev.out)[0], ref)
+
+
 def test_decode_seqlen_over_capacity_reports_bounds():
     import mla_absorbed_latent_gb300 as mla
     prob = make_problem(16, [100], seed=4)
