@@ -60,7 +60,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, const 
 __global__ void __launch_bounds__(THREADS, 2)
     attend_cc_kernel(const uint16_t* __restrict__ q_cat, int H, int num_pages, const uint8_t* __restrict__ pages,
                      const int32_t* __restrict__ page_table, int max_pages, int B, float scale_log2,
-                     const int* __restrict__ plan, float* __restrict__ part_o, float* __restrict__ part_lse,
+                     const int* __restrict__ plan, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
                      int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SmemCC& S = *reinterpret_cast<SmemCC*>(smem_raw);
@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float inv = 1.f / S.l[h];
-        float2 val = make_float2(o[h][0] * inv, o[h][1] * inv);
-        reinterpret_cast<float2*>(part_o + ((size_t)seg * H + hg * HG + h) * DC)[tid] = val;
+        reinterpret_cast<uint32_t*>(part_o + ((size_t)seg * H + hg * HG + h) * DC)[tid] =
+            pack_bf16x2(o[h][0] * inv, o[h][1] * inv);  // partials are stored in bf16
       }
       if (tid < HG)
         part_lse[(size_t)seg * H + hg * HG + tid] = (S.m[tid] + log2f(S.l[tid])) * 0.69314718055994531f;
@@ -270,7 +270,7 @@ int attend_cc_workers(int num_sms) { return 2 * num_sms; }
 
 cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s) {
+                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (fmt != MLA_FMT_BF16) return cudaErrorNotSupported;
   const size_t smem = sizeof(SmemCC);
   cudaError_t e = cudaFuncSetAttribute(attend_cc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

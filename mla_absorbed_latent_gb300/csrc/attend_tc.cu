@@ -179,7 +179,7 @@ struct TcArgs {
   const uint16_t* q_cat;  // [B][128][576] bf16
   const int* plan;
   const int32_t* page_table;
-  float* part_o;
+  uint16_t* part_o;  // bf16 [segments][128][512]
   float* part_lse;
   int* err;
   int B, max_pages, num_pages;
@@ -239,25 +239,27 @@ __device__ __noinline__ void scale_o_cols(uint32_t taddr, float f) {
   }
   tmem_st_wait();
 }
-// ... and times inv into 128 floats at dst (a segment's partial output; dst
-// of lane l is row l).  Each 128-byte line of the rows is written by four
-// lanes: the lanes of a group of four transpose their four rows' 32-byte
-// chunks (two xor-shuffle stages), so a store instruction covers eight whole
-// lines instead of 32 sectors of 32 lines (the store is transaction-bound).
-// Inlined: an out-of-line copy called from the segment-end branch returned
-// wrong data.
-__device__ __forceinline__ void store_o_cols(uint32_t taddr, float* dst, float inv) {
+// ... and times inv, rounded to bf16, into 128 values at dst (a segment's
+// partial output; dst of lane l is row l).  Each 128-byte line of the rows is
+// written by four lanes: the lanes of a group of four transpose their four
+// rows' 32-byte chunks (two xor-shuffle stages), so a store instruction covers
+// eight whole lines instead of 32 sectors of 32 lines.  Inlined: an
+// out-of-line copy called from the segment-end branch returned wrong data.
+__device__ __forceinline__ void store_o_cols(uint32_t taddr, uint16_t* dst, float inv) {
   const int lane = threadIdx.x & 31, j = lane & 3;
 #pragma unroll 1
-  for (int line = 0; line < 4; ++line) {
-    uint32_t raw[32];
-    tmem_ld32(taddr + 32 * line, raw);
-    tmem_ld_wait();
-    float c[4][8];  // c[k]: chunk k (8 floats) of a row of this group
+  for (int line = 0; line < 2; ++line) {  // 64 columns = 128 bytes of bf16
+    uint32_t c[4][8];                      // c[k]: chunk k (16 values, 8 words) of a row of this group
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t raw[32];
+      tmem_ld32(taddr + 64 * line + 32 * hf, raw);
+      tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c[k][e] = __uint_as_float(raw[8 * k + e]) * inv;
+      for (int w = 0; w < 16; ++w)
+        c[2 * hf + w / 8][w % 8] =
+            pack_bf16x2(__uint_as_float(raw[2 * w]) * inv, __uint_as_float(raw[2 * w + 1]) * inv);
+    }
     // 4 x 4 transpose of chunks across the group: afterwards c[s] of lane j is
     // chunk j of row s of the group
 #pragma unroll
@@ -268,8 +270,8 @@ __device__ __forceinline__ void store_o_cols(uint32_t taddr, float* dst, float i
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const bool hi = (j & b) != 0;
-          const float send = hi ? c[t][e] : c[t | b][e];
-          const float got = __shfl_xor_sync(0xffffffffu, send, b);
+          const uint32_t send = hi ? c[t][e] : c[t | b][e];
+          const uint32_t got = __shfl_xor_sync(0xffffffffu, send, b);
           if (hi) c[t][e] = got; else c[t | b][e] = got;
         }
       }
@@ -277,9 +279,12 @@ __device__ __forceinline__ void store_o_cols(uint32_t taddr, float* dst, float i
     // row 4(lane/4) + s of the warp, chunk j of this line
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
-      float* p = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), (lane & ~3) | s4)) +
-                 32 * line + 8 * j;
-      st_global_v8(p, c[s4][0], c[s4][1], c[s4][2], c[s4][3], c[s4][4], c[s4][5], c[s4][6], c[s4][7]);
+      uint16_t* p =
+          reinterpret_cast<uint16_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), (lane & ~3) | s4)) +
+          64 * line + 16 * j;
+      st_global_v8(reinterpret_cast<float*>(p), __uint_as_float(c[s4][0]), __uint_as_float(c[s4][1]),
+                   __uint_as_float(c[s4][2]), __uint_as_float(c[s4][3]), __uint_as_float(c[s4][4]),
+                   __uint_as_float(c[s4][5]), __uint_as_float(c[s4][6]), __uint_as_float(c[s4][7]));
     }
   }
 }
@@ -1110,7 +1115,7 @@ int attend_tc_workers(int num_sms) {
 
 cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s) {
+                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (H != 128 || workers < 1) return cudaErrorNotSupported;
   if (fmt != MLA_FMT_BF16 && fmt != MLA_FMT_INT8 && fmt != MLA_FMT_INT4) return cudaErrorNotSupported;
   if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling

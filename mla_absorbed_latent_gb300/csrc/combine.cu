@@ -9,8 +9,8 @@
 //
 // One CTA per (head h, group of RB rows).  The segments of a group's rows are
 // consecutive slots of the partial buffer (slot w + b for worker w, row b), so
-// for every 64-wide latent chunk TMA boxes bring that chunk of up to 80
-// segments at a time ([segments][64] fp32) into shared memory.  The merge threads (one
+// for every 64-wide latent chunk TMA boxes bring that chunk of up to 128
+// segments at a time ([segments][64] bf16) into shared memory.  The merge threads (one
 // per row and 8-dim unit) sum their row's segments with the softmax weights,
 // round o_lat once into a bf16 high part and a bf16 residual, and write both
 // as K-major 128B-swizzled operand tiles; one thread then issues the
@@ -29,9 +29,9 @@ using namespace tc;
 
 constexpr int KC = 64;                    // latent dims per chunk
 constexpr int NCHUNK = DC / KC;           // 8
-constexpr int SEGB = 80;                  // segments per partial tile (TMA box)
+constexpr int SEGB = 128;                 // segments per partial tile (TMA box)
 constexpr uint32_t W_TILE = DV * KC * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
-constexpr uint32_t P_TILE = SEGB * KC * 4;  // 20 KB: [80 segments][64 dims] fp32
+constexpr uint32_t P_TILE = SEGB * KC * 2;  // 16 KB: [128 segments][64 dims] bf16
 constexpr int WST = 2, PST = 3, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
 
 template <int RB>
@@ -233,18 +233,17 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
           ok = false;
           break;
         }
-        const float* tile = reinterpret_cast<const float*>(sm + L::OFF_P + st * P_TILE);
+        const uint16_t* tile = reinterpret_cast<const uint16_t*>(sm + L::OFF_P + st * P_TILE);
         const int base = s_lo + SEGB * sub;
         const int sa = max(rs.x, base), sz = min(rs.y, base + SEGB - 1);
         for (int s = sa; s <= sz; ++s) {
           const float wv = wgt[s - s_lo];
           if (wv == 0.f) continue;  // a slot no worker wrote (its contents are undefined)
-          const float4* v = reinterpret_cast<const float4*>(tile + (s - base) * KC + 8 * u);
-          const float4 x = v[0], y = v[1];
-          acc[0] = fmaf(wv, x.x, acc[0]); acc[1] = fmaf(wv, x.y, acc[1]);
-          acc[2] = fmaf(wv, x.z, acc[2]); acc[3] = fmaf(wv, x.w, acc[3]);
-          acc[4] = fmaf(wv, y.x, acc[4]); acc[5] = fmaf(wv, y.y, acc[5]);
-          acc[6] = fmaf(wv, y.z, acc[6]); acc[7] = fmaf(wv, y.w, acc[7]);
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + (s - base) * KC + 8 * u);  // 8 bf16
+          acc[0] = fmaf(wv, bf16lo(v.x), acc[0]); acc[1] = fmaf(wv, bf16hi(v.x), acc[1]);
+          acc[2] = fmaf(wv, bf16lo(v.y), acc[2]); acc[3] = fmaf(wv, bf16hi(v.y), acc[3]);
+          acc[4] = fmaf(wv, bf16lo(v.z), acc[4]); acc[5] = fmaf(wv, bf16hi(v.z), acc[5]);
+          acc[6] = fmaf(wv, bf16lo(v.w), acc[6]); acc[7] = fmaf(wv, bf16hi(v.w), acc[7]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[st]);
@@ -339,17 +338,17 @@ cudaError_t launch_rb(const CUtensorMap& tm_w, const CUtensorMap& tm_p, const vo
 
 }  // namespace
 
-cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
+cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, H heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, H, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // partials: (512 latent, H heads, segments), boxes of 64 dims x 1 head x 128 segments
+  // partials (bf16): (512 latent, H heads, segments), boxes of 64 dims x 1 head x 128 segments
   const uint64_t segs = (uint64_t)max_workers + B;
-  if (!encode_3d_box(&tm_p, part_o, DC, H, segs, DC * 4, (uint64_t)H * DC * 4, KC, 1, SEGB,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+  if (!encode_3d_box(&tm_p, part_o, DC, H, segs, DC * 2, (uint64_t)H * DC * 2, KC, 1, SEGB,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
   const int sms = device_sm_count();

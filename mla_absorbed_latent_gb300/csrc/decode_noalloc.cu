@@ -109,7 +109,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   const WsLayout L = ws_layout(B, H, workers);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   int* plan = reinterpret_cast<int*>(ws + L.plan);
-  float* part_o = reinterpret_cast<float*>(ws + L.part_o);
+  uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
 
   if (launch_plan(seqlens, B, max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;

@@ -180,7 +180,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int* plan = reinterpret_cast<const int*>(ws + L.plan);
-  float* part_o = reinterpret_cast<float*>(ws + L.part_o);
+  uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   const int sms = num_sms();
   const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
@@ -208,7 +208,7 @@ int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t w
   if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return status_of(launch_combine(W_UV, H, B, reinterpret_cast<const int*>(ws + L.plan),
-                                  reinterpret_cast<const float*>(ws + L.part_o),
+                                  reinterpret_cast<const uint16_t*>(ws + L.part_o),
                                   reinterpret_cast<const float*>(ws + L.part_lse), out, o_lat_out, err,
                                   L.max_segments - B, stream));
 }

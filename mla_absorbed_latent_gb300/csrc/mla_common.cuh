@@ -37,7 +37,7 @@ __device__ __forceinline__ void raise_error(int* err, int code, int info) {
 }
 
 // ---------------------------------------------------------------------------
-// decode workspace: [q_cat bf16 B*H*576][plan int32][partial O fp32][partial lse fp32]
+// decode workspace: [q_cat bf16 B*H*576][plan int32][partial O bf16][partial lse fp32]
 // ---------------------------------------------------------------------------
 struct WsLayout {
   size_t q_cat, plan, part_o, part_lse, total;
@@ -61,7 +61,7 @@ inline WsLayout ws_layout(int B, int H, int max_workers) {
   off = align_up(off + (size_t)(PLAN_HDR + 2 * B + 1 + max_workers) * 4, 1024);
   L.max_segments = max_workers + B;
   L.part_o = off;
-  off = align_up(off + (size_t)L.max_segments * H * DC * 4, 1024);
+  off = align_up(off + (size_t)L.max_segments * H * DC * 2, 1024);  // bf16 partials
   L.part_lse = off;
   off = align_up(off + (size_t)L.max_segments * H * 4, 1024);
   L.total = off;
@@ -179,11 +179,11 @@ cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int worker
                         cudaStream_t s);
 cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s);
+                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_cc_workers(int num_sms);
 cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, float* part_o, float* part_lse, int* err, cudaStream_t s);
+                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
 // library-internal accessors (defined in mla_api.cu)
 int* device_error_word();            // this device's error word, nullptr on failure
@@ -191,7 +191,7 @@ int device_sm_count();               // SMs of the current device, 0 on failure
 int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
 
 // max_workers: the partial buffer holds max_workers + B segment slots
-cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const float* part_o,
+cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s);
 

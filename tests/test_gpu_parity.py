@@ -250,10 +250,13 @@ def test_decode_quant_ragged_edges(fmt):
     _status_ok()
     rows = [b for b, n in enumerate(seqlens) if n > 0]
     _check_rows(dev, rows)  # the bf16 outputs, at the stated tolerance
-    # o_lat: the dequantized values are rounded once to bf16 for the MMA
-    # (half an ulp, 2^-9 relative), which the outlier channels (|x| up to ~40)
-    # turn into absolute errors above the output tolerance; bound each channel
-    # by 2^-8 of its largest magnitude on top of the usual tolerance
+    # o_lat: the dequantized values are rounded once to bf16 for the MMA and
+    # each split's partial o_lat is stored in bf16 (each half an ulp, 2^-9
+    # relative; both propagate into o_lat as at most 2^-9 of the channel's
+    # largest magnitude, o_lat being a convex combination of the latents),
+    # which the outlier channels (|x| up to ~40) turn into absolute errors above
+    # the output tolerance; bound each channel by 2^-8 of its largest magnitude
+    # on top of the usual tolerance
     ref = oracle_rows(prob, rows)
     got = o_lat.cpu().numpy().astype(np.float64)
     for b in rows:
