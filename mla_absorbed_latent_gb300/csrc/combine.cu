@@ -47,8 +47,7 @@ struct CombLayout {
   // barriers: w_full, w_empty, p_full, p_empty, b_full, b_free, d_full
   static constexpr uint32_t NBAR = 2 * WST + 2 * PST + 2 * BST + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
-  static constexpr uint32_t OFF_ROWS = OFF_MISC + 16;        // int2 [RB]: first / last segment of each row
-  static constexpr uint32_t OFF_WGT = OFF_ROWS + RB * 8;     // float [RB + max workers]: weight per segment
+  static constexpr uint32_t OFF_WGT = OFF_MISC + 16;         // float [RB + max workers]: weight per segment
   static size_t bytes(int max_workers) { return OFF_WGT + (size_t)(RB + max_workers) * 4 + 1024; }
 };
 
@@ -98,7 +97,6 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   uint64_t* d_full = b_free + BST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 12);
-  int2* rows = reinterpret_cast<int2*>(sm + L::OFF_ROWS);
   float* wgt = reinterpret_cast<float*>(sm + L::OFF_WGT);
 
   const int h = blockIdx.x, b0 = blockIdx.y * RB;
@@ -153,55 +151,24 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   const int s_hi = t1 > t0 ? worker_of_tile(t1 - 1, T, W) + b_end : 0;
   const int nsub = (s_hi - s_lo + SEGB - 1) / SEGB;  // partial tiles per chunk (0 when every row is empty)
 
-  if (!loader) {
-    // ---- each row's segments and their softmax weights (merge warps only;
-    // the loader already streams the partial tiles)
-    for (int k = tid; k < s_hi - s_lo; k += 32 * NW) wgt[k] = 0.f;
-    named_barrier(1, 32 * NW);
-    if (tid < RB) {
-      const int b = b0 + tid;
-      int2 r = make_int2(1, 0);  // empty
-      if (b < B && prefix[b + 1] > prefix[b]) {
-        r.x = worker_of_tile(prefix[b], T, W) + b;
-        r.y = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
-      }
-      rows[tid] = r;
-      // log-sum-exp of segment s = w + b (-inf for a worker without tiles)
-      // into wgt, all loads in flight together; then the weights in place
-      float mx = -INFINITY;
-#pragma unroll 4
-      for (int s = r.x; s <= r.y; ++s) {
-        const long long w = s - b;
-        const float lw = worker_begin(w, T, W) == worker_begin(w + 1, T, W) ? -INFINITY : part_lse[(size_t)s * H + h];
-        wgt[s - s_lo] = lw;
-        mx = fmaxf(mx, lw);
-      }
-      float den = 0.f;
-      for (int s = r.x; s <= r.y; ++s) {
-        const float lw = wgt[s - s_lo];
-        const float e = lw == -INFINITY ? 0.f : expf(lw - mx);
-        wgt[s - s_lo] = e;
-        den += e;
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      for (int s = r.x; s <= r.y; ++s) wgt[s - s_lo] *= inv;
-    }
-    named_barrier(1, 32 * NW);
-  }
-
   if (loader) {
-    // ------------------------------------------------------------ TMA loader
+    // ------------------------------------------------------------ TMA loaders:
+    // lane 0 refills the W_UV ring, lane 1 streams the partial tiles (so
+    // neither ring waits for the other)
     if (lane == 0) {
+      int wi = WST;  // W tiles issued so far
+      for (int kc = WST; kc < NCHUNK; ++kc, ++wi) {  // stage kc % WST was read by chunk kc - WST's MMAs
+        const int st = kc % WST;
+        if (!cwait(&w_empty[st], ((kc / WST) & 1) ^ 1, abort, err, 0)) break;
+        mbar_arrive_expect_tx(&w_full[st], W_TILE);
+        tma_load_3d(sm + L::OFF_W + st * W_TILE, &tm_w, KC * kc, 0, h, &w_full[st]);
+      }
+      if (*abort)  // let copies in flight land before the CTA exits
+        for (int k = max(0, wi - WST); k < wi; ++k) (void)mbar_wait(&w_full[k % WST], (k / WST) & 1);
+    } else if (lane == 1) {
       int pu = 0;  // partial tiles issued so far
       bool ok = true;
       for (int kc = 0; kc < NCHUNK && ok; ++kc) {
-        if (kc >= WST) {  // stage kc % WST was read by chunk kc - WST's MMAs
-          const int st = kc % WST;
-          ok = cwait(&w_empty[st], ((kc / WST) & 1) ^ 1, abort, err, 0);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&w_full[st], W_TILE);
-          tma_load_3d(sm + L::OFF_W + st * W_TILE, &tm_w, KC * kc, 0, h, &w_full[st]);
-        }
         for (int sub = 0; sub < nsub; ++sub, ++pu) {
           const int st = pu % PST;
           ok = cwait(&p_empty[st], ((pu / PST) & 1) ^ 1, abort, err, 1);
@@ -210,16 +177,43 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
           tma_load_3d(sm + L::OFF_P + st * P_TILE, &tm_p, KC * kc, h, s_lo + SEGB * sub, &p_full[st]);
         }
       }
-      if (*abort) {  // let copies in flight land before the CTA exits
+      if (*abort)
         for (int k = max(0, pu - PST); k < pu; ++k) (void)mbar_wait(&p_full[k % PST], (k / PST) & 1);
-        for (int kc = 0; kc < NCHUNK; ++kc) (void)mbar_wait(&w_full[kc % WST], (kc / WST) & 1);
-      }
     }
   } else {
     // ------------------------------------------------------------ merge warps
     const int r = tid >> 3, u = tid & 7;  // row of the group, 8-dim unit of the chunk
     const int b = b0 + r;
-    const int2 rs = rows[r];
+    // ---- the row's segments [rs.x, rs.y] (segment w + b of row b; empty when
+    // x > y) and their softmax weights e^{LSE_s - LSE} into wgt, the row's
+    // 8 threads sharing the segments (a worker without tiles left no partial:
+    // weight 0).  Slots between rows are never read.
+    int2 rs = make_int2(1, 0);
+    if (b < B) {
+      const int p0 = prefix[b], p1 = prefix[b + 1];
+      if (p1 > p0) rs = make_int2(worker_of_tile(p0, T, W) + b, worker_of_tile(p1 - 1, T, W) + b);
+    }
+    float mx = -INFINITY;
+    for (int s = rs.x + u; s <= rs.y; s += 8) {
+      const long long w = s - b;
+      const float lw = worker_begin(w, T, W) == worker_begin(w + 1, T, W) ? -INFINITY : part_lse[(size_t)s * H + h];
+      wgt[s - s_lo] = lw;
+      mx = fmaxf(mx, lw);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float den = 0.f;
+    for (int s = rs.x + u; s <= rs.y; s += 8) {
+      const float lw = wgt[s - s_lo];
+      const float e = lw == -INFINITY ? 0.f : expf(lw - mx);
+      wgt[s - s_lo] = e;
+      den += e;
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int s = rs.x + u; s <= rs.y; s += 8) wgt[s - s_lo] *= inv;
+    __syncwarp();  // the row's weights, written by its 8 threads (one warp)
     const uint32_t idesc = idesc_bf16_f32(128, RB, false, false);
     int pu = 0;
     bool ok = true, final_commit = false;
