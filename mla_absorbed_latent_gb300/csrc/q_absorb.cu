@@ -5,12 +5,13 @@
 // "手搓 MLA" §四 writes it as einsum("thd,hdc->thc", q_nope, W_UK).
 //
 // Per head this is a small GEMM, M = B rows, N = 512, K = 128, run on the
-// fifth-generation tensor core: one CTA per head; q_nope rows (A) and W_UK[h]
-// (B) arrive as K-major 128B-swizzled TMA tiles; 16 tcgen05.mma (M=128 rows,
-// N=256, K=16) accumulate the 128 x 512 fp32 result in tensor memory; the
-// epilogue rounds it once to bf16, the A operand of the score MMA.  The output
-// row is the 576-wide query of the latent attention: q_lat followed by a copy
-// of q_pe.
+// fifth-generation tensor core: two CTAs per head, each computing one half of
+// the 512 latent columns (so each reads half of W_UK[h] and two CTAs fit on
+// an SM); q_nope rows (A) and the W_UK[h] half (B) arrive as K-major
+// 128B-swizzled TMA tiles; 8 tcgen05.mma (M=128 rows, N=256, K=16) accumulate
+// the 128 x 256 fp32 result in tensor memory; the epilogue rounds it once to
+// bf16, the A operand of the score MMA.  The output row is the 576-wide query
+// of the latent attention: q_lat followed by a copy of q_pe.
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -23,7 +24,7 @@ constexpr uint32_t W_TILE = 256 * 128;    // 32 KB: 256 latent columns x 64 dims
 constexpr uint32_t Q_TILE = QROWS * 128;  // 16 KB: 128 rows x 64 dims, 128B-swizzled
 
 struct __align__(1024) QaSmem {
-  uint8_t w[4][W_TILE];  // tile 2*dc + nh: dims [64dc, 64dc+64) of latent columns [256nh, 256nh+256)
+  uint8_t w[2][W_TILE];  // tile dc: dims [64dc, 64dc+64) of this CTA's latent columns [256nh, 256nh+256)
   uint8_t q[2][Q_TILE];  // q_nope rows of the pass, dims [64dc, 64dc+64)
   uint64_t w_full, q_full, mma_done;
   uint32_t tmem_base;
@@ -36,7 +37,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
                                                            uint16_t* __restrict__ q_cat) {
   extern __shared__ uint8_t smem_raw[];
   QaSmem& S = *reinterpret_cast<QaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int h = blockIdx.x;
+  const int h = blockIdx.x, nh = blockIdx.y;  // head, half of the latent columns
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int passes = (B + QROWS - 1) / QROWS;
 
@@ -47,12 +48,11 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     fence_barrier_init();
     // W_UK is a weight, written (if at all) by a kernel that completed before
     // this chain started: its tiles load while the kernel before this one runs
-    mbar_arrive_expect_tx(&S.w_full, 4 * W_TILE);
-    for (int dc = 0; dc < 2; ++dc)
-      for (int nh = 0; nh < 2; ++nh) tma_load_3d(S.w[2 * dc + nh], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
+    mbar_arrive_expect_tx(&S.w_full, 2 * W_TILE);
+    for (int dc = 0; dc < 2; ++dc) tma_load_3d(S.w[dc], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
   }
   if (warp == 0) {
-    tmem_alloc(&S.tmem_base, 512);
+    tmem_alloc(&S.tmem_base, 256);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -73,19 +73,18 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
       if (p == 0) ok = mbar_wait(&S.w_full, 0) && ok;
       if (ok) {
         fence_after_sync();
-        for (int nh = 0; nh < 2; ++nh)
-          for (int dc = 0; dc < 2; ++dc) {
-            const uint64_t ad = smem_desc(smem_u32(S.q[dc]), 16, 1024, SWIZZLE_128B);
-            const uint64_t bd = smem_desc(smem_u32(S.w[2 * dc + nh]), 16, 1024, SWIZZLE_128B);
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + 256 * nh, ad + (uint64_t)((kk * 32) >> 4), bd + (uint64_t)((kk * 32) >> 4), idesc,
-                     (dc | kk) != 0 ? 1u : 0u);
-          }
+        for (int dc = 0; dc < 2; ++dc) {
+          const uint64_t ad = smem_desc(smem_u32(S.q[dc]), 16, 1024, SWIZZLE_128B);
+          const uint64_t bd = smem_desc(smem_u32(S.w[dc]), 16, 1024, SWIZZLE_128B);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem, ad + (uint64_t)((kk * 32) >> 4), bd + (uint64_t)((kk * 32) >> 4), idesc,
+                   (dc | kk) != 0 ? 1u : 0u);
+        }
       }
       mma_commit(&S.mma_done);  // arrives even if nothing was issued
     }
-    // q_pe rows of this pass, while the MMAs run
-    for (int i = tid; i < QROWS * 8; i += blockDim.x) {
+    // q_pe rows of this pass, while the MMAs run (each CTA of the head half of them)
+    for (int i = tid + nh * (QROWS * 4); i < (nh + 1) * (QROWS * 4); i += blockDim.x) {
       const int r = b0 + i / 8, v = i % 8;
       if (r < B)
         reinterpret_cast<uint4*>(q_cat + ((size_t)r * H + h) * DK + DC)[v] =
@@ -101,7 +100,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     const int r0 = b0 + warp * 32;
     if (r0 < B) {
       uint8_t* stg = &S.q[0][0] + warp * 8192;
-      for (int rd = 0; rd < DC / 128; ++rd) {
+      for (int rd = 0; rd < 2; ++rd) {  // this CTA's 256 latent columns, 128 per round
         if (rd > 0 && lane == 0) bulk_wait_read_all();  // the last round's stores have read the tile
         __syncwarp();
 #pragma unroll
@@ -124,8 +123,8 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
         fence_proxy_async_smem();  // generic writes -> the TMA engine's reads
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tm_qc, stg, 128 * rd, h, r0);
-          tma_store_3d(&tm_qc, stg + 4096, 128 * rd + 64, h, r0);
+          tma_store_3d(&tm_qc, stg, 256 * nh + 128 * rd, h, r0);
+          tma_store_3d(&tm_qc, stg + 4096, 256 * nh + 128 * rd + 64, h, r0);
           bulk_commit_group();
         }
       }
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
   __syncthreads();
   if (warp == 0) {
     fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -161,7 +160,7 @@ cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_
   const size_t smem = sizeof(QaSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(q_absorb_kernel, dim3(H), dim3(128), smem, s, tm_w, tm_q, tm_qc, static_cast<const uint16_t*>(q_pe), H,
+  return launch_pdl(q_absorb_kernel, dim3(H, 2), dim3(128), smem, s, tm_w, tm_q, tm_qc, static_cast<const uint16_t*>(q_pe), H,
                     B, static_cast<uint16_t*>(q_cat));
 }
 
