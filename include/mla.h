@@ -218,6 +218,20 @@ int mla_decode_noalloc(const void* q_nope, const void* q_pe, const void* W_UK, c
  */
 int mla_get_device_status(cudaStream_t stream, int* info);
 
+/*
+ * Self-test of the device failure path.  Enqueues on `stream` one CTA pair
+ * (a 2-CTA cluster, like the tcgen05 decode kernel) whose first CTA waits on a
+ * barrier that nothing completes, through the same bounded wait the decode
+ * kernel uses.  After that wait's limit (about 2 s at the maximum SM clock)
+ * it gives up, records MLA_ERR_TIMEOUT with detail 1 in the device status
+ * word and raises the abort flags of both CTAs; the second CTA, which starts
+ * its own wait later, leaves it through the abort flag (as the other roles of
+ * a decode kernel do).  The kernel then returns: nothing faults, the context
+ * stays usable.  Read the outcome with mla_get_device_status.  Returns MLA_OK
+ * once enqueued, MLA_ERR_CUDA if the launch fails.
+ */
+int mla_wait_selftest(cudaStream_t stream);
+
 /* Which attend kernel mla_decode uses for H heads: 1 = tcgen05, 0 = CUDA cores,
  * -1 = unsupported. */
 int mla_decode_kernel_kind(int H);

@@ -50,6 +50,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode_attend": (i, [i, cp, vp, i, vp, i, f, vp, sz, vp]),
         "mla_decode_combine": (i, [vp, i, i, vp, sz, vp, vp, vp]),
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
+        "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
         "mla_status_string": (ctypes.c_char_p, [i]),
     }
@@ -141,6 +142,12 @@ def mla_get_device_status(stream=None) -> tuple[int, int]:
     info = ctypes.c_int(0)
     st = _lib.mla_get_device_status(_stream(stream), ctypes.byref(info))
     return int(st), int(info.value)
+
+
+def mla_wait_selftest(stream=None) -> None:
+    """Enqueue the bounded-wait self-test (about 2 s on the device); read its
+    outcome with mla_get_device_status."""
+    _check(_lib.mla_wait_selftest(_stream(stream)), "mla_wait_selftest")
 
 
 def mla_decode_kernel_kind(H: int) -> int:

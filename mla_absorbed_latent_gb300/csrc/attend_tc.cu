@@ -1066,6 +1066,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
+// Self-test of the failure path of the waits above: a CTA pair in which CTA 0
+// waits on a barrier that nothing completes.  Its wait gives up after
+// WAIT_LIMIT_CYCLES, records MLA_ERR_TIMEOUT (detail 1) and raises the abort
+// flags of both CTAs; CTA 1 starts its own wait a quarter of the limit later
+// and leaves it through the abort flag.  Every wait is bounded: the kernel
+// returns and nothing faults.
+struct SelftestSmem {
+  uint64_t bar;
+  int abort_flag;
+};
+__global__ void __launch_bounds__(32, 1) wait_selftest_kernel(int* err) {
+  __shared__ SelftestSmem S;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    mbar_init(&S.bar, 1);
+    S.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  cluster_sync();  // both flags are initialised before either CTA can raise the other's
+  if (threadIdx.x == 0) {
+    if (rank == 1) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < WAIT_LIMIT_CYCLES / 4 && !*reinterpret_cast<volatile int*>(&S.abort_flag)) {
+      }
+    }
+    (void)wait_bar<true>(S, &S.bar, 0, err, 1 + (int)rank);
+  }
+  __syncwarp();
+  cluster_sync();  // neither CTA leaves while the other may still write its flag
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1093,6 +1125,21 @@ cudaLaunchConfig_t launch_config(int workers, cudaStream_t s, cudaLaunchAttribut
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, wait_selftest_kernel, err);
+}
 
 // persistent workers (CTA pairs) that fit on the device at once
 int attend_tc_workers(int num_sms) {

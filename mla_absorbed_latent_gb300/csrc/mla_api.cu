@@ -249,6 +249,12 @@ int mla_get_device_status(cudaStream_t stream, int* info) {
   return host[0];
 }
 
+int mla_wait_selftest(cudaStream_t stream) {
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  return status_of(launch_wait_selftest(err, stream));
+}
+
 int mla_decode_kernel_kind(int H) { return attend_kind(H, MLA_FMT_BF16); }
 
 const char* mla_status_string(int status) {

@@ -185,6 +185,8 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
+// a CTA pair whose bounded wait runs out on purpose (see mla_wait_selftest)
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
 // library-internal accessors (defined in mla_api.cu)
 int* device_error_word();            // this device's error word, nullptr on failure
 int device_sm_count();               // SMs of the current device, 0 on failure

@@ -292,6 +292,30 @@ def test_decode_bad_page_id_reports_bounds():
     assert st == mla.MLA_ERR_BOUNDS and info == prob.num_pages + 100
 
 
+def test_bounded_wait_times_out_and_reports():
+    """The failure path of the decode kernel's bounded waits, run out on
+    purpose with no fault: in a CTA pair, CTA 0 waits on a barrier that nothing
+    completes; after the limit (about 2 s) it records MLA_ERR_TIMEOUT (detail 1,
+    CTA 0's) and raises both abort flags, and CTA 1 leaves its later wait
+    through its flag without a report of its own.  Afterwards the context still
+    decodes correctly (an H=128 case through the tcgen05 kernel)."""
+    import time
+    import mla_absorbed_latent_gb300 as mla
+    _status_ok()
+    t0 = time.time()
+    mla.mla_wait_selftest()
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_ERR_TIMEOUT and info == 1, (mla.mla_status_string(st), info)
+    assert time.time() - t0 < 60
+    prob = make_problem(128, [300, 64, 1], seed=12)
+    dev = DeviceDecode(prob)
+    o_lat = torch.empty((prob.B, 128, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, list(range(prob.B)), o_lat)
+
+
 def test_decode_score_beyond_tracked_range_is_reported():
     """H=128: a token of the second page whose RoPE key is 200 x one head's
     q_pe raises that head's score far more than 100 (log2 units) above the
