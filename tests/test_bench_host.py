@@ -1,0 +1,105 @@
+"""Host logic of bench.py that needs no GPU: the roofline denominators, the
+DRAM-traffic record keyed on the attend kernel's source, and the parsing of
+the nvidia-smi clock samples taken during the timed region."""
+import hashlib
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _fake_root(tmp_path, source_text=b"__global__ void k() {}\n", record=None):
+    csrc = tmp_path / "mla_absorbed_latent_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "attend_tc.cu").write_bytes(source_text)
+    (tmp_path / "profiles").mkdir()
+    if record is not None:
+        (tmp_path / "profiles" / "attend_traffic.json").write_text(json.dumps(record))
+    return tmp_path
+
+
+def _record(source_text, **over):
+    d = {"source": "attend_tc.cu", "source_sha256": hashlib.sha256(source_text).hexdigest(), "kind": "tcgen05",
+         "fmt": "bf16", "dram_bytes_per_launch": 617000000}
+    d.update(over)
+    return d
+
+
+def test_traffic_is_reported_for_the_captured_source(tmp_path, monkeypatch):
+    src = b"__global__ void attend() {}\n"
+    monkeypatch.setattr(bench, "ROOT", str(_fake_root(tmp_path, src, _record(src))))
+    assert bench.kernel_traffic("tcgen05", "bf16") == 617000000
+
+
+@pytest.mark.parametrize("change", ["source", "kind", "fmt", "missing"])
+def test_traffic_is_dropped_when_it_no_longer_describes_the_kernel(tmp_path, monkeypatch, change):
+    src = b"__global__ void attend() {}\n"
+    rec = _record(src)
+    if change == "source":
+        rec["source_sha256"] = hashlib.sha256(src + b"// edited\n").hexdigest()
+    elif change == "kind":
+        rec["kind"] = "cuda-core"
+    elif change == "fmt":
+        rec["fmt"] = "int8"
+    root = _fake_root(tmp_path, src, None if change == "missing" else rec)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.kernel_traffic("tcgen05", "bf16") is None
+
+
+def test_peaks_measured_and_fallback(tmp_path, monkeypatch):
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        d = json.load(f)
+    hbm, tf, tf_sus, src = bench.load_peaks()
+    assert src == "measured" and hbm == float(d["hbm_gbs"]) and tf == float(d["bf16_tflops"])
+    assert tf_sus == float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))  # no peaks file there
+    assert bench.load_peaks() == (6800.0, 1900.0, 1700.0, "fallback")
+
+
+class _FakeProc:
+    def __init__(self, text):
+        self.text = text
+
+    def terminate(self):
+        pass
+
+    def kill(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.text, ""
+
+
+def test_clock_samples_median_max_and_reasons():
+    # index, sm, max sm, power, active mask, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    rows = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1200.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 10.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    cs = bench.ClockSampler(0)
+    cs.proc = _FakeProc("\n".join(rows) + "\n")
+    got = cs.stop()
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_samples_flag_thermal_slowdown():
+    rows = ["0, 1400, 2070, 1390.0, 0x28, Active, Not Active, Active, Not Active"]
+    cs = bench.ClockSampler(0)
+    cs.proc = _FakeProc("\n".join(rows) + "\n")
+    got = cs.stop()
+    assert got["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and got["sm_mhz"] == 1400.0
+
+
+def test_clock_sampler_without_nvidia_smi_reports_nothing():
+    cs = bench.ClockSampler(0)
+    assert cs.stop() is None
