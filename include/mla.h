@@ -212,9 +212,11 @@ int mla_decode_noalloc(const void* q_nope, const void* q_pe, const void* W_UK, c
 
 /*
  * Wait for `stream`, then return (and clear) the first device-detected error
- * recorded since the last call on the current device: MLA_OK,
- * MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).
- * If `info` is non-NULL it receives a detail value (the offending row or page).
+ * recorded since the last call on the current device: MLA_OK, MLA_ERR_BOUNDS,
+ * MLA_ERR_RANGE or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).
+ * If `info` is non-NULL it receives a detail value: the offending row or page
+ * id for MLA_ERR_BOUNDS, the number of the wait site that gave up for
+ * MLA_ERR_TIMEOUT (1 for mla_wait_selftest), 0 for MLA_ERR_RANGE.
  */
 int mla_get_device_status(cudaStream_t stream, int* info);
 
