@@ -27,6 +27,7 @@ import io
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -69,17 +70,28 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def source_digest(text: str) -> str:
+    """sha256 of a CUDA source with its comments and whitespace removed, so that
+    the digest changes with the code and not with its comments (no string
+    literal in the hashed source holds a comment marker)."""
+    code = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    code = re.sub(r"//[^\n]*", " ", code)
+    code = re.sub(r"\s+", " ", code).strip()
+    return hashlib.sha256(code.encode()).hexdigest()
+
+
 def kernel_traffic(kind: str, fmt: str = "bf16"):
     """DRAM bytes per launch of the attend kernel from the committed ncu summary,
-    or None when missing or taken on a different kernel source."""
+    or None when missing or taken on a different kernel source (code, not
+    comments: see source_digest)."""
     path = os.path.join(ROOT, "profiles", "attend_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         src = os.path.join(ROOT, "mla_absorbed_latent_gb300", "csrc", d["source"])
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
-        if h != d["source_sha256"] or d.get("kind") != kind or d.get("fmt", "bf16") != fmt:
+        with open(src, encoding="utf-8") as f:
+            h = source_digest(f.read())
+        if h != d["source_digest"] or d.get("kind") != kind or d.get("fmt", "bf16") != fmt:
             return None
         return int(d["dram_bytes_per_launch"])
     except Exception:

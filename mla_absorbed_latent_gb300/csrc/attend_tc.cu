@@ -7,7 +7,7 @@
 //   S[h,t] = q_lat[h] . c_t + q_pe[h] . k_pe_t          (M = 128 heads, K = 576)
 //   online softmax over t (log2 domain, scale folded in)
 //   O[h,:] += P[h,t] c_t                                (M = 128, N = 512)
-//   emitted per segment as O / l and LSE = (m + log2 l) ln 2.
+//   emitted per segment as O / l (rounded to bf16) and LSE = (m + log2 l) ln 2.
 //
 // Why a CTA pair.  O is 128 x 512 fp32 = 256 KB, all of one SM's tensor memory.
 // The pair splits the latent width: CTA r owns latent dims [256r, 256r+256)
@@ -99,8 +99,8 @@ constexpr uint32_t PIN_Q = 2 * SL_Q;                          // messages from t
 constexpr uint32_t QPE_BYTES = 128 * PE_HALF * 2;             // 8,192: [128 heads][32 dims] 64B-swizzled
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
-constexpr int Q_AHEAD = 8;
-constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 heads][64 dims] 128B-swizzled  // pages before a row's end at which the producer prefetches the next query
+constexpr int Q_AHEAD = 8;  // pages before a row's end at which the producer prefetches the next query
+constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 heads][64 dims] 128B-swizzled
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
 constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p tolerated (O and l stay finite in fp32)

@@ -1,7 +1,6 @@
 """Host logic of bench.py that needs no GPU: the roofline denominators, the
 DRAM-traffic record keyed on the attend kernel's source, and the parsing of
 the nvidia-smi clock samples taken during the timed region."""
-import hashlib
 import json
 import os
 import sys
@@ -26,7 +25,7 @@ def _fake_root(tmp_path, source_text=b"__global__ void k() {}\n", record=None):
 
 
 def _record(source_text, **over):
-    d = {"source": "attend_tc.cu", "source_sha256": hashlib.sha256(source_text).hexdigest(), "kind": "tcgen05",
+    d = {"source": "attend_tc.cu", "source_digest": bench.source_digest(source_text.decode()), "kind": "tcgen05",
          "fmt": "bf16", "dram_bytes_per_launch": 617000000}
     d.update(over)
     return d
@@ -43,7 +42,7 @@ def test_traffic_is_dropped_when_it_no_longer_describes_the_kernel(tmp_path, mon
     src = b"__global__ void attend() {}\n"
     rec = _record(src)
     if change == "source":
-        rec["source_sha256"] = hashlib.sha256(src + b"// edited\n").hexdigest()
+        rec["source_digest"] = bench.source_digest((src + b"__device__ int edited;\n").decode())
     elif change == "kind":
         rec["kind"] = "cuda-core"
     elif change == "fmt":
@@ -51,6 +50,14 @@ def test_traffic_is_dropped_when_it_no_longer_describes_the_kernel(tmp_path, mon
     root = _fake_root(tmp_path, src, None if change == "missing" else rec)
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.kernel_traffic("tcgen05", "bf16") is None
+
+
+def test_digest_follows_code_not_comments():
+    a = "__global__ void k(int* x) {\n  x[0] = 1;  // one\n}\n"
+    b = "/* the kernel */\n__global__ void k(int* x) {   x[0] = 1;\n\n  // set the first element\n}"
+    c = "__global__ void k(int* x) {\n  x[0] = 2;  // one\n}\n"
+    assert bench.source_digest(a) == bench.source_digest(b)
+    assert bench.source_digest(a) != bench.source_digest(c)
 
 
 def test_peaks_measured_and_fallback(tmp_path, monkeypatch):
