@@ -16,7 +16,11 @@ Sources (pages are cited by title and section):
 Pins (tests/test_oracle.py): the worked example's byte counts ([audit] §4.1,
 §4.2), naive == absorbed to 1e-10 in fp64 ([audit] §2.2/§2.3, [tutorial] §四),
 pure-Python brute-force attention on tiny inputs, closed forms (one token,
-zero query, one dominant token), and hand-worked quantizer vectors.
+zero query, one dominant token), and hand-worked quantizer vectors.  The
+producer of the cache payload (down-projection, RMSNorm, RoPE) is pinned by
+hand-worked values, closed forms (unit RMS, scale invariance, rotation by
+position 0 and by one radian), the relative-position property of RoPE and a
+pure-Python brute force on odd tiny dimensions.
 The quantizer's rounding rules are readings of [report] §3.2, which gives no
 formula; the pages' own error figures use an unstated metric, so the
 quantization *error* is parity unpinned (the codes themselves are pinned to
@@ -44,6 +48,7 @@ __all__ = [
     "pack_nibbles", "page_bytes", "PAGE_LAYOUT",
     "quantize_token", "dequantized_tokens", "expected_page_pool",
     "decode_batch",
+    "rms_norm", "rope", "project_latent",
 ]
 
 
@@ -148,6 +153,61 @@ def decode_batch(q_nope, q_pe, seqs, W_UK, W_UV, scale: float, rows=None):
     rows = range(len(seqs)) if rows is None else rows
     return {b: absorbed_decode(q_nope[b], q_pe[b], seqs[b][0], seqs[b][1], W_UK, W_UV, scale)
             for b in rows}
+
+
+# ----------------------------------------------------------------------------
+# the step before the cache: down-projection, RMSNorm, RoPE
+# ----------------------------------------------------------------------------
+
+def rms_norm(v, weight, eps: float):
+    """RMSNorm over the last axis: v / sqrt(mean(v^2) + eps) * weight.
+
+    [tutorial] §三 normalises the down-projected latent before it is cached,
+    c_kv = rmsnorm(x @ W_DKV.T, W_KVN); [audit] §3.3 maps the learned gain
+    W_KVN to the checkpoint's kv_norm weight.  The page states no epsilon:
+    it is an argument here.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    ms = np.mean(v * v, axis=-1, keepdims=True)
+    return v / np.sqrt(ms + eps) * np.asarray(weight, dtype=np.float64)
+
+
+def rope(x, pos, theta: float = 10000.0):
+    """Rotary position embedding of the last axis at integer positions `pos`.
+
+    [tutorial] §三 rotates the shared key before caching, k_pe = rope(x @
+    W_KR.T).  The pages give no pairing convention; read here as consecutive
+    pairs (2i, 2i+1) rotated by the angle pos * theta^(-2i/d):
+    (a, b) -> (a cos - b sin, a sin + b cos), all in fp64.
+    x [..., d] (d even), pos broadcastable to x.shape[:-1].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    freq = theta ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * freq
+    cos, sin = np.cos(ang), np.sin(ang)
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * cos - b * sin
+    out[..., 1::2] = a * sin + b * cos
+    return out
+
+
+def project_latent(x, wkv_a, kv_norm_w, pos, eps: float, theta: float = 10000.0):
+    """The cache payload of n tokens from their attention inputs.
+
+    [tutorial] §三: c_kv = rmsnorm(x @ W_DKV.T, W_KVN) and k_pe =
+    rope(x @ W_KR.T).  [audit] §3.3 names the joint projection wkv_a
+    (kv_a_proj_with_mqa): its first d_c rows are W_DKV, the remaining d_r rows
+    W_KR (the shared RoPE key appended to the latent projection).
+    x [n, hidden], wkv_a [d_c + d_r, hidden], kv_norm_w [d_c], pos [n].
+    Returns c_kv [n, d_c] and k_pe [n, d_r] in fp64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(wkv_a, dtype=np.float64)
+    d_c = np.shape(kv_norm_w)[-1]
+    y = x @ w.T                                   # [n, d_c + d_r]
+    return rms_norm(y[:, :d_c], kv_norm_w, eps), rope(y[:, d_c:], pos, theta)
 
 
 # ----------------------------------------------------------------------------

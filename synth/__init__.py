@@ -8,10 +8,13 @@ either of them.
 """
 
 from .workloads import (  # noqa: F401
+    HIDDEN,
     WORKLOADS,
     Workload,
     bf16_bits_to_f32,
     f32_to_bf16_bits,
+    gen_hidden,
+    gen_project_weights,
     gen_queries,
     gen_seqlens,
     gen_sequence,

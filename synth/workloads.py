@@ -34,6 +34,7 @@ PAGE = 64      # tokens per cache page
 
 # stream ids inside one workload seed
 _S_WEIGHTS, _S_QUERY, _S_SEQLEN, _S_PAGES, _S_OUTLIER, _S_SEQ = 0, 1, 2, 3, 4, 100
+_S_PROJ_W, _S_PROJ_X = 5, 200
 
 
 @dataclass(frozen=True)
@@ -186,3 +187,28 @@ def make_page_table(seqlens, seed: int, paged: bool, spare_pages: int = 0):
         table[b, :m] = phys[k:k + m]
         k += m
     return table, max(num_pages, 1)
+
+
+# ----------------------------------------------------------------------------
+# inputs of the cache producer (down-projection, RMSNorm, RoPE before append)
+# ----------------------------------------------------------------------------
+# hidden width of the attention input: 2048 for the V2-Lite layer (its outputs
+# are [1, 1, 2048]), 7168 for DeepSeek-V3 ("dim" of its config)
+HIDDEN = {"v2lite": 2048, "v3": 7168}
+
+
+def gen_project_weights(hidden: int, seed: int):
+    """wkv_a [576, hidden] ~ N(0, 1/sqrt(hidden)) and kv_norm weight [512] ~
+    1 + 0.1 N(0,1), both as bf16 bits (the latent rows first, then the 64
+    RoPE-key rows)."""
+    r = _rng(seed, _S_PROJ_W)
+    w = r.standard_normal((D_C + D_R, hidden), dtype=np.float32) * np.float32(1.0 / math.sqrt(hidden))
+    g = np.float32(1.0) + np.float32(0.1) * r.standard_normal(D_C, dtype=np.float32)
+    return f32_to_bf16_bits(w), f32_to_bf16_bits(g)
+
+
+def gen_hidden(hidden: int, seed: int, b: int, n: int) -> np.ndarray:
+    """Attention inputs of n tokens of row b, [n, hidden] bf16 bits, N(0,1) (the
+    layer input after its own RMSNorm has unit scale per element)."""
+    x = _rng(seed, _S_PROJ_X, b).standard_normal((n, hidden), dtype=np.float32)
+    return f32_to_bf16_bits(x)

@@ -368,3 +368,110 @@ def test_random_roundtrip_rope_norm():
     assert np.allclose(x[0], y[0])
     assert np.allclose(np.hypot(x[:, 0::2], x[:, 1::2]), np.hypot(y[:, 0::2], y[:, 1::2]))
     random.seed(0)
+
+
+# ----------------------------------------------------------------------------
+# the cache payload producer: c_kv = rmsnorm(x W_DKV^T, W_KVN), k_pe = rope(x W_KR^T)
+# ("手搓 MLA" §三; weight names "DeepSeek MLA 吸收式缓存" §3.3)
+# ----------------------------------------------------------------------------
+
+def test_rms_norm_hand_values():
+    """[1, 2, 3, 4]: mean square 30/4 = 7.5, so each entry is divided by sqrt(7.5)
+    = 2.7386127875258306; then the gain multiplies elementwise."""
+    out = O.rms_norm(np.array([1.0, 2.0, 3.0, 4.0]), np.array([1.0, 1.0, 2.0, -1.0]), 0.0)
+    want = [0.3651483716701107, 0.7302967433402214, 2.1908902300206643, -1.4605934866804429]
+    assert np.allclose(out, want, rtol=0, atol=1e-15)
+    # a constant vector normalises to the gain itself; eps enters under the root
+    g = np.linspace(0.5, 1.5, 512)
+    assert np.allclose(O.rms_norm(np.full(512, -3.0), g, 0.0), -g, atol=1e-15)
+    assert O.rms_norm(np.full(4, 2.0), np.ones(4), 12.0)[0] == pytest.approx(2.0 / 4.0, abs=1e-15)
+
+
+def test_rms_norm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((5, 512)) * 7.0
+    out = O.rms_norm(v, np.ones(512), 0.0)
+    assert np.allclose(np.sqrt(np.mean(out ** 2, axis=1)), 1.0, atol=1e-14)
+    assert np.allclose(O.rms_norm(v * 1e-3, np.ones(512), 0.0), out, atol=1e-12)
+    # the normalisation is per row: a row scaled alone does not move the others
+    v2 = v.copy()
+    v2[2] *= 50.0
+    assert np.allclose(O.rms_norm(v2, np.ones(512), 0.0), out, atol=1e-12)
+
+
+def test_rope_position_zero_and_one_radian():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 64))
+    assert np.array_equal(O.rope(x, np.zeros(3)), x)
+    # pair 0 turns by exactly pos radians (theta^0 = 1): (1, 0) at pos 1 -> (cos 1, sin 1)
+    e0 = np.zeros(64)
+    e0[0] = 1.0
+    r = O.rope(e0, 1)
+    assert r[0] == pytest.approx(0.5403023058681398, abs=1e-15)
+    assert r[1] == pytest.approx(0.8414709848078965, abs=1e-15)
+    assert np.all(r[2:] == 0.0)
+    # pair 1 (dims 2, 3) turns by 10000^(-2/64) = 0.7498942093324559 radians per position:
+    # (0, 1) at pos 2 -> (-sin 1.4997884186649117, cos 1.4997884186649117)
+    e3 = np.zeros(64)
+    e3[3] = 1.0
+    r = O.rope(e3, 2)
+    assert r[2] == pytest.approx(-math.sin(1.4997884186649117), abs=1e-14)
+    assert r[3] == pytest.approx(math.cos(1.4997884186649117), abs=1e-14)
+    assert np.all(np.delete(r, [2, 3]) == 0.0)
+    # the last pair (dims 62, 63) turns by 10000^(-62/64) = 1.333521432163324e-4 per position
+    e62 = np.zeros(64)
+    e62[62] = 1.0
+    r = O.rope(e62, 1000)
+    assert r[62] == pytest.approx(math.cos(0.1333521432163324), abs=1e-14)
+    assert r[63] == pytest.approx(math.sin(0.1333521432163324), abs=1e-14)
+
+
+def test_rope_relative_position_and_norm():
+    """The defining property: <rope(q, m), rope(k, n)> depends on m - n only; each
+    pair keeps its length; rotations by a and then b compose to a + b."""
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    d1 = np.dot(O.rope(q, 37), O.rope(k, 5))
+    d2 = np.dot(O.rope(q, 1032), O.rope(k, 1000))
+    assert d1 == pytest.approx(d2, abs=1e-9)
+    assert d1 != pytest.approx(np.dot(O.rope(q, 38), O.rope(k, 5)), abs=1e-3)
+    x = rng.standard_normal(64)
+    r = O.rope(x, 12345)
+    assert np.allclose(np.hypot(r[0::2], r[1::2]), np.hypot(x[0::2], x[1::2]), atol=1e-12)
+    assert np.allclose(O.rope(O.rope(x, 300), 45), O.rope(x, 345), atol=1e-10)
+
+
+def _project_bruteforce(x, w, g, pos, eps, theta, dc):
+    """Explicit loops, math.fsum: the projection, RMSNorm and RoPE as written."""
+    out_c, out_p = [], []
+    for t, row in enumerate(x):
+        y = [math.fsum(row[k] * w[j][k] for k in range(len(row))) for j in range(len(w))]
+        lat, rot = y[:dc], y[dc:]
+        inv = 1.0 / math.sqrt(math.fsum(v * v for v in lat) / dc + eps)
+        out_c.append([lat[j] * inv * g[j] for j in range(dc)])
+        d = len(rot)
+        pr = []
+        for i in range(d // 2):
+            ang = pos[t] * theta ** (-2.0 * i / d)
+            a, b = rot[2 * i], rot[2 * i + 1]
+            pr += [a * math.cos(ang) - b * math.sin(ang), a * math.sin(ang) + b * math.cos(ang)]
+        out_p.append(pr)
+    return np.array(out_c), np.array(out_p)
+
+
+@pytest.mark.parametrize("n", [1, 3])
+def test_project_latent_bruteforce_odd_dims(n):
+    """Odd, unequal dims (hidden 5, latent 3, RoPE key 4): a transposed weight, the
+    latent/key row split taken the other way round or the norm over the wrong
+    axis fails."""
+    rng = np.random.default_rng(20 + n)
+    hidden, dc, dr = 5, 3, 4
+    x = rng.standard_normal((n, hidden))
+    w = rng.standard_normal((dc + dr, hidden))
+    g = rng.standard_normal(dc)
+    pos = np.arange(7, 7 + n)
+    c, p = O.project_latent(x, w, g, pos, eps=0.25, theta=100.0)
+    bc, bp = _project_bruteforce(x.tolist(), w.tolist(), g.tolist(), pos.tolist(), 0.25, 100.0, dc)
+    assert c.shape == (n, dc) and p.shape == (n, dr)
+    assert np.max(np.abs(c - bc)) < 1e-12
+    assert np.max(np.abs(p - bp)) < 1e-12
