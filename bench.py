@@ -393,13 +393,151 @@ def run_ours(args, wl, fmt):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# the cache producer (down-projection + RMSNorm + RoPE + page write), a second workload
+# ----------------------------------------------------------------------------
+PROJECT_METRIC = "fused cache producer (kv down-projection, RMSNorm, RoPE, page write) tokens/s, 1 GB300"
+PROJECT = {
+    # name: (hidden, B, T, description)
+    "v3_project_prefill": (7168, 16, 2048, "DeepSeek-V3 width (hidden 7168): 16 rows x 2048 new tokens "
+                                           "(a 32,768-token prefill chunk) into a paged pool"),
+    "v3_project_decode": (7168, 64, 1, "DeepSeek-V3 width (hidden 7168): one new token for each of 64 rows "
+                                       "(the decode-time append)"),
+}
+PROJECT_EPS, PROJECT_THETA = 1e-6, 10000.0
+
+
+def _project_problem(name, fmt):
+    hidden, B, T, _ = PROJECT[name]
+    seed = 40
+    w, g = synth.gen_project_weights(hidden, seed)
+    x = np.stack([synth.gen_hidden(hidden, seed, b, T) for b in range(B)])
+    pos0 = np.full(B, 8192 - T, dtype=np.int32) if T < 64 else np.zeros(B, dtype=np.int32)
+    table, num_pages = synth.make_page_table(pos0 + T, seed, True)
+    return hidden, B, T, w, g, x, pos0, table, num_pages
+
+
+def project_oracle_time(name, fmt, budget_s):
+    """fp64 oracle producer over successive tokens until budget_s of oracle work;
+    returns (tokens, seconds)."""
+    import oracle as O
+    hidden, B, T, w, g, x, pos0, _, _ = _project_problem(name, fmt)
+    wf, gf = synth.bf16_bits_to_f32(w), synth.bf16_bits_to_f32(g)
+    done, spent = 0, 0.0
+    for b in range(B):
+        for t0 in range(0, T, 64):
+            xs = synth.bf16_bits_to_f32(x[b, t0:t0 + 64])
+            t1 = time.perf_counter()
+            O.project_latent(xs, wf, gf, pos0[b] + np.arange(t0, t0 + len(xs)), PROJECT_EPS, PROJECT_THETA)
+            spent += time.perf_counter() - t1
+            done += len(xs)
+            if spent >= budget_s:
+                return done, spent
+    return done, spent
+
+
+def run_project(args, name, fmt):
+    import torch
+    torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+    import mla_absorbed_latent_gb300 as mla
+    from synth.device import bits_to_device
+    hidden, B, T, w, g, x, pos0, table, num_pages = _project_problem(name, fmt)
+    ntok = B * T
+    dev_x, dev_w, dev_g = bits_to_device(x), bits_to_device(w), bits_to_device(g)
+    pool = torch.zeros(num_pages * mla.mla_cache_page_bytes(fmt), dtype=torch.uint8, device="cuda")
+    cache = mla.cache_struct(fmt, num_pages, pool)
+    pt = torch.from_numpy(table).cuda()
+    pos = torch.from_numpy(pos0).cuda()
+    ws_bytes = mla.mla_cache_project_workspace_bytes(B, T, hidden, 0)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")  # > L2: scrubbed between steps
+
+    def call(xin=dev_x, latent=None):
+        mla.mla_cache_project_append(cache, xin, hidden, dev_w, dev_g, PROJECT_EPS, PROJECT_THETA, pt,
+                                     table.shape[1], pos, B, T, latent, 0, ws, ws_bytes, stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after timing: {mla.mla_status_string(st)} ({info})")
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+
+    # end to end: x from pinned host memory in, the bf16 payload out, every step
+    h_x = dev_x.cpu().pin_memory()
+    lat = torch.empty((B, T, 576), dtype=torch.bfloat16, device="cuda")
+    h_lat = torch.empty(lat.shape, dtype=lat.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev_x.copy_(h_x, non_blocking=True)
+        call(latent=lat)
+        h_lat.copy_(lat, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        n, secs = project_oracle_time(name, fmt, min(args.cpu_seconds, 10.0))
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} of {ntok} tokens of {name}, fp64 numpy oracle producer, {secs:.1f} s"}
+
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    flops = 2.0 * ntok * 576 * hidden
+    nbytes = 576 * hidden * 2 + ntok * hidden * 2 + ntok * BYTES_PER_TOKEN[fmt]  # weight, inputs, pool writes
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    if flops / nbytes > tf_burst * 1e12 / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s", "frac": tflops / tf_burst,
+                "traffic": None, "peak_source": peak_src + " (bf16, burst)", "hbm_gbs": gbs}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "peak_source": peak_src, "tensor_tflops": tflops}
+    line = {
+        "metric": PROJECT_METRIC, "value": ntok / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: {PROJECT[name][3]}", "hidden": hidden, "B": B, "T": T, "cache_fmt": fmt,
+                   "k_split_workspace_bytes": ws_bytes, "l2": "256 MB scrub between timed steps",
+                   "algorithmic_bytes": nbytes, "flops": flops},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": ntok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h_x.numel() * 2,
+                "d2h_bytes_per_step": h_lat.numel() * 2},
+        "gpu_launches": (2 if ws_bytes > 0 else 1) * args.steps,  # the producer (and the workspace clear)
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR))
+    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR) + sorted(PROJECT))
     ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
@@ -408,6 +546,21 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in PROJECT:
+        fmt = args.fmt or "bf16"
+        if args.impl == "reference":
+            if _env_int("RANK", 0) != 0:
+                return 0
+            n, secs = project_oracle_time(args.workload, fmt, 10.0)
+            print(json.dumps({"impl": "reference", "metric": PROJECT_METRIC, "value": n / secs, "unit": "tokens/s",
+                              "n_gpus": args.gpus, "steps": 1, "warmup": 0, "higher_is_better": True,
+                              "dtype": "f64", "data": "synthetic", "config": {"workload": args.workload},
+                              "cpu_baseline": {"value": n / secs, "unit": "tokens/s", "cores": host_cores(),
+                                               "kind": "oracle", "sample": f"{n} tokens"},
+                              "e2e": {"value": n / secs, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+            return 0
+        return run_project(args, args.workload, fmt)
     wl = synth.get_workload(args.workload)
     if args.seqlen is not None:
         if wl.ragged or args.seqlen < 1:

@@ -130,6 +130,50 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
                      int B, int T, cudaStream_t stream);
 
 /*
+ * The step before the append, fused with it: computes each new token's cache
+ * payload from its attention input and writes it like mla_cache_append.
+ * "手搓 MLA" §三: c_kv = rmsnorm(x W_DKV^T, W_KVN), k_pe = rope(x W_KR^T);
+ * "DeepSeek MLA 吸收式缓存" §3.3 names the joint projection wkv_a
+ * (kv_a_proj_with_mqa) and the gain kv_norm.
+ *   x          : bf16 [B][T][hidden], the attention inputs of the new tokens
+ *   hidden     : a multiple of 64 in [64, 65536] (2048 for V2-Lite, 7168 for V3),
+ *                else MLA_ERR_UNSUPPORTED
+ *   wkv_a      : bf16 [576][hidden]; rows 0..511 are W_DKV (the latent), rows
+ *                512..575 W_KR (the shared RoPE key)
+ *   kv_norm_w  : bf16 [512], the RMSNorm gain W_KVN
+ *   eps        : RMSNorm epsilon, >= 0 (1e-6 for these models)
+ *   rope_theta : RoPE base, > 0 (10000 for these models)
+ *   page_table, max_pages, pos, B, T : as for mla_cache_append; token t of row b
+ *                has position pos[b]+t, which also sets its rotation
+ *   latent_out : NULL, or bf16 [B][T][576]: receives each token's payload
+ *                before quantization (c_kv then k_pe, the bf16 values a bf16
+ *                pool would hold), whether or not its page write succeeded
+ *   k_splits   : 0 picks the split of the projection's K dimension by size;
+ *                n > 0 forces n CTA pairs per 128-token tile (capped at hidden/64)
+ *   workspace  : device scratch of >= mla_cache_project_workspace_bytes(B, T,
+ *                hidden, k_splits) bytes, 256-byte aligned (may be NULL when that
+ *                is 0); cleared by the call itself
+ * Per token, in fp32 from bf16 operands: y = wkv_a x (tensor cores, fp32
+ * accumulation); c = y[0..511] / sqrt(mean(y[0..511]^2) + eps) * kv_norm_w;
+ * pairs (2i, 2i+1) of y[512..575] rotated by the angle pos * rope_theta^(-2i/64)
+ * (the angle reduced modulo 2 pi in fp64); each value rounded once to bf16,
+ * then quantized exactly as mla_cache_append does.  With a K split the partial
+ * products are summed by fp32 atomic adds, so the last bit of a value may vary
+ * between runs; without one (many tokens) the result is deterministic.  Bad
+ * positions and page ids are skipped and raise MLA_ERR_BOUNDS as in
+ * mla_cache_append.  x, wkv_a, kv_norm_w and latent_out 16-byte aligned.
+ */
+int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden, const void* wkv_a,
+                             const void* kv_norm_w, float eps, float rope_theta,
+                             const int32_t* page_table, int max_pages, const int32_t* pos,
+                             int B, int T, void* latent_out, int k_splits,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace for mla_cache_project_append on the current device (0 when no K
+ * split is used, or for arguments that call would reject). */
+size_t mla_cache_project_workspace_bytes(int B, int T, int hidden, int k_splits);
+
+/*
  * Workspace needed by mla_decode for B rows and H heads on the current
  * device (the split-KV partials, the query-side latent and the split plan).
  */

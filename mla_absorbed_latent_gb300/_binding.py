@@ -43,6 +43,8 @@ def _load() -> ctypes.CDLL:
         "mla_cache_page_bytes": (sz, [i]),
         "mla_absorb_weights": (i, [vp, i, vp, vp, vp]),
         "mla_cache_append": (i, [cp, vp, vp, vp, i, vp, i, i, vp]),
+        "mla_cache_project_append": (i, [cp, vp, i, vp, vp, f, f, vp, i, vp, i, i, vp, i, vp, sz, vp]),
+        "mla_cache_project_workspace_bytes": (sz, [i, i, i, i]),
         "mla_decode_workspace_bytes": (sz, [i, i]),
         "mla_decode": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, sz, vp, vp]),
         "mla_decode_plan": (i, [i, i, vp, i, i, vp, sz, vp]),
@@ -100,6 +102,19 @@ def mla_cache_append(cache: mla_cache_t, c_kv, k_pe, page_table, max_pages: int,
                      stream=None) -> None:
     _check(_lib.mla_cache_append(ctypes.byref(cache), _ptr(c_kv), _ptr(k_pe), _ptr(page_table), max_pages,
                                  _ptr(pos), B, T, _stream(stream)), "mla_cache_append")
+
+
+def mla_cache_project_workspace_bytes(B: int, T: int, hidden: int, k_splits: int = 0) -> int:
+    return int(_lib.mla_cache_project_workspace_bytes(B, T, hidden, k_splits))
+
+
+def mla_cache_project_append(cache: mla_cache_t, x, hidden: int, wkv_a, kv_norm_w, eps: float, rope_theta: float,
+                             page_table, max_pages: int, pos, B: int, T: int, latent_out=None, k_splits: int = 0,
+                             workspace=None, workspace_bytes: int = 0, stream=None) -> None:
+    _check(_lib.mla_cache_project_append(ctypes.byref(cache), _ptr(x), hidden, _ptr(wkv_a), _ptr(kv_norm_w), eps,
+                                         rope_theta, _ptr(page_table), max_pages, _ptr(pos), B, T, _ptr(latent_out),
+                                         k_splits, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mla_cache_project_append")
 
 
 def mla_decode_workspace_bytes(B: int, H: int) -> int:

@@ -7,11 +7,11 @@
 // 32-channel groups of c_KV, asymmetric INT4 (scale + zero) over 32-channel
 // groups, and INT8 over 8-dim groups of k_pe.  The rounding rules (fp32,
 // round-half-even, bf16 scales) are stated in include/mla.h and are bit-exact
-// by construction: every decision is one IEEE fp32 operation.
+// by construction: every decision is one IEEE fp32 operation (quant.cuh).
 //
 // One warp per token.  bf16: lanes copy 16-byte chunks.  Quantized: lane g < 16
 // owns c_KV group g, lanes 16..23 own the k_pe groups.
-#include "mla_common.cuh"
+#include "quant.cuh"
 
 namespace mla {
 namespace {
@@ -26,32 +26,6 @@ __device__ __forceinline__ void load32(const uint16_t* src, float* x) {
     x[8 * i + 4] = bf16lo(v.z); x[8 * i + 5] = bf16hi(v.z);
     x[8 * i + 6] = bf16lo(v.w); x[8 * i + 7] = bf16hi(v.w);
   }
-}
-
-// Symmetric INT8 of n values: returns the bf16 scale bits, writes codes.
-template <int N>
-__device__ __forceinline__ uint16_t quant_i8(const float* x, int8_t* code) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const __nv_bfloat16 sb = __float2bfloat16_rn(amax / 127.0f);
-  const float s = __bfloat162float(sb);
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    float q = 0.f;
-    if (s != 0.f) q = fminf(fmaxf(rintf(x[i] / s), -127.f), 127.f);
-    code[i] = static_cast<int8_t>(q);
-  }
-  return __bfloat16_as_ushort(sb);
-}
-
-__device__ __forceinline__ void store_i8x8(uint8_t* dst, const int8_t* c) {
-  uint2 v;
-  v.x = (uint32_t)(uint8_t)c[0] | ((uint32_t)(uint8_t)c[1] << 8) | ((uint32_t)(uint8_t)c[2] << 16) |
-        ((uint32_t)(uint8_t)c[3] << 24);
-  v.y = (uint32_t)(uint8_t)c[4] | ((uint32_t)(uint8_t)c[5] << 8) | ((uint32_t)(uint8_t)c[6] << 16) |
-        ((uint32_t)(uint8_t)c[7] << 24);
-  *reinterpret_cast<uint2*>(dst) = v;
 }
 
 __global__ void __launch_bounds__(256) append_kernel(int fmt, int num_pages, uint8_t* __restrict__ pages,
@@ -105,22 +79,12 @@ __global__ void __launch_bounds__(256) append_kernel(int fmt, int num_pages, uin
       for (int i = 0; i < 4; ++i) store_i8x8(dst + 8 * i, code + 8 * i);
       reinterpret_cast<uint16_t*>(page + I8_C_SCALE)[slot * 16 + g] = sb;
     } else {
-      float mn = x[0], mx = x[0];
-#pragma unroll
-      for (int i = 1; i < 32; ++i) { mn = fminf(mn, x[i]); mx = fmaxf(mx, x[i]); }
-      const __nv_bfloat16 sb = __float2bfloat16_rn((mx - mn) / 15.0f);
-      const __nv_bfloat16 zb = __float2bfloat16_rn(mn);
-      const float s = __bfloat162float(sb), z = __bfloat162float(zb);
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        uint32_t q = 0u;
-        if (s != 0.f) q = (uint32_t)fminf(fmaxf(rintf((x[i] - z) / s), 0.f), 15.f);
-        w[i / 8] |= q << (4 * (i % 8));
-      }
+      uint32_t w[4];
+      uint16_t sb, zb;
+      quant_i4_32(x, w, &sb, &zb);
       *reinterpret_cast<uint4*>(page + I4_C_CODE + slot * (DC / 2) + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint16_t*>(page + I4_C_SCALE)[slot * 16 + g] = __bfloat16_as_ushort(sb);
-      reinterpret_cast<uint16_t*>(page + I4_C_ZERO)[slot * 16 + g] = __bfloat16_as_ushort(zb);
+      reinterpret_cast<uint16_t*>(page + I4_C_SCALE)[slot * 16 + g] = sb;
+      reinterpret_cast<uint16_t*>(page + I4_C_ZERO)[slot * 16 + g] = zb;
     }
   } else if (lane < 24) {
     const int g = lane - 16;

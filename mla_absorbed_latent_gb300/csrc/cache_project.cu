@@ -1,0 +1,440 @@
+// Cache producer: the step before the append, fused with it.
+//
+// "手搓 MLA" §三 derives what the absorbed cache holds from each token's
+// attention input x: c_kv = rmsnorm(x W_DKV^T, W_KVN) (512 wide) and
+// k_pe = rope(x W_KR^T) (64 wide).  "DeepSeek MLA 吸收式缓存" §3.3 names the
+// joint projection wkv_a (kv_a_proj_with_mqa: rows 0..511 are W_DKV, rows
+// 512..575 W_KR) and the gain kv_norm.  Here the projection runs on the
+// fifth-generation tensor cores and the epilogue finishes every token: the
+// RMSNorm, the rotation, one bf16 rounding, then the page write of
+// mla_cache_append (quantized per the pool's format, quant.cuh).
+//
+// Tiling.  A CTA pair (2-CTA cluster) owns a tile of 128 tokens; CTA r
+// computes latent columns [256r, 256r+256) and RoPE-key columns
+// [512+32r, 512+32r+32): M = 128 tokens, N = 256 + 32, K = hidden in 64-wide
+// chunks through a 4-stage TMA ring (x tile 16 KB, weight tiles 32 + 4 KB, all
+// 128B-swizzled, K-major).  The 288 fp32 accumulator columns fit in the CTA's
+// tensor memory (the full 576 would not).  The RMSNorm needs both halves' sums
+// of squares: the pair swaps its per-token sums (128 floats) through
+// distributed shared memory.  A RoPE pair (2i, 2i+1) never straddles the two
+// halves.
+//
+// Few tokens (decode appends one per row) would leave most SMs idle and read
+// the 576 x hidden weight through two of them, so the hidden dimension is then
+// split over `ksplit` CTA pairs per token tile: each adds its partial product
+// into an fp32 accumulator in the caller's workspace (atomic adds: the
+// summation order, and so the last bit of a result, can vary between runs), and
+// the last pair to finish (a ticket counter per tile) loads the sums into its
+// tensor memory and runs the same epilogue.
+//
+// Thread roles (128 threads): lane 0 of warp 0 issues the TMA loads, lane 0 of
+// warp 1 the MMAs; then all four warps run the epilogue, warp w on the tokens
+// of TMEM lanes 32w..32w+31 (one token per thread).  Every mbarrier wait is
+// bounded; a timeout is recorded as MLA_ERR_TIMEOUT.
+#include <cmath>
+
+#include "quant.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int PJ_ROWS = 128;                  // tokens per tile (MMA M)
+constexpr int PJ_STAGES = 4;
+constexpr int PJ_THREADS = 128;
+constexpr int PJ_HALF = DC / 2;               // latent columns per CTA
+constexpr int PJ_ROPE = DR / 2;               // RoPE-key columns per CTA
+constexpr uint32_t PJ_X_TILE = PJ_ROWS * 128;   // 16 KB: 128 tokens x 64 hidden
+constexpr uint32_t PJ_WC_TILE = PJ_HALF * 128;  // 32 KB: 256 latent rows of wkv_a x 64 hidden
+constexpr uint32_t PJ_WR_TILE = PJ_ROPE * 128;  // 4 KB: 32 RoPE-key rows x 64 hidden
+constexpr uint32_t PJ_STAGE_BYTES = PJ_X_TILE + PJ_WC_TILE + PJ_WR_TILE;
+constexpr uint32_t PJ_TMEM_COLS = 512;        // 288 used: latent half at 0, RoPE key at 256
+
+struct RopeFreq {
+  double f[DR / 2];  // theta^(-2i/64), i = 0..31
+};
+
+struct __align__(1024) PjSmem {
+  uint8_t x[PJ_STAGES][PJ_X_TILE];
+  uint8_t wc[PJ_STAGES][PJ_WC_TILE];
+  uint8_t wr[PJ_STAGES][PJ_WR_TILE];
+  float gamma[PJ_HALF];  // kv_norm gain of this CTA's latent columns
+  float ss[PJ_ROWS];     // per-token sum of squares of this CTA's latent columns (read by the peer)
+  double freq[PJ_ROPE / 2];  // rotation frequencies of this CTA's 16 RoPE pairs
+  uint64_t full[PJ_STAGES], empty[PJ_STAGES], mma_done;
+  uint32_t tmem_base;
+  int last;      // split mode: this pair runs the epilogue of its tile
+  int issued;    // chunks whose loads the producer issued
+  int consumed;  // chunks whose loads the MMA issuer saw land
+};
+
+__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// sin and cos of pos * freq: the angle is formed and reduced modulo 2 pi in fp64
+// (Cody and Waite's two-constant reduction), then sincosf on the reduced angle
+__device__ __forceinline__ void rope_sincos(double pos, double freq, float* s, float* c) {
+  const double a = pos * freq;
+  const double k = rint(a * 0.15915494309189535);   // a / (2 pi), to the nearest integer
+  double r = fma(-k, 6.283185307179586, a);          // 2 pi = 6.283185307179586 + 2.4492935982947064e-16
+  r = fma(-k, 2.4492935982947064e-16, r);
+  sincosf((float)r, s, c);
+}
+
+__device__ __forceinline__ void store_bf16x32(uint8_t* dst, const float* y) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d[q] = make_uint4(pack_bf16x2(y[8 * q], y[8 * q + 1]), pack_bf16x2(y[8 * q + 2], y[8 * q + 3]),
+                      pack_bf16x2(y[8 * q + 4], y[8 * q + 5]), pack_bf16x2(y[8 * q + 6], y[8 * q + 7]));
+}
+
+// Writes 32 finished (bf16-representable) values of one token: `col` is the
+// position of y[0] in the 576-wide payload (a multiple of 32); `page` the
+// token's physical page (nullptr: no page write), `slot` its slot.
+__device__ __forceinline__ void write_group32(const float* y, int col, int fmt, uint8_t* page, int slot,
+                                              uint8_t* latent_row) {
+  if (latent_row != nullptr) store_bf16x32(latent_row + col * 2, y);
+  if (page == nullptr) return;
+  if (fmt == MLA_FMT_BF16) {
+    store_bf16x32(page + (size_t)slot * DK * 2 + col * 2, y);
+    return;
+  }
+  if (col < DC) {
+    const int g = col / 32;
+    if (fmt == MLA_FMT_INT8) {
+      int8_t code[32];
+      const uint16_t sb = quant_i8<32>(y, code);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) store_i8x8(page + I8_C_CODE + slot * DC + col + 8 * i, code + 8 * i);
+      reinterpret_cast<uint16_t*>(page + I8_C_SCALE)[slot * 16 + g] = sb;
+    } else {
+      uint32_t w[4];
+      uint16_t sb, zb;
+      quant_i4_32(y, w, &sb, &zb);
+      *reinterpret_cast<uint4*>(page + I4_C_CODE + slot * (DC / 2) + col / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint16_t*>(page + I4_C_SCALE)[slot * 16 + g] = sb;
+      reinterpret_cast<uint16_t*>(page + I4_C_ZERO)[slot * 16 + g] = zb;
+    }
+    return;
+  }
+  // RoPE key: INT8 in groups of 8 dims in both quantized formats
+  const int pe_code_off = fmt == MLA_FMT_INT8 ? I8_PE_CODE : I4_PE_CODE;
+  const int pe_scale_off = fmt == MLA_FMT_INT8 ? I8_PE_SCALE : I4_PE_SCALE;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int d = col - DC + 8 * q;  // first RoPE dim of the group
+    int8_t code[8];
+    const uint16_t sb = quant_i8<8>(y + 8 * q, code);
+    store_i8x8(page + pe_code_off + slot * DR + d, code);
+    reinterpret_cast<uint16_t*>(page + pe_scale_off)[slot * 8 + d / 8] = sb;
+  }
+}
+
+__global__ void __launch_bounds__(PJ_THREADS, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wc,
+                   const __grid_constant__ CUtensorMap tm_wr, const uint16_t* __restrict__ kv_norm_w, float eps,
+                   const RopeFreq freq, int fmt, int num_pages, uint8_t* __restrict__ pages,
+                   const int32_t* __restrict__ page_table, int max_pages, const int32_t* __restrict__ pos, int T,
+                   int ntok, int chunks, int ksplit, uint16_t* __restrict__ latent_out, float* __restrict__ acc,
+                   int* __restrict__ tickets, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  PjSmem& S = *reinterpret_cast<PjSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int mt = pair / ksplit, split = pair - mt * ksplit;
+  const int tok0 = mt * PJ_ROWS;
+  const int c_begin = (int)((long long)split * chunks / ksplit);
+  const int nk = (int)((long long)(split + 1) * chunks / ksplit) - c_begin;
+
+  if (tid == 0) {
+    for (int s = 0; s < PJ_STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.mma_done, 1);
+    S.issued = 0;
+    S.consumed = 0;
+    S.last = 0;
+    fence_barrier_init();
+  }
+  for (int i = tid; i < PJ_HALF; i += PJ_THREADS)
+    S.gamma[i] = __uint_as_float((uint32_t)kv_norm_w[PJ_HALF * rank + i] << 16);
+  if (tid < PJ_ROPE / 2) S.freq[tid] = rank == 0 ? freq.f[tid] : freq.f[PJ_ROPE / 2 + tid];
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, PJ_TMEM_COLS);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % PJ_STAGES;
+      if (i >= PJ_STAGES && !mbar_wait(&S.empty[s], (uint32_t)((i / PJ_STAGES) - 1) & 1u)) {
+        raise_error(err, MLA_ERR_TIMEOUT, 20);
+        break;
+      }
+      const int k = (c_begin + i) * 64;
+      mbar_arrive_expect_tx(&S.full[s], PJ_STAGE_BYTES);
+      tma_load_3d_hint(S.x[s], &tm_x, k, tok0, 0, &S.full[s], pol_x);  // token rows past ntok read as zeros
+      tma_load_3d_hint(S.wc[s], &tm_wc, k, PJ_HALF * rank, 0, &S.full[s], pol_w);
+      tma_load_3d_hint(S.wr[s], &tm_wr, k, DC + PJ_ROPE * rank, 0, &S.full[s], pol_w);
+    }
+    S.issued = i;
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: D_lat[128 x 256] (+)= X . Wc^T, D_rope[128 x 32] (+)= X . Wr^T
+    const uint32_t id_c = idesc_bf16_f32(PJ_ROWS, PJ_HALF, false, false);
+    const uint32_t id_r = idesc_bf16_f32(PJ_ROWS, PJ_ROPE, false, false);
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % PJ_STAGES;
+      if (!mbar_wait(&S.full[s], (uint32_t)(i / PJ_STAGES) & 1u)) {
+        raise_error(err, MLA_ERR_TIMEOUT, 21);
+        break;
+      }
+      fence_after_sync();
+      const uint64_t ad = smem_desc(smem_u32(S.x[s]), 16, 1024, SWIZZLE_128B);
+      const uint64_t bc = smem_desc(smem_u32(S.wc[s]), 16, 1024, SWIZZLE_128B);
+      const uint64_t br = smem_desc(smem_u32(S.wr[s]), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // K = 16 per MMA: 32 bytes further along the swizzled row
+        const uint32_t accum = (i | kk) != 0 ? 1u : 0u;
+        mma_ss(tmem, ad + (uint64_t)(kk * 2), bc + (uint64_t)(kk * 2), id_c, accum);
+        mma_ss(tmem + PJ_HALF, ad + (uint64_t)(kk * 2), br + (uint64_t)(kk * 2), id_r, accum);
+      }
+      mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
+    }
+    S.consumed = i;
+    mma_commit(&S.mma_done);  // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+  if (!mbar_wait(&S.mma_done, 0)) raise_error(err, MLA_ERR_TIMEOUT, 22);
+  __syncwarp();
+  fence_after_sync();
+  __syncthreads();  // S.issued / S.consumed are final
+  if (warp == 0 && lane == 0) {
+    // loads issued but never seen landing (only after a timeout): let them land before exit
+    for (int i = S.consumed; i < S.issued; ++i)
+      if (!mbar_wait(&S.full[i % PJ_STAGES], (uint32_t)(i / PJ_STAGES) & 1u)) break;
+  }
+
+  const int row = warp * 32 + lane;
+  const int tok = tok0 + row;
+  const bool live = tok < ntok;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+
+  bool run = true;
+  if (ksplit > 1) {
+    // add this pair's partial product into the tile's fp32 sums
+    float* arow = acc + (size_t)tok * DK;
+    for (int cc = 0; cc < 9; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + 32 * cc, v);
+      tmem_ld_wait();
+      if (live) {
+        const int col = cc < 8 ? PJ_HALF * rank + 32 * cc : DC + PJ_ROPE * rank;
+        float4* dst = reinterpret_cast<float4*>(arow + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          atomicAdd(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+      }
+    }
+    __threadfence();
+    fence_before_sync();
+    cluster_sync();  // both CTAs' adds are issued and fenced
+    if (rank == 0 && tid == 0) {
+      const int t = atomicAdd(tickets + mt, 1);
+      const int last = t == ksplit - 1 ? 1 : 0;
+      S.last = last;
+      st_cluster_u32(mapa(smem_u32(&S.last), 1u), (uint32_t)last);
+    }
+    cluster_sync();
+    run = S.last != 0;  // the same in both CTAs of the pair
+    fence_after_sync();
+    if (run) {
+      __threadfence();
+      for (int cc = 0; cc < 9; ++cc) {
+        uint32_t v[32];
+        if (live) {
+          const int col = cc < 8 ? PJ_HALF * rank + 32 * cc : DC + PJ_ROPE * rank;
+          const float4* src = reinterpret_cast<const float4*>(arow + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = __ldcg(src + q);
+            v[4 * q] = __float_as_uint(f.x);
+            v[4 * q + 1] = __float_as_uint(f.y);
+            v[4 * q + 2] = __float_as_uint(f.z);
+            v[4 * q + 3] = __float_as_uint(f.w);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = 0u;
+        }
+        tmem_st32(trow + 32 * cc, v);
+      }
+      tmem_st_wait();
+    }
+  }
+
+  if (run) {
+    // the token's slot in the pool (and the position its key is rotated by)
+    uint8_t* page = nullptr;
+    int slot = 0;
+    long long p = 0;
+    if (live) {
+      const int b = tok / T, t = tok - b * T;
+      const int p0 = pos[b];
+      p = (long long)p0 + t;
+      if (p0 < 0 || p >= (long long)max_pages * PAGE) {
+        raise_error(err, MLA_ERR_BOUNDS, b);
+      } else {
+        const int phys = page_table[(size_t)b * max_pages + (int)(p / PAGE)];
+        if (phys < 0 || phys >= num_pages) {
+          raise_error(err, MLA_ERR_BOUNDS, phys);
+        } else {
+          const size_t pb = fmt == MLA_FMT_BF16 ? PAGE_BYTES_BF16 : fmt == MLA_FMT_INT8 ? PAGE_BYTES_INT8
+                                                                                       : PAGE_BYTES_INT4;
+          page = pages + (size_t)phys * pb;
+          slot = (int)(p % PAGE);
+        }
+      }
+    }
+    uint8_t* lrow = (live && latent_out != nullptr) ? reinterpret_cast<uint8_t*>(latent_out + (size_t)tok * DK)
+                                                    : nullptr;
+
+    // RMSNorm: sum of squares over this CTA's 256 columns, plus the peer's
+    float ss = 0.f;
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + 32 * cc, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = __uint_as_float(v[j]);
+        ss = fmaf(a, a, ss);
+      }
+    }
+    S.ss[row] = ss;
+    cluster_sync();
+    const float tot = ss + ld_cluster_f32(mapa(smem_u32(&S.ss[row]), (uint32_t)rank ^ 1u));
+    const float rinv = rsqrtf(tot * (1.0f / DC) + eps);
+
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + 32 * cc, v);
+      tmem_ld_wait();
+      if (live) {
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = bf16r(__uint_as_float(v[j]) * rinv * S.gamma[32 * cc + j]);
+        write_group32(y, PJ_HALF * rank + 32 * cc, fmt, page, slot, lrow);
+      }
+    }
+    {
+      uint32_t v[32];
+      tmem_ld32(trow + PJ_HALF, v);
+      tmem_ld_wait();
+      if (live) {
+        float y[32];
+        const double pd = (double)p;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float sn, cs;
+          rope_sincos(pd, S.freq[j / 2], &sn, &cs);
+          const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
+          y[j] = bf16r(a * cs - b * sn);
+          y[j + 1] = bf16r(a * sn + b * cs);
+        }
+        write_group32(y, DC + PJ_ROPE * rank, fmt, page, slot, lrow);
+      }
+    }
+  }
+
+  fence_before_sync();
+  cluster_sync();  // the peer has read S.ss; nothing touches TMEM any more
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc(tmem, PJ_TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int project_splits(long long ntok, int hidden, int sms, int requested) {
+  const int chunks = hidden / 64;
+  const long long mtiles = (ntok + PJ_ROWS - 1) / PJ_ROWS;
+  if (chunks <= 0 || mtiles <= 0) return 1;
+  if (requested > 0) return requested < chunks ? requested : chunks;
+  if (2 * mtiles >= sms) return 1;
+  const int want = (int)(sms / (2 * mtiles));
+  const int cap = chunks / 4 > 1 ? chunks / 4 : 1;  // at least four 64-wide chunks of hidden per pair
+  const int k = want < cap ? want : cap;
+  return k > 1 ? k : 1;
+}
+
+size_t project_workspace_bytes(long long ntok, int ksplit) {
+  if (ksplit <= 1 || ntok <= 0) return 0;
+  const long long mtiles = (ntok + PJ_ROWS - 1) / PJ_ROWS;
+  return align_up((size_t)mtiles * PJ_ROWS * DK * 4, 256) + align_up((size_t)mtiles * 4, 256);
+}
+
+cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, const void* kv_norm_w, float eps,
+                                 float rope_theta, int fmt, int num_pages, void* pages, const int32_t* page_table,
+                                 int max_pages, const int32_t* pos, int B, int T, void* latent_out, int ksplit,
+                                 void* workspace, int* err, cudaStream_t s) {
+  const long long ntok = (long long)B * T;
+  if (ntok == 0) return cudaSuccess;
+  const long long mtiles = (ntok + PJ_ROWS - 1) / PJ_ROWS;
+  const int chunks = hidden / 64;
+  CUtensorMap tm_x, tm_wc, tm_wr;
+  // x: (hidden, tokens) bf16, boxes of 64 x 128; wkv_a: (hidden, 576), boxes of 64 x 256 and 64 x 32
+  if (!encode_3d(&tm_x, x, (uint64_t)hidden, (uint64_t)ntok, 1, (uint64_t)hidden * 2, (uint64_t)ntok * hidden * 2, 64,
+                 PJ_ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_3d(&tm_wc, wkv_a, (uint64_t)hidden, DK, 1, (uint64_t)hidden * 2, (uint64_t)DK * hidden * 2, 64, PJ_HALF,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_3d(&tm_wr, wkv_a, (uint64_t)hidden, DK, 1, (uint64_t)hidden * 2, (uint64_t)DK * hidden * 2, 64, PJ_ROPE,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  RopeFreq fr;
+  for (int i = 0; i < DR / 2; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / DR);
+  float* acc = nullptr;
+  int* tickets = nullptr;
+  if (ksplit > 1) {
+    const size_t acc_bytes = align_up((size_t)mtiles * PJ_ROWS * DK * 4, 256);
+    acc = static_cast<float*>(workspace);
+    tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + acc_bytes);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, project_workspace_bytes(ntok, ksplit), s);
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = sizeof(PjSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * mtiles * ksplit));
+  cfg.blockDim = dim3(PJ_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, project_kernel, tm_x, tm_wc, tm_wr, static_cast<const uint16_t*>(kv_norm_w), eps,
+                            fr, fmt, num_pages, static_cast<uint8_t*>(pages), page_table, max_pages, pos, T,
+                            (int)ntok, chunks, ksplit, static_cast<uint16_t*>(latent_out), acc, tickets, err);
+}
+
+}  // namespace mla

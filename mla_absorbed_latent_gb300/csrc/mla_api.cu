@@ -50,6 +50,10 @@ int num_sms() {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool heads_ok(int H) { return H == 16 || H == 128; }
 bool fmt_ok(int fmt) { return fmt == MLA_FMT_BF16 || fmt == MLA_FMT_INT8 || fmt == MLA_FMT_INT4; }
+// hidden width of the cache producer's input: whole 64-wide chunks of the projection's K
+bool hidden_ok(int hidden) { return hidden >= 64 && hidden <= 65536 && hidden % 64 == 0; }
+// the producer indexes tokens with 32-bit integers
+constexpr long long MAX_PROJECT_TOKENS = 2147483647LL - 128;
 
 size_t page_bytes(int fmt) {
   switch (fmt) {
@@ -119,6 +123,45 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
   if (err == nullptr) return MLA_ERR_CUDA;
   return status_of(launch_cache_append(cache->fmt, cache->num_pages, cache->pages, c_kv, k_pe, page_table, max_pages,
                                        pos, B, T, err, stream));
+}
+
+size_t mla_cache_project_workspace_bytes(int B, int T, int hidden, int k_splits) {
+  if (B < 0 || T < 0 || k_splits < 0 || !hidden_ok(hidden)) return 0;
+  const long long ntok = (long long)B * T;
+  if (ntok > MAX_PROJECT_TOKENS) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  return project_workspace_bytes(ntok, project_splits(ntok, hidden, sms, k_splits));
+}
+
+int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden, const void* wkv_a,
+                             const void* kv_norm_w, float eps, float rope_theta, const int32_t* page_table,
+                             int max_pages, const int32_t* pos, int B, int T, void* latent_out, int k_splits,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (cache == nullptr) return MLA_ERR_INVALID;
+  if (!fmt_ok(cache->fmt) || !hidden_ok(hidden)) return MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache) || B < 0 || T < 0 || max_pages <= 0 || k_splits < 0) return MLA_ERR_INVALID;
+  const long long ntok = (long long)B * T;
+  if (ntok == 0) return MLA_OK;
+  if (ntok > MAX_PROJECT_TOKENS) return MLA_ERR_UNSUPPORTED;
+  if (!x || !wkv_a || !kv_norm_w || !page_table || !pos || !aligned(x, 16) || !aligned(wkv_a, 16) ||
+      !aligned(kv_norm_w, 16) || !aligned(page_table, 4) || !aligned(pos, 4) ||
+      (latent_out != nullptr && !aligned(latent_out, 16)))
+    return MLA_ERR_INVALID;
+  if (!(eps >= 0.f) || eps == INFINITY || !(rope_theta > 0.f) || rope_theta == INFINITY) return MLA_ERR_INVALID;
+  const int sms = num_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const int ksplit = project_splits(ntok, hidden, sms, k_splits);
+  const size_t need = project_workspace_bytes(ntok, ksplit);
+  if (need > 0) {
+    if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
+    if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  }
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  return status_of(launch_cache_project(x, hidden, wkv_a, kv_norm_w, eps, rope_theta, cache->fmt, cache->num_pages,
+                                        cache->pages, page_table, max_pages, pos, B, T, latent_out, ksplit,
+                                        workspace, err, stream));
 }
 
 size_t mla_decode_workspace_bytes(int B, int H) {

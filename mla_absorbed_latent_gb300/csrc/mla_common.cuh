@@ -166,6 +166,16 @@ cudaError_t launch_absorb_weights(const void* wkv_b, int H, void* W_UK, void* W_
 cudaError_t launch_cache_append(int fmt, int num_pages, void* pages, const void* c_kv, const void* k_pe,
                                 const int32_t* page_table, int max_pages, const int32_t* pos, int B, int T,
                                 int* err, cudaStream_t s);
+// fused producer of the cache payload (cache_project.cu): down-projection on the
+// tensor cores, RMSNorm, RoPE, page write; ksplit pairs per 128-token tile
+cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, const void* kv_norm_w, float eps,
+                                 float rope_theta, int fmt, int num_pages, void* pages, const int32_t* page_table,
+                                 int max_pages, const int32_t* pos, int B, int T, void* latent_out, int ksplit,
+                                 void* workspace, int* err, cudaStream_t s);
+// CTA pairs per token tile that the producer uses (`requested` > 0 forces it, capped at hidden/64)
+int project_splits(long long ntok, int hidden, int sms, int requested);
+// workspace of the producer for ntok tokens and ksplit pairs per tile (0 when ksplit is 1)
+size_t project_workspace_bytes(long long ntok, int ksplit);
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
                             cudaStream_t s);
 cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,

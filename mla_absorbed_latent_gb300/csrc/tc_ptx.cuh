@@ -32,6 +32,12 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// 32-bit load from another CTA's shared memory (cluster address)
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // bulk copy of `bytes` from this CTA's shared memory into another CTA's shared
 // memory (cluster address), completion counted on that CTA's mbarrier
 __device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes,

@@ -62,6 +62,22 @@ def test_host_validation_without_gpu(lib):
                           None) == m.MLA_ERR_UNSUPPORTED
     assert raw.mla_decode_workspace_bytes(-1, 128) == 0
     assert raw.mla_decode_workspace_bytes(4, 3) == 0
+    # the fused producer: hidden must be whole 64-wide chunks; empty batches enqueue nothing
+    proj = raw.mla_cache_project_append
+    assert proj(ctypes.byref(cache), None, 100, None, None, 1e-6, 1e4, None, 1, None, 1, 1, None, 0, None, 0,
+                None) == m.MLA_ERR_UNSUPPORTED
+    assert proj(ctypes.byref(bad_fmt), None, 2048, None, None, 1e-6, 1e4, None, 1, None, 1, 1, None, 0, None, 0,
+                None) == m.MLA_ERR_UNSUPPORTED
+    assert proj(None, None, 2048, None, None, 1e-6, 1e4, None, 1, None, 1, 1, None, 0, None, 0,
+                None) == m.MLA_ERR_INVALID
+    assert proj(ctypes.byref(cache), None, 2048, None, None, 1e-6, 1e4, None, 1, None, 1, 1, None, -1, None, 0,
+                None) == m.MLA_ERR_INVALID
+    assert proj(ctypes.byref(cache), None, 2048, None, None, 1e-6, 1e4, None, 1, None, 0, 7, None, 0, None, 0,
+                None) == m.MLA_OK
+    assert proj(ctypes.byref(cache), None, 2048, None, None, 1e-6, 1e4, None, 1, None, 2, 1, None, 0, None, 0,
+                None) == m.MLA_ERR_INVALID   # null inputs
+    assert raw.mla_cache_project_workspace_bytes(1, 1, 100, 0) == 0
+    assert raw.mla_cache_project_workspace_bytes(-1, 1, 2048, 0) == 0
 
 
 def test_status_strings(lib):
