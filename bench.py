@@ -448,14 +448,15 @@ def run_project(args, name, fmt):
     cache = mla.cache_struct(fmt, num_pages, pool)
     pt = torch.from_numpy(table).cuda()
     pos = torch.from_numpy(pos0).cuda()
-    ws_bytes = mla.mla_cache_project_workspace_bytes(B, T, hidden, 0)
+    ksplit = args.k_splits
+    ws_bytes = mla.mla_cache_project_workspace_bytes(B, T, hidden, ksplit)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")  # > L2: scrubbed between steps
 
     def call(xin=dev_x, latent=None):
         mla.mla_cache_project_append(cache, xin, hidden, dev_w, dev_g, PROJECT_EPS, PROJECT_THETA, pt,
-                                     table.shape[1], pos, B, T, latent, 0, ws, ws_bytes, stream)
+                                     table.shape[1], pos, B, T, latent, ksplit, ws, ws_bytes, stream)
 
     for _ in range(args.warmup):
         call()
@@ -518,7 +519,7 @@ def run_project(args, name, fmt):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{name}: {PROJECT[name][3]}", "hidden": hidden, "B": B, "T": T, "cache_fmt": fmt,
-                   "k_split_workspace_bytes": ws_bytes, "l2": "256 MB scrub between timed steps",
+                   "k_splits": ksplit or "auto", "k_split_workspace_bytes": ws_bytes, "l2": "256 MB scrub between timed steps",
                    "algorithmic_bytes": nbytes, "flops": flops},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -542,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--k-splits", type=int, default=0,
+                    help="producer workloads: CTA pairs per 128-token tile over the hidden dimension (0 = by size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -90,20 +90,14 @@ __device__ __forceinline__ void store_bf16x32(uint8_t* dst, const float* y) {
                       pack_bf16x2(y[8 * q + 4], y[8 * q + 5]), pack_bf16x2(y[8 * q + 6], y[8 * q + 7]));
 }
 
-// Writes 32 finished (bf16-representable) values of one token: `col` is the
-// position of y[0] in the 576-wide payload (a multiple of 32); `page` the
-// token's physical page (nullptr: no page write), `slot` its slot.
-__device__ __forceinline__ void write_group32(const float* y, int col, int fmt, uint8_t* page, int slot,
-                                              uint8_t* latent_row) {
-  if (latent_row != nullptr) store_bf16x32(latent_row + col * 2, y);
-  if (page == nullptr) return;
-  if (fmt == MLA_FMT_BF16) {
-    store_bf16x32(page + (size_t)slot * DK * 2 + col * 2, y);
-    return;
-  }
+// Quantized page write of 32 finished (bf16-representable) values of one token
+// (out of line: one copy of the quantizer code, called once per 32-value group).
+// `col` is the position of y[0] in the 576-wide payload (a multiple of 32).
+template <int FMT>
+__device__ __noinline__ void write_quantized32(const float* y, int col, uint8_t* page, int slot) {
   if (col < DC) {
     const int g = col / 32;
-    if (fmt == MLA_FMT_INT8) {
+    if (FMT == MLA_FMT_INT8) {
       int8_t code[32];
       const uint16_t sb = quant_i8<32>(y, code);
 #pragma unroll
@@ -120,9 +114,9 @@ __device__ __forceinline__ void write_group32(const float* y, int col, int fmt, 
     return;
   }
   // RoPE key: INT8 in groups of 8 dims in both quantized formats
-  const int pe_code_off = fmt == MLA_FMT_INT8 ? I8_PE_CODE : I4_PE_CODE;
-  const int pe_scale_off = fmt == MLA_FMT_INT8 ? I8_PE_SCALE : I4_PE_SCALE;
-#pragma unroll
+  constexpr int pe_code_off = FMT == MLA_FMT_INT8 ? I8_PE_CODE : I4_PE_CODE;
+  constexpr int pe_scale_off = FMT == MLA_FMT_INT8 ? I8_PE_SCALE : I4_PE_SCALE;
+#pragma unroll 1
   for (int q = 0; q < 4; ++q) {
     const int d = col - DC + 8 * q;  // first RoPE dim of the group
     int8_t code[8];
@@ -132,10 +126,24 @@ __device__ __forceinline__ void write_group32(const float* y, int col, int fmt, 
   }
 }
 
+// Writes 32 finished values of one token: to the optional bf16 payload row and,
+// when `page` is not null, to the token's slot in the pool.
+template <int FMT>
+__device__ __forceinline__ void write_group32(const float* y, int col, uint8_t* page, int slot,
+                                              uint8_t* latent_row) {
+  if (latent_row != nullptr) store_bf16x32(latent_row + col * 2, y);
+  if (page == nullptr) return;
+  if (FMT == MLA_FMT_BF16)
+    store_bf16x32(page + (size_t)slot * DK * 2 + col * 2, y);
+  else
+    write_quantized32<FMT>(y, col, page, slot);
+}
+
+template <int FMT>
 __global__ void __launch_bounds__(PJ_THREADS, 1)
     project_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wc,
                    const __grid_constant__ CUtensorMap tm_wr, const uint16_t* __restrict__ kv_norm_w, float eps,
-                   const RopeFreq freq, int fmt, int num_pages, uint8_t* __restrict__ pages,
+                   const RopeFreq freq, int num_pages, uint8_t* __restrict__ pages,
                    const int32_t* __restrict__ page_table, int max_pages, const int32_t* __restrict__ pos, int T,
                    int ntok, int chunks, int ksplit, uint16_t* __restrict__ latent_out, float* __restrict__ acc,
                    int* __restrict__ tickets, int* err) {
@@ -235,17 +243,17 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   if (ksplit > 1) {
     // add this pair's partial product into the tile's fp32 sums
     float* arow = acc + (size_t)tok * DK;
+#pragma unroll 1
     for (int cc = 0; cc < 9; ++cc) {
       uint32_t v[32];
       tmem_ld32(trow + 32 * cc, v);
       tmem_ld_wait();
       if (live) {
         const int col = cc < 8 ? PJ_HALF * rank + 32 * cc : DC + PJ_ROPE * rank;
-        float4* dst = reinterpret_cast<float4*>(arow + col);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          atomicAdd(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+          red_add_v4(arow + col + 4 * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
       }
     }
     __threadfence();
@@ -262,6 +270,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     fence_after_sync();
     if (run) {
       __threadfence();
+#pragma unroll 1
       for (int cc = 0; cc < 9; ++cc) {
         uint32_t v[32];
         if (live) {
@@ -301,8 +310,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
         if (phys < 0 || phys >= num_pages) {
           raise_error(err, MLA_ERR_BOUNDS, phys);
         } else {
-          const size_t pb = fmt == MLA_FMT_BF16 ? PAGE_BYTES_BF16 : fmt == MLA_FMT_INT8 ? PAGE_BYTES_INT8
-                                                                                       : PAGE_BYTES_INT4;
+          constexpr size_t pb = FMT == MLA_FMT_BF16   ? PAGE_BYTES_BF16
+                                : FMT == MLA_FMT_INT8 ? PAGE_BYTES_INT8
+                                                      : PAGE_BYTES_INT4;
           page = pages + (size_t)phys * pb;
           slot = (int)(p % PAGE);
         }
@@ -313,6 +323,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 
     // RMSNorm: sum of squares over this CTA's 256 columns, plus the peer's
     float ss = 0.f;
+#pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       uint32_t v[32];
       tmem_ld32(trow + 32 * cc, v);
@@ -328,6 +339,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     const float tot = ss + ld_cluster_f32(mapa(smem_u32(&S.ss[row]), (uint32_t)rank ^ 1u));
     const float rinv = rsqrtf(tot * (1.0f / DC) + eps);
 
+#pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       uint32_t v[32];
       tmem_ld32(trow + 32 * cc, v);
@@ -336,25 +348,34 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = bf16r(__uint_as_float(v[j]) * rinv * S.gamma[32 * cc + j]);
-        write_group32(y, PJ_HALF * rank + 32 * cc, fmt, page, slot, lrow);
+        write_group32<FMT>(y, PJ_HALF * rank + 32 * cc, page, slot, lrow);
       }
     }
     {
+      // cos and sin of this token's 16 rotation angles, one at a time (a rolled
+      // loop keeps one copy of that code), into the first x stage of the ring,
+      // free now that every MMA has completed: [pair][token] float2
+      float2* rot = reinterpret_cast<float2*>(S.x[0]);
+      const double pd = (double)p;
+#pragma unroll 1
+      for (int i = 0; i < PJ_ROPE / 2; ++i) {
+        float sn, cs;
+        rope_sincos(pd, S.freq[i], &sn, &cs);
+        rot[i * PJ_ROWS + row] = make_float2(cs, sn);
+      }
       uint32_t v[32];
       tmem_ld32(trow + PJ_HALF, v);
       tmem_ld_wait();
       if (live) {
         float y[32];
-        const double pd = (double)p;
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          float sn, cs;
-          rope_sincos(pd, S.freq[j / 2], &sn, &cs);
+          const float2 r = rot[(j / 2) * PJ_ROWS + row];
           const float a = __uint_as_float(v[j]), b = __uint_as_float(v[j + 1]);
-          y[j] = bf16r(a * cs - b * sn);
-          y[j + 1] = bf16r(a * sn + b * cs);
+          y[j] = bf16r(a * r.x - b * r.y);
+          y[j + 1] = bf16r(a * r.y + b * r.x);
         }
-        write_group32(y, DC + PJ_ROPE * rank, fmt, page, slot, lrow);
+        write_group32<FMT>(y, DC + PJ_ROPE * rank, page, slot, lrow);
       }
     }
   }
@@ -418,7 +439,12 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
     if (e != cudaSuccess) return e;
   }
   const size_t smem = sizeof(PjSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, const uint16_t*, float, RopeFreq, int, uint8_t*,
+                 const int32_t*, int, const int32_t*, int, int, int, int, uint16_t*, float*, int*, int*) =
+      fmt == MLA_FMT_BF16 ? project_kernel<MLA_FMT_BF16>
+      : fmt == MLA_FMT_INT8 ? project_kernel<MLA_FMT_INT8>
+                            : project_kernel<MLA_FMT_INT4>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * mtiles * ksplit));
@@ -432,9 +458,9 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, project_kernel, tm_x, tm_wc, tm_wr, static_cast<const uint16_t*>(kv_norm_w), eps,
-                            fr, fmt, num_pages, static_cast<uint8_t*>(pages), page_table, max_pages, pos, T,
-                            (int)ntok, chunks, ksplit, static_cast<uint16_t*>(latent_out), acc, tickets, err);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_wc, tm_wr, static_cast<const uint16_t*>(kv_norm_w), eps, fr,
+                            num_pages, static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, (int)ntok,
+                            chunks, ksplit, static_cast<uint16_t*>(latent_out), acc, tickets, err);
 }
 
 }  // namespace mla

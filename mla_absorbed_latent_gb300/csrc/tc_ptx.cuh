@@ -124,6 +124,10 @@ __device__ __forceinline__ void st_global_v8(float* p, float a, float b, float c
                "f"(e), "f"(f), "f"(g), "f"(h)
                : "memory");
 }
+// fire-and-forget add of 4 floats to a 16-byte aligned global address (L2 atomic)
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
