@@ -149,10 +149,12 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  *                before quantization (c_kv then k_pe, the bf16 values a bf16
  *                pool would hold), whether or not its page write succeeded
  *   k_splits   : 0 picks the split of the projection's K dimension by size;
- *                n > 0 forces n CTA pairs per 128-token tile (capped at hidden/64)
+ *                n > 0 forces n CTA pairs per 128-token tile (capped at hidden/64;
+ *                MLA_ERR_UNSUPPORTED if the tiles times the pairs exceed a grid)
  *   workspace  : device scratch of >= mla_cache_project_workspace_bytes(B, T,
  *                hidden, k_splits) bytes, 256-byte aligned (may be NULL when that
- *                is 0); cleared by the call itself
+ *                is 0); cleared by the call itself, so calls that share one
+ *                workspace must not overlap on the GPU
  * Per token, in fp32 from bf16 operands: y = wkv_a x (tensor cores, fp32
  * accumulation); c = y[0..511] / sqrt(mean(y[0..511]^2) + eps) * kv_norm_w;
  * pairs (2i, 2i+1) of y[512..575] rotated by the angle pos * rope_theta^(-2i/64)

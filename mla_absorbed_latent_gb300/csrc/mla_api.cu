@@ -152,6 +152,7 @@ int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden
   const int sms = num_sms();
   if (sms <= 0) return MLA_ERR_CUDA;
   const int ksplit = project_splits(ntok, hidden, sms, k_splits);
+  if (2 * ((ntok + 127) / 128) * (long long)ksplit > 2147483647LL) return MLA_ERR_UNSUPPORTED;  // one CTA per grid x
   const size_t need = project_workspace_bytes(ntok, ksplit);
   if (need > 0) {
     if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
