@@ -92,7 +92,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   if (!aligned_to(q_nope, 16) || !aligned_to(q_pe, 16) || !aligned_to(W_UK, 16) || !aligned_to(W_UV, 16) ||
       !aligned_to(out, 16) || !aligned_to(page_table, 4) || !aligned_to(seqlens, 4))
     return MLA_ERR_INVALID;
-  if (!(scale == scale)) return MLA_ERR_INVALID;
+  if (!(scale > 0.f) || scale == INFINITY) return MLA_ERR_INVALID;  // the same rule as mla_decode
 
   const int sms = device_sm_count();
   if (sms <= 0) return MLA_ERR_CUDA;

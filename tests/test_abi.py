@@ -76,6 +76,16 @@ def test_host_validation_without_gpu(lib):
                 None) == m.MLA_OK
     assert proj(ctypes.byref(cache), None, 2048, None, None, 1e-6, 1e4, None, 1, None, 2, 1, None, 0, None, 0,
                 None) == m.MLA_ERR_INVALID   # null inputs
+    # the no-allocation decode checks its arguments like mla_decode, before any CUDA call
+    fake = 1 << 20  # a non-null, aligned stand-in address (never dereferenced: the checks fail first)
+    for bad_scale in (-1.0, 0.0, float("inf"), float("nan")):
+        with pytest.raises(m.MLAError) as e:
+            m.mla_decode_noalloc(fake, fake, fake, fake, 16, cache, fake, 1, fake, 1, bad_scale, fake, stream=0)
+        assert e.value.status == m.MLA_ERR_INVALID
+    with pytest.raises(m.MLAError) as e:
+        m.mla_decode_noalloc(fake, fake, fake, fake, 12, cache, fake, 1, fake, 1, 0.07, fake, stream=0)
+    assert e.value.status == m.MLA_ERR_UNSUPPORTED
+    m.mla_decode_noalloc(None, None, None, None, 16, cache, None, 1, None, 0, 0.07, None, stream=0)  # B = 0
     assert raw.mla_cache_project_workspace_bytes(1, 1, 100, 0) == 0
     assert raw.mla_cache_project_workspace_bytes(-1, 1, 2048, 0) == 0
 
