@@ -49,6 +49,7 @@ __all__ = [
     "quantize_token", "dequantized_tokens", "expected_page_pool",
     "decode_batch",
     "rms_norm", "rope", "project_latent",
+    "naive_attend_causal", "absorbed_attend_causal",
 ]
 
 
@@ -153,6 +154,69 @@ def decode_batch(q_nope, q_pe, seqs, W_UK, W_UV, scale: float, rows=None):
     rows = range(len(seqs)) if rows is None else rows
     return {b: absorbed_decode(q_nope[b], q_pe[b], seqs[b][0], seqs[b][1], W_UK, W_UV, scale)
             for b in rows}
+
+
+# ----------------------------------------------------------------------------
+# several query tokens per row (prefill chunk, incremental decode), causal
+# ----------------------------------------------------------------------------
+
+def _causal_visible(n: int, q_pos):
+    """[T, n] boolean: cached token s is visible to query t iff s <= q_pos[t]."""
+    return np.arange(n)[None, :] <= np.asarray(q_pos)[:, None]
+
+
+def naive_attend_causal(q_nope, q_pe, c_kv, k_pe, W_UK, W_UV, scale: float, q_pos=None):
+    """Expand-then-attend for T query tokens over n cached tokens, causal.
+
+    [audit] §3.4 runs the same layer as a 25-token prefill and a 1-token
+    incremental decode on the causal path; [audit] §2.1 expands every cached
+    latent into per-head keys W_UK c_t (with the shared RoPE key appended,
+    §2.4) and values W_UV c_t.  Query t sits at position q_pos[t] (default: the
+    last T positions, n-T .. n-1) and sees cached tokens 0 .. q_pos[t].
+
+    q_nope [T, H, dn], q_pe [T, H, dr], c_kv [n, dc], k_pe [n, dr] -> out [T, H, dv].
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_pe = np.asarray(q_pe, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    Kpe = np.asarray(k_pe, np.float64)
+    T, H = q_nope.shape[:2]
+    n = C.shape[0]
+    q_pos = np.arange(n - T, n) if q_pos is None else np.asarray(q_pos)
+    vis = _causal_visible(n, q_pos)
+    out = np.zeros((T, H, W_UV.shape[1]))
+    for h in range(H):
+        K = np.concatenate([C @ W_UK[h].T, Kpe], axis=1)     # [n, dn+dr]
+        V = C @ W_UV[h].T                                    # [n, dv]
+        Q = np.concatenate([q_nope[:, h], q_pe[:, h]], axis=1)  # [T, dn+dr]
+        s = np.where(vis, scale * (Q @ K.T), -np.inf)        # [T, n]
+        out[:, h] = softmax(s) @ V
+    return out
+
+
+def absorbed_attend_causal(q_nope, q_pe, c_kv, k_pe, W_UK, W_UV, scale: float, q_pos=None):
+    """Absorbed attention for T query tokens over n cached tokens, causal.
+
+    The einsums of [tutorial] §四 with the query-token axis t and the cached
+    axis s: q_lat = einsum("thd,hdc->thc"), scores = einsum("thc,sc->hts") +
+    einsum("thd,sd->hts") (the RoPE key shared by all heads), a causal mask
+    (query t sees s <= q_pos[t], [audit] §3.4), softmax over s, o_lat =
+    einsum("hts,sc->thc"), out = einsum("thc,hdc->thd").  Returns out
+    [T, H, dv] and o_lat [T, H, dc].
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_pe = np.asarray(q_pe, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    Kpe = np.asarray(k_pe, np.float64)
+    T = q_nope.shape[0]
+    n = C.shape[0]
+    q_pos = np.arange(n - T, n) if q_pos is None else np.asarray(q_pos)
+    q_lat = np.einsum("thd,hdc->thc", q_nope, W_UK)
+    s = scale * (np.einsum("thc,sc->hts", q_lat, C) + np.einsum("thd,sd->hts", q_pe, Kpe))
+    s = np.where(_causal_visible(n, q_pos)[None, :, :], s, -np.inf)
+    p = softmax(s)                                           # over s, per (h, t)
+    o_lat = np.einsum("hts,sc->thc", p, C)
+    return np.einsum("thc,hdc->thd", o_lat, W_UV), o_lat
 
 
 # ----------------------------------------------------------------------------

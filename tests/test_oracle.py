@@ -475,3 +475,82 @@ def test_project_latent_bruteforce_odd_dims(n):
     assert c.shape == (n, dc) and p.shape == (n, dr)
     assert np.max(np.abs(c - bc)) < 1e-12
     assert np.max(np.abs(p - bp)) < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# several query tokens per row, causal ("DeepSeek MLA 吸收式缓存" §3.4 prefill +
+# incremental decode; the t axis of the "手搓 MLA" §四 einsums)
+# ----------------------------------------------------------------------------
+
+def _bruteforce_causal(q_nope, q_pe, C, Kpe, Wuk, Wuv, scale, q_pos):
+    """Explicit loops: for each query token and head, expand the visible keys and
+    values, exponentiate, normalise with math.fsum, sum."""
+    T, H = len(q_nope), len(q_nope[0])
+    dn, dc, dv = len(Wuk[0]), len(C[0]), len(Wuv[0])
+    out = []
+    for t in range(T):
+        rows = []
+        for h in range(H):
+            s = []
+            for j in range(q_pos[t] + 1):
+                k = [math.fsum(Wuk[h][d][c] * C[j][c] for c in range(dc)) for d in range(dn)] + list(Kpe[j])
+                q = list(q_nope[t][h]) + list(q_pe[t][h])
+                s.append(scale * math.fsum(a * b for a, b in zip(q, k)))
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            z = math.fsum(e)
+            v = [[math.fsum(Wuv[h][d][c] * C[j][c] for c in range(dc)) for d in range(dv)] for j in range(len(s))]
+            rows.append([math.fsum(e[j] / z * v[j][d] for j in range(len(s))) for d in range(dv)])
+        out.append(rows)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("q_pos", [[2, 3, 4], [0, 1, 2], [4, 1, 3]])
+def test_causal_bruteforce_tiny_odd_dims(q_pos):
+    """T = 3 queries over n = 5 tokens, odd unequal dims; the last positions, a
+    full prefill of the first three tokens, and an unordered set of positions."""
+    rng = np.random.default_rng(40)
+    T, H, dn, dr, dc, dv, n = 3, 2, 3, 2, 7, 5, 5
+    qn, qp = rng.standard_normal((T, H, dn)), rng.standard_normal((T, H, dr))
+    C, Kpe = rng.standard_normal((n, dc)), rng.standard_normal((n, dr))
+    Wuk, Wuv = rng.standard_normal((H, dn, dc)), rng.standard_normal((H, dv, dc))
+    ref = _bruteforce_causal(qn.tolist(), qp.tolist(), C.tolist(), Kpe.tolist(), Wuk.tolist(), Wuv.tolist(), 0.41,
+                             q_pos)
+    naive = O.naive_attend_causal(qn, qp, C, Kpe, Wuk, Wuv, 0.41, q_pos)
+    absorbed, _ = O.absorbed_attend_causal(qn, qp, C, Kpe, Wuk, Wuv, 0.41, q_pos)
+    assert np.max(np.abs(naive - ref)) < 1e-12
+    assert np.max(np.abs(absorbed - ref)) < 1e-12
+
+
+def test_causal_first_prefill_token_sees_only_itself():
+    """Full prefill (T = n): query 0 sees token 0 alone, so its latent sum is c_0
+    and its output W_UV c_0 for every head, whatever the scores."""
+    rng = np.random.default_rng(41)
+    T = n = 6
+    H, dc = 3, 8
+    qn, qp = rng.standard_normal((T, H, 4)) * 30, rng.standard_normal((T, H, 2)) * 30
+    C, Kpe = rng.standard_normal((n, dc)), rng.standard_normal((n, 2))
+    Wuk, Wuv = rng.standard_normal((H, 4, dc)), rng.standard_normal((H, 5, dc))
+    out, o_lat = O.absorbed_attend_causal(qn, qp, C, Kpe, Wuk, Wuv, 0.3, np.arange(n))
+    assert np.allclose(o_lat[0], np.broadcast_to(C[0], (H, dc)), atol=1e-14)
+    assert np.allclose(out[0], Wuv @ C[0], atol=1e-12)
+
+
+def test_causal_v2lite_prefill_and_decode_agree():
+    """The 26-token V2-Lite case run as [audit] §3.4 runs it: a 25-token causal
+    prefill, then the 26th token as an incremental decode.  Naive and absorbed
+    agree to 1e-10 (associativity); the prefill's last query sees the same 25
+    tokens as a decode over the first 25, and the decode token as a decode
+    over all 26."""
+    qn1, qp1, C, P, Wuk, Wuv, sc = _tiny_inputs()
+    rng = np.random.default_rng(42)
+    T, H = 25, qn1.shape[0]
+    qn = np.concatenate([rng.standard_normal((T, H, 128)), qn1[None]], axis=0)
+    qp = np.concatenate([rng.standard_normal((T, H, 64)), qp1[None]], axis=0)
+    a, _ = O.absorbed_attend_causal(qn, qp, C, P, Wuk, Wuv, sc)   # positions 0..25
+    nv = O.naive_attend_causal(qn, qp, C, P, Wuk, Wuv, sc)
+    assert np.max(np.abs(a - nv)) < 1e-10
+    last_prefill, _, _ = O.absorbed_decode(qn[24], qp[24], C[:25], P[:25], Wuk, Wuv, sc)
+    assert np.max(np.abs(a[24] - last_prefill)) < 1e-12
+    decode, _, _ = O.absorbed_decode(qn[25], qp[25], C, P, Wuk, Wuv, sc)
+    assert np.max(np.abs(a[25] - decode)) < 1e-12
