@@ -436,6 +436,27 @@ def project_oracle_time(name, fmt, budget_s):
     return done, spent
 
 
+def project_work(ntok: int, hidden: int, fmt: str):
+    """Algorithmic FLOPs and bytes of one producer call: the projection (2 x 576 x
+    hidden per token); the weight once, the inputs and the page writes."""
+    flops = 2.0 * ntok * 576 * hidden
+    nbytes = 576 * hidden * 2 + ntok * hidden * 2 + ntok * BYTES_PER_TOKEN[fmt]
+    return flops, nbytes
+
+
+def project_roofline(flops: float, nbytes: int, ms: float, peaks):
+    """The binding roofline of a producer call: the tensor peak when its FLOP per
+    byte is above the ridge of the measured peaks, else the HBM copy bandwidth."""
+    hbm, tf_burst, _tf_sus, peak_src = peaks
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    if flops / nbytes > tf_burst * 1e12 / (hbm * 1e9):
+        return {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s", "frac": tflops / tf_burst,
+                "traffic": None, "peak_source": peak_src + " (bf16, burst)", "hbm_gbs": gbs}
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+            "peak_source": peak_src, "tensor_tflops": tflops}
+
+
 def run_project(args, name, fmt):
     import torch
     torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
@@ -503,17 +524,8 @@ def run_project(args, name, fmt):
         cpu = {"value": n / secs, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"{n} of {ntok} tokens of {name}, fp64 numpy oracle producer, {secs:.1f} s"}
 
-    hbm, tf_burst, tf_sus, peak_src = load_peaks()
-    flops = 2.0 * ntok * 576 * hidden
-    nbytes = 576 * hidden * 2 + ntok * hidden * 2 + ntok * BYTES_PER_TOKEN[fmt]  # weight, inputs, pool writes
-    tflops = flops / (ms * 1e-3) / 1e12
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    if flops / nbytes > tf_burst * 1e12 / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s", "frac": tflops / tf_burst,
-                "traffic": None, "peak_source": peak_src + " (bf16, burst)", "hbm_gbs": gbs}
-    else:
-        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
-                "peak_source": peak_src, "tensor_tflops": tflops}
+    flops, nbytes = project_work(ntok, hidden, fmt)
+    roof = project_roofline(flops, nbytes, ms, load_peaks())
     line = {
         "metric": PROJECT_METRIC, "value": ntok / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

@@ -110,3 +110,20 @@ def test_clock_samples_flag_thermal_slowdown():
 def test_clock_sampler_without_nvidia_smi_reports_nothing():
     cs = bench.ClockSampler(0)
     assert cs.stop() is None
+
+
+def test_producer_roofline_picks_the_binding_ceiling():
+    """A 32,768-token chunk at hidden 7168 does ~525 FLOP per byte: tensor-bound on
+    these peaks; a 64-token decode-time append (~57 FLOP/B) is bound by HBM."""
+    peaks = (6677.8, 1939.3, 1751.0, "measured")
+    flops, nbytes = bench.project_work(32768, 7168, "bf16")
+    assert flops == 2.0 * 32768 * 576 * 7168
+    assert nbytes == 576 * 7168 * 2 + 32768 * 7168 * 2 + 32768 * 1152
+    r = bench.project_roofline(flops, nbytes, 0.25, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(flops / 0.25e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / 1939.3)
+    flops, nbytes = bench.project_work(64, 7168, "int8")
+    assert nbytes == 576 * 7168 * 2 + 64 * 7168 * 2 + 64 * 624
+    r = bench.project_roofline(flops, nbytes, 0.01, peaks)
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(nbytes / 1e-5 / 1e9 / 6677.8)
