@@ -50,6 +50,8 @@ __all__ = [
     "decode_batch",
     "rms_norm", "rope", "project_latent",
     "naive_attend_causal", "absorbed_attend_causal",
+    "output_projection", "quantize_int8_per_token", "quantize_int8_per_tensor", "quantize_int4_sym",
+    "dequantize_int4_sym",
 ]
 
 
@@ -272,6 +274,64 @@ def project_latent(x, wkv_a, kv_norm_w, pos, eps: float, theta: float = 10000.0)
     d_c = np.shape(kv_norm_w)[-1]
     y = x @ w.T                                   # [n, d_c + d_r]
     return rms_norm(y[:, :d_c], kv_norm_w, eps), rope(y[:, d_c:], pos, theta)
+
+
+# ----------------------------------------------------------------------------
+# after the up-projection: the layer's output projection
+# ----------------------------------------------------------------------------
+
+def output_projection(out_heads, wo):
+    """The layer output: the heads' outputs side by side, times Wo^T.
+
+    [tutorial] §三 and §四 end both paths with "@ Wo.T" after reshaping the
+    per-head outputs to [T, H*dv] (its MHA listing does the reshape
+    explicitly); [audit] §3.3 maps o_proj to wo.  out_heads [T, H, dv],
+    wo [hidden, H*dv] -> [T, hidden].
+    """
+    o = np.asarray(out_heads, dtype=np.float64)
+    T = o.shape[0]
+    return o.reshape(T, -1) @ np.asarray(wo, dtype=np.float64).T
+
+
+# ----------------------------------------------------------------------------
+# the other cache quantizers [report] §3.2 compares (same rounding rules)
+# ----------------------------------------------------------------------------
+
+def quantize_int8_per_token(x):
+    """INT8 with one scale per token over all its channels ([report] §3.2
+    "per-token INT8"): the symmetric INT8 rule of quantize_int8 with a group
+    that spans the whole row."""
+    x = np.asarray(x, dtype=np.float32)
+    return quantize_int8(x, x.shape[-1])
+
+
+def quantize_int8_per_tensor(x):
+    """INT8 with one scale for the whole tensor ([report] §3.2 "per-tensor
+    INT8"): s = bf16(amax / 127) over every element, code = clamp(rint(x / s),
+    -127, 127).  Returns int8 codes (shape of x) and the scalar scale."""
+    x = np.asarray(x, dtype=np.float32)
+    codes, s = quantize_int8(x.reshape(1, -1), x.size)
+    return codes.reshape(x.shape), s.reshape(())
+
+
+def quantize_int4_sym(x, group: int):
+    """Symmetric INT4 over contiguous groups ([report] §3.2 "对称 INT4 (32块)" for
+    c_KV and "k_pe 对称 INT4 (8块)").  Reading, by analogy with the INT8 rule
+    (the page gives no formula): s = bf16(amax / 7) in fp32, code = clamp(
+    rint(x / s), -7, 7) half to even, all-zero codes when s is 0; x^ = code * s.
+    Returns int8 codes in -7..7 (shape of x) and float32 scales [..., k]."""
+    x = np.asarray(x, dtype=np.float32)
+    g = x.reshape(*x.shape[:-1], x.shape[-1] // group, group)
+    amax = np.max(np.abs(g), axis=-1)
+    s = bf16_round(amax / np.float32(7.0))
+    safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+    q = np.clip(np.rint(g / safe[..., None]), -7, 7)
+    q = np.where((s == 0)[..., None], 0, q)
+    return q.astype(np.int8).reshape(x.shape), s
+
+
+def dequantize_int4_sym(codes, scales, group: int) -> np.ndarray:
+    return dequantize_int8(codes, scales, group)
 
 
 # ----------------------------------------------------------------------------
