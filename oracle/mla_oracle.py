@@ -20,7 +20,11 @@ zero query, one dominant token), and hand-worked quantizer vectors.  The
 producer of the cache payload (down-projection, RMSNorm, RoPE) is pinned by
 hand-worked values, closed forms (unit RMS, scale invariance, rotation by
 position 0 and by one radian), the relative-position property of RoPE and a
-pure-Python brute force on odd tiny dimensions.
+pure-Python brute force on odd tiny dimensions.  Causal attention of several
+query tokens is pinned by a brute force, the first-prefill-token closed form
+and the prefill-then-decode split of the V2-Lite case; the output projection
+and the other quantizers of [report] §3.2 by hand-worked vectors, brute force
+and error bounds.
 The quantizer's rounding rules are readings of [report] §3.2, which gives no
 formula; the pages' own error figures use an unstated metric, so the
 quantization *error* is parity unpinned (the codes themselves are pinned to
