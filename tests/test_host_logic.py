@@ -1,0 +1,123 @@
+"""The library's host-side scheduling logic, compiled from its own sources and run
+on the CPU (no GPU involved): the split plan's partition of the global page list
+over the persistent workers, the decode workspace layout, and the producer's
+choice of K split and its workspace size."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "mla_absorbed_latent_gb300", "csrc")
+
+HARNESS = r"""
+#include "cache_project.cu"
+#include "tensor_map.cu"
+#include <cstdio>
+using namespace mla;
+
+static int fails = 0;
+#define CHECK(cond, ...)                                   \
+  do {                                                     \
+    if (!(cond)) {                                         \
+      if (++fails <= 20) {                                 \
+        std::printf("FAIL %s: ", #cond);                   \
+        std::printf(__VA_ARGS__);                          \
+        std::printf("\n");                                 \
+      }                                                    \
+    }                                                      \
+  } while (0)
+
+int main() {
+  // 1. T tiles cut into W contiguous ranges: ranges cover [0, T) in order and
+  //    worker_of_tile names the range that holds each tile
+  for (long long T = 1; T <= 700; T += (T < 100 ? 1 : 37))
+    for (long long W = 1; W <= 320; W += (W < 40 ? 1 : 13)) {
+      CHECK(worker_begin(0, T, W) == 0, "T=%lld W=%lld", T, W);
+      CHECK(worker_begin(W, T, W) == T, "T=%lld W=%lld", T, W);
+      for (long long w = 0; w < W; ++w)
+        CHECK(worker_begin(w, T, W) <= worker_begin(w + 1, T, W), "T=%lld W=%lld w=%lld", T, W, w);
+      for (long long x = 0; x < T; ++x) {
+        const int w = worker_of_tile(x, T, W);
+        CHECK(w >= 0 && w < W && worker_begin(w, T, W) <= x && x < worker_begin(w + 1, T, W),
+              "T=%lld W=%lld x=%lld w=%d", T, W, x, w);
+      }
+    }
+
+  // 2. decode workspace: regions in order, 1 KB aligned, each large enough
+  const int Bs[] = {1, 7, 64, 128, 1000}, Hs[] = {16, 128}, Ws[] = {1, 152, 304};
+  for (int B : Bs)
+    for (int H : Hs)
+      for (int Wk : Ws) {
+        const WsLayout L = ws_layout(B, H, Wk);
+        CHECK(L.q_cat == 0, "B=%d", B);
+        CHECK(L.plan >= L.q_cat + (size_t)B * H * DK * 2, "B=%d H=%d", B, H);
+        CHECK(L.part_o >= L.plan + (size_t)(PLAN_HDR + 2 * B + 1 + Wk) * 4, "B=%d W=%d", B, Wk);
+        CHECK(L.part_lse >= L.part_o + (size_t)(Wk + B) * H * DC * 2, "B=%d H=%d W=%d", B, H, Wk);
+        CHECK(L.total >= L.part_lse + (size_t)(Wk + B) * H * 4, "B=%d H=%d W=%d", B, H, Wk);
+        CHECK(L.plan % 1024 == 0 && L.part_o % 1024 == 0 && L.part_lse % 1024 == 0 && L.total % 1024 == 0,
+              "B=%d H=%d W=%d", B, H, Wk);
+        CHECK(L.max_segments == Wk + B, "B=%d W=%d", B, Wk);
+      }
+
+  // 3. the producer's K split: within [1, hidden/64], forced values honoured (capped),
+  //    automatic ones only when the tiles leave SMs idle, every split non-empty,
+  //    and a workspace exactly when there is a split
+  const long long ntoks[] = {1, 64, 127, 128, 129, 1000, 9728, 9729, 32768};
+  const int hiddens[] = {64, 128, 2048, 7168, 65536}, smss[] = {1, 2, 148, 152}, reqs[] = {0, 1, 3, 5, 1000};
+  for (long long ntok : ntoks)
+    for (int hidden : hiddens)
+      for (int sms : smss)
+        for (int req : reqs) {
+          const int k = project_splits(ntok, hidden, sms, req);
+          const int chunks = hidden / 64;
+          const long long mtiles = (ntok + 127) / 128;
+          CHECK(k >= 1 && k <= chunks, "ntok=%lld hidden=%d sms=%d req=%d k=%d", ntok, hidden, sms, req, k);
+          if (req > 0) {
+            CHECK(k == (req < chunks ? req : chunks), "req=%d chunks=%d k=%d", req, chunks, k);
+          } else if (2 * mtiles >= sms) {
+            CHECK(k == 1, "ntok=%lld sms=%d k=%d", ntok, sms, k);
+          } else {
+            const long long cap = chunks / 4 > 1 ? chunks / 4 : 1;
+            const long long want = sms / (2 * mtiles);
+            CHECK(k <= cap && k <= (want > 1 ? want : 1), "ntok=%lld hidden=%d sms=%d k=%d", ntok, hidden, sms, k);
+          }
+          for (int s = 0; s < k; ++s)
+            CHECK((long long)(s + 1) * chunks / k - (long long)s * chunks / k >= 1, "chunks=%d k=%d s=%d", chunks, k,
+                  s);
+          const size_t ws = project_workspace_bytes(ntok, k);
+          if (k == 1) {
+            CHECK(ws == 0, "ntok=%lld", ntok);
+          } else {
+            CHECK(ws >= (size_t)mtiles * 128 * DK * 4 + (size_t)mtiles * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok,
+                  k);
+          }
+        }
+  std::printf("%d\n", fails);
+  return fails != 0;
+}
+"""
+
+
+def _nvcc():
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    return None
+
+
+def test_scheduling_host_logic(tmp_path):
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not found")
+    src = tmp_path / "host_logic.cu"
+    src.write_text(HARNESS)
+    exe = tmp_path / "host_logic"
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "--expt-relaxed-constexpr",
+                        "-I", CSRC, "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip().endswith("0"), run.stdout[-2000:]
