@@ -149,9 +149,10 @@ class ClockSampler:
 # CPU oracle timing (reference arm and cpu_baseline)
 # ----------------------------------------------------------------------------
 
-def oracle_time(prob, budget_s: float, max_rows: int | None = None):
+def oracle_time(prob, budget_s: float, max_rows: int | None = None, outputs: dict | None = None):
     """Time the fp64 absorbed oracle over successive rows until budget_s of oracle
-    work; returns (cache bytes processed, seconds, rows)."""
+    work; returns (cache bytes processed, seconds, rows).  With `outputs`, each
+    row's oracle output [H, 128] is stored there under its row index."""
     import oracle as O
     Wuk, Wuv = O.split_wkv_b(synth.bf16_bits_to_f32(prob.wkv), prob.H)
     qn = synth.bf16_bits_to_f32(prob.q_nope)
@@ -162,13 +163,39 @@ def oracle_time(prob, budget_s: float, max_rows: int | None = None):
         c, p = prob.sequence(b)
         C, P = O.dequantized_tokens(prob.fmt, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))
         t0 = time.perf_counter()
-        O.absorbed_decode(qn[b], qp[b], C, P, Wuk, Wuv, prob.scale)
+        out, _, _ = O.absorbed_decode(qn[b], qp[b], C, P, Wuk, Wuv, prob.scale)
         spent += time.perf_counter() - t0
+        if outputs is not None:
+            outputs[b] = out
         done_bytes += int(prob.seqlens[b]) * bpt
         rows += 1
         if spent >= budget_s or (max_rows is not None and rows >= max_rows):
             break
     return done_bytes, spent, rows
+
+
+def parity_stats(got: dict, ref: dict):
+    """Agreement of the timed decode's output rows with the oracle's rows (both
+    {row: [H, 128] array}): largest absolute error, worst per-head relative RMS
+    error, and whether every element is within 2e-2 + 1e-2 |ref| and every head
+    within 1e-2 relative RMS (the parity tests' tolerance)."""
+    rows = sorted(set(got) & set(ref))
+    if not rows:
+        return None
+    max_abs, worst_rel, ok = 0.0, 0.0, True
+    for b in rows:
+        g = np.asarray(got[b], np.float64)
+        r = np.asarray(ref[b], np.float64)
+        err = np.abs(g - r)
+        max_abs = max(max_abs, float(err.max()))
+        ok = ok and bool(np.all(err <= 2e-2 + 1e-2 * np.abs(r))) and bool(np.all(np.isfinite(g)))
+        nref = np.linalg.norm(r, axis=-1)
+        live = nref > 0
+        if live.any():
+            rel = np.linalg.norm(g - r, axis=-1)[live] / nref[live]
+            worst_rel = max(worst_rel, float(rel.max()))
+    ok = ok and worst_rel <= 1e-2
+    return {"rows": len(rows), "max_abs_err": max_abs, "worst_head_rel_rms": worst_rel, "within_tolerance": ok}
 
 
 def max_over_ranks(values, dist=None, device="cpu"):
@@ -327,12 +354,18 @@ def run_ours(args, wl, fmt):
     d2h = h_out.numel() * 2
 
     # CPU oracle on the host cores (rank 0, one GPU only), bounded sample
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nbytes, secs, rows = oracle_time(prob, args.cpu_seconds)
+        ref_rows = {}
+        nbytes, secs, rows = oracle_time(prob, args.cpu_seconds, outputs=ref_rows)
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"{rows} of {B} rows of {wl.name} (all {H} heads, full sequences), fp64 numpy absorbed "
                          f"oracle, {secs:.1f} s"}
+        try:  # the same rows of the last timed end-to-end decode against the oracle
+            got = synth.bf16_bits_to_f32(h_out.view(torch.int16).numpy().view(np.uint16))
+            parity = parity_stats({b: got[b] for b in ref_rows}, ref_rows)
+        except Exception:
+            parity = None
 
     if rank != 0:
         if world > 1:
@@ -382,6 +415,7 @@ def run_ours(args, wl, fmt):
         "attend_ms": attend_ms,
         "stage_ms": stage_ms,  # mean per-stage times of one step, from events recorded between its launches
         "cpu_baseline": cpu,
+        "parity": parity,  # the oracle rows of cpu_baseline against the timed decode's output
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 4 * args.steps,  # plan, absorb_q, attend, combine (merge + up-projection)

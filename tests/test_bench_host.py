@@ -5,6 +5,7 @@ import json
 import os
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -127,3 +128,18 @@ def test_producer_roofline_picks_the_binding_ceiling():
     assert nbytes == 576 * 7168 * 2 + 64 * 7168 * 2 + 64 * 624
     r = bench.project_roofline(flops, nbytes, 0.01, peaks)
     assert r["bound"] == "hbm" and r["frac"] == pytest.approx(nbytes / 1e-5 / 1e9 / 6677.8)
+
+
+def test_parity_stats_of_the_timed_output():
+    rng = np.random.default_rng(3)
+    ref = {b: rng.standard_normal((16, 128)) for b in (0, 5)}
+    good = {b: r + 1e-4 * rng.standard_normal(r.shape) for b, r in ref.items()}
+    st = bench.parity_stats(good, ref)
+    assert st["rows"] == 2 and st["within_tolerance"] and st["max_abs_err"] < 1e-3
+    bad = dict(good)
+    bad[5] = ref[5] * 1.05          # 5 % off: elementwise within 2e-2 + 1e-2|ref| fails somewhere
+    st = bench.parity_stats(bad, ref)
+    assert not st["within_tolerance"] and st["worst_head_rel_rms"] == pytest.approx(0.05, rel=1e-6)
+    zero = {0: np.zeros((16, 128))}  # an all-zero output does not pass on rows with real values
+    assert not bench.parity_stats(zero, {0: ref[0]})["within_tolerance"]
+    assert bench.parity_stats({}, ref) is None
