@@ -664,3 +664,36 @@ def test_quantizer_variants_order_on_outlier_latents():
     assert e["int8_channel32"] < e["int8_token"] < e["int8_tensor"]
     assert e["int4_asym32"] < e["int4_sym32"]
     assert e["int8_channel32"] < e["int4_asym32"]
+
+
+# ----------------------------------------------------------------------------
+# the seeded input generators both sides take their inputs from (not oracle pins)
+# ----------------------------------------------------------------------------
+
+def test_generator_draws_in_pieces_equal_whole():
+    """A sequence drawn as a 25-token prefill then one decode token equals the
+    26-token draw, bit for bit; the same seed gives the same bits again."""
+    c, p = synth.gen_sequence(0, 3, 26)
+    c1, p1 = synth.gen_sequence(0, 3, 25)
+    c2, p2 = synth.gen_sequence(0, 3, 1, start=25)
+    assert np.array_equal(c, np.concatenate([c1, c2])) and np.array_equal(p, np.concatenate([p1, p2]))
+    c3, _ = synth.gen_sequence(0, 3, 26)
+    assert np.array_equal(c, c3)
+    x = synth.gen_hidden(2048, 1, 2, 5)
+    assert np.array_equal(x, synth.gen_hidden(2048, 1, 2, 5)) and x.shape == (5, 2048)
+
+
+def test_generator_page_tables_and_lengths():
+    """Each physical page belongs to exactly one (row, logical page); rows get the
+    pages their lengths need; ragged lengths stay in the stated clip range."""
+    w = synth.get_workload("v3_ragged")
+    lens = synth.gen_seqlens(w)
+    assert lens.min() >= 256 and lens.max() <= 32768 and len(lens) == w.B
+    table, num_pages = synth.make_page_table(lens, w.seed, True, spare_pages=2)
+    need = (lens.astype(np.int64) + 63) // 64
+    used = np.concatenate([table[b, :need[b]] for b in range(len(lens))])
+    assert len(used) == need.sum() and len(np.unique(used)) == len(used)
+    assert used.min() >= 0 and used.max() < num_pages and num_pages == need.sum() + 2
+    assert all(np.all(table[b, need[b]:] == -1) for b in range(len(lens)))
+    ident, _ = synth.make_page_table([70, 10], 0, False)
+    assert ident.tolist() == [[0, 1], [2, -1]]
