@@ -51,6 +51,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode_absorb_q": (i, [vp, vp, vp, i, i, vp, sz, vp]),
         "mla_decode_attend": (i, [i, cp, vp, i, vp, i, f, vp, sz, vp]),
         "mla_decode_combine": (i, [vp, i, i, vp, sz, vp, vp, vp]),
+        "mla_decode_noalloc": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, vp]),
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
         "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
@@ -177,13 +178,9 @@ def mla_decode_noalloc(q_nope, q_pe, W_UK, W_UV, H: int, cache: mla_cache_t, pag
                        B: int, scale: float, out, stream=None) -> None:
     """mla_decode with the library's fixed device scratch instead of a workspace
     (for hosts that cannot allocate; see include/mla.h)."""
-    fn = _lib.mla_decode_noalloc
-    if fn.argtypes is None:
-        vp, i = ctypes.c_void_p, ctypes.c_int
-        fn.restype = i
-        fn.argtypes = [vp, vp, vp, vp, i, ctypes.POINTER(mla_cache_t), vp, i, vp, i, ctypes.c_float, vp, vp]
-    _check(fn(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, ctypes.byref(cache), _ptr(page_table),
-              max_pages, _ptr(seqlens), B, scale, _ptr(out), _stream(stream)), "mla_decode_noalloc")
+    _check(_lib.mla_decode_noalloc(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, ctypes.byref(cache),
+                                   _ptr(page_table), max_pages, _ptr(seqlens), B, scale, _ptr(out), _stream(stream)),
+           "mla_decode_noalloc")
 
 
 def raw_library() -> ctypes.CDLL:
