@@ -51,7 +51,6 @@ __all__ = [
     "quantize_int8", "quantize_int4_asym", "dequantize_int8", "dequantize_int4",
     "pack_nibbles", "page_bytes", "PAGE_LAYOUT",
     "quantize_token", "dequantized_tokens", "expected_page_pool",
-    "decode_batch",
     "rms_norm", "rope", "project_latent",
     "naive_attend_causal", "absorbed_attend_causal",
     "output_projection", "quantize_int8_per_token", "quantize_int8_per_tensor", "quantize_int4_sym",
@@ -149,17 +148,6 @@ def absorbed_decode(q_nope, q_pe, c_kv, k_pe, W_UK, W_UV, scale: float):
     out = np.einsum("hc,hdc->hd", o_lat, W_UV)       # W_UV[h] o_lat[h]
     lse = m[:, 0] + np.log(l[:, 0])
     return out, o_lat, lse
-
-
-def decode_batch(q_nope, q_pe, seqs, W_UK, W_UV, scale: float, rows=None):
-    """Absorbed decode for every (or the listed) batch row.
-
-    seqs[b] = (c_kv [n_b, dc], k_pe [n_b, dr]) as real values.  Returns
-    {b: (out, o_lat, lse)}.
-    """
-    rows = range(len(seqs)) if rows is None else rows
-    return {b: absorbed_decode(q_nope[b], q_pe[b], seqs[b][0], seqs[b][1], W_UK, W_UV, scale)
-            for b in rows}
 
 
 # ----------------------------------------------------------------------------
@@ -530,9 +518,3 @@ def expected_page_pool(fmt: str, num_pages: int, writes, page: int = PAGE) -> np
                 assert raw.size == per_tok
                 pool[phys, off + slot * per_tok: off + (slot + 1) * per_tok] = raw
     return pool
-
-
-def _self_check():  # pragma: no cover - debugging aid
-    assert latent_cache_bytes(26) == 29952
-    assert expanded_cache_bytes(26, 16) == 266240
-    assert math.isclose(decode_arithmetic_intensity(128), 241.7777, rel_tol=1e-4)

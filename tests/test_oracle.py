@@ -358,6 +358,31 @@ def test_quant_pool_sections():
     assert np.array_equal(got_z, O.bf16_to_bits(z[0]))
 
 
+def test_int8_pool_sections():
+    """INT8 page image, indexed by hand: c codes int8 [64][512] from byte 0,
+    k_pe codes int8 [64][64] from 64*512 = 32768, c scales bf16 [64][16] from
+    32768 + 64*64 = 36864, k_pe scales bf16 [64][8] from 36864 + 64*16*2 =
+    38912; the page ends at 38912 + 64*8*2 = 39936.  Two tokens at slots 5, 6."""
+    rng = np.random.default_rng(2)
+    c = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((2, 512)).astype(np.float32)))
+    p = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((2, 64)).astype(np.float32)))
+    pool = O.expected_page_pool("int8", 1, [(np.array([0]), 5, c, p)])[0]
+    assert pool.size == 39936
+    cc, cs = O.quantize_int8(c, 32)
+    pc, ps = O.quantize_int8(p, 8)
+    for k, slot in enumerate((5, 6)):
+        assert np.array_equal(pool[slot * 512:(slot + 1) * 512].view(np.int8), cc[k])
+        assert np.array_equal(pool[32768 + slot * 64:32768 + (slot + 1) * 64].view(np.int8), pc[k])
+        assert np.array_equal(pool[36864 + slot * 32:36864 + (slot + 1) * 32].view(np.uint16), O.bf16_to_bits(cs[k]))
+        assert np.array_equal(pool[38912 + slot * 16:38912 + (slot + 1) * 16].view(np.uint16), O.bf16_to_bits(ps[k]))
+    # every other byte of the page is untouched
+    mask = np.zeros(pool.size, bool)
+    for slot in (5, 6):
+        for off, per in ((0, 512), (32768, 64), (36864, 32), (38912, 16)):
+            mask[off + slot * per:off + (slot + 1) * per] = True
+    assert not pool[~mask].any()
+
+
 def test_random_roundtrip_rope_norm():
     """Generator sanity (not oracle): RoPE keeps pair norms, c_KV rows have unit RMS."""
     c, p = synth.gen_sequence(0, 0, 30)
