@@ -32,6 +32,10 @@
  *    substitutes page 0, or clamps the length) and the first such error is
  *    reported by mla_get_device_status.
  *  - The functions act on the CUDA device current on the calling thread.
+ *  - The library resolves device addresses of its own globals (the status
+ *    word, the no-allocation scratch) once per device and keeps them for the
+ *    life of the process: do not use it across a device reset
+ *    (cudaDeviceReset) or any other teardown of the device's primary context.
  *  - No C++ exception crosses this interface.
  */
 #ifndef MLA_H_
@@ -59,9 +63,7 @@ typedef enum {
   MLA_ERR_CUDA = -3,         /* a CUDA runtime call (launch, attribute) failed        */
   MLA_ERR_BOUNDS = -4,       /* device: page id outside the pool / sequence too long  */
   MLA_ERR_TIMEOUT = -5,      /* device: a bounded wait inside a kernel gave up        */
-  MLA_ERR_WORKSPACE = -6,    /* workspace smaller than mla_decode_workspace_bytes     */
-  MLA_ERR_RANGE = -7         /* device: a score exceeded its segment's running maximum
-                                by more than 100 (log2 units); weights were capped  */
+  MLA_ERR_WORKSPACE = -6     /* workspace smaller than mla_decode_workspace_bytes     */
 } mla_status_t;
 
 /* Cache storage formats. */
@@ -199,6 +201,14 @@ size_t mla_decode_workspace_bytes(int B, int H);
  * then one bf16 rounding); H = 16 reads bf16 pools only (MLA_ERR_UNSUPPORTED
  * otherwise).  Equivalent to mla_decode_plan + mla_decode_absorb_q +
  * mla_decode_attend + mla_decode_combine on the same stream.
+ * The softmax is exact for every input ("DeepSeek MLA 吸收式缓存" §2.3 and the
+ * online softmax it rests on): the H = 128 kernel tracks a lazily moved
+ * reference maximum and exchanges half scores in fp16; a row whose scores
+ * jump more than 2^100 above that reference, or whose half scores exceed 32
+ * in magnitude (log2 units), is flagged by it and recomputed by
+ * mla_decode_combine with an online softmax that rescales at every new
+ * maximum (fp32, straight from the cache), so such rows cost more time, not
+ * accuracy.
  */
 int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H,
                const mla_cache_t* cache, const int32_t* page_table, int max_pages,
@@ -214,6 +224,21 @@ int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const voi
 int mla_decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Step 0 with a chosen number of split workers, 1 <= workers <=
+ * mla_decode_max_workers(H, fmt) (MLA_ERR_INVALID otherwise); the steps after
+ * it follow the plan.  The split count changes only where the sequence is cut
+ * into partials, so results agree with the default plan's within the stated
+ * tolerance (not bit for bit).  For tests of that invariance and for
+ * load-balance studies; mla_decode uses the default. */
+int mla_decode_plan_workers(int H, int fmt, const int32_t* seqlens, int B, int max_pages, int workers,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The default (largest) number of split workers of the attend kernel for H
+ * heads over a `fmt` cache on the current device: persistent CTA pairs of the
+ * tcgen05 kernel, CTAs of the CUDA-core kernel; a negative status for an
+ * unsupported pair. */
+int mla_decode_max_workers(int H, int fmt);
+
 /* Step 1: q_lat = W_UK^T q_nope (fp32 accumulation, rounded to bf16) and
  * q_pe, stored in the workspace as the query operand of step 2. */
 int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B,
@@ -228,7 +253,9 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
 
 /* Step 3: LSE-merge of the splits into o_lat, then out = W_UV o_lat (bf16).
  * o_lat_out (fp32 [B][H][512]) may be NULL; when given, the merged latent
- * sum is stored there too. */
+ * sum is stored there too.  Rows that step 2 flagged are recomputed here
+ * exactly from the cache that step 2 read (its pointers are kept in the
+ * workspace), so the cache and page table must be unchanged in between. */
 int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes,
                        void* out, float* o_lat_out, cudaStream_t stream);
 
@@ -258,11 +285,11 @@ int mla_decode_noalloc(const void* q_nope, const void* q_pe, const void* W_UK, c
 
 /*
  * Wait for `stream`, then return (and clear) the first device-detected error
- * recorded since the last call on the current device: MLA_OK, MLA_ERR_BOUNDS,
- * MLA_ERR_RANGE or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).
- * If `info` is non-NULL it receives a detail value: the offending row or page
- * id for MLA_ERR_BOUNDS, the number of the wait site that gave up for
- * MLA_ERR_TIMEOUT (1 for mla_wait_selftest), 0 for MLA_ERR_RANGE.
+ * recorded since the last call on the current device: MLA_OK, MLA_ERR_BOUNDS
+ * or MLA_ERR_TIMEOUT (MLA_ERR_CUDA when the wait itself failed).  If `info` is
+ * non-NULL it receives a detail value: the offending row or page id for
+ * MLA_ERR_BOUNDS, the number of the wait site that gave up for MLA_ERR_TIMEOUT
+ * (1 for mla_wait_selftest).
  */
 int mla_get_device_status(cudaStream_t stream, int* info);
 

@@ -18,9 +18,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
-MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE, MLA_ERR_RANGE = -4, -5, -6, -7
+MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = -4, -5, -6
 FMT = {"bf16": 0, "int8": 1, "int4": 2}
 D_C, D_R, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # the fixed scratch of mla_decode_noalloc
 
 
 class MLAError(RuntimeError):
@@ -48,6 +49,8 @@ def _load() -> ctypes.CDLL:
         "mla_decode_workspace_bytes": (sz, [i, i]),
         "mla_decode": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, sz, vp, vp]),
         "mla_decode_plan": (i, [i, i, vp, i, i, vp, sz, vp]),
+        "mla_decode_plan_workers": (i, [i, i, vp, i, i, i, vp, sz, vp]),
+        "mla_decode_max_workers": (i, [i, i]),
         "mla_decode_absorb_q": (i, [vp, vp, vp, i, i, vp, sz, vp]),
         "mla_decode_attend": (i, [i, cp, vp, i, vp, i, f, vp, sz, vp]),
         "mla_decode_combine": (i, [vp, i, i, vp, sz, vp, vp, vp]),
@@ -134,6 +137,20 @@ def mla_decode_plan(H: int, fmt: str | int, seqlens, B: int, max_pages: int, wor
     f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
     _check(_lib.mla_decode_plan(H, f, _ptr(seqlens), B, max_pages, _ptr(workspace), workspace_bytes,
                                 _stream(stream)), "mla_decode_plan")
+
+
+def mla_decode_plan_workers(H: int, fmt: str | int, seqlens, B: int, max_pages: int, workers: int, workspace,
+                            workspace_bytes: int, stream=None) -> None:
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(_lib.mla_decode_plan_workers(H, f, _ptr(seqlens), B, max_pages, workers, _ptr(workspace),
+                                        workspace_bytes, _stream(stream)), "mla_decode_plan_workers")
+
+
+def mla_decode_max_workers(H: int, fmt: str | int = "bf16") -> int:
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    n = int(_lib.mla_decode_max_workers(H, f))
+    _check(min(n, 0), "mla_decode_max_workers")
+    return n
 
 
 def mla_decode_absorb_q(q_nope, q_pe, W_UK, H: int, B: int, workspace, workspace_bytes: int, stream=None) -> None:

@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int worker = blockIdx.x, hg = blockIdx.y;
   const int T = plan[0], W = plan[1];
   const int* prefix = plan + PLAN_HDR;
-  const int* seq_c = plan + PLAN_HDR + B + 1;
+  const int* seq_c = plan + plan_off_seq(B);
+  if (worker >= W) return;  // a plan may use fewer workers than this launch has CTAs
   const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
   if (x0 >= x1) return;
 

@@ -44,8 +44,12 @@
 // already in the old reference, so O is rescaled by the same factor on both
 // sides once the last of those pages' P.V has completed, before the next
 // page's P.V (which needs this CTA's next P).  A score more than 2^100 above
-// its reference is capped there and reported as MLA_ERR_RANGE (the result
-// stays finite; it is no longer exact).
+// its reference cannot be weighted exactly in that reference: p is capped
+// there (O and l stay finite) and the row is flagged in the plan block, and the
+// combine kernel recomputes the flagged rows with a plain online softmax that
+// rescales at every new maximum.  So does a row whose exchanged fp16 half
+// scores exceed 2^5 in magnitude (beyond it an fp16 half score carries more
+// than 2^-7 of absolute error, 0.5 % on p).
 //
 // MMA issue.  A tcgen05.mma blocks its issuing thread while an MMA on the same
 // accumulator is in flight, so three threads issue MMAs: S of even pages, S of
@@ -103,7 +107,8 @@ constexpr int Q_AHEAD = 8;  // pages before a row's end at which the producer pr
 constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 heads][64 dims] 128B-swizzled
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
 constexpr float FP16_MAX = 65504.f;
-constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p tolerated (O and l stay finite in fp32)
+constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p formed here (O and l stay finite in fp32)
+constexpr float EXCH_LOG2 = 32.f;    // largest |half score| (log2 units) exchanged in fp16 for an exact row
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
 
 // Per cache format: bf16 pages are TMA-copied straight into the MMA operand
@@ -177,7 +182,8 @@ static_assert(offsetof(SmemTC<MLA_FMT_BF16>, qpe) % 1024 == 0 && offsetof(SmemTC
 
 struct TcArgs {
   const uint16_t* q_cat;  // [B][128][576] bf16
-  const int* plan;
+  int* plan;              // read; the exact-recompute flags and context are written
+  const uint8_t* pages;
   const int32_t* page_table;
   uint16_t* part_o;  // bf16 [segments][128][512]
   float* part_lse;
@@ -192,6 +198,8 @@ struct TcArgs {
 // probes.
 // error reports from hot loops, out of line
 __device__ __noinline__ void report_error(int* err, int code, int info) { raise_error(err, code, info); }
+// a row whose weights cannot be formed exactly here: the combine kernel recomputes it
+__device__ __noinline__ void flag_row(int* fix, int b) { fix[b] = 1; }
 
 template <bool kCluster>
 __device__ __forceinline__ bool probe_bar(uint64_t* bar, uint32_t parity) {
@@ -443,9 +451,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   grid_dep_launch();
   const int T = a.plan[0], W = a.plan[1], B = a.B;
   const int* prefix = a.plan + PLAN_HDR;
-  const int* seq_c = a.plan + PLAN_HDR + B + 1;
-  const int row0 = a.plan[PLAN_HDR + 2 * B + 1 + worker];  // first row of this worker's range
-  const int x0 = (int)worker_begin(worker, T, W), x1 = (int)worker_begin(worker + 1, T, W);
+  const int* seq_c = a.plan + plan_off_seq(B);
+  int* const fix = a.plan + plan_off_fix(B);
+  // a plan may use fewer workers than this launch has CTA pairs: the rest idle
+  const bool live = worker < W;
+  const int row0 = live ? a.plan[plan_off_wrow(B) + worker] : 0;  // first row of this worker's range
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // what the combine kernel reads to recompute a flagged row
+    FixCtx* fx = reinterpret_cast<FixCtx*>(a.plan + PLAN_CTX);
+    fx->pages = a.pages;
+    fx->page_table = a.page_table;
+    fx->q_cat = a.q_cat;
+    fx->max_pages = a.max_pages;
+    fx->num_pages = a.num_pages;
+    fx->fmt = FMT;
+    fx->scale_log2 = a.scale_log2;
+  }
+  const int x0 = live ? (int)worker_begin(worker, T, W) : 0, x1 = live ? (int)worker_begin(worker + 1, T, W) : 0;
   const int ntiles = x1 - x0;
 
   // Roles of warps 0..3 (warp w runs on SM sub-partition w % 4; the pair's two
@@ -885,9 +907,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           l = 0.f;
         }
-        if (mraw - m_ref > RANGE_LOG2) report_error(a.err, MLA_ERR_RANGE, 0);
+        if (mraw - m_ref > RANGE_LOG2) flag_row(fix, rc.b);
         // p = 2^(s - m_ref), rounded to bf16 for the MMA (exponent capped at
-        // RANGE_LOG2, beyond which the range error above is reported)
+        // RANGE_LOG2: beyond it the row was flagged above for the exact recompute)
         uint32_t pk[TPW / 2];
         float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
@@ -1027,9 +1049,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_proxy_async_smem();
         }
         uint32_t h[HALF_T / 2];
+        float amax = 0.f;  // largest |half score| of the page's tokens, for the exactness flag
 #pragma unroll
-        for (int k = 0; k < HALF_T / 2; ++k)
-          h[k] = f2_to_h2(fp16_clamp(u2f(v[2 * k]) * c), fp16_clamp(u2f(v[2 * k + 1]) * c));
+        for (int k = 0; k < HALF_T / 2; ++k) {
+          const float x0 = u2f(v[2 * k]) * c, x1 = u2f(v[2 * k + 1]) * c;
+          amax = fmaxf(amax, tok0 + 2 * k < nvalid ? fabsf(x0) : 0.f);
+          amax = fmaxf(amax, tok0 + 2 * k + 1 < nvalid ? fabsf(x1) : 0.f);
+          h[k] = f2_to_h2(fp16_clamp(x0), fp16_clamp(x1));
+        }
+        if (amax > EXCH_LOG2) flag_row(fix, rc.b);
         // the peer has consumed what we sent into its buffer two pages ago (so
         // the copy that read xout[sb] then has completed too); with a single
         // staging tile, also last page's
@@ -1161,7 +1189,7 @@ int attend_tc_workers(int num_sms) {
 }
 
 cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
-                             const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
+                             const int32_t* page_table, int max_pages, int B, float scale, int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (H != 128 || workers < 1) return cudaErrorNotSupported;
   if (fmt != MLA_FMT_BF16 && fmt != MLA_FMT_INT8 && fmt != MLA_FMT_INT4) return cudaErrorNotSupported;
@@ -1198,6 +1226,7 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   TcArgs args;
   args.q_cat = static_cast<const uint16_t*>(q_cat);
   args.plan = plan;
+  args.pages = pg;
   args.page_table = page_table;
   args.part_o = part_o;
   args.part_lse = part_lse;

@@ -77,6 +77,178 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// ---------------------------------------------------------------------------
+// Exact recompute of a flagged row.  The attend kernel flags a row whose
+// weights it could not form exactly in its running reference (a score far
+// above it, or exchanged half scores too large for fp16); here each (row,
+// head) of such a row is recomputed from the cache with the online softmax of
+// the pages, which rescales at every new maximum, in fp32: one token per
+// thread for the scores of a chunk, then every thread its latent dims of
+// sum_t p_t c_t; o_lat = that / l; out = W_UV[h] o_lat.  Rare path: plain
+// loads, no staging.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ size_t fmt_page_bytes(int fmt) {
+  return fmt == MLA_FMT_BF16 ? PAGE_BYTES_BF16 : fmt == MLA_FMT_INT8 ? PAGE_BYTES_INT8 : PAGE_BYTES_INT4;
+}
+__device__ __forceinline__ float bf16_at(const uint8_t* p) {
+  return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(p) << 16);
+}
+// physical page of logical page j of row b (an id outside the pool reads page 0 and is reported)
+__device__ const uint8_t* fix_page(const FixCtx& fx, int b, int j, int* err) {
+  int pid = fx.page_table[(size_t)b * fx.max_pages + j];
+  if (pid < 0 || pid >= fx.num_pages) {
+    raise_error(err, MLA_ERR_BOUNDS, pid);
+    pid = 0;
+  }
+  return fx.pages + (size_t)pid * fmt_page_bytes(fx.fmt);
+}
+// elements 8u .. 8u+7 (u < 72) of the 576-wide key of slot `slot`, in fp32;
+// quantized codes as x = code * s (+ z), the block quantizers of "DeepSeek-V2-Lite
+// MLA 吸收式 KV 缓存优化" §3.2
+__device__ void fix_key_unit(int fmt, const uint8_t* pg, int slot, int u, float* f) {
+  if (fmt == MLA_FMT_BF16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(pg + (size_t)slot * DK * 2 + u * 16);
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+    return;
+  }
+  const bool i8 = fmt == MLA_FMT_INT8;
+  if (u >= DC / 8) {  // RoPE key: INT8 codes, one bf16 scale per 8 dims (both quantized formats)
+    const int g = u - DC / 8;
+    const int8_t* c = reinterpret_cast<const int8_t*>(pg + (i8 ? I8_PE_CODE : I4_PE_CODE) + slot * DR + 8 * g);
+    const float sc = bf16_at(pg + (i8 ? I8_PE_SCALE : I4_PE_SCALE) + (slot * (DR / 8) + g) * 2);
+    for (int k = 0; k < 8; ++k) f[k] = (float)c[k] * sc;
+    return;
+  }
+  const int grp = u / 4;  // 32-channel group
+  if (i8) {
+    const int8_t* c = reinterpret_cast<const int8_t*>(pg + I8_C_CODE + slot * DC + 8 * u);
+    const float sc = bf16_at(pg + I8_C_SCALE + (slot * (DC / 32) + grp) * 2);
+    for (int k = 0; k < 8; ++k) f[k] = (float)c[k] * sc;
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(pg + I4_C_CODE + slot * (DC / 2) + 4 * u);
+    const float sc = bf16_at(pg + I4_C_SCALE + (slot * (DC / 32) + grp) * 2);
+    const float z = bf16_at(pg + I4_C_ZERO + (slot * (DC / 32) + grp) * 2);
+    for (int k = 0; k < 8; ++k) f[k] = fmaf((float)((w >> (4 * k)) & 0xFu), sc, z);
+  }
+}
+// latent element d (< 512) of slot `slot`, in fp32
+__device__ __forceinline__ float fix_latent(int fmt, const uint8_t* pg, int slot, int d) {
+  if (fmt == MLA_FMT_BF16) return bf16_at(pg + ((size_t)slot * DK + d) * 2);
+  const int grp = d / 32;
+  if (fmt == MLA_FMT_INT8)
+    return (float)*reinterpret_cast<const int8_t*>(pg + I8_C_CODE + slot * DC + d) *
+           bf16_at(pg + I8_C_SCALE + (slot * (DC / 32) + grp) * 2);
+  const uint32_t code = (pg[I4_C_CODE + slot * (DC / 2) + d / 2] >> (4 * (d & 1))) & 0xFu;
+  return fmaf((float)code, bf16_at(pg + I4_C_SCALE + (slot * (DC / 32) + grp) * 2),
+              bf16_at(pg + I4_C_ZERO + (slot * (DC / 32) + grp) * 2));
+}
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) r = fmaxf(r, red[w]);
+  __syncthreads();
+  return r;
+}
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) r += red[w];
+  __syncthreads();
+  return r;
+}
+// out[b][h] (and o_lat[b][h] when given) of one row of n > 0 tokens, exactly;
+// every thread of the CTA calls it (NT threads); scratch: 1,408 + NT floats of shared memory
+template <int NT>
+__device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, int n, const uint16_t* W_UV,
+                                        uint16_t* out, float* o_lat, float* scratch, int* err) {
+  constexpr int DPT = (DC + NT - 1) / NT;  // latent dims per thread
+  const int tid = threadIdx.x;
+  float* q = scratch;          // [576]
+  float* pw = q + DK;          // [NT] weights of the chunk's tokens
+  float* red = pw + NT;        // [32]
+  float* ol = red + 32;        // [512]
+  const uint16_t* qrow = fx.q_cat + ((size_t)b * H + h) * DK;
+  for (int i = tid; i < DK; i += NT) q[i] = __uint_as_float((uint32_t)qrow[i] << 16);
+  __syncthreads();
+  float acc[DPT];
+#pragma unroll
+  for (int k = 0; k < DPT; ++k) acc[k] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  for (int t0 = 0; t0 < n; t0 += NT) {
+    const int t = t0 + tid;
+    float sc = -INFINITY;
+    if (t < n) {
+      const uint8_t* pg = fix_page(fx, b, t / PAGE, err);
+      float dot = 0.f;
+      for (int u = 0; u < DK / 8; ++u) {
+        float f[8];
+        fix_key_unit(fx.fmt, pg, t % PAGE, u, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dot = fmaf(q[8 * u + k], f[k], dot);
+      }
+      sc = dot * fx.scale_log2;
+    }
+    const float m_new = fmaxf(m, block_max<NT>(sc, red));  // finite: token t0 < n is valid
+    const float alpha = exp2f(m - m_new);                    // 0 at the first chunk
+    const float p = t < n ? exp2f(sc - m_new) : 0.f;
+    pw[tid] = p;
+    l = l * alpha + block_sum<NT>(p, red);  // its barriers also publish pw
+    const int cnt = min(NT, n - t0);
+#pragma unroll
+    for (int k = 0; k < DPT; ++k) {
+      const int d = tid + k * NT;
+      if (d < DC) {
+        float a = acc[k] * alpha;
+        const uint8_t* pg = nullptr;
+        for (int j = 0; j < cnt; ++j) {
+          const int tj = t0 + j;
+          if (j == 0 || tj % PAGE == 0) pg = fix_page(fx, b, tj / PAGE, err);
+          a = fmaf(pw[j], fix_latent(fx.fmt, pg, tj % PAGE, d), a);
+        }
+        acc[k] = a;
+      }
+    }
+    m = m_new;
+    __syncthreads();  // pw is rewritten by the next chunk
+  }
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int k = 0; k < DPT; ++k) {
+    const int d = tid + k * NT;
+    if (d < DC) {
+      ol[d] = acc[k] * inv;
+      if (o_lat != nullptr) o_lat[((size_t)b * H + h) * DC + d] = acc[k] * inv;
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j < DV; j += NT) {
+    const uint4* w = reinterpret_cast<const uint4*>(W_UV + ((size_t)h * DV + j) * DC);
+    float o = 0.f;
+    for (int c8 = 0; c8 < DC / 8; ++c8) {
+      const uint4 v = w[c8];
+      const float* x = ol + 8 * c8;
+      o = fmaf(bf16lo(v.x), x[0], o); o = fmaf(bf16hi(v.x), x[1], o);
+      o = fmaf(bf16lo(v.y), x[2], o); o = fmaf(bf16hi(v.y), x[3], o);
+      o = fmaf(bf16lo(v.z), x[4], o); o = fmaf(bf16hi(v.z), x[5], o);
+      o = fmaf(bf16lo(v.w), x[6], o); o = fmaf(bf16hi(v.w), x[7], o);
+    }
+    const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+    out[((size_t)b * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
+  }
+  __syncthreads();  // scratch reuse by the next row
+}
+
 template <int RB>
 __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     combine_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
@@ -140,6 +312,10 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   }
   grid_dep_wait();  // the partials and their log-sum-exps
   grid_dep_launch();
+  // rows of this group the attend kernel flagged for an exact recompute (read
+  // now, used at the end)
+  const int* fixf = plan + plan_off_fix(B);
+  const int myfix = (tid < RB && b0 + tid < B) ? fixf[b0 + tid] : 0;
 
   // ---- the slots [s_lo, s_hi) that hold every segment of the group's rows:
   // segment w + b of row b, rows and workers both increasing along the tiles
@@ -316,6 +492,15 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   if (loader) {
     fence_after_sync();
     tmem_dealloc(tmem, L::TCOLS);
+  }
+  if (__syncthreads_or(myfix) && !*abort) {
+    // every ring load has landed and been read: the partial ring is free scratch
+    const FixCtx fx = *reinterpret_cast<const FixCtx*>(plan + PLAN_CTX);
+    const int* seq_c = plan + plan_off_seq(B);
+    for (int r = 0; r < RB && b0 + r < B; ++r)
+      if (fixf[b0 + r])
+        exact_head<L::THREADS>(fx, b0 + r, h, H, seq_c[b0 + r], W_UV, out, o_lat,
+                               reinterpret_cast<float*>(sm + L::OFF_P), err);
   }
 }
 

@@ -59,19 +59,6 @@ int scratch_address(void** out) {
   return MLA_OK;
 }
 
-// Largest worker count <= want whose workspace layout fits the scratch; 0 if none.
-int fitting_workers(int B, int H, int want) {
-  if (want < 1) return 0;
-  if (ws_layout(B, H, want).total <= kScratchBytes) return want;
-  if (ws_layout(B, H, 1).total > kScratchBytes) return 0;
-  int lo = 1, hi = want;  // layout(lo) fits, layout(hi) does not
-  while (hi - lo > 1) {
-    const int mid = lo + (hi - lo) / 2;
-    if (ws_layout(B, H, mid).total <= kScratchBytes) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -97,7 +84,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   const int sms = device_sm_count();
   if (sms <= 0) return MLA_ERR_CUDA;
   const int want = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
-  const int workers = fitting_workers(B, H, want);
+  const int workers = fitting_workers(B, H, want, kScratchBytes);
   if (workers < 1) return MLA_ERR_WORKSPACE;  // batch too large for the fixed scratch
 
   void* scratch = nullptr;

@@ -28,7 +28,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   const int lo = min(B, tid * per), hi = min(B, lo + per);
   const long long cap = (long long)max_pages * PAGE;
   int* prefix = plan + PLAN_HDR;
-  int* seq_c = plan + PLAN_HDR + B + 1;
+  int* seq_c = plan + plan_off_seq(B);
+  int* fix = plan + plan_off_fix(B);
 
   int local = 0, first_n = 0;  // first_n: the clamped length of row lo (one row per thread when B <= 1024)
   for (int b = lo; b < hi; ++b) {
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       n = n < 0 ? 0 : cap;
     }
     seq_c[b] = (int)n;
+    fix[b] = 0;
     if (b == lo) first_n = (int)n;
     local += (int)((n + PAGE - 1) / PAGE);
   }
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   // first row of each worker's range: the largest b with prefix[b] <= its first
   // tile (so a worker starts its cursor with one load instead of a search)
   const int* pf = in_smem ? s_prefix : prefix;
-  int* wrow = plan + PLAN_HDR + 2 * B + 1;
+  int* wrow = plan + plan_off_wrow(B);
   const long long T = pf[B];
   for (int w = tid; w < workers; w += blockDim.x) {
     const long long x = worker_begin(w, T, workers);

@@ -186,23 +186,51 @@ int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, 
   return status_of(launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream));
 }
 
-int mla_decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, void* workspace,
-                    size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// Step 0 with `req` split workers (0: the attend kernel's default count; else
+// 1 <= req <= that count)
+int decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, int req, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
   if (!heads_ok(H) || !fmt_ok(fmt)) return MLA_ERR_UNSUPPORTED;
   const int kind = attend_kind(H, fmt);
   if (kind < 0) return MLA_ERR_UNSUPPORTED;
-  if (B < 0 || max_pages <= 0) return MLA_ERR_INVALID;
+  if (B < 0 || max_pages <= 0 || req < 0) return MLA_ERR_INVALID;
   WsLayout L;
   int st = check_ws(B, H, workspace, workspace_bytes, &L);
   if (st != MLA_OK) return st;
+  const int sms = num_sms();
+  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  if (req > workers) return MLA_ERR_INVALID;
   if (B == 0) return MLA_OK;
   if (!seqlens || !aligned(seqlens, 4)) return MLA_ERR_INVALID;
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
-  const int sms = num_sms();
-  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
   int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.plan);
-  return status_of(launch_plan(seqlens, B, max_pages, workers, plan, err, stream));
+  return status_of(launch_plan(seqlens, B, max_pages, req > 0 ? req : workers, plan, err, stream));
+}
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  return decode_plan(H, fmt, seqlens, B, max_pages, 0, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_plan_workers(int H, int fmt, const int32_t* seqlens, int B, int max_pages, int workers,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (workers < 1) return MLA_ERR_INVALID;
+  return decode_plan(H, fmt, seqlens, B, max_pages, workers, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_max_workers(int H, int fmt) {
+  const int kind = attend_kind(H, fmt);
+  if (kind < 0) return MLA_ERR_UNSUPPORTED;
+  const int sms = num_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  return kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
 }
 
 int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table, int max_pages,
@@ -223,7 +251,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int* plan = reinterpret_cast<const int*>(ws + L.plan);
+  int* plan = reinterpret_cast<int*>(ws + L.plan);
   uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   const int sms = num_sms();
@@ -310,7 +338,6 @@ const char* mla_status_string(int status) {
     case MLA_ERR_BOUNDS: return "page id or sequence length out of bounds";
     case MLA_ERR_TIMEOUT: return "bounded device wait timed out";
     case MLA_ERR_WORKSPACE: return "workspace too small";
-    case MLA_ERR_RANGE: return "score range beyond the kernel's reference tracking (weights capped)";
     default: return "unknown status";
   }
 }

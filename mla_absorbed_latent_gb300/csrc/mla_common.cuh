@@ -44,11 +44,31 @@ struct WsLayout {
   int max_segments;
 };
 
-// plan block (int32): [0] total tiles, [1] workers, [2] B, [3] reserved,
-//                     [4 .. 4+B]  tile prefix (B+1 entries),
-//                     [5+B .. 5+2B) clamped sequence lengths,
-//                     [5+2B .. 5+2B+W) first row of each worker's tile range
-constexpr int PLAN_HDR = 4;
+// plan block (int32):
+//   [0] total tiles, [1] workers, [2] B, [3] reserved,
+//   [4 .. 14)  the exact-recompute context (FixCtx, written by the tcgen05 attend kernel),
+//   [PLAN_HDR .. +B+1)      tile prefix (B+1 entries),
+//   then B clamped sequence lengths,
+//   then B exact-recompute flags (zeroed by the plan, set by the attend kernel for a row
+//        whose weights it could not form exactly; the combine kernel recomputes it),
+//   then W first rows, one per worker's tile range.
+constexpr int PLAN_HDR = 16;
+constexpr int PLAN_CTX = 4;  // int offset of the FixCtx record (byte offset 16: 8-byte aligned)
+__host__ __device__ constexpr int plan_off_seq(int B) { return PLAN_HDR + B + 1; }
+__host__ __device__ constexpr int plan_off_fix(int B) { return PLAN_HDR + 2 * B + 1; }
+__host__ __device__ constexpr int plan_off_wrow(int B) { return PLAN_HDR + 3 * B + 1; }
+__host__ __device__ constexpr long long plan_ints(int B, int W) { return (long long)PLAN_HDR + 3LL * B + 1 + W; }
+
+// What the combine kernel needs to recompute a flagged row from the cache: the
+// attend kernel's cache, page table, query operand and scale.
+struct FixCtx {
+  const uint8_t* pages;
+  const int32_t* page_table;
+  const uint16_t* q_cat;  // [B][H][576] bf16: q_lat then q_pe
+  int max_pages, num_pages, fmt;
+  float scale_log2;       // softmax scale times log2(e)
+};
+static_assert(sizeof(FixCtx) <= (PLAN_HDR - PLAN_CTX) * 4, "FixCtx fits the plan header");
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -58,7 +78,7 @@ inline WsLayout ws_layout(int B, int H, int max_workers) {
   L.q_cat = off;
   off = align_up(off + (size_t)B * H * DK * 2, 1024);
   L.plan = off;
-  off = align_up(off + (size_t)(PLAN_HDR + 2 * B + 1 + max_workers) * 4, 1024);
+  off = align_up(off + (size_t)plan_ints(B, max_workers) * 4, 1024);
   L.max_segments = max_workers + B;
   L.part_o = off;
   off = align_up(off + (size_t)L.max_segments * H * DC * 2, 1024);  // bf16 partials
@@ -66,6 +86,20 @@ inline WsLayout ws_layout(int B, int H, int max_workers) {
   off = align_up(off + (size_t)L.max_segments * H * 4, 1024);
   L.total = off;
   return L;
+}
+
+// Largest worker count <= want whose decode workspace for B rows and H heads
+// fits in cap bytes; 0 when even one worker does not fit.
+inline int fitting_workers(int B, int H, int want, size_t cap) {
+  if (want < 1) return 0;
+  if (ws_layout(B, H, want).total <= cap) return want;
+  if (ws_layout(B, H, 1).total > cap) return 0;
+  int lo = 1, hi = want;  // layout(lo) fits, layout(hi) does not
+  while (hi - lo > 1) {
+    const int mid = lo + (hi - lo) / 2;
+    if (ws_layout(B, H, mid).total <= cap) lo = mid; else hi = mid;
+  }
+  return lo;
 }
 
 // worker that owns global tile x when T tiles are cut into W contiguous ranges
@@ -185,7 +219,7 @@ cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, c
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_cc_workers(int num_sms);
 cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
-                             const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
+                             const int32_t* page_table, int max_pages, int B, float scale, int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
 // a CTA pair whose bounded wait runs out on purpose (see mla_wait_selftest)

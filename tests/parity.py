@@ -33,6 +33,40 @@ def oracle_rows(prob, rows, W=None):
     return res
 
 
+def _oracle_rows_task(args):
+    prob, rows = args
+    return {b: r[0] for b, r in oracle_rows(prob, rows).items()}
+
+
+def oracle_outputs(prob, rows, procs: int | None = None):
+    """{b: out [H,128]} of the fp64 oracle for many rows, computed by a pool of
+    spawned worker processes (spawn: the parent may already hold a CUDA
+    context), each with single-threaded BLAS."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+    rows = list(rows)
+    procs = procs or max(1, min(len(rows), (os.cpu_count() or 2) - 1, 16))
+    if procs == 1 or len(rows) <= 2:
+        return _oracle_rows_task((prob, rows))
+    chunks = [rows[i::procs] for i in range(procs)]
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"  # inherited by the spawned workers
+    try:
+        with cf.ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn")) as ex:
+            res = {}
+            for part in ex.map(_oracle_rows_task, [(prob, c) for c in chunks if c]):
+                res.update(part)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return res
+
+
 def assert_close(got, ref, what="out"):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)

@@ -14,7 +14,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(),
 import oracle as O  # noqa: E402
 import synth  # noqa: E402
 from synth.device import DeviceDecode, bits_to_device, make_problem, problem_from_workload  # noqa: E402
-from tests.parity import assert_close, oracle_rows, weights  # noqa: E402
+from tests.parity import assert_close, oracle_outputs, oracle_rows, weights  # noqa: E402
 
 
 def _np_bf16(t):
@@ -130,6 +130,20 @@ def test_append_out_of_bounds_is_reported_not_written():
 # decode parity
 # ----------------------------------------------------------------------------
 
+def _check_all_rows(dev, rows=None):
+    """Every listed row (default: all non-empty rows) of dev.out against the fp64
+    oracle, the oracle rows computed in parallel worker processes."""
+    prob = dev.prob
+    rows = [b for b in range(prob.B) if prob.seqlens[b] > 0] if rows is None else rows
+    ref = oracle_outputs(prob, rows)
+    got = _out_f64(dev.out)
+    worst = 0.0
+    for b in rows:
+        _, r = assert_close(got[b], ref[b], what=f"out[{b}]")
+        worst = max(worst, r)
+    return worst
+
+
 def _check_rows(dev, rows, o_lat=None):
     prob = dev.prob
     ref = oracle_rows(prob, rows)
@@ -209,31 +223,28 @@ def test_decode_v2lite_batch_full():
 
 
 def test_decode_v3_paged_full():
-    """H=128, B=64, seqlen 8192, random page table: sampled rows + whole-batch sanity."""
+    """H=128, B=64, seqlen 8192, random page table: every row against the oracle."""
     prob = problem_from_workload(synth.get_workload("v3_paged"))
     dev = DeviceDecode(prob)
     o_lat = torch.empty((prob.B, 128, 512), dtype=torch.float32, device="cuda")
     dev.decode_steps(o_lat)
     torch.cuda.synchronize()
     _status_ok()
-    _check_rows(dev, [0, 21, 42, 63], o_lat)
-    out = _out_f64(dev.out)
-    assert np.all(np.isfinite(out))
+    _check_all_rows(dev)
+    _check_rows(dev, [0, 63], o_lat)
     # every row's o_lat is a convex combination of unit-RMS latents: RMS <= 1
     rms = torch.sqrt(torch.mean(o_lat ** 2, dim=-1))
     assert bool(torch.all(rms <= 1.0 + 1e-3))
 
 
 def test_decode_v3_ragged_full():
-    """H=128, B=128, lognormal lengths: shortest, longest and a middle row."""
+    """H=128, B=128, lognormal lengths (segments cross worker boundaries): every row."""
     prob = problem_from_workload(synth.get_workload("v3_ragged"))
     dev = DeviceDecode(prob)
     dev.decode()
     torch.cuda.synchronize()
     _status_ok()
-    order = np.argsort(prob.seqlens)
-    rows = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})
-    _check_rows(dev, rows)
+    _check_all_rows(dev)
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
@@ -271,15 +282,105 @@ def test_decode_quant_ragged_edges(fmt):
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
 def test_decode_v3_quant_full(fmt):
-    """H=128, B=64, seqlen 32768, random page table, quantized pool: first and
-    last rows against the oracle, the whole batch finite."""
+    """H=128, B=64, seqlen 32768, random page table, quantized pool: every row
+    against the oracle over the dequantized values."""
     prob = problem_from_workload(synth.get_workload("v3_quant"), fmt=fmt)
     dev = DeviceDecode(prob)
     dev.decode()
     torch.cuda.synchronize()
     _status_ok()
-    _check_rows(dev, [0, prob.B - 1])
-    assert np.all(np.isfinite(_out_f64(dev.out)))
+    _check_all_rows(dev)
+
+
+# ----------------------------------------------------------------------------
+# invariants of the result
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_split_count_invariance(H):
+    """The same rows decoded with 1, a few and the default number of split
+    workers (so with different cut points, partial counts and merges): each
+    result within tolerance of the oracle, and all within tolerance of the
+    default plan's."""
+    import mla_absorbed_latent_gb300 as mla
+    seqlens = [4000, 1, 777, 64, 2049, 0, 130, 9000, 65]
+    prob = make_problem(H, seqlens, seed=50 + H)
+    dev = DeviceDecode(prob)
+    wmax = mla.mla_decode_max_workers(H, "bf16")
+    ref = oracle_outputs(prob, [b for b, n in enumerate(seqlens) if n > 0])
+    outs = {}
+    for w in sorted({1, 3, 37 % wmax or 1, wmax}):
+        mla.mla_decode_plan_workers(H, "bf16", dev.seqlens, prob.B, prob.max_pages, w, dev.workspace, dev.ws_bytes)
+        mla.mla_decode_absorb_q(dev.q_nope, dev.q_pe, dev.W_UK, H, prob.B, dev.workspace, dev.ws_bytes)
+        mla.mla_decode_attend(H, dev.cache, dev.page_table, prob.max_pages, dev.seqlens, prob.B, prob.scale,
+                              dev.workspace, dev.ws_bytes)
+        mla.mla_decode_combine(dev.W_UV, H, prob.B, dev.workspace, dev.ws_bytes, dev.out)
+        torch.cuda.synchronize()
+        _status_ok()
+        outs[w] = _out_f64(dev.out)
+        for b in ref:
+            assert_close(outs[w][b], ref[b], what=f"W={w} out[{b}]")
+        assert not outs[w][seqlens.index(0)].any()
+    for w in outs:
+        assert_close(outs[w], outs[wmax], what=f"W={w} vs W={wmax}")
+    with pytest.raises(mla.MLAError):
+        mla.mla_decode_plan_workers(H, "bf16", dev.seqlens, prob.B, prob.max_pages, wmax + 1, dev.workspace,
+                                    dev.ws_bytes)
+
+
+def test_decode_row_independence():
+    """H=128: a row's output does not depend on the other rows.  Changing every
+    other row's queries and cache contents (lengths kept, so the split plan is
+    the same) leaves row 2's output bit for bit; changing the other rows'
+    lengths (a different plan) keeps it within tolerance of the oracle."""
+    import mla_absorbed_latent_gb300 as mla
+    seqlens = [3000, 500, 5000, 64, 1200, 7]
+    prob = make_problem(128, seqlens, seed=61)
+    dev = DeviceDecode(prob)
+    a = dev.decode().clone()
+    torch.cuda.synchronize()
+    # other rows: new queries and new cache contents
+    g = torch.Generator(device="cuda").manual_seed(5)
+    others = [b for b in range(prob.B) if b != 2]
+    for b in others:
+        dev.q_nope[b] = torch.randn((128, 128), generator=g, device="cuda").to(torch.bfloat16)
+        dev.q_pe[b] = torch.randn((128, 64), generator=g, device="cuda").to(torch.bfloat16)
+        for j in range((seqlens[b] + 63) // 64):
+            pg = int(dev.page_table[b, j])
+            vals = torch.randn(64 * 576, generator=g, device="cuda").to(torch.bfloat16)
+            dev.pool[pg * dev.page_bytes:(pg + 1) * dev.page_bytes] = vals.view(torch.uint8)
+    b_ = dev.decode().clone()
+    torch.cuda.synchronize()
+    _status_ok()
+    assert torch.equal(a[2], b_[2])
+    assert not torch.equal(a[0], b_[0])
+    # other rows' lengths change: a different plan, row 2 still matches the oracle
+    lens = torch.tensor([100, 4000, 5000, 1, 64, 2000], dtype=torch.int32, device="cuda")
+    mla.mla_decode(dev.q_nope, dev.q_pe, dev.W_UK, dev.W_UV, 128, dev.cache, dev.page_table, prob.max_pages, lens,
+                   prob.B, prob.scale, dev.workspace, dev.ws_bytes, dev.out)
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, [2])
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_nan_workspace(H):
+    """A workspace filled with all-ones bytes (NaN in bf16 and fp32) before the
+    decode: every value the decode reads from it must have been written by the
+    same call (an unwritten partial or flag would show up as NaN or a wrong
+    row).  Ragged lengths with an empty row, against the oracle."""
+    seqlens = [1, 31, 64, 65, 0, 700, 129, 2000]
+    prob = make_problem(H, seqlens, seed=70 + H)
+    dev = DeviceDecode(prob)
+    dev.workspace.fill_(0xFF)
+    o_lat = torch.full((prob.B, H, 512), float("nan"), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    rows = [b for b, n in enumerate(seqlens) if n > 0]
+    _check_rows(dev, rows, o_lat)
+    assert torch.count_nonzero(dev.out[seqlens.index(0)]) == 0
+    assert torch.count_nonzero(o_lat[seqlens.index(0)]) == 0
 
 
 def test_decode_bad_page_id_reports_bounds():
@@ -316,55 +417,116 @@ def test_bounded_wait_times_out_and_reports():
     _check_rows(dev, list(range(prob.B)), o_lat)
 
 
-def test_decode_score_beyond_tracked_range_is_reported():
-    """H=128: a token of the second page whose RoPE key is 200 x one head's
-    q_pe raises that head's score far more than 100 (log2 units) above the
-    first page's maximum; the kernel reports MLA_ERR_RANGE (weights capped)
-    and the output stays finite.  The row is long enough (304 pages) that the
-    first worker's range holds several pages, so page 1 is not the first page
-    of its split."""
+def _boost_rope_keys(dev, prob, boosts):
+    """Replace the RoPE keys of (head, token, lam) triples of row 0 by lam x that
+    head's q_pe (in the pool, and in the returned fp64 values the oracle reads);
+    each such token's score for that head rises by about lam x 6.7 log2 units."""
+    qp = synth.bf16_bits_to_f32(prob.q_pe)
+    c, p = prob.sequence(0)
+    C, P = synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p)
+    for head, token, lam in boosts:
+        bits = synth.f32_to_bf16_bits((lam * qp[0, head]).astype(np.float32))
+        P[token] = synth.bf16_bits_to_f32(bits)
+        page, slot = divmod(token, 64)
+        off = int(dev.page_table[0, page]) * dev.page_bytes + slot * 1152 + 1024  # the token's k_pe (bf16 pool)
+        dev.pool[off:off + 128] = torch.from_numpy(bits.view(np.uint8).copy()).to(dev.pool.device)
+    return C, P
+
+
+def _check_boosted_row(dev, prob, C, P, o_lat=None):
     import mla_absorbed_latent_gb300 as mla
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+    qn = synth.bf16_bits_to_f32(prob.q_nope)
+    qp = synth.bf16_bits_to_f32(prob.q_pe)
+    Wuk, Wuv = weights(prob)
+    ref_out, ref_lat, _ = O.absorbed_decode(qn[0], qp[0], C, P, Wuk, Wuv, prob.scale)
+    assert_close(_out_f64(dev.out)[0], ref_out)
+    if o_lat is not None:
+        assert_close(o_lat[0].cpu().numpy(), ref_lat, what="o_lat")
+
+
+def test_decode_score_beyond_tracked_range_is_exact():
+    """H=128: a token of the second page whose RoPE key is 200 x one head's
+    q_pe raises that head's score about 1,300 log2 units above the first
+    page's maximum, far past the 2^100 the fast path can weight in its running
+    reference; the row is recomputed exactly and must match the oracle (all
+    heads, out and o_lat).  The row is long enough (304 pages) that the first
+    worker's range holds several pages, so page 1 is not the first page of its
+    split."""
     prob = make_problem(128, [64 * 304], seed=6, paged=False)
     dev = DeviceDecode(prob)
-    qpe0 = synth.bf16_bits_to_f32(prob.q_pe)[0, 0]  # [64] of head 0
-    big = torch.from_numpy(synth.f32_to_bf16_bits(200.0 * qpe0).view(np.uint8).copy())
-    phys = int(dev.page_table[0, 1])
-    off = phys * dev.page_bytes + 0 * 1152 + 1024  # token 64 (slot 0 of page 1): its k_pe
-    dev.pool[off:off + 128] = big.to(dev.pool.device)
+    C, P = _boost_rope_keys(dev, prob, [(0, 64, 200.0)])
+    o_lat = torch.empty((1, 128, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _check_boosted_row(dev, prob, C, P, o_lat)
+
+
+def test_decode_large_half_scores_are_exact():
+    """H=128, paged: RoPE keys 12 x a head's q_pe (about 80 log2 units above the
+    rest, within the tracked range) make the half scores the CTA pair exchanges
+    exceed what fp16 carries to 2^-7; the row is recomputed exactly.  Two
+    further rows stay on the fast path and must still match."""
+    prob = make_problem(128, [64 * 40, 777, 64 * 9], seed=8)
+    dev = DeviceDecode(prob)
+    C, P = _boost_rope_keys(dev, prob, [(3, 64 * 5 + 7, 12.0), (100, 64 * 30 + 63, 12.0), (3, 2000, -12.0)])
     dev.decode()
     torch.cuda.synchronize()
-    st, _ = mla.mla_get_device_status()
-    assert st == mla.MLA_ERR_RANGE
-    assert bool(torch.all(torch.isfinite(dev.out.float())))
+    _check_boosted_row(dev, prob, C, P)
+    _check_rows(dev, [1, 2])
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_decode_quant_range_jump_is_exact(fmt):
+    """H=128 over quantized pools: one token's RoPE key (in its INT8 k_pe codes)
+    turned into 127 x sign(q_pe) of one head, scale 2, so that head's score jumps
+    far past the tracked range; the exact recompute reads the quantized page
+    (codes, scales, zeros) and must match the oracle over the dequantized
+    values."""
+    prob = make_problem(128, [64 * 150, 300], seed=33, fmt=fmt, dist="outlier")
+    dev = DeviceDecode(prob)
+    import mla_absorbed_latent_gb300 as mla
+    qp = synth.bf16_bits_to_f32(prob.q_pe)[0, 5]
+    token = 64 * 3 + 9
+    page, slot = divmod(token, 64)
+    base = int(dev.page_table[0, page]) * dev.page_bytes
+    pe_code, pe_scale = (32768, 38912) if fmt == "int8" else (16384, 24576)
+    codes = np.where(qp >= 0, 127, -127).astype(np.int8)
+    dev.pool[base + pe_code + slot * 64: base + pe_code + slot * 64 + 64] = torch.from_numpy(
+        codes.view(np.uint8).copy()).cuda()
+    scale_bits = synth.f32_to_bf16_bits(np.full(8, 2.0, np.float32))
+    dev.pool[base + pe_scale + slot * 16: base + pe_scale + slot * 16 + 16] = torch.from_numpy(
+        scale_bits.view(np.uint8).copy()).cuda()
+    dev.decode()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+    # the oracle over the dequantized values, with that token's RoPE key replaced
+    c, p = prob.sequence(0)
+    Cq, Pq = O.dequantized_tokens(fmt, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))
+    Pq = Pq.copy()
+    Pq[token] = codes.astype(np.float64) * 2.0
+    qn = synth.bf16_bits_to_f32(prob.q_nope)
+    Wuk, Wuv = weights(prob)
+    ref = O.absorbed_decode(qn[0], synth.bf16_bits_to_f32(prob.q_pe)[0], Cq, Pq, Wuk, Wuv, prob.scale)[0]
+    assert_close(_out_f64(dev.out)[0], ref)
+    _check_rows(dev, [1])
 
 
 def test_decode_reference_moves_keep_the_result_exact():
     """H=128: tokens of later pages whose RoPE keys are 3x one head's q_pe lift
     that head's scores by about 20 log2 units over the first page's maximum, so
-    the kernel moves its running reference (rescaling O) while staying far
-    inside its tracked range; the output must still match the oracle on the
-    same modified cache."""
-    import mla_absorbed_latent_gb300 as mla
+    the kernel moves its running reference (rescaling O) while staying inside
+    both its tracked range and the fp16 exchange bound (the fast path); the
+    output must still match the oracle on the same modified cache."""
     n = 64 * 304
     prob = make_problem(128, [n], seed=7, paged=False)
     dev = DeviceDecode(prob)
-    qn = synth.bf16_bits_to_f32(prob.q_nope)
-    qp = synth.bf16_bits_to_f32(prob.q_pe)
-    c, p = prob.sequence(0)
-    C, P = synth.bf16_bits_to_f32(c).astype(np.float64), synth.bf16_bits_to_f32(p).astype(np.float64)
-    for head, token, lam in ((0, 64 * 3 + 5, 3.0), (1, 64 * 9 + 40, 3.0), (0, 64 * 40 + 1, 5.0)):
-        bits = synth.f32_to_bf16_bits((lam * qp[0, head]).astype(np.float32))
-        P[token] = synth.bf16_bits_to_f32(bits)
-        page, slot = divmod(token, 64)
-        off = int(dev.page_table[0, page]) * dev.page_bytes + slot * 1152 + 1024  # the token's k_pe
-        dev.pool[off:off + 128] = torch.from_numpy(bits.view(np.uint8).copy()).to(dev.pool.device)
+    C, P = _boost_rope_keys(dev, prob, [(0, 64 * 3 + 5, 3.0), (1, 64 * 9 + 40, 3.0), (0, 64 * 40 + 1, 5.0)])
     dev.decode()
     torch.cuda.synchronize()
-    st, info = mla.mla_get_device_status()
-    assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
-    Wuk, Wuv = weights(prob)
-    ref = O.absorbed_decode(qn[0], qp[0], C, P, Wuk, Wuv, prob.scale)[0]
-    assert_close(_out_f64(dev.out)[0], ref)
+    _check_boosted_row(dev, prob, C, P)
 
 
 def test_decode_seqlen_over_capacity_reports_bounds():

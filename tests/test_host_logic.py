@@ -1,7 +1,8 @@
 """The library's host-side scheduling logic, compiled from its own sources and run
 on the CPU (no GPU involved): the split plan's partition of the global page list
-over the persistent workers, the decode workspace layout, and the producer's
-choice of K split and its workspace size."""
+over the persistent workers, the decode workspace layout (with the plan block's
+sections), the no-allocation decode's worker count, and the producer's choice of
+K split and its workspace size."""
 
 import os
 import shutil
@@ -54,7 +55,10 @@ int main() {
         const WsLayout L = ws_layout(B, H, Wk);
         CHECK(L.q_cat == 0, "B=%d", B);
         CHECK(L.plan >= L.q_cat + (size_t)B * H * DK * 2, "B=%d H=%d", B, H);
-        CHECK(L.part_o >= L.plan + (size_t)(PLAN_HDR + 2 * B + 1 + Wk) * 4, "B=%d W=%d", B, Wk);
+        CHECK(L.part_o >= L.plan + (size_t)(PLAN_HDR + 3 * B + 1 + Wk) * 4, "B=%d W=%d", B, Wk);
+        CHECK(plan_off_seq(B) == PLAN_HDR + B + 1 && plan_off_fix(B) == plan_off_seq(B) + B &&
+                  plan_off_wrow(B) == plan_off_fix(B) + B && PLAN_CTX * 4 + sizeof(FixCtx) <= PLAN_HDR * 4,
+              "B=%d", B);
         CHECK(L.part_lse >= L.part_o + (size_t)(Wk + B) * H * DC * 2, "B=%d H=%d W=%d", B, H, Wk);
         CHECK(L.total >= L.part_lse + (size_t)(Wk + B) * H * 4, "B=%d H=%d W=%d", B, H, Wk);
         CHECK(L.plan % 1024 == 0 && L.part_o % 1024 == 0 && L.part_lse % 1024 == 0 && L.total % 1024 == 0,
@@ -93,6 +97,23 @@ int main() {
           } else {
             CHECK(ws >= (size_t)mtiles * 128 * DK * 4 + (size_t)mtiles * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok,
                   k);
+          }
+        }
+  // 4. the no-allocation decode's worker count: the largest count <= want whose
+  //    workspace fits the capacity, 0 when one worker does not fit
+  const size_t caps[] = {1u << 20, 16u << 20, 64ull << 20};
+  const int wants[] = {1, 76, 304};
+  for (size_t cap : caps)
+    for (int H : Hs)
+      for (int want : wants)
+        for (int B = 1; B <= 2000; B += (B < 300 ? 7 : 101)) {
+          const int w = fitting_workers(B, H, want, cap);
+          CHECK(w >= 0 && w <= want, "B=%d H=%d want=%d w=%d", B, H, want, w);
+          if (w > 0) {
+            CHECK(ws_layout(B, H, w).total <= cap, "B=%d H=%d w=%d", B, H, w);
+            if (w < want) CHECK(ws_layout(B, H, w + 1).total > cap, "B=%d H=%d w=%d", B, H, w);
+          } else {
+            CHECK(ws_layout(B, H, 1).total > cap, "B=%d H=%d", B, H);
           }
         }
   std::printf("%d\n", fails);

@@ -37,6 +37,54 @@ def test_noalloc_matches_workspace_decode_twice(H, seqlens):
         assert_close(_f64(out), ref, what="noalloc vs workspace decode")
 
 
+def _noalloc_twice_vs_workspace(prob, dev):
+    import mla_absorbed_latent_gb300 as mla
+    ref = _f64(dev.decode())
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out = torch.full_like(dev.out, float("nan"))
+        mla.mla_decode_noalloc(dev.q_nope, dev.q_pe, dev.W_UK, dev.W_UV, prob.H, dev.cache, dev.page_table,
+                               prob.max_pages, dev.seqlens, prob.B, prob.scale, out)
+        torch.cuda.synchronize()
+        st, info = mla.mla_get_device_status()
+        assert st == mla.MLA_OK, (mla.mla_status_string(st), info)
+        assert_close(_f64(out), ref, what="noalloc vs workspace decode")
+    return out
+
+
+def test_noalloc_fewer_workers_than_decode():
+    """H=128, B=230: the query latent (34 MB) plus the partials of the default
+    worker count do not fit the 64 MiB scratch, but fewer workers do, so the
+    plan, attend and combine run with a reduced split count (and a partial
+    tensor map and merge sized by it); against the workspace decode twice, and
+    a few rows against the oracle."""
+    import mla_absorbed_latent_gb300 as mla
+    from tests.parity import oracle_outputs
+    H, B = 128, 230
+    # 34 MB of query latent + 76 default workers' partials (B + 76 slots of 131.6 KB) > 64 MiB;
+    # one worker's (B + 1 slots) fits
+    assert B * H * 576 * 2 + (B + mla.mla_decode_max_workers(H, "bf16")) * H * 1028 > mla.MLA_NOALLOC_SCRATCH_BYTES
+    assert B * H * 576 * 2 + (B + 1) * H * 1028 + (1 << 16) < mla.MLA_NOALLOC_SCRATCH_BYTES
+    seqlens = [(1, 64, 65, 130, 200, 7)[b % 6] for b in range(B)]
+    prob = make_problem(H, seqlens, seed=44)
+    dev = DeviceDecode(prob)
+    out = _noalloc_twice_vs_workspace(prob, dev)
+    rows = [0, 1, 2, 3, 4, 5, 117, 229]
+    ref = oracle_outputs(prob, rows)
+    got = _f64(out)
+    for b in rows:
+        assert_close(got[b], ref[b], what=f"noalloc out[{b}]")
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_noalloc_quantized_pools(fmt):
+    """H=128 over INT8 / INT4 pools through the no-allocation entry point,
+    against the workspace decode on two calls in a row."""
+    prob = make_problem(128, [3000, 1, 129, 640], seed=46, fmt=fmt, dist="outlier")
+    dev = DeviceDecode(prob)
+    _noalloc_twice_vs_workspace(prob, dev)
+
+
 def test_noalloc_rejects_batch_beyond_scratch():
     import mla_absorbed_latent_gb300 as mla
     prob = make_problem(128, [64], seed=3)
