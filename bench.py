@@ -418,7 +418,7 @@ def run_ours(args, wl, fmt):
         "parity": parity,  # the oracle rows of cpu_baseline against the timed decode's output
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,  # plan, absorb_q, attend, combine (merge + up-projection)
+        "gpu_launches": 5 * args.steps,  # plan, absorb_q, attend, combine (merge + up-projection), exact-recompute check
         "clocks": clock_info,
     }
     print(json.dumps(line), flush=True)

@@ -106,7 +106,6 @@ constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
 constexpr int Q_AHEAD = 8;  // pages before a row's end at which the producer prefetches the next query
 constexpr uint32_t QT_BYTES = 128 * 64 * 2;  // 16,384: one q_lat tile, [128 heads][64 dims] 128B-swizzled
 constexpr float RESCALE_LOG2 = 8.f;  // move the running max only when it grows by > 2^8
-constexpr float FP16_MAX = 65504.f;
 constexpr float RANGE_LOG2 = 100.f;  // largest exponent of p formed here (O and l stay finite in fp32)
 constexpr float EXCH_LOG2 = 32.f;    // largest |half score| (log2 units) exchanged in fp16 for an exact row
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;  // ~2 s at the maximum SM clock
@@ -323,11 +322,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
   static_assert(N == 16 || N == 32, "16 or 32 columns");
   if constexpr (N == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
 }
-// two fp16 in one 32-bit word <-> two floats, in registers (low half = first value)
-__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
+// two fp16 in one 32-bit word <-> two floats, in registers (low half = first
+// value); the conversion saturates to the largest finite fp16 (+-65504)
+__device__ __forceinline__ uint32_t f2_to_h2_sat(float lo, float hi) {
   uint32_t u;
-  memcpy(&u, &h, 4);
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(u) : "f"(hi), "f"(lo));
   return u;
 }
 __device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
@@ -335,7 +334,6 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
   memcpy(&h, &u, 4);
   return __half22float2(h);
 }
-__device__ __forceinline__ float fp16_clamp(float v) { return fminf(fmaxf(v, -FP16_MAX), FP16_MAX); }
 
 // byte offset of 16-byte unit u (0..3, 8 tokens) of row r in a 64B-swizzled tile of 64-byte rows
 // (the P half tiles, read by the tensor core, and the fp16 exchange tiles)
@@ -1049,15 +1047,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_proxy_async_smem();
         }
         uint32_t h[HALF_T / 2];
-        float amax = 0.f;  // largest |half score| of the page's tokens, for the exactness flag
 #pragma unroll
-        for (int k = 0; k < HALF_T / 2; ++k) {
-          const float x0 = u2f(v[2 * k]) * c, x1 = u2f(v[2 * k + 1]) * c;
-          amax = fmaxf(amax, tok0 + 2 * k < nvalid ? fabsf(x0) : 0.f);
-          amax = fmaxf(amax, tok0 + 2 * k + 1 < nvalid ? fabsf(x1) : 0.f);
-          h[k] = f2_to_h2(fp16_clamp(x0), fp16_clamp(x1));
-        }
-        if (amax > EXCH_LOG2) flag_row(fix, rc.b);
+        for (int k = 0; k < HALF_T / 2; ++k) h[k] = f2_to_h2_sat(u2f(v[2 * k]) * c, u2f(v[2 * k + 1]) * c);
         // the peer has consumed what we sent into its buffer two pages ago (so
         // the copy that read xout[sb] then has completed too); with a single
         // staging tile, also last page's
@@ -1073,6 +1064,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) bulk_s2peer(peer_xin + sb * X_BYTES, xo + X_Q * q4, X_Q, peer_xfull + BAR_SB * sb);
+        // after the copy is on its way (the peer waits for it, not for this): the
+        // exactness check of the shipped half scores of the page's valid tokens
+        {
+          const int lim = nvalid - tok0;  // valid tokens of the shipped half
+          float amax = 0.f;
+#pragma unroll
+          for (int k = 0; k < HALF_T; ++k)
+            if (k < lim) amax = fmaxf(amax, fabsf(u2f(v[k])));
+          if (amax * c > EXCH_LOG2) flag_row(fix, rc.b);
+        }
         if constexpr (kQuant) {
           // page i+2's operands (its stage was last read by page i+2-KV_ST's P.V)
           if (x + 2 < x1) {

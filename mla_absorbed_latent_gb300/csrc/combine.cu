@@ -168,7 +168,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return r;
 }
 // out[b][h] (and o_lat[b][h] when given) of one row of n > 0 tokens, exactly;
-// every thread of the CTA calls it (NT threads); scratch: 1,408 + NT floats of shared memory
+// every thread of the CTA calls it (NT threads); scratch: 1,120 + NT floats of shared memory
 template <int NT>
 __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, int n, const uint16_t* W_UV,
                                         uint16_t* out, float* o_lat, float* scratch, int* err) {
@@ -312,10 +312,6 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   }
   grid_dep_wait();  // the partials and their log-sum-exps
   grid_dep_launch();
-  // rows of this group the attend kernel flagged for an exact recompute (read
-  // now, used at the end)
-  const int* fixf = plan + plan_off_fix(B);
-  const int myfix = (tid < RB && b0 + tid < B) ? fixf[b0 + tid] : 0;
 
   // ---- the slots [s_lo, s_hi) that hold every segment of the group's rows:
   // segment w + b of row b, rows and workers both increasing along the tiles
@@ -493,15 +489,26 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     fence_after_sync();
     tmem_dealloc(tmem, L::TCOLS);
   }
-  if (__syncthreads_or(myfix) && !*abort) {
-    // every ring load has landed and been read: the partial ring is free scratch
-    const FixCtx fx = *reinterpret_cast<const FixCtx*>(plan + PLAN_CTX);
-    const int* seq_c = plan + plan_off_seq(B);
-    for (int r = 0; r < RB && b0 + r < B; ++r)
-      if (fixf[b0 + r])
-        exact_head<L::THREADS>(fx, b0 + r, h, H, seq_c[b0 + r], W_UV, out, o_lat,
-                               reinterpret_cast<float*>(sm + L::OFF_P), err);
-  }
+}
+
+// The exact recompute as its own kernel, after the merge: one CTA per (head,
+// group of 32 rows) reads the group's flags and leaves at once when none is set
+// (the common case costs one launch of the decode chain); otherwise it
+// overwrites the flagged rows' outputs (and o_lat) with the exact values.
+template <int NT>
+__global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, int B, const int* plan, uint16_t* out,
+                                                 float* o_lat, int* err) {
+  __shared__ float scratch[DK + NT + 32 + DC];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int h = blockIdx.x, b0 = blockIdx.y * 32;
+  const int* fixf = plan + plan_off_fix(B);
+  const int f = (threadIdx.x < 32 && b0 + (int)threadIdx.x < B) ? fixf[b0 + threadIdx.x] : 0;
+  if (!__syncthreads_or(f)) return;
+  const FixCtx fx = *reinterpret_cast<const FixCtx*>(plan + PLAN_CTX);
+  const int* seq_c = plan + plan_off_seq(B);
+  for (int r = 0; r < 32 && b0 + r < B; ++r)
+    if (fixf[b0 + r]) exact_head<NT>(fx, b0 + r, h, H, seq_c[b0 + r], W_UV, out, o_lat, scratch, err);
 }
 
 template <int RB>
@@ -531,9 +538,14 @@ cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, cons
     return cudaErrorInvalidValue;
   // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
   const int sms = device_sm_count();
+  cudaError_t e;
   if ((long long)H * ((B + 31) / 32) >= sms)
-    return launch_rb<32>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
-  return launch_rb<16>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+    e = launch_rb<32>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+  else
+    e = launch_rb<16>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(fix_kernel<256>, dim3(H, (B + 31) / 32), dim3(256), 0, s, static_cast<const uint16_t*>(W_UV), H, B,
+                    plan, static_cast<uint16_t*>(out), o_lat, err);
 }
 
 }  // namespace mla
