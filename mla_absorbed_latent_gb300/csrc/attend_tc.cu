@@ -342,33 +342,150 @@ __device__ __forceinline__ uint32_t sw64(int r, int u) { return (uint32_t)(r * 6
 // ---- dequantization ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 block
 // quantizers): x = code * s (INT8), x = code * s + z (INT4), evaluated in fp32
 // and rounded once to bf16 for the MMA.  Integer codes reach fp32 exactly by
-// placing them in the low mantissa bits of 2^23 and subtracting the offset.
+// placing them in the low mantissa bits of 2^23 (a byte permute) and
+// subtracting the offset; pairs of values go through the packed fp32 pipe
+// (add/mul/fma.rn.f32x2), whose results equal the scalar ones (the code
+// product with a bf16 scale is exact in fp32; INT4's fma rounds once).
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-// byte k (0..3) of a word of signed 8-bit codes, as an exact float
-__device__ __forceinline__ float i8_at(uint32_t w, int k) {
-  const uint32_t biased = w ^ 0x80808080u;  // code + 128 in 0..255
-  return __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u + (uint32_t)k)) - 8388736.f;  // 2^23 + 128
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// two fp32 (one packed pair) rounded to a bf16x2 word (low half = first value)
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return pack_bf16x2(lo, hi);
+}
+// bytes k, k+1 of a word (already biased / masked into 0..255) as 2^23 + byte, packed
+__device__ __forceinline__ uint64_t magic_pair(uint32_t w, int k) {
+  return f2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + (uint32_t)k)),
+            __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7441u + (uint32_t)k)));
+}
+// bytes k, k+1 of a word of signed 8-bit codes times s2 = {s, s} -> bf16x2
+__device__ __forceinline__ uint32_t deq_i8_pair(uint32_t biased, int k, uint64_t s2) {
+  const uint64_t off = f2(-8388736.f, -8388736.f);  // -(2^23 + 128): the codes exactly
+  return f2_to_bf16x2(mul_f2(add_f2(magic_pair(biased, k), off), s2));
 }
 // 8 signed 8-bit codes times s -> 8 bf16 (one 16-byte unit)
-__device__ __forceinline__ uint4 deq_i8x8(uint2 w, float s) {
-  uint4 o;
-  o.x = pack_bf16x2(i8_at(w.x, 0) * s, i8_at(w.x, 1) * s);
-  o.y = pack_bf16x2(i8_at(w.x, 2) * s, i8_at(w.x, 3) * s);
-  o.z = pack_bf16x2(i8_at(w.y, 0) * s, i8_at(w.y, 1) * s);
-  o.w = pack_bf16x2(i8_at(w.y, 2) * s, i8_at(w.y, 3) * s);
-  return o;
+__device__ __forceinline__ uint4 deq_i8x8(uint32_t c0, uint32_t c1, float s) {
+  const uint64_t s2 = f2(s, s);
+  const uint32_t w0 = c0 ^ 0x80808080u, w1 = c1 ^ 0x80808080u;
+  return make_uint4(deq_i8_pair(w0, 0, s2), deq_i8_pair(w0, 2, s2), deq_i8_pair(w1, 0, s2), deq_i8_pair(w1, 2, s2));
 }
-// nibble j (0..7) of a word of 4-bit codes (element 2i in the low nibble of byte i), as an exact float
-__device__ __forceinline__ float u4_at(uint32_t w, int j) {
-  return __uint_as_float(0x4B000000u | ((w >> (4 * j)) & 0xFu)) - 8388608.f;  // 2^23
+// 16 signed 8-bit codes (one 16-byte load) times s -> 16 bf16 (two 16-byte units)
+__device__ __forceinline__ void deq_i8x16(uint4 c, float s, uint4& o0, uint4& o1) {
+  const uint64_t s2 = f2(s, s);
+  const uint32_t w0 = c.x ^ 0x80808080u, w1 = c.y ^ 0x80808080u, w2 = c.z ^ 0x80808080u, w3 = c.w ^ 0x80808080u;
+  o0 = make_uint4(deq_i8_pair(w0, 0, s2), deq_i8_pair(w0, 2, s2), deq_i8_pair(w1, 0, s2), deq_i8_pair(w1, 2, s2));
+  o1 = make_uint4(deq_i8_pair(w2, 0, s2), deq_i8_pair(w2, 2, s2), deq_i8_pair(w3, 0, s2), deq_i8_pair(w3, 2, s2));
 }
-__device__ __forceinline__ uint4 deq_u4x8(uint32_t w, float s, float z) {
-  uint4 o;
-  o.x = pack_bf16x2(fmaf(u4_at(w, 0), s, z), fmaf(u4_at(w, 1), s, z));
-  o.y = pack_bf16x2(fmaf(u4_at(w, 2), s, z), fmaf(u4_at(w, 3), s, z));
-  o.z = pack_bf16x2(fmaf(u4_at(w, 4), s, z), fmaf(u4_at(w, 5), s, z));
-  o.w = pack_bf16x2(fmaf(u4_at(w, 6), s, z), fmaf(u4_at(w, 7), s, z));
-  return o;
+// 8 unsigned 4-bit codes of one word (element 2i in the low nibble of byte i)
+// as code * s + z -> 8 bf16 (one 16-byte unit)
+__device__ __forceinline__ uint4 deq_u4x8(uint32_t w, uint64_t s2, uint64_t z2) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint64_t off = f2(-8388608.f, -8388608.f);  // -2^23
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t m = f2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + (uint32_t)i)),
+                          __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + (uint32_t)i)));
+    r[i] = f2_to_bf16x2(fma_f2(add_f2(m, off), s2, z2));
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// One staged page half (codes, scales, zeros of this CTA's dims) -> the bf16
+// operand stage, by the 128 threads sid = 0..127 of the four PT warps.  Every
+// thread owns fixed 16-byte code chunks:
+//   INT8 latent: 64 tokens x 16 chunks of 16 codes; chunk k = sid + 128 i is
+//     token k / 16, dims 16 (k % 16) .. (operand chunk (k % 16) / 4), scale
+//     group (k % 16) / 2;
+//   INT4 latent: 64 tokens x 8 chunks of 32 codes (one group each); chunk
+//     k = sid + 128 i is token k / 8, group k % 8 (operand chunk (k % 8) / 2);
+//   RoPE key (INT8 in both): token sid / 2, dims 16 (sid % 2) .., groups
+//     4 rank + 2 (sid % 2) + {0, 1}.
+// Tokens at or past nvalid are written as zeros.  A thread's latent rows share
+// one swizzle (their tokens differ by multiples of 8).  The 8 lanes of a
+// quarter warp (one phase of a 16-byte store) write 8 different 16-byte bank
+// groups: the operand chunks are 8 KB apart (the same banks), so lanes of odd
+// operand chunks store their two INT8 units in the other order, and INT4 lanes
+// rotate their four units by the chunk index.  Out of line and rolled (with
+// the next chunk's loads in flight): instruction fetch, not arithmetic, bounds
+// this stage.
+template <int FMT>
+__device__ __noinline__ void dequant_page(const uint8_t* cd, uint8_t* kv, int nvalid, int sid, int rank) {
+  using FT = FmtTraits<FMT>;
+  constexpr bool kI8 = FMT == MLA_FMT_INT8;
+  constexpr int NCH = kI8 ? 8 : 4, QN = kI8 ? 16 : 8, ROW = kI8 ? 256 : 128, TSTEP = 128 / QN;
+  const int q = sid % QN, t0 = sid / QN, sw = t0 & 7;
+  const int ci = kI8 ? q >> 2 : q >> 1, u0 = kI8 ? 2 * (q & 3) : 4 * (q & 1);
+  const uint8_t* cp = cd + FT::C_OFF + t0 * ROW + 16 * q;
+  const uint16_t* sp = reinterpret_cast<const uint16_t*>(cd + FT::CS_OFF) + t0 * 8 + (kI8 ? q >> 1 : q);
+  const uint16_t* zp = reinterpret_cast<const uint16_t*>(cd + FT::ZS_OFF) + t0 * 8 + q;
+  uint8_t* row = kv + ci * KV_CHUNK + t0 * 128;
+  uint4 cn = *reinterpret_cast<const uint4*>(cp);
+  uint16_t sn = sp[0], zn = kI8 ? 0 : zp[0];
+#pragma unroll 1
+  for (int i = 0; i < NCH; ++i) {
+    const uint4 c = cn;
+    const uint16_t sc = sn, zc = zn;
+    const int nx = i + 1 < NCH ? i + 1 : i;  // the next chunk's loads go out now
+    cn = *reinterpret_cast<const uint4*>(cp + nx * TSTEP * ROW);
+    sn = sp[nx * TSTEP * 8];
+    if constexpr (!kI8) zn = zp[nx * TSTEP * 8];
+    const bool live = t0 + TSTEP * i < nvalid;
+    uint8_t* r = row + i * TSTEP * 128;
+    if constexpr (kI8) {
+      const bool odd = ci & 1;  // store the second unit first
+      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+      if (live)
+        deq_i8x16(odd ? make_uint4(c.z, c.w, c.x, c.y) : c, bf16_to_f(sc), o0, o1);
+      *reinterpret_cast<uint4*>(r + (((u0 + (odd ? 1 : 0)) ^ sw) << 4)) = o0;
+      *reinterpret_cast<uint4*>(r + (((u0 + (odd ? 0 : 1)) ^ sw) << 4)) = o1;
+    } else {
+      const float s1 = bf16_to_f(sc), z1 = bf16_to_f(zc);
+      const uint64_t s2 = f2(s1, s1), z2 = f2(z1, z1);
+      // the four words rotated by ci: store k writes unit (u0 + (k + ci) % 4)
+      uint32_t w0 = c.x, w1 = c.y, w2 = c.z, w3 = c.w;
+      if (ci & 1) { const uint32_t t = w0; w0 = w1; w1 = w2; w2 = w3; w3 = t; }
+      if (ci & 2) { uint32_t t = w0; w0 = w2; w2 = t; t = w1; w1 = w3; w3 = t; }
+      const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(r + (((u0 + ((k + ci) & 3)) ^ sw) << 4)) =
+            live ? deq_u4x8(w[k], s2, z2) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // RoPE key
+  const int tp = sid >> 1, hh = sid & 1;
+  const uint4 pw = *reinterpret_cast<const uint4*>(cd + FT::PE_OFF + tp * 32 + 16 * hh);
+  const uint16_t* psc = reinterpret_cast<const uint16_t*>(cd + FT::PS_OFF) + tp * 8 + 4 * rank + 2 * hh;
+  uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+  if (tp < nvalid) {
+    o0 = deq_i8x8(pw.x, pw.y, bf16_to_f(psc[0]));  // dims 0..7: the first group's scale
+    o1 = deq_i8x8(pw.z, pw.w, bf16_to_f(psc[1]));  // dims 8..15: the second's
+  }
+  uint8_t* pr = kv + KV_PE_OFF + tp * 64;
+  const int psw = (tp >> 1) & 3;
+  *reinterpret_cast<uint4*>(pr + (((2 * hh) ^ psw) << 4)) = o0;
+  *reinterpret_cast<uint4*>(pr + (((2 * hh + 1) ^ psw) << 4)) = o1;
 }
 
 // The cache tensor maps: bf16 pages use m0 (latent, 128B-swizzled boxes of 64
@@ -972,35 +1089,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // the P.V that last read this operand stage has completed
         if (!wait_bar<false>(S, &S.kv_empty[st], ((uint32_t)(j / KV_ST) & 1u) ^ 1u, a.err, 24)) ok = false;
         __syncwarp();
-        const uint8_t* cd = S.code[cs];
-        uint8_t* kv = S.kv[st];
-        // latent: 4 chunks x 64 tokens x 8 units of 8 dims, 128B-swizzled rows
-        for (int idx = sid; idx < 4 * TILE * 8; idx += NSEND) {
-          const int t = idx >> 5, ci = (idx >> 3) & 3, u = idx & 7;
-          const int d0 = 64 * ci + 8 * u;  // local latent dim of the unit's first element
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (t < nvalid) {
-            const float sc = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::CS_OFF)[t * 8 + (d0 >> 5)]);
-            if constexpr (FMT == MLA_FMT_INT8) {
-              o = deq_i8x8(*reinterpret_cast<const uint2*>(cd + FT::C_OFF + t * 256 + d0), sc);
-            } else {
-              const float z = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::ZS_OFF)[t * 8 + (d0 >> 5)]);
-              o = deq_u4x8(*reinterpret_cast<const uint32_t*>(cd + FT::C_OFF + t * 128 + (d0 >> 1)), sc, z);
-            }
-          }
-          *reinterpret_cast<uint4*>(kv + ci * KV_CHUNK + t * 128 + ((u ^ (t & 7)) << 4)) = o;
-        }
-        // RoPE key: 64 tokens x 4 units of 8 dims, 64B-swizzled rows; unit u is
-        // the 8-dim group 4r + u of the token
-        for (int idx = sid; idx < TILE * 4; idx += NSEND) {
-          const int t = idx >> 2, u = idx & 3;
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (t < nvalid) {
-            const float sc = bf16_to_f(reinterpret_cast<const uint16_t*>(cd + FT::PS_OFF)[t * 8 + 4 * (int)rank + u]);
-            o = deq_i8x8(*reinterpret_cast<const uint2*>(cd + FT::PE_OFF + t * 32 + 8 * u), sc);
-          }
-          *reinterpret_cast<uint4*>(kv + KV_PE_OFF + t * 64 + ((u ^ ((t >> 1) & 3)) << 4)) = o;
-        }
+        if constexpr (kQuant) dequant_page<FMT>(S.code[cs], S.kv[st], nvalid, sid, (int)rank);
         fence_proxy_async_smem();  // generic writes -> the tensor core's reads
         __syncwarp();
         if (lane == 0) {
