@@ -260,6 +260,38 @@ int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t w
                        void* out, float* o_lat_out, cudaStream_t stream);
 
 /*
+ * Several query tokens per row, causal: the absorbed attention of T new tokens
+ * of every row over its cache (speculative / multi-token prediction decode, or
+ * a prefill chunk run in absorbed form).  "手搓 MLA" §四 writes the absorbed
+ * einsums with a query-token axis t (thd,hdc->thc; thc,sc->hts; hts,sc->thc;
+ * thc,hdc->thd); "DeepSeek MLA 吸收式缓存" §3.4 runs the same layer as a
+ * 25-token causal prefill and a 1-token incremental decode.
+ *   q_nope    : bf16 [B][T][H][128]    q_pe : bf16 [B][T][H][64] (RoPE-rotated)
+ *   seqlens   : int32 [B] (device): row b holds n_b >= T cached tokens whose
+ *               last T are the queries (appended first): query t sits at
+ *               position n_b - T + t and attends to tokens 0 .. n_b - T + t.
+ *               n_b < T raises MLA_ERR_BOUNDS (queries then see no more than
+ *               the row holds).
+ *   workspace : >= mla_decode_q_workspace_bytes(B, H, T) bytes, 256-byte aligned
+ *   out       : bf16 [B][T][H][128], written
+ *   o_lat_out : NULL, or fp32 [B][T][H][512]: the merged latent sums
+ * 1 <= T <= 65536, H in {16, 128}, every cache format; other arguments as
+ * mla_decode.  Runs on the tcgen05 kernel for both head counts: its MMA has
+ * 128 rows, so G = 128 / H query tokens of a row share one pass over the
+ * row's cache (H = 16: 8 tokens, so the work per cached byte grows 8x;
+ * H = 128: one token per pass) and each of those rows sees its own causal
+ * prefix.  Same tolerance and exactness as mla_decode.
+ */
+int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H, int T,
+                 const mla_cache_t* cache, const int32_t* page_table, int max_pages,
+                 const int32_t* seqlens, int B, float scale,
+                 void* workspace, size_t workspace_bytes, void* out, float* o_lat_out, cudaStream_t stream);
+
+/* Workspace of mla_decode_q for B rows, H heads and T query tokens per row on
+ * the current device (0 for arguments it would reject). */
+size_t mla_decode_q_workspace_bytes(int B, int H, int T);
+
+/*
  * Decode without any allocation (no counterpart on the pages: an interface
  * addition of this library for hosts that cannot allocate device memory, e.g.
  * an engine whose custom-op interface passes only inputs and outputs, a

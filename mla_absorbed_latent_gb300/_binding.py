@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
         "mla_decode_attend": (i, [i, cp, vp, i, vp, i, f, vp, sz, vp]),
         "mla_decode_combine": (i, [vp, i, i, vp, sz, vp, vp, vp]),
         "mla_decode_noalloc": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, vp]),
+        "mla_decode_q": (i, [vp, vp, vp, vp, i, i, cp, vp, i, vp, i, f, vp, sz, vp, vp, vp]),
+        "mla_decode_q_workspace_bytes": (sz, [i, i, i]),
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
         "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
@@ -130,6 +132,18 @@ def mla_decode(q_nope, q_pe, W_UK, W_UV, H: int, cache: mla_cache_t, page_table,
     _check(_lib.mla_decode(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, ctypes.byref(cache),
                            _ptr(page_table), max_pages, _ptr(seqlens), B, scale, _ptr(workspace),
                            workspace_bytes, _ptr(out), _stream(stream)), "mla_decode")
+
+
+def mla_decode_q_workspace_bytes(B: int, H: int, T: int) -> int:
+    return int(_lib.mla_decode_q_workspace_bytes(B, H, T))
+
+
+def mla_decode_q(q_nope, q_pe, W_UK, W_UV, H: int, T: int, cache: mla_cache_t, page_table, max_pages: int, seqlens,
+                 B: int, scale: float, workspace, workspace_bytes: int, out, o_lat_out=None, stream=None) -> None:
+    """T causal query tokens per row (the last T cached tokens of each row)."""
+    _check(_lib.mla_decode_q(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, T, ctypes.byref(cache),
+                             _ptr(page_table), max_pages, _ptr(seqlens), B, scale, _ptr(workspace), workspace_bytes,
+                             _ptr(out), _ptr(o_lat_out), _stream(stream)), "mla_decode_q")
 
 
 def mla_decode_plan(H: int, fmt: str | int, seqlens, B: int, max_pages: int, workspace, workspace_bytes: int,

@@ -187,8 +187,10 @@ struct TcArgs {
   uint16_t* part_o;  // bf16 [segments][128][512]
   float* part_lse;
   int* err;
-  int B, max_pages, num_pages;
+  int B, max_pages, num_pages;  // B: plan rows (virtual rows of the query layout)
   float scale_log2;
+  QSpec qs;           // query layout: virtual row r reads page-table row r / qs.NG
+  long long q_rows;   // flat rows of q_cat
 };
 
 // Bounded wait shared by all roles: gives up after WAIT_LIMIT_CYCLES (records
@@ -199,6 +201,16 @@ struct TcArgs {
 __device__ __noinline__ void report_error(int* err, int code, int info) { raise_error(err, code, info); }
 // a row whose weights cannot be formed exactly here: the combine kernel recomputes it
 __device__ __noinline__ void flag_row(int* fix, int b) { fix[b] = 1; }
+// Query layout lookups, out of line (rare: at row changes, and only with several
+// query tokens per row) so that the page loops' code stays small: the flat
+// query row of a virtual row, its page-table row, a lane's causal shift.
+__device__ __noinline__ long long qrow_of(const QSpec qs, int r) { return qs.qrow(r); }
+__device__ __noinline__ int page_row_of(const QSpec qs, int r) { return r / qs.NG; }
+__device__ __noinline__ int shift_of(const QSpec qs, int r, int v) { return qs.shift(r, v); }
+__device__ __forceinline__ long long qrow_at(const QSpec& qs, int r) {
+  return qs.NG == 1 && qs.T == 1 ? (long long)r * 128 : qrow_of(qs, r);
+}
+__device__ __forceinline__ int page_row_at(const QSpec& qs, int r) { return qs.NG == 1 ? r : page_row_of(qs, r); }
 
 template <bool kCluster>
 __device__ __forceinline__ bool probe_bar(uint64_t* bar, uint32_t parity) {
@@ -581,6 +593,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fx->num_pages = a.num_pages;
     fx->fmt = FMT;
     fx->scale_log2 = a.scale_log2;
+    fx->qs = a.qs;
   }
   const int x0 = live ? (int)worker_begin(worker, T, W) : 0, x1 = live ? (int)worker_begin(worker + 1, T, W) : 0;
   const int ntiles = x1 - x0;
@@ -620,7 +633,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // with a high retention priority (each CTA of the pair half of it)
         RowCursor nx = rc;
         nx.advance(prefix, seq_c, rc.end);
-        prefetch_l2_bulk_hint(a.q_cat + ((size_t)nx.b * 128 + 64 * rank) * DK, 64 * DK * 2, policy_evict_last());
+        const long long qr = qrow_at(a.qs, nx.b) + 64 * rank;
+        if (qr + 64 <= a.q_rows) prefetch_l2_bulk_hint(a.q_cat + qr * DK, 64 * DK * 2, policy_evict_last());
       }
       if (rc.b != page_row || j - jbase >= 32) {
         if (rc.b != page_row && rc.end < x1) {
@@ -629,13 +643,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // the next segment change
           RowCursor nx = rc;
           nx.advance(prefix, seq_c, rc.end);
-          const int32_t* pt = a.page_table + (size_t)nx.b * a.max_pages;
+          const int32_t* pt = a.page_table + (size_t)page_row_at(a.qs, nx.b) * a.max_pages;
           const int nt = nx.end - nx.start;
           for (int k = 32 * lane; k < nt; k += 32 * 32) prefetch_l2_line(pt + k);
         }
         page_row = rc.b;
         jbase = j;
-        page_reg = (j + lane < rc.end - rc.start) ? a.page_table[(size_t)rc.b * a.max_pages + j + lane] : 0;
+        page_reg = (j + lane < rc.end - rc.start)
+                       ? a.page_table[(size_t)page_row_at(a.qs, rc.b) * a.max_pages + j + lane]
+                       : 0;
       }
       int page = __shfl_sync(0xffffffffu, page_reg, j - jbase);
       int ok = 1;
@@ -648,9 +664,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ok = wait_bar<false>(S, &S.kv_empty[st], ((u / KV_ST) & 1) ^ 1, a.err, 1);
             if (ok) {
               mbar_arrive_expect_tx(&S.kv_full[st], 2 * QT_BYTES + QPE_BYTES / 2);
+              const int qr = (int)qrow_at(a.qs, rc.b);  // flat query rows (past the end: zeros)
               for (int c = 0; c < 2; ++c)
-                tma_load_3d(S.kv[st] + c * QT_BYTES, &tm_m2, HALF_C * rank + 128 * h + 64 * c, 0, rc.b, &S.kv_full[st]);
-              tma_load_3d(S.kv[st] + 2 * QT_BYTES, &tm_m3, DC + PE_HALF * rank, 64 * h, rc.b, &S.kv_full[st]);
+                tma_load_3d(S.kv[st] + c * QT_BYTES, &tm_m2, HALF_C * rank + 128 * h + 64 * c, qr, 0, &S.kv_full[st]);
+              tma_load_3d(S.kv[st] + 2 * QT_BYTES, &tm_m3, DC + PE_HALF * rank, qr + 64 * h, 0, &S.kv_full[st]);
               ++issued;
             }
           }
@@ -820,13 +837,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // the query of row b into place: the q_lat half into TMEM (each thread its
     // 2*QCOLS latent dims), the q_pe half into shared memory by one TMA copy
     auto load_query = [&](int b) {
-      const uint16_t* qrow = a.q_cat + ((size_t)b * 128 + row) * DK;
+      // flat query row of this lane (rows past the end of q_cat read as zeros)
+      const long long qr = qrow_at(a.qs, b) + row;
+      const bool have = qr < a.q_rows;
+      const uint16_t* qrow = a.q_cat + (have ? qr : 0) * DK;
       const uint4* qc = reinterpret_cast<const uint4*>(qrow + HALF_C * rank + 2 * QCOLS * sub);
       // every global read is issued before the first TMEM store (one round trip)
       uint32_t v[QCOLS];
 #pragma unroll
       for (int k = 0; k < QCOLS / 4; ++k) {
-        const uint4 u = qc[k];
+        const uint4 u = have ? qc[k] : make_uint4(0u, 0u, 0u, 0u);
         v[4 * k] = u.x; v[4 * k + 1] = u.y; v[4 * k + 2] = u.z; v[4 * k + 3] = u.w;
       }
 #pragma unroll
@@ -837,7 +857,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (lane == 0) mbar_arrive(&S.q_ready);
       if (stid == 0) {
         mbar_arrive_expect_tx(&S.q_ready, QPE_BYTES);
-        tma_load_3d(S.qpe, &tm_q_pe, DC + PE_HALF * rank, 0, b, &S.q_ready);
+        tma_load_3d(S.qpe, &tm_q_pe, DC + PE_HALF * rank, (int)qrow_at(a.qs, b), 0, &S.q_ready);
       }
     };
     // The pair splits every page by token half: CTA r runs the softmax of all
@@ -888,6 +908,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       //  alpha_prev  factor of the reference move made at the last check (1 if none)
       float m_ref = -INFINITY, l = 0.f, alpha_prev = 1.f;
       int fcnt = 0;  // segment starts seen (phases of mx_full, mx_empty)
+      // tokens at the end of the row's view that this lane's query does not see
+      // (several query tokens per row: causal; padding lanes see nothing).  Such
+      // a lane can have a whole segment masked: its reference stays -inf, its p
+      // are 0, and its segment is stored as O = 0, LSE = -inf.
+      int shift = 0;
       // check of page j, at the end of page j+1 (so it waits for nothing in
       // the common case): the four slice messages of page j have arrived.  If
       // page j's maximum exceeded its reference by more than RESCALE_LOG2 the
@@ -929,7 +954,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!wait_bar<false>(S, &S.pv_done[jb], (uint32_t)(j >> 1) & 1u, a.err, 22)) ok = false;
           __syncwarp();
           fence_after_sync();
-          store_o(seg, 1.f / L);
+          store_o(seg, L > 0.f ? 1.f / L : 0.f);  // a segment this lane sees nothing of: O = 0
           if (rank == 0 && ms == 0) a.part_lse[(size_t)seg * 128 + row] = (ref_j + log2f(Lm)) * 0.69314718055994531f;
           fence_before_sync();
           __syncwarp();
@@ -948,7 +973,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         rc.advance(prefix, seq_c, x);
         const bool first = (x == x0) || (x == rc.start);
         last = (x + 1 == x1) || (x + 1 == rc.end);
-        const int nvalid = min(TILE, rc.n - TILE * (x - rc.start));
+        if (first) shift = a.qs.G > 1 ? shift_of(a.qs, rc.b, row) : 0;
+        // tokens of this page this lane's query sees (may be <= 0)
+        const int nvalid = min(TILE, rc.n - shift - TILE * (x - rc.start));
         const int sb = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
 
@@ -1027,10 +1054,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // RANGE_LOG2: beyond it the row was flagged above for the exact recompute)
         uint32_t pk[TPW / 2];
         float sum0 = 0.f, sum1 = 0.f;
+        const float mr = fmaxf(m_ref, -3.0e38f);  // m_ref = -inf only when every s is -inf (p = 0)
 #pragma unroll
         for (int k = 0; k < TPW / 2; ++k) {
-          const float p0 = ex2(fminf(s[2 * k] - m_ref, RANGE_LOG2));
-          const float p1 = ex2(fminf(s[2 * k + 1] - m_ref, RANGE_LOG2));
+          const float p0 = ex2(fminf(s[2 * k] - mr, RANGE_LOG2));
+          const float p1 = ex2(fminf(s[2 * k + 1] - mr, RANGE_LOG2));
           sum0 += p0;
           sum1 += p1;
           pk[k] = pack_bf16x2(p0, p1);
@@ -1278,24 +1306,29 @@ int attend_tc_workers(int num_sms) {
   return g_tc_workers[dev];
 }
 
-cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
-                             const int32_t* page_table, int max_pages, int B, float scale, int* plan,
+cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int num_pages, const void* pages,
+                             const int32_t* page_table, int max_pages, int Bv, float scale, int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
-  if (H != 128 || workers < 1) return cudaErrorNotSupported;
+  if (qs.G * qs.Hr != 128 || qs.T < 1 || qs.NG != (qs.T + qs.G - 1) / qs.G || workers < 1) return cudaErrorNotSupported;
   if (fmt != MLA_FMT_BF16 && fmt != MLA_FMT_INT8 && fmt != MLA_FMT_INT4) return cudaErrorNotSupported;
   if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling
+  const long long q_rows = (long long)(Bv / qs.NG) * qs.T * qs.Hr;
+  if (q_rows > 2147483647LL - 256) return cudaErrorNotSupported;  // query rows are TMA coordinates
   CUtensorMap m[5], tq_pe;
   const uint64_t row = (uint64_t)DK * 2;  // 1,152 bytes per bf16 token slot / query row
   const uint8_t* pg = static_cast<const uint8_t*>(pages);
   const uint64_t P = (uint64_t)num_pages;
+  const uint64_t QR = (uint64_t)q_rows;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle NS = CU_TENSOR_MAP_SWIZZLE_NONE;
-  bool ok = encode_3d(&tq_pe, q_cat, DK, 128, B, row, row * 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+  // the query: flat rows of 576 (a virtual row's 128 virtual heads are 128
+  // consecutive rows from qs.qrow(r)); rows past the end read as zeros
+  bool ok = encode_3d(&tq_pe, q_cat, DK, QR, 1, row, row * QR, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
   if (fmt == MLA_FMT_BF16) {
     ok = ok && encode_3d(&m[0], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
          encode_3d(&m[1], pg, DK, PAGE, P, row, PAGE_BYTES_BF16, 32, TILE, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         encode_3d(&m[2], q_cat, DK, 128, B, row, row * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_3d(&m[3], q_cat, DK, 128, B, row, row * 128, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+         encode_3d(&m[2], q_cat, DK, QR, 1, row, row * QR, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_3d(&m[3], q_cat, DK, QR, 1, row, row * QR, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
     m[4] = m[0];
   } else if (fmt == MLA_FMT_INT8) {
     const uint64_t PB = PAGE_BYTES_INT8;  // sections at 0, 32768, 36864, 38912
@@ -1321,10 +1354,12 @@ cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, c
   args.part_o = part_o;
   args.part_lse = part_lse;
   args.err = err;
-  args.B = B;
+  args.B = Bv;
   args.max_pages = max_pages;
   args.num_pages = num_pages;
   args.scale_log2 = scale * 1.4426950408889634f;
+  args.qs = qs;
+  args.q_rows = q_rows;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(workers, s, attr);
   auto go = [&](auto kernel, size_t smem) -> cudaError_t {

@@ -167,10 +167,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   return r;
 }
-// out[b][h] (and o_lat[b][h] when given) of one row of n > 0 tokens, exactly;
-// every thread of the CTA calls it (NT threads); scratch: 1,120 + NT floats of shared memory
+// One (row, head) over the first n > 0 tokens of page-table row pb, exactly:
+// qrow is its 576-wide query, w_uv its head's W_UV [128][512]; writes out[128]
+// (bf16) and, when given, o_lat[512].  Every thread of the CTA calls it (NT
+// threads); scratch: 1,120 + NT floats of shared memory.
 template <int NT>
-__device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, int n, const uint16_t* W_UV,
+__device__ __noinline__ void exact_head(const FixCtx fx, int pb, int n, const uint16_t* qrow, const uint16_t* w_uv,
                                         uint16_t* out, float* o_lat, float* scratch, int* err) {
   constexpr int DPT = (DC + NT - 1) / NT;  // latent dims per thread
   const int tid = threadIdx.x;
@@ -178,7 +180,6 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
   float* pw = q + DK;          // [NT] weights of the chunk's tokens
   float* red = pw + NT;        // [32]
   float* ol = red + 32;        // [512]
-  const uint16_t* qrow = fx.q_cat + ((size_t)b * H + h) * DK;
   for (int i = tid; i < DK; i += NT) q[i] = __uint_as_float((uint32_t)qrow[i] << 16);
   __syncthreads();
   float acc[DPT];
@@ -189,7 +190,7 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
     const int t = t0 + tid;
     float sc = -INFINITY;
     if (t < n) {
-      const uint8_t* pg = fix_page(fx, b, t / PAGE, err);
+      const uint8_t* pg = fix_page(fx, pb, t / PAGE, err);
       float dot = 0.f;
       for (int u = 0; u < DK / 8; ++u) {
         float f[8];
@@ -213,7 +214,7 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
         const uint8_t* pg = nullptr;
         for (int j = 0; j < cnt; ++j) {
           const int tj = t0 + j;
-          if (j == 0 || tj % PAGE == 0) pg = fix_page(fx, b, tj / PAGE, err);
+          if (j == 0 || tj % PAGE == 0) pg = fix_page(fx, pb, tj / PAGE, err);
           a = fmaf(pw[j], fix_latent(fx.fmt, pg, tj % PAGE, d), a);
         }
         acc[k] = a;
@@ -228,12 +229,12 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
     const int d = tid + k * NT;
     if (d < DC) {
       ol[d] = acc[k] * inv;
-      if (o_lat != nullptr) o_lat[((size_t)b * H + h) * DC + d] = acc[k] * inv;
+      if (o_lat != nullptr) o_lat[d] = acc[k] * inv;
     }
   }
   __syncthreads();
   for (int j = tid; j < DV; j += NT) {
-    const uint4* w = reinterpret_cast<const uint4*>(W_UV + ((size_t)h * DV + j) * DC);
+    const uint4* w = reinterpret_cast<const uint4*>(w_uv + (size_t)j * DC);
     float o = 0.f;
     for (int c8 = 0; c8 < DC / 8; ++c8) {
       const uint4 v = w[c8];
@@ -244,7 +245,7 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
       o = fmaf(bf16lo(v.w), x[6], o); o = fmaf(bf16hi(v.w), x[7], o);
     }
     const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-    out[((size_t)b * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
+    out[j] = *reinterpret_cast<const uint16_t*>(&ob);
   }
   __syncthreads();  // scratch reuse by the next row
 }
@@ -252,7 +253,7 @@ __device__ __noinline__ void exact_head(const FixCtx fx, int b, int h, int H, in
 template <int RB>
 __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     combine_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
-                   const uint16_t* __restrict__ W_UV, int H, int B,
+                   const uint16_t* __restrict__ W_UV, int H, int B, QSpec qs,
                    const int* __restrict__ plan, const float* __restrict__ part_lse, uint16_t* __restrict__ out,
                    float* __restrict__ o_lat, int* err) {
   using L = CombLayout<RB>;
@@ -271,9 +272,18 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 12);
   float* wgt = reinterpret_cast<float*>(sm + L::OFF_WGT);
 
-  const int h = blockIdx.x, b0 = blockIdx.y * RB;
+  const int h = blockIdx.x, b0 = blockIdx.y * RB;  // h: head of the partials (a virtual head)
+  const int hr = h % qs.Hr;                        // its real head: the W_UV it applies
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool loader = warp == NW;
+  // output row ((row, token) * heads + head) of plan row bv for this head; -1
+  // for padding (one query token per row: bv * heads + head, no division)
+  const bool single = qs.NG == 1 && qs.T == 1;
+  auto out_row = [&](int bv) -> long long {
+    if (single) return (long long)bv * qs.Hr + hr;
+    const int t = qs.token(bv, h);
+    return t < qs.T ? ((long long)(bv / qs.NG) * qs.T + t) * qs.Hr + hr : -1;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < WST; ++s) {
@@ -304,10 +314,10 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     // W_UV is a weight: its first tiles load while the attention step finishes
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_p);
-    prefetch_l2_bulk(W_UV + (size_t)h * DV * DC, DV * DC * 2);  // W_UV[h] into L2 for the later tiles
+    prefetch_l2_bulk(W_UV + (size_t)hr * DV * DC, DV * DC * 2);  // W_UV[hr] into L2 for the later tiles
     for (int kc = 0; kc < WST; ++kc) {
       mbar_arrive_expect_tx(&w_full[kc], W_TILE);
-      tma_load_3d(sm + L::OFF_W + kc * W_TILE, &tm_w, KC * kc, 0, h, &w_full[kc]);
+      tma_load_3d(sm + L::OFF_W + kc * W_TILE, &tm_w, KC * kc, 0, hr, &w_full[kc]);
     }
   }
   grid_dep_wait();  // the partials and their log-sum-exps
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
         const int st = kc % WST;
         if (!cwait(&w_empty[st], ((kc / WST) & 1) ^ 1, abort, err, 0)) break;
         mbar_arrive_expect_tx(&w_full[st], W_TILE);
-        tma_load_3d(sm + L::OFF_W + st * W_TILE, &tm_w, KC * kc, 0, h, &w_full[st]);
+        tma_load_3d(sm + L::OFF_W + st * W_TILE, &tm_w, KC * kc, 0, hr, &w_full[st]);
       }
       if (*abort)  // let copies in flight land before the CTA exits
         for (int k = max(0, wi - WST); k < wi; ++k) (void)mbar_wait(&w_full[k % WST], (k / WST) & 1);
@@ -356,6 +366,7 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     // ------------------------------------------------------------ merge warps
     const int r = tid >> 3, u = tid & 7;  // row of the group, 8-dim unit of the chunk
     const int b = b0 + r;
+    const long long orow = b < B ? out_row(b) : -1;
     // ---- the row's segments [rs.x, rs.y] (segment w + b of row b; empty when
     // x > y) and their softmax weights e^{LSE_s - LSE} into wgt, the row's
     // 8 threads sharing the segments (a worker without tiles left no partial:
@@ -415,8 +426,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
         if (lane == 0) mbar_arrive(&p_empty[st]);
       }
       if (!ok) break;
-      if (o_lat != nullptr && b < B)
-        st_global_v8(o_lat + ((size_t)b * H + h) * DC + KC * kc + 8 * u, acc[0], acc[1], acc[2], acc[3], acc[4],
+      if (o_lat != nullptr && orow >= 0)
+        st_global_v8(o_lat + orow * DC + KC * kc + 8 * u, acc[0], acc[1], acc[2], acc[3], acc[4],
                      acc[5], acc[6], acc[7]);
       // o_lat = hi + lo, both bf16, into the operand tiles of this chunk
       const int bs = kc % BST;
@@ -472,9 +483,10 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int bb = b0 + 16 * cg + k;
-        if (bb < B) {
+        const long long ob = bb < B ? out_row(bb) : -1;
+        if (ob >= 0) {
           const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[k]));
-          out[((size_t)bb * H + h) * DV + 32 * q + lane] = *reinterpret_cast<const uint16_t*>(&o);
+          out[ob * DV + 32 * q + lane] = *reinterpret_cast<const uint16_t*>(&o);
         }
       }
     }
@@ -491,61 +503,72 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   }
 }
 
-// The exact recompute as its own kernel, after the merge: one CTA per (head,
-// group of 32 rows) reads the group's flags and leaves at once when none is set
-// (the common case costs one launch of the decode chain); otherwise it
-// overwrites the flagged rows' outputs (and o_lat) with the exact values.
+// The exact recompute as its own kernel, after the merge: one CTA per (head of
+// the partials, group of 32 plan rows) reads the group's flags and leaves at
+// once when none is set (the common case costs one launch of the decode
+// chain); otherwise it overwrites the flagged rows' outputs (and o_lat) with
+// the exact values, each virtual head over its own causal view.
 template <int NT>
-__global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, int B, const int* plan, uint16_t* out,
-                                                 float* o_lat, int* err) {
+__global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, int B, QSpec qs, const int* plan,
+                                                 uint16_t* out, float* o_lat, int* err) {
   __shared__ float scratch[DK + NT + 32 + DC];
   grid_dep_wait();
   grid_dep_launch();
-  const int h = blockIdx.x, b0 = blockIdx.y * 32;
+  const int h = blockIdx.x, b0 = blockIdx.y * 32, hr = h % qs.Hr;
   const int* fixf = plan + plan_off_fix(B);
   const int f = (threadIdx.x < 32 && b0 + (int)threadIdx.x < B) ? fixf[b0 + threadIdx.x] : 0;
   if (!__syncthreads_or(f)) return;
   const FixCtx fx = *reinterpret_cast<const FixCtx*>(plan + PLAN_CTX);
   const int* seq_c = plan + plan_off_seq(B);
-  for (int r = 0; r < 32 && b0 + r < B; ++r)
-    if (fixf[b0 + r]) exact_head<NT>(fx, b0 + r, h, H, seq_c[b0 + r], W_UV, out, o_lat, scratch, err);
+  for (int r = 0; r < 32 && b0 + r < B; ++r) {
+    const int bv = b0 + r;
+    const int t = qs.token(bv, h);
+    if (!fixf[bv] || t >= qs.T) continue;  // uniform over the CTA
+    const int n = seq_c[bv] - qs.shift(bv, h);
+    if (n <= 0) continue;
+    const long long orow = ((long long)(bv / qs.NG) * qs.T + t) * qs.Hr + hr;
+    exact_head<NT>(fx, bv / qs.NG, n, fx.q_cat + (qs.qrow(bv) + h) * DK, W_UV + (size_t)hr * DV * DC, out + orow * DV,
+                   o_lat != nullptr ? o_lat + orow * DC : nullptr, scratch, err);
+  }
 }
 
 template <int RB>
-cudaError_t launch_rb(const CUtensorMap& tm_w, const CUtensorMap& tm_p, const void* W_UV, int H, int B, const int* plan,
-                      const float* part_lse, void* out, float* o_lat, int* err, int max_workers, cudaStream_t s) {
+cudaError_t launch_rb(const CUtensorMap& tm_w, const CUtensorMap& tm_p, const void* W_UV, int H, int B, const QSpec& qs,
+                      const int* plan, const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
+                      cudaStream_t s) {
   using L = CombLayout<RB>;
   const size_t smem = L::bytes(max_workers);
   cudaError_t e = cudaFuncSetAttribute(combine_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel<RB>, dim3(H, (B + RB - 1) / RB), dim3(L::THREADS), smem, s, tm_w, tm_p,
-                    static_cast<const uint16_t*>(W_UV), H, B, plan, part_lse, static_cast<uint16_t*>(out), o_lat, err);
+                    static_cast<const uint16_t*>(W_UV), H, B, qs, plan, part_lse, static_cast<uint16_t*>(out), o_lat,
+                    err);
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const uint16_t* part_o,
+cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s) {
-  if (B == 0) return cudaSuccess;
-  CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, H heads), tiles of 64 x 128, 128B swizzle
-  if (!encode_3d(&tm_w, W_UV, DC, DV, H, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (Bv == 0) return cudaSuccess;
+  CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
+  if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // partials (bf16): (512 latent, H heads, segments), boxes of 64 dims x 1 head x 128 segments
-  const uint64_t segs = (uint64_t)max_workers + B;
-  if (!encode_3d_box(&tm_p, part_o, DC, H, segs, DC * 2, (uint64_t)H * DC * 2, KC, 1, SEGB,
+  // partials (bf16): (512 latent, Hv heads, segments), boxes of 64 dims x 1 head x 128 segments
+  const uint64_t segs = (uint64_t)max_workers + Bv;
+  if (!encode_3d_box(&tm_p, part_o, DC, Hv, segs, DC * 2, (uint64_t)Hv * DC * 2, KC, 1, SEGB,
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
   const int sms = device_sm_count();
   cudaError_t e;
-  if ((long long)H * ((B + 31) / 32) >= sms)
-    e = launch_rb<32>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+  if ((long long)Hv * ((Bv + 31) / 32) >= sms)
+    e = launch_rb<32>(tm_w, tm_p, W_UV, Hv, Bv, qs, plan, part_lse, out, o_lat, err, max_workers, s);
   else
-    e = launch_rb<16>(tm_w, tm_p, W_UV, H, B, plan, part_lse, out, o_lat, err, max_workers, s);
+    e = launch_rb<16>(tm_w, tm_p, W_UV, Hv, Bv, qs, plan, part_lse, out, o_lat, err, max_workers, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(fix_kernel<256>, dim3(H, (B + 31) / 32), dim3(256), 0, s, static_cast<const uint16_t*>(W_UV), H, B,
-                    plan, static_cast<uint16_t*>(out), o_lat, err);
+  return launch_pdl(fix_kernel<256>, dim3(Hv, (Bv + 31) / 32), dim3(256), 0, s, static_cast<const uint16_t*>(W_UV), Hv,
+                    Bv, qs, plan, static_cast<uint16_t*>(out), o_lat, err);
 }
 
 }  // namespace mla

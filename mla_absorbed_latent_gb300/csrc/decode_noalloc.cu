@@ -99,17 +99,17 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
 
-  if (launch_plan(seqlens, B, max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_plan(seqlens, B, qspec_single(H), max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream) != cudaSuccess) return MLA_ERR_CUDA;
   cudaError_t e;
   if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   else
     e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine(W_UV, H, B, plan, part_o, part_lse, out, nullptr, err, workers, stream) != cudaSuccess)
+  if (launch_combine(W_UV, H, B, qspec_single(H), plan, part_o, part_lse, out, nullptr, err, workers, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

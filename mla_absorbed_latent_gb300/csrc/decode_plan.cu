@@ -16,8 +16,10 @@ namespace {
 
 constexpr int SMEM_ROWS = 8192;  // rows whose tile prefix the worker search reads from shared memory
 
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seqlens, int B, int max_pages,
-                                                     int workers, int* __restrict__ plan, int* err) {
+// B: plan rows (virtual rows); their lengths come from the real rows' lengths
+// and the query layout qs (one query token per row: the lengths themselves)
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seqlens, int B, QSpec qs,
+                                                     int max_pages, int workers, int* __restrict__ plan, int* err) {
   __shared__ int warp_sums[32];
   __shared__ int s_prefix[SMEM_ROWS + 1];
   const bool in_smem = B <= SMEM_ROWS;
@@ -33,10 +35,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
   int local = 0, first_n = 0;  // first_n: the clamped length of row lo (one row per thread when B <= 1024)
   for (int b = lo; b < hi; ++b) {
-    long long n = seqlens[b];
+    const int br = b / qs.NG;  // the real row
+    long long n = seqlens[br];
     if (n < 0 || n > cap) {
-      raise_error(err, MLA_ERR_BOUNDS, b);
+      raise_error(err, MLA_ERR_BOUNDS, br);
       n = n < 0 ? 0 : cap;
+    }
+    if (qs.T > 1) {
+      // the row's last T tokens are its queries; this virtual row's view ends
+      // with its last query token's
+      if (n < qs.T) raise_error(err, MLA_ERR_BOUNDS, br);
+      n -= qs.T - 1 - qs.last_token(b);
+      if (n < 0) n = 0;
     }
     seq_c[b] = (int)n;
     fix[b] = 0;
@@ -96,9 +106,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,
-                        cudaStream_t s) {
-  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, seqlens, B, max_pages, workers, plan, err);
+cudaError_t launch_plan(const int32_t* seqlens, int B, const QSpec& qs, int max_pages, int workers, int* plan,
+                        int* err, cudaStream_t s) {
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, seqlens, B * qs.NG, qs, max_pages, workers, plan, err);
 }
 
 }  // namespace mla

@@ -208,7 +208,7 @@ int decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, in
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
   int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + L.plan);
-  return status_of(launch_plan(seqlens, B, max_pages, req > 0 ? req : workers, plan, err, stream));
+  return status_of(launch_plan(seqlens, B, qspec_single(H), max_pages, req > 0 ? req : workers, plan, err, stream));
 }
 }  // namespace
 
@@ -258,7 +258,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
   cudaError_t e;
   if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   else
     e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
@@ -279,7 +279,7 @@ int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t w
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return status_of(launch_combine(W_UV, H, B, reinterpret_cast<const int*>(ws + L.plan),
+  return status_of(launch_combine(W_UV, H, B, qspec_single(H), reinterpret_cast<const int*>(ws + L.plan),
                                   reinterpret_cast<const uint16_t*>(ws + L.part_o),
                                   reinterpret_cast<const float*>(ws + L.part_lse), out, o_lat_out, err,
                                   L.max_segments - B, stream));
@@ -305,6 +305,74 @@ int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const voi
   st = mla_decode_attend(H, cache, page_table, max_pages, seqlens, B, scale, workspace, workspace_bytes, stream);
   if (st != MLA_OK) return st;
   return mla_decode_combine(W_UV, H, B, workspace, workspace_bytes, out, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace {
+constexpr int MAX_Q_LEN = 65536;
+// T query tokens per row for H heads on the tcgen05 kernel's 128 MMA rows
+QSpec qspec_multi(int H, int T) {
+  const int G = 128 / H;
+  return QSpec{T, G, (T + G - 1) / G, H};
+}
+WsLayout ws_layout_multi(int B, int H, int T, int workers) {
+  const QSpec qs = qspec_multi(H, T);
+  return ws_layout_q(B * qs.NG, 128, (long long)B * T * H, workers);
+}
+bool multi_ok(int B, int H, int T) {
+  if (!heads_ok(H) || T < 1 || T > MAX_Q_LEN || B < 0) return false;
+  const long long rows = (long long)B * T * H;  // flat query rows: TMA coordinates
+  return rows <= 2147483647LL - 256 && (long long)B * qspec_multi(H, T).NG <= 2147483647LL / 4;
+}
+}  // namespace
+
+extern "C" {
+
+size_t mla_decode_q_workspace_bytes(int B, int H, int T) {
+  if (!multi_ok(B, H, T)) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  return ws_layout_multi(B, H, T, attend_tc_workers(sms)).total;
+}
+
+int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const void* W_UV, int H, int T,
+                 const mla_cache_t* cache, const int32_t* page_table, int max_pages, const int32_t* seqlens, int B,
+                 float scale, void* workspace, size_t workspace_bytes, void* out, float* o_lat_out,
+                 cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (cache == nullptr || B < 0 || max_pages <= 0 || T < 1) return MLA_ERR_INVALID;
+  if (!multi_ok(B, H, T)) return MLA_ERR_UNSUPPORTED;
+  if (!fmt_ok(cache->fmt)) return MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache)) return MLA_ERR_INVALID;
+  const int sms = num_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const int workers = attend_tc_workers(sms);
+  const WsLayout L = ws_layout_multi(B, H, T, workers);
+  if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !W_UK || !W_UV || !out || !page_table || !seqlens) return MLA_ERR_INVALID;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(W_UK, 16) || !aligned(W_UV, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(seqlens, 4) || (o_lat_out && !aligned(o_lat_out, 16)))
+    return MLA_ERR_INVALID;
+  if (!(scale > 0.f) || scale == INFINITY) return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  const QSpec qs = qspec_multi(H, T);
+  const int Bv = B * qs.NG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* plan = reinterpret_cast<int*>(ws + L.plan);
+  uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  cudaError_t e = launch_plan(seqlens, B, qs, max_pages, workers, plan, err, stream);
+  if (e == cudaSuccess) e = launch_q_absorb(q_nope, q_pe, W_UK, H, B * T, ws + L.q_cat, stream);
+  if (e == cudaSuccess)
+    e = launch_attend_tc(ws + L.q_cat, qs, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, Bv,
+                         scale, plan, workers, part_o, part_lse, err, stream);
+  if (e == cudaSuccess)
+    e = launch_combine(W_UV, 128, Bv, qs, plan, part_o, part_lse, out, o_lat_out, err, L.max_segments - Bv, stream);
+  return status_of(e);
 }
 
 int mla_get_device_status(cudaStream_t stream, int* info) {

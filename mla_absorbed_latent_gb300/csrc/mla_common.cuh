@@ -52,41 +52,76 @@ struct WsLayout {
 //   then B exact-recompute flags (zeroed by the plan, set by the attend kernel for a row
 //        whose weights it could not form exactly; the combine kernel recomputes it),
 //   then W first rows, one per worker's tile range.
-constexpr int PLAN_HDR = 16;
+constexpr int PLAN_HDR = 20;
 constexpr int PLAN_CTX = 4;  // int offset of the FixCtx record (byte offset 16: 8-byte aligned)
 __host__ __device__ constexpr int plan_off_seq(int B) { return PLAN_HDR + B + 1; }
 __host__ __device__ constexpr int plan_off_fix(int B) { return PLAN_HDR + 2 * B + 1; }
 __host__ __device__ constexpr int plan_off_wrow(int B) { return PLAN_HDR + 3 * B + 1; }
 __host__ __device__ constexpr long long plan_ints(int B, int W) { return (long long)PLAN_HDR + 3LL * B + 1 + W; }
 
+// Several query tokens per row ("手搓 MLA" §四 with its query-token axis t;
+// causal as in "DeepSeek MLA 吸收式缓存" §3.4's prefill and incremental decode):
+// row b holds n_b cached tokens whose last T are its queries, and query t sees
+// tokens 0 .. n_b - T + t.  The attend kernel's MMA has 128 rows, so G = 128 / Hr
+// query tokens of a row share one pass over its cache (a "virtual row" of G
+// tokens x Hr heads = 128 virtual heads, virtual head v = token (v / Hr) of the
+// group, head v % Hr); NG = ceil(T / G) virtual rows per row.  A virtual row's
+// length is that of its last token's view; each virtual head sees a prefix of
+// it (shorter by the tokens after its own query), and virtual heads past T are
+// padding (they see nothing).  One query token per row is T = G = NG = 1 with
+// Hr = 128, or the H = 16 CUDA-core path.
+struct QSpec {
+  int T, G, NG, Hr;
+  // flat q_cat row ([B][T][Hr][576] bf16) of virtual row r's first virtual head
+  __host__ __device__ __forceinline__ long long qrow(int r) const {
+    return ((long long)(r / NG) * T + (long long)(r % NG) * G) * Hr;
+  }
+  // query token (0 .. T-1, or >= T for padding) of virtual head v of virtual row r
+  __host__ __device__ __forceinline__ int token(int r, int v) const { return (r % NG) * G + v / Hr; }
+  // the last query token of virtual row r
+  __host__ __device__ __forceinline__ int last_token(int r) const {
+    const int e = (r % NG) * G + G;
+    return (e < T ? e : T) - 1;
+  }
+  // tokens of virtual row r's view that virtual head v does not see (huge for padding)
+  __host__ __device__ __forceinline__ int shift(int r, int v) const {
+    const int t = token(r, v), tl = last_token(r);
+    return t <= tl ? tl - t : (1 << 30);
+  }
+};
+__host__ __device__ inline QSpec qspec_single(int H) { return QSpec{1, 1, 1, H}; }
+
 // What the combine kernel needs to recompute a flagged row from the cache: the
-// attend kernel's cache, page table, query operand and scale.
+// attend kernel's cache, page table, query operand, scale and query layout.
 struct FixCtx {
   const uint8_t* pages;
   const int32_t* page_table;
-  const uint16_t* q_cat;  // [B][H][576] bf16: q_lat then q_pe
+  const uint16_t* q_cat;  // flat rows of 576 bf16: q_lat then q_pe
   int max_pages, num_pages, fmt;
   float scale_log2;       // softmax scale times log2(e)
+  QSpec qs;
 };
 static_assert(sizeof(FixCtx) <= (PLAN_HDR - PLAN_CTX) * 4, "FixCtx fits the plan header");
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int B, int H, int max_workers) {
+// Bv plan rows (virtual rows), Hv heads of the partials, q_rows flat query rows
+inline WsLayout ws_layout_q(int Bv, int Hv, long long q_rows, int max_workers) {
   WsLayout L;
   size_t off = 0;
   L.q_cat = off;
-  off = align_up(off + (size_t)B * H * DK * 2, 1024);
+  off = align_up(off + (size_t)q_rows * DK * 2, 1024);
   L.plan = off;
-  off = align_up(off + (size_t)plan_ints(B, max_workers) * 4, 1024);
-  L.max_segments = max_workers + B;
+  off = align_up(off + (size_t)plan_ints(Bv, max_workers) * 4, 1024);
+  L.max_segments = max_workers + Bv;
   L.part_o = off;
-  off = align_up(off + (size_t)L.max_segments * H * DC * 2, 1024);  // bf16 partials
+  off = align_up(off + (size_t)L.max_segments * Hv * DC * 2, 1024);  // bf16 partials
   L.part_lse = off;
-  off = align_up(off + (size_t)L.max_segments * H * 4, 1024);
+  off = align_up(off + (size_t)L.max_segments * Hv * 4, 1024);
   L.total = off;
   return L;
 }
+inline WsLayout ws_layout(int B, int H, int max_workers) { return ws_layout_q(B, H, (long long)B * H, max_workers); }
 
 // Largest worker count <= want whose decode workspace for B rows and H heads
 // fits in cap bytes; 0 when even one worker does not fit.
@@ -212,14 +247,16 @@ int project_splits(long long ntok, int hidden, int sms, int requested);
 size_t project_workspace_bytes(long long ntok, int ksplit);
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
                             cudaStream_t s);
-cudaError_t launch_plan(const int32_t* seqlens, int B, int max_pages, int workers, int* plan, int* err,
-                        cudaStream_t s);
+// B real rows, query layout qs (B * qs.NG plan rows)
+cudaError_t launch_plan(const int32_t* seqlens, int B, const QSpec& qs, int max_pages, int workers, int* plan,
+                        int* err, cudaStream_t s);
 cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_cc_workers(int num_sms);
-cudaError_t launch_attend_tc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
-                             const int32_t* page_table, int max_pages, int B, float scale, int* plan,
+// Bv virtual rows of the query layout qs (q_cat: Bv / qs.NG * qs.T * qs.Hr flat rows)
+cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int num_pages, const void* pages,
+                             const int32_t* page_table, int max_pages, int Bv, float scale, int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
 // a CTA pair whose bounded wait runs out on purpose (see mla_wait_selftest)
@@ -229,8 +266,9 @@ int* device_error_word();            // this device's error word, nullptr on fai
 int device_sm_count();               // SMs of the current device, 0 on failure
 int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
 
-// max_workers: the partial buffer holds max_workers + B segment slots
-cudaError_t launch_combine(const void* W_UV, int H, int B, const int* plan, const uint16_t* part_o,
+// Hv heads of the partials (virtual heads), Bv plan rows, query layout qs;
+// max_workers: the partial buffer holds max_workers + Bv segment slots
+cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s);
 

@@ -16,6 +16,7 @@ from .workloads import (  # noqa: F401
     gen_hidden,
     gen_project_weights,
     gen_queries,
+    gen_queries_multi,
     gen_seqlens,
     gen_sequence,
     gen_weights,

@@ -140,6 +140,19 @@ def gen_queries(H: int, seqlens, seed: int):
     return f32_to_bf16_bits(q_nope), f32_to_bf16_bits(q_pe)
 
 
+def gen_queries_multi(H: int, T: int, seqlens, seed: int):
+    """T query tokens per row: q_nope [B,T,H,128] and q_pe [B,T,H,64] rotated at
+    their positions n_b - T + t (the row's last T tokens), bf16 bits."""
+    seqlens = np.asarray(seqlens)
+    B = len(seqlens)
+    r = _rng(seed, _S_QUERY, T)
+    q_nope = r.standard_normal((B, T, H, D_NOPE), dtype=np.float32)
+    q_pe = r.standard_normal((B, T, H, D_R), dtype=np.float32)
+    pos = (seqlens.astype(np.int64)[:, None] - T + np.arange(T)[None, :]).clip(min=0)
+    q_pe = rope_interleaved(q_pe, pos[:, :, None] * np.ones((1, 1, H))).astype(np.float32)
+    return f32_to_bf16_bits(q_nope), f32_to_bf16_bits(q_pe)
+
+
 def _outlier_channels(seed: int) -> np.ndarray:
     return np.sort(_rng(seed, _S_OUTLIER).choice(D_C, size=max(1, D_C // 100), replace=False))
 
