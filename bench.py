@@ -49,6 +49,8 @@ DESCR = {
     "v3_ragged": "DeepSeek-V3 shape ragged decode: H=128, B=128, lognormal seqlens (median 4096, clip 256..32768), "
                  "paged",
     "v3_quant": "DeepSeek-V3 shape decode over a quantized cache: H=128, B=64, seqlen 32768, paged",
+    "v2lite_mtp": "V2-Lite shape, 8 causal query tokens per row: H=16, B=32, seqlen 4096, contiguous bf16 cache",
+    "v3_mtp": "DeepSeek-V3 shape, 2 causal query tokens per row: H=128, B=64, seqlen 8192, paged bf16 cache",
 }
 
 
@@ -174,6 +176,29 @@ def oracle_time(prob, budget_s: float, max_rows: int | None = None, outputs: dic
     return done_bytes, spent, rows
 
 
+def oracle_time_q(prob, T, qn, qp, budget_s: float, max_rows: int | None = None, outputs: dict | None = None):
+    """oracle_time for T causal query tokens per row (absorbed_attend_causal);
+    outputs[b] = out [T, H, 128]."""
+    import oracle as O
+    Wuk, Wuv = O.split_wkv_b(synth.bf16_bits_to_f32(prob.wkv), prob.H)
+    done_bytes, spent, rows = 0, 0.0, 0
+    bpt = BYTES_PER_TOKEN[prob.fmt]
+    for b in range(prob.B):
+        c, p = prob.sequence(b)
+        C, P = O.dequantized_tokens(prob.fmt, synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p))
+        t0 = time.perf_counter()
+        out, _ = O.absorbed_attend_causal(synth.bf16_bits_to_f32(qn[b]), synth.bf16_bits_to_f32(qp[b]), C, P, Wuk, Wuv,
+                                          prob.scale)
+        spent += time.perf_counter() - t0
+        if outputs is not None:
+            outputs[b] = out
+        done_bytes += int(prob.seqlens[b]) * bpt
+        rows += 1
+        if spent >= budget_s or (max_rows is not None and rows >= max_rows):
+            break
+    return done_bytes, spent, rows
+
+
 def parity_stats(got: dict, ref: dict):
     """Agreement of the timed decode's output rows with the oracle's rows (both
     {row: [H, 128] array}): largest absolute error, worst per-head relative RMS
@@ -233,12 +258,18 @@ def run_reference(args, wl, fmt):
         return 0
     from synth.device import problem_from_workload
     prob = problem_from_workload(wl, fmt)
+    T = q_len_of(args, wl)
+    if T is not None:
+        qn, qp = synth.gen_queries_multi(prob.H, T, prob.seqlens, prob.seed)
+        one = lambda: oracle_time_q(prob, T, qn, qp, 0.0, max_rows=1)  # noqa: E731
+    else:
+        one = lambda: oracle_time(prob, 0.0, max_rows=1)  # noqa: E731
     # warm-up: one row, untimed
     for _ in range(args.warmup):
-        oracle_time(prob, 0.0, max_rows=1)
+        one()
     total_bytes, total_s = 0, 0.0
     for _ in range(args.steps):
-        nbytes, s, _rows = oracle_time(prob, 0.0, max_rows=1)   # one row per step
+        nbytes, s, _rows = one()   # one row per step
         total_bytes += nbytes
         total_s += s
     gbs = total_bytes / total_s / 1e9
@@ -249,10 +280,158 @@ def run_reference(args, wl, fmt):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {DESCR.get(wl.name, '')}", "cache_fmt": fmt,
                    "sample": "one batch row (all heads, full sequence) per step"},
-        "queries_per_s": gbs * 1e9 / bpq,
+        "queries_per_s": gbs * 1e9 / bpq * (T or 1),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
                          "sample": f"{args.steps} rows of {wl.name}, one per step, fp64 numpy absorbed oracle"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+SCRUB_BELOW = 512 * 2 ** 20   # cache streams under this are timed with an L2 scrub between steps
+SCRUB_BYTES = 256 * 2 ** 20   # > the 129 MB L2
+
+
+def timed_steps(step, steps, stream, scrub_buf=None):
+    """Mean ms of `steps` steps on `stream`: back to back between two events, or,
+    with scrub_buf, each step alone between its own events after writing
+    scrub_buf (a buffer larger than L2), so no step finds the cache in L2."""
+    import torch
+    if scrub_buf is None:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for k in range(steps):
+        scrub_buf.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+
+
+def l2_note(cache_bytes, scrub):
+    if scrub:
+        return (f"{SCRUB_BYTES >> 20} MB L2 scrub before every timed step (cache stream {cache_bytes / 1e6:.0f} MB, "
+                f"near the 129 MB L2); each step timed alone")
+    return "inputs larger than L2 (cache stream per step > 129 MB), no flush"
+
+
+def q_len_of(args, wl):
+    """Query tokens per row when the step runs through mla_decode_q (None: the
+    single-query chain)."""
+    if args.q_len is not None:
+        return args.q_len
+    return wl.q_len if wl.q_len > 1 else None
+
+
+def run_ours_q(args, wl, fmt, T):
+    """One step = one mla_decode_q call: T causal query tokens per row."""
+    import torch
+    torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+    import mla_absorbed_latent_gb300 as mla
+    from synth.device import DeviceDecode, bits_to_device, problem_from_workload
+    prob = problem_from_workload(wl, fmt)
+    dev = DeviceDecode(prob)
+    H, B = prob.H, prob.B
+    qn, qp = synth.gen_queries_multi(H, T, prob.seqlens, prob.seed)
+    d_qn, d_qp = bits_to_device(qn), bits_to_device(qp)
+    ws_bytes = mla.mla_decode_q_workspace_bytes(B, H, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    cache_bytes = int(np.sum(prob.seqlens)) * BYTES_PER_TOKEN[fmt]
+
+    def step():
+        mla.mla_decode_q(d_qn, d_qp, dev.W_UK, dev.W_UV, H, T, dev.cache, dev.page_table, prob.max_pages,
+                         dev.seqlens, B, prob.scale, ws, ws_bytes, out, None, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
+    scrub = cache_bytes < SCRUB_BELOW
+    scrub_buf = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device="cuda") if scrub else None
+    clocks = ClockSampler(torch.cuda.current_device())
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ms_step = timed_steps(step, args.steps, stream, scrub_buf)
+    clock_info = clocks.stop()
+    # each call alone (events between the calls; scrubbed when the step is)
+    call_ms = timed_steps(step, args.steps, stream, scrub_buf) if not scrub else ms_step
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after timing: {mla.mla_status_string(st)} ({info})")
+
+    h_qn, h_qp = d_qn.cpu().pin_memory(), d_qp.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qp.copy_(h_qp, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    cpu, parity = None, None
+    if not args.no_cpu_baseline:
+        ref_rows = {}
+        nbytes, secs, rows = oracle_time_q(prob, T, qn, qp, args.cpu_seconds, outputs=ref_rows)
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{rows} of {B} rows of {wl.name} ({T} queries x {H} heads, full sequences), fp64 numpy "
+                         f"causal absorbed oracle, {secs:.1f} s"}
+        try:
+            got = synth.bf16_bits_to_f32(h_out.view(torch.int16).numpy().view(np.uint16))
+            parity = parity_stats({b: got[b] for b in ref_rows}, ref_rows)
+        except Exception as exc:
+            parity = {"error": repr(exc), "within_tolerance": False}
+
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    flops_tok = 2 * H * T * (576 + 512)  # useful work: T queries of H heads per cached token
+    ai = flops_tok / BYTES_PER_TOKEN[fmt]
+    ridge = tf_burst * 1e12 / (hbm * 1e9)
+    gbs = cache_bytes / (call_ms * 1e-3) / 1e9
+    tflops = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (call_ms * 1e-3) / 1e12
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "peak_source": peak_src, "tensor_tflops": tflops, "arith_intensity": ai}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s", "frac": tflops / tf_burst,
+                "traffic": None, "peak_source": peak_src + " (bf16, burst)", "hbm_gbs": gbs, "arith_intensity": ai}
+    roof["timed"] = "the whole mla_decode_q call (plan, q-absorb, attend, merge): a lower bound of the attend kernel's"
+    G = 128 // H
+    line = {
+        "metric": METRIC, "value": cache_bytes / (ms_step * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {DESCR.get(wl.name, '')}", "H": H, "B": B, "q_len": T,
+                   "seqlen": int(prob.seqlens.max()), "cache_fmt": fmt, "cache_bytes_per_step": cache_bytes,
+                   "l2": l2_note(cache_bytes, scrub),
+                   "passes_over_cache": -(-T // G),
+                   "attend_kernel": f"tcgen05, {min(T, G)} of {G} token lanes per pass in use"},
+        "queries_per_s": B * T / (ms_step * 1e-3),
+        "roofline": roof,
+        "call_ms": call_ms,
+        "cpu_baseline": cpu,
+        "parity": parity,
+        "e2e": {"value": cache_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h_qn.numel() * 2 + h_qp.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2},
+        "gpu_launches": 5 * args.steps,  # plan, q-absorb, attend, merge, exact-recompute check
+        "clocks": clock_info,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -304,7 +483,8 @@ def run_ours(args, wl, fmt):
         raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
 
     attend_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    scrub = cache_bytes < SCRUB_BELOW
+    scrub_buf = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device="cuda") if scrub else None
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -312,16 +492,14 @@ def run_ours(args, wl, fmt):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    t0.record(stream)
-    for k in range(args.steps):
-        step()  # no events between the launches: consecutive kernels overlap their prologues
-    t1.record(stream)
-    torch.cuda.synchronize()
+    # no events between the launches of a step: consecutive kernels overlap their prologues
+    elapsed_ms = timed_steps(step, args.steps, stream, scrub_buf) * args.steps
     clock_info = clocks.stop() if clocks else None
-    elapsed_ms = t0.elapsed_time(t1)
     # per-stage times (and the attend time of the roofline) from a second run of
     # the same steps with events between the launches
     for k in range(args.steps):
+        if scrub_buf is not None:
+            scrub_buf.zero_()
         step(attend_ev[k])
     torch.cuda.synchronize()
     attend_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in attend_ev]))
@@ -406,7 +584,7 @@ def run_ours(args, wl, fmt):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {DESCR.get(wl.name, '')}", "H": H, "B": B,
                    "seqlen": int(prob.seqlens.max()), "cache_fmt": fmt, "cache_bytes_per_step": cache_bytes,
-                   "l2": "inputs larger than L2 (cache stream per step > 129 MB), no flush",
+                   "l2": l2_note(cache_bytes, scrub),
                    "parallelism": f"replicas x{world} (batch-sharded, no collective)",
                    "attend_kernel": "tcgen05" if kind == 1 else "cuda-core"},
         "pct_hbm_peak": 100.0 * value / (hbm * world),
@@ -592,6 +770,9 @@ def main(argv=None):
     ap.add_argument("--k-splits", type=int, default=0,
                     help="producer workloads: CTA pairs per 128-token tile over the hidden dimension (0 = by size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-len", type=int, default=None,
+                    help="query tokens per row through mla_decode_q (default: the workload's; 1 runs the single-"
+                         "query step of an H=16 workload on the tensor cores)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -618,6 +799,11 @@ def main(argv=None):
     fmt = args.fmt or wl.fmts[0]
     if args.impl == "reference":
         return run_reference(args, wl, fmt)
+    T = q_len_of(args, wl)
+    if T is not None:
+        if _env_int("WORLD_SIZE", 1) > 1:
+            raise SystemExit("the multi-query workloads run on one GPU")
+        return run_ours_q(args, wl, fmt, T)
     return run_ours(args, wl, fmt)
 
 

@@ -208,7 +208,7 @@ __device__ __noinline__ long long qrow_of(const QSpec qs, int r) { return qs.qro
 __device__ __noinline__ int page_row_of(const QSpec qs, int r) { return r / qs.NG; }
 __device__ __noinline__ int shift_of(const QSpec qs, int r, int v) { return qs.shift(r, v); }
 __device__ __forceinline__ long long qrow_at(const QSpec& qs, int r) {
-  return qs.NG == 1 && qs.T == 1 ? (long long)r * 128 : qrow_of(qs, r);
+  return qs.NG == 1 ? (long long)r * qs.T * qs.Hr : qrow_of(qs, r);  // one virtual row per row: r * T * Hr
 }
 __device__ __forceinline__ int page_row_at(const QSpec& qs, int r) { return qs.NG == 1 ? r : page_row_of(qs, r); }
 

@@ -277,8 +277,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool loader = warp == NW;
   // output row ((row, token) * heads + head) of plan row bv for this head; -1
-  // for padding (one query token per row: bv * heads + head, no division)
-  const bool single = qs.NG == 1 && qs.T == 1;
+  // for padding (one query token per row and pass: bv * heads + head, no division)
+  const bool single = qs.NG == 1 && qs.T == 1 && qs.G == 1;
   auto out_row = [&](int bv) -> long long {
     if (single) return (long long)bv * qs.Hr + hr;
     const int t = qs.token(bv, h);

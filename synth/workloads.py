@@ -49,6 +49,7 @@ class Workload:
     dist: str = "rmsnorm"  # "rmsnorm" or "outlier"
     fmts: tuple = ("bf16",)
     prefill: int = 0       # tokens appended before the decode token (tiny case)
+    q_len: int = 1         # query tokens per row (the row's last q_len cached tokens, causal)
 
     @property
     def scale(self) -> float:
@@ -67,6 +68,11 @@ WORKLOADS = {
     # V3 shape over a quantized cache (INT8, then INT4), latents with outlier channels
     "v3_quant": Workload("v3_quant", H=128, B=64, seqlen=32768, seed=4, dist="outlier",
                          fmts=("int8", "int4")),
+    # several query tokens per row (speculative / multi-token-prediction decode):
+    # the V2-Lite batch's cache with 8 causal queries per row, and the V3 paged
+    # cache with 2
+    "v2lite_mtp": Workload("v2lite_mtp", H=16, B=32, seqlen=4096, seed=1, paged=False, q_len=8),
+    "v3_mtp": Workload("v3_mtp", H=128, B=64, seqlen=8192, seed=2, q_len=2),
 }
 
 
