@@ -292,6 +292,29 @@ int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const v
 size_t mla_decode_q_workspace_bytes(int B, int H, int T);
 
 /*
+ * The unabsorbed ("compute-friendly") causal prefill: the same attention as
+ * mla_decode_q (T queries per row, the row's last T tokens, query t sees
+ * tokens 0 .. n_b - T + t), computed by expanding every cached latent of the
+ * rows into per-head keys and values once and running standard attention over
+ * them.  "手搓 MLA" §三 (k_nope, v = split(kv_up); k = [k_nope; k_pe]) and its
+ * closing notes (engines run this form at prefill, the absorbed one at decode);
+ * "DeepSeek MLA 吸收式缓存" §2.1 (the expand path).  Per (query, key) pair it
+ * costs 2H(192 + 128) FLOPs against the absorbed 2H(576 + 512), for a one-time
+ * 2H x 256 x 512 per cached token.
+ *   q_nope, q_pe, T, cache, page_table, max_pages, seqlens, B, scale, out : as mla_decode_q
+ *   wkv_b     : bf16 [H*256][512], the joint up-projection (rows h*256.. : k_nope, then v)
+ *   workspace : >= mla_prefill_workspace_bytes(B, H, max_pages) bytes, 256-byte
+ *               aligned: the expanded keys and values, bf16 [B][max_pages*64][H][256]
+ * bf16 pools only (MLA_ERR_UNSUPPORTED otherwise), H in {16, 128}.  Keys and
+ * values are rounded to bf16 once after fp32 accumulation; the attention
+ * accumulates in fp32.  Rows shorter than T raise MLA_ERR_BOUNDS.
+ */
+int mla_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, int T, const mla_cache_t* cache,
+                const int32_t* page_table, int max_pages, const int32_t* seqlens, int B, float scale,
+                void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream);
+size_t mla_prefill_workspace_bytes(int B, int H, int max_pages);
+
+/*
  * Decode without any allocation (no counterpart on the pages: an interface
  * addition of this library for hosts that cannot allocate device memory, e.g.
  * an engine whose custom-op interface passes only inputs and outputs, a

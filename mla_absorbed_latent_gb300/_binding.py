@@ -57,6 +57,8 @@ def _load() -> ctypes.CDLL:
         "mla_decode_noalloc": (i, [vp, vp, vp, vp, i, cp, vp, i, vp, i, f, vp, vp]),
         "mla_decode_q": (i, [vp, vp, vp, vp, i, i, cp, vp, i, vp, i, f, vp, sz, vp, vp, vp]),
         "mla_decode_q_workspace_bytes": (sz, [i, i, i]),
+        "mla_prefill": (i, [vp, vp, vp, i, i, cp, vp, i, vp, i, f, vp, sz, vp, vp]),
+        "mla_prefill_workspace_bytes": (sz, [i, i, i]),
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
         "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
@@ -144,6 +146,18 @@ def mla_decode_q(q_nope, q_pe, W_UK, W_UV, H: int, T: int, cache: mla_cache_t, p
     _check(_lib.mla_decode_q(_ptr(q_nope), _ptr(q_pe), _ptr(W_UK), _ptr(W_UV), H, T, ctypes.byref(cache),
                              _ptr(page_table), max_pages, _ptr(seqlens), B, scale, _ptr(workspace), workspace_bytes,
                              _ptr(out), _ptr(o_lat_out), _stream(stream)), "mla_decode_q")
+
+
+def mla_prefill_workspace_bytes(B: int, H: int, max_pages: int) -> int:
+    return int(_lib.mla_prefill_workspace_bytes(B, H, max_pages))
+
+
+def mla_prefill(q_nope, q_pe, wkv_b, H: int, T: int, cache: mla_cache_t, page_table, max_pages: int, seqlens, B: int,
+                scale: float, workspace, workspace_bytes: int, out, stream=None) -> None:
+    """The unabsorbed causal prefill (expanded keys and values, standard attention)."""
+    _check(_lib.mla_prefill(_ptr(q_nope), _ptr(q_pe), _ptr(wkv_b), H, T, ctypes.byref(cache), _ptr(page_table),
+                            max_pages, _ptr(seqlens), B, scale, _ptr(workspace), workspace_bytes, _ptr(out),
+                            _stream(stream)), "mla_prefill")
 
 
 def mla_decode_plan(H: int, fmt: str | int, seqlens, B: int, max_pages: int, workspace, workspace_bytes: int,

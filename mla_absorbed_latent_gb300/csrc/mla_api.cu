@@ -375,6 +375,36 @@ int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const v
   return status_of(e);
 }
 
+size_t mla_prefill_workspace_bytes(int B, int H, int max_pages) {
+  if (B < 0 || !heads_ok(H) || max_pages <= 0) return 0;
+  if ((long long)B * max_pages * PAGE > 2147483647LL - 256) return 0;  // key rows are TMA coordinates
+  return prefill_workspace_bytes(B, H, max_pages);
+}
+
+int mla_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, int T, const mla_cache_t* cache,
+                const int32_t* page_table, int max_pages, const int32_t* seqlens, int B, float scale,
+                void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (cache == nullptr || B < 0 || T < 1 || max_pages <= 0) return MLA_ERR_INVALID;
+  if (cache->fmt != MLA_FMT_BF16) return MLA_ERR_UNSUPPORTED;
+  if (!cache_ok(cache)) return MLA_ERR_INVALID;
+  if ((long long)B * T > 2147483647LL - 256 || (long long)B * max_pages * PAGE > 2147483647LL - 256)
+    return MLA_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(B, H, max_pages);
+  if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !wkv_b || !out || !page_table || !seqlens) return MLA_ERR_INVALID;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(wkv_b, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4) || !aligned(seqlens, 4))
+    return MLA_ERR_INVALID;
+  if (!(scale > 0.f) || scale == INFINITY) return MLA_ERR_INVALID;
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  return status_of(launch_prefill(q_nope, q_pe, wkv_b, H, T, cache->num_pages, cache->pages, page_table, max_pages,
+                                  seqlens, B, scale, workspace, out, err, stream));
+}
+
 int mla_get_device_status(cudaStream_t stream, int* info) {
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;

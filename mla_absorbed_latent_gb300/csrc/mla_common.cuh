@@ -267,6 +267,12 @@ int device_sm_count();               // SMs of the current device, 0 on failure
 int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
 
 // Hv heads of the partials (virtual heads), Bv plan rows, query layout qs;
+// unabsorbed causal prefill (prefill.cu): expand the rows' latents into per-head
+// keys and values in the workspace, then flash attention over them
+size_t prefill_workspace_bytes(int B, int H, int max_pages);
+cudaError_t launch_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, int T, int num_pages,
+                           const void* pages, const int32_t* page_table, int max_pages, const int32_t* seqlens, int B,
+                           float scale, void* workspace, void* out, int* err, cudaStream_t s);
 // max_workers: the partial buffer holds max_workers + Bv segment slots
 cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
