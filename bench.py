@@ -756,13 +756,139 @@ def run_project(args, name, fmt):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# the unabsorbed causal prefill (expanded keys and values), a third workload
+# ----------------------------------------------------------------------------
+PREFILL_METRIC = "unabsorbed causal MLA prefill query tokens/s (expansion + attention), 1 GB300"
+PREFILL = {
+    # name: (H, B, n = T, seed, description)
+    "v2lite_prefill": (16, 4, 4096, 60, "V2-Lite shape: H=16, 4 rows x a 4096-token causal prefill, paged bf16 cache"),
+    "v3_prefill": (128, 1, 8192, 61, "DeepSeek-V3 shape: H=128, one 8192-token causal prefill, paged bf16 cache"),
+}
+
+
+def prefill_work(H, B, n, T):
+    """Algorithmic FLOPs of one prefill call: the expansion (2 x 256 x 512 per
+    cached token and head) and the causal attention (2 x (192 + 128) per visible
+    (query, key) pair and head)."""
+    pairs = B * sum(n - T + t + 1 for t in range(T))
+    return 2.0 * B * n * H * 256 * 512 + 2.0 * H * (192 + 128) * pairs
+
+
+def run_prefill(args, name):
+    import torch
+    torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+    import mla_absorbed_latent_gb300 as mla
+    from synth.device import DeviceDecode, bits_to_device, make_problem
+    H, B, n, seed, desc = PREFILL[name]
+    T = n
+    prob = make_problem(H, [n] * B, seed)
+    dev = DeviceDecode(prob)
+    qn, qp = synth.gen_queries_multi(H, T, prob.seqlens, seed)
+    d_qn, d_qp = bits_to_device(qn), bits_to_device(qp)
+    ws_bytes = mla.mla_prefill_workspace_bytes(B, H, prob.max_pages)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mla.mla_prefill(d_qn, d_qp, dev.wkv, H, T, dev.cache, dev.page_table, prob.max_pages, dev.seqlens, B,
+                        prob.scale, ws, ws_bytes, out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after warm-up: {mla.mla_status_string(st)} ({info})")
+    clocks = ClockSampler(torch.cuda.current_device())
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed_steps(step, args.steps, stream, None)  # the workspace (expanded K/V) is far larger than L2
+    clock_info = clocks.stop()
+    # the same queries through the absorbed multi-query decode, for comparison
+    wq = mla.mla_decode_q_workspace_bytes(B, H, T)
+    wsq = torch.empty(wq, dtype=torch.uint8, device="cuda")
+    outq = torch.empty_like(out)
+
+    def step_abs():
+        mla.mla_decode_q(d_qn, d_qp, dev.W_UK, dev.W_UV, H, T, dev.cache, dev.page_table, prob.max_pages, dev.seqlens,
+                         B, prob.scale, wsq, wq, outq, None, stream)
+
+    step_abs()
+    torch.cuda.synchronize()
+    ms_abs = timed_steps(step_abs, max(1, min(args.steps, 3)), stream, None)
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after timing: {mla.mla_status_string(st)} ({info})")
+
+    h_qn, h_qp = d_qn.cpu().pin_memory(), d_qp.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qp.copy_(h_qp, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    cpu, parity = None, None
+    if not args.no_cpu_baseline:
+        # the oracle's expand-then-attend path on a bounded sample: the last few
+        # queries of row 0 (every head, full causal views)
+        import oracle as O
+        Wuk, Wuv = O.split_wkv_b(synth.bf16_bits_to_f32(prob.wkv), H)
+        c, p = prob.sequence(0)
+        C, P = synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p)
+        k = 16
+        t_start = time.perf_counter()
+        ref = O.naive_attend_causal(synth.bf16_bits_to_f32(qn[0, T - k:]), synth.bf16_bits_to_f32(qp[0, T - k:]),
+                                    C, P, Wuk, Wuv, prob.scale, q_pos=np.arange(n - k, n))
+        secs = time.perf_counter() - t_start
+        cpu = {"value": k / secs, "unit": "query tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"the last {k} of {T} queries of row 0 of {name} (all {H} heads, full causal views), fp64 "
+                         f"numpy expand-then-attend oracle, {secs:.1f} s"}
+        got = synth.bf16_bits_to_f32(h_out.view(torch.int16).numpy().view(np.uint16))[0, T - k:]
+        parity = parity_stats({0: got}, {0: ref})
+
+    flops = prefill_work(H, B, n, T)
+    hbm, tf_burst, _tf_sus, peak_src = load_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": tflops, "peak": tf_burst, "unit": "TFLOP/s", "frac": tflops / tf_burst,
+            "traffic": None, "peak_source": peak_src + " (bf16, burst)",
+            "timed": "the whole mla_prefill call (expansion and attention kernels)"}
+    line = {
+        "metric": PREFILL_METRIC, "value": B * T / (ms * 1e-3), "unit": "query tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: {desc}", "H": H, "B": B, "seqlen": n, "q_len": T, "cache_fmt": "bf16",
+                   "flops": flops, "l2": "expanded keys/values larger than L2, no flush"},
+        "roofline": roof,
+        "absorbed_ms": ms_abs,  # the same causal queries through mla_decode_q
+        "cpu_baseline": cpu,
+        "parity": parity,
+        "e2e": {"value": B * T / (e2e_ms * 1e-3), "unit": "query tokens/s",
+                "h2d_bytes_per_step": h_qn.numel() * 2 + h_qp.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2},
+        "gpu_launches": 2 * args.steps,  # expansion, attention
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR) + sorted(PROJECT))
+    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR) + sorted(PROJECT) + sorted(PREFILL))
     ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
@@ -776,6 +902,32 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in PREFILL:
+        if args.impl == "reference":
+            if _env_int("RANK", 0) != 0:
+                return 0
+            import oracle as O
+            H, B, n, seed, desc = PREFILL[args.workload]
+            from synth.device import make_problem
+            prob = make_problem(H, [n] * B, seed)
+            qn, qp = synth.gen_queries_multi(H, n, prob.seqlens, seed)
+            Wuk, Wuv = O.split_wkv_b(synth.bf16_bits_to_f32(prob.wkv), H)
+            c, p = prob.sequence(0)
+            k = 16
+            t0 = time.perf_counter()
+            O.naive_attend_causal(synth.bf16_bits_to_f32(qn[0, n - k:]), synth.bf16_bits_to_f32(qp[0, n - k:]),
+                                  synth.bf16_bits_to_f32(c), synth.bf16_bits_to_f32(p), Wuk, Wuv, prob.scale,
+                                  q_pos=np.arange(n - k, n))
+            v = k / (time.perf_counter() - t0)
+            print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "query tokens/s",
+                              "n_gpus": args.gpus, "steps": 1, "warmup": 0, "higher_is_better": True, "dtype": "f64",
+                              "data": "synthetic", "config": {"workload": args.workload},
+                              "cpu_baseline": {"value": v, "unit": "query tokens/s", "cores": host_cores(),
+                                               "kind": "oracle", "sample": f"the last {k} queries of row 0"},
+                              "e2e": {"value": v, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+            return 0
+        return run_prefill(args, args.workload)
     if args.workload in PROJECT:
         fmt = args.fmt or "bf16"
         if args.impl == "reference":
