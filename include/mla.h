@@ -315,6 +315,28 @@ int mla_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, 
 size_t mla_prefill_workspace_bytes(int B, int H, int max_pages);
 
 /*
+ * The layer's output projection after the value up-projection:
+ * y[r, :] = W_O . (out[r, 0, :], ..., out[r, H-1, :]), i.e. y = o Wo^T over
+ * the heads' outputs side by side ("手搓 MLA" §三/§四 end both paths with
+ * "@ Wo.T"; "DeepSeek MLA 吸收式缓存" §3.3 maps o_proj to wo).  It sums over
+ * heads, so it follows the per-head merge as the next kernel of the chain:
+ * called on the same stream right after mla_decode / mla_decode_q /
+ * mla_prefill, it reads their bf16 output directly and streams its weight
+ * while they finish.
+ *   o         : bf16 [R][H][128] (the out of those calls; R = B, or B*T)
+ *   W_O       : bf16 [hidden][H*128]
+ *   hidden    : a multiple of 128, <= 65536 (2048 for V2-Lite, 7168 for V3)
+ *   y         : bf16 [R][hidden], written (fp32 accumulation, one rounding)
+ *   workspace : >= mla_output_projection_workspace_bytes(R, H, hidden) bytes,
+ *               256-byte aligned (NULL when that is 0): fp32 sums when the
+ *               reduction is split over several CTAs; cleared by the call, so
+ *               calls sharing a workspace must not overlap on the GPU
+ */
+int mla_output_projection(const void* o, const void* W_O, int R, int H, int hidden, void* y,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t mla_output_projection_workspace_bytes(int R, int H, int hidden);
+
+/*
  * Decode without any allocation (no counterpart on the pages: an interface
  * addition of this library for hosts that cannot allocate device memory, e.g.
  * an engine whose custom-op interface passes only inputs and outputs, a

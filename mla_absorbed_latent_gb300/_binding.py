@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
         "mla_decode_q_workspace_bytes": (sz, [i, i, i]),
         "mla_prefill": (i, [vp, vp, vp, i, i, cp, vp, i, vp, i, f, vp, sz, vp, vp]),
         "mla_prefill_workspace_bytes": (sz, [i, i, i]),
+        "mla_output_projection": (i, [vp, vp, i, i, i, vp, vp, sz, vp]),
+        "mla_output_projection_workspace_bytes": (sz, [i, i, i]),
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
         "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
@@ -158,6 +160,17 @@ def mla_prefill(q_nope, q_pe, wkv_b, H: int, T: int, cache: mla_cache_t, page_ta
     _check(_lib.mla_prefill(_ptr(q_nope), _ptr(q_pe), _ptr(wkv_b), H, T, ctypes.byref(cache), _ptr(page_table),
                             max_pages, _ptr(seqlens), B, scale, _ptr(workspace), workspace_bytes, _ptr(out),
                             _stream(stream)), "mla_prefill")
+
+
+def mla_output_projection_workspace_bytes(R: int, H: int, hidden: int) -> int:
+    return int(_lib.mla_output_projection_workspace_bytes(R, H, hidden))
+
+
+def mla_output_projection(o, W_O, R: int, H: int, hidden: int, y, workspace=None, workspace_bytes: int = 0,
+                          stream=None) -> None:
+    """y [R][hidden] = o [R][H*128] W_O^T (the step after the value up-projection)."""
+    _check(_lib.mla_output_projection(_ptr(o), _ptr(W_O), R, H, hidden, _ptr(y), _ptr(workspace), workspace_bytes,
+                                      _stream(stream)), "mla_output_projection")
 
 
 def mla_decode_plan(H: int, fmt: str | int, seqlens, B: int, max_pages: int, workspace, workspace_bytes: int,

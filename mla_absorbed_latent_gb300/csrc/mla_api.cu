@@ -405,6 +405,31 @@ int mla_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, 
                                   seqlens, B, scale, workspace, out, err, stream));
 }
 
+size_t mla_output_projection_workspace_bytes(int R, int H, int hidden) {
+  if (R < 0 || !heads_ok(H) || hidden <= 0 || hidden % 128 != 0) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  return out_proj_workspace_bytes(R, H * DV, hidden, sms);
+}
+
+int mla_output_projection(const void* o, const void* W_O, int R, int H, int hidden, void* y, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (!heads_ok(H) || hidden <= 0 || hidden % 128 != 0 || hidden > 65536) return MLA_ERR_UNSUPPORTED;
+  if (R < 0) return MLA_ERR_INVALID;
+  if (R == 0) return MLA_OK;
+  if (!o || !W_O || !y || !aligned(o, 16) || !aligned(W_O, 16) || !aligned(y, 16)) return MLA_ERR_INVALID;
+  const int sms = num_sms();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const size_t need = out_proj_workspace_bytes(R, H * DV, hidden, sms);
+  if (need > 0) {
+    if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
+    if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  }
+  int* err = err_ptr();
+  if (err == nullptr) return MLA_ERR_CUDA;
+  return status_of(launch_out_proj(o, W_O, R, H * DV, hidden, y, workspace, err, stream));
+}
+
 int mla_get_device_status(cudaStream_t stream, int* info) {
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;

@@ -273,6 +273,11 @@ size_t prefill_workspace_bytes(int B, int H, int max_pages);
 cudaError_t launch_prefill(const void* q_nope, const void* q_pe, const void* wkv_b, int H, int T, int num_pages,
                            const void* pages, const int32_t* page_table, int max_pages, const int32_t* seqlens, int B,
                            float scale, void* workspace, void* out, int* err, cudaStream_t s);
+// the output projection after W_UV (out_proj.cu): y [R][hidden] = o [R][K] . W_O^T
+int out_proj_splits(int R, int K, int hidden, int sms);
+size_t out_proj_workspace_bytes(int R, int K, int hidden, int sms);
+cudaError_t launch_out_proj(const void* o, const void* W_O, int R, int K, int hidden, void* y, void* workspace,
+                            int* err, cudaStream_t s);
 // max_workers: the partial buffer holds max_workers + Bv segment slots
 cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, const int* plan, const uint16_t* part_o,
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,

@@ -14,6 +14,7 @@ from .workloads import (  # noqa: F401
     bf16_bits_to_f32,
     f32_to_bf16_bits,
     gen_hidden,
+    gen_out_weights,
     gen_project_weights,
     gen_queries,
     gen_queries_multi,

@@ -226,6 +226,13 @@ def gen_project_weights(hidden: int, seed: int):
     return f32_to_bf16_bits(w), f32_to_bf16_bits(g)
 
 
+def gen_out_weights(H: int, hidden: int, seed: int) -> np.ndarray:
+    """Wo [hidden, H*128] ~ N(0, 1/sqrt(H*128)) as bf16 bits (the layer's output
+    projection after the heads)."""
+    w = _rng(seed, _S_PROJ_W, 1).standard_normal((hidden, H * D_V), dtype=np.float32)
+    return f32_to_bf16_bits(w * np.float32(1.0 / math.sqrt(H * D_V)))
+
+
 def gen_hidden(hidden: int, seed: int, b: int, n: int) -> np.ndarray:
     """Attention inputs of n tokens of row b, [n, hidden] bf16 bits, N(0,1) (the
     layer input after its own RMSNorm has unit scale per element)."""
