@@ -882,13 +882,99 @@ def run_prefill(args, name):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# the output projection after the value up-projection (y = o Wo^T)
+# ----------------------------------------------------------------------------
+OPROJ_METRIC = "MLA output projection (o Wo^T) weight-stream GB/s (% HBM peak), 1 GB300"
+OPROJ = {
+    # name: (H, R rows, hidden, description)
+    "v3_oproj": (128, 64, 7168, "DeepSeek-V3 shape: 64 decode rows x (128 heads x 128) -> hidden 7168"),
+    "v2lite_oproj": (16, 32, 2048, "V2-Lite shape: 32 decode rows x (16 heads x 128) -> hidden 2048"),
+}
+
+
+def run_oproj(args, name):
+    import torch
+    torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+    import mla_absorbed_latent_gb300 as mla
+    from synth.device import bits_to_device
+    H, R, hidden, desc = OPROJ[name]
+    rng = np.random.default_rng(130)
+    o_bits = synth.f32_to_bf16_bits(rng.standard_normal((R, H, 128)).astype(np.float32))
+    wo = synth.gen_out_weights(H, hidden, seed=131)
+    d_o, d_w = bits_to_device(o_bits), bits_to_device(wo)
+    y = torch.empty((R, hidden), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = mla.mla_output_projection_workspace_bytes(R, H, hidden)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    w_bytes = hidden * H * 128 * 2
+    scrub = torch.empty(SCRUB_BYTES, dtype=torch.uint8, device="cuda") if w_bytes < SCRUB_BELOW else None
+
+    def step():
+        mla.mla_output_projection(d_o, d_w, R, H, hidden, y, ws, ws_bytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed_steps(step, args.steps, stream, scrub)
+    clock_info = clocks.stop()
+    st, info = mla.mla_get_device_status()
+    if st != mla.MLA_OK:
+        raise RuntimeError(f"device status after timing: {mla.mla_status_string(st)} ({info})")
+    h_o = d_o.cpu().pin_memory()
+    h_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(5):
+        d_o.copy_(h_o, non_blocking=True)
+        step()
+        h_y.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / 5
+    cpu, parity = None, None
+    if not args.no_cpu_baseline:
+        import oracle as O
+        t0 = time.perf_counter()
+        ref = O.output_projection(synth.bf16_bits_to_f32(o_bits), synth.bf16_bits_to_f32(wo))
+        secs = time.perf_counter() - t0
+        cpu = {"value": w_bytes / secs / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"the whole {name} projection, fp64 numpy oracle, {secs:.2f} s"}
+        got = synth.bf16_bits_to_f32(h_y.view(torch.int16).numpy().view(np.uint16))
+        parity = parity_stats({0: got}, {0: ref})
+    hbm, *_rest = load_peaks()
+    gbs = w_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": OPROJ_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{name}: {desc}", "H": H, "R": R, "hidden": hidden, "weight_bytes": w_bytes,
+                   "k_splits": "by size", "l2": l2_note(w_bytes, scrub is not None)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                     "peak_source": load_peaks()[3], "algorithmic_bytes": "the weight (hidden x H*128 bf16)"},
+        "cpu_baseline": cpu,
+        "parity": parity,
+        "e2e": {"value": w_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h_o.numel() * 2,
+                "d2h_bytes_per_step": h_y.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="v3_paged", choices=sorted(DESCR) + sorted(PROJECT) + sorted(PREFILL))
+    ap.add_argument("--workload", default="v3_paged",
+                    choices=sorted(DESCR) + sorted(PROJECT) + sorted(PREFILL) + sorted(OPROJ))
     ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
@@ -902,6 +988,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in OPROJ:
+        if args.impl == "reference":
+            return 0 if _env_int("RANK", 0) != 0 else print(json.dumps(
+                {"impl": "reference", "unavailable": "the output projection has no separate reference arm; its oracle "
+                 "timing is the cpu_baseline of the default arm"})) or 0
+        return run_oproj(args, args.workload)
     if args.workload in PREFILL:
         if args.impl == "reference":
             if _env_int("RANK", 0) != 0:

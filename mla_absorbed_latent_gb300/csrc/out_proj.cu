@@ -184,12 +184,13 @@ __global__ void __launch_bounds__(128, 1)
 
 }  // namespace
 
-// K splits per (feature tile, row tile): enough CTAs for two per SM, each at
-// least 8 chunks of K
+// K splits per (feature tile, row tile): as many CTAs as fit two per SM in
+// one wave (rounding up would leave a short second wave), each at least 8
+// chunks of K
 int out_proj_splits(int R, int K, int hidden, int sms) {
   const long long tiles = (long long)(hidden / OP_M) * ((R + OP_N - 1) / OP_N);
   const int chunks = K / 64;
-  const long long want = tiles > 0 ? (2LL * sms + tiles - 1) / tiles : 1;
+  const long long want = tiles > 0 ? (2LL * sms) / tiles : 1;
   long long k = want < chunks / 8 ? want : chunks / 8;
   return k > 1 ? (int)k : 1;
 }
