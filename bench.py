@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "absorbed-MLA decode latent-cache GB/s (% HBM peak) and queries/s, 1 GB300"
-BYTES_PER_TOKEN = {"bf16": 1152, "int8": 624, "int4": 400}
+BYTES_PER_TOKEN = {"bf16": 1152, "int8": 624, "int4": 400, "int8_token": 624, "int4_sym": 400}
 DESCR = {
     "v2lite_batch": "V2-Lite shape decode: H=16, B=32, seqlen 4096, contiguous bf16 latent cache",
     "v3_paged": "DeepSeek-V3 shape decode: H=128, B=64, seqlen 8192, paged bf16 latent cache "
@@ -975,7 +975,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v3_paged",
                     choices=sorted(DESCR) + sorted(PROJECT) + sorted(PREFILL) + sorted(OPROJ))
-    ap.add_argument("--fmt", default=None, choices=["bf16", "int8", "int4"])
+    ap.add_argument("--fmt", default=None, choices=sorted(BYTES_PER_TOKEN))
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override every row's length (a smaller case of the workload's shape, e.g. for ncu)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

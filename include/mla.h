@@ -68,9 +68,11 @@ typedef enum {
 
 /* Cache storage formats. */
 typedef enum {
-  MLA_FMT_BF16 = 0,  /* c_KV and k_pe in bfloat16                                   */
-  MLA_FMT_INT8 = 1,  /* c_KV INT8 per 32-channel group, k_pe INT8 per 8, bf16 scales */
-  MLA_FMT_INT4 = 2   /* c_KV asymmetric INT4 per 32 (bf16 scale + zero), k_pe INT8/8 */
+  MLA_FMT_BF16 = 0,       /* c_KV and k_pe in bfloat16                                   */
+  MLA_FMT_INT8 = 1,       /* c_KV INT8 per 32-channel group, k_pe INT8 per 8, bf16 scales */
+  MLA_FMT_INT4 = 2,       /* c_KV asymmetric INT4 per 32 (bf16 scale + zero), k_pe INT8/8 */
+  MLA_FMT_INT8_TOKEN = 3, /* c_KV INT8 with one scale per token, k_pe INT8/8 (INT8 pages) */
+  MLA_FMT_INT4_SYM = 4    /* c_KV symmetric INT4 per 32, k_pe INT8/8 (INT4 pages)         */
 } mla_fmt_t;
 
 /*
@@ -92,6 +94,15 @@ typedef enum {
  *   INT4 group:  s = bf16_rne((max - min) / 15); z = min;
  *                code = clamp(rint((x - z) / s), 0, 15); x^ = code * s + z
  *   rint rounds half to even; a group with s == 0 stores zero codes.
+ * The other quantizers "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 compares
+ * write the same two page layouts, so the decode reads them unchanged:
+ *   MLA_FMT_INT8_TOKEN (INT8 pages): s = bf16_rne(amax over the token's 512
+ *     channels / 127), stored in all 16 of its c scale slots; codes as INT8.
+ *   MLA_FMT_INT4_SYM (INT4 pages): per 32-channel group s = bf16_rne(amax / 7),
+ *     q = clamp(rint(x / s), -7, 7) (0 when s == 0), stored as the nibble q + 8
+ *     with zero = -8 s (exact in bf16), so that code * s + zero = q * s.
+ * (One scale for the whole tensor cannot serve an append-only cache: it would
+ * change as tokens arrive.)
  */
 typedef struct {
   int fmt;          /* mla_fmt_t                                                  */
@@ -166,6 +177,9 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  * between runs; without one (many tokens) the result is deterministic.  Bad
  * positions and page ids are skipped and raise MLA_ERR_BOUNDS as in
  * mla_cache_append.  x, wkv_a, kv_norm_w and latent_out 16-byte aligned.
+ * Formats MLA_FMT_BF16, MLA_FMT_INT8 and MLA_FMT_INT4; the per-token INT8 and
+ * symmetric INT4 variants return MLA_ERR_UNSUPPORTED here (append their
+ * payload, from latent_out of a bf16 call, with mla_cache_append).
  */
 int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden, const void* wkv_a,
                              const void* kv_norm_w, float eps, float rope_theta,

@@ -10,7 +10,8 @@
 // by construction: every decision is one IEEE fp32 operation (quant.cuh).
 //
 // One warp per token.  bf16: lanes copy 16-byte chunks.  Quantized: lane g < 16
-// owns c_KV group g, lanes 16..23 own the k_pe groups.
+// owns c_KV group g, lanes 16..23 own the k_pe groups.  The per-token INT8 and
+// symmetric INT4 quantizers write INT8 and INT4 pages (include/mla.h).
 #include "quant.cuh"
 
 namespace mla {
@@ -62,16 +63,44 @@ __global__ void __launch_bounds__(256) append_kernel(int fmt, int num_pages, uin
     return;
   }
 
-  const size_t pb = fmt == MLA_FMT_INT8 ? PAGE_BYTES_INT8 : PAGE_BYTES_INT4;
+  const bool i8 = layout_fmt(fmt) == MLA_FMT_INT8;
+  const size_t pb = i8 ? PAGE_BYTES_INT8 : PAGE_BYTES_INT4;
   uint8_t* page = pages + (size_t)phys * pb;
-  const int pe_code_off = fmt == MLA_FMT_INT8 ? I8_PE_CODE : I4_PE_CODE;
-  const int pe_scale_off = fmt == MLA_FMT_INT8 ? I8_PE_SCALE : I4_PE_SCALE;
+  const int pe_code_off = i8 ? I8_PE_CODE : I4_PE_CODE;
+  const int pe_scale_off = i8 ? I8_PE_SCALE : I4_PE_SCALE;
+
+  // per-token INT8: the token's one scale over all 512 channels (lanes 0..15
+  // own the 32-channel groups; the maximum is reduced over them)
+  float tok_amax = 0.f;
+  float x[32];
+  if (lane < 16) {
+    load32(c + lane * 32, x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) tok_amax = fmaxf(tok_amax, fabsf(x[i]));
+  }
+  if (fmt == MLA_FMT_INT8_TOKEN) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) tok_amax = fmaxf(tok_amax, __shfl_xor_sync(0xffffffffu, tok_amax, o));
+  }
 
   if (lane < 16) {
     const int g = lane;
-    float x[32];
-    load32(c + g * 32, x);
-    if (fmt == MLA_FMT_INT8) {
+    if (fmt == MLA_FMT_INT8_TOKEN) {
+      const __nv_bfloat16 sb = __float2bfloat16_rn(tok_amax / 127.0f);
+      int8_t code[32];
+      quant_i8_scaled<32>(x, __bfloat162float(sb), code);
+      uint8_t* dst = page + I8_C_CODE + slot * DC + g * 32;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) store_i8x8(dst + 8 * i, code + 8 * i);
+      reinterpret_cast<uint16_t*>(page + I8_C_SCALE)[slot * 16 + g] = __bfloat16_as_ushort(sb);
+    } else if (fmt == MLA_FMT_INT4_SYM) {
+      uint32_t w[4];
+      uint16_t sb, zb;
+      quant_i4sym_32(x, w, &sb, &zb);
+      *reinterpret_cast<uint4*>(page + I4_C_CODE + slot * (DC / 2) + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint16_t*>(page + I4_C_SCALE)[slot * 16 + g] = sb;
+      reinterpret_cast<uint16_t*>(page + I4_C_ZERO)[slot * 16 + g] = zb;
+    } else if (fmt == MLA_FMT_INT8) {
       int8_t code[32];
       const uint16_t sb = quant_i8<32>(x, code);
       uint8_t* dst = page + I8_C_CODE + slot * DC + g * 32;

@@ -103,7 +103,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream) != cudaSuccess) return MLA_ERR_CUDA;
   cudaError_t e;
   if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   else
     e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,

@@ -49,14 +49,14 @@ int num_sms() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool heads_ok(int H) { return H == 16 || H == 128; }
-bool fmt_ok(int fmt) { return fmt == MLA_FMT_BF16 || fmt == MLA_FMT_INT8 || fmt == MLA_FMT_INT4; }
+bool fmt_ok(int fmt) { return fmt >= MLA_FMT_BF16 && fmt <= MLA_FMT_INT4_SYM; }
 // hidden width of the cache producer's input: whole 64-wide chunks of the projection's K
 bool hidden_ok(int hidden) { return hidden >= 64 && hidden <= 65536 && hidden % 64 == 0; }
 // the producer indexes tokens with 32-bit integers
 constexpr long long MAX_PROJECT_TOKENS = 2147483647LL - 128;
 
 size_t page_bytes(int fmt) {
-  switch (fmt) {
+  switch (layout_fmt(fmt)) {
     case MLA_FMT_BF16: return PAGE_BYTES_BF16;
     case MLA_FMT_INT8: return PAGE_BYTES_INT8;
     case MLA_FMT_INT4: return PAGE_BYTES_INT4;
@@ -139,7 +139,7 @@ int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden
                              int max_pages, const int32_t* pos, int B, int T, void* latent_out, int k_splits,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (cache == nullptr) return MLA_ERR_INVALID;
-  if (!fmt_ok(cache->fmt) || !hidden_ok(hidden)) return MLA_ERR_UNSUPPORTED;
+  if (!fmt_ok(cache->fmt) || !hidden_ok(hidden) || layout_fmt(cache->fmt) != cache->fmt) return MLA_ERR_UNSUPPORTED;
   if (!cache_ok(cache) || B < 0 || T < 0 || max_pages <= 0 || k_splits < 0) return MLA_ERR_INVALID;
   const long long ntok = (long long)B * T;
   if (ntok == 0) return MLA_OK;
@@ -258,7 +258,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
   cudaError_t e;
   if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
+    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, B,
                          scale, plan, workers, part_o, part_lse, err, stream);
   else
     e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
@@ -368,7 +368,7 @@ int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const v
   cudaError_t e = launch_plan(seqlens, B, qs, max_pages, workers, plan, err, stream);
   if (e == cudaSuccess) e = launch_q_absorb(q_nope, q_pe, W_UK, H, B * T, ws + L.q_cat, stream);
   if (e == cudaSuccess)
-    e = launch_attend_tc(ws + L.q_cat, qs, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, Bv,
+    e = launch_attend_tc(ws + L.q_cat, qs, layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, Bv,
                          scale, plan, workers, part_o, part_lse, err, stream);
   if (e == cudaSuccess)
     e = launch_combine(W_UV, 128, Bv, qs, plan, part_o, part_lse, out, o_lat_out, err, L.max_segments - Bv, stream);

@@ -24,6 +24,12 @@ constexpr size_t PAGE_BYTES_BF16 = (size_t)PAGE * DK * 2;                       
 constexpr size_t PAGE_BYTES_INT8 = (size_t)PAGE * (DC + DR + 2 * 16 + 2 * 8);   // 39,936
 constexpr size_t PAGE_BYTES_INT4 = (size_t)PAGE * (DC / 2 + DR + 4 * 16 + 2 * 8);  // 25,600
 
+// the page layout (and decode kernel) a cache format uses: the per-token INT8
+// and symmetric INT4 quantizers write INT8 and INT4 pages
+__host__ __device__ constexpr int layout_fmt(int fmt) {
+  return fmt == MLA_FMT_INT8_TOKEN ? MLA_FMT_INT8 : fmt == MLA_FMT_INT4_SYM ? MLA_FMT_INT4 : fmt;
+}
+
 // section offsets inside a quantized page
 constexpr int I8_C_CODE = 0, I8_PE_CODE = 32768, I8_C_SCALE = 36864, I8_PE_SCALE = 38912;
 constexpr int I4_C_CODE = 0, I4_PE_CODE = 16384, I4_C_SCALE = 20480, I4_C_ZERO = 22528,

@@ -3,7 +3,8 @@
 // mla_cache_project_append).  Every decision is one IEEE fp32 operation on
 // bf16-representable inputs, so the codes and scales are bit-exact and
 // deterministic: INT8 over 32-channel groups of c_KV and 8-dim groups of k_pe,
-// asymmetric INT4 (scale + zero) over 32-channel groups of c_KV
+// asymmetric INT4 (scale + zero) over 32-channel groups of c_KV, and the
+// per-token INT8 and symmetric INT4 variants
 // ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 names the block sizes; the
 // rounding rules are the library's, stated in include/mla.h).
 #pragma once
@@ -50,6 +51,38 @@ __device__ __forceinline__ void quant_i4_32(const float* x, uint32_t* w, uint16_
   }
   *scale_bits = __bfloat16_as_ushort(sb);
   *zero_bits = __bfloat16_as_ushort(zb);
+}
+
+// INT8 codes of N values with a given scale (bf16 value s): the per-token
+// quantizer's groups, which share the token's scale
+template <int N>
+__device__ __forceinline__ void quant_i8_scaled(const float* x, float s, int8_t* code) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float q = 0.f;
+    if (s != 0.f) q = fminf(fmaxf(rintf(x[i] / s), -127.f), 127.f);
+    code[i] = static_cast<int8_t>(q);
+  }
+}
+
+// Symmetric INT4 of 32 values, written in the asymmetric INT4 page form: the
+// nibbles hold q + 8 (q = clamp(rint(x / s), -7, 7), s = bf16(amax / 7)) and
+// the zero is -8 s, so that code * s + zero = q * s exactly.
+__device__ __forceinline__ void quant_i4sym_32(const float* x, uint32_t* w, uint16_t* scale_bits, uint16_t* zero_bits) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const __nv_bfloat16 sb = __float2bfloat16_rn(amax / 7.0f);
+  const float s = __bfloat162float(sb);
+  w[0] = w[1] = w[2] = w[3] = 0u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float q = 0.f;
+    if (s != 0.f) q = fminf(fmaxf(rintf(x[i] / s), -7.f), 7.f);
+    w[i / 8] |= (uint32_t)(q + 8.f) << (4 * (i % 8));
+  }
+  *scale_bits = __bfloat16_as_ushort(sb);
+  *zero_bits = __bfloat16_as_ushort(__float2bfloat16_rn(-8.f * s));  // exact: a power-of-two multiple
 }
 
 __device__ __forceinline__ void store_i8x8(uint8_t* dst, const int8_t* c) {

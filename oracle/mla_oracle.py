@@ -443,6 +443,10 @@ PAGE_LAYOUT = {
              ("c_scale", "bf16", (D_C // 32,)), ("c_zero", "bf16", (D_C // 32,)),
              ("pe_scale", "bf16", (D_R // 8,))],
 }
+# the per-token INT8 and symmetric INT4 quantizers of [report] §3.2 write the
+# INT8 and INT4 page layouts (the library's reading: one page form per code width)
+PAGE_LAYOUT["int8_token"] = PAGE_LAYOUT["int8"]
+PAGE_LAYOUT["int4_sym"] = PAGE_LAYOUT["int4"]
 _ELEM = {"bf16": 2, "i8": 1, "u4x2": 1}
 
 
@@ -478,6 +482,17 @@ def quantize_token(fmt: str, c_kv, k_pe):
         cc, cs, cz = quantize_int4_asym(c, 32)
         return {"c_code": pack_nibbles(cc), "pe_code": pc, "c_scale": bf16_to_bits(cs),
                 "c_zero": bf16_to_bits(cz), "pe_scale": bf16_to_bits(ps)}
+    if fmt == "int8_token":
+        # one scale per token, repeated in the token's 16 group-scale slots
+        cc, cs = quantize_int8_per_token(c)
+        return {"c_code": cc, "pe_code": pc, "c_scale": bf16_to_bits(np.repeat(cs, D_C // 32, axis=-1)),
+                "pe_scale": bf16_to_bits(ps)}
+    if fmt == "int4_sym":
+        # codes q in -7..7 stored as q + 8, zero -8 s: code * s + zero = q * s
+        q, cs = quantize_int4_sym(c, 32)
+        return {"c_code": pack_nibbles((q.astype(np.int16) + 8).astype(np.uint8)), "pe_code": pc,
+                "c_scale": bf16_to_bits(cs), "c_zero": bf16_to_bits(np.float32(-8.0) * cs),
+                "pe_scale": bf16_to_bits(ps)}
     raise ValueError(fmt)
 
 
@@ -492,6 +507,12 @@ def dequantized_tokens(fmt: str, c_kv, k_pe):
     if fmt == "int8":
         cc, cs = quantize_int8(c, 32)
         return dequantize_int8(cc, cs, 32), pe
+    if fmt == "int8_token":
+        cc, cs = quantize_int8_per_token(c)
+        return dequantize_int8(cc, cs, D_C), pe
+    if fmt == "int4_sym":
+        q, cs = quantize_int4_sym(c, 32)
+        return dequantize_int4_sym(q, cs, 32), pe
     cc, cs, cz = quantize_int4_asym(c, 32)
     return dequantize_int4(cc, cs, cz, 32), pe
 

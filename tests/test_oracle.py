@@ -722,3 +722,36 @@ def test_generator_page_tables_and_lengths():
     assert all(np.all(table[b, need[b]:] == -1) for b in range(len(lens)))
     ident, _ = synth.make_page_table([70, 10], 0, False)
     assert ident.tolist() == [[0, 1], [2, -1]]
+
+
+def test_variant_pool_sections():
+    """The per-token INT8 and symmetric INT4 quantizers in their page images,
+    indexed by hand: per-token INT8 keeps the INT8 layout with the token's one
+    scale s = bf16(amax / 127) in all 16 group-scale slots; symmetric INT4 keeps
+    the INT4 layout with nibbles q + 8 and zero = -8 s, so that code * s + zero
+    equals q * s (the symmetric dequantization)."""
+    rng = np.random.default_rng(3)
+    c = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((1, 512)).astype(np.float32) * 2))
+    p = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(rng.standard_normal((1, 64)).astype(np.float32)))
+    # per-token INT8, slot 9
+    pool = O.expected_page_pool("int8_token", 1, [(np.array([0]), 9, c, p)])[0]
+    s_tok = float(np.asarray(O.bf16_round(np.max(np.abs(c)) / np.float32(127.0))).reshape(-1)[0])
+    scales = pool[36864 + 9 * 32:36864 + 10 * 32].view(np.uint16)
+    assert np.all(scales == O.bf16_to_bits(np.float32(s_tok)))
+    codes = pool[9 * 512:10 * 512].view(np.int8).astype(np.float64)
+    assert np.all(np.abs(codes) <= 127) and np.max(np.abs(codes)) == 127
+    assert np.allclose(codes * float(s_tok), O.dequantized_tokens("int8_token", c, p)[0][0], rtol=0, atol=0)
+    # symmetric INT4, slot 3
+    pool = O.expected_page_pool("int4_sym", 1, [(np.array([0]), 3, c, p)])[0]
+    q, s = O.quantize_int4_sym(c, 32)
+    nib = pool[3 * 256:4 * 256]
+    lo, hi = (nib & 0xF).astype(np.int16), (nib >> 4).astype(np.int16)
+    assert np.array_equal(lo - 8, q[0, 0::2]) and np.array_equal(hi - 8, q[0, 1::2])
+    sc = synth.bf16_bits_to_f32(pool[20480 + 3 * 32:20480 + 4 * 32].view(np.uint16))
+    zr = synth.bf16_bits_to_f32(pool[22528 + 3 * 32:22528 + 4 * 32].view(np.uint16))
+    assert np.array_equal(sc, s[0]) and np.array_equal(zr, -8 * s[0])
+    codes = np.empty(512)
+    codes[0::2], codes[1::2] = lo, hi
+    g = np.repeat(np.arange(16), 32)
+    assert np.array_equal(codes * sc[g].astype(np.float64) + zr[g], q[0] * s[0][g].astype(np.float64))
+    assert np.array_equal(O.dequantized_tokens("int4_sym", c, p)[0][0], q[0] * s[0][g].astype(np.float64))
