@@ -39,24 +39,6 @@ struct __align__(16) SmemCC {
   uint64_t full[2];
 };
 
-struct Cursor {
-  int x, half, b;
-};
-
-__device__ __forceinline__ int page_valid(const int* prefix, const int* seq_c, int b, int x) {
-  return min(PAGE, seq_c[b] - PAGE * (x - prefix[b]));
-}
-
-__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, const int* seq_c, int B) {
-  if (c.half == 0 && page_valid(prefix, seq_c, c.b, c.x) > HT) {
-    c.half = 1;
-    return;
-  }
-  c.half = 0;
-  ++c.x;
-  while (c.b < B - 1 && c.x >= prefix[c.b + 1]) ++c.b;
-}
-
 __global__ void __launch_bounds__(THREADS, 2)
     attend_cc_kernel(const uint16_t* __restrict__ q_cat, int H, int num_pages, const uint8_t* __restrict__ pages,
                      const int32_t* __restrict__ page_table, int max_pages, int B, float scale_log2,
@@ -89,7 +71,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
 
   const uint64_t policy = policy_evict_first();
-  auto issue = [&](const Cursor& c, int stage) {
+  auto issue = [&](const HalfCursor& c, int stage) {
     const int j = c.x - prefix[c.b];
     int phys = page_table[(size_t)c.b * max_pages + j];
     if (phys < 0 || phys >= num_pages) {
@@ -101,8 +83,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     bulk_g2s_hint(S.kv[stage], src, HALF_BYTES, &S.full[stage], policy);
   };
 
-  Cursor cons{x0, 0, lo};
-  Cursor prod = cons;
+  HalfCursor cons{x0, 0, lo};
+  HalfCursor prod = cons;
   if (tid == 0) issue(prod, 0);
   cursor_next(prod, prefix, seq_c, B);
   int issued = 1;
@@ -240,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
     }
 
-    Cursor nxt = cons;
+    HalfCursor nxt = cons;
     cursor_next(nxt, prefix, seq_c, B);
     // end of this row's segment: emit O / l and the natural-log LSE
     if (nxt.x >= x1 || nxt.b != cons.b) {

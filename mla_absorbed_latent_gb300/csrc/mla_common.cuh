@@ -304,6 +304,25 @@ bool encode_3d_box(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
 // still running; it must call grid_dep_wait before touching any memory that
 // earlier work may write (or read), and calls grid_dep_launch after that wait,
 // letting the next kernel of the chain begin its own prologue.
+// Walk over a worker's pages in halves of 32 tokens (the CUDA-core and
+// warp-MMA decode kernels): page tile x of row b, half 0 or 1; a page's second
+// half is visited only when it holds tokens.
+struct HalfCursor {
+  int x, half, b;
+};
+__device__ __forceinline__ int page_valid(const int* prefix, const int* seq_c, int b, int x) {
+  return min(PAGE, seq_c[b] - PAGE * (x - prefix[b]));
+}
+__device__ __forceinline__ void cursor_next(HalfCursor& c, const int* prefix, const int* seq_c, int B) {
+  if (c.half == 0 && page_valid(prefix, seq_c, c.b, c.x) > PAGE / 2) {
+    c.half = 1;
+    return;
+  }
+  c.half = 0;
+  ++c.x;
+  while (c.b < B - 1 && c.x >= prefix[c.b + 1]) ++c.b;
+}
+
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
