@@ -454,7 +454,12 @@ def run_ours(args, wl, fmt):
     H, B = prob.H, prob.B
     stream = torch.cuda.current_stream()
     cache_bytes = int(np.sum(prob.seqlens)) * BYTES_PER_TOKEN[fmt]
-    kind = mla.mla_decode_kernel_kind(H) if fmt == "bf16" else 1
+    if H == 16:
+        mla.mla_decode_select_kernel(16, {"mma": mla.MLA_KERNEL_MMA,
+                                          "cuda_cores": mla.MLA_KERNEL_CUDA_CORES}[args.h16_kernel])
+    kind = mla.mla_decode_kernel_kind(H) if fmt == "bf16" else mla.MLA_KERNEL_TCGEN05
+    kind_name = {mla.MLA_KERNEL_TCGEN05: "tcgen05", mla.MLA_KERNEL_MMA: "mma.sync",
+                 mla.MLA_KERNEL_CUDA_CORES: "cuda-core"}[kind]
 
     def step(ev=None):
         # ev: 5 events bracketing plan | absorb_q | attend | combine
@@ -556,8 +561,14 @@ def run_ours(args, wl, fmt):
     value = job_throughput(cache_bytes, world, ms_step)
     attend_gbs = cache_bytes / (attend_ms * 1e-3) / 1e9
     flops_tok = 2 * H * (576 + 512)
-    traffic = kernel_traffic("tcgen05" if kind == 1 else "cuda-core", fmt)
-    if kind == 1:
+    traffic = kernel_traffic(kind_name, fmt)
+    if kind == mla.MLA_KERNEL_MMA:
+        # 16 heads: 30 FLOP per cache byte, far below any tensor ridge; the cache stream binds
+        tflops = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12
+        roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s", "frac": attend_gbs / hbm,
+                "traffic": traffic, "peak_source": peak_src, "tensor_tflops": tflops,
+                "arith_intensity": flops_tok / BYTES_PER_TOKEN[fmt]}
+    elif kind == mla.MLA_KERNEL_TCGEN05:
         tflops = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12
         ai = flops_tok / BYTES_PER_TOKEN[fmt]            # FLOP per cache byte
         ridge = tf_burst * 1e12 / (hbm * 1e9)
@@ -586,7 +597,7 @@ def run_ours(args, wl, fmt):
                    "seqlen": int(prob.seqlens.max()), "cache_fmt": fmt, "cache_bytes_per_step": cache_bytes,
                    "l2": l2_note(cache_bytes, scrub),
                    "parallelism": f"replicas x{world} (batch-sharded, no collective)",
-                   "attend_kernel": "tcgen05" if kind == 1 else "cuda-core"},
+                   "attend_kernel": kind_name},
         "pct_hbm_peak": 100.0 * value / (hbm * world),
         "queries_per_s": B * world / (ms_step * 1e-3),
         "roofline": roof,
@@ -982,6 +993,9 @@ def main(argv=None):
     ap.add_argument("--k-splits", type=int, default=0,
                     help="producer workloads: CTA pairs per 128-token tile over the hidden dimension (0 = by size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--h16-kernel", choices=["mma", "cuda_cores"], default="mma",
+                    help="attend kernel of the 16-head decode workloads (the warp-level MMA kernel, or the "
+                         "CUDA-core baseline)")
     ap.add_argument("--q-len", type=int, default=None,
                     help="query tokens per row through mla_decode_q (default: the workload's; 1 runs the single-"
                          "query step of an H=16 workload on the tensor cores)")

@@ -210,7 +210,8 @@ size_t mla_decode_workspace_bytes(int B, int H);
  *               256-byte aligned; contents need no initialisation
  *   out       : bf16 [B][H][128], written
  * H in {16, 128}: H = 128 runs the tcgen05 tensor-core kernel, H = 16 the
- * CUDA-core kernel.  Formats: H = 128 reads bf16, INT8 and INT4 pools (codes
+ * warp-level MMA kernel (or the CUDA-core kernel, mla_decode_select_kernel).
+ * Formats: H = 128 reads bf16, INT8 and INT4 pools (codes
  * are dequantized to bf16 in the kernel's load stage, x = code*s (+ z), fp32
  * then one bf16 rounding); H = 16 reads bf16 pools only (MLA_ERR_UNSUPPORTED
  * otherwise).  Equivalent to mla_decode_plan + mla_decode_absorb_q +
@@ -249,7 +250,7 @@ int mla_decode_plan_workers(int H, int fmt, const int32_t* seqlens, int B, int m
 
 /* The default (largest) number of split workers of the attend kernel for H
  * heads over a `fmt` cache on the current device: persistent CTA pairs of the
- * tcgen05 kernel, CTAs of the CUDA-core kernel; a negative status for an
+ * tcgen05 kernel, CTAs of the 16-head kernels; a negative status for an
  * unsupported pair. */
 int mla_decode_max_workers(int H, int fmt);
 
@@ -398,9 +399,31 @@ int mla_get_device_status(cudaStream_t stream, int* info);
  */
 int mla_wait_selftest(cudaStream_t stream);
 
-/* Which attend kernel mla_decode uses for H heads: 1 = tcgen05, 0 = CUDA cores,
- * -1 = unsupported. */
+/* The split-KV attend kernels of the single-query decode.  H = 128 runs on the
+ * fifth-generation tensor cores (tcgen05, a CTA pair per worker, every cache
+ * format).  H = 16 over bf16 pages has two: the warp-level MMA kernel
+ * (mma.sync m16n8k16, whose 16 rows are exactly the 16 heads; the default) and
+ * the CUDA-core kernel (fp32 FMA; kept as the baseline the other is measured
+ * against).  Both compute the defined softmax (fp32 online softmax with a
+ * rescale at every new maximum). */
+typedef enum {
+  MLA_KERNEL_CUDA_CORES = 0,
+  MLA_KERNEL_TCGEN05 = 1,
+  MLA_KERNEL_MMA = 2
+} mla_kernel_t;
+
+/* Which attend kernel mla_decode (and the calls of its steps, and
+ * mla_decode_noalloc) uses for H heads over bf16 pages: an mla_kernel_t value,
+ * or -1 when H is unsupported. */
 int mla_decode_kernel_kind(int H);
+
+/* Selects the attend kernel for H heads, process-wide, for the calls that
+ * start after it returns: H = 16 takes MLA_KERNEL_MMA or MLA_KERNEL_CUDA_CORES,
+ * H = 128 only MLA_KERNEL_TCGEN05.  Returns MLA_OK or MLA_ERR_UNSUPPORTED.
+ * The plan, attend and combine of one decode must see the same selection (do
+ * not switch between mla_decode_plan and mla_decode_attend); the workspace
+ * size does not depend on it. */
+int mla_decode_select_kernel(int H, int kind);
 
 /* Human-readable name of a status code (static string). */
 const char* mla_status_string(int status);

@@ -22,6 +22,7 @@ MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = -4, -5, -6
 FMT = {"bf16": 0, "int8": 1, "int4": 2, "int8_token": 3, "int4_sym": 4}
 D_C, D_R, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # the fixed scratch of mla_decode_noalloc
+MLA_KERNEL_CUDA_CORES, MLA_KERNEL_TCGEN05, MLA_KERNEL_MMA = 0, 1, 2  # mla_kernel_t
 
 
 class MLAError(RuntimeError):
@@ -64,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "mla_get_device_status": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
         "mla_wait_selftest": (i, [vp]),
         "mla_decode_kernel_kind": (i, [i]),
+        "mla_decode_select_kernel": (i, [i, i]),
         "mla_status_string": (ctypes.c_char_p, [i]),
     }
     for name, (res, args) in sigs.items():
@@ -226,6 +228,11 @@ def mla_wait_selftest(stream=None) -> None:
 
 def mla_decode_kernel_kind(H: int) -> int:
     return int(_lib.mla_decode_kernel_kind(H))
+
+
+def mla_decode_select_kernel(H: int, kind: int) -> None:
+    """Process-wide choice of the attend kernel for H heads (see include/mla.h)."""
+    _check(_lib.mla_decode_select_kernel(H, kind), "mla_decode_select_kernel")
 
 
 def mla_status_string(status: int) -> str:

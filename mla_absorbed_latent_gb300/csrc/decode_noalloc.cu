@@ -83,7 +83,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
 
   const int sms = device_sm_count();
   if (sms <= 0) return MLA_ERR_CUDA;
-  const int want = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  const int want = attend_workers(kind, sms);
   const int workers = fitting_workers(B, H, want, kScratchBytes);
   if (workers < 1) return MLA_ERR_WORKSPACE;  // batch too large for the fixed scratch
 
@@ -101,14 +101,9 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
 
   if (launch_plan(seqlens, B, qspec_single(H), max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  cudaError_t e;
-  if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, B,
-                         scale, plan, workers, part_o, part_lse, err, stream);
-  else
-    e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
-                         scale, plan, workers, part_o, part_lse, err, stream);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers, part_o, part_lse,
+                         err, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (launch_combine(W_UV, H, B, qspec_single(H), plan, part_o, part_lse, out, nullptr, err, workers, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;

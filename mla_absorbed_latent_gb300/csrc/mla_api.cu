@@ -1,5 +1,6 @@
 // C ABI of libmla: argument checks, workspace layout, kernel dispatch and the
 // device error word.  Declarations and the contract live in include/mla.h.
+#include <atomic>
 #include <mutex>
 
 #include "mla_common.cuh"
@@ -64,15 +65,22 @@ size_t page_bytes(int fmt) {
   }
 }
 
-// attend kernel for H heads over a `fmt` cache: 1 = tcgen05, 0 = CUDA cores, -1 = none
+// the kernel of 16-head decodes over bf16 pages (mla_decode_select_kernel)
+std::atomic<int> g_small_head_kernel{MLA_KERNEL_MMA};
+
+// attend kernel for H heads over a `fmt` cache (an mla_kernel_t value), -1 = none
 int attend_kind(int H, int fmt) {
   if (!heads_ok(H) || !fmt_ok(fmt)) return -1;
-  if (H == 128) return 1;  // every format: quantized pages are dequantized in the load stage
-  return fmt == MLA_FMT_BF16 ? 0 : -1;
+  if (H == 128) return MLA_KERNEL_TCGEN05;  // every format: quantized pages are dequantized in the load stage
+  return fmt == MLA_FMT_BF16 ? g_small_head_kernel.load() : -1;
 }
 
-int max_workers(int sms) { return attend_cc_workers(sms) > attend_tc_workers(sms) ? attend_cc_workers(sms)
-                                                                                 : attend_tc_workers(sms); }
+int max_workers(int sms) {
+  int w = attend_tc_workers(sms);
+  if (attend_cc_workers(sms) > w) w = attend_cc_workers(sms);
+  if (attend_mma_workers(sms) > w) w = attend_mma_workers(sms);
+  return w;
+}
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
@@ -95,6 +103,28 @@ int check_ws(int B, int H, void* ws, size_t ws_bytes, WsLayout* L) {
 int* device_error_word() { return err_ptr(); }
 int device_sm_count() { return num_sms(); }
 int attend_kernel_kind(int H, int fmt) { return attend_kind(H, fmt); }
+int attend_workers(int kind, int sms) {
+  return kind == MLA_KERNEL_TCGEN05 ? attend_tc_workers(sms)
+         : kind == MLA_KERNEL_MMA   ? attend_mma_workers(sms)
+                                    : attend_cc_workers(sms);
+}
+cudaError_t launch_attend_kind(int kind, const void* q_cat, int H, const mla_cache_t* cache,
+                               const int32_t* page_table, int max_pages, int B, float scale, int* plan, int workers,
+                               uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
+  switch (kind) {
+    case MLA_KERNEL_TCGEN05:
+      return launch_attend_tc(q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages,
+                              page_table, max_pages, B, scale, plan, workers, part_o, part_lse, err, s);
+    case MLA_KERNEL_MMA:
+      return launch_attend_mma(q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B, scale,
+                               plan, workers, part_o, part_lse, err, s);
+    case MLA_KERNEL_CUDA_CORES:
+      return launch_attend_cc(q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B, scale,
+                              plan, workers, part_o, part_lse, err, s);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
 
 }  // namespace mla
 
@@ -201,7 +231,7 @@ int decode_plan(int H, int fmt, const int32_t* seqlens, int B, int max_pages, in
   int st = check_ws(B, H, workspace, workspace_bytes, &L);
   if (st != MLA_OK) return st;
   const int sms = num_sms();
-  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  const int workers = attend_workers(kind, sms);
   if (req > workers) return MLA_ERR_INVALID;
   if (B == 0) return MLA_OK;
   if (!seqlens || !aligned(seqlens, 4)) return MLA_ERR_INVALID;
@@ -230,7 +260,7 @@ int mla_decode_max_workers(int H, int fmt) {
   if (kind < 0) return MLA_ERR_UNSUPPORTED;
   const int sms = num_sms();
   if (sms <= 0) return MLA_ERR_CUDA;
-  return kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
+  return attend_workers(kind, sms);
 }
 
 int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table, int max_pages,
@@ -255,15 +285,9 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   const int sms = num_sms();
-  const int workers = kind == 1 ? attend_tc_workers(sms) : attend_cc_workers(sms);
-  cudaError_t e;
-  if (kind == 1)
-    e = launch_attend_tc(ws + L.q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, B,
-                         scale, plan, workers, part_o, part_lse, err, stream);
-  else
-    e = launch_attend_cc(ws + L.q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B,
-                         scale, plan, workers, part_o, part_lse, err, stream);
-  return status_of(e);
+  const int workers = attend_workers(kind, sms);
+  return status_of(launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers,
+                                      part_o, part_lse, err, stream));
 }
 
 int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes, void* out,
@@ -451,6 +475,14 @@ int mla_wait_selftest(cudaStream_t stream) {
 }
 
 int mla_decode_kernel_kind(int H) { return attend_kind(H, MLA_FMT_BF16); }
+
+int mla_decode_select_kernel(int H, int kind) {
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if (H == 128) return kind == MLA_KERNEL_TCGEN05 ? MLA_OK : MLA_ERR_UNSUPPORTED;
+  if (kind != MLA_KERNEL_MMA && kind != MLA_KERNEL_CUDA_CORES) return MLA_ERR_UNSUPPORTED;
+  g_small_head_kernel.store(kind);
+  return MLA_OK;
+}
 
 const char* mla_status_string(int status) {
   switch (status) {

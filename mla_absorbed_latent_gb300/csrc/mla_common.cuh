@@ -260,6 +260,10 @@ cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, c
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_cc_workers(int num_sms);
+cudaError_t launch_attend_mma(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
+                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
+                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
+int attend_mma_workers(int num_sms);
 // Bv virtual rows of the query layout qs (q_cat: Bv / qs.NG * qs.T * qs.Hr flat rows)
 cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int Bv, float scale, int* plan,
@@ -270,7 +274,12 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
 // library-internal accessors (defined in mla_api.cu)
 int* device_error_word();            // this device's error word, nullptr on failure
 int device_sm_count();               // SMs of the current device, 0 on failure
-int attend_kernel_kind(int H, int fmt);  // 1 = tcgen05, 0 = CUDA cores, -1 = unsupported
+int attend_kernel_kind(int H, int fmt);  // an mla_kernel_t value, -1 = unsupported
+int attend_workers(int kind, int sms);   // persistent workers of that kernel
+// the single-query attend step with the kernel `kind` (B rows, H heads)
+cudaError_t launch_attend_kind(int kind, const void* q_cat, int H, const mla_cache_t* cache,
+                               const int32_t* page_table, int max_pages, int B, float scale, int* plan, int workers,
+                               uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 
 // Hv heads of the partials (virtual heads), Bv plan rows, query layout qs;
 // unabsorbed causal prefill (prefill.cu): expand the rows' latents into per-head

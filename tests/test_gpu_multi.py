@@ -143,18 +143,26 @@ def test_multi_quantized_pools(fmt):
         _check(prob, qn, qp, out, ol, T)
 
 
-def test_multi_h16_t1_matches_cuda_core_decode():
-    """T=1 at H=16 runs on the tensor cores (7 of 8 token lanes padding) and must
-    agree with the CUDA-core single-query decode and the oracle."""
+def test_multi_h16_t1_matches_single_query_decodes():
+    """T=1 at H=16 runs on the fifth-generation tensor cores (7 of 8 token lanes
+    padding) and must agree with the oracle and with both 16-head single-query
+    kernels (warp-level MMA, CUDA cores)."""
+    import mla_absorbed_latent_gb300 as mla
     seqlens = [1, 64, 65, 4096, 333]
     prob = make_problem(16, seqlens, seed=86)
     dev = DeviceDecode(prob)
     out, ol = _decode_q(dev, 1, prob.q_nope[:, None], prob.q_pe[:, None])
     _status_ok()
     _check(prob, prob.q_nope[:, None], prob.q_pe[:, None], out, ol, 1)
-    ref = _f64(dev.decode())
-    torch.cuda.synchronize()
-    assert_close(out[:, 0], ref, what="tcgen05 vs CUDA-core decode")
+    try:
+        for kind in (mla.MLA_KERNEL_MMA, mla.MLA_KERNEL_CUDA_CORES):
+            mla.mla_decode_select_kernel(16, kind)
+            ref = _f64(dev.decode())
+            torch.cuda.synchronize()
+            _status_ok()
+            assert_close(out[:, 0], ref, what=f"tcgen05 vs single-query kernel {kind}")
+    finally:
+        mla.mla_decode_select_kernel(16, mla.MLA_KERNEL_MMA)
 
 
 def test_multi_range_jump_is_exact():

@@ -95,3 +95,18 @@ def test_noalloc_rejects_batch_beyond_scratch():
     with pytest.raises(mla.MLAError) as e:
         mla.mla_decode_noalloc(big, big, dev.W_UK, dev.W_UV, 128, dev.cache, pt, 1, pt, B, prob.scale, big)
     assert e.value.status == mla.MLA_ERR_WORKSPACE
+
+
+def test_noalloc_16_head_kernels():
+    """H=16 with each 16-head attend kernel selected (warp-level MMA, CUDA
+    cores): the no-allocation call against the workspace decode with the same
+    kernel, twice."""
+    import mla_absorbed_latent_gb300 as mla
+    prob = make_problem(16, [700, 1, 64, 3000], seed=124)
+    dev = DeviceDecode(prob)
+    try:
+        for kind in (mla.MLA_KERNEL_MMA, mla.MLA_KERNEL_CUDA_CORES):
+            mla.mla_decode_select_kernel(16, kind)
+            _noalloc_twice_vs_workspace(prob, dev)
+    finally:
+        mla.mla_decode_select_kernel(16, mla.MLA_KERNEL_MMA)
