@@ -532,6 +532,153 @@ __global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, in
   }
 }
 
+// ---------------------------------------------------------------------------
+// The merge and the up-projection for few heads (the 16-head single-query
+// decode), on CUDA cores in fp32: the tensor-core kernel above gives each
+// (head, 16..32 rows) one CTA, only 32 CTAs for 16 heads and a 32-row batch, and
+// its chunk loop is then latency-bound.  Here one CTA per (head, group of 4
+// rows): W_UV[h] (128 KB) is copied into shared memory before the kernel waits
+// for the attention step; every warp of a row loads the row's segment
+// log-sum-exps in one round and forms the weights e^{LSE_s - LSE}; o_lat of each
+// row is the weighted sum of its segments' partials (the same formula), two rows
+// at a time in the two halves of the block; then out[b, h, :] =
+// W_UV[h] o_lat[b, h, :], 128 dot products of length 512 per row.
+// ---------------------------------------------------------------------------
+constexpr int SRB = 4;      // rows per CTA
+constexpr int SNT = 512;    // threads: two rows at a time in the merge (2 latent dims per thread), 8 output dims per warp after it
+
+struct __align__(16) SmallSmem {
+  uint16_t w[DV * DC];           // W_UV[h], 128 KB
+  float ol[SRB][DC];             // o_lat of the rows
+  uint64_t w_full;
+};
+
+__global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __restrict__ W_UV, int H, int B,
+                                                            const int* __restrict__ plan,
+                                                            const uint16_t* __restrict__ part_o,
+                                                            const float* __restrict__ part_lse,
+                                                            uint16_t* __restrict__ out, float* __restrict__ o_lat,
+                                                            int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  SmallSmem& S = *reinterpret_cast<SmallSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int h = blockIdx.x, b0 = blockIdx.y * SRB, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&S.w_full, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {  // W_UV[h] is a weight: its copy overlaps the attention step's tail
+    constexpr uint32_t CH = 32768;
+    mbar_arrive_expect_tx(&S.w_full, DV * DC * 2);
+    for (uint32_t o = 0; o < DV * DC * 2; o += CH)
+      bulk_g2s_hint(reinterpret_cast<uint8_t*>(S.w) + o, reinterpret_cast<const uint8_t*>(W_UV + (size_t)h * DV * DC) + o,
+                    CH, &S.w_full, policy_evict_last());
+  }
+  grid_dep_wait();  // the partials and their log-sum-exps
+  grid_dep_launch();
+  const long long T = plan[0], W = plan[1];
+  const int* prefix = plan + PLAN_HDR;
+  const int half = tid >> 8, ht = tid & 255;  // thread half (one row at a time), its thread
+  for (int r0 = 0; r0 < SRB; r0 += 2) {
+    const int r = r0 + half, b = b0 + r;
+    float a0 = 0.f, a1 = 0.f, den = 0.f;  // latent dims 2 ht, 2 ht + 1
+    if (b < B && prefix[b + 1] > prefix[b]) {
+      // segment w + b of row b for the workers w whose ranges hold its tiles (a
+      // worker without tiles left no partial: weight 0).  Every warp forms the
+      // weights itself, lane k those of segment c0 + k, and hands them out by
+      // shuffles: no block barrier.
+      const int sx = worker_of_tile(prefix[b], T, W) + b, sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
+      auto lse_of = [&](int sg) -> float {
+        const long long w = sg - b;
+        return worker_begin(w, T, W) == worker_begin(w + 1, T, W) ? -INFINITY : part_lse[(size_t)sg * H + h];
+      };
+      float l0 = sx + lane <= sy ? lse_of(sx + lane) : -INFINITY;  // the first 32 segments
+      float mx = l0;
+      for (int sg = sx + 32 + lane; sg <= sy; sg += 32) mx = fmaxf(mx, lse_of(sg));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const size_t stride = (size_t)H * DC / 2;  // one segment, in bf16 pairs
+      for (int c0 = sx; c0 <= sy; c0 += 32) {
+        const int cn = min(32, sy - c0 + 1);
+        const float lk = c0 == sx ? l0 : (lane < cn ? lse_of(c0 + lane) : -INFINITY);
+        const float e = lk == -INFINITY ? 0.f : expf(lk - mx);
+        const uint32_t* po = reinterpret_cast<const uint32_t*>(part_o + ((size_t)c0 * H + h) * DC) + ht;
+        int k = 0;
+        for (; k + 4 <= cn; k += 4) {  // four loads in flight
+          const float e0 = __shfl_sync(0xffffffffu, e, k), e1 = __shfl_sync(0xffffffffu, e, k + 1),
+                      e2 = __shfl_sync(0xffffffffu, e, k + 2), e3 = __shfl_sync(0xffffffffu, e, k + 3);
+          // a slot no worker wrote holds undefined bits: skipped, not weighted by 0
+          const uint32_t v0 = e0 != 0.f ? po[(k + 0) * stride] : 0u, v1 = e1 != 0.f ? po[(k + 1) * stride] : 0u,
+                         v2 = e2 != 0.f ? po[(k + 2) * stride] : 0u, v3 = e3 != 0.f ? po[(k + 3) * stride] : 0u;
+          a0 = fmaf(e0, bf16lo(v0), a0); a1 = fmaf(e0, bf16hi(v0), a1);
+          a0 = fmaf(e1, bf16lo(v1), a0); a1 = fmaf(e1, bf16hi(v1), a1);
+          a0 = fmaf(e2, bf16lo(v2), a0); a1 = fmaf(e2, bf16hi(v2), a1);
+          a0 = fmaf(e3, bf16lo(v3), a0); a1 = fmaf(e3, bf16hi(v3), a1);
+          den += (e0 + e1) + (e2 + e3);
+        }
+        for (; k < cn; ++k) {
+          const float ek = __shfl_sync(0xffffffffu, e, k);
+          const uint32_t v = ek != 0.f ? po[k * stride] : 0u;
+          a0 = fmaf(ek, bf16lo(v), a0);
+          a1 = fmaf(ek, bf16hi(v), a1);
+          den += ek;
+        }
+      }
+      const float inv = 1.f / den;  // den >= 1: the largest term is e^0
+      a0 *= inv;
+      a1 *= inv;
+    }
+    S.ol[r][2 * ht] = a0;
+    S.ol[r][2 * ht + 1] = a1;
+    if (o_lat != nullptr && b < B)
+      *reinterpret_cast<float2*>(o_lat + ((size_t)b * H + h) * DC + 2 * ht) = make_float2(a0, a1);
+  }
+  __syncthreads();
+  if (!mbar_wait(&S.w_full, 0)) {
+    if (tid == 0) raise_error(err, MLA_ERR_TIMEOUT, 150);
+    return;
+  }
+  // ---- out[b][h][j] = W_UV[h][j, :] . o_lat[b]: warp `warp` takes output dims
+  // 8 warp .. 8 warp + 7, lane `lane` latent dims 8 lane .. +7 and 256 + 8 lane .. +7
+  float x[SRB][16];
+#pragma unroll
+  for (int r = 0; r < SRB; ++r)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      x[r][k] = S.ol[r][8 * lane + k];
+      x[r][8 + k] = S.ol[r][256 + 8 * lane + k];
+    }
+#pragma unroll 4
+  for (int jj = 0; jj < 8; ++jj) {
+    const int j = 8 * warp + jj;
+    const uint4* wr = reinterpret_cast<const uint4*>(S.w + (size_t)j * DC);
+    const uint4 u0 = wr[lane], u1 = wr[32 + lane];
+    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float d[SRB];
+#pragma unroll
+    for (int r = 0; r < SRB; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc = fmaf(bf16lo(wv[k]), x[r][2 * k], acc);
+        acc = fmaf(bf16hi(wv[k]), x[r][2 * k + 1], acc);
+      }
+      d[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < SRB; ++r)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d[r] += __shfl_xor_sync(0xffffffffu, d[r], o);
+    if (lane < SRB && b0 + lane < B) {
+      float v = d[0];
+#pragma unroll
+      for (int r = 1; r < SRB; ++r) v = lane == r ? d[r] : v;
+      const __nv_bfloat16 ob = __float2bfloat16_rn(v);
+      out[((size_t)(b0 + lane) * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
+    }
+  }
+}
+
 template <int RB>
 cudaError_t launch_rb(const CUtensorMap& tm_w, const CUtensorMap& tm_p, const void* W_UV, int H, int B, const QSpec& qs,
                       const int* plan, const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
@@ -551,6 +698,17 @@ cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, co
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s) {
   if (Bv == 0) return cudaSuccess;
+  if (Hv < 128) {
+    // the 16-head single-query decode (its attend kernels compute the defined
+    // softmax themselves and flag no row, so no exact-recompute pass follows)
+    if (qs.T != 1 || qs.G != 1 || qs.NG != 1 || qs.Hr != Hv) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(SmallSmem) + 16;
+    cudaError_t e = cudaFuncSetAttribute(combine_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(combine_small_kernel, dim3(Hv, (Bv + SRB - 1) / SRB), dim3(SNT), smem, s,
+                      static_cast<const uint16_t*>(W_UV), Hv, Bv, plan, part_o, part_lse, static_cast<uint16_t*>(out),
+                      o_lat, err);
+  }
   CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
