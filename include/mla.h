@@ -166,15 +166,18 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  *                MLA_ERR_UNSUPPORTED if the tiles times the pairs exceed a grid)
  *   workspace  : device scratch of >= mla_cache_project_workspace_bytes(B, T,
  *                hidden, k_splits) bytes, 256-byte aligned (may be NULL when that
- *                is 0); cleared by the call itself, so calls that share one
- *                workspace must not overlap on the GPU
+ *                is 0); every byte the call reads it writes first (the split
+ *                pairs' partial payloads), so calls that share one workspace
+ *                must not overlap on the GPU
  * Per token, in fp32 from bf16 operands: y = wkv_a x (tensor cores, fp32
  * accumulation); c = y[0..511] / sqrt(mean(y[0..511]^2) + eps) * kv_norm_w;
  * pairs (2i, 2i+1) of y[512..575] rotated by the angle pos * rope_theta^(-2i/64)
  * (the angle reduced modulo 2 pi in fp64); each value rounded once to bf16,
- * then quantized exactly as mla_cache_append does.  With a K split the partial
- * products are summed by fp32 atomic adds, so the last bit of a value may vary
- * between runs; without one (many tokens) the result is deterministic.  Bad
+ * then quantized exactly as mla_cache_append does.  With a K split each pair's
+ * partial product goes to its own slice of the workspace and a second kernel
+ * (one CTA per token) sums the slices in split order before the same epilogue,
+ * so the result is deterministic either way (the split count can change the
+ * last bit of a value, being another fp32 summation order).  Bad
  * positions and page ids are skipped and raise MLA_ERR_BOUNDS as in
  * mla_cache_append.  x, wkv_a, kv_norm_w and latent_out 16-byte aligned.
  * Formats MLA_FMT_BF16, MLA_FMT_INT8 and MLA_FMT_INT4; the per-token INT8 and

@@ -21,11 +21,11 @@
 //
 // Few tokens (decode appends one per row) would leave most SMs idle and read
 // the 576 x hidden weight through two of them, so the hidden dimension is then
-// split over `ksplit` CTA pairs per token tile: each adds its partial product
-// into an fp32 accumulator in the caller's workspace (atomic adds: the
-// summation order, and so the last bit of a result, can vary between runs), and
-// the last pair to finish (a ticket counter per tile) loads the sums into its
-// tensor memory and runs the same epilogue.
+// split over `ksplit` CTA pairs per token tile: each stores its partial product
+// (fp32) into its own slice of the caller's workspace, and project_finish_kernel
+// (a CTA per token, chained by programmatic dependent launch) sums the slices in
+// split order and runs the same epilogue: deterministic, and the epilogue of
+// the few tokens spread over as many SMs.
 //
 // Thread roles (128 threads): lane 0 of warp 0 issues the TMA loads, lane 0 of
 // warp 1 the MMAs; then all four warps run the epilogue, warp w on the tokens
@@ -146,10 +146,11 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
                    const RopeFreq freq, int num_pages, uint8_t* __restrict__ pages,
                    const int32_t* __restrict__ page_table, int max_pages, const int32_t* __restrict__ pos, int T,
                    int ntok, int chunks, int ksplit, uint16_t* __restrict__ latent_out, float* __restrict__ acc,
-                   int* __restrict__ tickets, int* err) {
+                   int* err) {
   extern __shared__ uint8_t smem_raw[];
   PjSmem& S = *reinterpret_cast<PjSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_launch();  // a split projection's finishing kernel may start its prologue (it waits for this grid)
   const int rank = (int)cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   const int mt = pair / ksplit, split = pair - mt * ksplit;
@@ -241,57 +242,25 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 
   bool run = true;
   if (ksplit > 1) {
-    // add this pair's partial product into the tile's fp32 sums
-    float* arow = acc + (size_t)tok * DK;
+    // this pair's partial product into its own slice of the workspace, live
+    // token rows only; project_finish_kernel sums the slices in split order and
+    // runs the epilogue, a CTA per token
+    float* prow = acc + ((size_t)split * ntok + (live ? tok : 0)) * DK;
 #pragma unroll 1
     for (int cc = 0; cc < 9; ++cc) {
       uint32_t v[32];
-      tmem_ld32(trow + 32 * cc, v);
+      tmem_ld32(trow + 32 * cc, v);  // warp-wide: every lane loads
       tmem_ld_wait();
       if (live) {
         const int col = cc < 8 ? PJ_HALF * rank + 32 * cc : DC + PJ_ROPE * rank;
+        float4* dst = reinterpret_cast<float4*>(prow + col);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          red_add_v4(arow + col + 4 * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                               __uint_as_float(v[4 * q + 3]));
       }
     }
-    __threadfence();
-    fence_before_sync();
-    cluster_sync();  // both CTAs' adds are issued and fenced
-    if (rank == 0 && tid == 0) {
-      const int t = atomicAdd(tickets + mt, 1);
-      const int last = t == ksplit - 1 ? 1 : 0;
-      S.last = last;
-      st_cluster_u32(mapa(smem_u32(&S.last), 1u), (uint32_t)last);
-    }
-    cluster_sync();
-    run = S.last != 0;  // the same in both CTAs of the pair
-    fence_after_sync();
-    if (run) {
-      __threadfence();
-#pragma unroll 1
-      for (int cc = 0; cc < 9; ++cc) {
-        uint32_t v[32];
-        if (live) {
-          const int col = cc < 8 ? PJ_HALF * rank + 32 * cc : DC + PJ_ROPE * rank;
-          const float4* src = reinterpret_cast<const float4*>(arow + col);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 f = __ldcg(src + q);
-            v[4 * q] = __float_as_uint(f.x);
-            v[4 * q + 1] = __float_as_uint(f.y);
-            v[4 * q + 2] = __float_as_uint(f.z);
-            v[4 * q + 3] = __float_as_uint(f.w);
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = 0u;
-        }
-        tmem_st32(trow + 32 * cc, v);
-      }
-      tmem_st_wait();
-    }
+    run = false;
   }
 
   if (run) {
@@ -388,6 +357,93 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   }
 }
 
+// The epilogue of a split projection (few tokens): one CTA per token, one
+// thread per payload column.  The column's value is the sum of the ksplit pairs'
+// partials in split order (so the result does not depend on which pair finished
+// first); then, as in project_kernel: RMSNorm over the 512 latent columns with
+// the gain, the rotation of the RoPE key's pairs (2i, 2i+1), one bf16 rounding,
+// the page write (quantized per the pool's format) and the optional payload row.
+constexpr int PF_THREADS = DK;  // 576
+
+template <int FMT>
+__global__ void __launch_bounds__(PF_THREADS) project_finish_kernel(
+    const float* __restrict__ acc, int ksplit, int ntok, const uint16_t* __restrict__ kv_norm_w, float eps,
+    const RopeFreq freq, int num_pages, uint8_t* __restrict__ pages, const int32_t* __restrict__ page_table,
+    int max_pages, const int32_t* __restrict__ pos, int T, uint16_t* __restrict__ latent_out, int* err) {
+  __shared__ __align__(16) float y[DK];
+  __shared__ float red[PF_THREADS / 32];
+  const int tok = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  const float g = c < DC ? __uint_as_float((uint32_t)kv_norm_w[c] << 16) : 0.f;
+  grid_dep_wait();  // the partials of every pair
+  // the projection of column c: the pairs' partials, summed in split order
+  const float* a = acc + (size_t)tok * DK + c;
+  const size_t sstride = (size_t)ntok * DK;
+  float v = 0.f;
+  int s = 0;
+  for (; s + 8 <= ksplit; s += 8) {  // eight loads in flight
+    float q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = a[(s + k) * sstride];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v += q[k];
+  }
+  for (; s < ksplit; ++s) v += a[s * sstride];
+  // the token's slot in the pool (and the position its key is rotated by)
+  const int b = tok / T, t = tok - b * T;
+  const int p0 = pos[b];
+  const long long p = (long long)p0 + t;
+  uint8_t* page = nullptr;
+  int slot = 0;
+  if (p0 < 0 || p >= (long long)max_pages * PAGE) {
+    if (c == 0) raise_error(err, MLA_ERR_BOUNDS, b);
+  } else {
+    const int phys = page_table[(size_t)b * max_pages + (int)(p / PAGE)];
+    if (phys < 0 || phys >= num_pages) {
+      if (c == 0) raise_error(err, MLA_ERR_BOUNDS, phys);
+    } else {
+      constexpr size_t pb = FMT == MLA_FMT_BF16 ? PAGE_BYTES_BF16 : FMT == MLA_FMT_INT8 ? PAGE_BYTES_INT8 : PAGE_BYTES_INT4;
+      page = pages + (size_t)phys * pb;
+      slot = (int)(p % PAGE);
+    }
+  }
+  // RMSNorm: the sum of squares of the 512 latent columns (warps 0..15)
+  float ss = c < DC ? v * v : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (c < DC) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < DC / 32; ++w) tot += red[w];
+    const float rinv = rsqrtf(tot * (1.0f / DC) + eps);
+    y[c] = bf16r(v * rinv * g);
+  } else {
+    // RoPE key: pair (2i, 2i+1) is the lane pair (even, odd) of warps 16, 17
+    const int rc = c - DC, i = rc >> 1;
+    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+    float sn, cs;
+    rope_sincos((double)p, freq.f[i], &sn, &cs);
+    const float x0 = (rc & 1) ? other : v, x1 = (rc & 1) ? v : other;  // y[2i], y[2i+1] before the rotation
+    y[c] = bf16r((rc & 1) ? x0 * sn + x1 * cs : x0 * cs - x1 * sn);
+  }
+  __syncthreads();
+  if (latent_out != nullptr && c < DK / 8)
+    reinterpret_cast<uint4*>(latent_out + (size_t)tok * DK)[c] =
+        make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
+                   pack_bf16x2(y[8 * c + 4], y[8 * c + 5]), pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+  if (page != nullptr) {
+    if (FMT == MLA_FMT_BF16) {
+      if (c < DK / 8)
+        reinterpret_cast<uint4*>(page + (size_t)slot * DK * 2)[c] =
+            make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
+                       pack_bf16x2(y[8 * c + 4], y[8 * c + 5]), pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+    } else if (c < DK / 32) {
+      write_quantized32<FMT>(y + 32 * c, 32 * c, page, slot);
+    }
+  }
+}
+
 }  // namespace
 
 int project_splits(long long ntok, int hidden, int sms, int requested) {
@@ -397,15 +453,14 @@ int project_splits(long long ntok, int hidden, int sms, int requested) {
   if (requested > 0) return requested < chunks ? requested : chunks;
   if (2 * mtiles >= sms) return 1;
   const int want = (int)(sms / (2 * mtiles));
-  const int cap = chunks / 4 > 1 ? chunks / 4 : 1;  // at least four 64-wide chunks of hidden per pair
+  const int cap = chunks / 2 > 1 ? chunks / 2 : 1;  // at least two 64-wide chunks of hidden per pair
   const int k = want < cap ? want : cap;
   return k > 1 ? k : 1;
 }
 
 size_t project_workspace_bytes(long long ntok, int ksplit) {
   if (ksplit <= 1 || ntok <= 0) return 0;
-  const long long mtiles = (ntok + PJ_ROWS - 1) / PJ_ROWS;
-  return align_up((size_t)mtiles * PJ_ROWS * DK * 4, 256) + align_up((size_t)mtiles * 4, 256);
+  return align_up((size_t)ksplit * ntok * DK * 4, 256);  // one fp32 partial payload per (pair, token)
 }
 
 cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, const void* kv_norm_w, float eps,
@@ -429,18 +484,10 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
     return cudaErrorInvalidValue;
   RopeFreq fr;
   for (int i = 0; i < DR / 2; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / DR);
-  float* acc = nullptr;
-  int* tickets = nullptr;
-  if (ksplit > 1) {
-    const size_t acc_bytes = align_up((size_t)mtiles * PJ_ROWS * DK * 4, 256);
-    acc = static_cast<float*>(workspace);
-    tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + acc_bytes);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, project_workspace_bytes(ntok, ksplit), s);
-    if (e != cudaSuccess) return e;
-  }
+  float* acc = ksplit > 1 ? static_cast<float*>(workspace) : nullptr;
   const size_t smem = sizeof(PjSmem) + 1024;
   void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, const uint16_t*, float, RopeFreq, int, uint8_t*,
-                 const int32_t*, int, const int32_t*, int, int, int, int, uint16_t*, float*, int*, int*) =
+                 const int32_t*, int, const int32_t*, int, int, int, int, uint16_t*, float*, int*) =
       fmt == MLA_FMT_BF16 ? project_kernel<MLA_FMT_BF16>
       : fmt == MLA_FMT_INT8 ? project_kernel<MLA_FMT_INT8>
                             : project_kernel<MLA_FMT_INT4>;
@@ -458,9 +505,19 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_wc, tm_wr, static_cast<const uint16_t*>(kv_norm_w), eps, fr,
-                            num_pages, static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, (int)ntok,
-                            chunks, ksplit, static_cast<uint16_t*>(latent_out), acc, tickets, err);
+  e = cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_wc, tm_wr, static_cast<const uint16_t*>(kv_norm_w), eps, fr, num_pages,
+                         static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, (int)ntok, chunks, ksplit,
+                         static_cast<uint16_t*>(latent_out), acc, err);
+  if (e != cudaSuccess || ksplit <= 1) return e;
+  void (*finish)(const float*, int, int, const uint16_t*, float, RopeFreq, int, uint8_t*, const int32_t*, int,
+                 const int32_t*, int, uint16_t*, int*) =
+      fmt == MLA_FMT_BF16 ? project_finish_kernel<MLA_FMT_BF16>
+      : fmt == MLA_FMT_INT8 ? project_finish_kernel<MLA_FMT_INT8>
+                            : project_finish_kernel<MLA_FMT_INT4>;
+  return launch_pdl(finish, dim3((unsigned)ntok), dim3(PF_THREADS), 0, s, static_cast<const float*>(acc), ksplit,
+                    (int)ntok, static_cast<const uint16_t*>(kv_norm_w), eps, fr, num_pages,
+                    static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, static_cast<uint16_t*>(latent_out),
+                    err);
 }
 
 }  // namespace mla

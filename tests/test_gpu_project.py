@@ -132,7 +132,8 @@ def test_project_quantized_pool_bitexact(fmt):
 
 def test_project_v3_decode_shape():
     """DeepSeek-V3 width (hidden 7168), one new token for each of 64 rows at seeded
-    positions up to 8191 (the decode-time append: one tile, K split over pairs)."""
+    positions up to 8191 (the decode-time append: one tile, K split over pairs,
+    the pairs' partials summed in split order: bit-identical on a second call)."""
     pos0 = np.random.default_rng(33).integers(0, 8192, size=64).astype(np.int32)
     p = Produced(7168, B=64, T=1, pos0=pos0, seed=33)
     nbytes = p.run()
@@ -140,6 +141,9 @@ def test_project_v3_decode_shape():
     assert _status() == (0, 0)
     _check_rows(p)
     assert np.array_equal(p.pool_bytes(), p.expected_pool())
+    first = _np_bf16(p.latent).copy()
+    p.run()
+    assert np.array_equal(_np_bf16(p.latent), first)
 
 
 def test_project_v3_prefill_many_tiles():

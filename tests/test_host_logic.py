@@ -84,7 +84,7 @@ int main() {
           } else if (2 * mtiles >= sms) {
             CHECK(k == 1, "ntok=%lld sms=%d k=%d", ntok, sms, k);
           } else {
-            const long long cap = chunks / 4 > 1 ? chunks / 4 : 1;
+            const long long cap = chunks / 2 > 1 ? chunks / 2 : 1;  // at least two 64-wide chunks per pair
             const long long want = sms / (2 * mtiles);
             CHECK(k <= cap && k <= (want > 1 ? want : 1), "ntok=%lld hidden=%d sms=%d k=%d", ntok, hidden, sms, k);
           }
@@ -95,8 +95,8 @@ int main() {
           if (k == 1) {
             CHECK(ws == 0, "ntok=%lld", ntok);
           } else {
-            CHECK(ws >= (size_t)mtiles * 128 * DK * 4 + (size_t)mtiles * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok,
-                  k);
+            // one fp32 partial payload per (pair, token)
+            CHECK(ws >= (size_t)k * ntok * DK * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok, k);
           }
         }
   // 4. the no-allocation decode's worker count: the largest count <= want whose
