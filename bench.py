@@ -8,7 +8,12 @@ table (603,979,776 cache bytes per step, larger than the 129 MB L2, so no
 flush is needed between steps).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--fmt bf16|int8|int4]
+                  [--workload NAME] [--fmt FORMAT] [--q-len T] [--h16-kernel mma|cuda_cores]
+
+Other workloads (--workload): the V2-Lite batch and the ragged / quantized V3
+decodes, several query tokens per row (v2lite_mtp, v3_mtp), the unabsorbed
+prefill (v2lite_prefill, v3_prefill), the output projection (v2lite_oproj,
+v3_oproj) and the fused cache producer (v3_project_prefill, v3_project_decode).
 
 --impl reference times the fp64 CPU oracle on this host's cores on a bounded
 sample of the same workload (the only place the bench runs the oracle, with
