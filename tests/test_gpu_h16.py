@@ -162,3 +162,25 @@ def test_h16_extreme_scores_are_exact(kind, select):
     assert_close(_f64(dev.out)[0], ref)
     assert_close(o_lat[0].cpu().numpy(), ref_lat, what="o_lat")
     assert_close(_f64(dev.out)[1], oracle_rows(prob, [1])[1][0], what="out[1]")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_h16_long_row_many_segments(kind, select):
+    """One 40,000-token row (625 pages) beside short rows: every split worker takes
+    a piece of the long row, so its merge has more than 32 segments (the merge's
+    weights go out in chunks of 32) and the short rows sit inside one worker's
+    range.  Out and o_lat of every row against the oracle."""
+    select(kind)
+    seqlens = [40000, 3, 64, 1000]
+    prob = make_problem(16, seqlens, seed=125)
+    dev = DeviceDecode(prob)
+    o_lat = torch.empty((prob.B, 16, 512), dtype=torch.float32, device="cuda")
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    ref = oracle_rows(prob, range(prob.B))
+    got = _f64(dev.out)
+    lat = o_lat.cpu().numpy().astype(np.float64)
+    for b in range(prob.B):
+        assert_close(got[b], ref[b][0], what=f"out[{b}]")
+        assert_close(lat[b], ref[b][1], what=f"o_lat[{b}]")
