@@ -46,7 +46,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "absorbed-MLA decode latent-cache GB/s (% HBM peak) and queries/s, 1 GB300"
-BYTES_PER_TOKEN = {"bf16": 1152, "int8": 624, "int4": 400, "int8_token": 624, "int4_sym": 400}
+BYTES_PER_TOKEN = {"bf16": 1152, "int8": 624, "int4": 400, "int8_token": 624, "int4_sym": 400, "int4_pe4": 400}
 DESCR = {
     "v2lite_batch": "V2-Lite shape decode: H=16, B=32, seqlen 4096, contiguous bf16 latent cache",
     "v3_paged": "DeepSeek-V3 shape decode: H=128, B=64, seqlen 8192, paged bf16 latent cache "

@@ -72,7 +72,8 @@ typedef enum {
   MLA_FMT_INT8 = 1,       /* c_KV INT8 per 32-channel group, k_pe INT8 per 8, bf16 scales */
   MLA_FMT_INT4 = 2,       /* c_KV asymmetric INT4 per 32 (bf16 scale + zero), k_pe INT8/8 */
   MLA_FMT_INT8_TOKEN = 3, /* c_KV INT8 with one scale per token, k_pe INT8/8 (INT8 pages) */
-  MLA_FMT_INT4_SYM = 4    /* c_KV symmetric INT4 per 32, k_pe INT8/8 (INT4 pages)         */
+  MLA_FMT_INT4_SYM = 4,   /* c_KV symmetric INT4 per 32, k_pe INT8/8 (INT4 pages)         */
+  MLA_FMT_INT4_PE4 = 5    /* c_KV asymmetric INT4 per 32, k_pe symmetric INT4/8 (INT4 pages) */
 } mla_fmt_t;
 
 /*
@@ -101,6 +102,12 @@ typedef enum {
  *   MLA_FMT_INT4_SYM (INT4 pages): per 32-channel group s = bf16_rne(amax / 7),
  *     q = clamp(rint(x / s), -7, 7) (0 when s == 0), stored as the nibble q + 8
  *     with zero = -8 s (exact in bf16), so that code * s + zero = q * s.
+ *   MLA_FMT_INT4_PE4 (INT4 pages): c_KV as MLA_FMT_INT4; the RoPE key symmetric
+ *     INT4 per 8-dim group ("k_pe 对称 INT4 (8块)"): s = bf16_rne(amax / 7),
+ *     q = clamp(rint(x / s), -7, 7) (0 when s == 0), stored as INT8 codes in
+ *     the page's k_pe code section with s in its k_pe scale slot, so x^ = q * s
+ *     as for the INT8 RoPE key (4 bits of precision in an 8-bit slot: the
+ *     quantizer's accuracy, not its smaller footprint).
  * (One scale for the whole tensor cannot serve an append-only cache: it would
  * change as tokens arrive.)
  */

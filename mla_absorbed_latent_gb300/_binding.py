@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, -1, -2, -3
 MLA_ERR_BOUNDS, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = -4, -5, -6
-FMT = {"bf16": 0, "int8": 1, "int4": 2, "int8_token": 3, "int4_sym": 4}
+FMT = {"bf16": 0, "int8": 1, "int4": 2, "int8_token": 3, "int4_sym": 4, "int4_pe4": 5}
 D_C, D_R, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # the fixed scratch of mla_decode_noalloc
 MLA_KERNEL_CUDA_CORES, MLA_KERNEL_TCGEN05, MLA_KERNEL_MMA = 0, 1, 2  # mla_kernel_t

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256) append_kernel(int fmt, int num_pages, uin
     float x[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
                   bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
     int8_t code[8];
-    const uint16_t sb = quant_i8<8>(x, code);
+    const uint16_t sb = fmt == MLA_FMT_INT4_PE4 ? quant_i4sym_i8<8>(x, code) : quant_i8<8>(x, code);
     store_i8x8(page + pe_code_off + slot * DR + g * 8, code);
     reinterpret_cast<uint16_t*>(page + pe_scale_off)[slot * 8 + g] = sb;
   }

@@ -50,7 +50,7 @@ int num_sms() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool heads_ok(int H) { return H == 16 || H == 128; }
-bool fmt_ok(int fmt) { return fmt >= MLA_FMT_BF16 && fmt <= MLA_FMT_INT4_SYM; }
+bool fmt_ok(int fmt) { return fmt >= MLA_FMT_BF16 && fmt <= MLA_FMT_INT4_PE4; }
 // hidden width of the cache producer's input: whole 64-wide chunks of the projection's K
 bool hidden_ok(int hidden) { return hidden >= 64 && hidden <= 65536 && hidden % 64 == 0; }
 // the producer indexes tokens with 32-bit integers

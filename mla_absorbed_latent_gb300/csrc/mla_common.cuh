@@ -25,9 +25,10 @@ constexpr size_t PAGE_BYTES_INT8 = (size_t)PAGE * (DC + DR + 2 * 16 + 2 * 8);   
 constexpr size_t PAGE_BYTES_INT4 = (size_t)PAGE * (DC / 2 + DR + 4 * 16 + 2 * 8);  // 25,600
 
 // the page layout (and decode kernel) a cache format uses: the per-token INT8
-// and symmetric INT4 quantizers write INT8 and INT4 pages
+// quantizer writes INT8 pages, the symmetric INT4 latent and the INT4 RoPE key
+// quantizers INT4 pages
 __host__ __device__ constexpr int layout_fmt(int fmt) {
-  return fmt == MLA_FMT_INT8_TOKEN ? MLA_FMT_INT8 : fmt == MLA_FMT_INT4_SYM ? MLA_FMT_INT4 : fmt;
+  return fmt == MLA_FMT_INT8_TOKEN ? MLA_FMT_INT8 : (fmt == MLA_FMT_INT4_SYM || fmt == MLA_FMT_INT4_PE4) ? MLA_FMT_INT4 : fmt;
 }
 
 // section offsets inside a quantized page

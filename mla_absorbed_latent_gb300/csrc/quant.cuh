@@ -4,7 +4,7 @@
 // bf16-representable inputs, so the codes and scales are bit-exact and
 // deterministic: INT8 over 32-channel groups of c_KV and 8-dim groups of k_pe,
 // asymmetric INT4 (scale + zero) over 32-channel groups of c_KV, and the
-// per-token INT8 and symmetric INT4 variants
+// per-token INT8, symmetric INT4 and 4-bit RoPE-key variants
 // ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化" §3.2 names the block sizes; the
 // rounding rules are the library's, stated in include/mla.h).
 #pragma once
@@ -83,6 +83,25 @@ __device__ __forceinline__ void quant_i4sym_32(const float* x, uint32_t* w, uint
   }
   *scale_bits = __bfloat16_as_ushort(sb);
   *zero_bits = __bfloat16_as_ushort(__float2bfloat16_rn(-8.f * s));  // exact: a power-of-two multiple
+}
+
+// Symmetric INT4 of N values as INT8 codes (-7..7): returns the bf16 scale bits
+// (s = bf16(amax / 7)); the 4-bit RoPE-key quantizer, stored in the INT8 code
+// section of a page
+template <int N>
+__device__ __forceinline__ uint16_t quant_i4sym_i8(const float* x, int8_t* code) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const __nv_bfloat16 sb = __float2bfloat16_rn(amax / 7.0f);
+  const float s = __bfloat162float(sb);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float q = 0.f;
+    if (s != 0.f) q = fminf(fmaxf(rintf(x[i] / s), -7.f), 7.f);
+    code[i] = static_cast<int8_t>(q);
+  }
+  return __bfloat16_as_ushort(sb);
 }
 
 __device__ __forceinline__ void store_i8x8(uint8_t* dst, const int8_t* c) {

@@ -443,10 +443,12 @@ PAGE_LAYOUT = {
              ("c_scale", "bf16", (D_C // 32,)), ("c_zero", "bf16", (D_C // 32,)),
              ("pe_scale", "bf16", (D_R // 8,))],
 }
-# the per-token INT8 and symmetric INT4 quantizers of [report] §3.2 write the
-# INT8 and INT4 page layouts (the library's reading: one page form per code width)
+# the per-token INT8, symmetric INT4 and 4-bit k_pe quantizers of [report] §3.2
+# write the INT8 and INT4 page layouts (the library's reading: one page form per
+# code width; the 4-bit k_pe codes -7..7 sit in the INT8 k_pe code section)
 PAGE_LAYOUT["int8_token"] = PAGE_LAYOUT["int8"]
 PAGE_LAYOUT["int4_sym"] = PAGE_LAYOUT["int4"]
+PAGE_LAYOUT["int4_pe4"] = PAGE_LAYOUT["int4"]
 _ELEM = {"bf16": 2, "i8": 1, "u4x2": 1}
 
 
@@ -473,12 +475,13 @@ def quantize_token(fmt: str, c_kv, k_pe):
     p = np.asarray(k_pe, np.float32)
     if fmt == "bf16":
         return {"tok": bf16_to_bits(np.concatenate([c, p], axis=1))}
-    pc, ps = quantize_int8(p, 8)
+    # k_pe: INT8 in 8-dim groups, or symmetric INT4 in 8-dim groups ("k_pe 对称 INT4 (8块)")
+    pc, ps = quantize_int4_sym(p, 8) if fmt == "int4_pe4" else quantize_int8(p, 8)
     if fmt == "int8":
         cc, cs = quantize_int8(c, 32)
         return {"c_code": cc, "pe_code": pc, "c_scale": bf16_to_bits(cs),
                 "pe_scale": bf16_to_bits(ps)}
-    if fmt == "int4":
+    if fmt in ("int4", "int4_pe4"):
         cc, cs, cz = quantize_int4_asym(c, 32)
         return {"c_code": pack_nibbles(cc), "pe_code": pc, "c_scale": bf16_to_bits(cs),
                 "c_zero": bf16_to_bits(cz), "pe_scale": bf16_to_bits(ps)}
@@ -502,8 +505,12 @@ def dequantized_tokens(fmt: str, c_kv, k_pe):
     p = np.asarray(k_pe, np.float32)
     if fmt == "bf16":
         return c.astype(np.float64), p.astype(np.float64)
-    pc, ps = quantize_int8(p, 8)
-    pe = dequantize_int8(pc, ps, 8)
+    if fmt == "int4_pe4":
+        pc, ps = quantize_int4_sym(p, 8)
+        pe = dequantize_int4_sym(pc, ps, 8)
+    else:
+        pc, ps = quantize_int8(p, 8)
+        pe = dequantize_int8(pc, ps, 8)
     if fmt == "int8":
         cc, cs = quantize_int8(c, 32)
         return dequantize_int8(cc, cs, 32), pe

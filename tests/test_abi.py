@@ -42,6 +42,11 @@ def test_page_bytes(lib):
     assert lib.mla_cache_page_bytes(0) == 64 * 1152
     assert lib.mla_cache_page_bytes(1) == 64 * 624
     assert lib.mla_cache_page_bytes(2) == 64 * 400
+    # the quantizer variants write the INT8 / INT4 page layouts
+    assert lib.mla_cache_page_bytes(3) == 64 * 624
+    assert lib.mla_cache_page_bytes(4) == 64 * 400
+    assert lib.mla_cache_page_bytes(5) == 64 * 400
+    assert lib.mla_cache_page_bytes(6) == 0
     assert lib.mla_cache_page_bytes(7) == 0
 
 

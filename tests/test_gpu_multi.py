@@ -130,7 +130,7 @@ def test_multi_h128_t2():
     _check(prob, qn, qp, out, ol, T)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_multi_quantized_pools(fmt):
     """Causal multi-query decode over INT8 / INT4 pools (H=16, T=5; H=128, T=2)."""
     for H, T, seed in ((16, 5, 84), (128, 2, 85)):

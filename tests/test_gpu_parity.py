@@ -57,7 +57,7 @@ def _expected_pool(prob, writes):
     return O.expected_page_pool(prob.fmt, prob.num_pages, writes)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_append_prefill_then_decode_bitexact(fmt):
     """V2-Lite tiny case: 25-token prefill append, then the decode token at position 25."""
     w = synth.get_workload("v2lite_tiny")
@@ -69,7 +69,7 @@ def test_append_prefill_then_decode_bitexact(fmt):
     assert np.array_equal(_pool_bytes(dev), want)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_append_ragged_paged_bitexact(fmt):
     """Several rows, random page table, appends that start mid-page and cross pages."""
     import mla_absorbed_latent_gb300 as mla
@@ -247,7 +247,7 @@ def test_decode_v3_ragged_full():
     _check_all_rows(dev)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_decode_quant_ragged_edges(fmt):
     """H=128 over INT8 / INT4 pages (dequantized in the load stage): lengths
     around the page edges, an empty row, outlier channels; against the oracle
@@ -478,7 +478,7 @@ def test_decode_large_half_scores_are_exact():
     _check_rows(dev, [1, 2])
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_decode_quant_range_jump_is_exact(fmt):
     """H=128 over quantized pools: one token's RoPE key (in its INT8 k_pe codes)
     turned into 127 x sign(q_pe) of one head, scale 2, so that head's score jumps

@@ -725,7 +725,7 @@ def test_generator_page_tables_and_lengths():
 
 
 def test_variant_pool_sections():
-    """The per-token INT8 and symmetric INT4 quantizers in their page images,
+    """The per-token INT8, symmetric INT4 and 4-bit RoPE-key quantizers in their page images,
     indexed by hand: per-token INT8 keeps the INT8 layout with the token's one
     scale s = bf16(amax / 127) in all 16 group-scale slots; symmetric INT4 keeps
     the INT4 layout with nibbles q + 8 and zero = -8 s, so that code * s + zero
@@ -755,3 +755,18 @@ def test_variant_pool_sections():
     g = np.repeat(np.arange(16), 32)
     assert np.array_equal(codes * sc[g].astype(np.float64) + zr[g], q[0] * s[0][g].astype(np.float64))
     assert np.array_equal(O.dequantized_tokens("int4_sym", c, p)[0][0], q[0] * s[0][g].astype(np.float64))
+    # 4-bit RoPE key (symmetric INT4 in 8-dim groups) in the INT4 layout, slot 5: the
+    # latent sections are those of the plain INT4 image, the k_pe codes are -7..7 in
+    # the INT8 k_pe section with s = bf16(amax / 7) in the k_pe scale slots
+    pool4 = O.expected_page_pool("int4", 1, [(np.array([0]), 5, c, p)])[0]
+    pool = O.expected_page_pool("int4_pe4", 1, [(np.array([0]), 5, c, p)])[0]
+    assert np.array_equal(pool[:16384], pool4[:16384])                    # c codes
+    assert np.array_equal(pool[20480:24576], pool4[20480:24576])          # c scales and zeros
+    kq = pool[16384 + 5 * 64:16384 + 6 * 64].view(np.int8)
+    ks = synth.bf16_bits_to_f32(pool[24576 + 5 * 16:24576 + 6 * 16].view(np.uint16))
+    amax = np.max(np.abs(p[0].reshape(8, 8)), axis=1)
+    assert np.array_equal(ks, O.bf16_round(amax / np.float32(7.0)))
+    assert np.all(np.abs(kq) <= 7) and np.max(np.abs(kq)) == 7
+    assert np.all(np.abs(kq.astype(np.float64) * np.repeat(ks, 8) - p[0]) <= np.repeat(ks, 8) / 2 + 1e-12)
+    assert np.array_equal(O.dequantized_tokens("int4_pe4", c, p)[1][0], kq * np.repeat(ks, 8).astype(np.float64))
+    assert np.array_equal(O.dequantized_tokens("int4_pe4", c, p)[0], O.dequantized_tokens("int4", c, p)[0])

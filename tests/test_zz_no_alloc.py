@@ -76,7 +76,7 @@ def test_noalloc_fewer_workers_than_decode():
         assert_close(got[b], ref[b], what=f"noalloc out[{b}]")
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym"])
+@pytest.mark.parametrize("fmt", ["int8", "int4", "int8_token", "int4_sym", "int4_pe4"])
 def test_noalloc_quantized_pools(fmt):
     """H=128 over INT8 / INT4 pools through the no-allocation entry point,
     against the workspace decode on two calls in a row."""
