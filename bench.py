@@ -770,7 +770,7 @@ def run_project(args, name, fmt):
         "cpu_baseline": cpu,
         "e2e": {"value": ntok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h_x.numel() * 2,
                 "d2h_bytes_per_step": h_lat.numel() * 2},
-        "gpu_launches": (2 if ws_bytes > 0 else 1) * args.steps,  # the producer (and the workspace clear)
+        "gpu_launches": (2 if ws_bytes > 0 else 1) * args.steps,  # the projection (and the finishing kernel of a split)
         "clocks": clock_info,
     }
     print(json.dumps(line), flush=True)

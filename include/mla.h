@@ -168,9 +168,12 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  *   latent_out : NULL, or bf16 [B][T][576]: receives each token's payload
  *                before quantization (c_kv then k_pe, the bf16 values a bf16
  *                pool would hold), whether or not its page write succeeded
- *   k_splits   : 0 picks the split of the projection's K dimension by size;
- *                n > 0 forces n CTA pairs per 128-token tile (capped at hidden/64;
- *                MLA_ERR_UNSUPPORTED if the tiles times the pairs exceed a grid)
+ *   k_splits   : 0 picks the kernel and the split of the projection's K
+ *                dimension by size (at most 64 tokens in all: a warp-level MMA
+ *                kernel, one CTA per 64 output columns and hidden slice of at
+ *                most 512); n > 0 forces the tcgen05 kernel with n CTA pairs
+ *                per 128-token tile (capped at hidden/64; MLA_ERR_UNSUPPORTED if
+ *                the tiles times the pairs exceed a grid)
  *   workspace  : device scratch of >= mla_cache_project_workspace_bytes(B, T,
  *                hidden, k_splits) bytes, 256-byte aligned (may be NULL when that
  *                is 0); every byte the call reads it writes first (the split
@@ -180,7 +183,7 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  * accumulation); c = y[0..511] / sqrt(mean(y[0..511]^2) + eps) * kv_norm_w;
  * pairs (2i, 2i+1) of y[512..575] rotated by the angle pos * rope_theta^(-2i/64)
  * (the angle reduced modulo 2 pi in fp64); each value rounded once to bf16,
- * then quantized exactly as mla_cache_append does.  With a K split each pair's
+ * then quantized exactly as mla_cache_append does.  With a K split each CTA's
  * partial product goes to its own slice of the workspace and a second kernel
  * (one CTA per token) sums the slices in split order before the same epilogue,
  * so the result is deterministic either way (the split count can change the

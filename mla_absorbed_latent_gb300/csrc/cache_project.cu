@@ -35,6 +35,7 @@
 
 #include "quant.cuh"
 #include "tc_ptx.cuh"
+#include "warp_mma.cuh"
 
 namespace mla {
 namespace {
@@ -357,6 +358,95 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// At most 64 tokens (a decode-time append): the projection on the warp-level
+// tensor-core instruction, without clusters or tensor memory.  One CTA per (64
+// output columns, slice of the hidden dimension): its weight block [64
+// columns][slice] and the tokens' block [64 tokens][slice] arrive by TMA
+// (128B-swizzled 64 x 64 tiles, all at once), warp w multiplies tokens
+// 16 (w % 4) .. + 15 by columns 32 (w / 4) .. + 31 with mma.sync m16n8k16, and
+// the CTA stores its fp32 partial [tokens][64 columns] into its workspace
+// slice; project_finish_kernel sums the slices and runs the epilogue.
+// ---------------------------------------------------------------------------
+constexpr int PS_TOK = 64;           // tokens (the MMA's M: 4 tiles of 16)
+constexpr int PS_COLS = 64;          // output columns per CTA
+constexpr int PS_NG = DK / PS_COLS;  // 9 column groups (the last: the RoPE key)
+constexpr int PS_MAXCH = 8;          // 64-wide hidden chunks per CTA
+constexpr uint32_t PS_TILE = 64 * 128;  // 8 KB: 64 rows of 64 bf16
+
+struct __align__(1024) PsSmem {
+  uint8_t w[PS_MAXCH][PS_TILE];
+  uint8_t x[PS_MAXCH][PS_TILE];
+  uint64_t full[PS_MAXCH];  // chunk i's weight and token tiles have landed
+};
+
+__global__ void __launch_bounds__(256) project_small_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                            const __grid_constant__ CUtensorMap tm_w, int ntok,
+                                                            int chunks, int ksplit, float* __restrict__ acc,
+                                                            int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  PsSmem& S = *reinterpret_cast<PsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  grid_dep_launch();  // the finishing kernel may start its prologue (it waits for this grid)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cg = blockIdx.x, split = blockIdx.y;
+  const int c_begin = (int)((long long)split * chunks / ksplit);
+  const int nk = (int)((long long)(split + 1) * chunks / ksplit) - c_begin;  // 1..PS_MAXCH (host's choice)
+  if (tid == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_w);
+    for (int i = 0; i < PS_MAXCH; ++i) mbar_init(&S.full[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint64_t pol_w = policy_evict_first();  // the weight is read once per call
+    for (int i = 0; i < nk; ++i) {
+      const int k = (c_begin + i) * 64;
+      mbar_arrive_expect_tx(&S.full[i], 2u * PS_TILE);
+      tma_load_3d_hint(S.w[i], &tm_w, k, PS_COLS * cg, 0, &S.full[i], pol_w);
+      tma_load_3d(S.x[i], &tm_x, k, 0, 0, &S.full[i]);  // token rows past ntok read as zeros
+    }
+  }
+  const int mt = warp & 3, nh = warp >> 2;  // token tile, column half
+  float d[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll 1
+  for (int i = 0; i < nk; ++i) {
+    if (!mbar_wait(&S.full[i], 0)) {  // bounded
+      if (lane == 0) raise_error(err, MLA_ERR_TIMEOUT, 30);
+      for (int j = i + 1; j < nk; ++j) mbar_wait(&S.full[j], 0);  // the later copies, again bounded
+      return;
+    }
+    const uint32_t xb = smem_u32(S.x[i]), wb = smem_u32(S.w[i]);
+#pragma unroll
+    for (int kp = 0; kp < 2; ++kp) {
+      // A: tokens 16 mt + (lane % 16), dims 32 kp + 16 h + 8 (lane / 16) of k-step h;
+      // B: columns 32 nh + 8 j + (lane % 8), dims 32 kp + 8 (lane / 8) (two k-steps)
+      uint32_t a[2][4], b[4][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) ldsm_x4(a[h], xb + sw128(16 * mt + (lane & 15), 4 * kp + 2 * h + (lane >> 4)));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ldsm_x4(b[j], wb + sw128(32 * nh + 8 * j + (lane & 7), 4 * kp + (lane >> 3)));
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_bf16_16816(d[j], a[h], b[j][2 * h], b[j][2 * h + 1]);
+    }
+  }
+  // the partial: token rows 16 mt + g, + 8; columns 64 cg + 32 nh + 8 j + 2 t, + 1
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int tok = 16 * mt + g + 8 * r;
+    if (tok < ntok) {
+      float* row = acc + ((size_t)split * ntok + tok) * DK + PS_COLS * cg + 32 * nh + 2 * t;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<float2*>(row + 8 * j) = make_float2(d[j][2 * r], d[j][2 * r + 1]);
+    }
+  }
+}
+
 // The epilogue of a split projection (few tokens): one CTA per token, one
 // thread per payload column.  The column's value is the sum of the ksplit pairs'
 // partials in split order (so the result does not depend on which pair finished
@@ -374,21 +464,9 @@ __global__ void __launch_bounds__(PF_THREADS) project_finish_kernel(
   __shared__ float red[PF_THREADS / 32];
   const int tok = blockIdx.x, c = threadIdx.x, lane = c & 31, warp = c >> 5;
   const float g = c < DC ? __uint_as_float((uint32_t)kv_norm_w[c] << 16) : 0.f;
-  grid_dep_wait();  // the partials of every pair
-  // the projection of column c: the pairs' partials, summed in split order
-  const float* a = acc + (size_t)tok * DK + c;
-  const size_t sstride = (size_t)ntok * DK;
-  float v = 0.f;
-  int s = 0;
-  for (; s + 8 <= ksplit; s += 8) {  // eight loads in flight
-    float q[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) q[k] = a[(s + k) * sstride];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v += q[k];
-  }
-  for (; s < ksplit; ++s) v += a[s * sstride];
-  // the token's slot in the pool (and the position its key is rotated by)
+  // the token's slot in the pool (and the position its key is rotated by):
+  // inputs of the call, read before the wait (the kernel before this one in
+  // the stream writes only the partials)
   const int b = tok / T, t = tok - b * T;
   const int p0 = pos[b];
   const long long p = (long long)p0 + t;
@@ -406,6 +484,28 @@ __global__ void __launch_bounds__(PF_THREADS) project_finish_kernel(
       slot = (int)(p % PAGE);
     }
   }
+  grid_dep_wait();  // the partials of every split
+  // the projection of column c: the splits' partials, summed in split order
+  const float* a = acc + (size_t)tok * DK + c;
+  const size_t sstride = (size_t)ntok * DK;
+  float v = 0.f;
+  int s = 0;
+  for (; s + 16 <= ksplit; s += 16) {  // sixteen loads in flight
+    float q[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) q[k] = a[(s + k) * sstride];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v += q[k];
+  }
+  if (s + 8 <= ksplit) {
+    float q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) q[k] = a[(s + k) * sstride];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v += q[k];
+    s += 8;
+  }
+  for (; s < ksplit; ++s) v += a[s * sstride];
   // RMSNorm: the sum of squares of the 512 latent columns (warps 0..15)
   float ss = c < DC ? v * v : 0.f;
 #pragma unroll
@@ -458,6 +558,19 @@ int project_splits(long long ntok, int hidden, int sms, int requested) {
   return k > 1 ? k : 1;
 }
 
+int project_small_splits(int hidden, int sms) {
+  const int chunks = hidden / 64;
+  int k = sms / PS_NG;  // about one CTA per SM
+  const int need = (chunks + PS_MAXCH - 1) / PS_MAXCH;  // at most PS_MAXCH chunks per CTA
+  if (k < need) k = need;
+  if (k > chunks) k = chunks;
+  return k > 1 ? k : 1;
+}
+
+size_t project_small_workspace_bytes(long long ntok, int ksplit) {
+  return ntok <= 0 ? 0 : align_up((size_t)ksplit * ntok * DK * 4, 256);
+}
+
 size_t project_workspace_bytes(long long ntok, int ksplit) {
   if (ksplit <= 1 || ntok <= 0) return 0;
   return align_up((size_t)ksplit * ntok * DK * 4, 256);  // one fp32 partial payload per (pair, token)
@@ -466,9 +579,37 @@ size_t project_workspace_bytes(long long ntok, int ksplit) {
 cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, const void* kv_norm_w, float eps,
                                  float rope_theta, int fmt, int num_pages, void* pages, const int32_t* page_table,
                                  int max_pages, const int32_t* pos, int B, int T, void* latent_out, int ksplit,
-                                 void* workspace, int* err, cudaStream_t s) {
+                                 bool small, void* workspace, int* err, cudaStream_t s) {
   const long long ntok = (long long)B * T;
   if (ntok == 0) return cudaSuccess;
+  void (*finish)(const float*, int, int, const uint16_t*, float, RopeFreq, int, uint8_t*, const int32_t*, int,
+                 const int32_t*, int, uint16_t*, int*) =
+      fmt == MLA_FMT_BF16 ? project_finish_kernel<MLA_FMT_BF16>
+      : fmt == MLA_FMT_INT8 ? project_finish_kernel<MLA_FMT_INT8>
+                            : project_finish_kernel<MLA_FMT_INT4>;
+  if (small) {
+    if (ntok > PS_TOK || hidden % 64 != 0 || (hidden / 64 + ksplit - 1) / ksplit > PS_MAXCH) return cudaErrorInvalidValue;
+    CUtensorMap tm_x, tm_w;
+    // x: (hidden, tokens) bf16, wkv_a: (hidden, 576), innermost first; boxes of 64 x 64, 128B swizzle
+    if (!encode_3d(&tm_x, x, (uint64_t)hidden, (uint64_t)ntok, 1, (uint64_t)hidden * 2, (uint64_t)ntok * hidden * 2,
+                   64, PS_TOK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&tm_w, wkv_a, (uint64_t)hidden, DK, 1, (uint64_t)hidden * 2, (uint64_t)DK * hidden * 2, 64,
+                   PS_COLS, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    RopeFreq fr;
+    for (int i = 0; i < DR / 2; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / DR);
+    float* acc = static_cast<float*>(workspace);
+    const size_t smem = sizeof(PsSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(project_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    project_small_kernel<<<dim3(PS_NG, ksplit), 256, smem, s>>>(tm_x, tm_w, (int)ntok, hidden / 64, ksplit, acc, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(finish, dim3((unsigned)ntok), dim3(PF_THREADS), 0, s, static_cast<const float*>(acc), ksplit,
+                      (int)ntok, static_cast<const uint16_t*>(kv_norm_w), eps, fr, num_pages,
+                      static_cast<uint8_t*>(pages), page_table, max_pages, pos, T,
+                      static_cast<uint16_t*>(latent_out), err);
+  }
   const long long mtiles = (ntok + PJ_ROWS - 1) / PJ_ROWS;
   const int chunks = hidden / 64;
   CUtensorMap tm_x, tm_wc, tm_wr;
@@ -509,11 +650,6 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
                          static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, (int)ntok, chunks, ksplit,
                          static_cast<uint16_t*>(latent_out), acc, err);
   if (e != cudaSuccess || ksplit <= 1) return e;
-  void (*finish)(const float*, int, int, const uint16_t*, float, RopeFreq, int, uint8_t*, const int32_t*, int,
-                 const int32_t*, int, uint16_t*, int*) =
-      fmt == MLA_FMT_BF16 ? project_finish_kernel<MLA_FMT_BF16>
-      : fmt == MLA_FMT_INT8 ? project_finish_kernel<MLA_FMT_INT8>
-                            : project_finish_kernel<MLA_FMT_INT4>;
   return launch_pdl(finish, dim3((unsigned)ntok), dim3(PF_THREADS), 0, s, static_cast<const float*>(acc), ksplit,
                     (int)ntok, static_cast<const uint16_t*>(kv_norm_w), eps, fr, num_pages,
                     static_cast<uint8_t*>(pages), page_table, max_pages, pos, T, static_cast<uint16_t*>(latent_out),

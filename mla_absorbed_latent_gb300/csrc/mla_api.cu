@@ -161,6 +161,8 @@ size_t mla_cache_project_workspace_bytes(int B, int T, int hidden, int k_splits)
   if (ntok > MAX_PROJECT_TOKENS) return 0;
   const int sms = num_sms();
   if (sms <= 0) return 0;
+  if (k_splits == 0 && ntok <= PROJECT_SMALL_TOKENS)
+    return project_small_workspace_bytes(ntok, project_small_splits(hidden, sms));
   return project_workspace_bytes(ntok, project_splits(ntok, hidden, sms, k_splits));
 }
 
@@ -181,9 +183,11 @@ int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden
   if (!(eps >= 0.f) || eps == INFINITY || !(rope_theta > 0.f) || rope_theta == INFINITY) return MLA_ERR_INVALID;
   const int sms = num_sms();
   if (sms <= 0) return MLA_ERR_CUDA;
-  const int ksplit = project_splits(ntok, hidden, sms, k_splits);
+  // at most 64 tokens with the automatic split: the warp-level projection
+  const bool small = k_splits == 0 && ntok <= PROJECT_SMALL_TOKENS;
+  const int ksplit = small ? project_small_splits(hidden, sms) : project_splits(ntok, hidden, sms, k_splits);
   if (2 * ((ntok + 127) / 128) * (long long)ksplit > 2147483647LL) return MLA_ERR_UNSUPPORTED;  // one CTA per grid x
-  const size_t need = project_workspace_bytes(ntok, ksplit);
+  const size_t need = small ? project_small_workspace_bytes(ntok, ksplit) : project_workspace_bytes(ntok, ksplit);
   if (need > 0) {
     if (workspace == nullptr || !aligned(workspace, 256)) return MLA_ERR_INVALID;
     if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
@@ -191,7 +195,7 @@ int mla_cache_project_append(const mla_cache_t* cache, const void* x, int hidden
   int* err = err_ptr();
   if (err == nullptr) return MLA_ERR_CUDA;
   return status_of(launch_cache_project(x, hidden, wkv_a, kv_norm_w, eps, rope_theta, cache->fmt, cache->num_pages,
-                                        cache->pages, page_table, max_pages, pos, B, T, latent_out, ksplit,
+                                        cache->pages, page_table, max_pages, pos, B, T, latent_out, ksplit, small,
                                         workspace, err, stream));
 }
 

@@ -247,11 +247,17 @@ cudaError_t launch_cache_append(int fmt, int num_pages, void* pages, const void*
 cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, const void* kv_norm_w, float eps,
                                  float rope_theta, int fmt, int num_pages, void* pages, const int32_t* page_table,
                                  int max_pages, const int32_t* pos, int B, int T, void* latent_out, int ksplit,
-                                 void* workspace, int* err, cudaStream_t s);
+                                 bool small, void* workspace, int* err, cudaStream_t s);
 // CTA pairs per token tile that the producer uses (`requested` > 0 forces it, capped at hidden/64)
 int project_splits(long long ntok, int hidden, int sms, int requested);
 // workspace of the producer for ntok tokens and ksplit pairs per tile (0 when ksplit is 1)
 size_t project_workspace_bytes(long long ntok, int ksplit);
+// at most 64 tokens (small = true above): the warp-level projection's slices of
+// the hidden dimension per 64-column group, and its workspace (one fp32
+// partial payload per slice and token)
+constexpr int PROJECT_SMALL_TOKENS = 64;
+int project_small_splits(int hidden, int sms);
+size_t project_small_workspace_bytes(long long ntok, int ksplit);
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
                             cudaStream_t s);
 // B real rows, query layout qs (B * qs.NG plan rows)

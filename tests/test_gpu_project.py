@@ -146,6 +146,26 @@ def test_project_v3_decode_shape():
     assert np.array_equal(_np_bf16(p.latent), first)
 
 
+@pytest.mark.parametrize("hidden,fmt,B,T", [(64, "bf16", 1, 1), (2048, "int8", 5, 7), (2048, "int4", 5, 7),
+                                             (7168, "bf16", 3, 21), (65536, "bf16", 1, 3)])
+def test_project_few_tokens(hidden, fmt, B, T):
+    """At most 64 tokens with the automatic split: the warp-level MMA producer
+    (the hidden dimension in slices of at most 512, the 576 columns in groups of
+    64, token rows past the last one read as zeros).  Payload against the oracle,
+    page image bit-exact, and within one bf16 ulp of the forced tcgen05 path."""
+    p = Produced(hidden, B=B, T=T, pos0=[3 + 61 * b for b in range(B)], seed=35 + hidden % 7)
+    assert p.run() > 0
+    assert _status() == (0, 0)
+    _check_rows(p)
+    assert np.array_equal(p.pool_bytes(), p.expected_pool())
+    small = p.latent_f32().astype(np.float64)
+    p.run(k_splits=1)
+    assert _status() == (0, 0)
+    # two bf16 roundings of (nearly) the same fp32 value: at most one ulp apart
+    other = p.latent_f32().astype(np.float64)
+    assert np.all(np.abs(small - other) <= 2.0 ** -7 * np.abs(other) + 2 * ATOL)
+
+
 def test_project_v3_prefill_many_tiles():
     """V3 width, 4 rows x 2500 tokens (79 tiles, enough for one pair per tile:
     no K split, deterministic): sampled tokens of every row against the oracle,

@@ -99,6 +99,21 @@ int main() {
             CHECK(ws >= (size_t)k * ntok * DK * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok, k);
           }
         }
+  // 3b. the few-token producer (at most 64 tokens): slices of the hidden
+  //     dimension within [1, hidden/64], at most 8 chunks of 64 each, about one
+  //     CTA per SM when the hidden dimension allows it, and one fp32 partial
+  //     payload per slice and token
+  for (int hidden : hiddens)
+    for (int sms : smss) {
+      const int k = project_small_splits(hidden, sms);
+      const int chunks = hidden / 64;
+      CHECK(k >= 1 && k <= chunks && (chunks + k - 1) / k <= 8, "hidden=%d sms=%d k=%d", hidden, sms, k);
+      CHECK(k >= (sms / 9 < chunks ? sms / 9 : chunks), "hidden=%d sms=%d k=%d", hidden, sms, k);
+      for (long long ntok = 1; ntok <= PROJECT_SMALL_TOKENS; ntok += 21) {
+        const size_t ws = project_small_workspace_bytes(ntok, k);
+        CHECK(ws >= (size_t)k * ntok * DK * 4 && ws % 256 == 0, "ntok=%lld k=%d", ntok, k);
+      }
+    }
   // 4. the no-allocation decode's worker count: the largest count <= want whose
   //    workspace fits the capacity, 0 when one worker does not fit
   const size_t caps[] = {1u << 20, 16u << 20, 64ull << 20};
