@@ -182,7 +182,9 @@ int mla_cache_append(const mla_cache_t* cache, const void* c_kv, const void* k_p
  * Per token, in fp32 from bf16 operands: y = wkv_a x (tensor cores, fp32
  * accumulation); c = y[0..511] / sqrt(mean(y[0..511]^2) + eps) * kv_norm_w;
  * pairs (2i, 2i+1) of y[512..575] rotated by the angle pos * rope_theta^(-2i/64)
- * (the angle reduced modulo 2 pi in fp64); each value rounded once to bf16,
+ * (reduced to one turn in 64-bit fixed point: the frequency as a fraction of
+ * a turn in units of 2^-64, times pos modulo 2^64; angle error under 1e-6 rad
+ * for any int32 position); each value rounded once to bf16,
  * then quantized exactly as mla_cache_append does.  With a K split each CTA's
  * partial product goes to its own slice of the workspace and a second kernel
  * (one CTA per token) sums the slices in split order before the same epilogue,

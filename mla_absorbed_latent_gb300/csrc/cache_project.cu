@@ -53,8 +53,10 @@ constexpr uint32_t PJ_WR_TILE = PJ_ROPE * 128;  // 4 KB: 32 RoPE-key rows x 64 h
 constexpr uint32_t PJ_STAGE_BYTES = PJ_X_TILE + PJ_WC_TILE + PJ_WR_TILE;
 constexpr uint32_t PJ_TMEM_COLS = 512;        // 288 used: latent half at 0, RoPE key at 256
 
+// The RoPE rotation frequencies theta^(-2i/64), i = 0..31, as fixed-point phase
+// increments: turn[i] = theta^(-2i/64) / (2 pi) in units of 2^-64 turn.
 struct RopeFreq {
-  double f[DR / 2];  // theta^(-2i/64), i = 0..31
+  uint64_t turn[DR / 2];
 };
 
 struct __align__(1024) PjSmem {
@@ -63,7 +65,7 @@ struct __align__(1024) PjSmem {
   uint8_t wr[PJ_STAGES][PJ_WR_TILE];
   float gamma[PJ_HALF];  // kv_norm gain of this CTA's latent columns
   float ss[PJ_ROWS];     // per-token sum of squares of this CTA's latent columns (read by the peer)
-  double freq[PJ_ROPE / 2];  // rotation frequencies of this CTA's 16 RoPE pairs
+  uint64_t turn[PJ_ROPE / 2];  // phase increments of this CTA's 16 RoPE pairs (RopeFreq)
   uint64_t full[PJ_STAGES], empty[PJ_STAGES], mma_done;
   uint32_t tmem_base;
   int last;      // split mode: this pair runs the epilogue of its tile
@@ -73,14 +75,17 @@ struct __align__(1024) PjSmem {
 
 __device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// sin and cos of pos * freq: the angle is formed and reduced modulo 2 pi in fp64
-// (Cody and Waite's two-constant reduction), then sincosf on the reduced angle
-__device__ __forceinline__ void rope_sincos(double pos, double freq, float* s, float* c) {
-  const double a = pos * freq;
-  const double k = rint(a * 0.15915494309189535);   // a / (2 pi), to the nearest integer
-  double r = fma(-k, 6.283185307179586, a);          // 2 pi = 6.283185307179586 + 2.4492935982947064e-16
-  r = fma(-k, 2.4492935982947064e-16, r);
-  sincosf((float)r, s, c);
+// sin and cos of the angle pos * theta^(-2i/64), reduced to one turn as the
+// phase accumulator of direct digital synthesis does: the wrapping 64-bit
+// product pos * turn is the angle modulo one turn in units of 2^-64 turn
+// (exact up to the rounding of turn, under pos * 2^-55 turn), its top 32 bits
+// read as a signed number are the angle in [-pi, pi) in units of 2 pi / 2^32,
+// and sincosf takes it from there.  No floating-point product of pos and the
+// frequency is formed, so the reduction is as good at position 2^31 as at 0.
+__device__ __forceinline__ void rope_sincos(long long pos, uint64_t turn, float* s, float* c) {
+  const uint64_t ph = (uint64_t)pos * turn;
+  const int32_t hi = (int32_t)(uint32_t)(ph >> 32);
+  sincosf((float)hi * 1.46291807926715968e-09f, s, c);  // 2 pi / 2^32
 }
 
 __device__ __forceinline__ void store_bf16x32(uint8_t* dst, const float* y) {
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   }
   for (int i = tid; i < PJ_HALF; i += PJ_THREADS)
     S.gamma[i] = __uint_as_float((uint32_t)kv_norm_w[PJ_HALF * rank + i] << 16);
-  if (tid < PJ_ROPE / 2) S.freq[tid] = rank == 0 ? freq.f[tid] : freq.f[PJ_ROPE / 2 + tid];
+  if (tid < PJ_ROPE / 2) S.turn[tid] = rank == 0 ? freq.turn[tid] : freq.turn[PJ_ROPE / 2 + tid];
   if (warp == 0) {
     tmem_alloc(&S.tmem_base, PJ_TMEM_COLS);
     tmem_relinquish();
@@ -326,11 +331,10 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       // loop keeps one copy of that code), into the first x stage of the ring,
       // free now that every MMA has completed: [pair][token] float2
       float2* rot = reinterpret_cast<float2*>(S.x[0]);
-      const double pd = (double)p;
 #pragma unroll 1
       for (int i = 0; i < PJ_ROPE / 2; ++i) {
         float sn, cs;
-        rope_sincos(pd, S.freq[i], &sn, &cs);
+        rope_sincos(p, S.turn[i], &sn, &cs);
         rot[i * PJ_ROWS + row] = make_float2(cs, sn);
       }
       uint32_t v[32];
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(PF_THREADS) project_finish_kernel(
     const int rc = c - DC, i = rc >> 1;
     const float other = __shfl_xor_sync(0xffffffffu, v, 1);
     float sn, cs;
-    rope_sincos((double)p, freq.f[i], &sn, &cs);
+    rope_sincos(p, freq.turn[i], &sn, &cs);
     const float x0 = (rc & 1) ? other : v, x1 = (rc & 1) ? v : other;  // y[2i], y[2i+1] before the rotation
     y[c] = bf16r((rc & 1) ? x0 * sn + x1 * cs : x0 * cs - x1 * sn);
   }
@@ -545,6 +549,18 @@ __global__ void __launch_bounds__(PF_THREADS) project_finish_kernel(
 }
 
 }  // namespace
+
+// turn[i] = theta^(-2i/64) / (2 pi) modulo one turn, times 2^64, rounded:
+// formed in double (scaling by 2^64 is exact), wrapping to 0 at a whole turn
+RopeFreq rope_freq(float rope_theta) {
+  RopeFreq fr;
+  for (int i = 0; i < DR / 2; ++i) {
+    const double u = std::pow((double)rope_theta, -2.0 * i / DR) / 6.283185307179586;
+    const double v = std::nearbyint(std::ldexp(u - std::floor(u), 64));
+    fr.turn[i] = v >= 18446744073709551616.0 ? 0 : (uint64_t)v;
+  }
+  return fr;
+}
 
 int project_splits(long long ntok, int hidden, int sms, int requested) {
   const int chunks = hidden / 64;
@@ -596,8 +612,7 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
         !encode_3d(&tm_w, wkv_a, (uint64_t)hidden, DK, 1, (uint64_t)hidden * 2, (uint64_t)DK * hidden * 2, 64,
                    PS_COLS, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    RopeFreq fr;
-    for (int i = 0; i < DR / 2; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / DR);
+    const RopeFreq fr = rope_freq(rope_theta);
     float* acc = static_cast<float*>(workspace);
     const size_t smem = sizeof(PsSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(project_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -623,8 +638,7 @@ cudaError_t launch_cache_project(const void* x, int hidden, const void* wkv_a, c
   if (!encode_3d(&tm_wr, wkv_a, (uint64_t)hidden, DK, 1, (uint64_t)hidden * 2, (uint64_t)DK * hidden * 2, 64, PJ_ROPE,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  RopeFreq fr;
-  for (int i = 0; i < DR / 2; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / DR);
+  const RopeFreq fr = rope_freq(rope_theta);
   float* acc = ksplit > 1 ? static_cast<float*>(workspace) : nullptr;
   const size_t smem = sizeof(PjSmem) + 1024;
   void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, const uint16_t*, float, RopeFreq, int, uint8_t*,

@@ -166,6 +166,26 @@ def test_project_few_tokens(hidden, fmt, B, T):
     assert np.all(np.abs(small - other) <= 2.0 ** -7 * np.abs(other) + 2 * ATOL)
 
 
+@pytest.mark.parametrize("k_splits", [0, 1, 3])
+def test_project_far_positions(k_splits):
+    """Positions near 2^20, 2^22 and 2^24 (rotation angles of up to 1.7e7 rad on
+    the fastest pair): the angle is reduced to one turn in 64-bit fixed point,
+    so the RoPE key stays within tolerance of the fp64 oracle.  The few-token
+    kernel with its finishing kernel, the tcgen05 kernel's own epilogue, and the
+    tcgen05 kernel split three ways with the finishing kernel."""
+    far = np.array([(1 << 20) - 1, (1 << 20) + 12345, 3 * (1 << 22) + 7, (1 << 24) - 1], dtype=np.int32)
+    p = Produced(2048, B=4, T=1, pos0=[0, 0, 0, 0], seed=36)
+    max_pages = (1 << 24) // 64
+    table = np.repeat(p.page_table[:, :1], max_pages, axis=1).astype(np.int32)  # every page: the row's own
+    p.page_table, p.pos0 = np.ascontiguousarray(table), far
+    p.pt = torch.from_numpy(p.page_table).cuda()
+    p.pos = torch.from_numpy(far).cuda()
+    p.run(k_splits)
+    assert _status() == (0, 0)
+    _check_rows(p)
+    assert np.array_equal(p.pool_bytes(), p.expected_pool())
+
+
 def test_project_v3_prefill_many_tiles():
     """V3 width, 4 rows x 2500 tokens (79 tiles, enough for one pair per tile:
     no K split, deterministic): sampled tokens of every row against the oracle,
