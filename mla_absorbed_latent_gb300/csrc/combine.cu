@@ -538,14 +538,18 @@ __global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, in
 // (head, 16..32 rows) one CTA, only 32 CTAs for 16 heads and a 32-row batch, and
 // its chunk loop is then latency-bound.  Here one CTA per (head, group of 4
 // rows): W_UV[h] (128 KB) is copied into shared memory before the kernel waits
-// for the attention step; every warp of a row loads the row's segment
-// log-sum-exps in one round and forms the weights e^{LSE_s - LSE}; o_lat of each
-// row is the weighted sum of its segments' partials (the same formula), two rows
-// at a time in the two halves of the block; then out[b, h, :] =
-// W_UV[h] o_lat[b, h, :], 128 dot products of length 512 per row.
+// for the attention step.  Each row has a quarter of the block (4 latent dims
+// per thread) and merges its segments 8 at a time, every load of a chunk (the
+// 8 log-sum-exps and the 8 partials) in flight at once, as an online softmax
+// over the segments ("kv_budget.py" part C: o_lat = sum_s e^{LSE_s - LSE} o_s
+// with LSE = log sum_s e^{LSE_s}, the running maximum moved per chunk).  Then
+// out[b, h, :] = W_UV[h] o_lat[b, h, :]: each warp forms 8 output dims of the
+// 4 rows, lane-partial dot products reduced across the warp by a butterfly
+// reduce-scatter that leaves lane L with output 8 warp + L / 4 of row L % 4.
 // ---------------------------------------------------------------------------
 constexpr int SRB = 4;      // rows per CTA
-constexpr int SNT = 512;    // threads: two rows at a time in the merge (2 latent dims per thread), 8 output dims per warp after it
+constexpr int SNT = 512;    // threads: a quarter of the block per row in the merge, 8 output dims per warp after it
+constexpr int SCH = 8;      // segments per merge chunk
 
 struct __align__(16) SmallSmem {
   uint16_t w[DV * DC];           // W_UV[h], 128 KB
@@ -578,61 +582,53 @@ __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __re
   grid_dep_launch();
   const long long T = plan[0], W = plan[1];
   const int* prefix = plan + PLAN_HDR;
-  const int half = tid >> 8, ht = tid & 255;  // thread half (one row at a time), its thread
-  for (int r0 = 0; r0 < SRB; r0 += 2) {
-    const int r = r0 + half, b = b0 + r;
-    float a0 = 0.f, a1 = 0.f, den = 0.f;  // latent dims 2 ht, 2 ht + 1
-    if (b < B && prefix[b + 1] > prefix[b]) {
-      // segment w + b of row b for the workers w whose ranges hold its tiles (a
-      // worker without tiles left no partial: weight 0).  Every warp forms the
-      // weights itself, lane k those of segment c0 + k, and hands them out by
-      // shuffles: no block barrier.
-      const int sx = worker_of_tile(prefix[b], T, W) + b, sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
-      auto lse_of = [&](int sg) -> float {
-        const long long w = sg - b;
-        return worker_begin(w, T, W) == worker_begin(w + 1, T, W) ? -INFINITY : part_lse[(size_t)sg * H + h];
-      };
-      float l0 = sx + lane <= sy ? lse_of(sx + lane) : -INFINITY;  // the first 32 segments
-      float mx = l0;
-      for (int sg = sx + 32 + lane; sg <= sy; sg += 32) mx = fmaxf(mx, lse_of(sg));
+  const int r = tid >> 7, rt = tid & 127;  // the row of the group, latent dims 4 rt .. 4 rt + 3
+  const int b = b0 + r;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (b < B && prefix[b + 1] > prefix[b]) {
+    // segment w + b of row b for the workers w whose ranges hold its tiles (a
+    // worker without tiles left no partial: weight 0, its slot's undefined bits
+    // loaded with the others and discarded)
+    const int sx = worker_of_tile(prefix[b], T, W) + b, sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
+    const size_t stride = (size_t)H * DC / 4;  // one segment, in 4-value units
+    const uint2* po = reinterpret_cast<const uint2*>(part_o + (size_t)h * DC) + rt;
+    float m = -INFINITY, den = 0.f;
+    for (int c0 = sx; c0 <= sy; c0 += SCH) {
+      const int cn = min(SCH, sy - c0 + 1);
+      float lk = -INFINITY;  // lane k < cn: the log-sum-exp of segment c0 + k
+      if (lane < cn) {
+        const long long w = c0 + lane - b;
+        if (worker_begin(w, T, W) != worker_begin(w + 1, T, W)) lk = part_lse[(size_t)(c0 + lane) * H + h];
+      }
+      uint2 v[SCH];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const size_t stride = (size_t)H * DC / 2;  // one segment, in bf16 pairs
-      for (int c0 = sx; c0 <= sy; c0 += 32) {
-        const int cn = min(32, sy - c0 + 1);
-        const float lk = c0 == sx ? l0 : (lane < cn ? lse_of(c0 + lane) : -INFINITY);
-        const float e = lk == -INFINITY ? 0.f : expf(lk - mx);
-        const uint32_t* po = reinterpret_cast<const uint32_t*>(part_o + ((size_t)c0 * H + h) * DC) + ht;
-        int k = 0;
-        for (; k + 4 <= cn; k += 4) {  // four loads in flight
-          const float e0 = __shfl_sync(0xffffffffu, e, k), e1 = __shfl_sync(0xffffffffu, e, k + 1),
-                      e2 = __shfl_sync(0xffffffffu, e, k + 2), e3 = __shfl_sync(0xffffffffu, e, k + 3);
-          // a slot no worker wrote holds undefined bits: skipped, not weighted by 0
-          const uint32_t v0 = e0 != 0.f ? po[(k + 0) * stride] : 0u, v1 = e1 != 0.f ? po[(k + 1) * stride] : 0u,
-                         v2 = e2 != 0.f ? po[(k + 2) * stride] : 0u, v3 = e3 != 0.f ? po[(k + 3) * stride] : 0u;
-          a0 = fmaf(e0, bf16lo(v0), a0); a1 = fmaf(e0, bf16hi(v0), a1);
-          a0 = fmaf(e1, bf16lo(v1), a0); a1 = fmaf(e1, bf16hi(v1), a1);
-          a0 = fmaf(e2, bf16lo(v2), a0); a1 = fmaf(e2, bf16hi(v2), a1);
-          a0 = fmaf(e3, bf16lo(v3), a0); a1 = fmaf(e3, bf16hi(v3), a1);
-          den += (e0 + e1) + (e2 + e3);
-        }
-        for (; k < cn; ++k) {
-          const float ek = __shfl_sync(0xffffffffu, e, k);
-          const uint32_t v = ek != 0.f ? po[k * stride] : 0u;
-          a0 = fmaf(ek, bf16lo(v), a0);
-          a1 = fmaf(ek, bf16hi(v), a1);
+      for (int k = 0; k < SCH; ++k) v[k] = k < cn ? po[(size_t)(c0 + k) * stride] : make_uint2(0u, 0u);
+      float mc = lk;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+      const float mn = fmaxf(m, __shfl_sync(0xffffffffu, mc, 0));  // finite: the row's first segment has tiles
+      const float sc = m == -INFINITY ? 0.f : expf(m - mn);
+      const float e = lk == -INFINITY ? 0.f : expf(lk - mn);
+      a0 *= sc; a1 *= sc; a2 *= sc; a3 *= sc; den *= sc;
+#pragma unroll
+      for (int k = 0; k < SCH; ++k) {
+        const float ek = __shfl_sync(0xffffffffu, e, k);
+        if (ek != 0.f) {
+          a0 = fmaf(ek, bf16lo(v[k].x), a0);
+          a1 = fmaf(ek, bf16hi(v[k].x), a1);
+          a2 = fmaf(ek, bf16lo(v[k].y), a2);
+          a3 = fmaf(ek, bf16hi(v[k].y), a3);
           den += ek;
         }
       }
-      const float inv = 1.f / den;  // den >= 1: the largest term is e^0
-      a0 *= inv;
-      a1 *= inv;
+      m = mn;
     }
-    S.ol[r][2 * ht] = a0;
-    S.ol[r][2 * ht + 1] = a1;
-    if (o_lat != nullptr && b < B)
-      *reinterpret_cast<float2*>(o_lat + ((size_t)b * H + h) * DC + 2 * ht) = make_float2(a0, a1);
+    const float inv = 1.f / den;  // den >= 1: the largest term is e^0
+    a0 *= inv; a1 *= inv; a2 *= inv; a3 *= inv;
   }
+  *reinterpret_cast<float4*>(&S.ol[r][4 * rt]) = make_float4(a0, a1, a2, a3);
+  if (o_lat != nullptr && b < B)
+    *reinterpret_cast<float4*>(o_lat + ((size_t)b * H + h) * DC + 4 * rt) = make_float4(a0, a1, a2, a3);
   __syncthreads();
   if (!mbar_wait(&S.w_full, 0)) {
     if (tid == 0) raise_error(err, MLA_ERR_TIMEOUT, 150);
@@ -642,40 +638,44 @@ __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __re
   // 8 warp .. 8 warp + 7, lane `lane` latent dims 8 lane .. +7 and 256 + 8 lane .. +7
   float x[SRB][16];
 #pragma unroll
-  for (int r = 0; r < SRB; ++r)
+  for (int q = 0; q < SRB; ++q)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      x[r][k] = S.ol[r][8 * lane + k];
-      x[r][8 + k] = S.ol[r][256 + 8 * lane + k];
+      x[q][k] = S.ol[q][8 * lane + k];
+      x[q][8 + k] = S.ol[q][256 + 8 * lane + k];
     }
-#pragma unroll 4
+  float d[32];  // lane partials of output 8 warp + i / 4, row i % 4
+#pragma unroll
   for (int jj = 0; jj < 8; ++jj) {
-    const int j = 8 * warp + jj;
-    const uint4* wr = reinterpret_cast<const uint4*>(S.w + (size_t)j * DC);
+    const uint4* wr = reinterpret_cast<const uint4*>(S.w + (size_t)(8 * warp + jj) * DC);
     const uint4 u0 = wr[lane], u1 = wr[32 + lane];
     const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    float d[SRB];
 #pragma unroll
-    for (int r = 0; r < SRB; ++r) {
+    for (int q = 0; q < SRB; ++q) {
       float acc = 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        acc = fmaf(bf16lo(wv[k]), x[r][2 * k], acc);
-        acc = fmaf(bf16hi(wv[k]), x[r][2 * k + 1], acc);
+        acc = fmaf(bf16lo(wv[k]), x[q][2 * k], acc);
+        acc = fmaf(bf16hi(wv[k]), x[q][2 * k + 1], acc);
       }
-      d[r] = acc;
+      d[4 * jj + q] = acc;
     }
+  }
+  // reduce-scatter across the warp: at offset o the lane keeps the half of its
+  // values selected by its bit o and adds the partner's copy of that half
 #pragma unroll
-    for (int r = 0; r < SRB; ++r)
+  for (int o = 16, n = 16; o > 0; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) d[r] += __shfl_xor_sync(0xffffffffu, d[r], o);
-    if (lane < SRB && b0 + lane < B) {
-      float v = d[0];
-#pragma unroll
-      for (int r = 1; r < SRB; ++r) v = lane == r ? d[r] : v;
-      const __nv_bfloat16 ob = __float2bfloat16_rn(v);
-      out[((size_t)(b0 + lane) * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
+    for (int i = 0; i < n; ++i) {
+      const float keep = up ? d[i + n] : d[i], send = up ? d[i] : d[i + n];
+      d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
+  }
+  const int q = lane & 3, j = 8 * warp + (lane >> 2);
+  if (b0 + q < B) {
+    const __nv_bfloat16 ob = __float2bfloat16_rn(d[0]);
+    out[((size_t)(b0 + q) * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
   }
 }
 
