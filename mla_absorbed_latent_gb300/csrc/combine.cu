@@ -9,8 +9,9 @@
 //
 // One CTA per (head h, group of RB rows).  The segments of a group's rows are
 // consecutive slots of the partial buffer (slot w + b for worker w, row b), so
-// for every 64-wide latent chunk TMA boxes bring that chunk of up to 128
-// segments at a time ([segments][64] bf16) into shared memory.  The merge threads (one
+// for every 64-wide latent chunk TMA boxes of 16 segments bring that chunk of
+// up to 128 segments at a time ([segments][64] bf16) into shared memory, as
+// many boxes as the group's segments need.  The merge threads (one
 // per row and 8-dim unit) sum their row's segments with the softmax weights,
 // round o_lat once into a bf16 high part and a bf16 residual, and write both
 // as K-major 128B-swizzled operand tiles; one thread then issues the
@@ -29,7 +30,8 @@ using namespace tc;
 
 constexpr int KC = 64;                    // latent dims per chunk
 constexpr int NCHUNK = DC / KC;           // 8
-constexpr int SEGB = 128;                 // segments per partial tile (TMA box)
+constexpr int SEGB = 128;                 // segments per partial tile
+constexpr int SBOX = 16;                  // segments per TMA box: a tile holds as many boxes as its segments need
 constexpr uint32_t W_TILE = DV * KC * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
 constexpr uint32_t P_TILE = SEGB * KC * 2;  // 16 KB: [128 segments][64 dims] bf16
 constexpr int WST = 2, PST = 3, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
@@ -355,8 +357,11 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
           const int st = pu % PST;
           ok = cwait(&p_empty[st], ((pu / PST) & 1) ^ 1, abort, err, 1);
           if (!ok) break;
-          mbar_arrive_expect_tx(&p_full[st], P_TILE);
-          tma_load_3d(sm + L::OFF_P + st * P_TILE, &tm_p, KC * kc, h, s_lo + SEGB * sub, &p_full[st]);
+          const int nbox = (min(SEGB, s_hi - s_lo - SEGB * sub) + SBOX - 1) / SBOX;
+          mbar_arrive_expect_tx(&p_full[st], (uint32_t)nbox * SBOX * KC * 2);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_3d(sm + L::OFF_P + st * P_TILE + j * SBOX * KC * 2, &tm_p, KC * kc, h,
+                        s_lo + SEGB * sub + SBOX * j, &p_full[st]);
         }
       }
       if (*abort)
@@ -712,9 +717,9 @@ cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, co
   CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // partials (bf16): (512 latent, Hv heads, segments), boxes of 64 dims x 1 head x 128 segments
+  // partials (bf16): (512 latent, Hv heads, segments), boxes of 64 dims x 1 head x 16 segments
   const uint64_t segs = (uint64_t)max_workers + Bv;
-  if (!encode_3d_box(&tm_p, part_o, DC, Hv, segs, DC * 2, (uint64_t)Hv * DC * 2, KC, 1, SEGB,
+  if (!encode_3d_box(&tm_p, part_o, DC, Hv, segs, DC * 2, (uint64_t)Hv * DC * 2, KC, 1, SBOX,
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
