@@ -42,8 +42,8 @@ struct __align__(16) SmemCC {
 __global__ void __launch_bounds__(THREADS, 2)
     attend_cc_kernel(const uint16_t* __restrict__ q_cat, int H, int num_pages, const uint8_t* __restrict__ pages,
                      const int32_t* __restrict__ page_table, int max_pages, int B, float scale_log2,
-                     const int* __restrict__ plan, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
-                     int* err) {
+                     const int* __restrict__ plan, int seg_cap, uint16_t* __restrict__ part_o,
+                     float* __restrict__ part_lse, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SmemCC& S = *reinterpret_cast<SmemCC*>(smem_raw);
   grid_dep_wait();  // the plan, the query and the cache may come from the kernel before this one
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float inv = 1.f / S.l[h];
-        reinterpret_cast<uint32_t*>(part_o + ((size_t)seg * H + hg * HG + h) * DC)[tid] =
+        reinterpret_cast<uint32_t*>(part_o + ((size_t)(hg * HG + h) * seg_cap + seg) * DC)[tid] =
             pack_bf16x2(o[h][0] * inv, o[h][1] * inv);  // partials are stored in bf16
       }
       if (tid < HG)
@@ -253,14 +253,14 @@ int attend_cc_workers(int num_sms) { return 2 * num_sms; }
 
 cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
+                             int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (fmt != MLA_FMT_BF16) return cudaErrorNotSupported;
   const size_t smem = sizeof(SmemCC);
   cudaError_t e = cudaFuncSetAttribute(attend_cc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(attend_cc_kernel, dim3(workers, H / HG), dim3(THREADS), smem, s,
                     static_cast<const uint16_t*>(q_cat), H, num_pages, static_cast<const uint8_t*>(pages), page_table,
-                    max_pages, B, scale * 1.4426950408889634f, plan, part_o, part_lse, err);
+                    max_pages, B, scale * 1.4426950408889634f, plan, seg_cap, part_o, part_lse, err);
 }
 
 }  // namespace mla

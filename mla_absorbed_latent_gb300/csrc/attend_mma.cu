@@ -129,8 +129,8 @@ __device__ __forceinline__ bool mwait_warp(uint64_t* bar, uint32_t parity, volat
 __global__ void __launch_bounds__(MTHREADS, 1)
     attend_mma_kernel(const __grid_constant__ CUtensorMap tm_kv, const uint16_t* __restrict__ q_cat, int H,
                       int num_pages, const int32_t* __restrict__ page_table, int max_pages, int B, float scale_log2,
-                      const int* __restrict__ plan, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
-                      int* err) {
+                      const int* __restrict__ plan, int seg_cap, uint16_t* __restrict__ part_o,
+                      float* __restrict__ part_lse, int* err) {
   extern __shared__ uint8_t smem_raw[];
   SmemMMA& S = *reinterpret_cast<SmemMMA*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   grid_dep_wait();  // the plan, the query and the cache may come from the kernels before this one
@@ -397,12 +397,13 @@ __global__ void __launch_bounds__(MTHREADS, 1)
     if (lane == 0) mbar_arrive(&S.empty[st]);  // this warp's reads of the stage are done
     if (hp.z & HP_LAST_OF_SEG) {
       const float ig = 1.f / S.lfin[rb][g], ig8 = 1.f / S.lfin[rb][g + 8];
-      const size_t seg = (size_t)(worker + hp.x);
-      uint16_t* dst = part_o + (seg * H + hg * MH) * DC + 64 * w + 2 * t;
+      // heads hg * MH + g and + 8 (head-major partials: segment seg of head h at h * seg_cap + seg)
+      const size_t seg = (size_t)(worker + hp.x), hstride = (size_t)seg_cap * DC;
+      uint16_t* dst = part_o + ((size_t)(hg * MH + g) * seg_cap + seg) * DC + 64 * w + 2 * t;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        *reinterpret_cast<uint32_t*>(dst + (size_t)g * DC + 8 * j) = pack_bf16x2(o[j][0] * ig, o[j][1] * ig);
-        *reinterpret_cast<uint32_t*>(dst + (size_t)(g + 8) * DC + 8 * j) = pack_bf16x2(o[j][2] * ig8, o[j][3] * ig8);
+        *reinterpret_cast<uint32_t*>(dst + 8 * j) = pack_bf16x2(o[j][0] * ig, o[j][1] * ig);
+        *reinterpret_cast<uint32_t*>(dst + 8 * hstride + 8 * j) = pack_bf16x2(o[j][2] * ig8, o[j][3] * ig8);
       }
     }
     __syncwarp();
@@ -417,7 +418,7 @@ int attend_mma_workers(int num_sms) { return num_sms; }
 
 cudaError_t launch_attend_mma(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                               const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
+                              int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (fmt != MLA_FMT_BF16 || H % MH != 0) return cudaErrorNotSupported;
   CUtensorMap tm;
   // pages as [num_pages][64 tokens][576 dims] bf16; a box is 32 tokens x 64 dims
@@ -429,7 +430,7 @@ cudaError_t launch_attend_mma(const void* q_cat, int H, int fmt, int num_pages, 
   if (e != cudaSuccess) return e;
   return launch_pdl(attend_mma_kernel, dim3(workers, H / MH), dim3(MTHREADS), smem, s, tm,
                     static_cast<const uint16_t*>(q_cat), H, num_pages, page_table, max_pages, B,
-                    scale * 1.4426950408889634f, plan, part_o, part_lse, err);
+                    scale * 1.4426950408889634f, plan, seg_cap, part_o, part_lse, err);
 }
 
 }  // namespace mla

@@ -184,10 +184,11 @@ struct TcArgs {
   int* plan;              // read; the exact-recompute flags and context are written
   const uint8_t* pages;
   const int32_t* page_table;
-  uint16_t* part_o;  // bf16 [segments][128][512]
+  uint16_t* part_o;  // bf16 [128 heads][seg_cap segments][512]
   float* part_lse;
   int* err;
   int B, max_pages, num_pages;  // B: plan rows (virtual rows of the query layout)
+  int seg_cap;                  // segments per head in part_o
   float scale_log2;
   QSpec qs;           // query layout: virtual row r reads page-table row r / qs.NG
   long long q_rows;   // flat rows of q_cat
@@ -870,7 +871,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int ms = sub & 1;                   // MT: slice index within the token half
     auto scale_o = [&](float f) { scale_o_cols(t_row + TM_O + 128 * ms, f); };
     auto store_o = [&](int seg, float inv) {
-      store_o_cols(t_row + TM_O + 128 * ms, a.part_o + ((size_t)seg * 128 + row) * DC + HALF_C * rank + 128 * ms, inv);
+      store_o_cols(t_row + TM_O + 128 * ms, a.part_o + ((size_t)row * a.seg_cap + seg) * DC + HALF_C * rank + 128 * ms,
+                   inv);
     };
 
     bool failed = false;
@@ -1308,7 +1310,7 @@ int attend_tc_workers(int num_sms) {
 
 cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int Bv, float scale, int* plan,
-                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
+                             int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   if (qs.G * qs.Hr != 128 || qs.T < 1 || qs.NG != (qs.T + qs.G - 1) / qs.G || workers < 1) return cudaErrorNotSupported;
   if (fmt != MLA_FMT_BF16 && fmt != MLA_FMT_INT8 && fmt != MLA_FMT_INT4) return cudaErrorNotSupported;
   if (!(scale > 0.f)) return cudaErrorInvalidValue;  // the row max is taken before scaling
@@ -1352,6 +1354,7 @@ cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int nu
   args.pages = pg;
   args.page_table = page_table;
   args.part_o = part_o;
+  args.seg_cap = seg_cap;
   args.part_lse = part_lse;
   args.err = err;
   args.B = Bv;

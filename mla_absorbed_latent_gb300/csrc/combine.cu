@@ -9,9 +9,10 @@
 //
 // One CTA per (head h, group of RB rows).  The segments of a group's rows are
 // consecutive slots of the partial buffer (slot w + b for worker w, row b), so
-// for every 64-wide latent chunk TMA boxes of 16 segments bring that chunk of
+// for every 64-wide latent chunk TMA boxes of 64 segments bring that chunk of
 // up to 128 segments at a time ([segments][64] bf16) into shared memory, as
-// many boxes as the group's segments need.  The merge threads (one
+// many boxes as the group's segments need (head-major partials: a head's
+// segments are consecutive 1 KB rows).  The merge threads (one
 // per row and 8-dim unit) sum their row's segments with the softmax weights,
 // round o_lat once into a bf16 high part and a bf16 residual, and write both
 // as K-major 128B-swizzled operand tiles; one thread then issues the
@@ -30,16 +31,27 @@ using namespace tc;
 
 constexpr int KC = 64;                    // latent dims per chunk
 constexpr int NCHUNK = DC / KC;           // 8
-constexpr int SEGB = 128;                 // segments per partial tile
-constexpr int SBOX = 16;                  // segments per TMA box: a tile holds as many boxes as its segments need
+
+constexpr int SBOX = 64;                  // segments per TMA box: a tile holds as many boxes as its segments need
+                                          // (an issued box costs ~100-200 SM cycles: few, large boxes)
 constexpr uint32_t W_TILE = DV * KC * 2;  // 16 KB: W_UV[h] rows x 64 latent dims, 128B-swizzled
-constexpr uint32_t P_TILE = SEGB * KC * 2;  // 16 KB: [128 segments][64 dims] bf16
-constexpr int WST = 2, PST = 3, BST = 2;    // ring depths: W tiles, partial tiles, operand tiles
+
 
 template <int RB>
 struct CombLayout {
+  // ring depths of the W_UV tiles, the partial tiles and the operand tiles.
+  // An operand tile of chunk k is rewritten only after the MMAs of chunk
+  // k - BST (issued once every merge warp wrote chunk k - BST) complete, a
+  // round trip of about 2.5 us; with 64 rows (one CTA per SM) four operand
+  // tiles keep the merge warps that many chunks ahead of the tensor core
+  static constexpr int WST = RB >= 64 ? 3 : 2, PST = RB >= 64 ? 4 : 3, BST = RB >= 64 ? 4 : 2;
+  // segments per partial tile: every warp waits for every tile of a chunk and
+  // a ring slot is free only when all have read it, so the tile holds all of
+  // a typical group's segments (64 rows: B + W = 140 at 64 rows and 152 SMs)
+  static constexpr int SEGB = RB >= 64 ? 192 : 128;
+  static constexpr uint32_t P_TILE = SEGB * KC * 2;  // [SEGB segments][64 dims] bf16
   static constexpr int NW = RB / 4;          // merge warps: 4 rows x 8 units each
-  static constexpr int THREADS = 32 * (NW + 1);  // + a loader / TMEM-owner warp
+  static constexpr int THREADS = 32 * (NW + 3);  // + the W_UV loader / TMEM owner, partial loader and MMA warps
   static constexpr uint32_t TCOLS = RB < 32 ? 32 : RB;  // TMEM columns (allocations are >= 32)
   static constexpr uint32_t B_TILE = RB * 128;   // [RB rows][64 dims] bf16, 128B-swizzled
   static constexpr uint32_t OFF_W = 0;
@@ -260,6 +272,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
                    float* __restrict__ o_lat, int* err) {
   using L = CombLayout<RB>;
   constexpr int NW = L::NW;
+  constexpr int WST = L::WST, PST = L::PST, BST = L::BST, SEGB = L::SEGB;
+  constexpr uint32_t P_TILE = L::P_TILE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
@@ -277,7 +291,12 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   const int h = blockIdx.x, b0 = blockIdx.y * RB;  // h: head of the partials (a virtual head)
   const int hr = h % qs.Hr;                        // its real head: the W_UV it applies
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool loader = warp == NW;
+  // warp NW: TMEM owner and W_UV loader; warp NW + 1: partial loader; warp
+  // NW + 2: MMA issuer.  Each has a warp of its own: a lane blocked in
+  // mbarrier.try_wait stalls its whole warp, and a merge warp that also issued
+  // the chunk's MMAs (about a microsecond) fell behind the others and held back
+  // the release of the partial ring
+  const bool loader = warp >= NW, w_loader = warp == NW;
   // output row ((row, token) * heads + head) of plan row bv for this head; -1
   // for padding (one query token per row and pass: bv * heads + head, no division)
   const bool single = qs.NG == 1 && qs.T == 1 && qs.G == 1;
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     *abort = 0;
     fence_barrier_init();
   }
-  if (loader) {
+  if (w_loader) {
     tmem_alloc(tmem_slot, L::TCOLS);
     tmem_relinquish();
   }
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (loader && lane == 0) {
+  if (w_loader && lane == 0) {
     // W_UV is a weight: its first tiles load while the attention step finishes
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_p);
@@ -322,11 +341,13 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
       tma_load_3d(sm + L::OFF_W + kc * W_TILE, &tm_w, KC * kc, 0, hr, &w_full[kc]);
     }
   }
-  grid_dep_wait();  // the partials and their log-sum-exps
-  grid_dep_launch();
-
   // ---- the slots [s_lo, s_hi) that hold every segment of the group's rows:
-  // segment w + b of row b, rows and workers both increasing along the tiles
+  // segment w + b of row b, rows and workers both increasing along the tiles.
+  // The plan is read before the wait: every kernel of the decode chain waits
+  // for its predecessor before it lets the next one start, so the plan kernel
+  // has completed (and its writes are visible) once this grid runs at all;
+  // the attention step writes only the partials, their log-sum-exps and the
+  // exact-recompute flags, read after the wait.
   const long long T = plan[0], W = plan[1];
   const int* prefix = plan + PLAN_HDR;
   const int b_end = min(b0 + RB, B);
@@ -334,12 +355,23 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   const int s_lo = t1 > t0 ? worker_of_tile(t0, T, W) + b0 : 0;
   const int s_hi = t1 > t0 ? worker_of_tile(t1 - 1, T, W) + b_end : 0;
   const int nsub = (s_hi - s_lo + SEGB - 1) / SEGB;  // partial tiles per chunk (0 when every row is empty)
+  // this merge thread's row: its segments [rs.x, rs.y] (segment w + b of row
+  // b; empty when x > y)
+  const int r = tid >> 3, u = tid & 7;  // row of the group, 8-dim unit of the chunk
+  const int b = b0 + r;
+  int2 rs = make_int2(1, 0);
+  if (!loader && b < B) {
+    const int p0 = prefix[b], p1 = prefix[b + 1];
+    if (p1 > p0) rs = make_int2(worker_of_tile(p0, T, W) + b, worker_of_tile(p1 - 1, T, W) + b);
+  }
+  grid_dep_wait();  // the partials and their log-sum-exps
+  grid_dep_launch();
 
   if (loader) {
     // ------------------------------------------------------------ TMA loaders:
-    // lane 0 refills the W_UV ring, lane 1 streams the partial tiles (so
-    // neither ring waits for the other)
-    if (lane == 0) {
+    // lane 0 of warp NW refills the W_UV ring, lane 0 of warp NW + 1 streams
+    // the partial tiles
+    if (w_loader && lane == 0) {
       int wi = WST;  // W tiles issued so far
       for (int kc = WST; kc < NCHUNK; ++kc, ++wi) {  // stage kc % WST was read by chunk kc - WST's MMAs
         const int st = kc % WST;
@@ -349,7 +381,37 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
       }
       if (*abort)  // let copies in flight land before the CTA exits
         for (int k = max(0, wi - WST); k < wi; ++k) (void)mbar_wait(&w_full[k % WST], (k / WST) & 1);
-    } else if (lane == 1) {
+    } else if (warp == NW + 2 && lane == 0) {
+      // ---------------------------------------------------------- MMA issue
+      //   D[128 out dims][RB rows] += W_UV[h][:, chunk] . hi^T + W_UV[h][:, chunk] . lo^T
+      // (the 8 MMAs of a chunk take about 0.45 us to issue)
+      const uint32_t idesc = idesc_bf16_f32(128, RB, false, false);
+      bool final_commit = false;
+      for (int kc = 0; kc < NCHUNK; ++kc) {
+        const int bs = kc % BST, ws = kc % WST;
+        if (!cwait(&b_full[bs], (kc / BST) & 1, abort, err, 4) || !cwait(&w_full[ws], (kc / WST) & 1, abort, err, 5))
+          break;
+        fence_after_sync();
+        const uint32_t wa = smem_u32(sm + L::OFF_W + ws * W_TILE), ba = smem_u32(sm + L::OFF_B + bs * 2 * L::B_TILE);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kk = 0; kk < KC / 16; ++kk)
+            mma_ss(tmem, smem_desc(wa + kk * 32, 16, 1024, SWIZZLE_128B),
+                   smem_desc(ba + part * L::B_TILE + kk * 32, 16, 1024, SWIZZLE_128B), idesc,
+                   (kc | part | kk) != 0 ? 1u : 0u);
+        mma_commit(&b_free[bs]);
+        mma_commit(&w_empty[ws]);
+        if (kc == NCHUNK - 1) {
+          mma_commit(d_full);
+          final_commit = true;
+        }
+      }
+      if (*abort) {  // MMAs in flight finish before TMEM is freed
+        if (!final_commit) mma_commit(d_full);
+        (void)mbar_wait(d_full, 0);
+      }
+    } else if (warp == NW + 1 && lane == 0) {
       int pu = 0;  // partial tiles issued so far
       bool ok = true;
       for (int kc = 0; kc < NCHUNK && ok; ++kc) {
@@ -360,8 +422,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
           const int nbox = (min(SEGB, s_hi - s_lo - SEGB * sub) + SBOX - 1) / SBOX;
           mbar_arrive_expect_tx(&p_full[st], (uint32_t)nbox * SBOX * KC * 2);
           for (int j = 0; j < nbox; ++j)
-            tma_load_3d(sm + L::OFF_P + st * P_TILE + j * SBOX * KC * 2, &tm_p, KC * kc, h,
-                        s_lo + SEGB * sub + SBOX * j, &p_full[st]);
+            tma_load_3d(sm + L::OFF_P + st * P_TILE + j * SBOX * KC * 2, &tm_p, KC * kc,
+                        s_lo + SEGB * sub + SBOX * j, h, &p_full[st]);
         }
       }
       if (*abort)
@@ -369,18 +431,10 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ merge warps
-    const int r = tid >> 3, u = tid & 7;  // row of the group, 8-dim unit of the chunk
-    const int b = b0 + r;
     const long long orow = b < B ? out_row(b) : -1;
-    // ---- the row's segments [rs.x, rs.y] (segment w + b of row b; empty when
-    // x > y) and their softmax weights e^{LSE_s - LSE} into wgt, the row's
-    // 8 threads sharing the segments (a worker without tiles left no partial:
+    // ---- the row's softmax weights e^{LSE_s - LSE} into wgt, the row's 8
+    // threads sharing the segments (a worker without tiles left no partial:
     // weight 0).  Slots between rows are never read.
-    int2 rs = make_int2(1, 0);
-    if (b < B) {
-      const int p0 = prefix[b], p1 = prefix[b + 1];
-      if (p1 > p0) rs = make_int2(worker_of_tile(p0, T, W) + b, worker_of_tile(p1 - 1, T, W) + b);
-    }
     float mx = -INFINITY;
     for (int s = rs.x + u; s <= rs.y; s += 8) {
       const long long w = s - b;
@@ -402,9 +456,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int s = rs.x + u; s <= rs.y; s += 8) wgt[s - s_lo] *= inv;
     __syncwarp();  // the row's weights, written by its 8 threads (one warp)
-    const uint32_t idesc = idesc_bf16_f32(128, RB, false, false);
     int pu = 0;
-    bool ok = true, final_commit = false;
+    bool ok = true;
     for (int kc = 0; kc < NCHUNK && ok; ++kc) {
       float acc[8];
 #pragma unroll
@@ -454,29 +507,6 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
       fence_proxy_async_smem();  // generic writes -> the tensor core's reads
       __syncwarp();
       if (lane == 0) mbar_arrive(&b_full[bs]);
-      if (tid == 0) {
-        // ------------------------------------------------ MMA issue (one thread)
-        const int ws = kc % WST;
-        if (!cwait(&b_full[bs], (kc / BST) & 1, abort, err, 4) || !cwait(&w_full[ws], (kc / WST) & 1, abort, err, 5)) {
-          ok = false;
-          break;
-        }
-        fence_after_sync();
-        const uint32_t wa = smem_u32(sm + L::OFF_W + ws * W_TILE), ba = smem_u32(bt);
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int kk = 0; kk < KC / 16; ++kk)
-            mma_ss(tmem, smem_desc(wa + kk * 32, 16, 1024, SWIZZLE_128B),
-                   smem_desc(ba + part * L::B_TILE + kk * 32, 16, 1024, SWIZZLE_128B), idesc,
-                   (kc | part | kk) != 0 ? 1u : 0u);
-        mma_commit(&b_free[bs]);
-        mma_commit(&w_empty[ws]);
-        if (kc == NCHUNK - 1) {
-          mma_commit(d_full);
-          final_commit = true;
-        }
-      }
     }
     // ---- epilogue: D[out dim][row] -> out[b][h][:] (bf16)
     if (ok && cwait(d_full, 0, abort, err, 6)) {
@@ -495,14 +525,10 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
         }
       }
     }
-    if (tid == 0 && *abort) {  // MMAs in flight finish before TMEM is freed
-      if (!final_commit) mma_commit(d_full);
-      (void)mbar_wait(d_full, 0);
-    }
   }
   fence_before_sync();
   __syncthreads();
-  if (loader) {
+  if (w_loader) {
     fence_after_sync();
     tmem_dealloc(tmem, L::TCOLS);
   }
@@ -563,7 +589,7 @@ struct __align__(16) SmallSmem {
 };
 
 __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __restrict__ W_UV, int H, int B,
-                                                            const int* __restrict__ plan,
+                                                            const int* __restrict__ plan, int segs,
                                                             const uint16_t* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             uint16_t* __restrict__ out, float* __restrict__ o_lat,
@@ -595,8 +621,8 @@ __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __re
     // worker without tiles left no partial: weight 0, its slot's undefined bits
     // loaded with the others and discarded)
     const int sx = worker_of_tile(prefix[b], T, W) + b, sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
-    const size_t stride = (size_t)H * DC / 4;  // one segment, in 4-value units
-    const uint2* po = reinterpret_cast<const uint2*>(part_o + (size_t)h * DC) + rt;
+    const size_t stride = DC / 4;  // one segment, in 4-value units (head-major partials)
+    const uint2* po = reinterpret_cast<const uint2*>(part_o + (size_t)h * segs * DC) + rt;
     float m = -INFINITY, den = 0.f;
     for (int c0 = sx; c0 <= sy; c0 += SCH) {
       const int cn = min(SCH, sy - c0 + 1);
@@ -711,21 +737,27 @@ cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, co
     cudaError_t e = cudaFuncSetAttribute(combine_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(combine_small_kernel, dim3(Hv, (Bv + SRB - 1) / SRB), dim3(SNT), smem, s,
-                      static_cast<const uint16_t*>(W_UV), Hv, Bv, plan, part_o, part_lse, static_cast<uint16_t*>(out),
+                      static_cast<const uint16_t*>(W_UV), Hv, Bv, plan, max_workers + Bv, part_o, part_lse,
+                      static_cast<uint16_t*>(out),
                       o_lat, err);
   }
   CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
   if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // partials (bf16): (512 latent, Hv heads, segments), boxes of 64 dims x 1 head x 16 segments
+  // partials (bf16, head-major): (512 latent, segments, Hv heads), boxes of 64 dims x 64 segments x 1 head
+  // (segments past the buffer read as zeros, without memory traffic)
   const uint64_t segs = (uint64_t)max_workers + Bv;
-  if (!encode_3d_box(&tm_p, part_o, DC, Hv, segs, DC * 2, (uint64_t)Hv * DC * 2, KC, 1, SBOX,
+  if (!encode_3d_box(&tm_p, part_o, DC, segs, Hv, DC * 2, segs * DC * 2, KC, SBOX, 1,
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
-  // rows per CTA: 32 when that still gives every SM a CTA, else 16 (few heads or rows)
+  // rows per CTA: 64 (W_UV of the head loaded whole, one CTA per SM) when one
+  // wave of such CTAs covers the grid; else 32 when that still gives every SM
+  // a CTA; else 16 (few heads or rows)
   const int sms = device_sm_count();
   cudaError_t e;
-  if ((long long)Hv * ((Bv + 31) / 32) >= sms)
+  if (Bv > 32 && (long long)Hv * ((Bv + 63) / 64) <= sms)
+    e = launch_rb<64>(tm_w, tm_p, W_UV, Hv, Bv, qs, plan, part_lse, out, o_lat, err, max_workers, s);
+  else if ((long long)Hv * ((Bv + 31) / 32) >= sms)
     e = launch_rb<32>(tm_w, tm_p, W_UV, Hv, Bv, qs, plan, part_lse, out, o_lat, err, max_workers, s);
   else
     e = launch_rb<16>(tm_w, tm_p, W_UV, Hv, Bv, qs, plan, part_lse, out, o_lat, err, max_workers, s);

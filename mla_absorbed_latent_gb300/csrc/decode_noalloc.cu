@@ -101,8 +101,8 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
 
   if (launch_plan(seqlens, B, qspec_single(H), max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers, part_o, part_lse,
-                         err, stream) != cudaSuccess)
+  if (launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers,
+                         L.max_segments, part_o, part_lse, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (launch_combine(W_UV, H, B, qspec_single(H), plan, part_o, part_lse, out, nullptr, err, workers, stream) != cudaSuccess)
     return MLA_ERR_CUDA;

@@ -110,17 +110,17 @@ int attend_workers(int kind, int sms) {
 }
 cudaError_t launch_attend_kind(int kind, const void* q_cat, int H, const mla_cache_t* cache,
                                const int32_t* page_table, int max_pages, int B, float scale, int* plan, int workers,
-                               uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
+                               int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s) {
   switch (kind) {
     case MLA_KERNEL_TCGEN05:
       return launch_attend_tc(q_cat, qspec_single(H), layout_fmt(cache->fmt), cache->num_pages, cache->pages,
-                              page_table, max_pages, B, scale, plan, workers, part_o, part_lse, err, s);
+                              page_table, max_pages, B, scale, plan, workers, seg_cap, part_o, part_lse, err, s);
     case MLA_KERNEL_MMA:
       return launch_attend_mma(q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B, scale,
-                               plan, workers, part_o, part_lse, err, s);
+                               plan, workers, seg_cap, part_o, part_lse, err, s);
     case MLA_KERNEL_CUDA_CORES:
       return launch_attend_cc(q_cat, H, cache->fmt, cache->num_pages, cache->pages, page_table, max_pages, B, scale,
-                              plan, workers, part_o, part_lse, err, s);
+                              plan, workers, seg_cap, part_o, part_lse, err, s);
     default:
       return cudaErrorNotSupported;
   }
@@ -291,7 +291,7 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
   const int sms = num_sms();
   const int workers = attend_workers(kind, sms);
   return status_of(launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers,
-                                      part_o, part_lse, err, stream));
+                                      L.max_segments, part_o, part_lse, err, stream));
 }
 
 int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes, void* out,
@@ -397,7 +397,7 @@ int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const v
   if (e == cudaSuccess) e = launch_q_absorb(q_nope, q_pe, W_UK, H, B * T, ws + L.q_cat, stream);
   if (e == cudaSuccess)
     e = launch_attend_tc(ws + L.q_cat, qs, layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, Bv,
-                         scale, plan, workers, part_o, part_lse, err, stream);
+                         scale, plan, workers, L.max_segments, part_o, part_lse, err, stream);
   if (e == cudaSuccess)
     e = launch_combine(W_UV, 128, Bv, qs, plan, part_o, part_lse, out, o_lat_out, err, L.max_segments - Bv, stream);
   return status_of(e);

@@ -44,7 +44,11 @@ __device__ __forceinline__ void raise_error(int* err, int code, int info) {
 }
 
 // ---------------------------------------------------------------------------
-// decode workspace: [q_cat bf16 B*H*576][plan int32][partial O bf16][partial lse fp32]
+// decode workspace: [q_cat bf16 B*H*576][plan int32][partial O bf16][partial lse fp32].
+// The partial O is head-major, bf16 [heads][max_segments][512] (segment s of
+// head h at (h * max_segments + s) * 512): the merge of a head reads its rows'
+// segments from one contiguous block; the partial LSE is fp32
+// [max_segments][heads].
 // ---------------------------------------------------------------------------
 struct WsLayout {
   size_t q_cat, plan, part_o, part_lse, total;
@@ -265,16 +269,16 @@ cudaError_t launch_plan(const int32_t* seqlens, int B, const QSpec& qs, int max_
                         int* err, cudaStream_t s);
 cudaError_t launch_attend_cc(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
+                             int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_cc_workers(int num_sms);
 cudaError_t launch_attend_mma(const void* q_cat, int H, int fmt, int num_pages, const void* pages,
                               const int32_t* page_table, int max_pages, int B, float scale, const int* plan,
-                              int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
+                              int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_mma_workers(int num_sms);
 // Bv virtual rows of the query layout qs (q_cat: Bv / qs.NG * qs.T * qs.Hr flat rows)
 cudaError_t launch_attend_tc(const void* q_cat, const QSpec& qs, int fmt, int num_pages, const void* pages,
                              const int32_t* page_table, int max_pages, int Bv, float scale, int* plan,
-                             int workers, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
+                             int workers, int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 int attend_tc_workers(int num_sms);
 // a CTA pair whose bounded wait runs out on purpose (see mla_wait_selftest)
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
@@ -286,7 +290,7 @@ int attend_workers(int kind, int sms);   // persistent workers of that kernel
 // the single-query attend step with the kernel `kind` (B rows, H heads)
 cudaError_t launch_attend_kind(int kind, const void* q_cat, int H, const mla_cache_t* cache,
                                const int32_t* page_table, int max_pages, int B, float scale, int* plan, int workers,
-                               uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
+                               int seg_cap, uint16_t* part_o, float* part_lse, int* err, cudaStream_t s);
 
 // Hv heads of the partials (virtual heads), Bv plan rows, query layout qs;
 // unabsorbed causal prefill (prefill.cu): expand the rows' latents into per-head
