@@ -471,14 +471,24 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
         const uint16_t* tile = reinterpret_cast<const uint16_t*>(sm + L::OFF_P + st * P_TILE);
         const int base = s_lo + SEGB * sub;
         const int sa = max(rs.x, base), sz = min(rs.y, base + SEGB - 1);
-        for (int s = sa; s <= sz; ++s) {
-          const float wv = wgt[s - s_lo];
-          if (wv == 0.f) continue;  // a slot no worker wrote (its contents are undefined)
-          const uint4 v = *reinterpret_cast<const uint4*>(tile + (s - base) * KC + 8 * u);  // 8 bf16
-          acc[0] = fmaf(wv, bf16lo(v.x), acc[0]); acc[1] = fmaf(wv, bf16hi(v.x), acc[1]);
-          acc[2] = fmaf(wv, bf16lo(v.y), acc[2]); acc[3] = fmaf(wv, bf16hi(v.y), acc[3]);
-          acc[4] = fmaf(wv, bf16lo(v.z), acc[4]); acc[5] = fmaf(wv, bf16hi(v.z), acc[5]);
-          acc[6] = fmaf(wv, bf16lo(v.w), acc[6]); acc[7] = fmaf(wv, bf16hi(v.w), acc[7]);
+        for (int s0 = sa; s0 <= sz; s0 += 4) {  // four segments' loads at once
+          float wv[4];
+          uint4 v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bool in = s0 + k <= sz;
+            wv[k] = in ? wgt[s0 + k - s_lo] : 0.f;
+            v[k] = in ? *reinterpret_cast<const uint4*>(tile + (s0 + k - base) * KC + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (wv[k] == 0.f) continue;  // a slot no worker wrote (its contents are undefined)
+            const float w = wv[k];
+            acc[0] = fmaf(w, bf16lo(v[k].x), acc[0]); acc[1] = fmaf(w, bf16hi(v[k].x), acc[1]);
+            acc[2] = fmaf(w, bf16lo(v[k].y), acc[2]); acc[3] = fmaf(w, bf16hi(v[k].y), acc[3]);
+            acc[4] = fmaf(w, bf16lo(v[k].z), acc[4]); acc[5] = fmaf(w, bf16hi(v[k].z), acc[5]);
+            acc[6] = fmaf(w, bf16lo(v[k].w), acc[6]); acc[7] = fmaf(w, bf16hi(v[k].w), acc[7]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[st]);
