@@ -23,6 +23,7 @@
 // W_UV[h] streams through a 2-stage ring of 128B-swizzled TMA tiles whose first
 // loads are issued before the kernel waits for the attention step.
 #include "tc_ptx.cuh"
+#include "warp_mma.cuh"
 
 namespace mla {
 namespace {
@@ -575,37 +576,41 @@ __global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, in
 
 // ---------------------------------------------------------------------------
 // The merge and the up-projection for few heads (the 16-head single-query
-// decode), on CUDA cores in fp32: the tensor-core kernel above gives each
-// (head, 16..32 rows) one CTA, only 32 CTAs for 16 heads and a 32-row batch, and
-// its chunk loop is then latency-bound.  Here one CTA per (head, group of 4
-// rows): W_UV[h] (128 KB) is copied into shared memory before the kernel waits
-// for the attention step.  Each row has a quarter of the block (4 latent dims
-// per thread) and merges its segments 8 at a time, every load of a chunk (the
-// 8 log-sum-exps and the 8 partials) in flight at once, as an online softmax
-// over the segments ("kv_budget.py" part C: o_lat = sum_s e^{LSE_s - LSE} o_s
-// with LSE = log sum_s e^{LSE_s}, the running maximum moved per chunk).  Then
-// out[b, h, :] = W_UV[h] o_lat[b, h, :]: each warp forms 8 output dims of the
-// 4 rows, lane-partial dot products reduced across the warp by a butterfly
-// reduce-scatter that leaves lane L with output 8 warp + L / 4 of row L % 4.
+// decode): the tensor-core kernel above gives each (head, 16..32 rows) one CTA,
+// only 32 CTAs for 16 heads and a 32-row batch, and its chunk loop is then
+// latency-bound.  Here one CTA per (head, group of 4 rows): W_UV[h] (128 KB)
+// arrives by TMA as eight 128B-swizzled [128 out dims][64 latent] tiles before
+// the kernel waits for the attention step.  Each row has a quarter of the
+// block (4 latent dims per thread) and merges its segments 8 at a time in
+// fp32, every load of a chunk (the 8 log-sum-exps and the 8 partials) in
+// flight at once, as an online softmax over the segments ("kv_budget.py" part
+// C: o_lat = sum_s e^{LSE_s - LSE} o_s with LSE = log sum_s e^{LSE_s}, the
+// running maximum moved per chunk).  o_lat is then split into a bf16 high part
+// and a bf16 residual, written as 128B-swizzled operand rows (the group's 4,
+// then zero rows) of the warp-level tensor-core MMA (mma.sync m16n8k16):
+// out[b, h, :] = W_UV[h] o_lat[b, h, :] = W_UV[h] hi + W_UV[h] lo, fp32 accumulation
+// (the same roundings as the tensor-core kernel: W_UV's own bf16 and the
+// residual's, relative 2^-16), computed as out^T = W_UV[h] . o_lat^T so that
+// the 128 out dims are the MMA's M and the 4 rows pad only to its N of 8.
 // ---------------------------------------------------------------------------
 constexpr int SRB = 4;      // rows per CTA
-constexpr int SNT = 512;    // threads: a quarter of the block per row in the merge, 8 output dims per warp after it
+constexpr int SNT = 512;    // threads: a quarter of the block per row in the merge, 16 out dims x half the latent per warp after it
 constexpr int SCH = 8;      // segments per merge chunk
 
-struct __align__(16) SmallSmem {
-  uint16_t w[DV * DC];           // W_UV[h], 128 KB
-  float ol[SRB][DC];             // o_lat of the rows
+struct __align__(1024) SmallSmem {
+  uint8_t w[DC / 64][DV * 128];   // W_UV[h]: [128 out dims][64 latent] per 64-wide chunk, 128B-swizzled
+  uint8_t a[2][DC / 64][16 * 128];  // o_lat hi / lo: [16 rows][64 latent] per chunk, 128B-swizzled
   uint64_t w_full;
 };
 
-__global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __restrict__ W_UV, int H, int B,
+__global__ void __launch_bounds__(SNT) combine_small_kernel(const __grid_constant__ CUtensorMap tm_w, int H, int B,
                                                             const int* __restrict__ plan, int segs,
                                                             const uint16_t* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             uint16_t* __restrict__ out, float* __restrict__ o_lat,
                                                             int* err) {
   extern __shared__ uint8_t smem_raw[];
-  SmallSmem& S = *reinterpret_cast<SmallSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  SmallSmem& S = *reinterpret_cast<SmallSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int h = blockIdx.x, b0 = blockIdx.y * SRB, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(&S.w_full, 1);
@@ -613,24 +618,34 @@ __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __re
   }
   __syncthreads();
   if (tid == 0) {  // W_UV[h] is a weight: its copy overlaps the attention step's tail
-    constexpr uint32_t CH = 32768;
+    prefetch_tmap(&tm_w);
     mbar_arrive_expect_tx(&S.w_full, DV * DC * 2);
-    for (uint32_t o = 0; o < DV * DC * 2; o += CH)
-      bulk_g2s_hint(reinterpret_cast<uint8_t*>(S.w) + o, reinterpret_cast<const uint8_t*>(W_UV + (size_t)h * DV * DC) + o,
-                    CH, &S.w_full, policy_evict_last());
+    for (int c = 0; c < DC / 64; ++c) tma_load_3d_hint(S.w[c], &tm_w, 64 * c, 0, h, &S.w_full, policy_evict_last());
   }
-  grid_dep_wait();  // the partials and their log-sum-exps
-  grid_dep_launch();
+  // the operand rows past the group's 4 are zeros (12 rows x 8 chunks x hi, lo)
+  for (int i = tid; i < 2 * (DC / 64) * 12 * 8; i += SNT) {
+    const int u = i & 7, row = 4 + (i >> 3) % 12, t = i / 96;  // t: hi/lo and chunk
+    *reinterpret_cast<uint4*>(&S.a[t >> 3][t & 7][row * 128 + u * 16]) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // the row's segments [sx, sy] (segment w + b of row b for the workers w whose
+  // ranges hold its tiles), read before the wait: every kernel of the decode
+  // chain waits for its predecessor before it lets the next start, so the plan
+  // kernel has completed once this grid runs
   const long long T = plan[0], W = plan[1];
   const int* prefix = plan + PLAN_HDR;
   const int r = tid >> 7, rt = tid & 127;  // the row of the group, latent dims 4 rt .. 4 rt + 3
   const int b = b0 + r;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int sx = 1, sy = 0;
   if (b < B && prefix[b + 1] > prefix[b]) {
-    // segment w + b of row b for the workers w whose ranges hold its tiles (a
-    // worker without tiles left no partial: weight 0, its slot's undefined bits
-    // loaded with the others and discarded)
-    const int sx = worker_of_tile(prefix[b], T, W) + b, sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
+    sx = worker_of_tile(prefix[b], T, W) + b;
+    sy = worker_of_tile(prefix[b + 1] - 1, T, W) + b;
+  }
+  grid_dep_wait();  // the partials and their log-sum-exps
+  grid_dep_launch();
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (sx <= sy) {
+    // a worker without tiles left no partial: weight 0, its slot's undefined
+    // bits loaded with the others and discarded
     const size_t stride = DC / 4;  // one segment, in 4-value units (head-major partials)
     const uint2* po = reinterpret_cast<const uint2*>(part_o + (size_t)h * segs * DC) + rt;
     float m = -INFINITY, den = 0.f;
@@ -667,56 +682,68 @@ __global__ void __launch_bounds__(SNT) combine_small_kernel(const uint16_t* __re
     const float inv = 1.f / den;  // den >= 1: the largest term is e^0
     a0 *= inv; a1 *= inv; a2 *= inv; a3 *= inv;
   }
-  *reinterpret_cast<float4*>(&S.ol[r][4 * rt]) = make_float4(a0, a1, a2, a3);
   if (o_lat != nullptr && b < B)
     *reinterpret_cast<float4*>(o_lat + ((size_t)b * H + h) * DC + 4 * rt) = make_float4(a0, a1, a2, a3);
+  {
+    // o_lat = hi + lo (both bf16) into row r of the operand tiles: dims 4 rt .. +3
+    // are the half (rt & 1) of 16-byte unit (rt >> 1) & 7 of chunk rt >> 4
+    const uint32_t h0 = pack_bf16x2(a0, a1), h1 = pack_bf16x2(a2, a3);
+    const uint32_t l0 = pack_bf16x2(a0 - bf16lo(h0), a1 - bf16hi(h0)), l1 = pack_bf16x2(a2 - bf16lo(h1), a3 - bf16hi(h1));
+    const int c = rt >> 4, u = (rt >> 1) & 7;
+    const int off = r * 128 + ((u ^ r) << 4) + 8 * (rt & 1);  // rows 0..3: swizzle r & 7 = r
+    *reinterpret_cast<uint2*>(&S.a[0][c][off]) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(&S.a[1][c][off]) = make_uint2(l0, l1);
+  }
   __syncthreads();
   if (!mbar_wait(&S.w_full, 0)) {
     if (tid == 0) raise_error(err, MLA_ERR_TIMEOUT, 150);
     return;
   }
-  // ---- out[b][h][j] = W_UV[h][j, :] . o_lat[b]: warp `warp` takes output dims
-  // 8 warp .. 8 warp + 7, lane `lane` latent dims 8 lane .. +7 and 256 + 8 lane .. +7
-  float x[SRB][16];
+  // ---- out^T = W_UV[h] . hi^T + W_UV[h] . lo^T (M = 128 out dims, N = 8 rows of
+  // which the group's 4, K = 512): warp w takes out dims 16 (w % 8) .. + 15 over
+  // latent half w / 8, the hi and lo terms in two accumulators; the two halves
+  // are added through shared memory
+  const int mt = warp & 7, kh = warp >> 3;
+  float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int c = 4 * kh; c < 4 * kh + 4; ++c) {
+    const uint32_t wb = smem_u32(S.w[c]), ah = smem_u32(S.a[0][c]), al = smem_u32(S.a[1][c]);
 #pragma unroll
-  for (int q = 0; q < SRB; ++q)
+    for (int kp = 0; kp < 2; ++kp) {
+      // B: rows lane % 8 of o_lat (the 4 of the group, then zeros), latent
+      // 32 kp + 8 (lane / 8) (two k-steps); A: out dims 16 mt + lane % 16,
+      // latent 32 kp + 16 hk + 8 (lane / 16) of k-step hk
+      uint32_t bh[4], bl[4];
+      ldsm_x4(bh, ah + sw128(lane & 7, 4 * kp + (lane >> 3)));
+      ldsm_x4(bl, al + sw128(lane & 7, 4 * kp + (lane >> 3)));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      x[q][k] = S.ol[q][8 * lane + k];
-      x[q][8 + k] = S.ol[q][256 + 8 * lane + k];
-    }
-  float d[32];  // lane partials of output 8 warp + i / 4, row i % 4
-#pragma unroll
-  for (int jj = 0; jj < 8; ++jj) {
-    const uint4* wr = reinterpret_cast<const uint4*>(S.w + (size_t)(8 * warp + jj) * DC);
-    const uint4 u0 = wr[lane], u1 = wr[32 + lane];
-    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-    for (int q = 0; q < SRB; ++q) {
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        acc = fmaf(bf16lo(wv[k]), x[q][2 * k], acc);
-        acc = fmaf(bf16hi(wv[k]), x[q][2 * k + 1], acc);
+      for (int hk = 0; hk < 2; ++hk) {
+        uint32_t fa[4];
+        ldsm_x4(fa, wb + sw128(16 * mt + (lane & 15), 4 * kp + 2 * hk + (lane >> 4)));
+        mma_bf16_16816(dh, fa, bh[2 * hk], bh[2 * hk + 1]);
+        mma_bf16_16816(dl, fa, bl[2 * hk], bl[2 * hk + 1]);
       }
-      d[4 * jj + q] = acc;
     }
   }
-  // reduce-scatter across the warp: at offset o the lane keeps the half of its
-  // values selected by its bit o and adds the partner's copy of that half
+  // d[0], d[1]: out dim 16 mt + lane / 4, rows 2 (lane % 4), + 1; d[2], d[3]: out dim + 8
+  float* red = reinterpret_cast<float*>(S.a[0][0]);  // [8 m-tiles][32 lanes][4]: the upper latent half
+  __syncthreads();  // every warp has read the operand tiles
+  if (kh == 1)
+    *reinterpret_cast<float4*>(red + (mt * 32 + lane) * 4) =
+        make_float4(dh[0] + dl[0], dh[1] + dl[1], dh[2] + dl[2], dh[3] + dl[3]);
+  __syncthreads();
+  if (kh == 0 && (lane & 3) < SRB / 2) {
+    const float4 u = *reinterpret_cast<const float4*>(red + (mt * 32 + lane) * 4);
+    const float o[4] = {dh[0] + dl[0] + u.x, dh[1] + dl[1] + u.y, dh[2] + dl[2] + u.z, dh[3] + dl[3] + u.w};
+    const int j = 16 * mt + (lane >> 2);
 #pragma unroll
-  for (int o = 16, n = 16; o > 0; o >>= 1, n >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < n; ++i) {
-      const float keep = up ? d[i + n] : d[i], send = up ? d[i] : d[i + n];
-      d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    for (int k = 0; k < 4; ++k) {
+      const int row = 2 * (lane & 3) + (k & 1), jj = j + 8 * (k >> 1);
+      if (b0 + row < B) {
+        const __nv_bfloat16 ob = __float2bfloat16_rn(o[k]);
+        out[((size_t)(b0 + row) * H + h) * DV + jj] = *reinterpret_cast<const uint16_t*>(&ob);
+      }
     }
-  }
-  const int q = lane & 3, j = 8 * warp + (lane >> 2);
-  if (b0 + q < B) {
-    const __nv_bfloat16 ob = __float2bfloat16_rn(d[0]);
-    out[((size_t)(b0 + q) * H + h) * DV + j] = *reinterpret_cast<const uint16_t*>(&ob);
   }
 }
 
@@ -739,21 +766,19 @@ cudaError_t launch_combine(const void* W_UV, int Hv, int Bv, const QSpec& qs, co
                            const float* part_lse, void* out, float* o_lat, int* err, int max_workers,
                            cudaStream_t s) {
   if (Bv == 0) return cudaSuccess;
+  CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
+  if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   if (Hv < 128) {
     // the 16-head single-query decode (its attend kernels compute the defined
     // softmax themselves and flag no row, so no exact-recompute pass follows)
     if (qs.T != 1 || qs.G != 1 || qs.NG != 1 || qs.Hr != Hv) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(SmallSmem) + 16;
+    const size_t smem = sizeof(SmallSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(combine_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(combine_small_kernel, dim3(Hv, (Bv + SRB - 1) / SRB), dim3(SNT), smem, s,
-                      static_cast<const uint16_t*>(W_UV), Hv, Bv, plan, max_workers + Bv, part_o, part_lse,
-                      static_cast<uint16_t*>(out),
-                      o_lat, err);
+    return launch_pdl(combine_small_kernel, dim3(Hv, (Bv + SRB - 1) / SRB), dim3(SNT), smem, s, tm_w, Hv, Bv, plan,
+                      max_workers + Bv, part_o, part_lse, static_cast<uint16_t*>(out), o_lat, err);
   }
-  CUtensorMap tm_w, tm_p;  // W_UV: (512 latent, 128 rows, Hr heads), tiles of 64 x 128, 128B swizzle
-  if (!encode_3d(&tm_w, W_UV, DC, DV, qs.Hr, DC * 2, (uint64_t)DV * DC * 2, 64, DV, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
   // partials (bf16, head-major): (512 latent, segments, Hv heads), boxes of 64 dims x 64 segments x 1 head
   // (segments past the buffer read as zeros, without memory traffic)
   const uint64_t segs = (uint64_t)max_workers + Bv;
