@@ -87,10 +87,10 @@ def source_digest(text: str) -> str:
     return hashlib.sha256(code.encode()).hexdigest()
 
 
-def kernel_traffic(kind: str, fmt: str = "bf16"):
+def kernel_traffic(kind: str, fmt: str, workload: str, cache_bytes: int):
     """DRAM bytes per launch of the attend kernel from the committed ncu summary,
-    or None when missing or taken on a different kernel source (code, not
-    comments: see source_digest)."""
+    or None when missing, taken on a different kernel source (code, not
+    comments: see source_digest) or on another workload or size."""
     path = os.path.join(ROOT, "profiles", "attend_traffic.json")
     try:
         with open(path) as f:
@@ -99,6 +99,8 @@ def kernel_traffic(kind: str, fmt: str = "bf16"):
         with open(src, encoding="utf-8") as f:
             h = source_digest(f.read())
         if h != d["source_digest"] or d.get("kind") != kind or d.get("fmt", "bf16") != fmt:
+            return None
+        if d.get("workload_name") != workload or int(d.get("cache_bytes", -1)) != int(cache_bytes):
             return None
         return int(d["dram_bytes_per_launch"])
     except Exception:
@@ -570,7 +572,7 @@ def run_ours(args, wl, fmt):
     value = job_throughput(cache_bytes, world, ms_step)
     attend_gbs = cache_bytes / (attend_ms * 1e-3) / 1e9
     flops_tok = 2 * H * (576 + 512)
-    traffic = kernel_traffic(kind_name, fmt)
+    traffic = kernel_traffic(kind_name, fmt, wl.name, cache_bytes)
     if kind == mla.MLA_KERNEL_MMA:
         # 16 heads: 30 FLOP per cache byte, far below any tensor ridge; the cache stream binds
         tflops = cache_bytes / BYTES_PER_TOKEN[fmt] * flops_tok / (attend_ms * 1e-3) / 1e12

@@ -27,7 +27,7 @@ def _fake_root(tmp_path, source_text=b"__global__ void k() {}\n", record=None):
 
 def _record(source_text, **over):
     d = {"source": "attend_tc.cu", "source_digest": bench.source_digest(source_text.decode()), "kind": "tcgen05",
-         "fmt": "bf16", "dram_bytes_per_launch": 617000000}
+         "fmt": "bf16", "workload_name": "v3_paged", "cache_bytes": 603979776, "dram_bytes_per_launch": 617000000}
     d.update(over)
     return d
 
@@ -35,10 +35,10 @@ def _record(source_text, **over):
 def test_traffic_is_reported_for_the_captured_source(tmp_path, monkeypatch):
     src = b"__global__ void attend() {}\n"
     monkeypatch.setattr(bench, "ROOT", str(_fake_root(tmp_path, src, _record(src))))
-    assert bench.kernel_traffic("tcgen05", "bf16") == 617000000
+    assert bench.kernel_traffic("tcgen05", "bf16", "v3_paged", 603979776) == 617000000
 
 
-@pytest.mark.parametrize("change", ["source", "kind", "fmt", "missing"])
+@pytest.mark.parametrize("change", ["source", "kind", "fmt", "workload", "size", "missing"])
 def test_traffic_is_dropped_when_it_no_longer_describes_the_kernel(tmp_path, monkeypatch, change):
     src = b"__global__ void attend() {}\n"
     rec = _record(src)
@@ -50,7 +50,9 @@ def test_traffic_is_dropped_when_it_no_longer_describes_the_kernel(tmp_path, mon
         rec["fmt"] = "int8"
     root = _fake_root(tmp_path, src, None if change == "missing" else rec)
     monkeypatch.setattr(bench, "ROOT", str(root))
-    assert bench.kernel_traffic("tcgen05", "bf16") is None
+    workload, size = ("v3_ragged", 603979776) if change == "workload" else ("v3_paged", 150994944) if change == "size" \
+        else ("v3_paged", 603979776)
+    assert bench.kernel_traffic("tcgen05", "bf16", workload, size) is None
 
 
 def test_digest_follows_code_not_comments():
