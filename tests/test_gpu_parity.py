@@ -328,6 +328,32 @@ def test_decode_split_count_invariance(H):
                                     dev.ws_bytes)
 
 
+@pytest.mark.parametrize("B", [20, 37, 65])
+def test_decode_h128_merge_row_groups(B):
+    """H=128 batches that pick each shape of the merge kernel (16 rows per CTA at
+    B=20, 64 rows at B=37 with padding rows past the batch, 32 rows at B=65 with a
+    partial last group), seeded lengths from 0 to 2,000 tokens with an empty row
+    and a one-token row: out and o_lat of every row against the oracle."""
+    rng = np.random.default_rng(400 + B)
+    seqlens = [int(n) for n in rng.integers(1, 2000, size=B)]
+    seqlens[3], seqlens[B // 2] = 0, 1
+    prob = make_problem(128, seqlens, seed=400 + B)
+    dev = DeviceDecode(prob)
+    o_lat = torch.full((prob.B, 128, 512), float("nan"), dtype=torch.float32, device="cuda")
+    dev.workspace.fill_(0xFF)
+    dev.decode_steps(o_lat)
+    torch.cuda.synchronize()
+    _status_ok()
+    rows = [b for b, n in enumerate(seqlens) if n > 0]
+    ref = oracle_rows(prob, rows)
+    got = _out_f64(dev.out)
+    lat = o_lat.cpu().numpy().astype(np.float64)
+    for b in rows:
+        assert_close(got[b], ref[b][0], what=f"out[{b}]")
+        assert_close(lat[b], ref[b][1], what=f"o_lat[{b}]")
+    assert torch.count_nonzero(dev.out[3]) == 0
+
+
 def test_decode_row_independence():
     """H=128: a row's output does not depend on the other rows.  Changing every
     other row's queries and cache contents (lengths kept, so the split plan is
