@@ -338,6 +338,86 @@ def q_len_of(args, wl):
     return wl.q_len if wl.q_len > 1 else None
 
 
+E2E_PIPELINE_BYTES = 1 << 20  # a step's copies from which the end-to-end loop overlaps them with the neighbours
+
+
+def e2e_loop(torch, stream, steps, h_in, dev_in, h_out, dev_out, run):
+    """(ms per step, how the copies ran) of the end-to-end loop through the
+    public call.  Every step copies its inputs from pinned host memory and its
+    result back; with at least E2E_PIPELINE_BYTES of copies per step they run on
+    copy streams overlapping the neighbouring steps (pipelined_e2e), else in
+    line on the compute stream (measured on GB300: overlapping 5 MB per step
+    raises the v3_paged figure by 18 %, overlapping 0.3 MB lowers the v2lite one,
+    the cross-stream events costing more than the copies they hide)."""
+    nbytes = sum(t.numel() * t.element_size() for t in h_in) + h_out.numel() * h_out.element_size()
+    if nbytes >= E2E_PIPELINE_BYTES:
+        return (pipelined_e2e(torch, stream, steps, h_in, dev_in, h_out, dev_out, run),
+                "every step: its query from pinned host memory in and its output to pinned host memory out, on copy "
+                "streams with double-buffered device tensors (overlapping the neighbouring steps)")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        for h, d in zip(h_in, dev_in[0]):
+            d.copy_(h, non_blocking=True)
+        run(dev_in[0], dev_out[0])
+        h_out.copy_(dev_out[0], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return (e0.elapsed_time(e1) / steps,
+            "every step: its query from pinned host memory in and its output to pinned host memory out, in line on "
+            "the compute stream (under 1 MB of copies per step)")
+
+
+def pipelined_e2e(torch, stream, steps, h_in, dev_in, h_out, dev_out, run):
+    """ms per step of a serving loop through the public call: every step copies
+    its inputs from pinned host memory and its result back to pinned host
+    memory.  The copies run on their own streams (host-to-device, device-to-host)
+    with the device buffers doubled, so step k+1's inputs arrive and step k's
+    result leaves while the GPU computes (a step's own copies never overlap its
+    call).  h_in: pinned host inputs; dev_in: two lists of device inputs (one per
+    buffer); dev_out: two device results; run(inputs, result) enqueues one call
+    on `stream`."""
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    h2d.wait_stream(stream)
+    d2h.wait_stream(stream)
+
+    def load(k):
+        i = k % 2
+        with torch.cuda.stream(h2d):
+            if k >= 2:
+                h2d.wait_event(ev_done[i])  # the call of step k - 2 has read buffer i
+            for h, d in zip(h_in, dev_in[i]):
+                d.copy_(h, non_blocking=True)
+            ev_in[i].record(h2d)
+
+    load(0)
+    for k in range(steps):
+        i = k % 2
+        if k + 1 < steps:
+            load(k + 1)
+        stream.wait_event(ev_in[i])
+        if k >= 2:
+            stream.wait_event(ev_out[i])  # step k - 2's result has been read back
+        run(dev_in[i], dev_out[i])
+        ev_done[i].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_done[i])
+            h_out.copy_(dev_out[i], non_blocking=True)
+            ev_out[i].record(d2h)
+    stream.wait_stream(h2d)
+    stream.wait_stream(d2h)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_ours_q(args, wl, fmt, T):
     """One step = one mla_decode_q call: T causal query tokens per row."""
     import torch
@@ -381,18 +461,15 @@ def run_ours_q(args, wl, fmt, T):
 
     h_qn, h_qp = d_qn.cpu().pin_memory(), d_qp.cpu().pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 20))
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        d_qn.copy_(h_qn, non_blocking=True)
-        d_qp.copy_(h_qp, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    def call_q(ins, res):
+        mla.mla_decode_q(ins[0], ins[1], dev.W_UK, dev.W_UV, H, T, dev.cache, dev.page_table, prob.max_pages,
+                         dev.seqlens, B, prob.scale, ws, ws_bytes, res, None, stream)
+
+    e2e_ms, e2e_copies = e2e_loop(torch, stream, e2e_steps, [h_qn, h_qp],
+                                  [[d_qn, d_qp], [torch.empty_like(d_qn), torch.empty_like(d_qp)]], h_out,
+                                  [out, torch.empty_like(out)], call_q)
 
     cpu, parity = None, None
     if not args.no_cpu_baseline:
@@ -436,7 +513,8 @@ def run_ours_q(args, wl, fmt, T):
         "cpu_baseline": cpu,
         "parity": parity,
         "e2e": {"value": cache_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h_qn.numel() * 2 + h_qp.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2},
+                "h2d_bytes_per_step": h_qn.numel() * 2 + h_qp.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 2,
+                "copies": e2e_copies},
         "gpu_launches": 5 * args.steps,  # plan, q-absorb, attend, merge, exact-recompute check
         "clocks": clock_info,
     }
@@ -532,18 +610,16 @@ def run_ours(args, wl, fmt):
     h_qn = dev.q_nope.cpu().pin_memory()
     h_qp = dev.q_pe.cpu().pin_memory()
     h_out = torch.empty(dev.out.shape, dtype=dev.out.dtype).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 20))
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        dev.q_nope.copy_(h_qn, non_blocking=True)
-        dev.q_pe.copy_(h_qp, non_blocking=True)
-        dev.decode(stream)
-        h_out.copy_(dev.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    p_ = dev.prob
+
+    def call(ins, res):
+        mla.mla_decode(ins[0], ins[1], dev.W_UK, dev.W_UV, p_.H, dev.cache, dev.page_table, p_.max_pages,
+                       dev.seqlens, p_.B, p_.scale, dev.workspace, dev.ws_bytes, res, stream)
+
+    e2e_ms, e2e_copies = e2e_loop(torch, stream, e2e_steps, [h_qn, h_qp],
+                                  [[dev.q_nope, dev.q_pe], [torch.empty_like(dev.q_nope), torch.empty_like(dev.q_pe)]],
+                                  h_out, [dev.out, torch.empty_like(dev.out)], call)
     h2d = h_qn.numel() * 2 + h_qp.numel() * 2
     d2h = h_out.numel() * 2
 
@@ -617,7 +693,7 @@ def run_ours(args, wl, fmt):
         "cpu_baseline": cpu,
         "parity": parity,  # the oracle rows of cpu_baseline against the timed decode's output
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "copies": e2e_copies},
         # plan, absorb_q, attend, combine (merge + up-projection) and, after the tcgen05 kernel, the exact-recompute check
         "gpu_launches": (5 if kind == mla.MLA_KERNEL_TCGEN05 else 4) * args.steps,
         "clocks": clock_info,
