@@ -8,20 +8,20 @@
 // ("手搓 MLA" §四, einsum("thc,hdc->thd", out_lat, W_UV)).
 //
 // One CTA per (head h, group of RB rows).  The segments of a group's rows are
-// consecutive slots of the partial buffer (slot w + b for worker w, row b), so
+// consecutive slots of the partial buffer (slot w + b for worker w, row b), and
+// the partials are head-major (a head's segments are consecutive 1 KB rows), so
 // for every 64-wide latent chunk TMA boxes of 64 segments bring that chunk of
-// up to 128 segments at a time ([segments][64] bf16) into shared memory, as
-// many boxes as the group's segments need (head-major partials: a head's
-// segments are consecutive 1 KB rows).  The merge threads (one
-// per row and 8-dim unit) sum their row's segments with the softmax weights,
-// round o_lat once into a bf16 high part and a bf16 residual, and write both
-// as K-major 128B-swizzled operand tiles; one thread then issues the
-// fifth-generation tensor-core MMAs
+// the group's segments ([segments][64] bf16) into a ring slot, as many boxes as
+// the group needs.  The merge warps (a thread per row and 8-dim unit) sum their
+// row's segments with the softmax weights, round o_lat once into a bf16 high
+// part and a bf16 residual, and write both as K-major 128B-swizzled operand
+// tiles; an MMA warp issues the fifth-generation tensor-core MMAs
 //   D[128 out dims][RB rows] += W_UV[h][:, chunk] . hi^T + W_UV[h][:, chunk] . lo^T
 // (M = 128, N = RB, K = 64 per chunk), so the only roundings left are W_UV's
 // own bf16, the residual's (relative 2^-16) and the fp32 accumulation.
-// W_UV[h] streams through a 2-stage ring of 128B-swizzled TMA tiles whose first
-// loads are issued before the kernel waits for the attention step.
+// W_UV[h] streams through a ring of 128B-swizzled TMA tiles whose first loads
+// are issued before the kernel waits for the attention step; the two rings
+// have a loader warp each.
 #include "tc_ptx.cuh"
 #include "warp_mma.cuh"
 
