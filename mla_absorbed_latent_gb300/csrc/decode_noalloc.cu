@@ -100,7 +100,7 @@ extern "C" int mla_decode_noalloc(const void* q_nope, const void* q_pe, const vo
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
 
   if (launch_plan(seqlens, B, qspec_single(H), max_pages, workers, plan, err, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, true, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_attend_kind(kind, ws + L.q_cat, H, cache, page_table, max_pages, B, scale, plan, workers,
                          L.max_segments, part_o, part_lse, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;

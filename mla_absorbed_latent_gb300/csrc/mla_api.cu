@@ -206,8 +206,12 @@ size_t mla_decode_workspace_bytes(int B, int H) {
   return ws_layout(B, H, max_workers(sms)).total;
 }
 
-int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// step 1 with its checks; after_plan: called by mla_decode right after its plan step
+int absorb_q_checked(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* workspace,
+                     size_t workspace_bytes, bool after_plan, cudaStream_t stream) {
   if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
   if (B < 0) return MLA_ERR_INVALID;
   WsLayout L;
@@ -217,7 +221,15 @@ int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, 
   if (!q_nope || !q_pe || !W_UK || !aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(W_UK, 16))
     return MLA_ERR_INVALID;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return status_of(launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, stream));
+  return status_of(launch_q_absorb(q_nope, q_pe, W_UK, H, B, ws + L.q_cat, after_plan, stream));
+}
+}  // namespace
+
+extern "C" {
+
+int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  return absorb_q_checked(q_nope, q_pe, W_UK, H, B, workspace, workspace_bytes, false, stream);
 }
 
 }  // extern "C"
@@ -328,7 +340,7 @@ int mla_decode(const void* q_nope, const void* q_pe, const void* W_UK, const voi
   if (!q_nope || !q_pe || !W_UK || !W_UV || !out || !page_table || !seqlens) return MLA_ERR_INVALID;
   st = mla_decode_plan(H, cache->fmt, seqlens, B, max_pages, workspace, workspace_bytes, stream);
   if (st != MLA_OK) return st;
-  st = mla_decode_absorb_q(q_nope, q_pe, W_UK, H, B, workspace, workspace_bytes, stream);
+  st = absorb_q_checked(q_nope, q_pe, W_UK, H, B, workspace, workspace_bytes, true, stream);
   if (st != MLA_OK) return st;
   st = mla_decode_attend(H, cache, page_table, max_pages, seqlens, B, scale, workspace, workspace_bytes, stream);
   if (st != MLA_OK) return st;
@@ -394,7 +406,7 @@ int mla_decode_q(const void* q_nope, const void* q_pe, const void* W_UK, const v
   uint16_t* part_o = reinterpret_cast<uint16_t*>(ws + L.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   cudaError_t e = launch_plan(seqlens, B, qs, max_pages, workers, plan, err, stream);
-  if (e == cudaSuccess) e = launch_q_absorb(q_nope, q_pe, W_UK, H, B * T, ws + L.q_cat, stream);
+  if (e == cudaSuccess) e = launch_q_absorb(q_nope, q_pe, W_UK, H, B * T, ws + L.q_cat, true, stream);
   if (e == cudaSuccess)
     e = launch_attend_tc(ws + L.q_cat, qs, layout_fmt(cache->fmt), cache->num_pages, cache->pages, page_table, max_pages, Bv,
                          scale, plan, workers, L.max_segments, part_o, part_lse, err, stream);

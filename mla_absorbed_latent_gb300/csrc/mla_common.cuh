@@ -262,8 +262,10 @@ size_t project_workspace_bytes(long long ntok, int ksplit);
 constexpr int PROJECT_SMALL_TOKENS = 64;
 int project_small_splits(int hidden, int sms);
 size_t project_small_workspace_bytes(long long ntok, int ksplit);
+// after_plan: launched right after the plan kernel of the same decode (the
+// fused entry points), so the kernel need not wait for it before it starts
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
-                            cudaStream_t s);
+                            bool after_plan, cudaStream_t s);
 // B real rows, query layout qs (B * qs.NG plan rows)
 cudaError_t launch_plan(const int32_t* seqlens, int B, const QSpec& qs, int max_pages, int workers, int* plan,
                         int* err, cudaStream_t s);

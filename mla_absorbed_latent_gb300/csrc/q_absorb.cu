@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
                                                            const __grid_constant__ CUtensorMap tm_q,
                                                            const __grid_constant__ CUtensorMap tm_qc,
                                                            const uint16_t* __restrict__ q_pe, int H, int B,
-                                                           uint16_t* __restrict__ q_cat) {
+                                                           uint16_t* __restrict__ q_cat, int after_plan) {
   extern __shared__ uint8_t smem_raw[];
   QaSmem& S = *reinterpret_cast<QaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int h = blockIdx.x, nh = blockIdx.y;  // head, half of the latent columns
@@ -58,7 +58,13 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  grid_dep_wait();  // the queries, and the readers of q_cat in the step before
+  // The queries, and the readers of q_cat in the step before, come from work
+  // before the kernel ahead of this one.  When that kernel is the plan kernel
+  // of the same decode (after_plan), which waits for its own predecessor before
+  // it lets this grid start, they are complete already: this grid then runs
+  // beside the plan kernel and waits for it only before it exits (so that its
+  // completion still implies the plan's, which the later kernels rely on).
+  if (!after_plan) grid_dep_wait();
   grid_dep_launch();
   const uint32_t tmem = S.tmem_base;
   const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
@@ -135,6 +141,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     fence_after_sync();
   }
   if (passes == 0 && tid == 0) (void)mbar_wait(&S.w_full, 0);  // let the weight copies land before exit
+  if (after_plan) grid_dep_wait();
   fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
 }  // namespace
 
 cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B, void* q_cat,
-                            cudaStream_t s) {
+                            bool after_plan, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   CUtensorMap tm_w, tm_q;
   // W_UK: (128 dims, 512 latent columns, H heads), tiles of 64 x 256; q_nope: (128 dims, H, B), tiles of 64 x 1 x 128
@@ -161,7 +168,7 @@ cudaError_t launch_q_absorb(const void* q_nope, const void* q_pe, const void* W_
   cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(q_absorb_kernel, dim3(H, 2), dim3(128), smem, s, tm_w, tm_q, tm_qc, static_cast<const uint16_t*>(q_pe), H,
-                    B, static_cast<uint16_t*>(q_cat));
+                    B, static_cast<uint16_t*>(q_cat), after_plan ? 1 : 0);
 }
 
 }  // namespace mla
