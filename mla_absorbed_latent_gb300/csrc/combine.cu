@@ -554,12 +554,17 @@ template <int NT>
 __global__ void __launch_bounds__(NT) fix_kernel(const uint16_t* W_UV, int H, int B, QSpec qs, const int* plan,
                                                  uint16_t* out, float* o_lat, int* err) {
   __shared__ float scratch[DK + NT + 32 + DC];
-  grid_dep_wait();
-  grid_dep_launch();
   const int h = blockIdx.x, b0 = blockIdx.y * 32, hr = h % qs.Hr;
+  // The flags (and the recompute context) come from the attention step, which
+  // completed before the merge let this grid start: read before the wait.  The
+  // wait stays, before any exit, so that this grid's completion implies the
+  // merge's (the next step's plan kernel waits for this one).
   const int* fixf = plan + plan_off_fix(B);
   const int f = (threadIdx.x < 32 && b0 + (int)threadIdx.x < B) ? fixf[b0 + threadIdx.x] : 0;
-  if (!__syncthreads_or(f)) return;
+  const bool any = __syncthreads_or(f);
+  grid_dep_wait();  // flagged rows overwrite the merge's outputs
+  grid_dep_launch();
+  if (!any) return;
   const FixCtx fx = *reinterpret_cast<const FixCtx*>(plan + PLAN_CTX);
   const int* seq_c = plan + plan_off_seq(B);
   for (int r = 0; r < 32 && b0 + r < B; ++r) {
