@@ -283,7 +283,9 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
 
 /* Step 3: LSE-merge of the splits into o_lat, then out = W_UV o_lat (bf16).
  * o_lat_out (fp32 [B][H][512]) may be NULL; when given, the merged latent
- * sum is stored there too.  Rows that step 2 flagged are recomputed here
+ * sum is stored there too.  W_UV is read as a weight: its first tiles load
+ * while the kernel before this call in the stream (step 2) is still running,
+ * so the kernel that wrote W_UV must not be the one directly before this call.  Rows that step 2 flagged are recomputed here
  * exactly from the cache that step 2 read (its pointers are kept in the
  * workspace), so the cache and page table must be unchanged in between. */
 int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes,
@@ -352,7 +354,8 @@ size_t mla_prefill_workspace_bytes(int B, int H, int max_pages);
  * heads, so it follows the per-head merge as the next kernel of the chain:
  * called on the same stream right after mla_decode / mla_decode_q /
  * mla_prefill, it reads their bf16 output directly and streams its weight
- * while they finish.
+ * while they finish (so the kernel that wrote W_O must not be the one
+ * directly before this call in the stream).
  *   o         : bf16 [R][H][128] (the out of those calls; R = B, or B*T)
  *   W_O       : bf16 [hidden][H*128]
  *   hidden    : a multiple of 128, <= 65536 (2048 for V2-Lite, 7168 for V3)

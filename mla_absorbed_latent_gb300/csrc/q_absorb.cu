@@ -46,11 +46,16 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
     mbar_init(&S.q_full, 1);
     mbar_init(&S.mma_done, 1);
     fence_barrier_init();
-    // W_UK is a weight, written (if at all) by a kernel that completed before
-    // this chain started: its tiles load while the kernel before this one runs
+  }
+  // W_UK's tiles: inside a fused decode (after_plan) every write before the
+  // plan kernel is complete once this grid runs, so they load at once; a
+  // step-wise call may directly follow the kernel that wrote W_UK (a weight
+  // split), so it loads them only after its wait
+  auto load_w = [&]() {
     mbar_arrive_expect_tx(&S.w_full, 2 * W_TILE);
     for (int dc = 0; dc < 2; ++dc) tma_load_3d(S.w[dc], &tm_w, 64 * dc, 256 * nh, h, &S.w_full);
-  }
+  };
+  if (after_plan && tid == 0) load_w();
   if (warp == 0) {
     tmem_alloc(&S.tmem_base, 256);
     tmem_relinquish();
@@ -64,7 +69,10 @@ __global__ void __launch_bounds__(128, 1) q_absorb_kernel(const __grid_constant_
   // it lets this grid start, they are complete already: this grid then runs
   // beside the plan kernel and waits for it only before it exits (so that its
   // completion still implies the plan's, which the later kernels rely on).
-  if (!after_plan) grid_dep_wait();
+  if (!after_plan) {
+    grid_dep_wait();
+    if (tid == 0) load_w();
+  }
   grid_dep_launch();
   const uint32_t tmem = S.tmem_base;
   const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);

@@ -33,6 +33,33 @@ def _status_ok():
 
 # ----------------------------------------------------------------------------
 # weights and cache placement: bit-exact
+@pytest.mark.parametrize("H", [16, 128])
+def test_stepwise_absorb_right_after_weight_split(H):
+    """The weight split enqueued directly before the step-wise q-absorb (the plan
+    enqueued first), W_UK and W_UV filled with NaN bits beforehand: the q-absorb
+    step loads W_UK only after it has waited for the kernel before it, so the
+    decode reads the fresh split and matches the oracle."""
+    import mla_absorbed_latent_gb300 as mla
+    seqlens = [300, 2000, 64, 1]
+    prob = make_problem(H, seqlens, seed=70 + H)
+    dev = DeviceDecode(prob)
+    ref = oracle_outputs(prob, range(prob.B))
+    for _ in range(3):
+        dev.W_UK.view(torch.int16).fill_(-1)
+        dev.W_UV.view(torch.int16).fill_(-1)
+        mla.mla_decode_plan(H, "bf16", dev.seqlens, prob.B, prob.max_pages, dev.workspace, dev.ws_bytes)
+        mla.mla_absorb_weights(dev.wkv, H, dev.W_UK, dev.W_UV)
+        mla.mla_decode_absorb_q(dev.q_nope, dev.q_pe, dev.W_UK, H, prob.B, dev.workspace, dev.ws_bytes)
+        mla.mla_decode_attend(H, dev.cache, dev.page_table, prob.max_pages, dev.seqlens, prob.B, prob.scale,
+                              dev.workspace, dev.ws_bytes)
+        mla.mla_decode_combine(dev.W_UV, H, prob.B, dev.workspace, dev.ws_bytes, dev.out)
+        torch.cuda.synchronize()
+        _status_ok()
+        got = _out_f64(dev.out)
+        for bb in range(prob.B):
+            assert_close(got[bb], ref[bb], what=f"out[{bb}]")
+
+
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("H", [16, 128])
