@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(CombLayout<RB>::THREADS, 1)
   // warp NW: TMEM owner and W_UV loader; warp NW + 1: partial loader; warp
   // NW + 2: MMA issuer.  Each has a warp of its own: a lane blocked in
   // mbarrier.try_wait stalls its whole warp, and a merge warp that also issued
-  // the chunk's MMAs (about a microsecond) fell behind the others and held back
-  // the release of the partial ring
+  // a chunk's MMAs (about 0.45 us of issue) would fall behind the others and
+  // hold back the release of the partial ring, which waits for every warp
   const bool loader = warp >= NW, w_loader = warp == NW;
   // output row ((row, token) * heads + head) of plan row bv for this head; -1
   // for padding (one query token per row and pass: bv * heads + head, no division)
