@@ -271,6 +271,16 @@ def test_bf16_round_hand_values():
     assert np.array_equal(got, want)
 
 
+def test_bf16_bit_patterns_by_hand():
+    # sign | 8-bit exponent (bias 127) | 7-bit fraction, the top half of a float32
+    bits = np.array([0x3F80, 0xC040, 0x0000, 0x8000, 0x7F80, 0x3F81, 0x0001], dtype=np.uint16)
+    vals = np.array([1.0, -3.0, 0.0, -0.0, np.inf, 1 + 2 ** -7, 2.0 ** -133], dtype=np.float32)
+    got = O.bf16_from_bits(bits)
+    assert np.array_equal(got, vals)
+    assert np.array_equal(np.signbit(got), np.signbit(vals))
+    assert np.array_equal(O.bf16_to_bits(vals), bits)
+
+
 def test_int8_hand_vector():
     # amax 127 -> s = 1 exactly; codes = round-half-even of x
     x = np.zeros(32, dtype=np.float32)
