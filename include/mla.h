@@ -270,7 +270,9 @@ int mla_decode_plan_workers(int H, int fmt, const int32_t* seqlens, int B, int m
 int mla_decode_max_workers(int H, int fmt);
 
 /* Step 1: q_lat = W_UK^T q_nope (fp32 accumulation, rounded to bf16) and
- * q_pe, stored in the workspace as the query operand of step 2. */
+ * q_pe, stored in the workspace as the query operand of step 2.  Every input
+ * is read after the kernel before this call in the stream has completed, so
+ * that kernel may be the one that wrote W_UK (mla_absorb_weights). */
 int mla_decode_absorb_q(const void* q_nope, const void* q_pe, const void* W_UK, int H, int B,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -285,9 +287,10 @@ int mla_decode_attend(int H, const mla_cache_t* cache, const int32_t* page_table
  * o_lat_out (fp32 [B][H][512]) may be NULL; when given, the merged latent
  * sum is stored there too.  W_UV is read as a weight: its first tiles load
  * while the kernel before this call in the stream (step 2) is still running,
- * so the kernel that wrote W_UV must not be the one directly before this call.  Rows that step 2 flagged are recomputed here
- * exactly from the cache that step 2 read (its pointers are kept in the
- * workspace), so the cache and page table must be unchanged in between. */
+ * so the kernel that wrote W_UV must not be the one directly before this
+ * call.  Rows that step 2 flagged are recomputed here exactly from the cache
+ * that step 2 read (its pointers are kept in the workspace), so the cache and
+ * page table must be unchanged in between. */
 int mla_decode_combine(const void* W_UV, int H, int B, void* workspace, size_t workspace_bytes,
                        void* out, float* o_lat_out, cudaStream_t stream);
 
