@@ -921,7 +921,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // reference moves: the P of pages <= j+1 is already in the old one, so O
       // is rescaled once page j+1's P.V has completed (before page j+2's, which
       // needs this warp's next P), and l with it.  At a segment end the output
-      // is written.  ref_j: the reference page j's P was written in.
+      // is written.  ref_j: the reference in force after the check of page j-1,
+      // in which O and l hold page j (its P may have been written in the one
+      // before and rescaled by that check).
       auto check = [&](int j, bool j_last, int seg, float ref_j) -> bool {
         const int jb = j & 1;
         bool ok = wait_bar<true>(S, &S.pin_full[jb][q4], (uint32_t)(j >> 1) & 1u, a.err, 20);
@@ -949,7 +951,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         } else {
           // the four slices' sums were sent before the check of page j-1, so
-          // they miss that check's move; O has it
+          // they miss that check's move; O has it.  L is the sum in ref_j, the
+          // reference after that move, and the log-sum-exp is taken in it too
+          // (with Lm it would overstate the segment by the move whenever a
+          // segment's second-to-last page moved the reference)
           const float Lm = (m0 + m1) + (m2 + m3);
           const float L = alpha_prev * Lm;
           alpha_prev = 1.f;
@@ -957,7 +962,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           __syncwarp();
           fence_after_sync();
           store_o(seg, L > 0.f ? 1.f / L : 0.f);  // a segment this lane sees nothing of: O = 0
-          if (rank == 0 && ms == 0) a.part_lse[(size_t)seg * 128 + row] = (ref_j + log2f(Lm)) * 0.69314718055994531f;
+          if (rank == 0 && ms == 0) a.part_lse[(size_t)seg * 128 + row] = (ref_j + log2f(L)) * 0.69314718055994531f;
           fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.o_free);

@@ -583,6 +583,28 @@ def test_decode_reference_moves_keep_the_result_exact():
     _check_boosted_row(dev, prob, C, P)
 
 
+def test_decode_reference_move_on_a_second_to_last_page_is_exact():
+    """H=128, one 304-page row over the default split: a boosted token on the
+    second-to-last page of a worker's range moves that split's reference at
+    the check made during its last page, after the split's slice sums were
+    sent.  The split's log-sum-exp must be taken in the moved reference, or
+    the merge overweights the split by the size of the move.  Head 0 also
+    gets a larger boost on the first page of another worker's range (the true
+    maximum of the row), head 2 only the second-to-last-page one."""
+    import mla_absorbed_latent_gb300 as mla
+    n_pages = 304
+    prob = make_problem(128, [64 * n_pages], seed=9, paged=False)
+    dev = DeviceDecode(prob)
+    W = mla.mla_decode_max_workers(128, "bf16")
+    begin = [w * n_pages // W for w in range(W + 1)]  # the default plan's equal split of the pages
+    assert begin[2] - begin[1] >= 3 and begin[6] - begin[5] >= 3 and W > 10
+    C, P = _boost_rope_keys(dev, prob, [(0, 64 * (begin[2] - 2) + 5, 3.0), (0, 64 * begin[10] + 7, 4.0),
+                                        (2, 64 * (begin[6] - 2) + 33, 3.0)])
+    dev.decode()
+    torch.cuda.synchronize()
+    _check_boosted_row(dev, prob, C, P)
+
+
 def test_decode_seqlen_over_capacity_reports_bounds():
     import mla_absorbed_latent_gb300 as mla
     prob = make_problem(16, [100], seed=4)
