@@ -1,6 +1,7 @@
 """The library's host-side scheduling logic, compiled from its own sources and run
 on the CPU (no GPU involved): the split plan's partition of the global page list
-over the persistent workers, the decode workspace layout (with the plan block's
+over the persistent workers, the split slots the attend kernels write and the
+merge kernels read, the decode workspace layout (with the plan block's
 sections), the no-allocation decode's worker count, and the producer's choice of
 K split and its workspace size."""
 
@@ -17,6 +18,7 @@ HARNESS = r"""
 #include "cache_project.cu"
 #include "tensor_map.cu"
 #include <cstdio>
+#include <vector>
 using namespace mla;
 
 static int fails = 0;
@@ -46,6 +48,64 @@ int main() {
               "T=%lld W=%lld x=%lld w=%d", T, W, x, w);
       }
     }
+
+  // 1b. the split slots: a worker writes its split of row b to slot w + b; the
+  //     merge reads row b's slots [worker_of_tile(first tile) + b,
+  //     worker_of_tile(last tile) + b] and a row group's CTA loads the slots
+  //     [s_lo, s_hi) of its rows.  Over ragged rows (empty ones included):
+  //     written slots are distinct and below W + B, each slot a row reads was
+  //     written for that row or belongs to a worker without tiles (weight 0),
+  //     and a group's window holds every slot its rows read
+  {
+    unsigned rng = 777u;
+    auto rnd = [&](unsigned m) { rng = rng * 1103515245u + 12345u; return (rng >> 8) % m; };
+    const int gBs[] = {1, 2, 5, 33, 64, 130, 300}, gWs[] = {1, 2, 7, 76, 152}, RBs[] = {16, 32, 64};
+    for (int B : gBs)
+      for (int W : gWs)
+        for (int trial = 0; trial < 4; ++trial) {
+          std::vector<long long> pre(B + 1, 0);
+          for (int b = 0; b < B; ++b) {
+            const unsigned k = rnd(10);
+            pre[b + 1] = pre[b] + (k < 2 ? 0 : k < 6 ? (long long)rnd(3) + 1 : (long long)rnd(300) + 1);
+          }
+          const long long T = pre[B];
+          if (T == 0) continue;
+          std::vector<int> owner(W + B, -1);  // row whose split a slot holds
+          for (int w = 0; w < W; ++w) {
+            const long long a0 = worker_begin(w, T, W), a1 = worker_begin(w + 1, T, W);
+            for (int b = 0; b < B; ++b)
+              if (pre[b] < a1 && pre[b + 1] > a0) {
+                const int s = w + b;
+                CHECK(s < W + B && owner[s] < 0, "B=%d W=%d w=%d b=%d: slot %d", B, W, w, b, s);
+                if (s < W + B) owner[s] = b;
+              }
+          }
+          std::vector<int> rx(B, 1), ry(B, 0);
+          for (int b = 0; b < B; ++b) {
+            if (pre[b + 1] == pre[b]) continue;
+            rx[b] = worker_of_tile(pre[b], T, W) + b;
+            ry[b] = worker_of_tile(pre[b + 1] - 1, T, W) + b;
+            for (int s = rx[b]; s <= ry[b]; ++s) {
+              const long long w = s - b;
+              const bool empty = worker_begin(w, T, W) == worker_begin(w + 1, T, W);
+              CHECK(s >= 0 && s < W + B && (owner[s] == b || (empty && owner[s] < 0)), "B=%d W=%d b=%d s=%d", B, W,
+                    b, s);
+            }
+            for (int s = 0; s < W + B; ++s)
+              if (owner[s] == b) CHECK(rx[b] <= s && s <= ry[b], "B=%d W=%d b=%d: slot %d unread", B, W, b, s);
+          }
+          for (int RB : RBs)
+            for (int b0 = 0; b0 < B; b0 += RB) {
+              const int b_end = b0 + RB < B ? b0 + RB : B;
+              const long long t0 = pre[b0], t1 = pre[b_end];
+              if (t1 <= t0) continue;
+              const int s_lo = worker_of_tile(t0, T, W) + b0, s_hi = worker_of_tile(t1 - 1, T, W) + b_end;
+              CHECK(s_lo >= 0 && s_hi <= W + B, "B=%d W=%d b0=%d: [%d, %d)", B, W, b0, s_lo, s_hi);
+              for (int b = b0; b < b_end; ++b)
+                if (rx[b] <= ry[b]) CHECK(s_lo <= rx[b] && ry[b] < s_hi, "B=%d W=%d RB=%d b=%d", B, W, RB, b);
+            }
+        }
+  }
 
   // 2. decode workspace: regions in order, 1 KB aligned, each large enough
   const int Bs[] = {1, 7, 64, 128, 1000}, Hs[] = {16, 128}, Ws[] = {1, 152, 304};
