@@ -2,8 +2,9 @@
 on the CPU (no GPU involved): the split plan's partition of the global page list
 over the persistent workers, the split slots the attend kernels write and the
 merge kernels read, the decode workspace layout (with the plan block's
-sections), the no-allocation decode's worker count, and the producer's choice of
-K split and its workspace size."""
+sections), the no-allocation decode's worker count, the producer's choice of K
+split and its workspace size, and the query layout of several query tokens per
+row."""
 
 import os
 import shutil
@@ -191,6 +192,40 @@ int main() {
             CHECK(ws_layout(B, H, 1).total > cap, "B=%d H=%d", B, H);
           }
         }
+  // 5. the query layout of several query tokens per row (G = 128 / H tokens of
+  //    a row per virtual row of 128 MMA rows, NG virtual rows per row): every
+  //    (row, token, head) is one virtual head of one virtual row, whose flat
+  //    query row is that token's, and whose causal shift is the number of its
+  //    virtual row's view tokens after its own position; padding lanes see
+  //    nothing
+  {
+    const int qHs[] = {16, 128}, qTs[] = {1, 2, 3, 8, 9, 25, 64};
+    for (int H : qHs)
+      for (int T : qTs) {
+        const int G = 128 / H;
+        const QSpec qs{T, G, (T + G - 1) / G, H};
+        const int B = 3, Bv = B * qs.NG;
+        std::vector<int> seen((size_t)B * T * H, 0);
+        for (int r = 0; r < Bv; ++r) {
+          const int tl = qs.last_token(r);
+          CHECK(tl >= 0 && tl < T && tl >= (r % qs.NG) * G, "H=%d T=%d r=%d tl=%d", H, T, r, tl);
+          for (int v = 0; v < 128; ++v) {
+            const int t = qs.token(r, v), h = v % H, b = r / qs.NG;
+            if (t >= T) {
+              CHECK(qs.shift(r, v) >= (1 << 30), "H=%d T=%d r=%d v=%d: padding lane", H, T, r, v);
+              continue;
+            }
+            ++seen[((size_t)b * T + t) * H + h];
+            CHECK(qs.qrow(r) + v == ((long long)b * T + t) * H + h, "H=%d T=%d r=%d v=%d", H, T, r, v);
+            // query t sits at position n - T + t; the virtual row's view ends at n - T + tl
+            CHECK(qs.shift(r, v) == tl - t && t <= tl, "H=%d T=%d r=%d v=%d", H, T, r, v);
+          }
+        }
+        bool once = true;
+        for (int c : seen) once = once && c == 1;
+        CHECK(once, "H=%d T=%d: a (row, token, head) not covered exactly once", H, T);
+      }
+  }
   std::printf("%d\n", fails);
   return fails != 0;
 }
