@@ -623,3 +623,22 @@ def test_workspace_too_small_is_rejected():
         mla.mla_decode(dev.q_nope, dev.q_pe, dev.W_UK, dev.W_UV, 16, dev.cache, dev.page_table, prob.max_pages,
                        dev.seqlens, 1, prob.scale, dev.workspace, dev.ws_bytes - 1, dev.out)
     assert e.value.status == mla.MLA_ERR_WORKSPACE
+
+
+def test_decode_h128_garbage_past_row_end_is_ignored():
+    """H=128 over bf16 pages: the slots past each row's length in its last page
+    hold all-ones bytes (NaN in bf16).  They are neither keys nor values of the
+    row: the tensor-core kernel multiplies whole 64-token pages, so it masks
+    their scores and zeroes their value rows before the page's P.V."""
+    seqlens = [1, 33, 63, 100, 129, 2000]
+    prob = make_problem(128, seqlens, seed=123)
+    dev = DeviceDecode(prob)
+    for b, n in enumerate(seqlens):
+        last = (n - 1) // 64
+        page = int(dev.page_table[b, last])
+        lo = page * dev.page_bytes + (n - 64 * last) * 1152  # the first slot past the row's end
+        dev.pool[lo:(page + 1) * dev.page_bytes] = 0xFF
+    dev.decode()
+    torch.cuda.synchronize()
+    _status_ok()
+    _check_rows(dev, range(prob.B))
